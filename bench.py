@@ -1,0 +1,393 @@
+#!/usr/bin/env python3
+"""Benchmark of one CfC K-loop training step (forward + BPTT + dW/db/du/dh0) on GB300.
+
+A step is one pass of the whole hot path over one batch: cfc_forward (persistent cluster
+recurrence), then cfc_backward (reverse-time recurrence, the weight-gradient contraction,
+the reduce_axis0 bias sum, du), captured once into a CUDA graph and replayed.  The workload is
+the pages' shape (B=32 sequences, K=64 steps, C=128 hidden channels, n_x=48 inputs; page
+"K-loop Parallelization -- Block-per-Batch Kernel Refactor", section "Problem") with seeded
+synthetic inputs.  Printed: one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (a plain, deliberately slow program) on a bounded
+sample of the same workload on the host cores.  Under torchrun each rank runs its own replica
+(weak scaling, no data-path collective) and rank 0 prints the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CfC fwd+BPTT seq·steps/s at B=32,K=64,C=128; % of HBM & tensor-pipe roofline"
+UNIT = "seq·steps/s"
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", type=int, default=1)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work budget of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- algorithmic work per unit
+def work_per_unit(w):
+    """FLOPs and HBM bytes per (batch row, step) of each stage (fp32 = 4 bytes)."""
+    C, n_x, n_in = w.C, w.n_x, w.n_in
+    return {
+        # forward: 4C pre-activations over n_in; reads u_t, ts; writes h_t and 3C cache
+        "fwd": {"flop": 8 * C * n_in, "bytes": 4 * (n_x + 1 + 4 * C)},
+        # BPTT recurrence: W_h^T d_pre (4C x C); reads dH, cache, ts; writes d_pre
+        "bwd_rec": {"flop": 8 * C * C, "bytes": 4 * (C + 3 * C + 1 + 4 * C)},
+        # dW contraction (4C x n_in per row) + du (4C x n_x) + db; reads d_pre, u, h
+        "grad": {"flop": 8 * C * n_in + 8 * C * n_x + 4 * C,
+                 "bytes": 4 * (4 * C + n_x + C) + 4 * 4 * C + 4 * n_x},
+    }
+
+
+def source_digest(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, sources: list[str], workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as fh:
+        for line in fh:
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_sha256_16") != source_digest(sources):
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.remove(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- reference arm (oracle)
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    from recurrent_cfc_cell_gb300 import inputs
+
+    w = inputs.CONFIGS[args.workload]
+    inp = inputs.make_inputs(w)
+    # calibrate one single-row oracle step, then size each step's sample so the whole run
+    # stays near a minute of CPU work
+    one = {k: (v[:, :1] if k in ("u", "ts", "dH") else v[:1] if k == "h0" else v)
+           for k, v in inp.items()}
+    t0 = time.perf_counter()
+    oracle.step(one)
+    t_row = max(time.perf_counter() - t0, 1e-4)
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    rows = max(1, min(w.B, int(budget / t_row)))
+    sample = {k: (v[:, :rows] if k in ("u", "ts", "dH") else v[:rows] if k == "h0" else v)
+              for k, v in inp.items()}
+    for _ in range(args.warmup):
+        oracle.step(sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.step(sample)
+    dt = time.perf_counter() - t0
+    units = rows * w.K * args.steps
+    value = units / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": dict(w.describe(), sample_rows=rows, l2="n/a (CPU)"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{rows} of {w.B} batch rows x K={w.K} per step, fp64 C, "
+                                   "single thread"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(w, seconds: float) -> dict:
+    import oracle
+    from recurrent_cfc_cell_gb300 import inputs
+
+    inp = inputs.make_inputs(w)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.step(inp)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    return {"value": n * w.units / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} full oracle steps of the workload (B={w.B}, K={w.K}), fp64 C, "
+                      f"single thread, {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------- our arm
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+
+    from recurrent_cfc_cell_gb300 import _lib, build, inputs
+    from recurrent_cfc_cell_gb300.step import KLoopStep, to_device
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    _lib.load()
+
+    w = inputs.CONFIGS[args.workload]
+    inp = inputs.make_inputs(w)
+    dinp = to_device(inp, dev)
+    st = KLoopStep(w.B, w.K, w.C, w.n_x, device=dev).bind(**dinp)
+    st.capture()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        st.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K graph replays, L2 flushed between them (flush outside the events)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.zero_()
+        starts[k].record(stream)
+        st.replay()
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clock_info = clocks.stop()
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    units_per_step = w.units * world
+    value = units_per_step / (ms * 1e-3)
+    launches_per_step = 6  # fwd, bwd recurrence, dW contraction, reduce (dW), reduce (db), du
+
+    # ---- per-stage device times (same stream, L2 flushed before each launch)
+    n_stage = min(args.steps, 200)
+    stage_ms = {}
+
+    def time_stage(fn):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n_stage)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / n_stage
+
+    i = st.inputs
+    stage_ms["fwd"] = time_stage(st.forward)
+    stage_ms["bwd_rec"] = time_stage(lambda: _lib.cfc_backward_recurrence(
+        i["dH"], i["W"], i["ts"], st.cache, st.d_pre, st.dh0))
+    stage_ms["grad"] = time_stage(lambda: _lib.cfc_weight_grad(
+        st.d_pre, i["u"], i["h0"], i["W"], st.H, st.dW, st.db, st.du, st.ws))
+
+    pk = peaks()
+    props = torch.cuda.get_device_properties(dev)
+    fp32_peak_tflops = props.multi_processor_count * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
+    wpu = work_per_unit(w)
+    kernels = {}
+    for name, t in stage_ms.items():
+        flop = wpu[name]["flop"] * w.units
+        byt = wpu[name]["bytes"] * w.units
+        kernels[name] = {"ms": t, "tflops": flop / (t * 1e-3) / 1e12,
+                         "gbs": byt / (t * 1e-3) / 1e9}
+    dominant = max(("fwd", "bwd_rec"), key=lambda k: stage_ms[k])
+    kname = {"fwd": "cfc_fwd_kernel", "bwd_rec": "cfc_bwd_kernel"}[dominant]
+    ksrc = {"fwd": ["recurrent_cfc_cell_gb300/csrc/cfc_fwd.cu"],
+            "bwd_rec": ["recurrent_cfc_cell_gb300/csrc/cfc_bwd.cu"]}[dominant]
+    ksrc = ksrc + ["recurrent_cfc_cell_gb300/csrc/cfc_ptx.cuh",
+                   "recurrent_cfc_cell_gb300/csrc/cfc_kernels.h"]
+    achieved = kernels[dominant]["tflops"]
+    roofline = {"bound": "alu", "achieved": achieved, "peak": fp32_peak_tflops,
+                "unit": "TFLOP/s", "frac": achieved / fp32_peak_tflops,
+                "traffic": profiled_traffic(kname, ksrc, "pages_B32_K64"),
+                "kernel": kname,
+                "peak_note": f"fp32 FMA: {props.multi_processor_count} SMs x 128 lanes x 2 x "
+                             f"{pk['sm_max_mhz']:.0f} MHz",
+                "hbm_frac": kernels[dominant]["gbs"] / pk["hbm_gbs"]}
+
+    # ---- end to end through the public API with host buffers
+    pin = {k: torch.from_numpy(v).pin_memory() for k, v in inp.items()}
+    outs = {k: torch.empty(tuple(getattr(st, k).shape), dtype=torch.float32).pin_memory()
+            for k in ("dW", "db", "du", "dh0")}
+    h2d = sum(v.numel() * 4 for v in pin.values())
+    d2h = sum(v.numel() * 4 for v in outs.values())
+    n_e2e = min(args.steps, 200)
+
+    def e2e_step():
+        for k, v in pin.items():
+            dinp[k].copy_(v, non_blocking=True)
+        st.run()
+        for k, v in outs.items():
+            v.copy_(getattr(st, k), non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n_e2e)]
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in ev) / n_e2e
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": units_per_step / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    status = _lib.device_status()
+
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = cpu_baseline(w, args.cpu_seconds)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": dict(w.describe(), parallelism=f"replicas{world}",
+                           l2="flushed between timed steps (256 MB write)",
+                           graph="one CUDA graph per step", dw_mode="accurate"),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps, "clocks": clock_info,
+            "kernels": kernels, "device_status": status, "peaks_source": pk["source"],
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

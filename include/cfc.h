@@ -1,0 +1,163 @@
+/*
+ * cfc.h -- C ABI of the GB300 (sm_103a) CfC K-loop library: forward recurrence, reverse-time
+ * backpropagation through time, and deterministic weight / bias / input / initial-state
+ * gradients for a batch of B sequences over K steps.
+ *
+ * Source of the operations.  The K-loop parallelization spec (page "K-loop Parallelization --
+ * Block-per-Batch Kernel Refactor") names the per-step forward kernel cfc_step_batched and
+ * backward kernel cfc_step_backward_batched (section "Problem"), the per-(batch row, channel)
+ * gradient scratch and the reducer reduce_axis0 with overwrite semantics (section
+ * "Architecture Choice", item 3), and the rule that a final gradient buffer holds meaningful
+ * data only after its reducer ran (section "AdamW-after-reducer invariant").  The pages do not
+ * print the cell's equations; this library computes the four-gate closed-form continuous-time
+ * cell
+ *
+ *     z_t  = [u_t ; h_{t-1}]            (n_in = n_x + C, h_{-1} = h0)
+ *     P_g  = W_g z_t + b_g              for the gates g = ff1, ff2, ta, tb, in that order
+ *     h_t  = tanh(P_ff1) * (1 - s) + s * tanh(P_ff2),   s = sigmoid(P_ta * ts[t][b] + P_tb)
+ *
+ * and, for an upstream gradient dH = dL/dH, the exact gradients dW, db, du, dh0 of
+ * L = sum dH * H.
+ *
+ * Conventions shared by every entry point.
+ *   - Every tensor pointer is a DEVICE pointer to fp32 data, row-major with the last index
+ *     fastest, 16-byte aligned (CFC_ERR_MISALIGNED otherwise).  The caller allocates and owns
+ *     every buffer; the library never allocates, frees or synchronises.
+ *   - Every output is OVERWRITTEN in full (nothing accumulates across calls) and is valid only
+ *     after the work queued on `stream` has completed.
+ *   - `stream` is a cudaStream_t (0 = the legacy default stream).  Calls only enqueue work, so
+ *     they may be captured into a CUDA graph once an eager call with the same sizes has run
+ *     on the device (the first call per device and size class sets kernel attributes).
+ *   - Status: 0 on success, a negative CFC_ERR_* code otherwise; argument errors are detected
+ *     on the host before any work is enqueued.  Nothing aborts or throws.
+ *   - Size envelope of the recurrence kernels: 1 <= C <= 256; n_x >= 1 with
+ *     roundup(n_x, 4) + 16 * cs(C) <= 320 where cs(C) is the smallest power of two >= C/16;
+ *     B, K >= 1 with K * B * 4 * C < 2^31.
+ */
+#ifndef CFC_H
+#define CFC_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CFC_OK 0
+#define CFC_ERR_INVALID_DIM (-1)        /* a size is <= 0 or outside the envelope above      */
+#define CFC_ERR_NULL_PTR (-2)           /* a required pointer is NULL                        */
+#define CFC_ERR_MISALIGNED (-3)         /* a tensor pointer is not 16-byte aligned           */
+#define CFC_ERR_WS_TOO_SMALL (-4)       /* workspace shorter than cfc_workspace_bytes()      */
+#define CFC_ERR_UNSUPPORTED_DEVICE (-5) /* current device is not compute capability 10.3     */
+#define CFC_ERR_LAUNCH_FAILED (-6)      /* a kernel launch returned an error                 */
+#define CFC_ERR_DEVICE_TIMEOUT (-7)     /* a kernel abandoned a wait (see cfc_device_status) */
+#define CFC_ERR_INVALID_ARG (-8)        /* an enumerated argument is out of range            */
+#define CFC_ERR_CUDA (-9)               /* another CUDA runtime call failed                  */
+
+/* Weight-gradient contraction modes for cfc_backward (argument dw_mode). */
+#define CFC_DW_ACCURATE 0  /* fp32-accurate result (relative error ~1e-6 of max|dW|)          */
+#define CFC_DW_SIMT_FP32 2 /* CUDA-core fp32 FMA contraction (the reference path)             */
+
+typedef void* cfc_stream_t; /* a cudaStream_t */
+
+/*
+ * cfc_workspace_bytes -- bytes of device workspace cfc_backward needs for these sizes and
+ * dw_mode.  Writes *bwd_ws_bytes; the forward cache is always K*B*3*C floats and needs no
+ * query.  Returns CFC_OK, CFC_ERR_INVALID_DIM, CFC_ERR_NULL_PTR or CFC_ERR_INVALID_ARG.
+ * The workspace layout is: d_pre [K][B][4][C] fp32 at offset 0 (the pre-activation gradients
+ * dL/dP, readable after cfc_backward completes), then internal split-contraction partials.
+ */
+int cfc_workspace_bytes(int B, int K, int C, int n_x, int dw_mode, size_t* bwd_ws_bytes);
+
+/*
+ * cfc_forward -- the K-step forward recurrence (successor of cfc_step_batched, which ran one
+ * step per launch; page "K-loop Parallelization -- Block-per-Batch Kernel Refactor", section
+ * "Problem").  One persistent launch runs all K steps.
+ *   u     [K][B][n_x]  inputs u_t
+ *   h0    [B][C]       initial state
+ *   W     [4][C][n_x+C] gate weights (ff1, ff2, ta, tb); columns follow z = [u_t ; h_{t-1}]
+ *   b     [4][C]       gate biases
+ *   ts    [K][B]       time-scale per step and row (multiplies P_ta only)
+ *   H     [K][B][C]    OUTPUT: h_t for every step
+ *   cache [K][B][3][C] OUTPUT: ff1, ff2 and the gate s for every step (read by cfc_backward)
+ */
+int cfc_forward(const float* u, const float* h0, const float* W, const float* b,
+                const float* ts, int B, int K, int C, int n_x, float* H, float* cache,
+                cfc_stream_t stream);
+
+/*
+ * cfc_backward -- reverse-time BPTT over the K steps (successor of cfc_step_backward_batched;
+ * same page, sections "Problem" and "Per-Kernel Breakdown"), then the weight gradient as one
+ * dense contraction over the B*K rows and the bias gradient through reduce_axis0: exactly
+ * cfc_backward_recurrence into the head of ws followed by cfc_weight_grad.
+ *   dH    [K][B][C]     upstream gradient dL/dh_t (the loss is L = sum dH * H)
+ *   u, h0, W, ts        the forward's inputs;  H, cache: the forward's outputs
+ *   dW    [4][C][n_x+C] OUTPUT: dL/dW
+ *   db    [4][C]        OUTPUT: dL/db
+ *   du    [K][B][n_x]   OUTPUT: dL/du (may be NULL to skip it)
+ *   dh0   [B][C]        OUTPUT: dL/dh0
+ *   ws, ws_bytes        device workspace of at least cfc_workspace_bytes() bytes, 16-byte
+ *                       aligned; its first K*B*4*C floats receive d_pre
+ *   dw_mode             CFC_DW_ACCURATE or CFC_DW_SIMT_FP32
+ */
+int cfc_backward(const float* dH, const float* u, const float* h0, const float* W,
+                 const float* ts, const float* H, const float* cache, int B, int K, int C,
+                 int n_x, float* dW, float* db, float* du, float* dh0, void* ws,
+                 size_t ws_bytes, int dw_mode, cfc_stream_t stream);
+
+/*
+ * cfc_backward_recurrence -- the first stage of cfc_backward alone: the reverse-time
+ * recurrence, writing the pre-activation gradients and dh0.
+ *   dH, W, ts, cache   as for cfc_backward
+ *   d_pre [K][B][4][C] OUTPUT: dL/dP for every step, row, gate and channel
+ *   dh0   [B][C]       OUTPUT: dL/dh0
+ */
+int cfc_backward_recurrence(const float* dH, const float* W, const float* ts,
+                            const float* cache, int B, int K, int C, int n_x, float* d_pre,
+                            float* dh0, cfc_stream_t stream);
+
+/*
+ * cfc_weight_grad -- the second stage of cfc_backward alone: dW = sum_{t,b} d_pre z^T as one
+ * contraction over the B*K rows (z = [u_t ; h_{t-1}], h_{-1} = h0), db = sum_{t,b} d_pre
+ * through reduce_axis0, and du = W_u^T d_pre (skipped when du is NULL).  The weight gradient
+ * as a dense contraction over the batch replaces the per-sample atomicAdd accumulation, as
+ * the DQN plan on page "H100 Epoch Optimization Phase 2" (Task 2) does for its layers.
+ *   d_pre [K][B][4][C]  input (e.g. from cfc_backward_recurrence)
+ *   u, h0, W, H         the forward's inputs and output
+ *   dW, db, du          OUTPUTS as for cfc_backward
+ *   ws, ws_bytes        workspace as for cfc_backward (d_pre may live at its head)
+ */
+int cfc_weight_grad(const float* d_pre, const float* u, const float* h0, const float* W,
+                    const float* H, int B, int K, int C, int n_x, float* dW, float* db,
+                    float* du, void* ws, size_t ws_bytes, int dw_mode, cfc_stream_t stream);
+
+/*
+ * reduce_axis0 -- out[n] = sum_{r < n_batch} per_batch[r][n] for n < n_tail, OVERWRITING out
+ * (page "K-loop Parallelization -- Block-per-Batch Kernel Refactor", section "Architecture
+ * Choice", item 3: block tree-reduce over the batch index, no atomicAdd, grid over the tail).
+ * The summation order depends only on (n_batch, n_tail): results are bitwise reproducible.
+ *   per_batch [n_batch][n_tail] device fp32, 4-byte aligned (16-byte alignment with n_tail a
+ *             multiple of 4 selects the vectorised path; both give identical sums)
+ *   out       [n_tail] device fp32
+ * Returns CFC_OK, CFC_ERR_INVALID_DIM (n_batch or n_tail <= 0), CFC_ERR_NULL_PTR,
+ * CFC_ERR_MISALIGNED, CFC_ERR_UNSUPPORTED_DEVICE or CFC_ERR_LAUNCH_FAILED.
+ */
+int reduce_axis0(const float* per_batch, int n_batch, int n_tail, float* out,
+                 cfc_stream_t stream);
+
+/* cfc_error_string -- static English text for a status code (never NULL). */
+const char* cfc_error_string(int code);
+
+/*
+ * cfc_device_status -- synchronises the current device, then reads and clears the library's
+ * device status word (set by a kernel that abandoned a bounded wait).  *status receives 0 when
+ * no kernel reported a problem.  Returns CFC_OK, CFC_ERR_NULL_PTR or CFC_ERR_CUDA.  This is
+ * the only entry point that synchronises.
+ */
+int cfc_device_status(int* status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CFC_H */

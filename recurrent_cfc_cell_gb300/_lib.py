@@ -1,0 +1,171 @@
+"""ctypes binding of libcfc.so (include/cfc.h): argument marshalling only.
+
+Every function takes torch tensors that already live on the current CUDA device, checks
+dtype / contiguity / shape on the host, passes raw pointers and the current stream to the C
+entry point of the same name and raises ``CfcError`` on a non-zero status.  All computation
+happens in the library's CUDA kernels.  If the library has not been built (or fails to load)
+importing it raises, so nothing can silently run elsewhere.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libcfc.so")
+
+CFC_OK = 0
+CFC_DW_ACCURATE = 0
+CFC_DW_SIMT_FP32 = 2
+
+# Public C symbols declared in include/cfc.h (checked by the test suite).
+EXPORTED = ("cfc_workspace_bytes", "cfc_forward", "cfc_backward", "cfc_backward_recurrence",
+            "cfc_weight_grad", "reduce_axis0", "cfc_error_string", "cfc_device_status")
+
+
+class CfcError(RuntimeError):
+    def __init__(self, func: str, code: int, text: str):
+        super().__init__(f"{func} failed: {code} ({text})")
+        self.code = code
+
+
+_lib = None
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libcfc.so (raises if it is missing: build it with recurrent_cfc_cell_gb300.build)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(f"libcfc.so not built ({p}); run python -m recurrent_cfc_cell_gb300.build")
+    lib = ctypes.CDLL(p)
+    vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.cfc_workspace_bytes.argtypes = [i, i, i, i, i, ctypes.POINTER(sz)]
+    lib.cfc_workspace_bytes.restype = i
+    lib.cfc_forward.argtypes = [vp] * 5 + [i] * 4 + [vp, vp, vp]
+    lib.cfc_forward.restype = i
+    lib.cfc_backward.argtypes = [vp] * 7 + [i] * 4 + [vp] * 5 + [sz, i, vp]
+    lib.cfc_backward.restype = i
+    lib.cfc_backward_recurrence.argtypes = [vp] * 4 + [i] * 4 + [vp, vp, vp]
+    lib.cfc_backward_recurrence.restype = i
+    lib.cfc_weight_grad.argtypes = [vp] * 5 + [i] * 4 + [vp] * 4 + [sz, i, vp]
+    lib.cfc_weight_grad.restype = i
+    lib.reduce_axis0.argtypes = [vp, i, i, vp, vp]
+    lib.reduce_axis0.restype = i
+    lib.cfc_error_string.argtypes = [i]
+    lib.cfc_error_string.restype = ctypes.c_char_p
+    lib.cfc_device_status.argtypes = [ctypes.POINTER(i)]
+    lib.cfc_device_status.restype = i
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def error_string(code: int) -> str:
+    return load().cfc_error_string(int(code)).decode()
+
+
+def _check(func: str, rc: int) -> None:
+    if rc != CFC_OK:
+        raise CfcError(func, rc, error_string(rc))
+
+
+def _ptr(t, name: str, shape=None):
+    import torch
+
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace_bytes(B: int, K: int, C: int, n_x: int, dw_mode: int = CFC_DW_ACCURATE) -> int:
+    out = ctypes.c_size_t(0)
+    _check("cfc_workspace_bytes",
+           load().cfc_workspace_bytes(B, K, C, n_x, dw_mode, ctypes.byref(out)))
+    return out.value
+
+
+def cfc_forward(u, h0, W, b, ts, H, cache, stream=None) -> None:
+    """H [K,B,C] and cache [K,B,3,C] <- forward recurrence over K steps."""
+    K, B, n_x = u.shape
+    C = h0.shape[1]
+    n_in = n_x + C
+    rc = load().cfc_forward(
+        _ptr(u, "u", (K, B, n_x)), _ptr(h0, "h0", (B, C)), _ptr(W, "W", (4, C, n_in)),
+        _ptr(b, "b", (4, C)), _ptr(ts, "ts", (K, B)), B, K, C, n_x,
+        _ptr(H, "H", (K, B, C)), _ptr(cache, "cache", (K, B, 3, C)), _stream(stream))
+    _check("cfc_forward", rc)
+
+
+def cfc_backward(dH, u, h0, W, ts, H, cache, dW, db, du, dh0, ws,
+                 dw_mode: int = CFC_DW_ACCURATE, stream=None) -> None:
+    """dW, db, du (optional), dh0 and d_pre (at the head of ws) <- BPTT + contractions."""
+    K, B, n_x = u.shape
+    C = h0.shape[1]
+    n_in = n_x + C
+    import torch
+
+    if ws.dtype != torch.uint8 or not ws.is_cuda or not ws.is_contiguous():
+        raise ValueError("ws must be a contiguous uint8 CUDA tensor")
+    rc = load().cfc_backward(
+        _ptr(dH, "dH", (K, B, C)), _ptr(u, "u", (K, B, n_x)), _ptr(h0, "h0", (B, C)),
+        _ptr(W, "W", (4, C, n_in)), _ptr(ts, "ts", (K, B)), _ptr(H, "H", (K, B, C)),
+        _ptr(cache, "cache", (K, B, 3, C)), B, K, C, n_x, _ptr(dW, "dW", (4, C, n_in)),
+        _ptr(db, "db", (4, C)), _ptr(du, "du", (K, B, n_x)), _ptr(dh0, "dh0", (B, C)),
+        ctypes.c_void_p(ws.data_ptr()), ws.numel(), dw_mode, _stream(stream))
+    _check("cfc_backward", rc)
+
+
+def cfc_backward_recurrence(dH, W, ts, cache, d_pre, dh0, stream=None) -> None:
+    """d_pre [K,B,4,C] and dh0 [B,C] <- reverse-time recurrence only."""
+    K, B, C = dH.shape
+    n_x = W.shape[2] - C
+    rc = load().cfc_backward_recurrence(
+        _ptr(dH, "dH", (K, B, C)), _ptr(W, "W", (4, C, n_x + C)), _ptr(ts, "ts", (K, B)),
+        _ptr(cache, "cache", (K, B, 3, C)), B, K, C, n_x, _ptr(d_pre, "d_pre", (K, B, 4, C)),
+        _ptr(dh0, "dh0", (B, C)), _stream(stream))
+    _check("cfc_backward_recurrence", rc)
+
+
+def cfc_weight_grad(d_pre, u, h0, W, H, dW, db, du, ws, dw_mode: int = CFC_DW_ACCURATE,
+                    stream=None) -> None:
+    """dW, db, du (optional) <- contractions of d_pre (second stage of cfc_backward)."""
+    K, B, n_x = u.shape
+    C = h0.shape[1]
+    n_in = n_x + C
+    rc = load().cfc_weight_grad(
+        _ptr(d_pre, "d_pre", (K, B, 4, C)), _ptr(u, "u", (K, B, n_x)), _ptr(h0, "h0", (B, C)),
+        _ptr(W, "W", (4, C, n_in)), _ptr(H, "H", (K, B, C)), B, K, C, n_x,
+        _ptr(dW, "dW", (4, C, n_in)), _ptr(db, "db", (4, C)), _ptr(du, "du", (K, B, n_x)),
+        ctypes.c_void_p(ws.data_ptr()), ws.numel(), dw_mode, _stream(stream))
+    _check("cfc_weight_grad", rc)
+
+
+def reduce_axis0(per_batch, out, stream=None) -> None:
+    """out[n] <- sum_r per_batch[r, n] (overwrite, deterministic order)."""
+    n_batch, n_tail = per_batch.shape
+    rc = load().reduce_axis0(_ptr(per_batch, "per_batch"), n_batch, n_tail,
+                             _ptr(out, "out", (n_tail,)), _stream(stream))
+    _check("reduce_axis0", rc)
+
+
+def device_status() -> int:
+    """Synchronise, then read and clear the device status word (0 = no kernel gave up)."""
+    v = ctypes.c_int(0)
+    _check("cfc_device_status", load().cfc_device_status(ctypes.byref(v)))
+    return v.value

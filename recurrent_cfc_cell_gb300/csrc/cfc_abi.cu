@@ -1,0 +1,332 @@
+// cfc_abi.cu -- extern "C" entry points of libcfc: argument validation on the host, per-device
+// set-up (kernel attributes, cluster occupancy), launch planning and kernel launches.  The
+// library allocates no memory and never synchronises (except cfc_device_status, whose purpose is
+// to synchronise and read the status word).
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "cfc.h"
+#include "cfc_kernels.h"
+
+namespace {
+
+// Kernels record abandoned waits here; cfc_device_status reads and clears it.
+__device__ int g_status_word;
+
+struct DeviceState {
+  bool init = false;
+  int init_rc = CFC_OK;
+  int sms = 0;
+  int* status = nullptr;  // device address of g_status_word on this device
+  std::map<std::tuple<int, int, int, size_t>, int> max_clusters;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_rc(cudaError_t e, int code) {
+  if (e == cudaSuccess) return CFC_OK;
+  (void)cudaGetLastError();  // clear the sticky-free error so later calls are unaffected
+  return code;
+}
+
+// Per-device initialisation under the lock; returns CFC_OK or an error code.
+int device_state(DeviceState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    (void)cudaGetLastError();
+    return CFC_ERR_UNSUPPORTED_DEVICE;
+  }
+  DeviceState& st = g_dev[dev];
+  if (!st.init) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return CFC_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (major != 10 || minor != 3) {
+      st.init = true;
+      st.init_rc = CFC_ERR_UNSUPPORTED_DEVICE;
+    } else {
+      st.sms = sms;
+      void* addr = nullptr;
+      int rc = cuda_rc(cudaGetSymbolAddress(&addr, g_status_word), CFC_ERR_CUDA);
+      if (rc == CFC_OK) rc = cuda_rc(cfc::reduce_axis0_prepare(), CFC_ERR_CUDA);
+      if (rc != CFC_OK) return rc;  // retried on the next call
+      st.status = static_cast<int*>(addr);
+      st.init = true;
+      st.init_rc = CFC_OK;
+    }
+  }
+  if (st.init_rc != CFC_OK) return st.init_rc;
+  *out = &st;
+  return CFC_OK;
+}
+
+// Smallest power of two >= ceil(C / 16): CTAs per cluster of the recurrence kernels.
+int cluster_size_for(int C) {
+  const int need = (C + cfc::kChanPerCta - 1) / cfc::kChanPerCta;
+  int cs = 1;
+  while (cs < need) cs <<= 1;
+  return cs;
+}
+
+int round_up4(int x) { return (x + 3) & ~3; }
+
+int check_dims(int B, int K, int C, int n_x) {
+  if (B <= 0 || K <= 0 || C <= 0 || n_x <= 0) return CFC_ERR_INVALID_DIM;
+  if (C > cfc::kChanPerCta * cfc::kMaxClusterSize) return CFC_ERR_INVALID_DIM;
+  const int cs = cluster_size_for(C);
+  if (cfc::fwd_kw_for(round_up4(n_x), cs) < 0) return CFC_ERR_INVALID_DIM;
+  const long long pre = 4LL * K * B * C;
+  if (pre >= (1LL << 31)) return CFC_ERR_INVALID_DIM;
+  return CFC_OK;
+}
+
+// Cached cudaOccupancyMaxActiveClusters (prepare also sets the kernel attributes).
+int max_clusters(DeviceState& st, int kind, int variant, int CS, size_t smem, int* out) {
+  const auto key = std::make_tuple(kind, variant, CS, smem);
+  auto it = st.max_clusters.find(key);
+  if (it != st.max_clusters.end()) {
+    *out = it->second;
+    return CFC_OK;
+  }
+  int n = 0;
+  const cudaError_t e = (kind == 0) ? cfc::fwd_prepare(variant, CS, smem, &n)
+                                    : cfc::bwd_prepare(CS, smem, &n);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return CFC_ERR_CUDA;
+  }
+  st.max_clusters[key] = n;
+  *out = n;
+  return CFC_OK;
+}
+
+// Rows per cluster: the smallest R (power of two, <= 32) whose clusters all fit in one wave,
+// else the largest that fits at all.  Results never depend on R (each row's arithmetic is the
+// same whatever the grouping).
+int plan_rows(DeviceState& st, int kind, int variant, int CS, int B, int NZp, int* R_out,
+              size_t* smem_out, int* clusters_out) {
+  int best_R = 0;
+  size_t best_smem = 0;
+  for (int R = 1; R <= cfc::kMaxRowsPerCluster; R *= 2) {
+    const size_t smem = (kind == 0) ? cfc::fwd_smem_bytes(R, NZp) : cfc::bwd_smem_bytes(R);
+    if (smem > 227 * 1024) break;
+    int n = 0;
+    const int rc = max_clusters(st, kind, variant, CS, smem, &n);
+    if (rc != CFC_OK) return rc;
+    if (n <= 0) break;
+    best_R = R;
+    best_smem = smem;
+    if ((B + R - 1) / R <= n) break;
+    if (R >= B) break;
+  }
+  if (best_R == 0) return CFC_ERR_INVALID_DIM;  // no cluster of this size can be scheduled
+  *R_out = best_R;
+  *smem_out = best_smem;
+  *clusters_out = (B + best_R - 1) / best_R;
+  return CFC_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct BwdLayout {
+  size_t d_pre_off, d_pre_bytes, part_off, part_bytes, total;
+  int S;
+};
+
+BwdLayout bwd_layout(int B, int K, int C, int n_x) {
+  BwdLayout L;
+  const size_t BK = static_cast<size_t>(B) * K;
+  L.d_pre_off = 0;
+  L.d_pre_bytes = BK * 4 * C * sizeof(float);
+  L.S = cfc::dw_simt_splits(static_cast<int>(BK));
+  L.part_off = align256(L.d_pre_bytes);
+  L.part_bytes = static_cast<size_t>(L.S) * 4 * C * (n_x + C) * sizeof(float);
+  L.total = L.part_off + L.part_bytes;
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* cfc_error_string(int code) {
+  switch (code) {
+    case CFC_OK: return "ok";
+    case CFC_ERR_INVALID_DIM: return "invalid or unsupported dimension";
+    case CFC_ERR_NULL_PTR: return "required pointer is NULL";
+    case CFC_ERR_MISALIGNED: return "tensor pointer is not 16-byte aligned";
+    case CFC_ERR_WS_TOO_SMALL: return "workspace smaller than cfc_workspace_bytes()";
+    case CFC_ERR_UNSUPPORTED_DEVICE: return "no usable compute capability 10.3 device";
+    case CFC_ERR_LAUNCH_FAILED: return "kernel launch failed";
+    case CFC_ERR_DEVICE_TIMEOUT: return "a kernel abandoned a bounded wait";
+    case CFC_ERR_INVALID_ARG: return "invalid enumerated argument";
+    case CFC_ERR_CUDA: return "CUDA runtime call failed";
+    default: return "unknown status code";
+  }
+}
+
+int cfc_workspace_bytes(int B, int K, int C, int n_x, int dw_mode, size_t* bwd_ws_bytes) {
+  const int rc = check_dims(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (dw_mode != CFC_DW_ACCURATE && dw_mode != CFC_DW_SIMT_FP32) return CFC_ERR_INVALID_ARG;
+  if (!bwd_ws_bytes) return CFC_ERR_NULL_PTR;
+  *bwd_ws_bytes = bwd_layout(B, K, C, n_x).total;
+  return CFC_OK;
+}
+
+int cfc_forward(const float* u, const float* h0, const float* W, const float* b,
+                const float* ts, int B, int K, int C, int n_x, float* H, float* cache,
+                cfc_stream_t stream) {
+  int rc = check_dims(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (!u || !h0 || !W || !b || !ts || !H || !cache) return CFC_ERR_NULL_PTR;
+  if (!aligned16(u) || !aligned16(h0) || !aligned16(W) || !aligned16(b) || !aligned16(ts) ||
+      !aligned16(H) || !aligned16(cache))
+    return CFC_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != CFC_OK) return rc;
+
+  cfc::FwdParams p;
+  p.u = u; p.h0 = h0; p.W = W; p.bias = b; p.ts = ts; p.H = H; p.cache = cache;
+  p.status = st->status;
+  p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
+  p.CS = cluster_size_for(C);
+  p.nxp = round_up4(n_x);
+  const int KW = cfc::fwd_kw_for(p.nxp, p.CS);
+  p.NZp = 4 * KW;
+  size_t smem = 0;
+  int n_clusters = 0;
+  rc = plan_rows(*st, 0, KW, p.CS, B, p.NZp, &p.R, &smem, &n_clusters);
+  if (rc != CFC_OK) return rc;
+  return cuda_rc(cfc::fwd_launch(KW, p, n_clusters, smem, static_cast<cudaStream_t>(stream)),
+                 CFC_ERR_LAUNCH_FAILED);
+}
+
+int cfc_backward_recurrence(const float* dH, const float* W, const float* ts,
+                            const float* cache, int B, int K, int C, int n_x, float* d_pre,
+                            float* dh0, cfc_stream_t stream) {
+  int rc = check_dims(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (!dH || !W || !ts || !cache || !d_pre || !dh0) return CFC_ERR_NULL_PTR;
+  if (!aligned16(dH) || !aligned16(W) || !aligned16(ts) || !aligned16(cache) ||
+      !aligned16(d_pre) || !aligned16(dh0))
+    return CFC_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != CFC_OK) return rc;
+  cfc::BwdParams p;
+  p.dH = dH; p.W = W; p.ts = ts; p.cache = cache; p.d_pre = d_pre; p.dh0 = dh0;
+  p.status = st->status;
+  p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
+  p.CS = cluster_size_for(C);
+  size_t smem = 0;
+  int n_clusters = 0;
+  rc = plan_rows(*st, 1, p.CS, p.CS, B, 0, &p.R, &smem, &n_clusters);
+  if (rc != CFC_OK) return rc;
+  return cuda_rc(cfc::bwd_launch(p, n_clusters, smem, static_cast<cudaStream_t>(stream)),
+                 CFC_ERR_LAUNCH_FAILED);
+}
+
+int cfc_weight_grad(const float* d_pre, const float* u, const float* h0, const float* W,
+                    const float* H, int B, int K, int C, int n_x, float* dW, float* db,
+                    float* du, void* ws, size_t ws_bytes, int dw_mode, cfc_stream_t stream) {
+  int rc = check_dims(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (dw_mode != CFC_DW_ACCURATE && dw_mode != CFC_DW_SIMT_FP32) return CFC_ERR_INVALID_ARG;
+  if (!d_pre || !u || !h0 || !W || !H || !dW || !db || !ws) return CFC_ERR_NULL_PTR;
+  if (!aligned16(d_pre) || !aligned16(u) || !aligned16(h0) || !aligned16(W) || !aligned16(H) ||
+      !aligned16(dW) || !aligned16(db) || (du && !aligned16(du)) || !aligned16(ws))
+    return CFC_ERR_MISALIGNED;
+  const BwdLayout L = bwd_layout(B, K, C, n_x);
+  if (ws_bytes < L.total) return CFC_ERR_WS_TOO_SMALL;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != CFC_OK) return rc;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + L.part_off);
+  const int BK = B * K;
+  const int M = 4 * C, N = n_x + C;
+  rc = cuda_rc(cfc::dw_simt_launch(d_pre, u, H, h0, B, K, C, n_x, L.S, partial, s),
+               CFC_ERR_LAUNCH_FAILED);
+  if (rc != CFC_OK) return rc;
+  rc = cuda_rc(cfc::reduce_axis0_launch(partial, L.S, M * N, dW, s), CFC_ERR_LAUNCH_FAILED);
+  if (rc != CFC_OK) return rc;
+  rc = cuda_rc(cfc::reduce_axis0_launch(d_pre, BK, M, db, s), CFC_ERR_LAUNCH_FAILED);
+  if (rc != CFC_OK) return rc;
+  if (du) rc = cuda_rc(cfc::du_simt_launch(d_pre, W, BK, C, n_x, du, s), CFC_ERR_LAUNCH_FAILED);
+  return rc;
+}
+
+int cfc_backward(const float* dH, const float* u, const float* h0, const float* W,
+                 const float* ts, const float* H, const float* cache, int B, int K, int C,
+                 int n_x, float* dW, float* db, float* du, float* dh0, void* ws,
+                 size_t ws_bytes, int dw_mode, cfc_stream_t stream) {
+  int rc = check_dims(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (dw_mode != CFC_DW_ACCURATE && dw_mode != CFC_DW_SIMT_FP32) return CFC_ERR_INVALID_ARG;
+  if (!dH || !u || !h0 || !W || !ts || !H || !cache || !dW || !db || !dh0 || !ws)
+    return CFC_ERR_NULL_PTR;
+  if (!aligned16(dH) || !aligned16(u) || !aligned16(h0) || !aligned16(W) || !aligned16(ts) ||
+      !aligned16(H) || !aligned16(cache) || !aligned16(dW) || !aligned16(db) ||
+      (du && !aligned16(du)) || !aligned16(dh0) || !aligned16(ws))
+    return CFC_ERR_MISALIGNED;
+  const BwdLayout L = bwd_layout(B, K, C, n_x);
+  if (ws_bytes < L.total) return CFC_ERR_WS_TOO_SMALL;
+  float* d_pre = reinterpret_cast<float*>(static_cast<char*>(ws) + L.d_pre_off);
+  rc = cfc_backward_recurrence(dH, W, ts, cache, B, K, C, n_x, d_pre, dh0, stream);
+  if (rc != CFC_OK) return rc;
+  return cfc_weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode,
+                         stream);
+}
+
+int reduce_axis0(const float* per_batch, int n_batch, int n_tail, float* out,
+                 cfc_stream_t stream) {
+  if (n_batch <= 0 || n_tail <= 0) return CFC_ERR_INVALID_DIM;
+  if (!per_batch || !out) return CFC_ERR_NULL_PTR;
+  if ((reinterpret_cast<uintptr_t>(per_batch) & 3u) || (reinterpret_cast<uintptr_t>(out) & 3u))
+    return CFC_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  const int rc = device_state(&st);
+  if (rc != CFC_OK) return rc;
+  return cuda_rc(cfc::reduce_axis0_launch(per_batch, n_batch, n_tail, out,
+                                          static_cast<cudaStream_t>(stream)),
+                 CFC_ERR_LAUNCH_FAILED);
+}
+
+int cfc_device_status(int* status) {
+  if (!status) return CFC_ERR_NULL_PTR;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  const int rc = device_state(&st);
+  if (rc != CFC_OK) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    (void)cudaGetLastError();
+    return CFC_ERR_CUDA;
+  }
+  int v = 0;
+  const int zero = 0;
+  if (cudaMemcpy(&v, st->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(st->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return CFC_ERR_CUDA;
+  }
+  *status = v;
+  return CFC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,147 @@
+// cfc_reduce.cu -- reduce_axis0: out[n] = sum_{r < n_batch} per_batch[r][n], OVERWRITE.
+//
+// The K-loop parallelization spec (page "K-loop Parallelization -- Block-per-Batch Kernel
+// Refactor", section "Architecture Choice", item 3) defines reduce_axis0(per_batch [B, N],
+// n_batch, n_tail, out [N]): a block tree-reduce across the batch index with no atomicAdd,
+// grid over the output tail dimension, output overwritten (never accumulated into).
+//
+// GB300 layout: grid = (column tiles, CZ) with a thread-block cluster of CZ CTAs along the
+// batch axis, so a tall input (e.g. 262144 x 1024 bias partials) still spreads over up to
+// 16 x (tiles) SMs.  Each CTA sums a fixed row range (8 row-lanes x 32 column-lanes, float4
+// columns when aligned); lanes are merged in shared memory in lane order and the CZ CTA sums
+// are merged through distributed shared memory in rank order.  The summation order depends only
+// on (n_batch, n_tail), so the result is bitwise reproducible run to run.
+#include "cfc_kernels.h"
+#include "cfc_ptx.cuh"
+
+namespace cfc {
+namespace {
+
+constexpr int kRowLanes = 8;
+constexpr int kColLanes = 32;
+
+template <int VEC>
+__global__ void __launch_bounds__(kRowLanes * kColLanes) reduce_axis0_kernel(
+    const float* __restrict__ in, int n_batch, int n_tail, int rows_per_cta,
+    float* __restrict__ out) {
+  constexpr int TC = kColLanes * VEC;
+  __shared__ __align__(16) float part[kRowLanes][TC];
+  __shared__ __align__(16) float cta_sum[TC];
+  const int tid = threadIdx.x;
+  const int cl = tid % kColLanes, rl = tid / kColLanes;
+  const int col = blockIdx.x * TC + cl * VEC;
+  const int q = static_cast<int>(cluster_rank());
+  const int CZ = static_cast<int>(gridDim.y);
+  const int lo = q * rows_per_cta;
+  const int hi = min(n_batch, lo + rows_per_cta);
+
+  float acc[VEC];
+#pragma unroll
+  for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+  if (col < n_tail) {
+    if constexpr (VEC == 4) {
+      const float* base = in + col;
+      int r = lo + rl;
+      for (; r + 3 * kRowLanes < hi; r += 4 * kRowLanes) {
+        const float4 v0 = __ldg(reinterpret_cast<const float4*>(base + static_cast<size_t>(r) * n_tail));
+        const float4 v1 = __ldg(reinterpret_cast<const float4*>(base + static_cast<size_t>(r + kRowLanes) * n_tail));
+        const float4 v2 = __ldg(reinterpret_cast<const float4*>(base + static_cast<size_t>(r + 2 * kRowLanes) * n_tail));
+        const float4 v3 = __ldg(reinterpret_cast<const float4*>(base + static_cast<size_t>(r + 3 * kRowLanes) * n_tail));
+        acc[0] += v0.x; acc[1] += v0.y; acc[2] += v0.z; acc[3] += v0.w;
+        acc[0] += v1.x; acc[1] += v1.y; acc[2] += v1.z; acc[3] += v1.w;
+        acc[0] += v2.x; acc[1] += v2.y; acc[2] += v2.z; acc[3] += v2.w;
+        acc[0] += v3.x; acc[1] += v3.y; acc[2] += v3.z; acc[3] += v3.w;
+      }
+      for (; r < hi; r += kRowLanes) {
+        const float4 v0 = __ldg(reinterpret_cast<const float4*>(base + static_cast<size_t>(r) * n_tail));
+        acc[0] += v0.x; acc[1] += v0.y; acc[2] += v0.z; acc[3] += v0.w;
+      }
+    } else {
+      const float* base = in + col;
+      int r = lo + rl;
+      for (; r + 3 * kRowLanes < hi; r += 4 * kRowLanes) {
+        const float v0 = __ldg(base + static_cast<size_t>(r) * n_tail);
+        const float v1 = __ldg(base + static_cast<size_t>(r + kRowLanes) * n_tail);
+        const float v2 = __ldg(base + static_cast<size_t>(r + 2 * kRowLanes) * n_tail);
+        const float v3 = __ldg(base + static_cast<size_t>(r + 3 * kRowLanes) * n_tail);
+        acc[0] += v0; acc[0] += v1; acc[0] += v2; acc[0] += v3;
+      }
+      for (; r < hi; r += kRowLanes) acc[0] += __ldg(base + static_cast<size_t>(r) * n_tail);
+    }
+  }
+#pragma unroll
+  for (int v = 0; v < VEC; ++v) part[rl][cl * VEC + v] = acc[v];
+  __syncthreads();
+  for (int c = tid; c < TC; c += kRowLanes * kColLanes) {
+    float sacc = part[0][c];
+#pragma unroll
+    for (int l = 1; l < kRowLanes; ++l) sacc += part[l][c];
+    cta_sum[c] = sacc;
+  }
+  if (CZ == 1) {
+    __syncthreads();
+    for (int c = tid; c < TC; c += kRowLanes * kColLanes) {
+      const int n = blockIdx.x * TC + c;
+      if (n < n_tail) out[n] = cta_sum[c];
+    }
+    return;
+  }
+  cluster_sync_all();
+  if (q == 0) {
+    for (int c = tid; c < TC; c += kRowLanes * kColLanes) {
+      const uint32_t a = smem_addr(&cta_sum[c]);
+      float sacc = cta_sum[c];
+      for (int qq = 1; qq < CZ; ++qq) sacc += ld_shared_cluster_f32(map_to_rank(a, qq));
+      const int n = blockIdx.x * TC + c;
+      if (n < n_tail) out[n] = sacc;
+    }
+  }
+  cluster_sync_all();
+}
+
+int choose_cz(int n_batch) {
+  int cz = (n_batch + 127) / 128;
+  if (cz < 1) cz = 1;
+  if (cz > kMaxClusterSize) cz = kMaxClusterSize;
+  return cz;
+}
+
+template <int VEC>
+cudaError_t launch_vec(const float* in, int n_batch, int n_tail, float* out, cudaStream_t s) {
+  constexpr int TC = kColLanes * VEC;
+  const int cz = choose_cz(n_batch);
+  const int rows_per_cta = (n_batch + cz - 1) / cz;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((n_tail + TC - 1) / TC, cz, 1);
+  cfg.blockDim = dim3(kRowLanes * kColLanes, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = cz;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, reduce_axis0_kernel<VEC>, in, n_batch, n_tail, rows_per_cta,
+                            out);
+}
+
+}  // namespace
+
+cudaError_t reduce_axis0_prepare() {
+  cudaError_t e = cudaFuncSetAttribute(reduce_axis0_kernel<4>,
+                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(reduce_axis0_kernel<1>,
+                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
+cudaError_t reduce_axis0_launch(const float* in, int n_batch, int n_tail, float* out,
+                                cudaStream_t s) {
+  const bool vec = (n_tail % 4 == 0) && (reinterpret_cast<uintptr_t>(in) % 16 == 0);
+  return vec ? launch_vec<4>(in, n_batch, n_tail, out, s)
+             : launch_vec<1>(in, n_batch, n_tail, out, s);
+}
+
+}  // namespace cfc

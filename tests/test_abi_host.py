@@ -1,0 +1,133 @@
+"""The C ABI on the host: the library loads, exports every symbol of include/cfc.h, and rejects
+bad arguments with the documented status codes before it touches a GPU (no kernel runs)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from recurrent_cfc_cell_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cfc.h")
+
+OK, INVALID_DIM, NULL_PTR, MISALIGNED, WS_TOO_SMALL, UNSUPPORTED = 0, -1, -2, -3, -4, -5
+INVALID_ARG = -8
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_documented_entry_points():
+    assert set(declared_functions()) == set(_lib.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_error_strings(lib):
+    for code in (OK, INVALID_DIM, NULL_PTR, MISALIGNED, WS_TOO_SMALL, UNSUPPORTED, -6, -7,
+                 INVALID_ARG, -9, 12345):
+        s = lib.cfc_error_string(code)
+        assert isinstance(s, bytes) and len(s) > 0
+
+
+def ws_bytes(lib, B, K, C, n_x, mode=0):
+    out = ctypes.c_size_t(0)
+    rc = lib.cfc_workspace_bytes(B, K, C, n_x, mode, ctypes.byref(out))
+    return rc, out.value
+
+
+@pytest.mark.parametrize("B,K,C,n_x", [(4, 8, 32, 16), (32, 64, 128, 48), (32, 64, 256, 64),
+                                        (256, 64, 128, 48), (2048, 128, 256, 64), (1, 1, 1, 1),
+                                        (3, 5, 40, 5)])
+def test_workspace_holds_d_pre(lib, B, K, C, n_x):
+    rc, n = ws_bytes(lib, B, K, C, n_x)
+    assert rc == OK
+    assert n >= K * B * 4 * C * 4
+
+
+@pytest.mark.parametrize("B,K,C,n_x", [(0, 8, 32, 16), (4, 0, 32, 16), (4, 8, 0, 16),
+                                        (4, 8, 32, 0), (4, 8, 257, 16), (4, 8, 256, 65),
+                                        (-1, 8, 32, 16)])
+def test_invalid_dims(lib, B, K, C, n_x):
+    assert ws_bytes(lib, B, K, C, n_x)[0] == INVALID_DIM
+    fake = ctypes.c_void_p(0x10000)
+    rc = lib.cfc_forward(fake, fake, fake, fake, fake, B, K, C, n_x, fake, fake, None)
+    assert rc == INVALID_DIM
+
+
+def test_invalid_dw_mode(lib):
+    assert ws_bytes(lib, 4, 8, 32, 16, mode=7)[0] == INVALID_ARG
+    f = ctypes.c_void_p(0x10000)
+    rc = lib.cfc_backward(f, f, f, f, f, f, f, 4, 8, 32, 16, f, f, f, f, f, 1 << 30, 7, None)
+    assert rc == INVALID_ARG
+
+
+def test_null_and_misaligned_pointers(lib):
+    f = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10004)
+    args = [f] * 5
+    for k in range(5):
+        a = list(args)
+        a[k] = None
+        assert lib.cfc_forward(*a, 4, 8, 32, 16, f, f, None) == NULL_PTR
+        a[k] = odd
+        assert lib.cfc_forward(*a, 4, 8, 32, 16, f, f, None) == MISALIGNED
+    assert lib.cfc_forward(*args, 4, 8, 32, 16, None, f, None) == NULL_PTR
+    assert lib.cfc_forward(*args, 4, 8, 32, 16, f, odd, None) == MISALIGNED
+    # backward: du may be NULL, everything else may not
+    b7 = [f] * 7
+    outs = [f, f, f, f, f]  # dW, db, du, dh0, ws
+    for k in (0, 1, 3, 4):
+        o = list(outs)
+        o[k] = None
+        assert lib.cfc_backward(*b7, 4, 8, 32, 16, *o, 1 << 30, 0, None) == NULL_PTR
+    o = list(outs)
+    o[4] = odd
+    assert lib.cfc_backward(*b7, 4, 8, 32, 16, *o, 1 << 30, 0, None) == MISALIGNED
+    assert lib.reduce_axis0(None, 4, 4, f, None) == NULL_PTR
+    assert lib.reduce_axis0(ctypes.c_void_p(0x10002), 4, 4, f, None) == MISALIGNED
+    assert lib.reduce_axis0(f, 0, 4, f, None) == INVALID_DIM
+    assert lib.reduce_axis0(f, 4, -3, f, None) == INVALID_DIM
+
+
+def test_short_workspace(lib):
+    f = ctypes.c_void_p(0x10000)
+    rc, need = ws_bytes(lib, 4, 8, 32, 16)
+    assert rc == OK
+    assert lib.cfc_backward(*([f] * 7), 4, 8, 32, 16, f, f, f, f, f, need - 1, 0,
+                            None) == WS_TOO_SMALL
+
+
+def test_no_device_is_reported_not_crashed(lib):
+    """On a machine without a GPU a well-formed call reports UNSUPPORTED_DEVICE."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    f = ctypes.c_void_p(0x10000)
+    assert lib.cfc_forward(*([f] * 5), 4, 8, 32, 16, f, f, None) == UNSUPPORTED
+    st = ctypes.c_int(0)
+    assert lib.cfc_device_status(ctypes.byref(st)) == UNSUPPORTED
+
+
+def test_binding_refuses_missing_library(tmp_path):
+    with pytest.raises(ImportError):
+        _lib.load(str(tmp_path / "libcfc.so"))

@@ -1,0 +1,102 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Tolerances (max|x - y| / max|y| per tensor): 1e-5 on H and the cached activations, 1e-4 on
+dW, db, du, dh0 and the pre-activation gradients."""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_helpers import GRAD_TOL, H_TOL, assert_parity, oracle_ref, run_gpu
+from recurrent_cfc_cell_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2, 3])
+def test_workload_parity(idx):
+    inp = inputs.make_inputs(inputs.CONFIGS[idx])
+    assert_parity(run_gpu(inp), oracle_ref(inp))
+
+
+RAGGED = [
+    dict(B=5, K=7, n_x=5, C=40),      # channels not a multiple of 16, odd n_x
+    dict(B=3, K=1, n_x=3, C=16),      # single step
+    dict(B=1, K=3, n_x=1, C=1),       # degenerate widths
+    dict(B=7, K=11, n_x=13, C=100),   # ragged everything
+    dict(B=2, K=5, n_x=64, C=256),    # widest supported state and input
+    dict(B=33, K=4, n_x=7, C=129),    # 16-CTA cluster with 127 padded channels
+    dict(B=70, K=3, n_x=48, C=128),   # more rows than one wave of clusters holds at R=1
+    dict(B=1, K=2, n_x=320 - 16, C=16),  # widest input at one CTA per cluster
+]
+
+
+@pytest.mark.parametrize("shape", RAGGED, ids=lambda s: "B{B}_K{K}_nx{n_x}_C{C}".format(**s))
+def test_ragged_parity(shape):
+    inp = inputs.make_inputs(inputs.custom(seed=17, **shape))
+    assert_parity(run_gpu(inp), oracle_ref(inp))
+
+
+def test_graph_replay_parity():
+    inp = inputs.make_inputs(inputs.CONFIGS[1])
+    assert_parity(run_gpu(inp, graph=True), oracle_ref(inp))
+
+
+def test_without_du():
+    inp = inputs.make_inputs(inputs.custom(B=4, K=6, n_x=10, C=48, seed=3))
+    g = run_gpu(inp, with_du=False)
+    assert "du" not in g
+    assert_parity(g, oracle_ref(inp), keys=("H", "dW", "db", "dh0"))
+
+
+def test_simt_fp32_mode_parity():
+    inp = inputs.make_inputs(inputs.CONFIGS[1])
+    assert_parity(run_gpu(inp, dw_mode=2), oracle_ref(inp))
+
+
+def test_zero_upstream_gradient_gives_zero_gradients():
+    inp = inputs.make_inputs(inputs.custom(B=4, K=5, n_x=8, C=32, seed=9))
+    inp["dH"][:] = 0.0
+    g = run_gpu(inp)
+    for k in ("dW", "db", "du", "dh0", "d_pre"):
+        assert np.all(g[k] == 0.0), k
+
+
+def test_ts_zero_gives_zero_time_a_gradient():
+    inp = inputs.make_inputs(inputs.custom(B=4, K=5, n_x=8, C=32, seed=9))
+    inp["ts"][:] = 0.0
+    g = run_gpu(inp)
+    assert np.all(g["d_pre"][:, :, 2] == 0.0)
+    assert np.max(np.abs(g["dW"][2])) <= 1e-6 * np.max(np.abs(g["dW"][3]))
+    assert_parity(g, oracle_ref(inp))
+
+
+@pytest.mark.slow
+def test_stress_workload_sampled_rows_and_contraction():
+    """Throughput-stress workload (B=2048, K=128, C=256) in the launch configuration the
+    benchmark times.  Batch rows are independent, so the oracle runs four sampled rows alone
+    and every per-row output (H, cache, d_pre, du, dh0) is compared on those rows.  dW and db
+    are sums over all rows; they are checked as the fp64 contraction of the kernel's own d_pre
+    with z = [u ; h_{t-1}] (a property that holds at any size)."""
+    import torch
+
+    w = inputs.CONFIGS[4]
+    inp = inputs.make_inputs(w)
+    g = run_gpu(inp)
+    rows = np.array([0, 777, 1500, w.B - 1])
+    sub = {"u": inp["u"][:, rows], "h0": inp["h0"][rows], "W": inp["W"], "b": inp["b"],
+           "ts": inp["ts"][:, rows], "dH": inp["dH"][:, rows]}
+    ref = oracle_ref(sub)
+    gsub = {"H": g["H"][:, rows], "cache": g["cache"][:, rows], "d_pre": g["d_pre"][:, rows],
+            "du": g["du"][:, rows], "dh0": g["dh0"][rows]}
+    assert_parity(gsub, ref, keys=("H", "cache", "d_pre", "du", "dh0"))
+
+    K, B, n_x = inp["u"].shape
+    C = inp["h0"].shape[1]
+    d_pre = torch.from_numpy(g["d_pre"]).reshape(K * B, 4 * C).double()
+    hprev = np.concatenate([inp["h0"][None], g["H"][:-1]], axis=0)
+    z = torch.from_numpy(np.concatenate([inp["u"], hprev], axis=2).reshape(K * B, n_x + C)).double()
+    dW_ref = (d_pre.T @ z).reshape(4, C, n_x + C).numpy()
+    db_ref = d_pre.sum(0).reshape(4, C).numpy()
+    assert oracle.rel_err(g["dW"], dW_ref) <= GRAD_TOL
+    assert oracle.rel_err(g["db"], db_ref) <= GRAD_TOL
+    assert H_TOL <= GRAD_TOL
