@@ -162,12 +162,19 @@ def step(inp: dict) -> dict:
     return default().step(inp)
 
 
-def rel_err(x, y) -> float:
-    """max|x - y| / max|y| over a whole tensor (the parity metric; 0 when both are all zero)."""
+FP32_NORMAL_MIN = 2.0 ** -126
+
+
+def rel_err(x, y, floor: float = FP32_NORMAL_MIN) -> float:
+    """max|x - y| / max(max|y|, floor) over a whole tensor (the parity metric).
+
+    The floor is fp32's smallest normal number: a tensor whose exact values all lie below
+    fp32's normal range (for instance dh0 after a hundred decaying steps) cannot be carried with
+    relative precision by an fp32 computation, so it is compared in absolute terms there.
+    """
     x = np.asarray(x, dtype=np.float64)
     y = np.asarray(y, dtype=np.float64)
-    den = float(np.max(np.abs(y))) if y.size else 0.0
-    num = float(np.max(np.abs(x - y))) if y.size else 0.0
-    if den == 0.0:
-        return num
-    return num / den
+    if y.size == 0:
+        return 0.0
+    den = max(float(np.max(np.abs(y))), floor)
+    return float(np.max(np.abs(x - y))) / den
