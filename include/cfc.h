@@ -30,9 +30,7 @@
  *     on the device (the first call per device and size class sets kernel attributes).
  *   - Status: 0 on success, a negative CFC_ERR_* code otherwise; argument errors are detected
  *     on the host before any work is enqueued.  Nothing aborts or throws.
- *   - Size envelope of the recurrence kernels: 1 <= C <= 256; n_x >= 1 with
- *     roundup(n_x, 4) + 16 * cs(C) <= 320 where cs(C) is the smallest power of two >= C/16;
- *     B, K >= 1 with K * B * 4 * C < 2^31.
+ *   - Size envelope: 1 <= C <= 256, 1 <= n_x <= 512, B >= 1, K >= 1, K * B * 4 * C < 2^31.
  */
 #ifndef CFC_H
 #define CFC_H

@@ -78,13 +78,10 @@ int cluster_size_for(int C) {
   return cs;
 }
 
-int round_up4(int x) { return (x + 3) & ~3; }
-
 int check_dims(int B, int K, int C, int n_x) {
   if (B <= 0 || K <= 0 || C <= 0 || n_x <= 0) return CFC_ERR_INVALID_DIM;
   if (C > cfc::kChanPerCta * cfc::kMaxClusterSize) return CFC_ERR_INVALID_DIM;
-  const int cs = cluster_size_for(C);
-  if (cfc::fwd_kw_for(round_up4(n_x), cs) < 0) return CFC_ERR_INVALID_DIM;
+  if (n_x > cfc::kMaxInputs) return CFC_ERR_INVALID_DIM;
   const long long pre = 4LL * K * B * C;
   if (pre >= (1LL << 31)) return CFC_ERR_INVALID_DIM;
   return CFC_OK;
@@ -99,7 +96,7 @@ int max_clusters(DeviceState& st, int kind, int variant, int CS, size_t smem, in
     return CFC_OK;
   }
   int n = 0;
-  const cudaError_t e = (kind == 0) ? cfc::fwd_prepare(variant, CS, smem, &n)
+  const cudaError_t e = (kind == 0) ? cfc::fwd_prepare(CS, variant, smem, &n)
                                     : cfc::bwd_prepare(CS, smem, &n);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
@@ -113,15 +110,15 @@ int max_clusters(DeviceState& st, int kind, int variant, int CS, size_t smem, in
 // Rows per cluster: the smallest R (power of two, <= 32) whose clusters all fit in one wave,
 // else the largest that fits at all.  Results never depend on R (each row's arithmetic is the
 // same whatever the grouping).
-int plan_rows(DeviceState& st, int kind, int variant, int CS, int B, int NZp, int* R_out,
+int plan_rows(DeviceState& st, int kind, int variant, int CS, int B, int n_x, int* R_out,
               size_t* smem_out, int* clusters_out) {
   int best_R = 0;
   size_t best_smem = 0;
-  for (int R = 1; R <= cfc::kMaxRowsPerCluster; R *= 2) {
-    const size_t smem = (kind == 0) ? cfc::fwd_smem_bytes(R, NZp) : cfc::bwd_smem_bytes(R);
-    if (smem > 227 * 1024) break;
+  const int r_max = (kind == 0) ? cfc::kMaxFwdRows : cfc::kMaxRowsPerCluster;
+  for (int R = 1; R <= r_max; R *= 2) {
+    const size_t smem = (kind == 0) ? cfc::fwd_smem_bytes(R, CS) : cfc::bwd_smem_bytes(R, CS);
     int n = 0;
-    const int rc = max_clusters(st, kind, variant, CS, smem, &n);
+    const int rc = max_clusters(st, kind, (kind == 0) ? R : variant, CS, smem, &n);
     if (rc != CFC_OK) return rc;
     if (n <= 0) break;
     best_R = R;
@@ -203,15 +200,14 @@ int cfc_forward(const float* u, const float* h0, const float* W, const float* b,
   p.status = st->status;
   p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
   p.CS = cluster_size_for(C);
-  p.nxp = round_up4(n_x);
-  const int KW = cfc::fwd_kw_for(p.nxp, p.CS);
-  p.NZp = 4 * KW;
   size_t smem = 0;
   int n_clusters = 0;
-  rc = plan_rows(*st, 0, KW, p.CS, B, p.NZp, &p.R, &smem, &n_clusters);
+  rc = plan_rows(*st, 0, 0, p.CS, B, n_x, &p.R, &smem, &n_clusters);
   if (rc != CFC_OK) return rc;
-  return cuda_rc(cfc::fwd_launch(KW, p, n_clusters, smem, static_cast<cudaStream_t>(stream)),
-                 CFC_ERR_LAUNCH_FAILED);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = cuda_rc(cfc::inproj_launch(u, W, b, B * K, C, n_x, H, cache, s), CFC_ERR_LAUNCH_FAILED);
+  if (rc != CFC_OK) return rc;
+  return cuda_rc(cfc::fwd_launch(p, n_clusters, smem, s), CFC_ERR_LAUNCH_FAILED);
 }
 
 int cfc_backward_recurrence(const float* dH, const float* W, const float* ts,
@@ -234,7 +230,7 @@ int cfc_backward_recurrence(const float* dH, const float* W, const float* ts,
   p.CS = cluster_size_for(C);
   size_t smem = 0;
   int n_clusters = 0;
-  rc = plan_rows(*st, 1, p.CS, p.CS, B, 0, &p.R, &smem, &n_clusters);
+  rc = plan_rows(*st, 1, 0, p.CS, B, n_x, &p.R, &smem, &n_clusters);
   if (rc != CFC_OK) return rc;
   return cuda_rc(cfc::bwd_launch(p, n_clusters, smem, static_cast<cudaStream_t>(stream)),
                  CFC_ERR_LAUNCH_FAILED);

@@ -14,170 +14,244 @@
 //   ds      = dh (ff2 - ff1) gate (1 - gate),  dP_ta = ds ts[t,b],  dP_tb = ds
 //   delta  <- W_h^T d_pre[t]      (W_h = the C recurrent columns of W);   dh0 = final delta.
 //
-// Layout: a cluster of CS CTAs serves R batch rows; CTA `rank` owns channels
-// [16*rank, 16*rank+16) and its 64 W rows.  Thread (j, rg) keeps W_h[rows of group rg][j] in
-// registers (4*CS values), computes the partial delta[j] over its rows and pushes it with
-// st.async to the CTA that owns channel j, into slot (rank, rg).  The owner adds its 16 slots
-// in a fixed order, so the result is bitwise reproducible.
+// Layout and schedule (every step is warp-local; no CTA-wide barrier inside the K-loop):
+//   * a cluster of CS CTAs serves R batch rows; CTA `rank` owns channels [16*rank, 16*rank+16)
+//     and warp w owns channels 16*rank + 2w + {0, 1};
+//   * every CTA pushes its 64 new d_pre values (16 channels x 4 gates) to every CTA with
+//     st.async (one 16-byte push per channel and destination), so each CTA holds the whole
+//     d_pre[t] vector (4C values) after one mbarrier wait;
+//   * warp w keeps the two W_h^T columns of its channels in REGISTERS, lane l holding both
+//     columns over the l-th thirty-second of the 4C gathered rows (2*CS rows), so every d_pre
+//     value loaded from shared memory feeds two FMAs; a 5-shuffle butterfly gives delta for
+//     channel 0 in lanes 0-15 and channel 1 in lanes 16-31, and the same warp forms dh, the
+//     four d_pre values of each channel and the pushes.  The gathered vector is stored in
+//     thirty-two slices padded to an odd number of 16-byte chunks, so the vector loads of a
+//     quarter-warp hit distinct banks.  The summation order is fixed: bitwise reproducible;
+//   * dH, ff1, ff2, gate and ts for a step arrive two steps ahead through a cp.async ring
+//     (10 lanes of each warp copy, the warp reads after __syncwarp), so no global-memory
+//     latency sits on the serial chain.
 #include "cfc_kernels.h"
 #include "cfc_ptx.cuh"
 
 namespace cfc {
 namespace {
 
-constexpr int kSlots = 16;  // partial-delta contributions each channel receives (CS * RG)
+constexpr int kWarps = kRecThreads / 32;
+constexpr int kPre = 3;      // prefetch ring depth (copies run two steps ahead)
+constexpr int kPreComp = 5;  // dH, ff1, ff2, gate, ts
+
+// Lanes 16*ci + c (c < 5) copy component c of this warp's channel ci for step t.
+__device__ __forceinline__ void issue_pre(const BwdParams& p, float* pre, int t, int row0,
+                                          int rank, int warp, int lane) {
+  if (t < 0) return;
+  const int ci = lane >> 4, c = lane & 15;
+  if (c >= kPreComp) return;
+  const int ch = kChanPerCta * rank + 2 * warp + ci;
+  if (ch >= p.C) return;
+  for (int r = 0; r < p.R; ++r) {
+    const int b = row0 + r;
+    if (b >= p.B) break;
+    const size_t tb = static_cast<size_t>(t) * p.B + b;
+    const float* src = (c == 0) ? p.dH + tb * p.C + ch
+                     : (c == 4) ? p.ts + tb
+                                : p.cache + (tb * 3 + (c - 1)) * p.C + ch;
+    float* dst = pre + ((((t % kPre) * p.R + r) * kWarps + warp) * 2 + ci) * kPreComp + c;
+    cp_async_4(smem_addr(dst), src);
+  }
+}
 
 template <int CS>
-__global__ void __launch_bounds__(kRecThreads, 1) cfc_bwd_kernel(const BwdParams p) {
-  constexpr int RG = 16 / CS;          // row groups per CTA
-  constexpr int RPT = kRowsPerCta / RG;  // W rows per thread (= 4 * CS)
-  constexpr int CHP = kChanPerCta * CS;  // padded channel count
+struct BwdShape {
+  static constexpr int CHP = kChanPerCta * CS;  // padded channel count
+  static constexpr int NG = 4 * CHP;            // gathered d_pre values per row
+  static constexpr int RS = NG / 32;            // rows per lane (= 2 * CS)
+  // Slice pitch: vector loads of 8 consecutive lanes must cover distinct banks.
+  static constexpr int RSP = (RS >= 4 && (RS / 4) % 2 == 0) ? RS + 4 : RS;
+  static constexpr int GROW = 32 * RSP;         // gathered row in shared memory
+};
 
+template <int CS>
+__device__ __forceinline__ int gpos(int gidx) {
+  using S = BwdShape<CS>;
+  return (gidx / S::RS) * S::RSP + (gidx % S::RS);
+}
+
+// delta for both channels of this warp from this lane's slice of the gathered d_pre vector;
+// lanes 0-15 return channel 0, lanes 16-31 channel 1.
+template <int RS>
+__device__ __forceinline__ float gathered_delta(const float (&wt)[2][RS], const float* dvp,
+                                                int lane) {
+  float dv[RS];
+  if constexpr (RS % 4 == 0) {
+#pragma unroll
+    for (int k = 0; k < RS; k += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(dvp + k);
+      dv[k] = v.x; dv[k + 1] = v.y; dv[k + 2] = v.z; dv[k + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < RS; k += 2) {
+      const float2 v = *reinterpret_cast<const float2*>(dvp + k);
+      dv[k] = v.x; dv[k + 1] = v.y;
+    }
+  }
+  float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
+#pragma unroll
+  for (int k = 0; k < RS; k += 2) {
+    a0 = fmaf(wt[0][k], dv[k], a0);
+    a1 = fmaf(wt[1][k], dv[k], a1);
+    c0 = fmaf(wt[0][k + 1], dv[k + 1], c0);
+    c1 = fmaf(wt[1][k + 1], dv[k + 1], c1);
+  }
+  a0 += c0;
+  a1 += c1;
+  const bool hi = lane & 16;
+  float d = (hi ? a1 : a0) + __shfl_xor_sync(0xffffffffu, hi ? a0 : a1, 16);
+  d += __shfl_xor_sync(0xffffffffu, d, 8);
+  d += __shfl_xor_sync(0xffffffffu, d, 4);
+  d += __shfl_xor_sync(0xffffffffu, d, 2);
+  d += __shfl_xor_sync(0xffffffffu, d, 1);
+  return d;
+}
+
+template <int CS>
+__global__ void __launch_bounds__(kRecThreads, 2) cfc_bwd_kernel(const BwdParams p) {
+  using S = BwdShape<CS>;
   extern __shared__ __align__(16) float smem[];
   const int R = p.R;
-  float* dbuf = smem;                                  // [2][R][16 slots][16]
-  float* dps = dbuf + 2 * R * kSlots * kChanPerCta;    // [2][R][64]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(dps + 2 * R * kRowsPerCta);
-  int* abort_flag = reinterpret_cast<int*>(bars + 2);
+  float* dg = smem;                      // [2][R][GROW]  d_pre[t+1] for step t in dg[t & 1]
+  float* pre = dg + 2 * R * S::GROW;     // [kPre][R][8 warps][2][5]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pre + kPre * R * kWarps * 2 * kPreComp);
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
+  const int warp = tid >> 5;
   const int rank = static_cast<int>(cluster_rank());
   const int row0 = static_cast<int>(cluster_id_x()) * R;
   const int B = p.B, K = p.K, C = p.C, n_x = p.n_x, n_in = p.n_in;
 
-  // ---- W_h^T block of this thread: column j, rows [rg*RPT, rg*RPT + RPT) ----
-  const int j = tid % CHP;
-  const int rg = tid / CHP;
-  float w[RPT];
+  // W_h^T columns of this warp's two channels over gathered rows [lane*RS, lane*RS + RS).
+  // Gathered row q*64 + 4i + g is W row g*C + 16q + i.
+  float wt[2][S::RS];
 #pragma unroll
-  for (int k = 0; k < RPT; ++k) {
-    const int lrow = rg * RPT + k;
-    const int ch = kChanPerCta * rank + (lrow >> 2);
-    const int g = lrow & 3;
-    w[k] = (ch < C && j < C) ? p.W[(static_cast<size_t>(g) * C + ch) * n_in + n_x + j] : 0.f;
+  for (int cc = 0; cc < 2; ++cc) {
+    const int j = kChanPerCta * rank + 2 * warp + cc;
+#pragma unroll
+    for (int k = 0; k < S::RS; ++k) {
+      const int gidx = lane * S::RS + k;
+      const int chr = kChanPerCta * (gidx >> 6) + ((gidx & 63) >> 2);
+      wt[cc][k] = (chr < C && j < C)
+                      ? p.W[(static_cast<size_t>(gidx & 3) * C + chr) * n_in + n_x + j] : 0.f;
+    }
   }
-  // Destination of this thread's partial: owner CTA of channel j, slot (rank, rg).
-  const int owner = j / kChanPerCta;
-  const int slot = rank * RG + rg;
-
-  // Gate-phase identity: row lr = 4 i + g of this CTA.
-  const int lr = tid & 63;
-  const int gi = lr & 3;
-  const int ch = kChanPerCta * rank + (lr >> 2);
+  const int ci = lane >> 4;        // channel of this half-warp
+  const int gq = (lane >> 2) & 3;  // gate this lane's d_pre belongs to
+  const int q = lane & 15;         // destination CTA of this lane's push
+  const int ch = kChanPerCta * rank + 2 * warp + ci;
+  const int half = lane & 16;
 
   const uint32_t bar0 = smem_addr(&bars[0]);  // bars[s] lives at bar0 + 8 s
-  const uint32_t tx_bytes = static_cast<uint32_t>(R * kSlots * kChanPerCta * 4);
+  const uint32_t tx_bytes = static_cast<uint32_t>(CS * R * kRowsPerCta * 4);
   if (tid == 0) {
-    mbar_init((bar0 + 0u), 1);
-    mbar_init((bar0 + 8u), 1);
-    *abort_flag = 0;
+    mbar_init(bar0, 1);
+    mbar_init(bar0 + 8u, 1);
     fence_mbar_init_cluster();
   }
-  // Consumer c (= the step that reads delta; -1 is the dh0 epilogue) uses bars[c & 1].
+  for (int e = tid; e < 2 * R * S::GROW; e += kRecThreads) dg[e] = 0.f;
+  // Consumer c (the step that reads d_pre[c+1]; -1 is the dh0 epilogue) uses bars[c & 1].
   // Consumers run c = K-2 .. -1; arm the first two.
   if (tid == 0) {
-    mbar_arrive_expect_tx((bar0 + 8u * ((K - 2) & 1)), tx_bytes);
-    if (K >= 2) mbar_arrive_expect_tx((bar0 + 8u * ((K - 3) & 1)), tx_bytes);
+    mbar_arrive_expect_tx(bar0 + 8u * ((K - 2) & 1), tx_bytes);
+    if (K >= 2) mbar_arrive_expect_tx(bar0 + 8u * ((K - 3) & 1), tx_bytes);
   }
+  issue_pre(p, pre, K - 1, row0, rank, warp, lane);
+  cp_async_commit();
+  issue_pre(p, pre, K - 2, row0, rank, warp, lane);
+  cp_async_commit();
   cluster_sync_all();
 
   uint32_t phase = 0;
+  bool ok = true;
   for (int t = K - 1; t >= 0; --t) {
     const int s = t & 1;
-    const float* din = dbuf + s * R * kSlots * kChanPerCta;
-    float* dp_s = dps + s * R * kRowsPerCta;
+    // Ring: step t-2 goes into the slot step t+1 used; every lane of the warp has read it.
+    __syncwarp();
+    issue_pre(p, pre, t - 2, row0, rank, warp, lane);
+    cp_async_commit();
 
     if (t < K - 1) {
-      const bool ok = mbar_wait_bounded_cluster((bar0 + 8u * (s)), (phase >> s) & 1u, p.status);
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait_bounded_cluster(bar0 + 8u * s, (phase >> s) & 1u, p.status));
       phase ^= (1u << s);
-      if (!ok) *abort_flag = 1;
-      if (tid == 0 && t - 2 >= -1) mbar_arrive_expect_tx((bar0 + 8u * (s)), tx_bytes);
+      if (!ok) break;
+      if (tid == 0 && t - 2 >= -1) mbar_arrive_expect_tx(bar0 + 8u * s, tx_bytes);
     }
+    cp_async_wait<2>();  // the warp's copies for step t (groups t-1, t-2 may be pending)
+    __syncwarp();
 
-    // d_pre for (row r, channel ch, gate gi); delta summed over the 16 slots in fixed order.
-    for (int idx = tid; idx < R * kRowsPerCta; idx += kRecThreads) {
-      const int r = idx >> 6;
+    const float* pre_t = pre + ((t % kPre) * R * kWarps + warp) * 2 * kPreComp + ci * kPreComp;
+    float* dn = dg + (s ^ 1) * R * S::GROW;
+    for (int r = 0; r < R; ++r) {
+      const float delta =
+          (t < K - 1) ? gathered_delta<S::RS>(wt, dg + (s * R + r) * S::GROW + lane * S::RSP, lane)
+                      : 0.f;
       const int b = row0 + r;
-      float dsum = 0.f;
-      if (t < K - 1) {
-        const float* sl = din + r * kSlots * kChanPerCta + (lr >> 2);
-        dsum = ((sl[(4 * gi + 0) * kChanPerCta] + sl[(4 * gi + 1) * kChanPerCta]) +
-                sl[(4 * gi + 2) * kChanPerCta]) + sl[(4 * gi + 3) * kChanPerCta];
-      }
-      dsum += __shfl_xor_sync(0xffffffffu, dsum, 1);
-      dsum += __shfl_xor_sync(0xffffffffu, dsum, 2);
       float dpv = 0.f;
       if (b < B && ch < C) {
-        const size_t tb = static_cast<size_t>(t) * B + b;
-        const float dh = p.dH[tb * C + ch] + dsum;
-        const float f1 = p.cache[(tb * 3 + 0) * C + ch];
-        const float f2 = p.cache[(tb * 3 + 1) * C + ch];
-        const float g = p.cache[(tb * 3 + 2) * C + ch];
+        const float* pv = pre_t + r * kWarps * 2 * kPreComp;
+        const float dh = pv[0] + delta;
+        const float f1 = pv[1], f2 = pv[2], g = pv[3];
         const float ds = dh * (f2 - f1) * g * (1.f - g);
-        if (gi == 0) dpv = dh * (1.f - g) * (1.f - f1 * f1);
-        else if (gi == 1) dpv = dh * g * (1.f - f2 * f2);
-        else if (gi == 2) dpv = ds * p.ts[tb];
+        if (gq == 0) dpv = dh * (1.f - g) * (1.f - f1 * f1);
+        else if (gq == 1) dpv = dh * g * (1.f - f2 * f2);
+        else if (gq == 2) dpv = ds * pv[4];
         else dpv = ds;
-        p.d_pre[(tb * 4 + gi) * C + ch] = dpv;
+        if ((lane & 3) == 0)
+          p.d_pre[((static_cast<size_t>(t) * B + b) * 4 + gq) * C + ch] = dpv;
       }
-      dp_s[r * kRowsPerCta + lr] = dpv;
-    }
-    __syncthreads();
-    if (*abort_flag) break;
-
-    // Partial delta[j] over this thread's rows, for every batch row; push to the owner.
-    const int sn = s ^ 1;  // buffer of consumer t-1
-    float* dst_base = dbuf + sn * R * kSlots * kChanPerCta;
-    for (int r = 0; r < R; ++r) {
-      const float4* d4 = reinterpret_cast<const float4*>(dp_s + r * kRowsPerCta + rg * RPT);
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-      for (int k = 0; k < RPT / 4; ++k) {
-        const float4 v = d4[k];
-        a0 = fmaf(w[4 * k + 0], v.x, a0);
-        a1 = fmaf(w[4 * k + 1], v.y, a1);
-        a2 = fmaf(w[4 * k + 2], v.z, a2);
-        a3 = fmaf(w[4 * k + 3], v.w, a3);
-      }
-      const float acc = (a0 + a1) + (a2 + a3);
-      // Gather four consecutive channels into the lane whose j is a multiple of 4.
-      const float v1 = __shfl_down_sync(0xffffffffu, acc, 1);
-      const float v2 = __shfl_down_sync(0xffffffffu, acc, 2);
-      const float v3 = __shfl_down_sync(0xffffffffu, acc, 3);
-      if ((lane & 3) == 0) {
+      // The four gates of channel ci -> one 16-byte push to every CTA of the cluster.
+      const float d0 = __shfl_sync(0xffffffffu, dpv, half + 0);
+      const float d1 = __shfl_sync(0xffffffffu, dpv, half + 4);
+      const float d2 = __shfl_sync(0xffffffffu, dpv, half + 8);
+      const float d3 = __shfl_sync(0xffffffffu, dpv, half + 12);
+      if (q < CS) {
         const uint32_t dst =
-            smem_addr(dst_base + (r * kSlots + slot) * kChanPerCta + (j % kChanPerCta));
-        st_async_v4(map_to_rank(dst, owner), acc, v1, v2, v3, map_to_rank((bar0 + 8u * (sn)), owner));
+            smem_addr(dn + r * S::GROW + gpos<CS>(rank * kRowsPerCta + 4 * (2 * warp + ci)));
+        st_async_v4(map_to_rank(dst, q), d0, d1, d2, d3, map_to_rank(bar0 + 8u * (s ^ 1), q));
       }
     }
   }
 
-  // Epilogue: dh0 = delta after step 0 (consumer -1 reads bars[1]).
-  if (!*abort_flag) {
-    const bool ok = mbar_wait_bounded_cluster((bar0 + 8u), (phase >> 1) & 1u, p.status);
-    if (!__syncthreads_or(ok ? 0 : 1)) {
-      const float* din = dbuf + 1 * R * kSlots * kChanPerCta;
-      for (int idx = tid; idx < R * kRowsPerCta; idx += kRecThreads) {
-        const int r = idx >> 6;
+  // Epilogue: dh0 = W_h^T d_pre[0] (consumer -1 reads bars[1]).
+  if (ok) {
+    ok = __all_sync(0xffffffffu, mbar_wait_bounded_cluster(bar0 + 8u, (phase >> 1) & 1u, p.status));
+    if (ok) {
+      for (int r = 0; r < R; ++r) {
+        const float delta =
+            gathered_delta<S::RS>(wt, dg + (1 * R + r) * S::GROW + lane * S::RSP, lane);
         const int b = row0 + r;
-        const float* sl = din + r * kSlots * kChanPerCta + (lr >> 2);
-        float dsum = ((sl[(4 * gi + 0) * kChanPerCta] + sl[(4 * gi + 1) * kChanPerCta]) +
-                      sl[(4 * gi + 2) * kChanPerCta]) + sl[(4 * gi + 3) * kChanPerCta];
-        dsum += __shfl_xor_sync(0xffffffffu, dsum, 1);
-        dsum += __shfl_xor_sync(0xffffffffu, dsum, 2);
-        if (gi == 0 && b < B && ch < C) p.dh0[static_cast<size_t>(b) * C + ch] = dsum;
+        if (q == 0 && b < B && ch < C) p.dh0[static_cast<size_t>(b) * C + ch] = delta;
       }
     }
   }
+  cp_async_wait<0>();
   cluster_sync_all();
 }
 
 template <int CS>
 cudaError_t prepare_cs(size_t smem, int* max_active) {
-  cudaError_t e = cudaFuncSetAttribute(cfc_bwd_kernel<CS>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  // The attribute is a per-function maximum: set it to the device's opt-in limit once, so any
+  // row grouping chosen later (from cached occupancy results) can launch.
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  if (smem > static_cast<size_t>(optin)) {
+    *max_active = 0;
+    return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(cfc_bwd_kernel<CS>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(cfc_bwd_kernel<CS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
@@ -214,8 +288,10 @@ cudaError_t launch_cs(const BwdParams& p, int n_clusters, size_t smem, cudaStrea
 
 }  // namespace
 
-size_t bwd_smem_bytes(int R) {
-  return sizeof(float) * (2ull * R * kSlots * kChanPerCta + 2ull * R * kRowsPerCta) +
+size_t bwd_smem_bytes(int R, int CS) {
+  const size_t RS = 2ull * CS;
+  const size_t GROW = 32 * ((RS >= 4 && (RS / 4) % 2 == 0) ? RS + 4 : RS);
+  return sizeof(float) * (2ull * R * GROW + 1ull * kPre * R * kWarps * 2 * kPreComp) +
          2 * sizeof(uint64_t) + 16;
 }
 

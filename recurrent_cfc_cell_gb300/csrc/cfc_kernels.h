@@ -12,8 +12,9 @@ constexpr int kChanPerCta = 16;
 constexpr int kRowsPerCta = 4 * kChanPerCta;  // W rows held by one CTA (gate-minor order)
 constexpr int kRecThreads = 256;
 constexpr int kMaxClusterSize = 16;
-constexpr int kMaxZ = 320;      // padded z width the forward kernel holds in registers
-constexpr int kMaxRowsPerCluster = 32;
+constexpr int kMaxInputs = 512;  // largest n_x (W_u rows of a CTA live in shared memory)
+constexpr int kMaxRowsPerCluster = 32;  // backward recurrence
+constexpr int kMaxFwdRows = 4;         // forward recurrence (rows are a template parameter)
 
 struct FwdParams {
   const float* u;      // [K][B][n_x]
@@ -27,8 +28,6 @@ struct FwdParams {
   int B, K, C, n_x, n_in;
   int CS;              // CTAs per cluster
   int R;               // batch rows per cluster
-  int nxp;             // n_x rounded up to a multiple of 4
-  int NZp;             // padded z width (4 slices x KW)
 };
 
 struct BwdParams {
@@ -44,14 +43,17 @@ struct BwdParams {
 };
 
 // Recurrence kernels (persistent over all K steps, one cluster per group of R batch rows).
-int fwd_kw_for(int nxp, int CS);  // register width per K-slice, or -1 if unsupported
-size_t fwd_smem_bytes(int R, int NZp);
-cudaError_t fwd_prepare(int KW, int CS, size_t smem, int* max_active_clusters);
-cudaError_t fwd_launch(int KW, const FwdParams& p, int n_clusters, size_t smem, cudaStream_t s);
+size_t fwd_smem_bytes(int R, int CS);
+cudaError_t fwd_prepare(int CS, int R, size_t smem, int* max_active_clusters);
+cudaError_t fwd_launch(const FwdParams& p, int n_clusters, size_t smem, cudaStream_t s);
 
-size_t bwd_smem_bytes(int R);
+size_t bwd_smem_bytes(int R, int CS);
 cudaError_t bwd_prepare(int CS, size_t smem, int* max_active_clusters);
 cudaError_t bwd_launch(const BwdParams& p, int n_clusters, size_t smem, cudaStream_t s);
+
+// X = W_u u + b for all steps, written in place into H (gate ff1) and cache (ff2, ta, tb).
+cudaError_t inproj_launch(const float* u, const float* W, const float* bias, int BK, int C,
+                          int n_x, float* H, float* cache, cudaStream_t s);
 
 // Weight gradient, split over the B*K reduction: partial[s][m][n] for m < 4C, n < n_in.
 int dw_simt_splits(int BK);

@@ -58,16 +58,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
-// One non-blocking-ish probe of phase `parity` with cluster-scope acquire (remote st.async
-// data written into this CTA's shared memory is visible once it returns true).
+// Upper bound (ns) a waiting thread may stay suspended inside one try_wait; the hardware
+// resumes it as soon as the phase completes.  Suspended warps take no issue slots, so the
+// warps still computing on the same SM run at full speed.
+constexpr uint32_t kSuspendHintNs = 100000u;
+
+// Probe of phase `parity` with cluster-scope acquire (remote st.async data written into this
+// CTA's shared memory is visible once it returns true); may suspend the thread meanwhile.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -76,10 +81,10 @@ __device__ __forceinline__ bool mbar_try_wait_cta(uint32_t bar, uint32_t parity)
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -159,7 +164,23 @@ __device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t raddr) {
   return v;
 }
 
-// Accurate single-precision activations (no approximate hardware tanh / exp variants).
-__device__ __forceinline__ float sigmoid_acc(float x) { return 1.0f / (1.0f + expf(-x)); }
+// 4-byte asynchronous global -> shared copy (completion tracked per thread by commit groups).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's most recent commit groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Accurate single-precision sigmoid: expf, then a correctly rounded reciprocal (the same value
+// as the IEEE quotient 1 / (1 + e)); no approximate hardware exp / tanh variants.
+__device__ __forceinline__ float sigmoid_acc(float x) { return __frcp_rn(1.0f + expf(-x)); }
 
 }  // namespace cfc

@@ -64,7 +64,7 @@ def test_workspace_holds_d_pre(lib, B, K, C, n_x):
 
 
 @pytest.mark.parametrize("B,K,C,n_x", [(0, 8, 32, 16), (4, 0, 32, 16), (4, 8, 0, 16),
-                                        (4, 8, 32, 0), (4, 8, 257, 16), (4, 8, 256, 65),
+                                        (4, 8, 32, 0), (4, 8, 257, 16), (4, 8, 256, 513),
                                         (-1, 8, 32, 16)])
 def test_invalid_dims(lib, B, K, C, n_x):
     assert ws_bytes(lib, B, K, C, n_x)[0] == INVALID_DIM

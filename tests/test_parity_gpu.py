@@ -26,7 +26,9 @@ RAGGED = [
     dict(B=2, K=5, n_x=64, C=256),    # widest supported state and input
     dict(B=33, K=4, n_x=7, C=129),    # 16-CTA cluster with 127 padded channels
     dict(B=70, K=3, n_x=48, C=128),   # more rows than one wave of clusters holds at R=1
-    dict(B=1, K=2, n_x=320 - 16, C=16),  # widest input at one CTA per cluster
+    dict(B=1, K=2, n_x=512, C=16),    # widest input, one CTA per cluster
+    dict(B=3, K=4, n_x=301, C=256),   # wide input with the widest state
+    dict(B=40, K=9, n_x=64, C=256),   # rows grouped several per 16-CTA cluster
 ]
 
 
