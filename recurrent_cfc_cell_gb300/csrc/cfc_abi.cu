@@ -59,6 +59,11 @@ int device_state(DeviceState** out) {
       void* addr = nullptr;
       int rc = cuda_rc(cudaGetSymbolAddress(&addr, g_status_word), CFC_ERR_CUDA);
       if (rc == CFC_OK) rc = cuda_rc(cfc::reduce_axis0_prepare(), CFC_ERR_CUDA);
+      int optin = 0;
+      if (rc == CFC_OK)
+        rc = cuda_rc(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
+                     CFC_ERR_CUDA);
+      if (rc == CFC_OK) rc = cuda_rc(cfc::tc_prepare(optin), CFC_ERR_CUDA);
       if (rc != CFC_OK) return rc;  // retried on the next call
       st.status = static_cast<int*>(addr);
       st.init = true;
@@ -137,7 +142,9 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct BwdLayout {
   size_t d_pre_off, d_pre_bytes, part_off, part_bytes, total;
-  int S;
+  int S_simt;          // split count of the CUDA-core contraction
+  cfc::TcPlan tc;      // plan of the tensor-core weight-gradient contraction
+  cfc::TcPlan tu;      // plan of the tensor-core input-gradient contraction
 };
 
 BwdLayout bwd_layout(int B, int K, int C, int n_x) {
@@ -145,9 +152,18 @@ BwdLayout bwd_layout(int B, int K, int C, int n_x) {
   const size_t BK = static_cast<size_t>(B) * K;
   L.d_pre_off = 0;
   L.d_pre_bytes = BK * 4 * C * sizeof(float);
-  L.S = cfc::dw_simt_splits(static_cast<int>(BK));
+  L.S_simt = cfc::dw_simt_splits(static_cast<int>(BK));
+  L.tc = cfc::dw_tc_plan(B, K, C, n_x);
+  L.tu = cfc::du_tc_plan(B, K, C, n_x);
+  const int S = L.S_simt > L.tc.splits ? L.S_simt : L.tc.splits;
+  // The dW partials are consumed before du runs, so du's partials reuse the same area.
+  size_t part = static_cast<size_t>(S) * 4 * C * (n_x + C);
+  if (L.tu.splits > 1) {
+    const size_t pu = static_cast<size_t>(L.tu.splits) * BK * n_x;
+    if (pu > part) part = pu;
+  }
   L.part_off = align256(L.d_pre_bytes);
-  L.part_bytes = static_cast<size_t>(L.S) * 4 * C * (n_x + C) * sizeof(float);
+  L.part_bytes = part * sizeof(float);
   L.total = L.part_off + L.part_bytes;
   return L;
 }
@@ -256,14 +272,35 @@ int cfc_weight_grad(const float* d_pre, const float* u, const float* h0, const f
   float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + L.part_off);
   const int BK = B * K;
   const int M = 4 * C, N = n_x + C;
-  rc = cuda_rc(cfc::dw_simt_launch(d_pre, u, H, h0, B, K, C, n_x, L.S, partial, s),
-               CFC_ERR_LAUNCH_FAILED);
+  int S = 0;
+  if (dw_mode == CFC_DW_SIMT_FP32) {
+    S = L.S_simt;
+    rc = cuda_rc(cfc::dw_simt_launch(d_pre, u, H, h0, B, K, C, n_x, S, partial, s),
+                 CFC_ERR_LAUNCH_FAILED);
+  } else {
+    S = L.tc.splits;
+    rc = cuda_rc(cfc::dw_tc_launch(L.tc, d_pre, u, H, h0, B, K, C, n_x, partial, st->status, s),
+                 CFC_ERR_LAUNCH_FAILED);
+  }
   if (rc != CFC_OK) return rc;
-  rc = cuda_rc(cfc::reduce_axis0_launch(partial, L.S, M * N, dW, s), CFC_ERR_LAUNCH_FAILED);
+  rc = cuda_rc(cfc::reduce_axis0_launch(partial, S, M * N, dW, s), CFC_ERR_LAUNCH_FAILED);
   if (rc != CFC_OK) return rc;
   rc = cuda_rc(cfc::reduce_axis0_launch(d_pre, BK, M, db, s), CFC_ERR_LAUNCH_FAILED);
   if (rc != CFC_OK) return rc;
-  if (du) rc = cuda_rc(cfc::du_simt_launch(d_pre, W, BK, C, n_x, du, s), CFC_ERR_LAUNCH_FAILED);
+  if (du) {
+    if (dw_mode == CFC_DW_SIMT_FP32) {
+      rc = cuda_rc(cfc::du_simt_launch(d_pre, W, BK, C, n_x, du, s), CFC_ERR_LAUNCH_FAILED);
+    } else if (L.tu.splits == 1) {
+      rc = cuda_rc(cfc::du_tc_launch(L.tu, d_pre, W, B, K, C, n_x, du, st->status, s),
+                   CFC_ERR_LAUNCH_FAILED);
+    } else {
+      rc = cuda_rc(cfc::du_tc_launch(L.tu, d_pre, W, B, K, C, n_x, partial, st->status, s),
+                   CFC_ERR_LAUNCH_FAILED);
+      if (rc == CFC_OK)
+        rc = cuda_rc(cfc::reduce_axis0_launch(partial, L.tu.splits, BK * n_x, du, s),
+                     CFC_ERR_LAUNCH_FAILED);
+    }
+  }
   return rc;
 }
 

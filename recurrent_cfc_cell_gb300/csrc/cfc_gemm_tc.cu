@@ -1,0 +1,395 @@
+// cfc_gemm_tc.cu -- the two dense contractions of the backward pass on the 5th-generation
+// tensor cores (tcgen05, accumulator in tensor memory):
+//
+//   dW[m][n] = sum_{r < B*K} d_pre[r][m] * z[r][n],   m < 4C, n < n_in,  z[r] = [u[r] ; h_{r-B}]
+//   du[r][k] = sum_{m < 4C}  d_pre[r][m] * W[m][k],   k < n_x
+//
+// (h_{r-B} is h0[r] for the first B rows).  The DQN plan on page "H100 Epoch Optimization
+// Phase 2" (Task 2) replaces per-sample atomic weight-gradient accumulation by one GEMM over
+// the batch, "dW = dY^T X"; here the sum runs over batch and time, B*K rows.
+//
+// Precision: operands are fp32.  Each is split into bf16 hi = bf16(x) and lo = bf16(x - hi),
+// and the tile product is hi*hi + hi*lo + lo*hi (three tcgen05.mma per 16-row step, fp32
+// accumulation in TMEM), which keeps the per-product relative error near 2^-16 -- well inside
+// the 1e-4 gradient tolerance, where a single bf16 pass (2^-9) is not.
+//
+// One kernel template serves both: a CTA computes a 128 x n_tile output block over a range of
+// the reduction index.  Warps 0-7 load fp32 operand rows (coalesced; two items per thread in
+// flight), split them and write the bf16 halves into 128-byte-swizzled K-major tiles (64
+// reduction entries per stage, two stages); warp 8 owns the TMEM accumulator and one lane
+// issues the MMAs; mbarriers hand the stages back and forth; after the last stage warps 0-7
+// read the accumulator with tcgen05.ld and store it.  When there are fewer output tiles than
+// about one per SM the reduction index is split, each split writing a partial block, and
+// reduce_axis0 sums the splits in order (bitwise reproducible; the split depends only on the
+// sizes).
+#include <cuda_bf16.h>
+
+#include "cfc_kernels.h"
+#include "cfc_ptx.cuh"
+
+namespace cfc {
+namespace {
+
+constexpr int kTcM = 128;          // rows of the output tile (UMMA M)
+constexpr int kTcK = 64;           // reduction rows per stage (128 bytes of bf16)
+constexpr int kStages = 2;
+constexpr int kConv = 256;         // converter / epilogue threads (warps 0-7)
+constexpr int kTcThreads = kConv + 32;
+
+struct TcParams {
+  const float* d_pre;  // [BK][4C]
+  const float* u;      // [BK][n_x]
+  const float* H;      // [BK][C]
+  const float* h0;     // [B][C]
+  const float* W;      // [4C][n_in]
+  float* out;          // dW partials [S][4C][n_in]  or  du [BK][n_x]
+  int* status;
+  int B, BK, C, n_x, n_in;
+  int rows, cols;      // output rows / columns of the GEMM (dW: 4C x n_in; du: BK x n_x)
+  int red;             // length of the reduction index (dW: BK; du: 4C)
+  int n_tile, m_tiles, kb_per_split, n_kb;
+  int vec;             // operand rows can be read as float4 (n_x % 4 == 0 and C % 4 == 0)
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 a, __nv_bfloat16 b) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+}
+
+// Split 8 fp32 values (consecutive reduction rows of one tile row) into hi / lo bf16 chunks and
+// store both 16-byte chunks at their swizzled position.
+__device__ __forceinline__ void store_split_chunk(uint8_t* hi_tile, uint8_t* lo_tile, int row,
+                                                  int kchunk, const float (&v)[8]) {
+  __nv_bfloat16 h[8], l[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    h[i] = __float2bfloat16_rn(v[i]);
+    l[i] = __float2bfloat16_rn(v[i] - __bfloat162float(h[i]));
+  }
+  const uint32_t off = sw128_offset(row, kchunk * 8);
+  *reinterpret_cast<uint4*>(hi_tile + off) =
+      make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]),
+                 pack_bf16x2(h[6], h[7]));
+  *reinterpret_cast<uint4*>(lo_tile + off) =
+      make_uint4(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]), pack_bf16x2(l[4], l[5]),
+                 pack_bf16x2(l[6], l[7]));
+}
+
+__device__ __forceinline__ float4 z_quad(const TcParams& p, int r, int n) {
+  if (n >= p.n_in) return make_float4(0.f, 0.f, 0.f, 0.f);
+  if (n < p.n_x) return __ldg(reinterpret_cast<const float4*>(p.u + static_cast<size_t>(r) * p.n_x + n));
+  const int j = n - p.n_x;
+  const float* src = (r >= p.B) ? p.H + static_cast<size_t>(r - p.B) * p.C + j
+                                : p.h0 + static_cast<size_t>(r) * p.C + j;
+  return __ldg(reinterpret_cast<const float4*>(src));
+}
+
+__device__ __forceinline__ float z_at(const TcParams& p, int r, int n) {
+  if (n >= p.n_in) return 0.f;
+  if (n < p.n_x) return __ldg(p.u + static_cast<size_t>(r) * p.n_x + n);
+  const int j = n - p.n_x;
+  return (r >= p.B) ? __ldg(p.H + static_cast<size_t>(r - p.B) * p.C + j)
+                    : __ldg(p.h0 + static_cast<size_t>(r) * p.C + j);
+}
+
+// Weight gradient: A = d_pre^T (rows m, reduction r), B = z^T (rows n, reduction r).
+// Item = (4 consecutive tile rows, 8 consecutive reduction rows); the 8 threads of a
+// quarter-warp take the 8 chunks of one row quad, so their 16-byte stores hit distinct banks.
+// Load 8 consecutive reduction entries of 4 consecutive rows (a "row quad") of d_pre^T:
+// d_pre[r0 + 8c + i][m .. m+3], i < 8.
+__device__ __forceinline__ void load_dpre_quad(const TcParams& p, int m, int r0c, float (&v)[4][8]) {
+  const int M = 4 * p.C;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = r0c + i;
+    float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < p.BK && m < M)
+      q = __ldg(reinterpret_cast<const float4*>(p.d_pre + static_cast<size_t>(r) * M + m));
+    v[0][i] = q.x; v[1][i] = q.y; v[2][i] = q.z; v[3][i] = q.w;
+  }
+}
+
+// The same for z^T: z[r0 + 8c + i][n .. n+3].
+__device__ __forceinline__ void load_z_quad(const TcParams& p, int n, int r0c, float (&v)[4][8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = r0c + i;
+    float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < p.BK) {
+      if (p.vec) {
+        q = z_quad(p, r, n);
+      } else {
+        q.x = z_at(p, r, n);
+        q.y = z_at(p, r, n + 1);
+        q.z = z_at(p, r, n + 2);
+        q.w = z_at(p, r, n + 3);
+      }
+    }
+    v[0][i] = q.x; v[1][i] = q.y; v[2][i] = q.z; v[3][i] = q.w;
+  }
+}
+
+// The same for W_u^T: W[m0 + 8c + i][n .. n+3] (columns >= n_x read as 0).
+__device__ __forceinline__ void load_wu_quad(const TcParams& p, int n, int m0c, float (&v)[4][8]) {
+  const int M = 4 * p.C;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int m = m0c + i;
+    float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (m < M) {
+      const float* src = p.W + static_cast<size_t>(m) * p.n_in + n;
+      if (p.vec && n < p.n_x) {
+        q = __ldg(reinterpret_cast<const float4*>(src));
+      } else {
+        q.x = (n < p.n_x) ? __ldg(src) : 0.f;
+        q.y = (n + 1 < p.n_x) ? __ldg(src + 1) : 0.f;
+        q.z = (n + 2 < p.n_x) ? __ldg(src + 2) : 0.f;
+        q.w = (n + 3 < p.n_x) ? __ldg(src + 3) : 0.f;
+      }
+    }
+    v[0][i] = q.x; v[1][i] = q.y; v[2][i] = q.z; v[3][i] = q.w;
+  }
+}
+
+// Row-quad items (4 tile rows x 8 reduction entries), two per thread at a time with all loads
+// issued before the stores.  The 8 threads of a quarter-warp take the 8 chunks of one quad, so
+// their 16-byte stores hit distinct banks.
+template <class Load>
+__device__ __forceinline__ void convert_quads(int n_quads, int row_base, int k_base, int tid,
+                                              uint8_t* hi, uint8_t* lo, Load load) {
+  const int n_items = n_quads * 8;
+  for (int it = tid; it < n_items; it += 2 * kConv) {
+    const int it1 = it + kConv;
+    float v0[4][8], v1[4][8];
+    load(row_base + 4 * (it >> 3), k_base + 8 * (it & 7), v0);
+    if (it1 < n_items) load(row_base + 4 * (it1 >> 3), k_base + 8 * (it1 & 7), v1);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) store_split_chunk(hi, lo, 4 * (it >> 3) + j, it & 7, v0[j]);
+    if (it1 < n_items) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) store_split_chunk(hi, lo, 4 * (it1 >> 3) + j, it1 & 7, v1[j]);
+    }
+  }
+}
+
+// Weight gradient: A = d_pre^T (rows m, reduction r), B = z^T (rows n, reduction r).
+struct DwProblem {
+  static __device__ __forceinline__ void convert(const TcParams& p, uint8_t* a_hi, uint8_t* a_lo,
+                                                 uint8_t* b_hi, uint8_t* b_lo, int m0, int n0,
+                                                 int r0, int tid) {
+    convert_quads(kTcM / 4, m0, r0, tid, a_hi, a_lo,
+                  [&](int m, int rc, float (&v)[4][8]) { load_dpre_quad(p, m, rc, v); });
+    convert_quads(p.n_tile / 4, n0, r0, tid, b_hi, b_lo,
+                  [&](int n, int rc, float (&v)[4][8]) { load_z_quad(p, n, rc, v); });
+  }
+};
+
+// Input gradient: A = d_pre (rows r, reduction m: already K-major), B = W_u^T (rows k,
+// reduction m).  A items are (row, 8-entry chunk), two per thread at a time, loads first; a
+// quarter-warp covers the 8 chunks of a row.
+struct DuProblem {
+  static __device__ __forceinline__ void load_row_chunk(const TcParams& p, int r, int m,
+                                                        float (&v)[8]) {
+    const int M = 4 * p.C;
+    float4 q0 = make_float4(0.f, 0.f, 0.f, 0.f), q1 = q0;
+    if (r < p.BK && m < M) {  // M is a multiple of 4: each quad is wholly in or out
+      const float* src = p.d_pre + static_cast<size_t>(r) * M + m;
+      q0 = __ldg(reinterpret_cast<const float4*>(src));
+      if (m + 4 < M) q1 = __ldg(reinterpret_cast<const float4*>(src + 4));
+    }
+    v[0] = q0.x; v[1] = q0.y; v[2] = q0.z; v[3] = q0.w;
+    v[4] = q1.x; v[5] = q1.y; v[6] = q1.z; v[7] = q1.w;
+  }
+  static __device__ __forceinline__ void convert(const TcParams& p, uint8_t* a_hi, uint8_t* a_lo,
+                                                 uint8_t* b_hi, uint8_t* b_lo, int r0, int n0,
+                                                 int m0, int tid) {
+    for (int it = tid; it < kTcM * 8; it += 2 * kConv) {
+      const int it1 = it + kConv;  // kTcM * 8 is a multiple of 2 * kConv
+      float v0[8], v1[8];
+      load_row_chunk(p, r0 + (it >> 3), m0 + 8 * (it & 7), v0);
+      load_row_chunk(p, r0 + (it1 >> 3), m0 + 8 * (it1 & 7), v1);
+      store_split_chunk(a_hi, a_lo, it >> 3, it & 7, v0);
+      store_split_chunk(a_hi, a_lo, it1 >> 3, it1 & 7, v1);
+    }
+    convert_quads(p.n_tile / 4, n0, m0, tid, b_hi, b_lo,
+                  [&](int n, int mc, float (&v)[4][8]) { load_wu_quad(p, n, mc, v); });
+  }
+};
+
+template <class Problem>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte aligned stage buffers (128-byte swizzle atoms), then the barriers.
+  const uint32_t raw = smem_addr(smem_raw);
+  uint8_t* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const int stage_bytes = 2 * kTcM * 128 + 2 * p.n_tile * 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kStages * stage_bytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 1);
+  const uint32_t full0 = smem_addr(&bars[0]);             // full[s]  = full0 + 8 s
+  const uint32_t empty0 = smem_addr(&bars[kStages]);      // empty[s] = empty0 + 8 s
+  const uint32_t accb = smem_addr(&bars[2 * kStages]);    // accumulator ready
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int m0 = (blockIdx.x % p.m_tiles) * kTcM;
+  const int n0 = (blockIdx.x / p.m_tiles) * p.n_tile;
+  const int split = blockIdx.y;
+  const int kb0 = split * p.kb_per_split;
+  const int nk = min(p.kb_per_split, p.n_kb - kb0);
+  uint32_t ncols = 32;
+  while (ncols < static_cast<uint32_t>(p.n_tile)) ncols <<= 1;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8u * s, kConv);
+      mbar_init(empty0 + 8u * s, 1);
+    }
+    mbar_init(accb, 1);
+    fence_mbar_init_cluster();
+  }
+  if (warp == kConv / 32) {
+    tmem_alloc(smem_addr(tmem_slot), ncols);
+    tc_fence_before_sync();
+  }
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < kConv / 32) {
+    // ---- converters ----
+    bool ok = true;
+    for (int i = 0; i < nk && ok; ++i) {
+      const int s = i % kStages;
+      if (i >= kStages)
+        ok = mbar_wait_bounded_cta(empty0 + 8u * s, ((i - kStages) / kStages) & 1u, p.status);
+      if (!ok) break;
+      uint8_t* st = base + s * stage_bytes;
+      Problem::convert(p, st, st + kTcM * 128, st + 2 * kTcM * 128,
+                       st + 2 * kTcM * 128 + p.n_tile * 128, m0, n0, (kb0 + i) * kTcK, tid);
+      fence_proxy_async_smem();
+      mbar_arrive(full0 + 8u * s);
+    }
+    // ---- epilogue: TMEM row (32 * (warp % 4) + lane) -> output row; the two warpgroups take
+    // alternate 16-column chunks ----
+    if (ok) ok = mbar_wait_bounded_cta(accb, 0, p.status);
+    tc_fence_after_sync();
+    const int quarter = warp & 3;  // TMEM lanes this warp may read
+    const int m = m0 + 32 * quarter + lane;
+    float* dst = p.out + (static_cast<size_t>(split) * p.rows + m) * p.cols;
+    const bool vec_out = (p.cols % 4) == 0;
+    for (int c0 = 16 * (warp >> 2); c0 < p.n_tile; c0 += 32) {
+      float v[16];
+      tmem_ld16(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + c0, v);
+      if (!ok || m >= p.rows) continue;
+#pragma unroll
+      for (int c = 0; c < 16; c += 4) {
+        const int n = n0 + c0 + c;
+        if (vec_out && n + 3 < p.cols) {
+          *reinterpret_cast<float4*>(dst + n) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (n + e < p.cols) dst[n + e] = v[c + e];
+        }
+      }
+    }
+  } else if (lane == 0) {
+    // ---- MMA issuer ----
+    const uint32_t idesc = umma_idesc_bf16(kTcM, p.n_tile);
+    uint32_t acc = 0;
+    bool ok = true;
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % kStages;
+      ok = mbar_wait_bounded_cta(full0 + 8u * s, (i / kStages) & 1u, p.status);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const uint32_t st = smem_addr(base + s * stage_bytes);
+      const uint32_t a_hi = st, a_lo = st + kTcM * 128;
+      const uint32_t b_hi = st + 2 * kTcM * 128, b_lo = b_hi + p.n_tile * 128;
+#pragma unroll
+      for (int j = 0; j < kTcK / 16; ++j) {
+        const uint32_t koff = 32u * j;
+        umma_bf16(tmem, umma_desc_sw128(a_hi + koff), umma_desc_sw128(b_hi + koff), idesc, acc);
+        acc = 1;
+        umma_bf16(tmem, umma_desc_sw128(a_hi + koff), umma_desc_sw128(b_lo + koff), idesc, 1);
+        umma_bf16(tmem, umma_desc_sw128(a_lo + koff), umma_desc_sw128(b_hi + koff), idesc, 1);
+      }
+      umma_commit(empty0 + 8u * s);  // stage reusable once these MMAs have read it
+    }
+    umma_commit(accb);  // accumulator complete (also after an early stop)
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kConv / 32) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, ncols);
+  }
+}
+
+
+TcPlan tc_plan(int rows, int cols, int red, bool split) {
+  TcPlan pl;
+  pl.n_tiles = (cols + 255) / 256;
+  pl.n_tile = (((cols + pl.n_tiles - 1) / pl.n_tiles) + 15) & ~15;
+  pl.m_tiles = (rows + kTcM - 1) / kTcM;
+  pl.n_kb = (red + kTcK - 1) / kTcK;
+  const int tiles = pl.m_tiles * pl.n_tiles;
+  int s0 = 1;
+  if (split) {
+    s0 = (148 + tiles - 1) / tiles;  // a fixed target (not the device's SM count): the
+    if (s0 > pl.n_kb) s0 = pl.n_kb;  // split -- hence the summation order -- depends only
+  }                                  // on the sizes
+  pl.kb_per_split = (pl.n_kb + s0 - 1) / s0;
+  pl.splits = (pl.n_kb + pl.kb_per_split - 1) / pl.kb_per_split;
+  pl.smem = kStages * (2 * kTcM * 128 + 2 * pl.n_tile * 128) + 1024 + 128;
+  return pl;
+}
+
+}  // namespace
+
+TcPlan dw_tc_plan(int B, int K, int C, int n_x) { return tc_plan(4 * C, n_x + C, B * K, true); }
+TcPlan du_tc_plan(int B, int K, int C, int n_x) { return tc_plan(B * K, n_x, 4 * C, true); }
+
+cudaError_t tc_prepare(int max_smem) {
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<DwProblem>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(tc_gemm_kernel<DuProblem>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+}
+
+namespace {
+TcParams make_params(const TcPlan& pl, const float* d_pre, int B, int K, int C, int n_x,
+                     int* status) {
+  TcParams p = {};
+  p.d_pre = d_pre; p.status = status;
+  p.B = B; p.BK = B * K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
+  p.n_tile = pl.n_tile; p.m_tiles = pl.m_tiles; p.kb_per_split = pl.kb_per_split;
+  p.n_kb = pl.n_kb;
+  p.vec = (n_x % 4 == 0) && (C % 4 == 0);
+  return p;
+}
+}  // namespace
+
+cudaError_t dw_tc_launch(const TcPlan& pl, const float* d_pre, const float* u, const float* H,
+                         const float* h0, int B, int K, int C, int n_x, float* partial,
+                         int* status, cudaStream_t s) {
+  TcParams p = make_params(pl, d_pre, B, K, C, n_x, status);
+  p.u = u; p.H = H; p.h0 = h0; p.out = partial;
+  p.rows = 4 * C; p.cols = n_x + C; p.red = B * K;
+  dim3 grid(pl.m_tiles * pl.n_tiles, pl.splits, 1);
+  tc_gemm_kernel<DwProblem><<<grid, kTcThreads, pl.smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t du_tc_launch(const TcPlan& pl, const float* d_pre, const float* W, int B, int K,
+                         int C, int n_x, float* du, int* status, cudaStream_t s) {
+  TcParams p = make_params(pl, d_pre, B, K, C, n_x, status);
+  p.W = W; p.out = du;
+  p.rows = B * K; p.cols = n_x; p.red = 4 * C;
+  dim3 grid(pl.m_tiles * pl.n_tiles, pl.splits, 1);
+  tc_gemm_kernel<DuProblem><<<grid, kTcThreads, pl.smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace cfc

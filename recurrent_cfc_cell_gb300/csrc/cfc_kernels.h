@@ -60,6 +60,21 @@ int dw_simt_splits(int BK);
 cudaError_t dw_simt_launch(const float* d_pre, const float* u, const float* H, const float* h0,
                            int B, int K, int C, int n_x, int S, float* partial, cudaStream_t s);
 
+// dW and du on tcgen05 tensor cores (bf16 hi/lo split, fp32 accumulation in TMEM).
+struct TcPlan {
+  int n_tiles, n_tile, m_tiles, n_kb, kb_per_split, splits;
+  size_t smem;
+};
+TcPlan dw_tc_plan(int B, int K, int C, int n_x);  // split over the B*K rows
+TcPlan du_tc_plan(int B, int K, int C, int n_x);  // split over 4C when B*K is small
+cudaError_t tc_prepare(int max_smem);
+cudaError_t dw_tc_launch(const TcPlan& pl, const float* d_pre, const float* u, const float* H,
+                         const float* h0, int B, int K, int C, int n_x, float* partial,
+                         int* status, cudaStream_t s);
+// du, or (when pl.splits > 1) its partial blocks [splits][B*K][n_x].
+cudaError_t du_tc_launch(const TcPlan& pl, const float* d_pre, const float* W, int B, int K,
+                         int C, int n_x, float* du, int* status, cudaStream_t s);
+
 // du[r][k] = sum_m d_pre[r][m] * W[m][k] for k < n_x (SIMT fp32).
 cudaError_t du_simt_launch(const float* d_pre, const float* W, int BK, int C, int n_x,
                            float* du, cudaStream_t s);
