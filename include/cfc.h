@@ -51,6 +51,7 @@ extern "C" {
 #define CFC_ERR_DEVICE_TIMEOUT (-7)     /* a kernel abandoned a wait (see cfc_device_status) */
 #define CFC_ERR_INVALID_ARG (-8)        /* an enumerated argument is out of range            */
 #define CFC_ERR_CUDA (-9)               /* another CUDA runtime call failed                  */
+#define CFC_ERR_SCRATCH_LIMIT (-10)     /* problem needs more than the built-in scratch holds */
 
 /* Weight-gradient contraction modes for cfc_backward (argument dw_mode). */
 #define CFC_DW_ACCURATE 0  /* fp32-accurate result (relative error ~1e-6 of max|dW|)          */
@@ -142,6 +143,35 @@ int cfc_weight_grad(const float* d_pre, const float* u, const float* h0, const f
  */
 int reduce_axis0(const float* per_batch, int n_batch, int n_tail, float* out,
                  cfc_stream_t stream);
+
+/*
+ * cfc_backward_noalloc -- cfc_backward for callers that cannot allocate device memory.  (The
+ * pages have no counterpart of this entry point.)
+ *
+ * Who needs it: a plugin or callback hosted by a framework that owns the GPU's memory and gives
+ * the plugin no allocator, or a program that fixes its device memory footprint at start-up and
+ * may not grow it later.  Such callers cannot provide cfc_backward's workspace.
+ *
+ * What it does: the same computation and outputs as cfc_backward with the same arguments
+ * (minus ws / ws_bytes), using as workspace a device array built into the library.  Every GPU
+ * that loads the library holds that array, CFC_NOALLOC_SCRATCH_BYTES bytes, until the process
+ * exits.  The call allocates and frees nothing.
+ *   - Limit: problems whose cfc_workspace_bytes() exceeds CFC_NOALLOC_SCRATCH_BYTES are
+ *     rejected with CFC_ERR_SCRATCH_LIMIT before any work is enqueued.  (The 32 x 64 x 128 and
+ *     32 x 64 x 256 workloads fit; 256 x 64 x 128 does not.)
+ *   - Set-up: the first call on each device looks up the array's device address on the current
+ *     device; make that first call before any stream capture begins.
+ *   - Sharing: all calls share the one array.  Nothing in it needs to start at zero (every
+ *     entry a call reads, the same call wrote first), but calls whose work overlaps on the GPU
+ *     -- concurrent streams, or several host threads -- race on it.  Serialise them (one
+ *     stream, or events between streams).
+ * Returns the codes of cfc_backward and cfc_workspace_bytes, plus CFC_ERR_SCRATCH_LIMIT.
+ */
+#define CFC_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int cfc_backward_noalloc(const float* dH, const float* u, const float* h0, const float* W,
+                         const float* ts, const float* H, const float* cache, int B, int K, int C,
+                         int n_x, float* dW, float* db, float* du, float* dh0, int dw_mode,
+                         cfc_stream_t stream);
 
 /* cfc_error_string -- static English text for a status code (never NULL). */
 const char* cfc_error_string(int code);

@@ -20,7 +20,10 @@ CFC_DW_SIMT_FP32 = 2
 
 # Public C symbols declared in include/cfc.h (checked by the test suite).
 EXPORTED = ("cfc_workspace_bytes", "cfc_forward", "cfc_backward", "cfc_backward_recurrence",
-            "cfc_weight_grad", "reduce_axis0", "cfc_error_string", "cfc_device_status")
+            "cfc_weight_grad", "reduce_axis0", "cfc_error_string", "cfc_device_status",
+            "cfc_backward_noalloc")
+CFC_ERR_SCRATCH_LIMIT = -10
+NOALLOC_SCRATCH_BYTES = 32 << 20  # size of cfc_backward_noalloc's built-in device scratch
 
 
 class CfcError(RuntimeError):
@@ -54,6 +57,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.cfc_weight_grad.restype = i
     lib.reduce_axis0.argtypes = [vp, i, i, vp, vp]
     lib.reduce_axis0.restype = i
+    lib.cfc_backward_noalloc.argtypes = [vp] * 7 + [i] * 4 + [vp] * 4 + [i, vp]
+    lib.cfc_backward_noalloc.restype = i
     lib.cfc_error_string.argtypes = [i]
     lib.cfc_error_string.restype = ctypes.c_char_p
     lib.cfc_device_status.argtypes = [ctypes.POINTER(i)]

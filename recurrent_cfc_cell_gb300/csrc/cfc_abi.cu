@@ -184,6 +184,8 @@ const char* cfc_error_string(int code) {
     case CFC_ERR_DEVICE_TIMEOUT: return "a kernel abandoned a bounded wait";
     case CFC_ERR_INVALID_ARG: return "invalid enumerated argument";
     case CFC_ERR_CUDA: return "CUDA runtime call failed";
+    case CFC_ERR_SCRATCH_LIMIT:
+      return "problem needs more workspace than cfc_backward_noalloc's built-in scratch holds";
     default: return "unknown status code";
   }
 }
