@@ -21,6 +21,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -70,8 +71,10 @@ def work_per_unit(w):
     """FLOPs and HBM bytes per (batch row, step) of each stage (fp32 = 4 bytes)."""
     C, n_x, n_in = w.C, w.n_x, w.n_in
     return {
-        # forward: 4C pre-activations over n_in; reads u_t, ts; writes h_t and 3C cache
-        "fwd": {"flop": 8 * C * n_in, "bytes": 4 * (n_x + 1 + 4 * C)},
+        # input projection W_u u + b for all steps: reads u, writes the 4C values X in place
+        "proj": {"flop": 8 * C * n_x, "bytes": 4 * (n_x + 4 * C)},
+        # forward recurrence: W_h h_{t-1} (4C x C); reads X and ts, writes h_t and the cache
+        "fwd_rec": {"flop": 8 * C * C, "bytes": 4 * (4 * C + 1 + 4 * C)},
         # BPTT recurrence: W_h^T d_pre (4C x C); reads dH, cache, ts; writes d_pre
         "bwd_rec": {"flop": 8 * C * C, "bytes": 4 * (C + 3 * C + 1 + 4 * C)},
         # dW contraction (4C x n_in per row) + du (4C x n_x) + db; reads d_pre, u, h
@@ -98,7 +101,9 @@ def profiled_traffic(kernel: str, sources: list[str], workload: str):
         for line in fh:
             if ":" in line and line.startswith("- "):
                 k, v = line[2:].split(":", 1)
-                fields[k.strip()] = v.strip().strip("`")
+                v = v.strip()
+                m = re.match(r"`([^`]*)`", v)  # a backticked value may carry a note after it
+                fields[k.strip()] = m.group(1) if m else v.split()[0] if v else v
     if fields.get("source_sha256_16") != source_digest(sources):
         return None
     try:
@@ -282,29 +287,31 @@ def main():
         ms = float(t.item())
     units_per_step = w.units * world
     value = units_per_step / (ms * 1e-3)
-    launches_per_step = 6  # fwd, bwd recurrence, dW contraction, reduce (dW), reduce (db), du
+    launches_per_step = _lib.step_launches(w.B, w.K, w.C, w.n_x)
 
-    # ---- per-stage device times (same stream, L2 flushed before each launch)
+    # ---- per-stage device times: events between the four stage calls, L2 flushed first
     n_stage = min(args.steps, 200)
-    stage_ms = {}
-
-    def time_stage(fn):
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(n_stage)]
-        for a, b in ev:
-            flush.zero_()
-            a.record(stream)
-            fn()
-            b.record(stream)
-        torch.cuda.synchronize()
-        return sum(a.elapsed_time(b) for a, b in ev) / n_stage
-
     i = st.inputs
-    stage_ms["fwd"] = time_stage(st.forward)
-    stage_ms["bwd_rec"] = time_stage(lambda: _lib.cfc_backward_recurrence(
-        i["dH"], i["W"], i["ts"], st.cache, st.d_pre, st.dh0))
-    stage_ms["grad"] = time_stage(lambda: _lib.cfc_weight_grad(
-        st.d_pre, i["u"], i["h0"], i["W"], st.H, st.dW, st.db, st.du, st.ws))
+    stages = [
+        ("proj", lambda: _lib.cfc_input_projection(i["u"], i["W"], i["b"], st.H, st.cache)),
+        ("fwd_rec", lambda: _lib.cfc_forward_recurrence(i["h0"], i["W"], i["ts"], st.H,
+                                                       st.cache)),
+        ("bwd_rec", lambda: _lib.cfc_backward_recurrence(i["dH"], i["W"], i["ts"], st.cache,
+                                                        st.d_pre, st.dh0)),
+        ("grad", lambda: _lib.cfc_weight_grad(st.d_pre, i["u"], i["h0"], i["W"], st.H, st.dW,
+                                             st.db, st.du, st.ws)),
+    ]
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+             for _ in range(n_stage)]
+    for ev in marks:
+        flush.zero_()
+        ev[0].record(stream)
+        for j, (_, fn) in enumerate(stages):
+            fn()
+            ev[j + 1].record(stream)
+    torch.cuda.synchronize()
+    stage_ms = {name: sum(ev[j].elapsed_time(ev[j + 1]) for ev in marks) / n_stage
+                for j, (name, _) in enumerate(stages)}
 
     pk = peaks()
     props = torch.cuda.get_device_properties(dev)
@@ -316,9 +323,10 @@ def main():
         byt = wpu[name]["bytes"] * w.units
         kernels[name] = {"ms": t, "tflops": flop / (t * 1e-3) / 1e12,
                          "gbs": byt / (t * 1e-3) / 1e9}
-    dominant = max(("fwd", "bwd_rec"), key=lambda k: stage_ms[k])
-    kname = {"fwd": "cfc_fwd_kernel", "bwd_rec": "cfc_bwd_kernel"}[dominant]
-    ksrc = {"fwd": ["recurrent_cfc_cell_gb300/csrc/cfc_fwd.cu"],
+    # The dominant kernel: the larger of the two recurrences (each stage is one launch).
+    dominant = max(("fwd_rec", "bwd_rec"), key=lambda k: stage_ms[k])
+    kname = {"fwd_rec": "cfc_fwd_kernel", "bwd_rec": "cfc_bwd_kernel"}[dominant]
+    ksrc = {"fwd_rec": ["recurrent_cfc_cell_gb300/csrc/cfc_fwd.cu"],
             "bwd_rec": ["recurrent_cfc_cell_gb300/csrc/cfc_bwd.cu"]}[dominant]
     ksrc = ksrc + ["recurrent_cfc_cell_gb300/csrc/cfc_ptx.cuh",
                    "recurrent_cfc_cell_gb300/csrc/cfc_kernels.h"]

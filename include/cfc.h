@@ -79,10 +79,35 @@ int cfc_workspace_bytes(int B, int K, int C, int n_x, int dw_mode, size_t* bwd_w
  *   ts    [K][B]       time-scale per step and row (multiplies P_ta only)
  *   H     [K][B][C]    OUTPUT: h_t for every step
  *   cache [K][B][3][C] OUTPUT: ff1, ff2 and the gate s for every step (read by cfc_backward)
+ * Exactly cfc_input_projection followed by cfc_forward_recurrence (two launches).
  */
 int cfc_forward(const float* u, const float* h0, const float* W, const float* b,
                 const float* ts, int B, int K, int C, int n_x, float* H, float* cache,
                 cfc_stream_t stream);
+
+/*
+ * cfc_input_projection -- the first stage of cfc_forward alone: X = W_u u_t + b for every step
+ * at once (it does not depend on h), one parallel contraction over the B*K rows.  X is handed
+ * to the recurrence in place: gate ff1 in H[t][b][:], gates ff2 / ta / tb in cache[t][b][0..2][:]
+ * (together exactly 4C values per row).  u, W, b, H, cache as for cfc_forward.
+ */
+int cfc_input_projection(const float* u, const float* W, const float* b, int B, int K, int C,
+                         int n_x, float* H, float* cache, cfc_stream_t stream);
+
+/*
+ * cfc_forward_recurrence -- the second stage of cfc_forward alone: the K-step recurrence,
+ * adding W_h h_{t-1} to the X that cfc_input_projection left in H / cache and overwriting
+ * H / cache with the outputs.  h0, W, ts, H, cache as for cfc_forward.
+ */
+int cfc_forward_recurrence(const float* h0, const float* W, const float* ts, int B, int K,
+                           int C, int n_x, float* H, float* cache, cfc_stream_t stream);
+
+/*
+ * cfc_step_launches -- number of kernel launches one cfc_forward plus one cfc_backward enqueue
+ * for these sizes (with_du = 0 when du is NULL).  Writes *launches; returns CFC_OK or the
+ * argument error codes of cfc_workspace_bytes.
+ */
+int cfc_step_launches(int B, int K, int C, int n_x, int dw_mode, int with_du, int* launches);
 
 /*
  * cfc_backward -- reverse-time BPTT over the K steps (successor of cfc_step_backward_batched;

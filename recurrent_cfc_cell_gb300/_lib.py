@@ -21,7 +21,8 @@ CFC_DW_SIMT_FP32 = 2
 # Public C symbols declared in include/cfc.h (checked by the test suite).
 EXPORTED = ("cfc_workspace_bytes", "cfc_forward", "cfc_backward", "cfc_backward_recurrence",
             "cfc_weight_grad", "reduce_axis0", "cfc_error_string", "cfc_device_status",
-            "cfc_backward_noalloc")
+            "cfc_backward_noalloc", "cfc_input_projection", "cfc_forward_recurrence",
+            "cfc_step_launches")
 CFC_ERR_SCRATCH_LIMIT = -10
 NOALLOC_SCRATCH_BYTES = 32 << 20  # size of cfc_backward_noalloc's built-in device scratch
 
@@ -57,6 +58,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.cfc_weight_grad.restype = i
     lib.reduce_axis0.argtypes = [vp, i, i, vp, vp]
     lib.reduce_axis0.restype = i
+    lib.cfc_input_projection.argtypes = [vp] * 3 + [i] * 4 + [vp, vp, vp]
+    lib.cfc_input_projection.restype = i
+    lib.cfc_forward_recurrence.argtypes = [vp] * 3 + [i] * 4 + [vp, vp, vp]
+    lib.cfc_forward_recurrence.restype = i
+    lib.cfc_step_launches.argtypes = [i] * 6 + [ctypes.POINTER(i)]
+    lib.cfc_step_launches.restype = i
     lib.cfc_backward_noalloc.argtypes = [vp] * 7 + [i] * 4 + [vp] * 4 + [i, vp]
     lib.cfc_backward_noalloc.restype = i
     lib.cfc_error_string.argtypes = [i]
@@ -115,6 +122,37 @@ def cfc_forward(u, h0, W, b, ts, H, cache, stream=None) -> None:
         _ptr(b, "b", (4, C)), _ptr(ts, "ts", (K, B)), B, K, C, n_x,
         _ptr(H, "H", (K, B, C)), _ptr(cache, "cache", (K, B, 3, C)), _stream(stream))
     _check("cfc_forward", rc)
+
+
+def cfc_input_projection(u, W, b, H, cache, stream=None) -> None:
+    """X = W_u u + b for all steps, written in place into H (ff1) and cache (ff2, ta, tb)."""
+    K, B, n_x = u.shape
+    C = H.shape[2]
+    rc = load().cfc_input_projection(
+        _ptr(u, "u", (K, B, n_x)), _ptr(W, "W", (4, C, n_x + C)), _ptr(b, "b", (4, C)),
+        B, K, C, n_x, _ptr(H, "H", (K, B, C)), _ptr(cache, "cache", (K, B, 3, C)),
+        _stream(stream))
+    _check("cfc_input_projection", rc)
+
+
+def cfc_forward_recurrence(h0, W, ts, H, cache, stream=None) -> None:
+    """The K-step recurrence on top of the projection left in H / cache."""
+    K, B, C = H.shape
+    n_x = W.shape[2] - C
+    rc = load().cfc_forward_recurrence(
+        _ptr(h0, "h0", (B, C)), _ptr(W, "W", (4, C, n_x + C)), _ptr(ts, "ts", (K, B)),
+        B, K, C, n_x, _ptr(H, "H", (K, B, C)), _ptr(cache, "cache", (K, B, 3, C)),
+        _stream(stream))
+    _check("cfc_forward_recurrence", rc)
+
+
+def step_launches(B: int, K: int, C: int, n_x: int, dw_mode: int = CFC_DW_ACCURATE,
+                  with_du: bool = True) -> int:
+    """Kernel launches of one cfc_forward + cfc_backward for these sizes."""
+    out = ctypes.c_int(0)
+    _check("cfc_step_launches",
+           load().cfc_step_launches(B, K, C, n_x, dw_mode, int(with_du), ctypes.byref(out)))
+    return out.value
 
 
 def cfc_backward(dH, u, h0, W, ts, H, cache, dW, db, du, dh0, ws,

@@ -199,6 +199,46 @@ int cfc_workspace_bytes(int B, int K, int C, int n_x, int dw_mode, size_t* bwd_w
   return CFC_OK;
 }
 
+int cfc_input_projection(const float* u, const float* W, const float* b, int B, int K, int C,
+                         int n_x, float* H, float* cache, cfc_stream_t stream) {
+  int rc = check_dims(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (!u || !W || !b || !H || !cache) return CFC_ERR_NULL_PTR;
+  if (!aligned16(u) || !aligned16(W) || !aligned16(b) || !aligned16(H) || !aligned16(cache))
+    return CFC_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != CFC_OK) return rc;
+  return cuda_rc(cfc::inproj_launch(u, W, b, B * K, C, n_x, H, cache,
+                                    static_cast<cudaStream_t>(stream)),
+                 CFC_ERR_LAUNCH_FAILED);
+}
+
+int cfc_forward_recurrence(const float* h0, const float* W, const float* ts, int B, int K,
+                           int C, int n_x, float* H, float* cache, cfc_stream_t stream) {
+  int rc = check_dims(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (!h0 || !W || !ts || !H || !cache) return CFC_ERR_NULL_PTR;
+  if (!aligned16(h0) || !aligned16(W) || !aligned16(ts) || !aligned16(H) || !aligned16(cache))
+    return CFC_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != CFC_OK) return rc;
+  cfc::FwdParams p;
+  p.u = nullptr; p.h0 = h0; p.W = W; p.bias = nullptr; p.ts = ts; p.H = H; p.cache = cache;
+  p.status = st->status;
+  p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
+  p.CS = cluster_size_for(C);
+  size_t smem = 0;
+  int n_clusters = 0;
+  rc = plan_rows(*st, 0, 0, p.CS, B, n_x, &p.R, &smem, &n_clusters);
+  if (rc != CFC_OK) return rc;
+  return cuda_rc(cfc::fwd_launch(p, n_clusters, smem, static_cast<cudaStream_t>(stream)),
+                 CFC_ERR_LAUNCH_FAILED);
+}
+
 int cfc_forward(const float* u, const float* h0, const float* W, const float* b,
                 const float* ts, int B, int K, int C, int n_x, float* H, float* cache,
                 cfc_stream_t stream) {
@@ -208,24 +248,25 @@ int cfc_forward(const float* u, const float* h0, const float* W, const float* b,
   if (!aligned16(u) || !aligned16(h0) || !aligned16(W) || !aligned16(b) || !aligned16(ts) ||
       !aligned16(H) || !aligned16(cache))
     return CFC_ERR_MISALIGNED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  DeviceState* st = nullptr;
-  rc = device_state(&st);
+  rc = cfc_input_projection(u, W, b, B, K, C, n_x, H, cache, stream);
   if (rc != CFC_OK) return rc;
+  return cfc_forward_recurrence(h0, W, ts, B, K, C, n_x, H, cache, stream);
+}
 
-  cfc::FwdParams p;
-  p.u = u; p.h0 = h0; p.W = W; p.bias = b; p.ts = ts; p.H = H; p.cache = cache;
-  p.status = st->status;
-  p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
-  p.CS = cluster_size_for(C);
-  size_t smem = 0;
-  int n_clusters = 0;
-  rc = plan_rows(*st, 0, 0, p.CS, B, n_x, &p.R, &smem, &n_clusters);
+int cfc_step_launches(int B, int K, int C, int n_x, int dw_mode, int with_du, int* launches) {
+  const int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rc = cuda_rc(cfc::inproj_launch(u, W, b, B * K, C, n_x, H, cache, s), CFC_ERR_LAUNCH_FAILED);
-  if (rc != CFC_OK) return rc;
-  return cuda_rc(cfc::fwd_launch(p, n_clusters, smem, s), CFC_ERR_LAUNCH_FAILED);
+  if (dw_mode != CFC_DW_ACCURATE && dw_mode != CFC_DW_SIMT_FP32) return CFC_ERR_INVALID_ARG;
+  if (!launches) return CFC_ERR_NULL_PTR;
+  // forward: projection + recurrence; backward: recurrence, dW contraction + its reduction,
+  // db reduction, and du (plus its reduction when the tensor-core plan splits it).
+  int n = 2 + 1 + 2 + 1;
+  if (with_du) {
+    n += 1;
+    if (dw_mode == CFC_DW_ACCURATE && bwd_layout(B, K, C, n_x).tu.splits > 1) n += 1;
+  }
+  *launches = n;
+  return CFC_OK;
 }
 
 int cfc_backward_recurrence(const float* dH, const float* W, const float* ts,
