@@ -102,7 +102,7 @@ int max_clusters(DeviceState& st, int kind, int variant, int CS, size_t smem, in
   }
   int n = 0;
   const cudaError_t e = (kind == 0) ? cfc::fwd_prepare(CS, variant, smem, &n)
-                                    : cfc::bwd_prepare(CS, smem, &n);
+                                    : cfc::bwd_prepare(CS, variant, smem, &n);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return CFC_ERR_CUDA;
@@ -123,7 +123,10 @@ int plan_rows(DeviceState& st, int kind, int variant, int CS, int B, int n_x, in
   for (int R = 1; R <= r_max; R *= 2) {
     const size_t smem = (kind == 0) ? cfc::fwd_smem_bytes(R, CS) : cfc::bwd_smem_bytes(R, CS);
     int n = 0;
-    const int rc = max_clusters(st, kind, (kind == 0) ? R : variant, CS, smem, &n);
+    // Each row count has its own kernel (and occupancy) up to four rows; the backward ring
+    // kernel serves every larger count.
+    const int kvar = (kind == 0 || R <= 4) ? R : 0;
+    const int rc = max_clusters(st, kind, kvar, CS, smem, &n);
     if (rc != CFC_OK) return rc;
     if (n <= 0) break;
     best_R = R;

@@ -27,9 +27,13 @@
 //     four d_pre values of each channel and the pushes.  The gathered vector is stored in
 //     thirty-two slices padded to an odd number of 16-byte chunks, so the vector loads of a
 //     quarter-warp hit distinct banks.  The summation order is fixed: bitwise reproducible;
-//   * dH, ff1, ff2, gate and ts for a step arrive two steps ahead through a cp.async ring
-//     (10 lanes of each warp copy, the warp reads after __syncwarp), so no global-memory
-//     latency sits on the serial chain.
+//   * dH, ff1, ff2, gate and ts of step t-1 are loaded into registers during step t when the
+//     cluster serves at most four rows (the row count is then a compile-time parameter); for
+//     larger row groups they arrive two steps ahead through a cp.async ring (10 lanes of each
+//     warp copy, the warp reads after __syncwarp).  Either way no global-memory latency sits
+//     on the serial chain;
+//   * the W_h^T columns are read once, coalesced, into shared memory and from there into
+//     registers (a direct load would fetch one 32-byte sector per 4-byte value).
 #include "cfc_kernels.h"
 #include "cfc_ptx.cuh"
 
@@ -114,14 +118,34 @@ __device__ __forceinline__ float gathered_delta(const float (&wt)[2][RS], const 
   return d;
 }
 
-template <int CS>
-__global__ void __launch_bounds__(kRecThreads, 2) cfc_bwd_kernel(const BwdParams p) {
+// Prefetched inputs of one step for RT rows (register path): dH, ff1, ff2, gate, ts.
+template <int RT>
+__device__ __forceinline__ void load_step_regs(const BwdParams& p, int t, int row0, int ch,
+                                               float (&v)[RT][kPreComp]) {
+  const int chc = ch < p.C ? ch : p.C - 1;  // clamped: padded lanes load a valid location
+#pragma unroll
+  for (int r = 0; r < RT; ++r) {
+    const int b = row0 + r < p.B ? row0 + r : p.B - 1;
+    const size_t tb = static_cast<size_t>(t) * p.B + b;
+    v[r][0] = __ldcg(p.dH + tb * p.C + chc);
+    v[r][1] = __ldcg(p.cache + (tb * 3 + 0) * p.C + chc);
+    v[r][2] = __ldcg(p.cache + (tb * 3 + 1) * p.C + chc);
+    v[r][3] = __ldcg(p.cache + (tb * 3 + 2) * p.C + chc);
+    v[r][4] = __ldg(p.ts + tb);
+  }
+}
+
+// RT = 1, 2, 4: rows per cluster fixed at compile time, inputs prefetched into registers.
+// RT = 0: p.R rows (any count), inputs through the cp.async ring.
+template <int CS, int RT>
+__global__ void __launch_bounds__(kRecThreads, CS >= 16 ? 1 : 2) cfc_bwd_kernel(const BwdParams p) {
   using S = BwdShape<CS>;
   extern __shared__ __align__(16) float smem[];
-  const int R = p.R;
+  const int R = RT > 0 ? RT : p.R;
   float* dg = smem;                      // [2][R][GROW]  d_pre[t+1] for step t in dg[t & 1]
-  float* pre = dg + 2 * R * S::GROW;     // [kPre][R][8 warps][2][5]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(pre + kPre * R * kWarps * 2 * kPreComp);
+  float* pre = dg + 2 * R * S::GROW;     // ring path: [kPre][R][8 warps][2][5]
+  const int pre_floats = RT > 0 ? 0 : kPre * R * kWarps * 2 * kPreComp;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pre + pre_floats);
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -132,17 +156,26 @@ __global__ void __launch_bounds__(kRecThreads, 2) cfc_bwd_kernel(const BwdParams
 
   // W_h^T columns of this warp's two channels over gathered rows [lane*RS, lane*RS + RS).
   // Gathered row q*64 + 4i + g is W row g*C + 16q + i.
+  // Staged through shared memory as [NG][17] (the whole smem area is free before the loop):
+  // consecutive threads read consecutive channels of one W row.
   float wt[2][S::RS];
-#pragma unroll
-  for (int cc = 0; cc < 2; ++cc) {
-    const int j = kChanPerCta * rank + 2 * warp + cc;
-#pragma unroll
-    for (int k = 0; k < S::RS; ++k) {
-      const int gidx = lane * S::RS + k;
+  {
+    float* wtmp = smem;
+    for (int e = tid; e < S::NG * kChanPerCta; e += kRecThreads) {
+      const int gidx = e >> 4, jl = e & 15;
       const int chr = kChanPerCta * (gidx >> 6) + ((gidx & 63) >> 2);
-      wt[cc][k] = (chr < C && j < C)
-                      ? p.W[(static_cast<size_t>(gidx & 3) * C + chr) * n_in + n_x + j] : 0.f;
+      const int j = kChanPerCta * rank + jl;
+      wtmp[gidx * (kChanPerCta + 1) + jl] =
+          (chr < C && j < C) ? p.W[(static_cast<size_t>(gidx & 3) * C + chr) * n_in + n_x + j]
+                             : 0.f;
     }
+    __syncthreads();
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+      for (int k = 0; k < S::RS; ++k)
+        wt[cc][k] = wtmp[(lane * S::RS + k) * (kChanPerCta + 1) + 2 * warp + cc];
+    __syncthreads();
   }
   const int ci = lane >> 4;        // channel of this half-warp
   const int gq = (lane >> 2) & 3;  // gate this lane's d_pre belongs to
@@ -164,20 +197,31 @@ __global__ void __launch_bounds__(kRecThreads, 2) cfc_bwd_kernel(const BwdParams
     mbar_arrive_expect_tx(bar0 + 8u * ((K - 2) & 1), tx_bytes);
     if (K >= 2) mbar_arrive_expect_tx(bar0 + 8u * ((K - 3) & 1), tx_bytes);
   }
-  issue_pre(p, pre, K - 1, row0, rank, warp, lane);
-  cp_async_commit();
-  issue_pre(p, pre, K - 2, row0, rank, warp, lane);
-  cp_async_commit();
+  constexpr int RR = RT > 0 ? RT : 1;
+  float cur[RR][kPreComp];  // register path: inputs of the current step
+  if constexpr (RT > 0) {
+    load_step_regs<RR>(p, K - 1, row0, ch, cur);
+  } else {
+    issue_pre(p, pre, K - 1, row0, rank, warp, lane);
+    cp_async_commit();
+    issue_pre(p, pre, K - 2, row0, rank, warp, lane);
+    cp_async_commit();
+  }
   cluster_sync_all();
 
   uint32_t phase = 0;
   bool ok = true;
   for (int t = K - 1; t >= 0; --t) {
     const int s = t & 1;
-    // Ring: step t-2 goes into the slot step t+1 used; every lane of the warp has read it.
-    __syncwarp();
-    issue_pre(p, pre, t - 2, row0, rank, warp, lane);
-    cp_async_commit();
+    float nxt[RR][kPreComp];
+    if constexpr (RT > 0) {
+      if (t >= 1) load_step_regs<RR>(p, t - 1, row0, ch, nxt);  // used one step later
+    } else {
+      // Ring: step t-2 goes into the slot step t+1 used; every lane of the warp has read it.
+      __syncwarp();
+      issue_pre(p, pre, t - 2, row0, rank, warp, lane);
+      cp_async_commit();
+    }
 
     if (t < K - 1) {
       ok = __all_sync(0xffffffffu,
@@ -186,11 +230,14 @@ __global__ void __launch_bounds__(kRecThreads, 2) cfc_bwd_kernel(const BwdParams
       if (!ok) break;
       if (tid == 0 && t - 2 >= -1) mbar_arrive_expect_tx(bar0 + 8u * s, tx_bytes);
     }
-    cp_async_wait<2>();  // the warp's copies for step t (groups t-1, t-2 may be pending)
-    __syncwarp();
+    if constexpr (RT == 0) {
+      cp_async_wait<2>();  // the warp's copies for step t (groups t-1, t-2 may be pending)
+      __syncwarp();
+    }
 
     const float* pre_t = pre + ((t % kPre) * R * kWarps + warp) * 2 * kPreComp + ci * kPreComp;
     float* dn = dg + (s ^ 1) * R * S::GROW;
+#pragma unroll(RT > 0 ? RT : 1)
     for (int r = 0; r < R; ++r) {
       const float delta =
           (t < K - 1) ? gathered_delta<S::RS>(wt, dg + (s * R + r) * S::GROW + lane * S::RSP, lane)
@@ -198,13 +245,16 @@ __global__ void __launch_bounds__(kRecThreads, 2) cfc_bwd_kernel(const BwdParams
       const int b = row0 + r;
       float dpv = 0.f;
       if (b < B && ch < C) {
-        const float* pv = pre_t + r * kWarps * 2 * kPreComp;
-        const float dh = pv[0] + delta;
-        const float f1 = pv[1], f2 = pv[2], g = pv[3];
+        float v[kPreComp];  // dH, ff1, ff2, gate, ts of (t, b, ch)
+#pragma unroll
+        for (int c = 0; c < kPreComp; ++c)
+          v[c] = RT > 0 ? cur[RT > 0 ? r : 0][c] : pre_t[r * kWarps * 2 * kPreComp + c];
+        const float dh = v[0] + delta;
+        const float f1 = v[1], f2 = v[2], g = v[3];
         const float ds = dh * (f2 - f1) * g * (1.f - g);
         if (gq == 0) dpv = dh * (1.f - g) * (1.f - f1 * f1);
         else if (gq == 1) dpv = dh * g * (1.f - f2 * f2);
-        else if (gq == 2) dpv = ds * pv[4];
+        else if (gq == 2) dpv = ds * v[4];
         else dpv = ds;
         if ((lane & 3) == 0)
           p.d_pre[((static_cast<size_t>(t) * B + b) * 4 + gq) * C + ch] = dpv;
@@ -218,6 +268,14 @@ __global__ void __launch_bounds__(kRecThreads, 2) cfc_bwd_kernel(const BwdParams
         const uint32_t dst =
             smem_addr(dn + r * S::GROW + gpos<CS>(rank * kRowsPerCta + 4 * (2 * warp + ci)));
         st_async_v4(map_to_rank(dst, q), d0, d1, d2, d3, map_to_rank(bar0 + 8u * (s ^ 1), q));
+      }
+    }
+    if constexpr (RT > 0) {
+      if (t >= 1) {
+#pragma unroll
+        for (int r = 0; r < RR; ++r)
+#pragma unroll
+          for (int c = 0; c < kPreComp; ++c) cur[r][c] = nxt[r][c];
       }
     }
   }
@@ -234,12 +292,12 @@ __global__ void __launch_bounds__(kRecThreads, 2) cfc_bwd_kernel(const BwdParams
       }
     }
   }
-  cp_async_wait<0>();
+  if constexpr (RT == 0) cp_async_wait<0>();
   cluster_sync_all();
 }
 
-template <int CS>
-cudaError_t prepare_cs(size_t smem, int* max_active) {
+template <int CS, int RT>
+cudaError_t prepare_k(size_t smem, int* max_active) {
   // The attribute is a per-function maximum: set it to the device's opt-in limit once, so any
   // row grouping chosen later (from cached occupancy results) can launch.
   int dev = 0, optin = 0;
@@ -251,9 +309,10 @@ cudaError_t prepare_cs(size_t smem, int* max_active) {
     *max_active = 0;
     return cudaSuccess;
   }
-  e = cudaFuncSetAttribute(cfc_bwd_kernel<CS>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  auto* kern = cfc_bwd_kernel<CS, RT>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(cfc_bwd_kernel<CS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CS, 1, 1);
@@ -266,11 +325,11 @@ cudaError_t prepare_cs(size_t smem, int* max_active) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(max_active, cfc_bwd_kernel<CS>, &cfg);
+  return cudaOccupancyMaxActiveClusters(max_active, kern, &cfg);
 }
 
-template <int CS>
-cudaError_t launch_cs(const BwdParams& p, int n_clusters, size_t smem, cudaStream_t s) {
+template <int CS, int RT>
+cudaError_t launch_k(const BwdParams& p, int n_clusters, size_t smem, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_clusters * CS, 1, 1);
   cfg.blockDim = dim3(kRecThreads, 1, 1);
@@ -283,7 +342,30 @@ cudaError_t launch_cs(const BwdParams& p, int n_clusters, size_t smem, cudaStrea
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, cfc_bwd_kernel<CS>, p);
+  return cudaLaunchKernelEx(&cfg, cfc_bwd_kernel<CS, RT>, p);
+}
+
+// Row groups of 1, 2 or 4 use the register-prefetch kernels, larger ones the ring kernel.
+int bwd_variant(int R) { return (R == 1 || R == 2 || R == 4) ? R : 0; }
+
+template <int CS>
+cudaError_t prepare_cs(int R, size_t smem, int* max_active) {
+  switch (bwd_variant(R)) {
+    case 1: return prepare_k<CS, 1>(smem, max_active);
+    case 2: return prepare_k<CS, 2>(smem, max_active);
+    case 4: return prepare_k<CS, 4>(smem, max_active);
+    default: return prepare_k<CS, 0>(smem, max_active);
+  }
+}
+
+template <int CS>
+cudaError_t launch_cs(const BwdParams& p, int n_clusters, size_t smem, cudaStream_t s) {
+  switch (bwd_variant(p.R)) {
+    case 1: return launch_k<CS, 1>(p, n_clusters, smem, s);
+    case 2: return launch_k<CS, 2>(p, n_clusters, smem, s);
+    case 4: return launch_k<CS, 4>(p, n_clusters, smem, s);
+    default: return launch_k<CS, 0>(p, n_clusters, smem, s);
+  }
 }
 
 }  // namespace
@@ -291,17 +373,20 @@ cudaError_t launch_cs(const BwdParams& p, int n_clusters, size_t smem, cudaStrea
 size_t bwd_smem_bytes(int R, int CS) {
   const size_t RS = 2ull * CS;
   const size_t GROW = 32 * ((RS >= 4 && (RS / 4) % 2 == 0) ? RS + 4 : RS);
-  return sizeof(float) * (2ull * R * GROW + 1ull * kPre * R * kWarps * 2 * kPreComp) +
-         2 * sizeof(uint64_t) + 16;
+  const size_t ring = bwd_variant(R) > 0 ? 0 : 1ull * kPre * R * kWarps * 2 * kPreComp;
+  const size_t loop = sizeof(float) * (2ull * R * GROW + ring) + 2 * sizeof(uint64_t) + 16;
+  // The prologue stages the CTA's W_h^T block ([4 * 16 CS][17] floats) in the same area.
+  const size_t stage = sizeof(float) * 4ull * kChanPerCta * CS * (kChanPerCta + 1);
+  return loop > stage ? loop : stage;
 }
 
-cudaError_t bwd_prepare(int CS, size_t smem, int* max_active) {
+cudaError_t bwd_prepare(int CS, int R, size_t smem, int* max_active) {
   switch (CS) {
-    case 1: return prepare_cs<1>(smem, max_active);
-    case 2: return prepare_cs<2>(smem, max_active);
-    case 4: return prepare_cs<4>(smem, max_active);
-    case 8: return prepare_cs<8>(smem, max_active);
-    case 16: return prepare_cs<16>(smem, max_active);
+    case 1: return prepare_cs<1>(R, smem, max_active);
+    case 2: return prepare_cs<2>(R, smem, max_active);
+    case 4: return prepare_cs<4>(R, smem, max_active);
+    case 8: return prepare_cs<8>(R, smem, max_active);
+    case 16: return prepare_cs<16>(R, smem, max_active);
     default: return cudaErrorInvalidValue;
   }
 }

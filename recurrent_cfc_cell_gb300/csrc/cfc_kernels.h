@@ -48,7 +48,7 @@ cudaError_t fwd_prepare(int CS, int R, size_t smem, int* max_active_clusters);
 cudaError_t fwd_launch(const FwdParams& p, int n_clusters, size_t smem, cudaStream_t s);
 
 size_t bwd_smem_bytes(int R, int CS);
-cudaError_t bwd_prepare(int CS, size_t smem, int* max_active_clusters);
+cudaError_t bwd_prepare(int CS, int R, size_t smem, int* max_active_clusters);
 cudaError_t bwd_launch(const BwdParams& p, int n_clusters, size_t smem, cudaStream_t s);
 
 // X = W_u u + b for all steps, written in place into H (gate ff1) and cache (ff2, ta, tb).
