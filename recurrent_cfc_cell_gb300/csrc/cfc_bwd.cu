@@ -118,20 +118,20 @@ __device__ __forceinline__ float gathered_delta(const float (&wt)[2][RS], const 
   return d;
 }
 
-// Prefetched inputs of one step for RT rows (register path): dH, ff1, ff2, gate, ts.
+// Prefetched inputs of one step for RT rows (register path): dH, ff1, ff2, gate, ts.  dHp,
+// cp and tsp address row row0 of the step; row r is C, 3C and 1 floats further on.
 template <int RT>
-__device__ __forceinline__ void load_step_regs(const BwdParams& p, int t, int row0, int ch,
+__device__ __forceinline__ void load_step_regs(const float* dHp, const float* cp,
+                                               const float* tsp, int C, const bool (&rok)[RT],
                                                float (&v)[RT][kPreComp]) {
-  const int chc = ch < p.C ? ch : p.C - 1;  // clamped: padded lanes load a valid location
 #pragma unroll
   for (int r = 0; r < RT; ++r) {
-    const int b = row0 + r < p.B ? row0 + r : p.B - 1;
-    const size_t tb = static_cast<size_t>(t) * p.B + b;
-    v[r][0] = __ldcg(p.dH + tb * p.C + chc);
-    v[r][1] = __ldcg(p.cache + (tb * 3 + 0) * p.C + chc);
-    v[r][2] = __ldcg(p.cache + (tb * 3 + 1) * p.C + chc);
-    v[r][3] = __ldcg(p.cache + (tb * 3 + 2) * p.C + chc);
-    v[r][4] = __ldg(p.ts + tb);
+    const size_t o = static_cast<size_t>(r) * C;
+    v[r][0] = rok[r] ? __ldcg(dHp + o) : 0.f;
+    v[r][1] = rok[r] ? __ldcg(cp + 3 * o) : 0.f;
+    v[r][2] = rok[r] ? __ldcg(cp + 3 * o + C) : 0.f;
+    v[r][3] = rok[r] ? __ldcg(cp + 3 * o + 2 * C) : 0.f;
+    v[r][4] = rok[r] ? __ldg(tsp + r) : 0.f;
   }
 }
 
@@ -197,10 +197,35 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 16 ? 1 : 2) cfc_bwd_kernel(
     mbar_arrive_expect_tx(bar0 + 8u * ((K - 2) & 1), tx_bytes);
     if (K >= 2) mbar_arrive_expect_tx(bar0 + 8u * ((K - 3) & 1), tx_bytes);
   }
+  // Per-lane addresses, computed once: the K-loop only moves pointers by a fixed stride per
+  // step and issues predicated loads and stores (no index arithmetic or divergent branches on
+  // the serial chain).  Pointers address row row0 of step t.
   constexpr int RR = RT > 0 ? RT : 1;
+  const int chc = ch < C ? ch : 0;  // padded channels address a valid location
+  const size_t t_last = static_cast<size_t>(K - 1) * B + row0;
+  const float* dHp = p.dH + t_last * C + chc;
+  const float* cp = p.cache + t_last * 3 * C + chc;
+  const float* tsp = p.ts + t_last;
+  float* dpp = p.d_pre + (t_last * 4 + gq) * C + chc;  // d_pre of this lane's gate
+  const size_t bc = static_cast<size_t>(B) * C;
+  bool rok[RR];
+#pragma unroll
+  for (int r = 0; r < RR; ++r) rok[r] = row0 + r < B;
+  const bool stores = (lane & 3) == 0 && ch < C;  // one lane per (channel, gate) stores d_pre
+  // The four d_pre of channel ci go to slot rank*64 + 4*(2w + ci) of every CTA's gathered
+  // vector; remote addresses of buffer 0 / row 0 (buffer d, row r: (d R + r) GROW floats on).
+  const bool pushes = q < CS;
+  const uint32_t push0 =
+      pushes ? map_to_rank(smem_addr(dg + gpos<CS>(rank * kRowsPerCta + 4 * (2 * warp + ci))), q)
+             : 0u;
+  const uint32_t rbar0 = pushes ? map_to_rank(bar0, q) : 0u;
+
   float cur[RR][kPreComp];  // register path: inputs of the current step
   if constexpr (RT > 0) {
-    load_step_regs<RR>(p, K - 1, row0, ch, cur);
+    load_step_regs<RR>(dHp, cp, tsp, C, rok, cur);
+    dHp -= bc;
+    cp -= 3 * bc;
+    tsp -= B;
   } else {
     issue_pre(p, pre, K - 1, row0, rank, warp, lane);
     cp_async_commit();
@@ -215,7 +240,12 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 16 ? 1 : 2) cfc_bwd_kernel(
     const int s = t & 1;
     float nxt[RR][kPreComp];
     if constexpr (RT > 0) {
-      if (t >= 1) load_step_regs<RR>(p, t - 1, row0, ch, nxt);  // used one step later
+      if (t >= 1) {  // step t - 1, used one step later
+        load_step_regs<RR>(dHp, cp, tsp, C, rok, nxt);
+        dHp -= bc;
+        cp -= 3 * bc;
+        tsp -= B;
+      }
     } else {
       // Ring: step t-2 goes into the slot step t+1 used; every lane of the warp has read it.
       __syncwarp();
@@ -236,40 +266,37 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 16 ? 1 : 2) cfc_bwd_kernel(
     }
 
     const float* pre_t = pre + ((t % kPre) * R * kWarps + warp) * 2 * kPreComp + ci * kPreComp;
-    float* dn = dg + (s ^ 1) * R * S::GROW;
+    const uint32_t pdst = push0 + static_cast<uint32_t>((s ^ 1) * R * S::GROW * 4);
+    const uint32_t pbar = rbar0 + 8u * (s ^ 1);
 #pragma unroll(RT > 0 ? RT : 1)
     for (int r = 0; r < R; ++r) {
       const float delta =
           (t < K - 1) ? gathered_delta<S::RS>(wt, dg + (s * R + r) * S::GROW + lane * S::RSP, lane)
                       : 0.f;
-      const int b = row0 + r;
-      float dpv = 0.f;
-      if (b < B && ch < C) {
-        float v[kPreComp];  // dH, ff1, ff2, gate, ts of (t, b, ch)
+      const bool valid = row0 + r < B && ch < C;
+      float v[kPreComp];  // dH, ff1, ff2, gate, ts of (t, b, ch)
 #pragma unroll
-        for (int c = 0; c < kPreComp; ++c)
-          v[c] = RT > 0 ? cur[RT > 0 ? r : 0][c] : pre_t[r * kWarps * 2 * kPreComp + c];
-        const float dh = v[0] + delta;
-        const float f1 = v[1], f2 = v[2], g = v[3];
-        const float ds = dh * (f2 - f1) * g * (1.f - g);
-        if (gq == 0) dpv = dh * (1.f - g) * (1.f - f1 * f1);
-        else if (gq == 1) dpv = dh * g * (1.f - f2 * f2);
-        else if (gq == 2) dpv = ds * v[4];
-        else dpv = ds;
-        if ((lane & 3) == 0)
-          p.d_pre[((static_cast<size_t>(t) * B + b) * 4 + gq) * C + ch] = dpv;
-      }
+      for (int c = 0; c < kPreComp; ++c)
+        v[c] = RT > 0 ? cur[RT > 0 ? r : 0][c] : pre_t[r * kWarps * 2 * kPreComp + c];
+      const float dh = v[0] + delta;
+      const float f1 = v[1], f2 = v[2], g = v[3];
+      const float ds = dh * (f2 - f1) * g * (1.f - g);
+      // This lane's gate, by selects (the four lanes of a gate group differ from their
+      // neighbours, so a branch here would split the warp four ways).
+      const float p0 = dh * (1.f - g) * (1.f - f1 * f1);
+      const float p1 = dh * g * (1.f - f2 * f2);
+      const float p2 = ds * v[4];
+      const float sel = (gq == 0) ? p0 : (gq == 1) ? p1 : (gq == 2) ? p2 : ds;
+      const float dpv = valid ? sel : 0.f;
+      if (stores && valid) dpp[static_cast<size_t>(r) * 4 * C] = dpv;
       // The four gates of channel ci -> one 16-byte push to every CTA of the cluster.
       const float d0 = __shfl_sync(0xffffffffu, dpv, half + 0);
       const float d1 = __shfl_sync(0xffffffffu, dpv, half + 4);
       const float d2 = __shfl_sync(0xffffffffu, dpv, half + 8);
       const float d3 = __shfl_sync(0xffffffffu, dpv, half + 12);
-      if (q < CS) {
-        const uint32_t dst =
-            smem_addr(dn + r * S::GROW + gpos<CS>(rank * kRowsPerCta + 4 * (2 * warp + ci)));
-        st_async_v4(map_to_rank(dst, q), d0, d1, d2, d3, map_to_rank(bar0 + 8u * (s ^ 1), q));
-      }
+      st_async_v4_if(pushes, pdst + static_cast<uint32_t>(r * S::GROW * 4), d0, d1, d2, d3, pbar);
     }
+    dpp -= 4 * bc;
     if constexpr (RT > 0) {
       if (t >= 1) {
 #pragma unroll

@@ -94,20 +94,36 @@ __global__ void __launch_bounds__(kRecThreads, 2) cfc_fwd_kernel(const FwdParams
       wh[gg][c] = (ch < C && j < C)
                       ? p.W[(static_cast<size_t>(gg) * C + ch) * n_in + n_x + j] : 0.f;
     }
-  // Source of this lane's X value (written in place into H / cache by the projection).
-  const bool xvalid = ch < C;
-  const float* xsrc = (g == 0) ? p.H + ch : p.cache + static_cast<size_t>(g - 1) * C + ch;
-  const size_t xrow = (g == 0) ? static_cast<size_t>(C) : 3ull * C;  // per batch row
+  // Per-lane addresses, computed once: the K-loop only advances pointers by a fixed stride
+  // per step and issues predicated loads and stores (no index arithmetic or divergent
+  // branches on the serial chain).
+  //   X of this lane's (channel, gate g) -- written in place into H / cache by the
+  //   projection -- for row row0 + r of step t: xp + t * xstep + r * xrow;
+  //   the value this lane stores (lane q < 4: H, ff1, ff2, gate) likewise with q for g.
   const int q = lane & 15;
+  const int chc = ch < C ? ch : 0;  // padded channels read a valid location
+  const size_t xrow = (g == 0) ? static_cast<size_t>(C) : 3ull * C;
+  const size_t srow = (q == 0) ? static_cast<size_t>(C) : 3ull * C;
+  const float* xp = ((g == 0) ? p.H : p.cache + static_cast<size_t>(g - 1) * C) + chc +
+                    static_cast<size_t>(row0 < B ? row0 : 0) * xrow;
+  float* sp = ((q == 0) ? p.H : p.cache + static_cast<size_t>(q > 0 && q < 4 ? q - 1 : 0) * C) +
+              chc + static_cast<size_t>(row0 < B ? row0 : 0) * srow;
+  const float* tsp = p.ts + (row0 < B ? row0 : 0);
+  const size_t xstep = static_cast<size_t>(B) * xrow, sstep = static_cast<size_t>(B) * srow;
+  bool xok[R], sok[R], rok[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    rok[r] = row0 + r < B;
+    xok[r] = rok[r] && ch < C;
+    sok[r] = xok[r] && q < 4;
+  }
 
-  // X and ts of step t for every row of the group, into registers.
-  auto load_step = [&](int t, float (&xv)[R], float (&tv)[R]) {
+  // X and ts of the step whose X row starts at xs (ts at tss), for every row of the group.
+  auto load_step = [&](const float* xs, const float* tss, float (&xv)[R], float (&tv)[R]) {
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const int b = row0 + r;
-      const size_t tb = static_cast<size_t>(t) * B + b;
-      xv[r] = (b < B && xvalid) ? __ldcg(xsrc + tb * xrow) : 0.f;
-      tv[r] = (b < B) ? __ldg(p.ts + tb) : 0.f;
+      xv[r] = xok[r] ? __ldcg(xs + r * xrow) : 0.f;
+      tv[r] = rok[r] ? __ldg(tss + r) : 0.f;
     }
   };
 
@@ -127,7 +143,7 @@ __global__ void __launch_bounds__(kRecThreads, 2) cfc_fwd_kernel(const FwdParams
       hbuf[r * S::HROW + hpos<CS>(j)] = p.h0[static_cast<size_t>(row0 + r) * C + j];
   }
   float xc[R], tc[R];  // X and ts of the current step
-  load_step(0, xc, tc);
+  load_step(xp, tsp, xc, tc);
   // Step t consumes h_{t-1} through bars[t & 1]; arm the first two consumers (t = 1, 2).
   if (tid == 0) {
     if (K >= 2) mbar_arrive_expect_tx(bar0 + 8u, tx_bytes);
@@ -136,12 +152,25 @@ __global__ void __launch_bounds__(kRecThreads, 2) cfc_fwd_kernel(const FwdParams
   __syncthreads();     // h0 visible to every warp
   cluster_sync_all();  // barrier inits and buffers ready cluster-wide
 
+  // Pushes of the new h: lane q < CS writes this lane's channel into CTA q's buffer.  Remote
+  // addresses of buffer 0 / row 0; buffer d, row r is (d * R + r) * HROW floats further on.
+  const bool pushes = q < CS;
+  // (ch, not the clamped chc: a padded channel has its own slot in the padded h row.)
+  const uint32_t push0 = pushes ? map_to_rank(smem_addr(hbuf + hpos<CS>(ch)), q) : 0u;
+  const uint32_t rbar0 = pushes ? map_to_rank(bar0, q) : 0u;
+
+  const float* xnext = xp + xstep;  // X and ts of step t + 1
+  const float* tsnext = tsp + B;
   uint32_t phase = 0;  // bit s: parity of the next phase of bars[s] to wait for
   for (int t = 0; t < K; ++t) {
     const int s = t & 1;
     // X and ts of the next step; consumed one step later, so their latency is hidden.
     float xn[R], tn[R];
-    if (t + 1 < K) load_step(t + 1, xn, tn);
+    if (t + 1 < K) {
+      load_step(xnext, tsnext, xn, tn);
+      xnext += xstep;
+      tsnext += B;
+    }
 
     // h_{t-1} from every CTA of the cluster.
     if (t > 0) {
@@ -153,7 +182,8 @@ __global__ void __launch_bounds__(kRecThreads, 2) cfc_fwd_kernel(const FwdParams
     }
 
     const float* hb = hbuf + s * R * S::HROW + sl * S::HSP;
-    float* hn = hbuf + (s ^ 1) * R * S::HROW;
+    const uint32_t pdst = push0 + static_cast<uint32_t>((s ^ 1) * R * S::HROW * 4);
+    const uint32_t pbar = rbar0 + 8u * (s ^ 1);
     const bool b3 = lane & 8, b2 = lane & 4;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -185,16 +215,12 @@ __global__ void __launch_bounds__(kRecThreads, 2) cfc_fwd_kernel(const FwdParams
       const float f2 = __shfl_sync(0xffffffffu, y, half + 4);
       const float gt = __shfl_sync(0xffffffffu, y, half + 8);
       const float h = f1 * (1.f - gt) + gt * f2;
-      const int b = row0 + r;
-      if (b < B && ch < C && q < 4) {
-        const size_t tb = static_cast<size_t>(t) * B + b;
-        if (q == 0) p.H[tb * C + ch] = h;
-        else p.cache[(tb * 3 + (q - 1)) * C + ch] = (q == 1) ? f1 : (q == 2 ? f2 : gt);
-      }
-      if (t + 1 < K && q < CS)
-        st_async_b32(map_to_rank(smem_addr(hn + r * S::HROW + hpos<CS>(ch)), q), h,
-                     map_to_rank(bar0 + 8u * (s ^ 1), q));
+      st_async_b32_if(pushes && t + 1 < K, pdst + static_cast<uint32_t>(r * S::HROW * 4), h,
+                      pbar);
+      const float sv = (q == 0) ? h : (q == 1) ? f1 : (q == 2 ? f2 : gt);
+      if (sok[r]) sp[r * srow] = sv;
     }
+    sp += sstep;
     if (t + 1 < K) {
 #pragma unroll
       for (int r = 0; r < R; ++r) {

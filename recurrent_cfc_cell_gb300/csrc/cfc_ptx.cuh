@@ -132,6 +132,28 @@ __device__ __forceinline__ void st_async_b32(uint32_t raddr, float v, uint32_t r
       : "memory");
 }
 
+// Predicated form: lanes with pred == false issue nothing (no divergent branch around it).
+__device__ __forceinline__ void st_async_b32_if(bool pred, uint32_t raddr, float v,
+                                                uint32_t rbar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %3, 0;\n\t"
+      "@p st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];\n\t}" ::"r"(
+          raddr),
+      "r"(__float_as_uint(v)), "r"(rbar), "r"(static_cast<uint32_t>(pred))
+      : "memory");
+}
+
+__device__ __forceinline__ void st_async_v4_if(bool pred, uint32_t raddr, float a, float b,
+                                               float c, float d, uint32_t rbar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "@p st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
+      "[%5];\n\t}" ::"r"(raddr),
+      "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)),
+      "r"(__float_as_uint(d)), "r"(rbar), "r"(static_cast<uint32_t>(pred))
+      : "memory");
+}
+
 __device__ __forceinline__ void st_async_v4(uint32_t raddr, float a, float b, float c, float d,
                                             uint32_t rbar) {
   asm volatile(
