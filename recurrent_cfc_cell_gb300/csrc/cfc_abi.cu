@@ -75,9 +75,9 @@ int device_state(DeviceState** out) {
   return CFC_OK;
 }
 
-// Smallest power of two >= ceil(C / 16): CTAs per cluster of the recurrence kernels.
-int cluster_size_for(int C) {
-  const int need = (C + cfc::kChanPerCta - 1) / cfc::kChanPerCta;
+// Smallest power of two >= ceil(C / channels per CTA): CTAs per cluster of a recurrence.
+int cluster_size_for(int C, int chan_per_cta) {
+  const int need = (C + chan_per_cta - 1) / chan_per_cta;
   int cs = 1;
   while (cs < need) cs <<= 1;
   return cs;
@@ -233,7 +233,7 @@ int cfc_forward_recurrence(const float* h0, const float* W, const float* ts, int
   p.u = nullptr; p.h0 = h0; p.W = W; p.bias = nullptr; p.ts = ts; p.H = H; p.cache = cache;
   p.status = st->status;
   p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
-  p.CS = cluster_size_for(C);
+  p.CS = cluster_size_for(C, cfc::kFwdChanPerCta);
   size_t smem = 0;
   int n_clusters = 0;
   rc = plan_rows(*st, 0, 0, p.CS, B, n_x, &p.R, &smem, &n_clusters);
@@ -289,7 +289,7 @@ int cfc_backward_recurrence(const float* dH, const float* W, const float* ts,
   p.dH = dH; p.W = W; p.ts = ts; p.cache = cache; p.d_pre = d_pre; p.dh0 = dh0;
   p.status = st->status;
   p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
-  p.CS = cluster_size_for(C);
+  p.CS = cluster_size_for(C, cfc::kChanPerCta);
   size_t smem = 0;
   int n_clusters = 0;
   rc = plan_rows(*st, 1, 0, p.CS, B, n_x, &p.R, &smem, &n_clusters);

@@ -160,14 +160,27 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 16 ? 1 : 2) cfc_bwd_kernel(
   // consecutive threads read consecutive channels of one W row.
   float wt[2][S::RS];
   {
+    // Chunks of loads are issued before their stores, so each chunk costs one round trip.
     float* wtmp = smem;
-    for (int e = tid; e < S::NG * kChanPerCta; e += kRecThreads) {
-      const int gidx = e >> 4, jl = e & 15;
-      const int chr = kChanPerCta * (gidx >> 6) + ((gidx & 63) >> 2);
-      const int j = kChanPerCta * rank + jl;
-      wtmp[gidx * (kChanPerCta + 1) + jl] =
-          (chr < C && j < C) ? p.W[(static_cast<size_t>(gidx & 3) * C + chr) * n_in + n_x + j]
-                             : 0.f;
+    constexpr int kPerThread = S::NG * kChanPerCta / kRecThreads;
+    constexpr int kChunk = kPerThread < 32 ? kPerThread : 32;
+    for (int i0 = 0; i0 < kPerThread; i0 += kChunk) {
+      float v[kChunk];
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        const int e = (i0 + i) * kRecThreads + tid;
+        const int gidx = e >> 4, jl = e & 15;
+        const int chr = kChanPerCta * (gidx >> 6) + ((gidx & 63) >> 2);
+        const int j = kChanPerCta * rank + jl;
+        v[i] = (chr < C && j < C)
+                   ? __ldg(p.W + (static_cast<size_t>(gidx & 3) * C + chr) * n_in + n_x + j)
+                   : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        const int e = (i0 + i) * kRecThreads + tid;
+        wtmp[(e >> 4) * (kChanPerCta + 1) + (e & 15)] = v[i];
+      }
     }
     __syncthreads();
 #pragma unroll

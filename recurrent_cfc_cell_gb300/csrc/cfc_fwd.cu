@@ -13,21 +13,30 @@
 //
 // Layout and schedule (every step is warp-local; no CTA-wide barrier inside the K-loop):
 //   * a thread-block cluster of CS CTAs serves R batch rows; CTA `rank` owns hidden channels
-//     [16*rank, 16*rank+16), and warp w of it owns channels 16*rank + 2w + {0, 1}: 8 W rows
-//     (2 channels x 4 gates);
-//   * lanes 16ci + sl keep the four gate rows of channel ci over the sl-th sixteenth of the
-//     recurrent columns (CS columns) in REGISTERS, so every h value loaded from shared memory
-//     feeds four FMAs; a 5-shuffle reduce-scatter over the 16 lanes leaves gate g of channel ci
-//     in lanes 16ci + 4g + (0..3), so activations, H / cache stores and the st.async pushes of
-//     the new h to all CS CTAs happen in the same warp;
-//   * h rows in shared memory are split into sixteen slices padded to an odd number of 16-byte
-//     chunks, so the vector loads of a quarter-warp hit distinct banks;
+//     [32*rank, 32*rank+32), and warp w of it owns channels 32*rank + 4w + {0..3}: 16 W rows
+//     (4 channels x 4 gates);
+//   * lanes 8cj + sl keep the four gate rows of channel cj over the sl-th eighth of the
+//     recurrent columns (4*CS columns) in REGISTERS, so every h value loaded from shared memory
+//     feeds four FMAs; a 4-shuffle reduce-scatter over the 8 lanes leaves gate g of channel cj
+//     in lanes 8cj + 2g + (0, 1), and the activations and H / cache stores happen in the same
+//     warp;
+//   * the warp's four new h values are contiguous in the h row, so they travel as ONE 16-byte
+//     st.async per destination CTA: a cluster moves 8*CS 16-byte pushes per CTA and step
+//     (measured on GB300: few wide pushes per step exchange markedly faster than many 4-byte
+//     ones once two clusters share an SM, and 32 channels per CTA halve the CTA count);
+//   * h rows in shared memory are split into eight slices padded to an odd number of 16-byte
+//     chunks, so the vector loads of the eight lanes of a channel hit distinct banks;
 //   * X and ts of step t+1 are loaded into registers during step t (X with an L2 load, since
 //     this kernel later overwrites that location with H / cache), so no global-memory latency
 //     sits on the serial chain; the number of batch rows per cluster (R) is a compile-time
 //     parameter so these per-row values stay in registers;
 //   * the destination mbarrier counts the pushed bytes, so a step waits on one local mbarrier.
-//     h buffers and mbarriers alternate with the step parity.
+//     h buffers and mbarriers alternate with the step parity;
+//   * per-lane addresses are computed once; the K-loop advances pointers by a fixed stride and
+//     uses predicated loads, stores and st.async (no index arithmetic or divergent branches on
+//     the serial chain);
+//   * the W_h block of the CTA is read coalesced into shared memory in the prologue and from
+//     there into registers.
 #include "cfc_kernels.h"
 #include "cfc_ptx.cuh"
 
@@ -36,11 +45,12 @@ namespace {
 
 template <int CS>
 struct FwdShape {
-  static constexpr int CHP = kChanPerCta * CS;  // padded channel count
-  static constexpr int HS = CHP / 16;           // h columns per lane (= CS)
-  // Slice pitch: vector loads of 8 consecutive lanes must cover distinct banks.
-  static constexpr int HSP = (HS >= 4 && (HS / 4) % 2 == 0) ? HS + 4 : HS;
-  static constexpr int HROW = 16 * HSP;         // h row in shared memory
+  static constexpr int CHP = kFwdChanPerCta * CS;  // padded channel count
+  static constexpr int HS = CHP / 8;               // h columns per lane (= 4 CS)
+  // Slice pitch: the vector loads of the 8 lanes of a channel must cover distinct banks.
+  static constexpr int HSP = ((HS / 4) % 2 == 0) ? HS + 4 : HS;
+  static constexpr int HROW = 8 * HSP;             // h row in shared memory
+  static constexpr int WP = CHP + 4;               // row pitch of the staged W_h block
 };
 
 // Load n consecutive floats (n = 1, 2 or a multiple of 4) from shared memory.
@@ -67,7 +77,7 @@ __device__ __forceinline__ int hpos(int j) {
 }
 
 template <int CS, int R>
-__global__ void __launch_bounds__(kRecThreads, 2) cfc_fwd_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(kRecThreads, CS >= 8 ? 1 : 2) cfc_fwd_kernel(const FwdParams p) {
   using S = FwdShape<CS>;
   extern __shared__ __align__(16) float smem[];
   float* hbuf = smem;  // [2][R][HROW]
@@ -80,42 +90,68 @@ __global__ void __launch_bounds__(kRecThreads, 2) cfc_fwd_kernel(const FwdParams
   const int row0 = static_cast<int>(cluster_id_x()) * R;  // first batch row of this cluster
   const int B = p.B, K = p.K, C = p.C, n_x = p.n_x, n_in = p.n_in;
 
-  // This lane: channel ci, column slice sl; after the reduce-scatter it holds gate g.
-  const int ci = lane >> 4;
-  const int sl = lane & 15;
-  const int g = (lane >> 2) & 3;
-  const int ch = kChanPerCta * rank + 2 * warp + ci;
+  // This lane: channel cj, column slice sl; after the reduce-scatter it holds gate g.
+  const int cj = lane >> 3;
+  const int sl = lane & 7;
+  const int g = (lane >> 1) & 3;
+  const int ch = kFwdChanPerCta * rank + 4 * warp + cj;
+
+  // W_h rows of the CTA's channels, staged coalesced as [4 gates x 32 channels][WP] (the whole
+  // shared-memory area is free before the K-loop), then this lane's 4 x HS block to registers.
   float wh[4][S::HS];
+  {
+    // Chunks of loads are issued before their stores, so each chunk costs one round trip.
+    float* wst = smem;
+    constexpr int kPerThread = 4 * kFwdChanPerCta * S::CHP / kRecThreads;
+    constexpr int kChunk = kPerThread < 32 ? kPerThread : 32;
+    for (int i0 = 0; i0 < kPerThread; i0 += kChunk) {
+      float v[kChunk];
 #pragma unroll
-  for (int gg = 0; gg < 4; ++gg)
+      for (int i = 0; i < kChunk; ++i) {
+        const int e = (i0 + i) * kRecThreads + tid;
+        const int lrow = e / S::CHP, col = e % S::CHP;
+        const int gg = lrow / kFwdChanPerCta, c = kFwdChanPerCta * rank + lrow % kFwdChanPerCta;
+        v[i] = (c < C && col < C) ? __ldg(p.W + (static_cast<size_t>(gg) * C + c) * n_in + n_x + col)
+                                  : 0.f;
+      }
 #pragma unroll
-    for (int c = 0; c < S::HS; ++c) {
-      const int j = sl * S::HS + c;
-      wh[gg][c] = (ch < C && j < C)
-                      ? p.W[(static_cast<size_t>(gg) * C + ch) * n_in + n_x + j] : 0.f;
+      for (int i = 0; i < kChunk; ++i) {
+        const int e = (i0 + i) * kRecThreads + tid;
+        wst[(e / S::CHP) * S::WP + e % S::CHP] = v[i];
+      }
     }
-  // Per-lane addresses, computed once: the K-loop only advances pointers by a fixed stride
-  // per step and issues predicated loads and stores (no index arithmetic or divergent
-  // branches on the serial chain).
+    __syncthreads();
+#pragma unroll
+    for (int gg = 0; gg < 4; ++gg) {
+      const float* src = wst + (gg * kFwdChanPerCta + 4 * warp + cj) * S::WP + sl * S::HS;
+#pragma unroll
+      for (int c = 0; c < S::HS; c += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src + c);
+        wh[gg][c] = v.x; wh[gg][c + 1] = v.y; wh[gg][c + 2] = v.z; wh[gg][c + 3] = v.w;
+      }
+    }
+    __syncthreads();
+  }
+
+  // Per-lane addresses, computed once.
   //   X of this lane's (channel, gate g) -- written in place into H / cache by the
   //   projection -- for row row0 + r of step t: xp + t * xstep + r * xrow;
-  //   the value this lane stores (lane q < 4: H, ff1, ff2, gate) likewise with q for g.
-  const int q = lane & 15;
+  //   the value this lane stores (lanes sl < 4: H, ff1, ff2, gate) likewise with sl for g.
   const int chc = ch < C ? ch : 0;  // padded channels read a valid location
   const size_t xrow = (g == 0) ? static_cast<size_t>(C) : 3ull * C;
-  const size_t srow = (q == 0) ? static_cast<size_t>(C) : 3ull * C;
+  const size_t srow = (sl == 0) ? static_cast<size_t>(C) : 3ull * C;
   const float* xp = ((g == 0) ? p.H : p.cache + static_cast<size_t>(g - 1) * C) + chc +
-                    static_cast<size_t>(row0 < B ? row0 : 0) * xrow;
-  float* sp = ((q == 0) ? p.H : p.cache + static_cast<size_t>(q > 0 && q < 4 ? q - 1 : 0) * C) +
-              chc + static_cast<size_t>(row0 < B ? row0 : 0) * srow;
-  const float* tsp = p.ts + (row0 < B ? row0 : 0);
+                    static_cast<size_t>(row0) * xrow;
+  float* sp = ((sl == 0) ? p.H : p.cache + static_cast<size_t>(sl > 0 && sl < 4 ? sl - 1 : 0) * C) +
+              chc + static_cast<size_t>(row0) * srow;
+  const float* tsp = p.ts + row0;
   const size_t xstep = static_cast<size_t>(B) * xrow, sstep = static_cast<size_t>(B) * srow;
   bool xok[R], sok[R], rok[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     rok[r] = row0 + r < B;
     xok[r] = rok[r] && ch < C;
-    sok[r] = xok[r] && q < 4;
+    sok[r] = xok[r] && sl < 4;
   }
 
   // X and ts of the step whose X row starts at xs (ts at tss), for every row of the group.
@@ -129,7 +165,7 @@ __global__ void __launch_bounds__(kRecThreads, 2) cfc_fwd_kernel(const FwdParams
 
   // ---- prologue ----
   const uint32_t bar0 = smem_addr(&bars[0]);  // bars[s] lives at bar0 + 8 s
-  const uint32_t tx_bytes = static_cast<uint32_t>(CS * R * kChanPerCta * 4);
+  const uint32_t tx_bytes = static_cast<uint32_t>(CS * R * kFwdChanPerCta * 4);
   if (tid == 0) {
     mbar_init(bar0, 1);
     mbar_init(bar0 + 8u, 1);
@@ -152,12 +188,13 @@ __global__ void __launch_bounds__(kRecThreads, 2) cfc_fwd_kernel(const FwdParams
   __syncthreads();     // h0 visible to every warp
   cluster_sync_all();  // barrier inits and buffers ready cluster-wide
 
-  // Pushes of the new h: lane q < CS writes this lane's channel into CTA q's buffer.  Remote
-  // addresses of buffer 0 / row 0; buffer d, row r is (d * R + r) * HROW floats further on.
-  const bool pushes = q < CS;
-  // (ch, not the clamped chc: a padded channel has its own slot in the padded h row.)
-  const uint32_t push0 = pushes ? map_to_rank(smem_addr(hbuf + hpos<CS>(ch)), q) : 0u;
-  const uint32_t rbar0 = pushes ? map_to_rank(bar0, q) : 0u;
+  // Pushes of the new h: lane q < CS writes the warp's four channels into CTA q's buffer.
+  // Remote addresses of buffer 0 / row 0; buffer d, row r is (d * R + r) * HROW floats on.
+  const bool pushes = lane < CS;
+  const uint32_t push0 =
+      pushes ? map_to_rank(smem_addr(hbuf + hpos<CS>(kFwdChanPerCta * rank + 4 * warp)), lane)
+             : 0u;
+  const uint32_t rbar0 = pushes ? map_to_rank(bar0, lane) : 0u;
 
   const float* xnext = xp + xstep;  // X and ts of step t + 1
   const float* tsnext = tsp + B;
@@ -184,7 +221,7 @@ __global__ void __launch_bounds__(kRecThreads, 2) cfc_fwd_kernel(const FwdParams
     const float* hb = hbuf + s * R * S::HROW + sl * S::HSP;
     const uint32_t pdst = push0 + static_cast<uint32_t>((s ^ 1) * R * S::HROW * 4);
     const uint32_t pbar = rbar0 + 8u * (s ^ 1);
-    const bool b3 = lane & 8, b2 = lane & 4;
+    const bool b2 = lane & 4, b1 = lane & 2;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       float hv[S::HS];
@@ -194,30 +231,33 @@ __global__ void __launch_bounds__(kRecThreads, 2) cfc_fwd_kernel(const FwdParams
       for (int c = 0; c < S::HS; ++c)
 #pragma unroll
         for (int gg = 0; gg < 4; ++gg) a[gg] = fmaf(wh[gg][c], hv[c], a[gg]);
-      // Reduce-scatter over the 16 lanes of the channel: lane keeps gate (lane >> 2) & 3.
-      const float k0 = b3 ? a[2] : a[0], k1 = b3 ? a[3] : a[1];
-      const float s0 = k0 + __shfl_xor_sync(0xffffffffu, b3 ? a[0] : a[2], 8);
-      const float s1 = k1 + __shfl_xor_sync(0xffffffffu, b3 ? a[1] : a[3], 8);
-      float acc = (b2 ? s1 : s0) + __shfl_xor_sync(0xffffffffu, b2 ? s0 : s1, 4);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      // Reduce-scatter over the 8 lanes of the channel: lane keeps gate (lane >> 1) & 3.
+      const float k0 = b2 ? a[2] : a[0], k1 = b2 ? a[3] : a[1];
+      const float s0 = k0 + __shfl_xor_sync(0xffffffffu, b2 ? a[0] : a[2], 4);
+      const float s1 = k1 + __shfl_xor_sync(0xffffffffu, b2 ? a[1] : a[3], 4);
+      float acc = (b1 ? s1 : s0) + __shfl_xor_sync(0xffffffffu, b1 ? s0 : s1, 2);
       acc += __shfl_xor_sync(0xffffffffu, acc, 1);
       const float P = acc + xc[r];
 
       // Activations: lanes of gate 0 / 1 evaluate tanh(P) = 2 sigmoid(2P) - 1, lanes of gate
-      // 2 the time gate sigmoid(P_ta ts + P_tb) (P_tb from the gate-3 lane four lanes up).
-      const float P_tb = __shfl_sync(0xffffffffu, P, (lane + 4) & 31);
-      const float x =
-          (g < 2) ? 2.f * P : fmaf(P, tc[r], P_tb);
+      // 2 the time gate sigmoid(P_ta ts + P_tb) (P_tb from the gate-3 lane two lanes up).
+      const float P_tb = __shfl_sync(0xffffffffu, P, (lane + 2) & 31);
+      const float x = (g < 2) ? 2.f * P : fmaf(P, tc[r], P_tb);
       const float sg = sigmoid_acc(x);
       const float y = (g < 2) ? fmaf(2.f, sg, -1.f) : sg;
-      const int half = lane & 16;
-      const float f1 = __shfl_sync(0xffffffffu, y, half + 0);
-      const float f2 = __shfl_sync(0xffffffffu, y, half + 4);
-      const float gt = __shfl_sync(0xffffffffu, y, half + 8);
+      const int base = lane & 24;
+      const float f1 = __shfl_sync(0xffffffffu, y, base + 0);
+      const float f2 = __shfl_sync(0xffffffffu, y, base + 2);
+      const float gt = __shfl_sync(0xffffffffu, y, base + 4);
       const float h = f1 * (1.f - gt) + gt * f2;
-      st_async_b32_if(pushes && t + 1 < K, pdst + static_cast<uint32_t>(r * S::HROW * 4), h,
-                      pbar);
-      const float sv = (q == 0) ? h : (q == 1) ? f1 : (q == 2 ? f2 : gt);
+      // The warp's four channels, gathered for one 16-byte push per destination CTA.
+      const float h0v = __shfl_sync(0xffffffffu, h, 0);
+      const float h1v = __shfl_sync(0xffffffffu, h, 8);
+      const float h2v = __shfl_sync(0xffffffffu, h, 16);
+      const float h3v = __shfl_sync(0xffffffffu, h, 24);
+      st_async_v4_if(pushes && t + 1 < K, pdst + static_cast<uint32_t>(r * S::HROW * 4), h0v,
+                     h1v, h2v, h3v, pbar);
+      const float sv = (sl == 0) ? h : (sl == 1) ? f1 : (sl == 2 ? f2 : gt);
       if (sok[r]) sp[r * srow] = sv;
     }
     sp += sstep;
@@ -304,9 +344,12 @@ cudaError_t launch_cs(const FwdParams& p, int n_clusters, size_t smem, cudaStrea
 }  // namespace
 
 size_t fwd_smem_bytes(int R, int CS) {
-  const size_t hs = CS;
-  const size_t hsp = (hs >= 4 && (hs / 4) % 2 == 0) ? hs + 4 : hs;
-  return sizeof(float) * 2ull * R * 16 * hsp + 2 * sizeof(uint64_t) + 16;
+  const size_t hs = 4ull * CS;
+  const size_t hsp = ((hs / 4) % 2 == 0) ? hs + 4 : hs;
+  const size_t loop = sizeof(float) * 2ull * R * 8 * hsp + 2 * sizeof(uint64_t) + 16;
+  // The prologue stages the CTA's W_h block ([4 x 32][32 CS + 4] floats) in the same area.
+  const size_t stage = sizeof(float) * 4ull * kFwdChanPerCta * (kFwdChanPerCta * CS + 4);
+  return loop > stage ? loop : stage;
 }
 
 cudaError_t fwd_prepare(int CS, int R, size_t smem, int* max_active) {
@@ -315,7 +358,6 @@ cudaError_t fwd_prepare(int CS, int R, size_t smem, int* max_active) {
     case 2: return prepare_cs<2>(R, smem, max_active);
     case 4: return prepare_cs<4>(R, smem, max_active);
     case 8: return prepare_cs<8>(R, smem, max_active);
-    case 16: return prepare_cs<16>(R, smem, max_active);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -326,7 +368,6 @@ cudaError_t fwd_launch(const FwdParams& p, int n_clusters, size_t smem, cudaStre
     case 2: return launch_cs<2>(p, n_clusters, smem, s);
     case 4: return launch_cs<4>(p, n_clusters, smem, s);
     case 8: return launch_cs<8>(p, n_clusters, smem, s);
-    case 16: return launch_cs<16>(p, n_clusters, smem, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -6,9 +6,10 @@
 
 namespace cfc {
 
-// Channel tiling shared by the two recurrence kernels: every CTA of a cluster owns 16 hidden
-// channels (all four gates of each), so a cluster of CS CTAs covers 16*CS >= C channels.
-constexpr int kChanPerCta = 16;
+// Channel tiling of the two recurrence kernels: every CTA of a cluster owns a fixed number of
+// hidden channels (all four gates of each), so a cluster of CS CTAs covers that many x CS >= C.
+constexpr int kChanPerCta = 16;     // backward recurrence
+constexpr int kFwdChanPerCta = 32;  // forward recurrence: a cluster of CS CTAs covers 32*CS
 constexpr int kRowsPerCta = 4 * kChanPerCta;  // W rows held by one CTA (gate-minor order)
 constexpr int kRecThreads = 256;
 constexpr int kMaxClusterSize = 16;
