@@ -214,12 +214,18 @@ int cfc_input_projection(const float* u, const float* W, const float* b, int B, 
   rc = device_state(&st);
   if (rc != CFC_OK) return rc;
   return cuda_rc(cfc::inproj_launch(u, W, b, B * K, C, n_x, H, cache,
-                                    static_cast<cudaStream_t>(stream)),
+                                    static_cast<cudaStream_t>(stream), false),
                  CFC_ERR_LAUNCH_FAILED);
 }
 
-int cfc_forward_recurrence(const float* h0, const float* W, const float* ts, int B, int K,
-                           int C, int n_x, float* H, float* cache, cfc_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// `pdl`: the previous kernel of the stream is one of this library's kernels of the same call
+// (see cfc_launch.cuh).
+int forward_recurrence(const float* h0, const float* W, const float* ts, int B, int K, int C,
+                       int n_x, float* H, float* cache, cfc_stream_t stream, bool pdl) {
   int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
   if (!h0 || !W || !ts || !H || !cache) return CFC_ERR_NULL_PTR;
@@ -238,8 +244,17 @@ int cfc_forward_recurrence(const float* h0, const float* W, const float* ts, int
   int n_clusters = 0;
   rc = plan_rows(*st, 0, 0, p.CS, B, n_x, &p.R, &smem, &n_clusters);
   if (rc != CFC_OK) return rc;
-  return cuda_rc(cfc::fwd_launch(p, n_clusters, smem, static_cast<cudaStream_t>(stream)),
+  return cuda_rc(cfc::fwd_launch(p, n_clusters, smem, static_cast<cudaStream_t>(stream), pdl),
                  CFC_ERR_LAUNCH_FAILED);
+}
+
+}  // namespace
+
+extern "C" {
+
+int cfc_forward_recurrence(const float* h0, const float* W, const float* ts, int B, int K,
+                           int C, int n_x, float* H, float* cache, cfc_stream_t stream) {
+  return forward_recurrence(h0, W, ts, B, K, C, n_x, H, cache, stream, false);
 }
 
 int cfc_forward(const float* u, const float* h0, const float* W, const float* b,
@@ -253,7 +268,10 @@ int cfc_forward(const float* u, const float* h0, const float* W, const float* b,
     return CFC_ERR_MISALIGNED;
   rc = cfc_input_projection(u, W, b, B, K, C, n_x, H, cache, stream);
   if (rc != CFC_OK) return rc;
-  return cfc_forward_recurrence(h0, W, ts, B, K, C, n_x, H, cache, stream);
+  // Not a dependent launch: scheduled early, the recurrence clusters land on SMs the
+  // projection still occupies and end up two CTAs to an SM, which slows every one of the K
+  // steps (measured on GB300: the training step took 149.6 us this way against 140.7 us).
+  return forward_recurrence(h0, W, ts, B, K, C, n_x, H, cache, stream, false);
 }
 
 int cfc_step_launches(int B, int K, int C, int n_x, int dw_mode, int with_du, int* launches) {
@@ -294,13 +312,19 @@ int cfc_backward_recurrence(const float* dH, const float* W, const float* ts,
   int n_clusters = 0;
   rc = plan_rows(*st, 1, 0, p.CS, B, n_x, &p.R, &smem, &n_clusters);
   if (rc != CFC_OK) return rc;
-  return cuda_rc(cfc::bwd_launch(p, n_clusters, smem, static_cast<cudaStream_t>(stream)),
+  return cuda_rc(cfc::bwd_launch(p, n_clusters, smem, static_cast<cudaStream_t>(stream), false),
                  CFC_ERR_LAUNCH_FAILED);
 }
 
-int cfc_weight_grad(const float* d_pre, const float* u, const float* h0, const float* W,
-                    const float* H, int B, int K, int C, int n_x, float* dW, float* db,
-                    float* du, void* ws, size_t ws_bytes, int dw_mode, cfc_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// `first_pdl`: the previous kernel of the stream is this library's BPTT recurrence of the same
+// backward call; every later kernel here follows one of this function's own kernels.
+int weight_grad(const float* d_pre, const float* u, const float* h0, const float* W,
+                const float* H, int B, int K, int C, int n_x, float* dW, float* db, float* du,
+                void* ws, size_t ws_bytes, int dw_mode, cfc_stream_t stream, bool first_pdl) {
   int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
   if (dw_mode != CFC_DW_ACCURATE && dw_mode != CFC_DW_SIMT_FP32) return CFC_ERR_INVALID_ARG;
@@ -321,33 +345,49 @@ int cfc_weight_grad(const float* d_pre, const float* u, const float* h0, const f
   int S = 0;
   if (dw_mode == CFC_DW_SIMT_FP32) {
     S = L.S_simt;
-    rc = cuda_rc(cfc::dw_simt_launch(d_pre, u, H, h0, B, K, C, n_x, S, partial, s),
+    rc = cuda_rc(cfc::dw_simt_launch(d_pre, u, H, h0, B, K, C, n_x, S, partial, s, first_pdl),
                  CFC_ERR_LAUNCH_FAILED);
   } else {
     S = L.tc.splits;
-    rc = cuda_rc(cfc::dw_tc_launch(L.tc, d_pre, u, H, h0, B, K, C, n_x, partial, st->status, s),
+    rc = cuda_rc(cfc::dw_tc_launch(L.tc, d_pre, u, H, h0, B, K, C, n_x, partial, st->status, s,
+                                   first_pdl),
                  CFC_ERR_LAUNCH_FAILED);
   }
   if (rc != CFC_OK) return rc;
-  rc = cuda_rc(cfc::reduce_axis0_launch(partial, S, M * N, dW, s), CFC_ERR_LAUNCH_FAILED);
+  rc = cuda_rc(cfc::reduce_axis0_launch(partial, S, M * N, dW, s, true), CFC_ERR_LAUNCH_FAILED);
   if (rc != CFC_OK) return rc;
-  rc = cuda_rc(cfc::reduce_axis0_launch(d_pre, BK, M, db, s), CFC_ERR_LAUNCH_FAILED);
+  rc = cuda_rc(cfc::reduce_axis0_launch(d_pre, BK, M, db, s, true), CFC_ERR_LAUNCH_FAILED);
   if (rc != CFC_OK) return rc;
   if (du) {
     if (dw_mode == CFC_DW_SIMT_FP32) {
-      rc = cuda_rc(cfc::du_simt_launch(d_pre, W, BK, C, n_x, du, s), CFC_ERR_LAUNCH_FAILED);
+      rc = cuda_rc(cfc::du_simt_launch(d_pre, W, BK, C, n_x, du, s, true),
+                   CFC_ERR_LAUNCH_FAILED);
     } else if (L.tu.splits == 1) {
-      rc = cuda_rc(cfc::du_tc_launch(L.tu, d_pre, W, B, K, C, n_x, du, st->status, s),
+      rc = cuda_rc(cfc::du_tc_launch(L.tu, d_pre, W, B, K, C, n_x, du, st->status, s, true),
                    CFC_ERR_LAUNCH_FAILED);
     } else {
-      rc = cuda_rc(cfc::du_tc_launch(L.tu, d_pre, W, B, K, C, n_x, partial, st->status, s),
-                   CFC_ERR_LAUNCH_FAILED);
+      // The du partials reuse the dW partial area: the dW reduction above has read it, and
+      // that reduction completes before this kernel passes its grid-dependency wait.
+      rc = cuda_rc(
+          cfc::du_tc_launch(L.tu, d_pre, W, B, K, C, n_x, partial, st->status, s, true),
+          CFC_ERR_LAUNCH_FAILED);
       if (rc == CFC_OK)
-        rc = cuda_rc(cfc::reduce_axis0_launch(partial, L.tu.splits, BK * n_x, du, s),
+        rc = cuda_rc(cfc::reduce_axis0_launch(partial, L.tu.splits, BK * n_x, du, s, true),
                      CFC_ERR_LAUNCH_FAILED);
     }
   }
   return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cfc_weight_grad(const float* d_pre, const float* u, const float* h0, const float* W,
+                    const float* H, int B, int K, int C, int n_x, float* dW, float* db,
+                    float* du, void* ws, size_t ws_bytes, int dw_mode, cfc_stream_t stream) {
+  return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode,
+                     stream, false);
 }
 
 int cfc_backward(const float* dH, const float* u, const float* h0, const float* W,
@@ -368,8 +408,8 @@ int cfc_backward(const float* dH, const float* u, const float* h0, const float* 
   float* d_pre = reinterpret_cast<float*>(static_cast<char*>(ws) + L.d_pre_off);
   rc = cfc_backward_recurrence(dH, W, ts, cache, B, K, C, n_x, d_pre, dh0, stream);
   if (rc != CFC_OK) return rc;
-  return cfc_weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode,
-                         stream);
+  return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode, stream,
+                     true);
 }
 
 int reduce_axis0(const float* per_batch, int n_batch, int n_tail, float* out,
@@ -383,7 +423,7 @@ int reduce_axis0(const float* per_batch, int n_batch, int n_tail, float* out,
   const int rc = device_state(&st);
   if (rc != CFC_OK) return rc;
   return cuda_rc(cfc::reduce_axis0_launch(per_batch, n_batch, n_tail, out,
-                                          static_cast<cudaStream_t>(stream)),
+                                          static_cast<cudaStream_t>(stream), false),
                  CFC_ERR_LAUNCH_FAILED);
 }
 

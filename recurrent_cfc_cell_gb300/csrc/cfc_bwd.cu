@@ -35,6 +35,7 @@
 //   * the W_h^T columns are read once, coalesced, into shared memory and from there into
 //     registers (a direct load would fetch one 32-byte sector per 4-byte value).
 #include "cfc_kernels.h"
+#include "cfc_launch.cuh"
 #include "cfc_ptx.cuh"
 
 namespace cfc {
@@ -146,6 +147,7 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 16 ? 1 : 2) cfc_bwd_kernel(
   float* pre = dg + 2 * R * S::GROW;     // ring path: [kPre][R][8 warps][2][5]
   const int pre_floats = RT > 0 ? 0 : kPre * R * kWarps * 2 * kPreComp;
   uint64_t* bars = reinterpret_cast<uint64_t*>(pre + pre_floats);
+  grid_dep_launch_dependents();
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -233,6 +235,8 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 16 ? 1 : 2) cfc_bwd_kernel(
              : 0u;
   const uint32_t rbar0 = pushes ? map_to_rank(bar0, q) : 0u;
 
+  // Everything above reads only W; dH and the forward cache may come from the previous kernel.
+  grid_dep_wait();
   float cur[RR][kPreComp];  // register path: inputs of the current step
   if constexpr (RT > 0) {
     load_step_regs<RR>(dHp, cp, tsp, C, rok, cur);
@@ -369,20 +373,15 @@ cudaError_t prepare_k(size_t smem, int* max_active) {
 }
 
 template <int CS, int RT>
-cudaError_t launch_k(const BwdParams& p, int n_clusters, size_t smem, cudaStream_t s) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_clusters * CS, 1, 1);
-  cfg.blockDim = dim3(kRecThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CS;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, cfc_bwd_kernel<CS, RT>, p);
+cudaError_t launch_k(const BwdParams& p, int n_clusters, size_t smem, cudaStream_t s, bool pdl) {
+  LaunchCfg c;
+  c.grid = dim3(n_clusters * CS, 1, 1);
+  c.block = dim3(kRecThreads, 1, 1);
+  c.smem = smem;
+  c.stream = s;
+  c.pdl = pdl;
+  c.cluster = dim3(CS, 1, 1);
+  return launch(c, cfc_bwd_kernel<CS, RT>, p);
 }
 
 // Row groups of 1, 2 or 4 use the register-prefetch kernels, larger ones the ring kernel.
@@ -399,12 +398,13 @@ cudaError_t prepare_cs(int R, size_t smem, int* max_active) {
 }
 
 template <int CS>
-cudaError_t launch_cs(const BwdParams& p, int n_clusters, size_t smem, cudaStream_t s) {
+cudaError_t launch_cs(const BwdParams& p, int n_clusters, size_t smem, cudaStream_t s,
+                      bool pdl) {
   switch (bwd_variant(p.R)) {
-    case 1: return launch_k<CS, 1>(p, n_clusters, smem, s);
-    case 2: return launch_k<CS, 2>(p, n_clusters, smem, s);
-    case 4: return launch_k<CS, 4>(p, n_clusters, smem, s);
-    default: return launch_k<CS, 0>(p, n_clusters, smem, s);
+    case 1: return launch_k<CS, 1>(p, n_clusters, smem, s, pdl);
+    case 2: return launch_k<CS, 2>(p, n_clusters, smem, s, pdl);
+    case 4: return launch_k<CS, 4>(p, n_clusters, smem, s, pdl);
+    default: return launch_k<CS, 0>(p, n_clusters, smem, s, pdl);
   }
 }
 
@@ -431,13 +431,14 @@ cudaError_t bwd_prepare(int CS, int R, size_t smem, int* max_active) {
   }
 }
 
-cudaError_t bwd_launch(const BwdParams& p, int n_clusters, size_t smem, cudaStream_t s) {
+cudaError_t bwd_launch(const BwdParams& p, int n_clusters, size_t smem, cudaStream_t s,
+                       bool pdl) {
   switch (p.CS) {
-    case 1: return launch_cs<1>(p, n_clusters, smem, s);
-    case 2: return launch_cs<2>(p, n_clusters, smem, s);
-    case 4: return launch_cs<4>(p, n_clusters, smem, s);
-    case 8: return launch_cs<8>(p, n_clusters, smem, s);
-    case 16: return launch_cs<16>(p, n_clusters, smem, s);
+    case 1: return launch_cs<1>(p, n_clusters, smem, s, pdl);
+    case 2: return launch_cs<2>(p, n_clusters, smem, s, pdl);
+    case 4: return launch_cs<4>(p, n_clusters, smem, s, pdl);
+    case 8: return launch_cs<8>(p, n_clusters, smem, s, pdl);
+    case 16: return launch_cs<16>(p, n_clusters, smem, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

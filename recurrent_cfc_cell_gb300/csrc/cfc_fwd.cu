@@ -38,6 +38,7 @@
 //   * the W_h block of the CTA is read coalesced into shared memory in the prologue and from
 //     there into registers.
 #include "cfc_kernels.h"
+#include "cfc_launch.cuh"
 #include "cfc_ptx.cuh"
 
 namespace cfc {
@@ -83,6 +84,7 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 8 ? 1 : 2) cfc_fwd_kernel(c
   float* hbuf = smem;  // [2][R][HROW]
   uint64_t* bars = reinterpret_cast<uint64_t*>(hbuf + 2 * R * S::HROW);
 
+  grid_dep_launch_dependents();
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -178,6 +180,8 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 8 ? 1 : 2) cfc_fwd_kernel(c
     if (row0 + r < B)
       hbuf[r * S::HROW + hpos<CS>(j)] = p.h0[static_cast<size_t>(row0 + r) * C + j];
   }
+  // Everything above reads only W and h0; X comes from the projection kernel.
+  grid_dep_wait();
   float xc[R], tc[R];  // X and ts of the current step
   load_step(xp, tsp, xc, tc);
   // Step t consumes h_{t-1} through bars[t & 1]; arm the first two consumers (t = 1, 2).
@@ -305,20 +309,15 @@ cudaError_t prepare_k(size_t smem, int* max_active) {
 }
 
 template <int CS, int R>
-cudaError_t launch_k(const FwdParams& p, int n_clusters, size_t smem, cudaStream_t s) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_clusters * CS, 1, 1);
-  cfg.blockDim = dim3(kRecThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CS;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, cfc_fwd_kernel<CS, R>, p);
+cudaError_t launch_k(const FwdParams& p, int n_clusters, size_t smem, cudaStream_t s, bool pdl) {
+  LaunchCfg c;
+  c.grid = dim3(n_clusters * CS, 1, 1);
+  c.block = dim3(kRecThreads, 1, 1);
+  c.smem = smem;
+  c.stream = s;
+  c.pdl = pdl;
+  c.cluster = dim3(CS, 1, 1);
+  return launch(c, cfc_fwd_kernel<CS, R>, p);
 }
 
 template <int CS>
@@ -332,11 +331,12 @@ cudaError_t prepare_cs(int R, size_t smem, int* max_active) {
 }
 
 template <int CS>
-cudaError_t launch_cs(const FwdParams& p, int n_clusters, size_t smem, cudaStream_t s) {
+cudaError_t launch_cs(const FwdParams& p, int n_clusters, size_t smem, cudaStream_t s,
+                      bool pdl) {
   switch (p.R) {
-    case 1: return launch_k<CS, 1>(p, n_clusters, smem, s);
-    case 2: return launch_k<CS, 2>(p, n_clusters, smem, s);
-    case 4: return launch_k<CS, 4>(p, n_clusters, smem, s);
+    case 1: return launch_k<CS, 1>(p, n_clusters, smem, s, pdl);
+    case 2: return launch_k<CS, 2>(p, n_clusters, smem, s, pdl);
+    case 4: return launch_k<CS, 4>(p, n_clusters, smem, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -362,12 +362,13 @@ cudaError_t fwd_prepare(int CS, int R, size_t smem, int* max_active) {
   }
 }
 
-cudaError_t fwd_launch(const FwdParams& p, int n_clusters, size_t smem, cudaStream_t s) {
+cudaError_t fwd_launch(const FwdParams& p, int n_clusters, size_t smem, cudaStream_t s,
+                       bool pdl) {
   switch (p.CS) {
-    case 1: return launch_cs<1>(p, n_clusters, smem, s);
-    case 2: return launch_cs<2>(p, n_clusters, smem, s);
-    case 4: return launch_cs<4>(p, n_clusters, smem, s);
-    case 8: return launch_cs<8>(p, n_clusters, smem, s);
+    case 1: return launch_cs<1>(p, n_clusters, smem, s, pdl);
+    case 2: return launch_cs<2>(p, n_clusters, smem, s, pdl);
+    case 4: return launch_cs<4>(p, n_clusters, smem, s, pdl);
+    case 8: return launch_cs<8>(p, n_clusters, smem, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

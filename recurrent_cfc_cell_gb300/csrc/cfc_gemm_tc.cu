@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 
 #include "cfc_kernels.h"
+#include "cfc_launch.cuh"
 #include "cfc_ptx.cuh"
 
 namespace cfc {
@@ -239,6 +240,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcParams p
   uint32_t ncols = 32;
   while (ncols < static_cast<uint32_t>(p.n_tile)) ncols <<= 1;
 
+  grid_dep_launch_dependents();
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full0 + 8u * s, kConv);
@@ -247,6 +249,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcParams p
     mbar_init(accb, 1);
     fence_mbar_init_cluster();
   }
+  // The operands come from the previous kernel; the tensor memory is taken only after it has
+  // finished, so this kernel never waits for tensor memory a running predecessor holds.
+  grid_dep_wait();
   if (warp == kConv / 32) {
     tmem_alloc(smem_addr(tmem_slot), ncols);
     tc_fence_before_sync();
@@ -373,23 +378,31 @@ TcParams make_params(const TcPlan& pl, const float* d_pre, int B, int K, int C, 
 
 cudaError_t dw_tc_launch(const TcPlan& pl, const float* d_pre, const float* u, const float* H,
                          const float* h0, int B, int K, int C, int n_x, float* partial,
-                         int* status, cudaStream_t s) {
+                         int* status, cudaStream_t s, bool pdl) {
   TcParams p = make_params(pl, d_pre, B, K, C, n_x, status);
   p.u = u; p.H = H; p.h0 = h0; p.out = partial;
   p.rows = 4 * C; p.cols = n_x + C; p.red = B * K;
-  dim3 grid(pl.m_tiles * pl.n_tiles, pl.splits, 1);
-  tc_gemm_kernel<DwProblem><<<grid, kTcThreads, pl.smem, s>>>(p);
-  return cudaGetLastError();
+  LaunchCfg c;
+  c.grid = dim3(pl.m_tiles * pl.n_tiles, pl.splits, 1);
+  c.block = dim3(kTcThreads, 1, 1);
+  c.smem = pl.smem;
+  c.stream = s;
+  c.pdl = pdl;
+  return launch(c, tc_gemm_kernel<DwProblem>, p);
 }
 
 cudaError_t du_tc_launch(const TcPlan& pl, const float* d_pre, const float* W, int B, int K,
-                         int C, int n_x, float* du, int* status, cudaStream_t s) {
+                         int C, int n_x, float* du, int* status, cudaStream_t s, bool pdl) {
   TcParams p = make_params(pl, d_pre, B, K, C, n_x, status);
   p.W = W; p.out = du;
   p.rows = B * K; p.cols = n_x; p.red = 4 * C;
-  dim3 grid(pl.m_tiles * pl.n_tiles, pl.splits, 1);
-  tc_gemm_kernel<DuProblem><<<grid, kTcThreads, pl.smem, s>>>(p);
-  return cudaGetLastError();
+  LaunchCfg c;
+  c.grid = dim3(pl.m_tiles * pl.n_tiles, pl.splits, 1);
+  c.block = dim3(kTcThreads, 1, 1);
+  c.smem = pl.smem;
+  c.stream = s;
+  c.pdl = pdl;
+  return launch(c, tc_gemm_kernel<DuProblem>, p);
 }
 
 }  // namespace cfc

@@ -12,6 +12,8 @@
 // These kernels are the fp32 reference path (exact fp32 FMA, no operand rounding); the
 // tensor-core contraction is the fast path.
 #include "cfc_kernels.h"
+#include "cfc_launch.cuh"
+#include "cfc_ptx.cuh"
 
 namespace cfc {
 namespace {
@@ -37,6 +39,8 @@ __global__ void __launch_bounds__(256) dw_simt_kernel(const float* __restrict__ 
                                                        float* __restrict__ partial) {
   __shared__ __align__(16) float As[kTK][kTM];
   __shared__ __align__(16) float Zs[kTK][kTN];
+  grid_dep_launch_dependents();
+  grid_dep_wait();
   const int M = 4 * C, N = n_x + C, BK = B * K;
   const int m0 = blockIdx.y * kTM, n0 = blockIdx.x * kTN;
   const int s = blockIdx.z;
@@ -88,6 +92,8 @@ __global__ void __launch_bounds__(256) du_simt_kernel(const float* __restrict__ 
                                                        int n_x, float* __restrict__ du) {
   __shared__ __align__(16) float As[kTK][kTM + 4];  // [m][r]
   __shared__ __align__(16) float Ws[kTK][kTN];      // [m][k]
+  grid_dep_launch_dependents();
+  grid_dep_wait();
   const int M = 4 * C, n_in = n_x + C;
   const int r0 = blockIdx.y * kTM, k0 = blockIdx.x * kTN;
   const int tid = threadIdx.x;
@@ -140,18 +146,25 @@ int dw_simt_splits(int BK) {
 }
 
 cudaError_t dw_simt_launch(const float* d_pre, const float* u, const float* H, const float* h0,
-                           int B, int K, int C, int n_x, int S, float* partial, cudaStream_t s) {
+                           int B, int K, int C, int n_x, int S, float* partial, cudaStream_t s,
+                           bool pdl) {
   const int M = 4 * C, N = n_x + C;
-  dim3 grid((N + kTN - 1) / kTN, (M + kTM - 1) / kTM, S);
-  dw_simt_kernel<<<grid, 256, 0, s>>>(d_pre, u, H, h0, B, K, C, n_x, S, partial);
-  return cudaGetLastError();
+  LaunchCfg c;
+  c.grid = dim3((N + kTN - 1) / kTN, (M + kTM - 1) / kTM, S);
+  c.block = dim3(256, 1, 1);
+  c.stream = s;
+  c.pdl = pdl;
+  return launch(c, dw_simt_kernel, d_pre, u, H, h0, B, K, C, n_x, S, partial);
 }
 
 cudaError_t du_simt_launch(const float* d_pre, const float* W, int BK, int C, int n_x,
-                           float* du, cudaStream_t s) {
-  dim3 grid((n_x + kTN - 1) / kTN, (BK + kTM - 1) / kTM, 1);
-  du_simt_kernel<<<grid, 256, 0, s>>>(d_pre, W, BK, C, n_x, du);
-  return cudaGetLastError();
+                           float* du, cudaStream_t s, bool pdl) {
+  LaunchCfg c;
+  c.grid = dim3((n_x + kTN - 1) / kTN, (BK + kTM - 1) / kTM, 1);
+  c.block = dim3(256, 1, 1);
+  c.stream = s;
+  c.pdl = pdl;
+  return launch(c, du_simt_kernel, d_pre, W, BK, C, n_x, du);
 }
 
 }  // namespace cfc

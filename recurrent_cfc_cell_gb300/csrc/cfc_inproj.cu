@@ -11,6 +11,8 @@
 // CUDA-core fp32: a 64 x 64 output tile per CTA (256 threads, 4 x 4 each), k in chunks of 16
 // through shared memory.
 #include "cfc_kernels.h"
+#include "cfc_launch.cuh"
+#include "cfc_ptx.cuh"
 
 namespace cfc {
 namespace {
@@ -24,6 +26,8 @@ __global__ void __launch_bounds__(256) inproj_kernel(const float* __restrict__ u
                                                       float* __restrict__ cache) {
   __shared__ __align__(16) float Us[kTK][kTR + 4];  // [k][row]
   __shared__ __align__(16) float Ws[kTK][kTM + 4];  // [k][m]
+  grid_dep_launch_dependents();
+  grid_dep_wait();
   const int M = 4 * C, n_in = n_x + C;
   const int r0 = blockIdx.y * kTR, m0 = blockIdx.x * kTM;
   const int tid = threadIdx.x;
@@ -73,10 +77,13 @@ __global__ void __launch_bounds__(256) inproj_kernel(const float* __restrict__ u
 }  // namespace
 
 cudaError_t inproj_launch(const float* u, const float* W, const float* bias, int BK, int C,
-                          int n_x, float* H, float* cache, cudaStream_t s) {
-  dim3 grid((4 * C + kTM - 1) / kTM, (BK + kTR - 1) / kTR, 1);
-  inproj_kernel<<<grid, 256, 0, s>>>(u, W, bias, BK, C, n_x, H, cache);
-  return cudaGetLastError();
+                          int n_x, float* H, float* cache, cudaStream_t s, bool pdl) {
+  LaunchCfg c;
+  c.grid = dim3((4 * C + kTM - 1) / kTM, (BK + kTR - 1) / kTR, 1);
+  c.block = dim3(256, 1, 1);
+  c.stream = s;
+  c.pdl = pdl;
+  return launch(c, inproj_kernel, u, W, bias, BK, C, n_x, H, cache);
 }
 
 }  // namespace cfc

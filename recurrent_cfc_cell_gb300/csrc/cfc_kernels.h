@@ -43,23 +43,30 @@ struct BwdParams {
   int CS, R;
 };
 
+// Every launch function takes `pdl`: schedule the kernel while the previous kernel of the
+// stream is still running (programmatic dependent launch; see cfc_launch.cuh).  Set only
+// between two kernels of the same entry point.
+
 // Recurrence kernels (persistent over all K steps, one cluster per group of R batch rows).
 size_t fwd_smem_bytes(int R, int CS);
 cudaError_t fwd_prepare(int CS, int R, size_t smem, int* max_active_clusters);
-cudaError_t fwd_launch(const FwdParams& p, int n_clusters, size_t smem, cudaStream_t s);
+cudaError_t fwd_launch(const FwdParams& p, int n_clusters, size_t smem, cudaStream_t s,
+                       bool pdl);
 
 size_t bwd_smem_bytes(int R, int CS);
 cudaError_t bwd_prepare(int CS, int R, size_t smem, int* max_active_clusters);
-cudaError_t bwd_launch(const BwdParams& p, int n_clusters, size_t smem, cudaStream_t s);
+cudaError_t bwd_launch(const BwdParams& p, int n_clusters, size_t smem, cudaStream_t s,
+                       bool pdl);
 
 // X = W_u u + b for all steps, written in place into H (gate ff1) and cache (ff2, ta, tb).
 cudaError_t inproj_launch(const float* u, const float* W, const float* bias, int BK, int C,
-                          int n_x, float* H, float* cache, cudaStream_t s);
+                          int n_x, float* H, float* cache, cudaStream_t s, bool pdl);
 
 // Weight gradient, split over the B*K reduction: partial[s][m][n] for m < 4C, n < n_in.
 int dw_simt_splits(int BK);
 cudaError_t dw_simt_launch(const float* d_pre, const float* u, const float* H, const float* h0,
-                           int B, int K, int C, int n_x, int S, float* partial, cudaStream_t s);
+                           int B, int K, int C, int n_x, int S, float* partial, cudaStream_t s,
+                           bool pdl);
 
 // dW and du on tcgen05 tensor cores (bf16 hi/lo split, fp32 accumulation in TMEM).
 struct TcPlan {
@@ -71,18 +78,18 @@ TcPlan du_tc_plan(int B, int K, int C, int n_x);  // split over 4C when B*K is s
 cudaError_t tc_prepare(int max_smem);
 cudaError_t dw_tc_launch(const TcPlan& pl, const float* d_pre, const float* u, const float* H,
                          const float* h0, int B, int K, int C, int n_x, float* partial,
-                         int* status, cudaStream_t s);
+                         int* status, cudaStream_t s, bool pdl);
 // du, or (when pl.splits > 1) its partial blocks [splits][B*K][n_x].
 cudaError_t du_tc_launch(const TcPlan& pl, const float* d_pre, const float* W, int B, int K,
-                         int C, int n_x, float* du, int* status, cudaStream_t s);
+                         int C, int n_x, float* du, int* status, cudaStream_t s, bool pdl);
 
 // du[r][k] = sum_m d_pre[r][m] * W[m][k] for k < n_x (SIMT fp32).
 cudaError_t du_simt_launch(const float* d_pre, const float* W, int BK, int C, int n_x,
-                           float* du, cudaStream_t s);
+                           float* du, cudaStream_t s, bool pdl);
 
 // Deterministic axis-0 sum with overwrite semantics.
 cudaError_t reduce_axis0_prepare();
 cudaError_t reduce_axis0_launch(const float* in, int n_batch, int n_tail, float* out,
-                                cudaStream_t s);
+                                cudaStream_t s, bool pdl);
 
 }  // namespace cfc

@@ -15,6 +15,17 @@ constexpr int kStatusTimeout = 1;
 // kStatusTimeout and winds down).  Correct launches never come near it.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// Programmatic dependent launch: wait until the previous kernel of the stream has completed
+// and its writes are visible (a no-op when the kernel was launched without the attribute) ...
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ... and allow the next kernel of the stream to be scheduled before this one completes.
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -12,6 +12,7 @@
 // are merged through distributed shared memory in rank order.  The summation order depends only
 // on (n_batch, n_tail), so the result is bitwise reproducible run to run.
 #include "cfc_kernels.h"
+#include "cfc_launch.cuh"
 #include "cfc_ptx.cuh"
 
 namespace cfc {
@@ -27,6 +28,8 @@ __global__ void __launch_bounds__(kRowLanes * kColLanes) reduce_axis0_kernel(
   constexpr int TC = kColLanes * VEC;
   __shared__ __align__(16) float part[kRowLanes][TC];
   __shared__ __align__(16) float cta_sum[TC];
+  grid_dep_launch_dependents();
+  grid_dep_wait();
   const int tid = threadIdx.x;
   const int cl = tid % kColLanes, rl = tid / kColLanes;
   const int col = blockIdx.x * TC + cl * VEC;
@@ -107,24 +110,18 @@ int choose_cz(int n_batch) {
 }
 
 template <int VEC>
-cudaError_t launch_vec(const float* in, int n_batch, int n_tail, float* out, cudaStream_t s) {
+cudaError_t launch_vec(const float* in, int n_batch, int n_tail, float* out, cudaStream_t s,
+                       bool pdl) {
   constexpr int TC = kColLanes * VEC;
   const int cz = choose_cz(n_batch);
   const int rows_per_cta = (n_batch + cz - 1) / cz;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((n_tail + TC - 1) / TC, cz, 1);
-  cfg.blockDim = dim3(kRowLanes * kColLanes, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = cz;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, reduce_axis0_kernel<VEC>, in, n_batch, n_tail, rows_per_cta,
-                            out);
+  LaunchCfg c;
+  c.grid = dim3((n_tail + TC - 1) / TC, cz, 1);
+  c.block = dim3(kRowLanes * kColLanes, 1, 1);
+  c.stream = s;
+  c.pdl = pdl;
+  c.cluster = dim3(1, cz, 1);
+  return launch(c, reduce_axis0_kernel<VEC>, in, n_batch, n_tail, rows_per_cta, out);
 }
 
 }  // namespace
@@ -138,10 +135,10 @@ cudaError_t reduce_axis0_prepare() {
 }
 
 cudaError_t reduce_axis0_launch(const float* in, int n_batch, int n_tail, float* out,
-                                cudaStream_t s) {
+                                cudaStream_t s, bool pdl) {
   const bool vec = (n_tail % 4 == 0) && (reinterpret_cast<uintptr_t>(in) % 16 == 0);
-  return vec ? launch_vec<4>(in, n_batch, n_tail, out, s)
-             : launch_vec<1>(in, n_batch, n_tail, out, s);
+  return vec ? launch_vec<4>(in, n_batch, n_tail, out, s, pdl)
+             : launch_vec<1>(in, n_batch, n_tail, out, s, pdl);
 }
 
 }  // namespace cfc
