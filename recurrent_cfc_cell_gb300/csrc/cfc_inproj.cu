@@ -8,8 +8,10 @@
 // have exactly that size; the recurrence reads each value (before the step that needs it)
 // and overwrites it with h, ff1, ff2, gate.  No extra memory is needed.
 //
-// CUDA-core fp32: a 64 x 64 output tile per CTA (256 threads, 4 x 4 each), k in chunks of 16
-// through shared memory.
+// CUDA-core fp32: a 64 x 64 output tile per CTA (256 threads, 4 rows x 4 consecutive gate
+// rows each), k in chunks of 64 through shared memory.  A chunk's global loads are all issued
+// before any is stored (one memory round trip per chunk; n_x <= 64 is one chunk), and each
+// thread writes its four consecutive outputs of a row as one 16-byte store when C % 4 == 0.
 #include "cfc_kernels.h"
 #include "cfc_launch.cuh"
 #include "cfc_ptx.cuh"
@@ -17,7 +19,8 @@
 namespace cfc {
 namespace {
 
-constexpr int kTR = 64, kTM = 64, kTK = 16;
+constexpr int kTR = 64, kTM = 64, kTK = 64;
+constexpr int kLoads = kTK * kTR / 256;  // elements of each operand tile per thread
 
 __global__ void __launch_bounds__(256) inproj_kernel(const float* __restrict__ u,
                                                       const float* __restrict__ W,
@@ -34,18 +37,25 @@ __global__ void __launch_bounds__(256) inproj_kernel(const float* __restrict__ u
   const int tr = tid >> 4, tm = tid & 15;
   float acc[4][4] = {};
   for (int k0 = 0; k0 < n_x; k0 += kTK) {
+    // Element e of a tile: row e / kTK, column e % kTK (consecutive threads walk k).
+    float ur[kLoads], wr[kLoads];
 #pragma unroll
-    for (int q = 0; q < (kTK * kTR) / 256; ++q) {
+    for (int q = 0; q < kLoads; ++q) {
       const int e = tid + q * 256;
-      const int rr = e / kTK, kk = e % kTK;  // consecutive threads walk k (coalesced rows)
-      const int r = r0 + rr, k = k0 + kk;
-      Us[kk][rr] = (r < BK && k < n_x) ? u[static_cast<size_t>(r) * n_x + k] : 0.f;
-      const int m = m0 + rr;
-      Ws[kk][rr] = (m < M && k < n_x) ? W[static_cast<size_t>(m) * n_in + k] : 0.f;
+      const int rr = e / kTK, kk = e % kTK;
+      const int r = r0 + rr, m = m0 + rr, k = k0 + kk;
+      ur[q] = (r < BK && k < n_x) ? __ldg(u + static_cast<size_t>(r) * n_x + k) : 0.f;
+      wr[q] = (m < M && k < n_x) ? __ldg(W + static_cast<size_t>(m) * n_in + k) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < kLoads; ++q) {
+      const int e = tid + q * 256;
+      Us[e % kTK][e / kTK] = ur[q];
+      Ws[e % kTK][e / kTK] = wr[q];
     }
     __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < kTK; ++kk) {
+    const int kn = min(kTK, n_x - k0);
+    for (int kk = 0; kk < kn; ++kk) {
       const float4 a = *reinterpret_cast<const float4*>(&Us[kk][tr * 4]);
       const float4 w = *reinterpret_cast<const float4*>(&Ws[kk][tm * 4]);
       const float av[4] = {a.x, a.y, a.z, a.w};
@@ -57,9 +67,27 @@ __global__ void __launch_bounds__(256) inproj_kernel(const float* __restrict__ u
     }
     __syncthreads();
   }
+  // Outputs m .. m + 3 of rows r: gate g = m / C goes to H (g = 0) or cache[.][g - 1].
+  const int mq = m0 + tm * 4;
+  if (mq >= M) return;
+  if ((C & 3) == 0) {  // the four outputs share a gate and a 16-byte aligned slot
+    const int g = mq / C, ch = mq - g * C;
+    const float4 bm = *reinterpret_cast<const float4*>(bias + mq);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = r0 + tr * 4 + i;
+      if (r >= BK) continue;
+      const float4 v = make_float4(acc[i][0] + bm.x, acc[i][1] + bm.y, acc[i][2] + bm.z,
+                                   acc[i][3] + bm.w);
+      float* dst = (g == 0) ? H + static_cast<size_t>(r) * C + ch
+                            : cache + (static_cast<size_t>(r) * 3 + (g - 1)) * C + ch;
+      *reinterpret_cast<float4*>(dst) = v;
+    }
+    return;
+  }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const int m = m0 + tm * 4 + j;
+    const int m = mq + j;
     if (m >= M) continue;
     const int g = m / C, ch = m - g * C;
     const float bm = bias[m];

@@ -38,6 +38,31 @@ def test_ragged_parity(shape):
     assert_parity(run_gpu(inp), oracle_ref(inp))
 
 
+@pytest.mark.parametrize("shape", [dict(B=32, K=64, n_x=48, C=128), dict(B=7, K=11, n_x=13, C=100),
+                                   dict(B=5, K=6, n_x=64, C=256)],
+                         ids=lambda s: "B{B}_K{K}_nx{n_x}_C{C}".format(**s))
+def test_two_stage_forward_matches_oracle(shape):
+    """The two stage entry points cfc_forward is made of, called one after the other: the
+    projection kernel, then the recurrence that reads X from H / cache."""
+    import torch
+
+    from recurrent_cfc_cell_gb300 import _lib, build
+    from recurrent_cfc_cell_gb300.step import to_device
+
+    build.build()
+    inp = inputs.make_inputs(inputs.custom(seed=23, **shape))
+    d = to_device(inp)
+    K, B, n_x = inp["u"].shape
+    C = inp["h0"].shape[1]
+    H = torch.full((K, B, C), float("nan"), device="cuda")
+    cache = torch.full((K, B, 3, C), float("nan"), device="cuda")
+    _lib.cfc_input_projection(d["u"], d["W"], d["b"], H, cache)
+    _lib.cfc_forward_recurrence(d["h0"], d["W"], d["ts"], H, cache)
+    torch.cuda.synchronize()
+    assert_parity({"H": H.cpu().numpy(), "cache": cache.cpu().numpy()}, oracle_ref(inp),
+                  keys=("H", "cache"))
+
+
 def test_graph_replay_parity():
     inp = inputs.make_inputs(inputs.CONFIGS[1])
     assert_parity(run_gpu(inp, graph=True), oracle_ref(inp))
