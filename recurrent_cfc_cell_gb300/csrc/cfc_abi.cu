@@ -85,7 +85,7 @@ int cluster_size_for(int C, int chan_per_cta) {
 
 int check_dims(int B, int K, int C, int n_x) {
   if (B <= 0 || K <= 0 || C <= 0 || n_x <= 0) return CFC_ERR_INVALID_DIM;
-  if (C > cfc::kChanPerCta * cfc::kMaxClusterSize) return CFC_ERR_INVALID_DIM;
+  if (C > cfc::kMaxChannels) return CFC_ERR_INVALID_DIM;
   if (n_x > cfc::kMaxInputs) return CFC_ERR_INVALID_DIM;
   const long long pre = 4LL * K * B * C;
   if (pre >= (1LL << 31)) return CFC_ERR_INVALID_DIM;
@@ -307,7 +307,7 @@ int cfc_backward_recurrence(const float* dH, const float* W, const float* ts,
   p.dH = dH; p.W = W; p.ts = ts; p.cache = cache; p.d_pre = d_pre; p.dh0 = dh0;
   p.status = st->status;
   p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
-  p.CS = cluster_size_for(C, cfc::kChanPerCta);
+  p.CS = cluster_size_for(C, cfc::kBwdChanPerCta);
   size_t smem = 0;
   int n_clusters = 0;
   rc = plan_rows(*st, 1, 0, p.CS, B, n_x, &p.R, &smem, &n_clusters);

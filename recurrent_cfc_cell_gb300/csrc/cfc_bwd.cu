@@ -15,23 +15,27 @@
 //   delta  <- W_h^T d_pre[t]      (W_h = the C recurrent columns of W);   dh0 = final delta.
 //
 // Layout and schedule (every step is warp-local; no CTA-wide barrier inside the K-loop):
-//   * a cluster of CS CTAs serves R batch rows; CTA `rank` owns channels [16*rank, 16*rank+16)
-//     and warp w owns channels 16*rank + 2w + {0, 1};
-//   * every CTA pushes its 64 new d_pre values (16 channels x 4 gates) to every CTA with
+//   * a cluster of CS CTAs serves R batch rows; CTA `rank` owns channels [32*rank, 32*rank+32)
+//     and warp w owns channels 32*rank + 4w + {0..3};
+//   * every CTA pushes its 128 new d_pre values (32 channels x 4 gates) to every CTA with
 //     st.async (one 16-byte push per channel and destination), so each CTA holds the whole
 //     d_pre[t] vector (4C values) after one mbarrier wait;
-//   * warp w keeps the two W_h^T columns of its channels in REGISTERS, lane l holding both
-//     columns over the l-th thirty-second of the 4C gathered rows (2*CS rows), so every d_pre
-//     value loaded from shared memory feeds two FMAs; a 5-shuffle butterfly gives delta for
-//     channel 0 in lanes 0-15 and channel 1 in lanes 16-31, and the same warp forms dh, the
-//     four d_pre values of each channel and the pushes.  The gathered vector is stored in
-//     thirty-two slices padded to an odd number of 16-byte chunks, so the vector loads of a
-//     quarter-warp hit distinct banks.  The summation order is fixed: bitwise reproducible;
+//   * warp w keeps the four W_h^T columns of its channels in REGISTERS, lane l holding them
+//     over the l-th thirty-second of the 4C gathered rows (4*CS rows), so every d_pre value
+//     loaded from shared memory feeds four FMAs; a 6-shuffle reduce-scatter leaves delta of
+//     channel cj in lanes 8cj .. 8cj+7, and the same warp forms dh, the four d_pre values of
+//     each channel and the pushes.  The gathered vector is stored in thirty-two slices padded
+//     to an odd number of 16-byte chunks, so the vector loads of a quarter-warp hit distinct
+//     banks.  The summation order is fixed: bitwise reproducible;
+//   * with 32 channels per CTA a cluster has C/32 CTAs: the 32x64x128 workload runs one CTA
+//     per SM (measured on GB300, CTAs that share an SM slow every step of the chain);
 //   * dH, ff1, ff2, gate and ts of step t-1 are loaded into registers during step t when the
 //     cluster serves at most four rows (the row count is then a compile-time parameter); for
-//     larger row groups they arrive two steps ahead through a cp.async ring (10 lanes of each
-//     warp copy, the warp reads after __syncwarp).  Either way no global-memory latency sits
-//     on the serial chain;
+//     larger row groups they arrive two steps ahead through a cp.async ring (5 lanes per
+//     channel copy, the warp reads after __syncwarp).  Either way no global-memory latency
+//     sits on the serial chain;
+//   * per-lane addresses are computed once; the K-loop advances pointers by a fixed stride and
+//     uses predicated loads, stores and st.async;
 //   * the W_h^T columns are read once, coalesced, into shared memory and from there into
 //     registers (a direct load would fetch one 32-byte sector per 4-byte value).
 #include "cfc_kernels.h"
@@ -45,13 +49,13 @@ constexpr int kWarps = kRecThreads / 32;
 constexpr int kPre = 3;      // prefetch ring depth (copies run two steps ahead)
 constexpr int kPreComp = 5;  // dH, ff1, ff2, gate, ts
 
-// Lanes 16*ci + c (c < 5) copy component c of this warp's channel ci for step t.
+// Lanes 8*cj + c (c < 5) copy component c of this warp's channel cj for step t.
 __device__ __forceinline__ void issue_pre(const BwdParams& p, float* pre, int t, int row0,
                                           int rank, int warp, int lane) {
   if (t < 0) return;
-  const int ci = lane >> 4, c = lane & 15;
+  const int cj = lane >> 3, c = lane & 7;
   if (c >= kPreComp) return;
-  const int ch = kChanPerCta * rank + 2 * warp + ci;
+  const int ch = kBwdChanPerCta * rank + 4 * warp + cj;
   if (ch >= p.C) return;
   for (int r = 0; r < p.R; ++r) {
     const int b = row0 + r;
@@ -60,16 +64,16 @@ __device__ __forceinline__ void issue_pre(const BwdParams& p, float* pre, int t,
     const float* src = (c == 0) ? p.dH + tb * p.C + ch
                      : (c == 4) ? p.ts + tb
                                 : p.cache + (tb * 3 + (c - 1)) * p.C + ch;
-    float* dst = pre + ((((t % kPre) * p.R + r) * kWarps + warp) * 2 + ci) * kPreComp + c;
+    float* dst = pre + ((((t % kPre) * p.R + r) * kWarps + warp) * 4 + cj) * kPreComp + c;
     cp_async_4(smem_addr(dst), src);
   }
 }
 
 template <int CS>
 struct BwdShape {
-  static constexpr int CHP = kChanPerCta * CS;  // padded channel count
-  static constexpr int NG = 4 * CHP;            // gathered d_pre values per row
-  static constexpr int RS = NG / 32;            // rows per lane (= 2 * CS)
+  static constexpr int CHP = kBwdChanPerCta * CS;  // padded channel count
+  static constexpr int NG = 4 * CHP;               // gathered d_pre values per row
+  static constexpr int RS = NG / 32;               // rows per lane (= 4 * CS)
   // Slice pitch: vector loads of 8 consecutive lanes must cover distinct banks.
   static constexpr int RSP = (RS >= 4 && (RS / 4) % 2 == 0) ? RS + 4 : RS;
   static constexpr int GROW = 32 * RSP;         // gathered row in shared memory
@@ -81,38 +85,29 @@ __device__ __forceinline__ int gpos(int gidx) {
   return (gidx / S::RS) * S::RSP + (gidx % S::RS);
 }
 
-// delta for both channels of this warp from this lane's slice of the gathered d_pre vector;
-// lanes 0-15 return channel 0, lanes 16-31 channel 1.
+// delta for the four channels of this warp from this lane's slice of the gathered d_pre
+// vector; lanes 8cj .. 8cj+7 return channel cj.
 template <int RS>
-__device__ __forceinline__ float gathered_delta(const float (&wt)[2][RS], const float* dvp,
+__device__ __forceinline__ float gathered_delta(const float (&wt)[4][RS], const float* dvp,
                                                 int lane) {
   float dv[RS];
-  if constexpr (RS % 4 == 0) {
 #pragma unroll
-    for (int k = 0; k < RS; k += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(dvp + k);
-      dv[k] = v.x; dv[k + 1] = v.y; dv[k + 2] = v.z; dv[k + 3] = v.w;
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < RS; k += 2) {
-      const float2 v = *reinterpret_cast<const float2*>(dvp + k);
-      dv[k] = v.x; dv[k + 1] = v.y;
-    }
+  for (int k = 0; k < RS; k += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(dvp + k);
+    dv[k] = v.x; dv[k + 1] = v.y; dv[k + 2] = v.z; dv[k + 3] = v.w;
   }
-  float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int k = 0; k < RS; k += 2) {
-    a0 = fmaf(wt[0][k], dv[k], a0);
-    a1 = fmaf(wt[1][k], dv[k], a1);
-    c0 = fmaf(wt[0][k + 1], dv[k + 1], c0);
-    c1 = fmaf(wt[1][k + 1], dv[k + 1], c1);
-  }
-  a0 += c0;
-  a1 += c1;
-  const bool hi = lane & 16;
-  float d = (hi ? a1 : a0) + __shfl_xor_sync(0xffffffffu, hi ? a0 : a1, 16);
-  d += __shfl_xor_sync(0xffffffffu, d, 8);
+  for (int k = 0; k < RS; ++k)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) a[c] = fmaf(wt[c][k], dv[k], a[c]);
+  // Reduce-scatter over the 32 lanes: xor 16 keeps channels {0,1} / {2,3}, xor 8 one channel,
+  // then the eight lanes of a channel sum.
+  const bool b16 = lane & 16, b8 = lane & 8;
+  const float k0 = b16 ? a[2] : a[0], k1 = b16 ? a[3] : a[1];
+  const float s0 = k0 + __shfl_xor_sync(0xffffffffu, b16 ? a[0] : a[2], 16);
+  const float s1 = k1 + __shfl_xor_sync(0xffffffffu, b16 ? a[1] : a[3], 16);
+  float d = (b8 ? s1 : s0) + __shfl_xor_sync(0xffffffffu, b8 ? s0 : s1, 8);
   d += __shfl_xor_sync(0xffffffffu, d, 4);
   d += __shfl_xor_sync(0xffffffffu, d, 2);
   d += __shfl_xor_sync(0xffffffffu, d, 1);
@@ -139,13 +134,13 @@ __device__ __forceinline__ void load_step_regs(const float* dHp, const float* cp
 // RT = 1, 2, 4: rows per cluster fixed at compile time, inputs prefetched into registers.
 // RT = 0: p.R rows (any count), inputs through the cp.async ring.
 template <int CS, int RT>
-__global__ void __launch_bounds__(kRecThreads, CS >= 16 ? 1 : 2) cfc_bwd_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kRecThreads, CS >= 4 ? 1 : 2) cfc_bwd_kernel(const BwdParams p) {
   using S = BwdShape<CS>;
   extern __shared__ __align__(16) float smem[];
   const int R = RT > 0 ? RT : p.R;
   float* dg = smem;                      // [2][R][GROW]  d_pre[t+1] for step t in dg[t & 1]
-  float* pre = dg + 2 * R * S::GROW;     // ring path: [kPre][R][8 warps][2][5]
-  const int pre_floats = RT > 0 ? 0 : kPre * R * kWarps * 2 * kPreComp;
+  float* pre = dg + 2 * R * S::GROW;     // ring path: [kPre][R][8 warps][4][5]
+  const int pre_floats = RT > 0 ? 0 : kPre * R * kWarps * 4 * kPreComp;
   uint64_t* bars = reinterpret_cast<uint64_t*>(pre + pre_floats);
   grid_dep_launch_dependents();
 
@@ -156,24 +151,24 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 16 ? 1 : 2) cfc_bwd_kernel(
   const int row0 = static_cast<int>(cluster_id_x()) * R;
   const int B = p.B, K = p.K, C = p.C, n_x = p.n_x, n_in = p.n_in;
 
-  // W_h^T columns of this warp's two channels over gathered rows [lane*RS, lane*RS + RS).
-  // Gathered row q*64 + 4i + g is W row g*C + 16q + i.
-  // Staged through shared memory as [NG][17] (the whole smem area is free before the loop):
-  // consecutive threads read consecutive channels of one W row.
-  float wt[2][S::RS];
+  // W_h^T columns of this warp's four channels over gathered rows [lane*RS, lane*RS + RS).
+  // Gathered row q*128 + 4i + g is W row g*C + 32q + i.  Staged through shared memory as
+  // [NG][33] (the whole smem area is free before the loop): consecutive threads read
+  // consecutive channels of one W row, a chunk of loads in flight before any store.
+  float wt[4][S::RS];
   {
-    // Chunks of loads are issued before their stores, so each chunk costs one round trip.
     float* wtmp = smem;
-    constexpr int kPerThread = S::NG * kChanPerCta / kRecThreads;
+    constexpr int kPitch = kBwdChanPerCta + 1;
+    constexpr int kPerThread = S::NG * kBwdChanPerCta / kRecThreads;
     constexpr int kChunk = kPerThread < 32 ? kPerThread : 32;
     for (int i0 = 0; i0 < kPerThread; i0 += kChunk) {
       float v[kChunk];
 #pragma unroll
       for (int i = 0; i < kChunk; ++i) {
         const int e = (i0 + i) * kRecThreads + tid;
-        const int gidx = e >> 4, jl = e & 15;
-        const int chr = kChanPerCta * (gidx >> 6) + ((gidx & 63) >> 2);
-        const int j = kChanPerCta * rank + jl;
+        const int gidx = e / kBwdChanPerCta, jl = e % kBwdChanPerCta;
+        const int chr = kBwdChanPerCta * (gidx / 128) + (gidx % 128) / 4;
+        const int j = kBwdChanPerCta * rank + jl;
         v[i] = (chr < C && j < C)
                    ? __ldg(p.W + (static_cast<size_t>(gidx & 3) * C + chr) * n_in + n_x + j)
                    : 0.f;
@@ -181,25 +176,25 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 16 ? 1 : 2) cfc_bwd_kernel(
 #pragma unroll
       for (int i = 0; i < kChunk; ++i) {
         const int e = (i0 + i) * kRecThreads + tid;
-        wtmp[(e >> 4) * (kChanPerCta + 1) + (e & 15)] = v[i];
+        wtmp[(e / kBwdChanPerCta) * kPitch + e % kBwdChanPerCta] = v[i];
       }
     }
     __syncthreads();
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc)
+    for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
       for (int k = 0; k < S::RS; ++k)
-        wt[cc][k] = wtmp[(lane * S::RS + k) * (kChanPerCta + 1) + 2 * warp + cc];
+        wt[cc][k] = wtmp[(lane * S::RS + k) * kPitch + 4 * warp + cc];
     __syncthreads();
   }
-  const int ci = lane >> 4;        // channel of this half-warp
-  const int gq = (lane >> 2) & 3;  // gate this lane's d_pre belongs to
-  const int q = lane & 15;         // destination CTA of this lane's push
-  const int ch = kChanPerCta * rank + 2 * warp + ci;
-  const int half = lane & 16;
+  const int cj = lane >> 3;        // channel of this 8-lane group
+  const int gq = (lane >> 1) & 3;  // gate this lane's d_pre belongs to
+  const int q = lane & 7;          // destination CTA of this lane's push
+  const int ch = kBwdChanPerCta * rank + 4 * warp + cj;
+  const int base = lane & 24;
 
   const uint32_t bar0 = smem_addr(&bars[0]);  // bars[s] lives at bar0 + 8 s
-  const uint32_t tx_bytes = static_cast<uint32_t>(CS * R * kRowsPerCta * 4);
+  const uint32_t tx_bytes = static_cast<uint32_t>(CS * R * 4 * kBwdChanPerCta * 4);
   if (tid == 0) {
     mbar_init(bar0, 1);
     mbar_init(bar0 + 8u, 1);
@@ -226,12 +221,12 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 16 ? 1 : 2) cfc_bwd_kernel(
   bool rok[RR];
 #pragma unroll
   for (int r = 0; r < RR; ++r) rok[r] = row0 + r < B;
-  const bool stores = (lane & 3) == 0 && ch < C;  // one lane per (channel, gate) stores d_pre
-  // The four d_pre of channel ci go to slot rank*64 + 4*(2w + ci) of every CTA's gathered
+  const bool stores = (lane & 1) == 0 && ch < C;  // one lane per (channel, gate) stores d_pre
+  // The four d_pre of channel cj go to slot rank*128 + 4*(4w + cj) of every CTA's gathered
   // vector; remote addresses of buffer 0 / row 0 (buffer d, row r: (d R + r) GROW floats on).
   const bool pushes = q < CS;
   const uint32_t push0 =
-      pushes ? map_to_rank(smem_addr(dg + gpos<CS>(rank * kRowsPerCta + 4 * (2 * warp + ci))), q)
+      pushes ? map_to_rank(smem_addr(dg + gpos<CS>(rank * 4 * kBwdChanPerCta + 4 * (4 * warp + cj))), q)
              : 0u;
   const uint32_t rbar0 = pushes ? map_to_rank(bar0, q) : 0u;
 
@@ -282,7 +277,7 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 16 ? 1 : 2) cfc_bwd_kernel(
       __syncwarp();
     }
 
-    const float* pre_t = pre + ((t % kPre) * R * kWarps + warp) * 2 * kPreComp + ci * kPreComp;
+    const float* pre_t = pre + ((t % kPre) * R * kWarps + warp) * 4 * kPreComp + cj * kPreComp;
     const uint32_t pdst = push0 + static_cast<uint32_t>((s ^ 1) * R * S::GROW * 4);
     const uint32_t pbar = rbar0 + 8u * (s ^ 1);
 #pragma unroll(RT > 0 ? RT : 1)
@@ -294,23 +289,23 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 16 ? 1 : 2) cfc_bwd_kernel(
       float v[kPreComp];  // dH, ff1, ff2, gate, ts of (t, b, ch)
 #pragma unroll
       for (int c = 0; c < kPreComp; ++c)
-        v[c] = RT > 0 ? cur[RT > 0 ? r : 0][c] : pre_t[r * kWarps * 2 * kPreComp + c];
+        v[c] = RT > 0 ? cur[RT > 0 ? r : 0][c] : pre_t[r * kWarps * 4 * kPreComp + c];
       const float dh = v[0] + delta;
       const float f1 = v[1], f2 = v[2], g = v[3];
       const float ds = dh * (f2 - f1) * g * (1.f - g);
-      // This lane's gate, by selects (the four lanes of a gate group differ from their
-      // neighbours, so a branch here would split the warp four ways).
+      // This lane's gate, by selects (neighbouring lane pairs hold different gates, so a
+      // branch here would split the warp four ways).
       const float p0 = dh * (1.f - g) * (1.f - f1 * f1);
       const float p1 = dh * g * (1.f - f2 * f2);
       const float p2 = ds * v[4];
       const float sel = (gq == 0) ? p0 : (gq == 1) ? p1 : (gq == 2) ? p2 : ds;
       const float dpv = valid ? sel : 0.f;
       if (stores && valid) dpp[static_cast<size_t>(r) * 4 * C] = dpv;
-      // The four gates of channel ci -> one 16-byte push to every CTA of the cluster.
-      const float d0 = __shfl_sync(0xffffffffu, dpv, half + 0);
-      const float d1 = __shfl_sync(0xffffffffu, dpv, half + 4);
-      const float d2 = __shfl_sync(0xffffffffu, dpv, half + 8);
-      const float d3 = __shfl_sync(0xffffffffu, dpv, half + 12);
+      // The four gates of channel cj -> one 16-byte push to every CTA of the cluster.
+      const float d0 = __shfl_sync(0xffffffffu, dpv, base + 0);
+      const float d1 = __shfl_sync(0xffffffffu, dpv, base + 2);
+      const float d2 = __shfl_sync(0xffffffffu, dpv, base + 4);
+      const float d3 = __shfl_sync(0xffffffffu, dpv, base + 6);
       st_async_v4_if(pushes, pdst + static_cast<uint32_t>(r * S::GROW * 4), d0, d1, d2, d3, pbar);
     }
     dpp -= 4 * bc;
@@ -332,7 +327,7 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 16 ? 1 : 2) cfc_bwd_kernel(
         const float delta =
             gathered_delta<S::RS>(wt, dg + (1 * R + r) * S::GROW + lane * S::RSP, lane);
         const int b = row0 + r;
-        if (q == 0 && b < B && ch < C) p.dh0[static_cast<size_t>(b) * C + ch] = delta;
+        if ((lane & 7) == 0 && b < B && ch < C) p.dh0[static_cast<size_t>(b) * C + ch] = delta;
       }
     }
   }
@@ -411,12 +406,12 @@ cudaError_t launch_cs(const BwdParams& p, int n_clusters, size_t smem, cudaStrea
 }  // namespace
 
 size_t bwd_smem_bytes(int R, int CS) {
-  const size_t RS = 2ull * CS;
-  const size_t GROW = 32 * ((RS >= 4 && (RS / 4) % 2 == 0) ? RS + 4 : RS);
-  const size_t ring = bwd_variant(R) > 0 ? 0 : 1ull * kPre * R * kWarps * 2 * kPreComp;
+  const size_t RS = 4ull * CS;
+  const size_t GROW = 32 * (((RS / 4) % 2 == 0) ? RS + 4 : RS);
+  const size_t ring = bwd_variant(R) > 0 ? 0 : 1ull * kPre * R * kWarps * 4 * kPreComp;
   const size_t loop = sizeof(float) * (2ull * R * GROW + ring) + 2 * sizeof(uint64_t) + 16;
-  // The prologue stages the CTA's W_h^T block ([4 * 16 CS][17] floats) in the same area.
-  const size_t stage = sizeof(float) * 4ull * kChanPerCta * CS * (kChanPerCta + 1);
+  // The prologue stages the CTA's W_h^T block ([4 * 32 CS][33] floats) in the same area.
+  const size_t stage = sizeof(float) * 4ull * kBwdChanPerCta * CS * (kBwdChanPerCta + 1);
   return loop > stage ? loop : stage;
 }
 
@@ -426,7 +421,6 @@ cudaError_t bwd_prepare(int CS, int R, size_t smem, int* max_active) {
     case 2: return prepare_cs<2>(R, smem, max_active);
     case 4: return prepare_cs<4>(R, smem, max_active);
     case 8: return prepare_cs<8>(R, smem, max_active);
-    case 16: return prepare_cs<16>(R, smem, max_active);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -438,7 +432,6 @@ cudaError_t bwd_launch(const BwdParams& p, int n_clusters, size_t smem, cudaStre
     case 2: return launch_cs<2>(p, n_clusters, smem, s, pdl);
     case 4: return launch_cs<4>(p, n_clusters, smem, s, pdl);
     case 8: return launch_cs<8>(p, n_clusters, smem, s, pdl);
-    case 16: return launch_cs<16>(p, n_clusters, smem, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

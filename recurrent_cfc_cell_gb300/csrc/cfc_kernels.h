@@ -8,11 +8,11 @@ namespace cfc {
 
 // Channel tiling of the two recurrence kernels: every CTA of a cluster owns a fixed number of
 // hidden channels (all four gates of each), so a cluster of CS CTAs covers that many x CS >= C.
-constexpr int kChanPerCta = 16;     // backward recurrence
 constexpr int kFwdChanPerCta = 32;  // forward recurrence: a cluster of CS CTAs covers 32*CS
-constexpr int kRowsPerCta = 4 * kChanPerCta;  // W rows held by one CTA (gate-minor order)
+constexpr int kBwdChanPerCta = 32;  // backward recurrence, likewise
 constexpr int kRecThreads = 256;
-constexpr int kMaxClusterSize = 16;
+constexpr int kMaxClusterSize = 16;  // reduce_axis0 (non-portable clusters up to 16)
+constexpr int kMaxChannels = 256;    // largest C: clusters of 8 CTAs x 32 channels
 constexpr int kMaxInputs = 512;  // largest n_x (W_u rows of a CTA live in shared memory)
 constexpr int kMaxRowsPerCluster = 32;  // backward recurrence
 constexpr int kMaxFwdRows = 4;         // forward recurrence (rows are a template parameter)
