@@ -158,9 +158,10 @@ BwdLayout bwd_layout(int B, int K, int C, int n_x) {
   L.S_simt = cfc::dw_simt_splits(static_cast<int>(BK));
   L.tc = cfc::dw_tc_plan(B, K, C, n_x);
   L.tu = cfc::du_tc_plan(B, K, C, n_x);
-  const int S = L.S_simt > L.tc.splits ? L.S_simt : L.tc.splits;
   // The dW partials are consumed before du runs, so du's partials reuse the same area.
-  size_t part = static_cast<size_t>(S) * 4 * C * (n_x + C);
+  size_t part = static_cast<size_t>(L.S_simt) * 4 * C * (n_x + C);
+  const size_t ptc = static_cast<size_t>(L.tc.splits) * 4 * C * cfc::dw_tc_pitch(n_x + C);
+  if (ptc > part) part = ptc;
   if (L.tu.splits > 1) {
     const size_t pu = static_cast<size_t>(L.tu.splits) * BK * n_x;
     if (pu > part) part = pu;
@@ -279,9 +280,10 @@ int cfc_step_launches(int B, int K, int C, int n_x, int dw_mode, int with_du, in
   if (rc != CFC_OK) return rc;
   if (dw_mode != CFC_DW_ACCURATE && dw_mode != CFC_DW_SIMT_FP32) return CFC_ERR_INVALID_ARG;
   if (!launches) return CFC_ERR_NULL_PTR;
-  // forward: projection + recurrence; backward: recurrence, dW contraction + its reduction,
-  // db reduction, and du (plus its reduction when the tensor-core plan splits it).
-  int n = 2 + 1 + 2 + 1;
+  // forward: projection + recurrence; backward: recurrence, dW contraction + its reduction
+  // (which also yields db with the tensor cores; a separate db reduction otherwise), and du
+  // (plus its reduction when the tensor-core plan splits it).
+  int n = 2 + 1 + 2 + (dw_mode == CFC_DW_ACCURATE ? 0 : 1);
   if (with_du) {
     n += 1;
     if (dw_mode == CFC_DW_ACCURATE && bwd_layout(B, K, C, n_x).tu.splits > 1) n += 1;
@@ -354,9 +356,17 @@ int weight_grad(const float* d_pre, const float* u, const float* h0, const float
                  CFC_ERR_LAUNCH_FAILED);
   }
   if (rc != CFC_OK) return rc;
-  rc = cuda_rc(cfc::reduce_axis0_launch(partial, S, M * N, dW, s, true), CFC_ERR_LAUNCH_FAILED);
-  if (rc != CFC_OK) return rc;
-  rc = cuda_rc(cfc::reduce_axis0_launch(d_pre, BK, M, db, s, true), CFC_ERR_LAUNCH_FAILED);
+  if (dw_mode == CFC_DW_SIMT_FP32) {
+    rc = cuda_rc(cfc::reduce_axis0_launch(partial, S, M * N, dW, s, true),
+                 CFC_ERR_LAUNCH_FAILED);
+    if (rc != CFC_OK) return rc;
+    rc = cuda_rc(cfc::reduce_axis0_launch(d_pre, BK, M, db, s, true), CFC_ERR_LAUNCH_FAILED);
+  } else {
+    // One merge for both: the partial rows carry the all-ones column, i.e. db.
+    const int pitch = cfc::dw_tc_pitch(N);
+    rc = cuda_rc(cfc::reduce_axis0_rows_launch(partial, S, M * pitch, pitch, N, dW, db, s, true),
+                 CFC_ERR_LAUNCH_FAILED);
+  }
   if (rc != CFC_OK) return rc;
   if (du) {
     if (dw_mode == CFC_DW_SIMT_FP32) {

@@ -22,6 +22,10 @@
 // about one per SM the reduction index is split, each split writing a partial block, and
 // reduce_axis0 sums the splits in order (bitwise reproducible; the split depends only on the
 // sizes).
+//
+// The bias gradient comes out of the same contraction: z gets one more column, all ones, so
+// the weight-gradient partial row m ends with sum_r d_pre[r][m] = db[m] (rows padded to
+// dw_tc_pitch(n_in) columns; the merge routes that column to db).
 #include <cuda_bf16.h>
 
 #include "cfc_kernels.h"
@@ -76,8 +80,9 @@ __device__ __forceinline__ void store_split_chunk(uint8_t* hi_tile, uint8_t* lo_
                  pack_bf16x2(l[6], l[7]));
 }
 
+// z[r][n] for n < n_in, 1 at n == n_in (the bias-gradient column), 0 beyond.
 __device__ __forceinline__ float4 z_quad(const TcParams& p, int r, int n) {
-  if (n >= p.n_in) return make_float4(0.f, 0.f, 0.f, 0.f);
+  if (n >= p.n_in) return make_float4(n == p.n_in ? 1.f : 0.f, 0.f, 0.f, 0.f);
   if (n < p.n_x) return __ldg(reinterpret_cast<const float4*>(p.u + static_cast<size_t>(r) * p.n_x + n));
   const int j = n - p.n_x;
   const float* src = (r >= p.B) ? p.H + static_cast<size_t>(r - p.B) * p.C + j
@@ -86,7 +91,7 @@ __device__ __forceinline__ float4 z_quad(const TcParams& p, int r, int n) {
 }
 
 __device__ __forceinline__ float z_at(const TcParams& p, int r, int n) {
-  if (n >= p.n_in) return 0.f;
+  if (n >= p.n_in) return n == p.n_in ? 1.f : 0.f;
   if (n < p.n_x) return __ldg(p.u + static_cast<size_t>(r) * p.n_x + n);
   const int j = n - p.n_x;
   return (r >= p.B) ? __ldg(p.H + static_cast<size_t>(r - p.B) * p.C + j)
@@ -352,7 +357,9 @@ TcPlan tc_plan(int rows, int cols, int red, bool split) {
 
 }  // namespace
 
-TcPlan dw_tc_plan(int B, int K, int C, int n_x) { return tc_plan(4 * C, n_x + C, B * K, true); }
+TcPlan dw_tc_plan(int B, int K, int C, int n_x) {
+  return tc_plan(4 * C, dw_tc_pitch(n_x + C), B * K, true);
+}
 TcPlan du_tc_plan(int B, int K, int C, int n_x) { return tc_plan(B * K, n_x, 4 * C, true); }
 
 cudaError_t tc_prepare(int max_smem) {
@@ -381,7 +388,7 @@ cudaError_t dw_tc_launch(const TcPlan& pl, const float* d_pre, const float* u, c
                          int* status, cudaStream_t s, bool pdl) {
   TcParams p = make_params(pl, d_pre, B, K, C, n_x, status);
   p.u = u; p.H = H; p.h0 = h0; p.out = partial;
-  p.rows = 4 * C; p.cols = n_x + C; p.red = B * K;
+  p.rows = 4 * C; p.cols = dw_tc_pitch(n_x + C); p.red = B * K;
   LaunchCfg c;
   c.grid = dim3(pl.m_tiles * pl.n_tiles, pl.splits, 1);
   c.block = dim3(kTcThreads, 1, 1);

@@ -91,5 +91,13 @@ cudaError_t du_simt_launch(const float* d_pre, const float* W, int BK, int C, in
 cudaError_t reduce_axis0_prepare();
 cudaError_t reduce_axis0_launch(const float* in, int n_batch, int n_tail, float* out,
                                 cudaStream_t s, bool pdl);
+// The same sum over a tail of rows of `pitch` values: columns < ncol of each row go to
+// out[row][ncol], column ncol to out2[row], the rest (padding) is dropped.
+cudaError_t reduce_axis0_rows_launch(const float* in, int n_batch, int n_tail, int pitch,
+                                     int ncol, float* out, float* out2, cudaStream_t s,
+                                     bool pdl);
+// Row pitch of the tensor-core weight-gradient partials: the n_in columns of z, the all-ones
+// column that yields db, padded to a multiple of 4.
+inline int dw_tc_pitch(int n_in) { return (n_in + 1 + 3) & ~3; }
 
 }  // namespace cfc

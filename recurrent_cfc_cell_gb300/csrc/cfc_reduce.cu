@@ -21,10 +21,28 @@ namespace {
 constexpr int kRowLanes = 8;
 constexpr int kColLanes = 32;
 
+// Where sum n goes: out[n], or -- for a tail that is rows of `pitch` values (pitch > 0) --
+// columns < ncol of row n / pitch to out[row * ncol + col], column ncol to out2[row], and the
+// rest of the row (padding) nowhere.
+struct OutMap {
+  float* out;
+  float* out2;
+  int pitch, ncol;
+};
+
+__device__ __forceinline__ void put(const OutMap& o, int n, float v) {
+  if (o.pitch == 0) {
+    o.out[n] = v;
+    return;
+  }
+  const int row = n / o.pitch, col = n - row * o.pitch;
+  if (col < o.ncol) o.out[static_cast<size_t>(row) * o.ncol + col] = v;
+  else if (col == o.ncol) o.out2[row] = v;
+}
+
 template <int VEC>
 __global__ void __launch_bounds__(kRowLanes * kColLanes) reduce_axis0_kernel(
-    const float* __restrict__ in, int n_batch, int n_tail, int rows_per_cta,
-    float* __restrict__ out) {
+    const float* __restrict__ in, int n_batch, int n_tail, int rows_per_cta, OutMap o) {
   constexpr int TC = kColLanes * VEC;
   __shared__ __align__(16) float part[kRowLanes][TC];
   __shared__ __align__(16) float cta_sum[TC];
@@ -85,7 +103,7 @@ __global__ void __launch_bounds__(kRowLanes * kColLanes) reduce_axis0_kernel(
     __syncthreads();
     for (int c = tid; c < TC; c += kRowLanes * kColLanes) {
       const int n = blockIdx.x * TC + c;
-      if (n < n_tail) out[n] = cta_sum[c];
+      if (n < n_tail) put(o, n, cta_sum[c]);
     }
     return;
   }
@@ -96,7 +114,7 @@ __global__ void __launch_bounds__(kRowLanes * kColLanes) reduce_axis0_kernel(
       float sacc = cta_sum[c];
       for (int qq = 1; qq < CZ; ++qq) sacc += ld_shared_cluster_f32(map_to_rank(a, qq));
       const int n = blockIdx.x * TC + c;
-      if (n < n_tail) out[n] = sacc;
+      if (n < n_tail) put(o, n, sacc);
     }
   }
   cluster_sync_all();
@@ -110,7 +128,7 @@ int choose_cz(int n_batch) {
 }
 
 template <int VEC>
-cudaError_t launch_vec(const float* in, int n_batch, int n_tail, float* out, cudaStream_t s,
+cudaError_t launch_vec(const float* in, int n_batch, int n_tail, const OutMap& o, cudaStream_t s,
                        bool pdl) {
   constexpr int TC = kColLanes * VEC;
   const int cz = choose_cz(n_batch);
@@ -121,7 +139,7 @@ cudaError_t launch_vec(const float* in, int n_batch, int n_tail, float* out, cud
   c.stream = s;
   c.pdl = pdl;
   c.cluster = dim3(1, cz, 1);
-  return launch(c, reduce_axis0_kernel<VEC>, in, n_batch, n_tail, rows_per_cta, out);
+  return launch(c, reduce_axis0_kernel<VEC>, in, n_batch, n_tail, rows_per_cta, o);
 }
 
 }  // namespace
@@ -136,9 +154,16 @@ cudaError_t reduce_axis0_prepare() {
 
 cudaError_t reduce_axis0_launch(const float* in, int n_batch, int n_tail, float* out,
                                 cudaStream_t s, bool pdl) {
+  return reduce_axis0_rows_launch(in, n_batch, n_tail, 0, 0, out, nullptr, s, pdl);
+}
+
+cudaError_t reduce_axis0_rows_launch(const float* in, int n_batch, int n_tail, int pitch,
+                                     int ncol, float* out, float* out2, cudaStream_t s,
+                                     bool pdl) {
+  const OutMap o{out, out2, pitch, ncol};
   const bool vec = (n_tail % 4 == 0) && (reinterpret_cast<uintptr_t>(in) % 16 == 0);
-  return vec ? launch_vec<4>(in, n_batch, n_tail, out, s, pdl)
-             : launch_vec<1>(in, n_batch, n_tail, out, s, pdl);
+  return vec ? launch_vec<4>(in, n_batch, n_tail, o, s, pdl)
+             : launch_vec<1>(in, n_batch, n_tail, o, s, pdl);
 }
 
 }  // namespace cfc
