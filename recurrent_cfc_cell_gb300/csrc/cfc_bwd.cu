@@ -151,62 +151,12 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 4 ? 1 : 2) cfc_bwd_kernel(c
   const int row0 = static_cast<int>(cluster_id_x()) * R;
   const int B = p.B, K = p.K, C = p.C, n_x = p.n_x, n_in = p.n_in;
 
-  // W_h^T columns of this warp's four channels over gathered rows [lane*RS, lane*RS + RS).
-  // Gathered row q*128 + 4i + g is W row g*C + 32q + i.  Staged through shared memory as
-  // [NG][33] (the whole smem area is free before the loop): consecutive threads read
-  // consecutive channels of one W row, a chunk of loads in flight before any store.
-  float wt[4][S::RS];
-  {
-    float* wtmp = smem;
-    constexpr int kPitch = kBwdChanPerCta + 1;
-    constexpr int kPerThread = S::NG * kBwdChanPerCta / kRecThreads;
-    constexpr int kChunk = kPerThread < 32 ? kPerThread : 32;
-    for (int i0 = 0; i0 < kPerThread; i0 += kChunk) {
-      float v[kChunk];
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        const int e = (i0 + i) * kRecThreads + tid;
-        const int gidx = e / kBwdChanPerCta, jl = e % kBwdChanPerCta;
-        const int chr = kBwdChanPerCta * (gidx / 128) + (gidx % 128) / 4;
-        const int j = kBwdChanPerCta * rank + jl;
-        v[i] = (chr < C && j < C)
-                   ? __ldg(p.W + (static_cast<size_t>(gidx & 3) * C + chr) * n_in + n_x + j)
-                   : 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        const int e = (i0 + i) * kRecThreads + tid;
-        wtmp[(e / kBwdChanPerCta) * kPitch + e % kBwdChanPerCta] = v[i];
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-      for (int k = 0; k < S::RS; ++k)
-        wt[cc][k] = wtmp[(lane * S::RS + k) * kPitch + 4 * warp + cc];
-    __syncthreads();
-  }
   const int cj = lane >> 3;        // channel of this 8-lane group
   const int gq = (lane >> 1) & 3;  // gate this lane's d_pre belongs to
   const int q = lane & 7;          // destination CTA of this lane's push
   const int ch = kBwdChanPerCta * rank + 4 * warp + cj;
   const int base = lane & 24;
 
-  const uint32_t bar0 = smem_addr(&bars[0]);  // bars[s] lives at bar0 + 8 s
-  const uint32_t tx_bytes = static_cast<uint32_t>(CS * R * 4 * kBwdChanPerCta * 4);
-  if (tid == 0) {
-    mbar_init(bar0, 1);
-    mbar_init(bar0 + 8u, 1);
-    fence_mbar_init_cluster();
-  }
-  for (int e = tid; e < 2 * R * S::GROW; e += kRecThreads) dg[e] = 0.f;
-  // Consumer c (the step that reads d_pre[c+1]; -1 is the dh0 epilogue) uses bars[c & 1].
-  // Consumers run c = K-2 .. -1; arm the first two.
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar0 + 8u * ((K - 2) & 1), tx_bytes);
-    if (K >= 2) mbar_arrive_expect_tx(bar0 + 8u * ((K - 3) & 1), tx_bytes);
-  }
   // Per-lane addresses, computed once: the K-loop only moves pointers by a fixed stride per
   // step and issues predicated loads and stores (no index arithmetic or divergent branches on
   // the serial chain).  Pointers address row row0 of step t.
@@ -222,6 +172,71 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 4 ? 1 : 2) cfc_bwd_kernel(c
 #pragma unroll
   for (int r = 0; r < RR; ++r) rok[r] = row0 + r < B;
   const bool stores = (lane & 1) == 0 && ch < C;  // one lane per (channel, gate) stores d_pre
+
+  // W_h^T columns of this warp's four channels over gathered rows [lane*RS, lane*RS + RS).
+  // Gathered row q*128 + 4i + g is W row g*C + 32q + i.  Staged through shared memory as
+  // [NG][33] (the whole smem area is free before the loop): consecutive threads read
+  // consecutive channels of one W row, a chunk of loads in flight before any store.
+  float wt[4][S::RS];
+  float cur[RR][kPreComp];  // register path: inputs of the current step
+  {
+    float* wtmp = smem;
+    constexpr int kPitch = kBwdChanPerCta + 1;
+    constexpr int kPerThread = S::NG * kBwdChanPerCta / kRecThreads;
+    constexpr int kChunk = kPerThread < 64 ? kPerThread : 64;
+    for (int i0 = 0; i0 < kPerThread; i0 += kChunk) {
+      float v[kChunk];
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        const int e = (i0 + i) * kRecThreads + tid;
+        const int gidx = e / kBwdChanPerCta, jl = e % kBwdChanPerCta;
+        const int chr = kBwdChanPerCta * (gidx / 128) + (gidx % 128) / 4;
+        const int j = kBwdChanPerCta * rank + jl;
+        v[i] = (chr < C && j < C)
+                   ? __ldg(p.W + (static_cast<size_t>(gidx & 3) * C + chr) * n_in + n_x + j)
+                   : 0.f;
+      }
+      if constexpr (RT > 0) {
+        if (i0 == 0) {
+          // dH and the forward cache may come from the previous kernel: wait for it (a no-op
+          // unless this launch is a dependent one), then start the step K-1 loads, in flight
+          // together with the first chunk of W_h^T.
+          grid_dep_wait();
+          load_step_regs<RR>(dHp, cp, tsp, C, rok, cur);
+          dHp -= bc;
+          cp -= 3 * bc;
+          tsp -= B;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        const int e = (i0 + i) * kRecThreads + tid;
+        wtmp[(e / kBwdChanPerCta) * kPitch + e % kBwdChanPerCta] = v[i];
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+      for (int k = 0; k < S::RS; ++k)
+        wt[cc][k] = wtmp[(lane * S::RS + k) * kPitch + 4 * warp + cc];
+    __syncthreads();
+  }
+
+  const uint32_t bar0 = smem_addr(&bars[0]);  // bars[s] lives at bar0 + 8 s
+  const uint32_t tx_bytes = static_cast<uint32_t>(CS * R * 4 * kBwdChanPerCta * 4);
+  if (tid == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar0 + 8u, 1);
+    fence_mbar_init_cluster();
+  }
+  for (int e = tid; e < 2 * R * S::GROW; e += kRecThreads) dg[e] = 0.f;
+  // Consumer c (the step that reads d_pre[c+1]; -1 is the dh0 epilogue) uses bars[c & 1].
+  // Consumers run c = K-2 .. -1; arm the first two.
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar0 + 8u * ((K - 2) & 1), tx_bytes);
+    if (K >= 2) mbar_arrive_expect_tx(bar0 + 8u * ((K - 3) & 1), tx_bytes);
+  }
   // The four d_pre of channel cj go to slot rank*128 + 4*(4w + cj) of every CTA's gathered
   // vector; remote addresses of buffer 0 / row 0 (buffer d, row r: (d R + r) GROW floats on).
   const bool pushes = q < CS;
@@ -230,15 +245,9 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 4 ? 1 : 2) cfc_bwd_kernel(c
              : 0u;
   const uint32_t rbar0 = pushes ? map_to_rank(bar0, q) : 0u;
 
-  // Everything above reads only W; dH and the forward cache may come from the previous kernel.
-  grid_dep_wait();
-  float cur[RR][kPreComp];  // register path: inputs of the current step
-  if constexpr (RT > 0) {
-    load_step_regs<RR>(dHp, cp, tsp, C, rok, cur);
-    dHp -= bc;
-    cp -= 3 * bc;
-    tsp -= B;
-  } else {
+  if constexpr (RT == 0) {
+    // The ring lives where the W_h^T staging was: start it only now.
+    grid_dep_wait();
     issue_pre(p, pre, K - 1, row0, rank, warp, lane);
     cp_async_commit();
     issue_pre(p, pre, K - 2, row0, rank, warp, lane);

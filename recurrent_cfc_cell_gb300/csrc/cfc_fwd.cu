@@ -98,43 +98,6 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 8 ? 1 : 2) cfc_fwd_kernel(c
   const int g = (lane >> 1) & 3;
   const int ch = kFwdChanPerCta * rank + 4 * warp + cj;
 
-  // W_h rows of the CTA's channels, staged coalesced as [4 gates x 32 channels][WP] (the whole
-  // shared-memory area is free before the K-loop), then this lane's 4 x HS block to registers.
-  float wh[4][S::HS];
-  {
-    // Chunks of loads are issued before their stores, so each chunk costs one round trip.
-    float* wst = smem;
-    constexpr int kPerThread = 4 * kFwdChanPerCta * S::CHP / kRecThreads;
-    constexpr int kChunk = kPerThread < 32 ? kPerThread : 32;
-    for (int i0 = 0; i0 < kPerThread; i0 += kChunk) {
-      float v[kChunk];
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        const int e = (i0 + i) * kRecThreads + tid;
-        const int lrow = e / S::CHP, col = e % S::CHP;
-        const int gg = lrow / kFwdChanPerCta, c = kFwdChanPerCta * rank + lrow % kFwdChanPerCta;
-        v[i] = (c < C && col < C) ? __ldg(p.W + (static_cast<size_t>(gg) * C + c) * n_in + n_x + col)
-                                  : 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        const int e = (i0 + i) * kRecThreads + tid;
-        wst[(e / S::CHP) * S::WP + e % S::CHP] = v[i];
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int gg = 0; gg < 4; ++gg) {
-      const float* src = wst + (gg * kFwdChanPerCta + 4 * warp + cj) * S::WP + sl * S::HS;
-#pragma unroll
-      for (int c = 0; c < S::HS; c += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src + c);
-        wh[gg][c] = v.x; wh[gg][c + 1] = v.y; wh[gg][c + 2] = v.z; wh[gg][c + 3] = v.w;
-      }
-    }
-    __syncthreads();
-  }
-
   // Per-lane addresses, computed once.
   //   X of this lane's (channel, gate g) -- written in place into H / cache by the
   //   projection -- for row row0 + r of step t: xp + t * xstep + r * xrow;
@@ -165,6 +128,62 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 8 ? 1 : 2) cfc_fwd_kernel(c
     }
   };
 
+  // h0 of this CTA's rows (element e = tid + 256 i of the R x C block), loaded now and written
+  // into the h buffer once the W staging area is free again.
+  constexpr int kH0 = (R * S::CHP + kRecThreads - 1) / kRecThreads;
+  float h0v[kH0];
+#pragma unroll
+  for (int i = 0; i < kH0; ++i) {
+    const int e = tid + i * kRecThreads, r = e / S::CHP, j = e % S::CHP;
+    h0v[i] = (e < R * S::CHP && row0 + r < B && j < C)
+                 ? __ldg(p.h0 + static_cast<size_t>(row0 + r) * C + j) : 0.f;
+  }
+
+  // W_h rows of the CTA's channels, staged coalesced as [4 gates x 32 channels][WP] (the whole
+  // shared-memory area is free before the K-loop), then this lane's 4 x HS block to registers.
+  // The loads of a chunk are all issued before its stores, and the first chunk is in flight
+  // together with h0 and the step-0 loads below.
+  float wh[4][S::HS];
+  float xc[R], tc[R];  // X and ts of the current step
+  {
+    float* wst = smem;
+    constexpr int kPerThread = 4 * kFwdChanPerCta * S::CHP / kRecThreads;
+    constexpr int kChunk = kPerThread < 64 ? kPerThread : 64;
+    for (int i0 = 0; i0 < kPerThread; i0 += kChunk) {
+      float v[kChunk];
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        const int e = (i0 + i) * kRecThreads + tid;
+        const int lrow = e / S::CHP, col = e % S::CHP;
+        const int gg = lrow / kFwdChanPerCta, c = kFwdChanPerCta * rank + lrow % kFwdChanPerCta;
+        v[i] = (c < C && col < C) ? __ldg(p.W + (static_cast<size_t>(gg) * C + c) * n_in + n_x + col)
+                                  : 0.f;
+      }
+      if (i0 == 0) {
+        // X comes from the projection kernel: wait for it (a no-op unless this launch is a
+        // dependent one), then start the step-0 loads.
+        grid_dep_wait();
+        load_step(xp, tsp, xc, tc);
+      }
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        const int e = (i0 + i) * kRecThreads + tid;
+        wst[(e / S::CHP) * S::WP + e % S::CHP] = v[i];
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int gg = 0; gg < 4; ++gg) {
+      const float* src = wst + (gg * kFwdChanPerCta + 4 * warp + cj) * S::WP + sl * S::HS;
+#pragma unroll
+      for (int c = 0; c < S::HS; c += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src + c);
+        wh[gg][c] = v.x; wh[gg][c + 1] = v.y; wh[gg][c + 2] = v.z; wh[gg][c + 3] = v.w;
+      }
+    }
+    __syncthreads();
+  }
+
   // ---- prologue ----
   const uint32_t bar0 = smem_addr(&bars[0]);  // bars[s] lives at bar0 + 8 s
   const uint32_t tx_bytes = static_cast<uint32_t>(CS * R * kFwdChanPerCta * 4);
@@ -175,15 +194,11 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 8 ? 1 : 2) cfc_fwd_kernel(c
   }
   for (int e = tid; e < 2 * R * S::HROW; e += kRecThreads) smem[e] = 0.f;
   __syncthreads();
-  for (int e = tid; e < R * C; e += kRecThreads) {
-    const int r = e / C, j = e - (e / C) * C;
-    if (row0 + r < B)
-      hbuf[r * S::HROW + hpos<CS>(j)] = p.h0[static_cast<size_t>(row0 + r) * C + j];
+#pragma unroll
+  for (int i = 0; i < kH0; ++i) {
+    const int e = tid + i * kRecThreads;
+    if (e < R * S::CHP) hbuf[(e / S::CHP) * S::HROW + hpos<CS>(e % S::CHP)] = h0v[i];
   }
-  // Everything above reads only W and h0; X comes from the projection kernel.
-  grid_dep_wait();
-  float xc[R], tc[R];  // X and ts of the current step
-  load_step(xp, tsp, xc, tc);
   // Step t consumes h_{t-1} through bars[t & 1]; arm the first two consumers (t = 1, 2).
   if (tid == 0) {
     if (K >= 2) mbar_arrive_expect_tx(bar0 + 8u, tx_bytes);
@@ -247,7 +262,7 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 8 ? 1 : 2) cfc_fwd_kernel(c
       // 2 the time gate sigmoid(P_ta ts + P_tb) (P_tb from the gate-3 lane two lanes up).
       const float P_tb = __shfl_sync(0xffffffffu, P, (lane + 2) & 31);
       const float x = (g < 2) ? 2.f * P : fmaf(P, tc[r], P_tb);
-      const float sg = sigmoid_acc(x);
+      const float sg = sigmoid_fast(x);
       const float y = (g < 2) ? fmaf(2.f, sg, -1.f) : sg;
       const int base = lane & 24;
       const float f1 = __shfl_sync(0xffffffffu, y, base + 0);
