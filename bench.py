@@ -339,30 +339,24 @@ def main():
                              f"{pk['sm_max_mhz']:.0f} MHz",
                 "hbm_frac": kernels[dominant]["gbs"] / pk["hbm_gbs"]}
 
-    # ---- end to end through the public API with host buffers
-    pin = {k: torch.from_numpy(v).pin_memory() for k, v in inp.items()}
-    outs = {k: torch.empty(tuple(getattr(st, k).shape), dtype=torch.float32).pin_memory()
-            for k in ("dW", "db", "du", "dh0")}
-    h2d = sum(v.numel() * 4 for v in pin.values())
-    d2h = sum(v.numel() * 4 for v in outs.values())
+    # ---- end to end through the public API with host buffers: every step copies its inputs
+    # in from pinned host memory and its gradients out to pinned host memory (one packed copy
+    # each way, captured with the step's kernels in one graph).
+    ste = KLoopStep(w.B, w.K, w.C, w.n_x, device=dev).stage_host()
+    for k, v in inp.items():
+        ste.host_in[k].copy_(torch.from_numpy(v))
+    h2d, d2h = ste.io_bytes()
     n_e2e = min(args.steps, 200)
-
-    def e2e_step():
-        for k, v in pin.items():
-            dinp[k].copy_(v, non_blocking=True)
-        st.run()
-        for k, v in outs.items():
-            v.copy_(getattr(st, k), non_blocking=True)
-
+    ste.capture(with_host_io=True)
     for _ in range(3):
-        e2e_step()
+        ste.replay()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n_e2e)]
     for a, b in ev:
         flush.zero_()
         a.record(stream)
-        e2e_step()
+        ste.replay()
         b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in ev) / n_e2e

@@ -62,13 +62,70 @@ class KLoopStep:
         self.forward(stream)
         self.backward(stream)
 
-    def capture(self) -> torch.cuda.CUDAGraph:
-        """Capture run() into a CUDA graph (one eager run first sets kernel attributes)."""
-        self.run()
+    # ---- host staging: one pinned buffer of inputs in, one of gradients out ----------------
+    @staticmethod
+    def _pack(shapes: dict, device, pinned: bool):
+        """One flat fp32 buffer holding every shape at a 256-byte-aligned offset, and its views."""
+        off, offs = 0, {}
+        for k, shp in shapes.items():
+            offs[k] = off
+            n = 1
+            for d in shp:
+                n *= d
+            off += (n + 63) // 64 * 64
+        buf = torch.empty(off, dtype=torch.float32, device=device)
+        if pinned:
+            buf = buf.pin_memory()
+        views = {}
+        for k, shp in shapes.items():
+            n = 1
+            for d in shp:
+                n *= d
+            views[k] = buf[offs[k]: offs[k] + n].view(*shp)
+        return buf, views
+
+    def stage_host(self) -> "KLoopStep":
+        """Give the step packed input and gradient buffers on the device, each with a pinned
+        host twin, so one copy brings a step's inputs in and one copy takes its gradients out
+        (capture(with_host_io=True) puts both copies in the step's graph).  Fill
+        ``host_in[name]``; read ``host_out[name]`` after the step."""
+        B, K, C, n_x, n_in = self.B, self.K, self.C, self.n_x, self.n_in
+        shapes_in = {"u": (K, B, n_x), "h0": (B, C), "W": (4, C, n_in), "b": (4, C),
+                     "ts": (K, B), "dH": (K, B, C)}
+        shapes_out = {"dW": (4, C, n_in), "db": (4, C), "dh0": (B, C)}
+        if self.du is not None:
+            shapes_out["du"] = (K, B, n_x)
+        self._dev_in, self.inputs = self._pack(shapes_in, self.device, False)
+        self._host_in_buf, self.host_in = self._pack(shapes_in, "cpu", True)
+        self._dev_out, outs = self._pack(shapes_out, self.device, False)
+        self._host_out_buf, self.host_out = self._pack(shapes_out, "cpu", True)
+        self.dW, self.db, self.dh0 = outs["dW"], outs["db"], outs["dh0"]
+        if self.du is not None:
+            self.du = outs["du"]
+        self.graph = None
+        return self
+
+    def io_bytes(self) -> tuple[int, int]:
+        """Bytes of real tensor data one staged step copies in and out."""
+        n_in = sum(v.numel() for v in self.host_in.values()) * 4
+        n_out = sum(v.numel() for v in self.host_out.values()) * 4
+        return n_in, n_out
+
+    def run_with_host_io(self, stream=None) -> None:
+        """Inputs in from the pinned host buffer, the step, gradients out to it."""
+        self._dev_in.copy_(self._host_in_buf, non_blocking=True)
+        self.run(stream)
+        self._host_out_buf.copy_(self._dev_out, non_blocking=True)
+
+    def capture(self, with_host_io: bool = False) -> torch.cuda.CUDAGraph:
+        """Capture run() (or run_with_host_io()) into a CUDA graph (one eager run first sets
+        kernel attributes)."""
+        fn = self.run_with_host_io if with_host_io else self.run
+        fn()
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.run()
+            fn()
         self.graph = g
         return g
 

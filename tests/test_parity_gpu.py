@@ -63,6 +63,32 @@ def test_two_stage_forward_matches_oracle(shape):
                   keys=("H", "cache"))
 
 
+def test_host_staged_graph_step_parity():
+    """The packed host-staging path: inputs copied in, the step, gradients copied out, all in
+    one graph; run twice with different inputs so the second replay must reflect new data."""
+    import torch
+
+    from recurrent_cfc_cell_gb300 import build
+    from recurrent_cfc_cell_gb300.step import KLoopStep
+
+    build.build()
+    w = inputs.custom(B=6, K=9, n_x=12, C=72, seed=31)
+    st = KLoopStep(w.B, w.K, w.C, w.n_x).stage_host()
+    st.capture(with_host_io=True)
+    for seed in (31, 32):
+        inp = inputs.make_inputs(inputs.custom(B=6, K=9, n_x=12, C=72, seed=seed))
+        for k, v in inp.items():
+            st.host_in[k].copy_(torch.from_numpy(v))
+        st.replay()
+        torch.cuda.synchronize()
+        got = {k: v.numpy().copy() for k, v in st.host_out.items()}
+        got["H"] = st.H.cpu().numpy()
+        assert_parity(got, oracle_ref(inp), keys=("H", "dW", "db", "du", "dh0"))
+    n_in, n_out = st.io_bytes()
+    assert n_in == 4 * sum(v.size for v in inp.values())
+    assert n_out == 4 * (4 * 72 * 84 + 4 * 72 + 9 * 6 * 12 + 6 * 72)
+
+
 def test_graph_replay_parity():
     inp = inputs.make_inputs(inputs.CONFIGS[1])
     assert_parity(run_gpu(inp, graph=True), oracle_ref(inp))
