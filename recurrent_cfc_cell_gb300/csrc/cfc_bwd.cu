@@ -88,19 +88,23 @@ __device__ __forceinline__ int gpos(int gidx) {
 // delta for the four channels of this warp from this lane's slice of the gathered d_pre
 // vector; lanes 8cj .. 8cj+7 return channel cj.
 template <int RS>
-__device__ __forceinline__ float gathered_delta(const float (&wt)[4][RS], const float* dvp,
+__device__ __forceinline__ float gathered_delta(const float2 (&wt)[4][RS / 2], const float* dvp,
                                                 int lane) {
-  float dv[RS];
+  float2 a2[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) a2[c] = make_float2(0.f, 0.f);
 #pragma unroll
   for (int k = 0; k < RS; k += 4) {
     const float4 v = *reinterpret_cast<const float4*>(dvp + k);
-    dv[k] = v.x; dv[k + 1] = v.y; dv[k + 2] = v.z; dv[k + 3] = v.w;
+    const float2 lo = make_float2(v.x, v.y), hi = make_float2(v.z, v.w);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) a2[c] = fma2(wt[c][k / 2], lo, a2[c]);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) a2[c] = fma2(wt[c][k / 2 + 1], hi, a2[c]);
   }
-  float a[4] = {0.f, 0.f, 0.f, 0.f};
+  float a[4];
 #pragma unroll
-  for (int k = 0; k < RS; ++k)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) a[c] = fmaf(wt[c][k], dv[k], a[c]);
+  for (int c = 0; c < 4; ++c) a[c] = a2[c].x + a2[c].y;
   // Reduce-scatter over the 32 lanes: xor 16 keeps channels {0,1} / {2,3}, xor 8 one channel,
   // then the eight lanes of a channel sum.
   const bool b16 = lane & 16, b8 = lane & 8;
@@ -177,7 +181,7 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 4 ? 1 : 2) cfc_bwd_kernel(c
   // Gathered row q*128 + 4i + g is W row g*C + 32q + i.  Staged through shared memory as
   // [NG][33] (the whole smem area is free before the loop): consecutive threads read
   // consecutive channels of one W row, a chunk of loads in flight before any store.
-  float wt[4][S::RS];
+  float2 wt[4][S::RS / 2];  // consecutive gathered rows paired for the packed FMA
   float cur[RR][kPreComp];  // register path: inputs of the current step
   {
     float* wtmp = smem;
@@ -218,8 +222,9 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 4 ? 1 : 2) cfc_bwd_kernel(c
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-      for (int k = 0; k < S::RS; ++k)
-        wt[cc][k] = wtmp[(lane * S::RS + k) * kPitch + 4 * warp + cc];
+      for (int k = 0; k < S::RS; k += 2)
+        wt[cc][k / 2] = make_float2(wtmp[(lane * S::RS + k) * kPitch + 4 * warp + cc],
+                                    wtmp[(lane * S::RS + k + 1) * kPitch + 4 * warp + cc]);
     __syncthreads();
   }
 

@@ -54,20 +54,15 @@ struct FwdShape {
   static constexpr int WP = CHP + 4;               // row pitch of the staged W_h block
 };
 
-// Load n consecutive floats (n = 1, 2 or a multiple of 4) from shared memory.
+// Load N consecutive floats (N a multiple of 4) from shared memory as N / 2 pairs.
 template <int N>
-__device__ __forceinline__ void lds_vec(const float* src, float (&dst)[N]) {
-  if constexpr (N % 4 == 0) {
+__device__ __forceinline__ void lds_pairs(const float* src, float2 (&dst)[N / 2]) {
+  static_assert(N % 4 == 0, "h slices are whole float4s");
 #pragma unroll
-    for (int c = 0; c < N; c += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(src + c);
-      dst[c] = v.x; dst[c + 1] = v.y; dst[c + 2] = v.z; dst[c + 3] = v.w;
-    }
-  } else if constexpr (N == 2) {
-    const float2 v = *reinterpret_cast<const float2*>(src);
-    dst[0] = v.x; dst[1] = v.y;
-  } else {
-    dst[0] = src[0];
+  for (int c = 0; c < N; c += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(src + c);
+    dst[c / 2] = make_float2(v.x, v.y);
+    dst[c / 2 + 1] = make_float2(v.z, v.w);
   }
 }
 
@@ -143,7 +138,7 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 8 ? 1 : 2) cfc_fwd_kernel(c
   // shared-memory area is free before the K-loop), then this lane's 4 x HS block to registers.
   // The loads of a chunk are all issued before its stores, and the first chunk is in flight
   // together with h0 and the step-0 loads below.
-  float wh[4][S::HS];
+  float2 wh[4][S::HS / 2];  // consecutive h inputs paired for the packed FMA
   float xc[R], tc[R];  // X and ts of the current step
   {
     float* wst = smem;
@@ -178,7 +173,8 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 8 ? 1 : 2) cfc_fwd_kernel(c
 #pragma unroll
       for (int c = 0; c < S::HS; c += 4) {
         const float4 v = *reinterpret_cast<const float4*>(src + c);
-        wh[gg][c] = v.x; wh[gg][c + 1] = v.y; wh[gg][c + 2] = v.z; wh[gg][c + 3] = v.w;
+        wh[gg][c / 2] = make_float2(v.x, v.y);
+        wh[gg][c / 2 + 1] = make_float2(v.z, v.w);
       }
     }
     __syncthreads();
@@ -243,13 +239,18 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 8 ? 1 : 2) cfc_fwd_kernel(c
     const bool b2 = lane & 4, b1 = lane & 2;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      float hv[S::HS];
-      lds_vec<S::HS>(hb + r * S::HROW, hv);
-      float a[4] = {0.f, 0.f, 0.f, 0.f};
+      float2 hv[S::HS / 2];
+      lds_pairs<S::HS>(hb + r * S::HROW, hv);
+      float2 a2[4];
 #pragma unroll
-      for (int c = 0; c < S::HS; ++c)
+      for (int gg = 0; gg < 4; ++gg) a2[gg] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int gg = 0; gg < 4; ++gg) a[gg] = fmaf(wh[gg][c], hv[c], a[gg]);
+      for (int c = 0; c < S::HS / 2; ++c)
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg) a2[gg] = fma2(wh[gg][c], hv[c], a2[gg]);
+      float a[4];
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) a[gg] = a2[gg].x + a2[gg].y;
       // Reduce-scatter over the 8 lanes of the channel: lane keeps gate (lane >> 1) & 3.
       const float k0 = b2 ? a[2] : a[0], k1 = b2 ? a[3] : a[1];
       const float s0 = k0 + __shfl_xor_sync(0xffffffffu, b2 ? a[0] : a[2], 4);

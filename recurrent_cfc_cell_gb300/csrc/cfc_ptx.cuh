@@ -313,4 +313,8 @@ __device__ __forceinline__ float sigmoid_fast(float x) {
   return __fdividef(1.0f, 1.0f + __expf(-x));
 }
 
+// Packed fp32 FMA (two independent lanes of fma.rn in one instruction on sm_100 and later):
+// the recurrences' matrix-vector products pair consecutive inputs, halving their FMA issue.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
 }  // namespace cfc
