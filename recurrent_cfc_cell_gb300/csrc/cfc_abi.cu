@@ -148,7 +148,14 @@ struct BwdLayout {
   int S_simt;          // split count of the CUDA-core contraction
   cfc::TcPlan tc;      // plan of the tensor-core weight-gradient contraction
   cfc::TcPlan tu;      // plan of the tensor-core input-gradient contraction
+  bool dual;           // du in the dW launch (unsplit) rather than after the dW merge
 };
+
+// Row tiles (of 128) from which unsplit du tiles keep enough SMs busy beside the dW splits:
+// measured on GB300, the combined launch took the gradient stage of B*K = 262144 from 3.85 to
+// 3.17 ms, while at B*K = 2048 (16 tiles) it was slower than dW, merge, split du (31.6 against
+// 26.3 us).
+constexpr int kDualMinDuTiles = 64;
 
 BwdLayout bwd_layout(int B, int K, int C, int n_x) {
   BwdLayout L;
@@ -157,8 +164,11 @@ BwdLayout bwd_layout(int B, int K, int C, int n_x) {
   L.d_pre_bytes = BK * 4 * C * sizeof(float);
   L.S_simt = cfc::dw_simt_splits(static_cast<int>(BK));
   L.tc = cfc::dw_tc_plan(B, K, C, n_x);
-  L.tu = cfc::du_tc_plan(B, K, C, n_x);
-  // The dW partials are consumed before du runs, so du's partials reuse the same area.
+  // With enough rows du runs unsplit beside the dW splits (one launch, du written directly);
+  // otherwise it runs after the dW merge, split over 4C, its partials reusing the dW area.
+  L.tu = cfc::du_tc_plan_unsplit(B, K, C, n_x);
+  L.dual = L.tu.m_tiles >= kDualMinDuTiles;
+  if (!L.dual) L.tu = cfc::du_tc_plan(B, K, C, n_x);
   size_t part = static_cast<size_t>(L.S_simt) * 4 * C * (n_x + C);
   const size_t ptc = static_cast<size_t>(L.tc.splits) * 4 * C * cfc::dw_tc_pitch(n_x + C);
   if (ptc > part) part = ptc;
@@ -282,11 +292,13 @@ int cfc_step_launches(int B, int K, int C, int n_x, int dw_mode, int with_du, in
   if (!launches) return CFC_ERR_NULL_PTR;
   // forward: projection + recurrence; backward: recurrence, dW contraction + its reduction
   // (which also yields db with the tensor cores; a separate db reduction otherwise), and du
-  // (plus its reduction when the tensor-core plan splits it).
+  // (inside the dW launch for large B*K with the tensor cores, else a launch of its own plus
+  // its reduction when the plan splits it).
   int n = 2 + 1 + 2 + (dw_mode == CFC_DW_ACCURATE ? 0 : 1);
   if (with_du) {
-    n += 1;
-    if (dw_mode == CFC_DW_ACCURATE && bwd_layout(B, K, C, n_x).tu.splits > 1) n += 1;
+    const BwdLayout L = bwd_layout(B, K, C, n_x);
+    if (dw_mode != CFC_DW_ACCURATE) n += 1;
+    else if (!L.dual) n += (L.tu.splits > 1) ? 2 : 1;
   }
   *launches = n;
   return CFC_OK;
@@ -349,6 +361,12 @@ int weight_grad(const float* d_pre, const float* u, const float* h0, const float
     S = L.S_simt;
     rc = cuda_rc(cfc::dw_simt_launch(d_pre, u, H, h0, B, K, C, n_x, S, partial, s, first_pdl),
                  CFC_ERR_LAUNCH_FAILED);
+  } else if (du && L.dual) {
+    // dW partials and du from one grid: both read only d_pre (and the inputs).
+    S = L.tc.splits;
+    rc = cuda_rc(cfc::dwdu_tc_launch(L.tc, L.tu, d_pre, u, H, h0, W, B, K, C, n_x, partial, du,
+                                     st->status, s, first_pdl),
+                 CFC_ERR_LAUNCH_FAILED);
   } else {
     S = L.tc.splits;
     rc = cuda_rc(cfc::dw_tc_launch(L.tc, d_pre, u, H, h0, B, K, C, n_x, partial, st->status, s,
@@ -368,11 +386,10 @@ int weight_grad(const float* d_pre, const float* u, const float* h0, const float
                  CFC_ERR_LAUNCH_FAILED);
   }
   if (rc != CFC_OK) return rc;
-  if (du) {
-    if (dw_mode == CFC_DW_SIMT_FP32) {
-      rc = cuda_rc(cfc::du_simt_launch(d_pre, W, BK, C, n_x, du, s, true),
-                   CFC_ERR_LAUNCH_FAILED);
-    } else if (L.tu.splits == 1) {
+  if (du && dw_mode == CFC_DW_SIMT_FP32) {
+    rc = cuda_rc(cfc::du_simt_launch(d_pre, W, BK, C, n_x, du, s, true), CFC_ERR_LAUNCH_FAILED);
+  } else if (du && !L.dual) {
+    if (L.tu.splits == 1) {
       rc = cuda_rc(cfc::du_tc_launch(L.tu, d_pre, W, B, K, C, n_x, du, st->status, s, true),
                    CFC_ERR_LAUNCH_FAILED);
     } else {

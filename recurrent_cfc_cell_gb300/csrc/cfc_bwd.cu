@@ -47,6 +47,7 @@ namespace {
 
 constexpr int kWarps = kRecThreads / 32;
 constexpr int kPre = 3;      // prefetch ring depth (copies run two steps ahead)
+constexpr int kRowBlock = 4; // rows per phase block of the ring path (its row counts are multiples)
 constexpr int kPreComp = 5;  // dH, ff1, ff2, gate, ts
 
 // Lanes 8*cj + c (c < 5) copy component c of this warp's channel cj for step t.
@@ -294,33 +295,54 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 4 ? 1 : 2) cfc_bwd_kernel(c
     const float* pre_t = pre + ((t % kPre) * R * kWarps + warp) * 4 * kPreComp + cj * kPreComp;
     const uint32_t pdst = push0 + static_cast<uint32_t>((s ^ 1) * R * S::GROW * 4);
     const uint32_t pbar = rbar0 + 8u * (s ^ 1);
-#pragma unroll(RT > 0 ? RT : 1)
-    for (int r = 0; r < R; ++r) {
-      const float delta =
-          (t < K - 1) ? gathered_delta<S::RS>(wt, dg + (s * R + r) * S::GROW + lane * S::RSP, lane)
-                      : 0.f;
-      const bool valid = row0 + r < B && ch < C;
-      float v[kPreComp];  // dH, ff1, ff2, gate, ts of (t, b, ch)
+    // Rows are independent within a step: each block of RB rows runs in phases (products,
+    // then gradients, then stores and pushes) so the rows' latency chains overlap and no
+    // asynchronous push sits between one row's shared loads and the next row's.
+    constexpr int RB = RT > 0 ? RT : kRowBlock;
+#pragma unroll 1
+    for (int r0 = 0; r0 < R; r0 += RB) {
+      float delta[RB];
 #pragma unroll
-      for (int c = 0; c < kPreComp; ++c)
-        v[c] = RT > 0 ? cur[RT > 0 ? r : 0][c] : pre_t[r * kWarps * 4 * kPreComp + c];
-      const float dh = v[0] + delta;
-      const float f1 = v[1], f2 = v[2], g = v[3];
-      const float ds = dh * (f2 - f1) * g * (1.f - g);
-      // This lane's gate, by selects (neighbouring lane pairs hold different gates, so a
-      // branch here would split the warp four ways).
-      const float p0 = dh * (1.f - g) * (1.f - f1 * f1);
-      const float p1 = dh * g * (1.f - f2 * f2);
-      const float p2 = ds * v[4];
-      const float sel = (gq == 0) ? p0 : (gq == 1) ? p1 : (gq == 2) ? p2 : ds;
-      const float dpv = valid ? sel : 0.f;
-      if (stores && valid) dpp[static_cast<size_t>(r) * 4 * C] = dpv;
+      for (int rb = 0; rb < RB; ++rb)
+        delta[rb] = (t < K - 1) ? gathered_delta<S::RS>(
+                                      wt, dg + (s * R + r0 + rb) * S::GROW + lane * S::RSP, lane)
+                                : 0.f;
+      float dpv[RB];
+#pragma unroll
+      for (int rb = 0; rb < RB; ++rb) {
+        const int r = r0 + rb;
+        const bool valid = row0 + r < B && ch < C;
+        float v[kPreComp];  // dH, ff1, ff2, gate, ts of (t, b, ch)
+#pragma unroll
+        for (int c = 0; c < kPreComp; ++c)
+          v[c] = RT > 0 ? cur[RT > 0 ? rb : 0][c] : pre_t[r * kWarps * 4 * kPreComp + c];
+        const float dh = v[0] + delta[rb];
+        const float f1 = v[1], f2 = v[2], g = v[3];
+        const float ds = dh * (f2 - f1) * g * (1.f - g);
+        // This lane's gate, by selects (neighbouring lane pairs hold different gates, so a
+        // branch here would split the warp four ways).
+        const float p0 = dh * (1.f - g) * (1.f - f1 * f1);
+        const float p1 = dh * g * (1.f - f2 * f2);
+        const float p2 = ds * v[4];
+        const float sel = (gq == 0) ? p0 : (gq == 1) ? p1 : (gq == 2) ? p2 : ds;
+        dpv[rb] = valid ? sel : 0.f;
+      }
       // The four gates of channel cj -> one 16-byte push to every CTA of the cluster.
-      const float d0 = __shfl_sync(0xffffffffu, dpv, base + 0);
-      const float d1 = __shfl_sync(0xffffffffu, dpv, base + 2);
-      const float d2 = __shfl_sync(0xffffffffu, dpv, base + 4);
-      const float d3 = __shfl_sync(0xffffffffu, dpv, base + 6);
-      st_async_v4_if(pushes, pdst + static_cast<uint32_t>(r * S::GROW * 4), d0, d1, d2, d3, pbar);
+      float4 dq[RB];
+#pragma unroll
+      for (int rb = 0; rb < RB; ++rb) {
+        dq[rb].x = __shfl_sync(0xffffffffu, dpv[rb], base + 0);
+        dq[rb].y = __shfl_sync(0xffffffffu, dpv[rb], base + 2);
+        dq[rb].z = __shfl_sync(0xffffffffu, dpv[rb], base + 4);
+        dq[rb].w = __shfl_sync(0xffffffffu, dpv[rb], base + 6);
+      }
+#pragma unroll
+      for (int rb = 0; rb < RB; ++rb)
+        st_async_v4_if(pushes, pdst + static_cast<uint32_t>((r0 + rb) * S::GROW * 4), dq[rb].x,
+                       dq[rb].y, dq[rb].z, dq[rb].w, pbar);
+#pragma unroll
+      for (int rb = 0; rb < RB; ++rb)
+        if (stores && row0 + r0 + rb < B) dpp[static_cast<size_t>(r0 + rb) * 4 * C] = dpv[rb];
     }
     dpp -= 4 * bc;
     if constexpr (RT > 0) {
@@ -413,7 +435,10 @@ cudaError_t launch_cs(const BwdParams& p, int n_clusters, size_t smem, cudaStrea
     case 1: return launch_k<CS, 1>(p, n_clusters, smem, s, pdl);
     case 2: return launch_k<CS, 2>(p, n_clusters, smem, s, pdl);
     case 4: return launch_k<CS, 4>(p, n_clusters, smem, s, pdl);
-    default: return launch_k<CS, 0>(p, n_clusters, smem, s, pdl);
+    default:
+      // The ring kernel walks its rows in whole blocks.
+      if (p.R % kRowBlock != 0) return cudaErrorInvalidValue;
+      return launch_k<CS, 0>(p, n_clusters, smem, s, pdl);
   }
 }
 

@@ -73,7 +73,7 @@ __device__ __forceinline__ int hpos(int j) {
 }
 
 template <int CS, int R>
-__global__ void __launch_bounds__(kRecThreads, CS >= 8 ? 1 : 2) cfc_fwd_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(kRecThreads, (CS >= 8 || R >= 8) ? 1 : 2) cfc_fwd_kernel(const FwdParams p) {
   using S = FwdShape<CS>;
   extern __shared__ __align__(16) float smem[];
   float* hbuf = smem;  // [2][R][HROW]
@@ -237,6 +237,11 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 8 ? 1 : 2) cfc_fwd_kernel(c
     const uint32_t pdst = push0 + static_cast<uint32_t>((s ^ 1) * R * S::HROW * 4);
     const uint32_t pbar = rbar0 + 8u * (s ^ 1);
     const bool b2 = lane & 4, b1 = lane & 2;
+    const int base = lane & 24;
+    // The rows are independent within a step, so the step runs in phases over all R rows
+    // (products, then activations, then pushes and stores): the rows' latency chains overlap,
+    // and no asynchronous push sits between one row's shared loads and the next row's.
+    float P[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       float2 hv[S::HS / 2];
@@ -257,29 +262,39 @@ __global__ void __launch_bounds__(kRecThreads, CS >= 8 ? 1 : 2) cfc_fwd_kernel(c
       const float s1 = k1 + __shfl_xor_sync(0xffffffffu, b2 ? a[1] : a[3], 4);
       float acc = (b1 ? s1 : s0) + __shfl_xor_sync(0xffffffffu, b1 ? s0 : s1, 2);
       acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      const float P = acc + xc[r];
-
+      P[r] = acc + xc[r];
+    }
+    float hn[R], sv[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
       // Activations: lanes of gate 0 / 1 evaluate tanh(P) = 2 sigmoid(2P) - 1, lanes of gate
       // 2 the time gate sigmoid(P_ta ts + P_tb) (P_tb from the gate-3 lane two lanes up).
-      const float P_tb = __shfl_sync(0xffffffffu, P, (lane + 2) & 31);
-      const float x = (g < 2) ? 2.f * P : fmaf(P, tc[r], P_tb);
+      const float P_tb = __shfl_sync(0xffffffffu, P[r], (lane + 2) & 31);
+      const float x = (g < 2) ? 2.f * P[r] : fmaf(P[r], tc[r], P_tb);
       const float sg = sigmoid_fast(x);
       const float y = (g < 2) ? fmaf(2.f, sg, -1.f) : sg;
-      const int base = lane & 24;
       const float f1 = __shfl_sync(0xffffffffu, y, base + 0);
       const float f2 = __shfl_sync(0xffffffffu, y, base + 2);
       const float gt = __shfl_sync(0xffffffffu, y, base + 4);
-      const float h = f1 * (1.f - gt) + gt * f2;
-      // The warp's four channels, gathered for one 16-byte push per destination CTA.
-      const float h0v = __shfl_sync(0xffffffffu, h, 0);
-      const float h1v = __shfl_sync(0xffffffffu, h, 8);
-      const float h2v = __shfl_sync(0xffffffffu, h, 16);
-      const float h3v = __shfl_sync(0xffffffffu, h, 24);
-      st_async_v4_if(pushes && t + 1 < K, pdst + static_cast<uint32_t>(r * S::HROW * 4), h0v,
-                     h1v, h2v, h3v, pbar);
-      const float sv = (sl == 0) ? h : (sl == 1) ? f1 : (sl == 2 ? f2 : gt);
-      if (sok[r]) sp[r * srow] = sv;
+      hn[r] = f1 * (1.f - gt) + gt * f2;
+      sv[r] = (sl == 0) ? hn[r] : (sl == 1) ? f1 : (sl == 2 ? f2 : gt);
     }
+    // The warp's four channels of each row, gathered for one 16-byte push per destination CTA.
+    float4 hq[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      hq[r].x = __shfl_sync(0xffffffffu, hn[r], 0);
+      hq[r].y = __shfl_sync(0xffffffffu, hn[r], 8);
+      hq[r].z = __shfl_sync(0xffffffffu, hn[r], 16);
+      hq[r].w = __shfl_sync(0xffffffffu, hn[r], 24);
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      st_async_v4_if(pushes && t + 1 < K, pdst + static_cast<uint32_t>(r * S::HROW * 4), hq[r].x,
+                     hq[r].y, hq[r].z, hq[r].w, pbar);
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      if (sok[r]) sp[r * srow] = sv[r];
     sp += sstep;
     if (t + 1 < K) {
 #pragma unroll
@@ -342,6 +357,7 @@ cudaError_t prepare_cs(int R, size_t smem, int* max_active) {
     case 1: return prepare_k<CS, 1>(smem, max_active);
     case 2: return prepare_k<CS, 2>(smem, max_active);
     case 4: return prepare_k<CS, 4>(smem, max_active);
+    case 8: return prepare_k<CS, 8>(smem, max_active);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -353,6 +369,7 @@ cudaError_t launch_cs(const FwdParams& p, int n_clusters, size_t smem, cudaStrea
     case 1: return launch_k<CS, 1>(p, n_clusters, smem, s, pdl);
     case 2: return launch_k<CS, 2>(p, n_clusters, smem, s, pdl);
     case 4: return launch_k<CS, 4>(p, n_clusters, smem, s, pdl);
+    case 8: return launch_k<CS, 8>(p, n_clusters, smem, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

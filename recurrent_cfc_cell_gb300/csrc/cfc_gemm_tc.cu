@@ -222,8 +222,9 @@ struct DuProblem {
   }
 };
 
+// One CTA's work: output tile `tile` (m-tile fastest) over reduction split `split`.
 template <class Problem>
-__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcParams p) {
+__device__ __forceinline__ void tc_gemm_body(const TcParams& p, int tile, int split) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned stage buffers (128-byte swizzle atoms), then the barriers.
   const uint32_t raw = smem_addr(smem_raw);
@@ -237,9 +238,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcParams p
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int m0 = (blockIdx.x % p.m_tiles) * kTcM;
-  const int n0 = (blockIdx.x / p.m_tiles) * p.n_tile;
-  const int split = blockIdx.y;
+  const int m0 = (tile % p.m_tiles) * kTcM;
+  const int n0 = (tile / p.m_tiles) * p.n_tile;
   const int kb0 = split * p.kb_per_split;
   const int nk = min(p.kb_per_split, p.n_kb - kb0);
   uint32_t ncols = 32;
@@ -336,6 +336,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcParams p
   }
 }
 
+template <class Problem>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcParams p) {
+  tc_gemm_body<Problem>(p, blockIdx.x, blockIdx.y);
+}
+
+// Both contractions in one grid: the first n_w CTAs take the weight-gradient tiles and splits,
+// the rest the input-gradient tiles (which run unsplit).  They read the same d_pre and write
+// disjoint outputs, so one launch replaces two dependent ones.
+__global__ void __launch_bounds__(kTcThreads, 1) tc_dual_kernel(const TcParams pw,
+                                                                const TcParams pu, int n_w) {
+  const int b = blockIdx.x;
+  const int tiles_w = pw.m_tiles * ((pw.cols + pw.n_tile - 1) / pw.n_tile);
+  if (b < n_w) tc_gemm_body<DwProblem>(pw, b % tiles_w, b / tiles_w);
+  else tc_gemm_body<DuProblem>(pu, b - n_w, 0);
+}
+
 
 TcPlan tc_plan(int rows, int cols, int red, bool split) {
   TcPlan pl;
@@ -361,13 +377,19 @@ TcPlan dw_tc_plan(int B, int K, int C, int n_x) {
   return tc_plan(4 * C, dw_tc_pitch(n_x + C), B * K, true);
 }
 TcPlan du_tc_plan(int B, int K, int C, int n_x) { return tc_plan(B * K, n_x, 4 * C, true); }
+TcPlan du_tc_plan_unsplit(int B, int K, int C, int n_x) {
+  return tc_plan(B * K, n_x, 4 * C, false);
+}
 
 cudaError_t tc_prepare(int max_smem) {
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<DwProblem>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(tc_gemm_kernel<DuProblem>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  e = cudaFuncSetAttribute(tc_gemm_kernel<DuProblem>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           max_smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(tc_dual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              max_smem);
 }
 
 namespace {
@@ -410,6 +432,27 @@ cudaError_t du_tc_launch(const TcPlan& pl, const float* d_pre, const float* W, i
   c.stream = s;
   c.pdl = pdl;
   return launch(c, tc_gemm_kernel<DuProblem>, p);
+}
+
+cudaError_t dwdu_tc_launch(const TcPlan& pw, const TcPlan& pu, const float* d_pre,
+                           const float* u, const float* H, const float* h0, const float* W, int B,
+                           int K, int C, int n_x, float* partial, float* du, int* status,
+                           cudaStream_t s, bool pdl) {
+  if (pu.splits != 1) return cudaErrorInvalidValue;  // du is written directly
+  TcParams a = make_params(pw, d_pre, B, K, C, n_x, status);
+  a.u = u; a.H = H; a.h0 = h0; a.out = partial;
+  a.rows = 4 * C; a.cols = dw_tc_pitch(n_x + C); a.red = B * K;
+  TcParams b = make_params(pu, d_pre, B, K, C, n_x, status);
+  b.W = W; b.out = du;
+  b.rows = B * K; b.cols = n_x; b.red = 4 * C;
+  const int n_w = pw.m_tiles * pw.n_tiles * pw.splits;
+  LaunchCfg c;
+  c.grid = dim3(n_w + pu.m_tiles * pu.n_tiles, 1, 1);
+  c.block = dim3(kTcThreads, 1, 1);
+  c.smem = pw.smem > pu.smem ? pw.smem : pu.smem;
+  c.stream = s;
+  c.pdl = pdl;
+  return launch(c, tc_dual_kernel, a, b, n_w);
 }
 
 }  // namespace cfc

@@ -15,7 +15,7 @@ constexpr int kMaxClusterSize = 16;  // reduce_axis0 (non-portable clusters up t
 constexpr int kMaxChannels = 256;    // largest C: clusters of 8 CTAs x 32 channels
 constexpr int kMaxInputs = 512;  // largest n_x (W_u rows of a CTA live in shared memory)
 constexpr int kMaxRowsPerCluster = 32;  // backward recurrence
-constexpr int kMaxFwdRows = 4;         // forward recurrence (rows are a template parameter)
+constexpr int kMaxFwdRows = 8;         // forward recurrence (rows are a template parameter)
 
 struct FwdParams {
   const float* u;      // [K][B][n_x]
@@ -82,6 +82,12 @@ cudaError_t dw_tc_launch(const TcPlan& pl, const float* d_pre, const float* u, c
 // du, or (when pl.splits > 1) its partial blocks [splits][B*K][n_x].
 cudaError_t du_tc_launch(const TcPlan& pl, const float* d_pre, const float* W, int B, int K,
                          int C, int n_x, float* du, int* status, cudaStream_t s, bool pdl);
+// Both in one launch: the dW partials of plan pw and du itself (plan pu must be unsplit).
+TcPlan du_tc_plan_unsplit(int B, int K, int C, int n_x);
+cudaError_t dwdu_tc_launch(const TcPlan& pw, const TcPlan& pu, const float* d_pre,
+                           const float* u, const float* H, const float* h0, const float* W, int B,
+                           int K, int C, int n_x, float* partial, float* du, int* status,
+                           cudaStream_t s, bool pdl);
 
 // du[r][k] = sum_m d_pre[r][m] * W[m][k] for k < n_x (SIMT fp32).
 cudaError_t du_simt_launch(const float* d_pre, const float* W, int BK, int C, int n_x,

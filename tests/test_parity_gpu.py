@@ -29,6 +29,9 @@ RAGGED = [
     dict(B=1, K=2, n_x=512, C=16),    # widest input, one CTA per cluster
     dict(B=3, K=4, n_x=301, C=256),   # wide input with the widest state
     dict(B=40, K=9, n_x=64, C=256),   # rows grouped several per 16-CTA cluster
+    dict(B=300, K=28, n_x=48, C=128),  # 8 rows per cluster, part-filled last cluster; dW and
+                                       # du in one launch with a ragged last row tile
+    dict(B=200, K=6, n_x=64, C=256),   # 8-row forward and 16-row BPTT clusters of 8 CTAs
 ]
 
 
