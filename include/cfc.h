@@ -130,6 +130,19 @@ int cfc_backward(const float* dH, const float* u, const float* h0, const float* 
                  size_t ws_bytes, int dw_mode, cfc_stream_t stream);
 
 /*
+ * cfc_forward_backward -- one training step: exactly cfc_forward followed by cfc_backward,
+ * with the same arguments, outputs and workspace, and bitwise the same results.  Because the
+ * forward writes nothing the backward recurrence reads before its dependency wait (W, dH),
+ * the recurrence is launched as a programmatic dependent of the forward: its clusters are
+ * scheduled and stage W_h^T while the forward's last steps run.  Returns the error codes of
+ * cfc_forward and cfc_backward; all arguments are checked before anything is launched.
+ */
+int cfc_forward_backward(const float* u, const float* h0, const float* W, const float* b,
+                         const float* ts, const float* dH, int B, int K, int C, int n_x,
+                         float* H, float* cache, float* dW, float* db, float* du, float* dh0,
+                         void* ws, size_t ws_bytes, int dw_mode, cfc_stream_t stream);
+
+/*
  * cfc_backward_recurrence -- the first stage of cfc_backward alone: the reverse-time
  * recurrence, writing the pre-activation gradients and dh0.
  *   dH, W, ts, cache   as for cfc_backward

@@ -22,7 +22,7 @@ CFC_DW_SIMT_FP32 = 2
 EXPORTED = ("cfc_workspace_bytes", "cfc_forward", "cfc_backward", "cfc_backward_recurrence",
             "cfc_weight_grad", "reduce_axis0", "cfc_error_string", "cfc_device_status",
             "cfc_backward_noalloc", "cfc_input_projection", "cfc_forward_recurrence",
-            "cfc_step_launches")
+            "cfc_step_launches", "cfc_forward_backward")
 CFC_ERR_SCRATCH_LIMIT = -10
 NOALLOC_SCRATCH_BYTES = 32 << 20  # size of cfc_backward_noalloc's built-in device scratch
 
@@ -52,6 +52,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.cfc_forward.restype = i
     lib.cfc_backward.argtypes = [vp] * 7 + [i] * 4 + [vp] * 5 + [sz, i, vp]
     lib.cfc_backward.restype = i
+    lib.cfc_forward_backward.argtypes = [vp] * 6 + [i] * 4 + [vp] * 7 + [sz, i, vp]
+    lib.cfc_forward_backward.restype = i
     lib.cfc_backward_recurrence.argtypes = [vp] * 4 + [i] * 4 + [vp, vp, vp]
     lib.cfc_backward_recurrence.restype = i
     lib.cfc_weight_grad.argtypes = [vp] * 5 + [i] * 4 + [vp] * 4 + [sz, i, vp]
@@ -172,6 +174,27 @@ def cfc_backward(dH, u, h0, W, ts, H, cache, dW, db, du, dh0, ws,
         _ptr(db, "db", (4, C)), _ptr(du, "du", (K, B, n_x)), _ptr(dh0, "dh0", (B, C)),
         ctypes.c_void_p(ws.data_ptr()), ws.numel(), dw_mode, _stream(stream))
     _check("cfc_backward", rc)
+
+
+def cfc_forward_backward(u, h0, W, b, ts, dH, H, cache, dW, db, du, dh0, ws,
+                         dw_mode: int = CFC_DW_ACCURATE, stream=None) -> None:
+    """One training step: cfc_forward then cfc_backward in one call (the backward recurrence
+    launched as a dependent of the forward)."""
+    K, B, n_x = u.shape
+    C = h0.shape[1]
+    n_in = n_x + C
+    import torch
+
+    if ws.dtype != torch.uint8 or not ws.is_cuda or not ws.is_contiguous():
+        raise ValueError("ws must be a contiguous uint8 CUDA tensor")
+    rc = load().cfc_forward_backward(
+        _ptr(u, "u", (K, B, n_x)), _ptr(h0, "h0", (B, C)), _ptr(W, "W", (4, C, n_in)),
+        _ptr(b, "b", (4, C)), _ptr(ts, "ts", (K, B)), _ptr(dH, "dH", (K, B, C)), B, K, C, n_x,
+        _ptr(H, "H", (K, B, C)), _ptr(cache, "cache", (K, B, 3, C)),
+        _ptr(dW, "dW", (4, C, n_in)), _ptr(db, "db", (4, C)), _ptr(du, "du", (K, B, n_x)),
+        _ptr(dh0, "dh0", (B, C)), ctypes.c_void_p(ws.data_ptr()), ws.numel(), dw_mode,
+        _stream(stream))
+    _check("cfc_forward_backward", rc)
 
 
 def cfc_backward_recurrence(dH, W, ts, cache, d_pre, dh0, stream=None) -> None:

@@ -116,12 +116,13 @@ int max_clusters(DeviceState& st, int kind, int variant, int CS, size_t smem, in
 // else the largest that fits at all.  Results never depend on R (each row's arithmetic is the
 // same whatever the grouping).
 int plan_rows(DeviceState& st, int kind, int variant, int CS, int B, int n_x, int* R_out,
-              size_t* smem_out, int* clusters_out) {
+              size_t* smem_out, int* clusters_out, size_t min_smem = 0) {
   int best_R = 0;
   size_t best_smem = 0;
   const int r_max = (kind == 0) ? cfc::kMaxFwdRows : cfc::kMaxRowsPerCluster;
   for (int R = 1; R <= r_max; R *= 2) {
-    const size_t smem = (kind == 0) ? cfc::fwd_smem_bytes(R, CS) : cfc::bwd_smem_bytes(R, CS);
+    size_t smem = (kind == 0) ? cfc::fwd_smem_bytes(R, CS) : cfc::bwd_smem_bytes(R, CS);
+    if (smem < min_smem) smem = min_smem;
     int n = 0;
     // Each row count has its own kernel (and occupancy) up to four rows; the backward ring
     // kernel serves every larger count.
@@ -156,6 +157,11 @@ struct BwdLayout {
 // 3.17 ms, while at B*K = 2048 (16 tiles) it was slower than dW, merge, split du (31.6 against
 // 26.3 us).
 constexpr int kDualMinDuTiles = 64;
+
+// Shared memory of a BPTT CTA launched as a dependent of the forward: more than half of an
+// SM's 228 KB (so two BPTT CTAs cannot be packed onto one SM for the whole recurrence) and
+// little enough to sit beside a forward CTA of 32 channels per CTA up to 128 channels.
+constexpr size_t kDependentBwdSmem = 116 * 1024;
 
 BwdLayout bwd_layout(int B, int K, int C, int n_x) {
   BwdLayout L;
@@ -259,6 +265,37 @@ int forward_recurrence(const float* h0, const float* W, const float* ts, int B, 
                  CFC_ERR_LAUNCH_FAILED);
 }
 
+// The BPTT recurrence.  As a dependent launch (pdl) it may be scheduled while the previous
+// kernel runs: it stages W_h^T and then waits for that kernel before it reads dH or the cache,
+// so a dependent launch is only for a predecessor that writes neither W nor dH.  Its shared
+// memory is then padded past half an SM, so that two BPTT CTAs never share one SM.
+int backward_recurrence(const float* dH, const float* W, const float* ts, const float* cache,
+                        int B, int K, int C, int n_x, float* d_pre, float* dh0,
+                        cfc_stream_t stream, bool pdl) {
+  int rc = check_dims(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (!dH || !W || !ts || !cache || !d_pre || !dh0) return CFC_ERR_NULL_PTR;
+  if (!aligned16(dH) || !aligned16(W) || !aligned16(ts) || !aligned16(cache) ||
+      !aligned16(d_pre) || !aligned16(dh0))
+    return CFC_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != CFC_OK) return rc;
+  cfc::BwdParams p;
+  p.dH = dH; p.W = W; p.ts = ts; p.cache = cache; p.d_pre = d_pre; p.dh0 = dh0;
+  p.status = st->status;
+  p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
+  p.CS = cluster_size_for(C, cfc::kBwdChanPerCta);
+  size_t smem = 0;
+  int n_clusters = 0;
+  rc = plan_rows(*st, 1, 0, p.CS, B, n_x, &p.R, &smem, &n_clusters,
+                 pdl ? kDependentBwdSmem : 0);
+  if (rc != CFC_OK) return rc;
+  return cuda_rc(cfc::bwd_launch(p, n_clusters, smem, static_cast<cudaStream_t>(stream), pdl),
+                 CFC_ERR_LAUNCH_FAILED);
+}
+
 }  // namespace
 
 extern "C" {
@@ -307,27 +344,7 @@ int cfc_step_launches(int B, int K, int C, int n_x, int dw_mode, int with_du, in
 int cfc_backward_recurrence(const float* dH, const float* W, const float* ts,
                             const float* cache, int B, int K, int C, int n_x, float* d_pre,
                             float* dh0, cfc_stream_t stream) {
-  int rc = check_dims(B, K, C, n_x);
-  if (rc != CFC_OK) return rc;
-  if (!dH || !W || !ts || !cache || !d_pre || !dh0) return CFC_ERR_NULL_PTR;
-  if (!aligned16(dH) || !aligned16(W) || !aligned16(ts) || !aligned16(cache) ||
-      !aligned16(d_pre) || !aligned16(dh0))
-    return CFC_ERR_MISALIGNED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  DeviceState* st = nullptr;
-  rc = device_state(&st);
-  if (rc != CFC_OK) return rc;
-  cfc::BwdParams p;
-  p.dH = dH; p.W = W; p.ts = ts; p.cache = cache; p.d_pre = d_pre; p.dh0 = dh0;
-  p.status = st->status;
-  p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
-  p.CS = cluster_size_for(C, cfc::kBwdChanPerCta);
-  size_t smem = 0;
-  int n_clusters = 0;
-  rc = plan_rows(*st, 1, 0, p.CS, B, n_x, &p.R, &smem, &n_clusters);
-  if (rc != CFC_OK) return rc;
-  return cuda_rc(cfc::bwd_launch(p, n_clusters, smem, static_cast<cudaStream_t>(stream), false),
-                 CFC_ERR_LAUNCH_FAILED);
+  return backward_recurrence(dH, W, ts, cache, B, K, C, n_x, d_pre, dh0, stream, false);
 }
 
 }  // extern "C"
@@ -434,6 +451,31 @@ int cfc_backward(const float* dH, const float* u, const float* h0, const float* 
   if (ws_bytes < L.total) return CFC_ERR_WS_TOO_SMALL;
   float* d_pre = reinterpret_cast<float*>(static_cast<char*>(ws) + L.d_pre_off);
   rc = cfc_backward_recurrence(dH, W, ts, cache, B, K, C, n_x, d_pre, dh0, stream);
+  if (rc != CFC_OK) return rc;
+  return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode, stream,
+                     true);
+}
+
+int cfc_forward_backward(const float* u, const float* h0, const float* W, const float* b,
+                         const float* ts, const float* dH, int B, int K, int C, int n_x,
+                         float* H, float* cache, float* dW, float* db, float* du, float* dh0,
+                         void* ws, size_t ws_bytes, int dw_mode, cfc_stream_t stream) {
+  int rc = check_dims(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (dw_mode != CFC_DW_ACCURATE && dw_mode != CFC_DW_SIMT_FP32) return CFC_ERR_INVALID_ARG;
+  if (!u || !h0 || !W || !b || !ts || !dH || !H || !cache || !dW || !db || !dh0 || !ws)
+    return CFC_ERR_NULL_PTR;
+  if (!aligned16(u) || !aligned16(h0) || !aligned16(W) || !aligned16(b) || !aligned16(ts) ||
+      !aligned16(dH) || !aligned16(H) || !aligned16(cache) || !aligned16(dW) ||
+      !aligned16(db) || (du && !aligned16(du)) || !aligned16(dh0) || !aligned16(ws))
+    return CFC_ERR_MISALIGNED;
+  const BwdLayout L = bwd_layout(B, K, C, n_x);
+  if (ws_bytes < L.total) return CFC_ERR_WS_TOO_SMALL;
+  rc = cfc_forward(u, h0, W, b, ts, B, K, C, n_x, H, cache, stream);
+  if (rc != CFC_OK) return rc;
+  // The forward writes only H and cache, which the BPTT reads after its dependency wait.
+  float* d_pre = reinterpret_cast<float*>(static_cast<char*>(ws) + L.d_pre_off);
+  rc = backward_recurrence(dH, W, ts, cache, B, K, C, n_x, d_pre, dh0, stream, true);
   if (rc != CFC_OK) return rc;
   return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode, stream,
                      true);

@@ -139,7 +139,11 @@ __device__ __forceinline__ void load_step_regs(const float* dHp, const float* cp
 // RT = 1, 2, 4: rows per cluster fixed at compile time, inputs prefetched into registers.
 // RT = 0: p.R rows (any count), inputs through the cp.async ring.
 template <int CS, int RT>
-__global__ void __launch_bounds__(kRecThreads, CS >= 4 ? 1 : 2) cfc_bwd_kernel(const BwdParams p) {
+// Two CTAs per SM fit (128 registers) wherever the variant allows it without spilling, so a
+// BPTT CTA launched as a dependent of the forward can stage its weights beside a running
+// forward CTA.
+__global__ void __launch_bounds__(kRecThreads, (CS >= 8 || (CS == 4 && (RT == 0 || RT == 4))) ? 1 : 2)
+    cfc_bwd_kernel(const BwdParams p) {
   using S = BwdShape<CS>;
   extern __shared__ __align__(16) float smem[];
   const int R = RT > 0 ? RT : p.R;

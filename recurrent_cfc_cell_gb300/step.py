@@ -1,7 +1,8 @@
 """One CfC K-loop training step (forward + BPTT + gradients) on the current CUDA device.
 
 ``KLoopStep`` owns the outputs and the workspace (allocated once through PyTorch), runs
-cfc_forward then cfc_backward on one stream, and can capture both into a CUDA graph so a step
+cfc_forward_backward (cfc_forward then cfc_backward) on one stream, and can capture it into a
+CUDA graph so a step
 is a single graph replay (the spec's "CUDA Graph capture / replay" of the training step,
 page "K-loop Parallelization -- Block-per-Batch Kernel Refactor", section "Trainer Wiring").
 """
@@ -58,9 +59,12 @@ class KLoopStep:
                           stream=stream)
 
     def run(self, stream=None) -> None:
-        """Forward then backward, enqueued on ``stream`` (default: current stream)."""
-        self.forward(stream)
-        self.backward(stream)
+        """Forward then backward in one cfc_forward_backward call, enqueued on ``stream``
+        (default: current stream)."""
+        i = self.inputs
+        _lib.cfc_forward_backward(i["u"], i["h0"], i["W"], i["b"], i["ts"], i["dH"], self.H,
+                                  self.cache, self.dW, self.db, self.du, self.dh0, self.ws,
+                                  self.dw_mode, stream=stream)
 
     # ---- host staging: one pinned buffer of inputs in, one of gradients out ----------------
     @staticmethod

@@ -108,6 +108,34 @@ def test_null_and_misaligned_pointers(lib):
     assert lib.reduce_axis0(f, 4, -3, f, None) == INVALID_DIM
 
 
+def test_forward_backward_checks_every_argument_before_launching(lib):
+    """The one-call training step rejects a bad argument of either half before it launches
+    the forward (no GPU is touched on these paths)."""
+    f = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10004)
+    rc, need = ws_bytes(lib, 4, 8, 32, 16)
+    assert rc == OK
+    ins = [f] * 6                   # u, h0, W, b, ts, dH
+    outs = [f] * 7                  # H, cache, dW, db, du, dh0, ws
+    def call(i, o, dims=(4, 8, 32, 16), nbytes=need, mode=0):
+        return lib.cfc_forward_backward(*i, *dims, *o, nbytes, mode, None)
+    for k in range(6):
+        a = list(ins)
+        a[k] = None
+        assert call(a, outs) == NULL_PTR
+        a[k] = odd
+        assert call(a, outs) == MISALIGNED
+    for k in (0, 1, 2, 3, 5, 6):    # du (index 4) may be NULL
+        o = list(outs)
+        o[k] = None
+        assert call(ins, o) == NULL_PTR
+        o[k] = odd
+        assert call(ins, o) == MISALIGNED
+    assert call(ins, outs, dims=(4, 8, 257, 16)) == INVALID_DIM
+    assert call(ins, outs, mode=7) == INVALID_ARG
+    assert call(ins, outs, nbytes=need - 1) == WS_TOO_SMALL
+
+
 def test_short_workspace(lib):
     f = ctypes.c_void_p(0x10000)
     rc, need = ws_bytes(lib, 4, 8, 32, 16)

@@ -92,6 +92,34 @@ def test_host_staged_graph_step_parity():
     assert n_out == 4 * (4 * 72 * 84 + 4 * 72 + 9 * 6 * 12 + 6 * 72)
 
 
+@pytest.mark.parametrize("shape", [dict(B=32, K=64, n_x=48, C=128), dict(B=7, K=11, n_x=13, C=100),
+                                   dict(B=40, K=9, n_x=64, C=256)],
+                         ids=lambda s: "B{B}_K{K}_nx{n_x}_C{C}".format(**s))
+def test_forward_backward_is_forward_then_backward(shape):
+    """cfc_forward_backward (BPTT launched as a dependent of the forward) gives bitwise the
+    results of cfc_forward followed by cfc_backward, and matches the oracle."""
+    import torch
+
+    from recurrent_cfc_cell_gb300 import build
+    from recurrent_cfc_cell_gb300.step import KLoopStep, to_device
+
+    build.build()
+    inp = inputs.make_inputs(inputs.custom(seed=23, **shape))
+    d = to_device(inp)
+    B, K, C, n_x = shape["B"], shape["K"], shape["C"], shape["n_x"]
+    a = KLoopStep(B, K, C, n_x).bind(**d)
+    a.forward()
+    a.backward()
+    b = KLoopStep(B, K, C, n_x).bind(**d)
+    b.run()
+    torch.cuda.synchronize()
+    for name, x in a.outputs().items():
+        y = b.outputs()[name]
+        assert torch.equal(x, y), name
+    out = {k: v.cpu().numpy() for k, v in b.outputs().items()}
+    assert_parity(out, oracle_ref(inp))
+
+
 def test_graph_replay_parity():
     inp = inputs.make_inputs(inputs.CONFIGS[1])
     assert_parity(run_gpu(inp, graph=True), oracle_ref(inp))
