@@ -158,6 +158,11 @@ struct BwdLayout {
 // 26.3 us).
 constexpr int kDualMinDuTiles = 64;
 
+// Rows (B*K) from which the input projection runs on the tensor cores (bf16 hi/lo split,
+// tc_gemm_kernel<ProjProblem>) rather than on the CUDA cores (inproj_kernel): below it the
+// CUDA-core kernel's single short wave is faster than the tensor-core kernel's set-up.
+constexpr int kTcProjMinRows = 8192;
+
 // Shared memory of a BPTT CTA launched as a dependent of the forward: more than half of an
 // SM's 228 KB (so two BPTT CTAs cannot be packed onto one SM for the whole recurrence) and
 // little enough to sit beside a forward CTA of 32 channels per CTA up to 128 channels.
@@ -230,8 +235,13 @@ int cfc_input_projection(const float* u, const float* W, const float* b, int B, 
   DeviceState* st = nullptr;
   rc = device_state(&st);
   if (rc != CFC_OK) return rc;
-  return cuda_rc(cfc::inproj_launch(u, W, b, B * K, C, n_x, H, cache,
-                                    static_cast<cudaStream_t>(stream), false),
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (B * K >= kTcProjMinRows) {
+    const cfc::TcPlan pl = cfc::proj_tc_plan(B, K, C, n_x);
+    return cuda_rc(cfc::proj_tc_launch(pl, u, W, b, B, K, C, n_x, H, cache, st->status, s, false),
+                   CFC_ERR_LAUNCH_FAILED);
+  }
+  return cuda_rc(cfc::inproj_launch(u, W, b, B * K, C, n_x, H, cache, s, false),
                  CFC_ERR_LAUNCH_FAILED);
 }
 

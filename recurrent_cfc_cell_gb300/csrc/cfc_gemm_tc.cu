@@ -37,7 +37,6 @@ namespace {
 
 constexpr int kTcM = 128;          // rows of the output tile (UMMA M)
 constexpr int kTcK = 64;           // reduction rows per stage (128 bytes of bf16)
-constexpr int kStages = 2;
 constexpr int kConv = 256;         // converter / epilogue threads (warps 0-7)
 constexpr int kTcThreads = kConv + 32;
 
@@ -48,6 +47,9 @@ struct TcParams {
   const float* h0;     // [B][C]
   const float* W;      // [4C][n_in]
   float* out;          // dW partials [S][4C][n_in]  or  du [BK][n_x]
+  const float* bias;   // projection: b [4C]
+  float* xh;           // projection: X of gate ff1 -> H [BK][C]
+  float* xcache;       // projection: X of gates ff2, ta, tb -> cache [BK][3][C]
   int* status;
   int B, BK, C, n_x, n_in;
   int rows, cols;      // output rows / columns of the GEMM (dW: 4C x n_in; du: BK x n_x)
@@ -75,6 +77,31 @@ __device__ __forceinline__ void store_split_chunk(uint8_t* hi_tile, uint8_t* lo_
   *reinterpret_cast<uint4*>(hi_tile + off) =
       make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]),
                  pack_bf16x2(h[6], h[7]));
+  *reinterpret_cast<uint4*>(lo_tile + off) =
+      make_uint4(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]), pack_bf16x2(l[4], l[5]),
+                 pack_bf16x2(l[6], l[7]));
+}
+
+// Split 8 fp32 values into three bf16 terms x = hi + mid + lo (8 significand bits each, so the
+// three carry all 24 of fp32; each difference is exact in fp32) and store the three chunks.
+__device__ __forceinline__ void store_split3_chunk(uint8_t* hi_tile, uint8_t* mid_tile,
+                                                   uint8_t* lo_tile, int row, int kchunk,
+                                                   const float (&v)[8]) {
+  __nv_bfloat16 h[8], m[8], l[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    h[i] = __float2bfloat16_rn(v[i]);
+    const float r1 = v[i] - __bfloat162float(h[i]);
+    m[i] = __float2bfloat16_rn(r1);
+    l[i] = __float2bfloat16_rn(r1 - __bfloat162float(m[i]));
+  }
+  const uint32_t off = sw128_offset(row, kchunk * 8);
+  *reinterpret_cast<uint4*>(hi_tile + off) =
+      make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]),
+                 pack_bf16x2(h[6], h[7]));
+  *reinterpret_cast<uint4*>(mid_tile + off) =
+      make_uint4(pack_bf16x2(m[0], m[1]), pack_bf16x2(m[2], m[3]), pack_bf16x2(m[4], m[5]),
+                 pack_bf16x2(m[6], m[7]));
   *reinterpret_cast<uint4*>(lo_tile + off) =
       make_uint4(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]), pack_bf16x2(l[4], l[5]),
                  pack_bf16x2(l[6], l[7]));
@@ -178,8 +205,29 @@ __device__ __forceinline__ void convert_quads(int n_quads, int row_base, int k_b
   }
 }
 
+// Output columns n .. n+15 of row m (v[0..15]) into the row-major block p.out of split `split`.
+struct RowMajorOut {
+  static __device__ __forceinline__ void store16(const TcParams& p, int split, int m, int n,
+                                                 const float (&v)[16]) {
+    float* dst = p.out + (static_cast<size_t>(split) * p.rows + m) * p.cols;
+    const bool vec_out = (p.cols % 4) == 0;
+#pragma unroll
+    for (int c = 0; c < 16; c += 4) {
+      const int nc = n + c;
+      if (vec_out && nc + 3 < p.cols) {
+        *reinterpret_cast<float4*>(dst + nc) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (nc + e < p.cols) dst[nc + e] = v[c + e];
+      }
+    }
+  }
+};
+
 // Weight gradient: A = d_pre^T (rows m, reduction r), B = z^T (rows n, reduction r).
-struct DwProblem {
+struct DwProblem : RowMajorOut {
+  static constexpr int kTerms = 2, kStages = 2;
   static __device__ __forceinline__ void convert(const TcParams& p, uint8_t* a_hi, uint8_t* a_lo,
                                                  uint8_t* b_hi, uint8_t* b_lo, int m0, int n0,
                                                  int r0, int tid) {
@@ -193,7 +241,8 @@ struct DwProblem {
 // Input gradient: A = d_pre (rows r, reduction m: already K-major), B = W_u^T (rows k,
 // reduction m).  A items are (row, 8-entry chunk), two per thread at a time, loads first; a
 // quarter-warp covers the 8 chunks of a row.
-struct DuProblem {
+struct DuProblem : RowMajorOut {
+  static constexpr int kTerms = 2, kStages = 2;
   static __device__ __forceinline__ void load_row_chunk(const TcParams& p, int r, int m,
                                                         float (&v)[8]) {
     const int M = 4 * p.C;
@@ -222,6 +271,94 @@ struct DuProblem {
   }
 };
 
+// Input projection: A = u (rows r, reduction k < n_x: K-major as stored), B = W_u (rows n < 4C,
+// the first n_x columns of W: K-major as stored).  The epilogue adds the bias and hands X to
+// the recurrence in place: column n = g C + c of row r goes to H[r][c] (g = 0) or
+// cache[r][g - 1][c].
+//
+// Precision: X feeds the forward, whose tolerance (1e-5 of max|H|) the two-term split's
+// ~2^-17 per operand can exceed, so operands are split in three bf16 terms and the tile
+// product keeps hi*hi + hi*mid + mid*hi + hi*lo + lo*hi + mid*mid (six MMAs per 16-step; the
+// dropped terms are below 2^-24 of the product).  The reduction (n_x <= 512) is at most eight
+// 64-entry blocks, and one stage of six tiles fits in shared memory.
+struct ProjProblem {
+  static constexpr int kTerms = 3, kStages = 1;
+  // Entries k .. k+7 of a row of `width` valid values (zero beyond), as two float4 loads when
+  // the row start is 16-byte aligned.
+  static __device__ __forceinline__ void load8(const float* row, int k, int width, bool vec,
+                                               float (&v)[8]) {
+    if (vec && k + 8 <= width) {
+      const float4 q0 = __ldg(reinterpret_cast<const float4*>(row + k));
+      const float4 q1 = __ldg(reinterpret_cast<const float4*>(row + k + 4));
+      v[0] = q0.x; v[1] = q0.y; v[2] = q0.z; v[3] = q0.w;
+      v[4] = q1.x; v[5] = q1.y; v[6] = q1.z; v[7] = q1.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = (k + i < width) ? __ldg(row + k + i) : 0.f;
+    }
+  }
+  // Tiles t = 0, 1, 2 (hi, mid, lo) of A start at a_hi + t kTcM 128, those of B at
+  // b_hi + t n_tile 128 (a_lo / b_lo are the second ones).
+  static __device__ __forceinline__ void convert(const TcParams& p, uint8_t* a_hi, uint8_t* a_lo,
+                                                 uint8_t* b_hi, uint8_t* b_lo, int r0, int n0,
+                                                 int k0, int tid) {
+    const int M = 4 * p.C;
+    // (row, 8-entry chunk) items, two per thread at a time with both loads issued first.
+    for (int it = tid; it < kTcM * 8; it += 2 * kConv) {
+      const int it1 = it + kConv;  // kTcM * 8 is a multiple of 2 * kConv
+      float v0[8], v1[8];
+      const int ra = r0 + (it >> 3), rb = r0 + (it1 >> 3);
+      const int ka = k0 + 8 * (it & 7), kb = k0 + 8 * (it1 & 7);
+      load8(p.u + static_cast<size_t>(ra < p.BK ? ra : 0) * p.n_x, ka, ra < p.BK ? p.n_x : 0,
+            p.vec, v0);
+      load8(p.u + static_cast<size_t>(rb < p.BK ? rb : 0) * p.n_x, kb, rb < p.BK ? p.n_x : 0,
+            p.vec, v1);
+      store_split3_chunk(a_hi, a_lo, a_lo + kTcM * 128, it >> 3, it & 7, v0);
+      store_split3_chunk(a_hi, a_lo, a_lo + kTcM * 128, it1 >> 3, it1 & 7, v1);
+    }
+    for (int it = tid; it < p.n_tile * 8; it += 2 * kConv) {
+      const int it1 = it + kConv;
+      float v0[8], v1[8];
+      const int na = n0 + (it >> 3), nb = n0 + (it1 >> 3);
+      const int ka = k0 + 8 * (it & 7), kb = k0 + 8 * (it1 & 7);
+      load8(p.W + static_cast<size_t>(na < M ? na : 0) * p.n_in, ka, na < M ? p.n_x : 0, p.vec,
+            v0);
+      if (it1 < p.n_tile * 8)
+        load8(p.W + static_cast<size_t>(nb < M ? nb : 0) * p.n_in, kb, nb < M ? p.n_x : 0,
+              p.vec, v1);
+      store_split3_chunk(b_hi, b_lo, b_lo + p.n_tile * 128, it >> 3, it & 7, v0);
+      if (it1 < p.n_tile * 8)
+        store_split3_chunk(b_hi, b_lo, b_lo + p.n_tile * 128, it1 >> 3, it1 & 7, v1);
+    }
+  }
+  static __device__ __forceinline__ void store16(const TcParams& p, int, int r, int n,
+                                                 const float (&v)[16]) {
+    const int M = 4 * p.C, C = p.C;
+    if (p.vec && (C % 16) == 0 && n + 16 <= M) {
+      // The 16 columns lie in one gate and one 16-byte aligned run of channels.
+      const int g = n / C, c = n - g * C;
+      float* dst = (g == 0) ? p.xh + static_cast<size_t>(r) * C + c
+                            : p.xcache + (static_cast<size_t>(r) * 3 + (g - 1)) * C + c;
+#pragma unroll
+      for (int q = 0; q < 16; q += 4) {
+        const float4 b = __ldg(reinterpret_cast<const float4*>(p.bias + n + q));
+        *reinterpret_cast<float4*>(dst + q) =
+            make_float4(v[q] + b.x, v[q + 1] + b.y, v[q + 2] + b.z, v[q + 3] + b.w);
+      }
+      return;
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int col = n + e;
+      if (col >= M) continue;
+      const int g = col / C, c = col - g * C;
+      const float x = v[e] + __ldg(p.bias + col);
+      if (g == 0) p.xh[static_cast<size_t>(r) * C + c] = x;
+      else p.xcache[(static_cast<size_t>(r) * 3 + (g - 1)) * C + c] = x;
+    }
+  }
+};
+
 // One CTA's work: output tile `tile` (m-tile fastest) over reduction split `split`.
 template <class Problem>
 __device__ __forceinline__ void tc_gemm_body(const TcParams& p, int tile, int split) {
@@ -229,7 +366,9 @@ __device__ __forceinline__ void tc_gemm_body(const TcParams& p, int tile, int sp
   // 1024-byte aligned stage buffers (128-byte swizzle atoms), then the barriers.
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  const int stage_bytes = 2 * kTcM * 128 + 2 * p.n_tile * 128;
+  constexpr int kStages = Problem::kStages, kTerms = Problem::kTerms;
+  // Stage: kTerms A tiles [kTcM rows x 128 B], then kTerms B tiles [n_tile rows x 128 B].
+  const int stage_bytes = kTerms * (kTcM + p.n_tile) * 128;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + kStages * stage_bytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 1);
   const uint32_t full0 = smem_addr(&bars[0]);             // full[s]  = full0 + 8 s
@@ -274,8 +413,8 @@ __device__ __forceinline__ void tc_gemm_body(const TcParams& p, int tile, int sp
         ok = mbar_wait_bounded_cta(empty0 + 8u * s, ((i - kStages) / kStages) & 1u, p.status);
       if (!ok) break;
       uint8_t* st = base + s * stage_bytes;
-      Problem::convert(p, st, st + kTcM * 128, st + 2 * kTcM * 128,
-                       st + 2 * kTcM * 128 + p.n_tile * 128, m0, n0, (kb0 + i) * kTcK, tid);
+      Problem::convert(p, st, st + kTcM * 128, st + kTerms * kTcM * 128,
+                       st + kTerms * kTcM * 128 + p.n_tile * 128, m0, n0, (kb0 + i) * kTcK, tid);
       fence_proxy_async_smem();
       mbar_arrive(full0 + 8u * s);
     }
@@ -285,23 +424,11 @@ __device__ __forceinline__ void tc_gemm_body(const TcParams& p, int tile, int sp
     tc_fence_after_sync();
     const int quarter = warp & 3;  // TMEM lanes this warp may read
     const int m = m0 + 32 * quarter + lane;
-    float* dst = p.out + (static_cast<size_t>(split) * p.rows + m) * p.cols;
-    const bool vec_out = (p.cols % 4) == 0;
     for (int c0 = 16 * (warp >> 2); c0 < p.n_tile; c0 += 32) {
       float v[16];
       tmem_ld16(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + c0, v);
       if (!ok || m >= p.rows) continue;
-#pragma unroll
-      for (int c = 0; c < 16; c += 4) {
-        const int n = n0 + c0 + c;
-        if (vec_out && n + 3 < p.cols) {
-          *reinterpret_cast<float4*>(dst + n) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (n + e < p.cols) dst[n + e] = v[c + e];
-        }
-      }
+      Problem::store16(p, split, m, n0 + c0, v);
     }
   } else if (lane == 0) {
     // ---- MMA issuer ----
@@ -315,7 +442,7 @@ __device__ __forceinline__ void tc_gemm_body(const TcParams& p, int tile, int sp
       tc_fence_after_sync();
       const uint32_t st = smem_addr(base + s * stage_bytes);
       const uint32_t a_hi = st, a_lo = st + kTcM * 128;
-      const uint32_t b_hi = st + 2 * kTcM * 128, b_lo = b_hi + p.n_tile * 128;
+      const uint32_t b_hi = st + kTerms * kTcM * 128, b_lo = b_hi + p.n_tile * 128;
 #pragma unroll
       for (int j = 0; j < kTcK / 16; ++j) {
         const uint32_t koff = 32u * j;
@@ -323,6 +450,12 @@ __device__ __forceinline__ void tc_gemm_body(const TcParams& p, int tile, int sp
         acc = 1;
         umma_bf16(tmem, umma_desc_sw128(a_hi + koff), umma_desc_sw128(b_lo + koff), idesc, 1);
         umma_bf16(tmem, umma_desc_sw128(a_lo + koff), umma_desc_sw128(b_hi + koff), idesc, 1);
+        if constexpr (kTerms == 3) {  // a_lo / b_lo hold the mid terms; lo follows them
+          const uint32_t a_l3 = a_lo + kTcM * 128, b_l3 = b_lo + p.n_tile * 128;
+          umma_bf16(tmem, umma_desc_sw128(a_hi + koff), umma_desc_sw128(b_l3 + koff), idesc, 1);
+          umma_bf16(tmem, umma_desc_sw128(a_l3 + koff), umma_desc_sw128(b_hi + koff), idesc, 1);
+          umma_bf16(tmem, umma_desc_sw128(a_lo + koff), umma_desc_sw128(b_lo + koff), idesc, 1);
+        }
       }
       umma_commit(empty0 + 8u * s);  // stage reusable once these MMAs have read it
     }
@@ -353,7 +486,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_dual_kernel(const TcParams p
 }
 
 
-TcPlan tc_plan(int rows, int cols, int red, bool split) {
+TcPlan tc_plan(int rows, int cols, int red, bool split, int terms = 2, int stages = 2) {
   TcPlan pl;
   pl.n_tiles = (cols + 255) / 256;
   pl.n_tile = (((cols + pl.n_tiles - 1) / pl.n_tiles) + 15) & ~15;
@@ -367,7 +500,7 @@ TcPlan tc_plan(int rows, int cols, int red, bool split) {
   }                                  // on the sizes
   pl.kb_per_split = (pl.n_kb + s0 - 1) / s0;
   pl.splits = (pl.n_kb + pl.kb_per_split - 1) / pl.kb_per_split;
-  pl.smem = kStages * (2 * kTcM * 128 + 2 * pl.n_tile * 128) + 1024 + 128;
+  pl.smem = static_cast<size_t>(stages) * terms * (kTcM + pl.n_tile) * 128 + 1024 + 128;
   return pl;
 }
 
@@ -388,8 +521,11 @@ cudaError_t tc_prepare(int max_smem) {
   e = cudaFuncSetAttribute(tc_gemm_kernel<DuProblem>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            max_smem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(tc_dual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              max_smem);
+  e = cudaFuncSetAttribute(tc_dual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           max_smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(tc_gemm_kernel<ProjProblem>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
 }
 
 namespace {
@@ -432,6 +568,25 @@ cudaError_t du_tc_launch(const TcPlan& pl, const float* d_pre, const float* W, i
   c.stream = s;
   c.pdl = pdl;
   return launch(c, tc_gemm_kernel<DuProblem>, p);
+}
+
+TcPlan proj_tc_plan(int B, int K, int C, int n_x) {
+  return tc_plan(B * K, 4 * C, n_x, false, ProjProblem::kTerms, ProjProblem::kStages);
+}
+
+cudaError_t proj_tc_launch(const TcPlan& pl, const float* u, const float* W, const float* bias,
+                           int B, int K, int C, int n_x, float* H, float* cache, int* status,
+                           cudaStream_t s, bool pdl) {
+  TcParams p = make_params(pl, nullptr, B, K, C, n_x, status);
+  p.u = u; p.W = W; p.bias = bias; p.xh = H; p.xcache = cache;
+  p.rows = B * K; p.cols = 4 * C; p.red = n_x;
+  LaunchCfg c;
+  c.grid = dim3(pl.m_tiles * pl.n_tiles, pl.splits, 1);
+  c.block = dim3(kTcThreads, 1, 1);
+  c.smem = pl.smem;
+  c.stream = s;
+  c.pdl = pdl;
+  return launch(c, tc_gemm_kernel<ProjProblem>, p);
 }
 
 cudaError_t dwdu_tc_launch(const TcPlan& pw, const TcPlan& pu, const float* d_pre,

@@ -82,6 +82,12 @@ cudaError_t dw_tc_launch(const TcPlan& pl, const float* d_pre, const float* u, c
 // du, or (when pl.splits > 1) its partial blocks [splits][B*K][n_x].
 cudaError_t du_tc_launch(const TcPlan& pl, const float* d_pre, const float* W, int B, int K,
                          int C, int n_x, float* du, int* status, cudaStream_t s, bool pdl);
+// The input projection X = W_u u + b on the tensor cores (bf16 hi/lo split), written in place
+// into H and cache like inproj_launch.
+TcPlan proj_tc_plan(int B, int K, int C, int n_x);
+cudaError_t proj_tc_launch(const TcPlan& pl, const float* u, const float* W, const float* bias,
+                           int B, int K, int C, int n_x, float* H, float* cache, int* status,
+                           cudaStream_t s, bool pdl);
 // Both in one launch: the dW partials of plan pw and du itself (plan pu must be unsplit).
 TcPlan du_tc_plan_unsplit(int B, int K, int C, int n_x);
 cudaError_t dwdu_tc_launch(const TcPlan& pw, const TcPlan& pu, const float* d_pre,

@@ -32,6 +32,8 @@ RAGGED = [
     dict(B=300, K=28, n_x=48, C=128),  # 8 rows per cluster, part-filled last cluster; dW and
                                        # du in one launch with a ragged last row tile
     dict(B=200, K=6, n_x=64, C=256),   # 8-row forward and 16-row BPTT clusters of 8 CTAs
+    dict(B=130, K=64, n_x=13, C=100),  # tensor-core projection: odd n_x (scalar loads), C not
+                                       # a multiple of 16 (element-wise epilogue), ragged tiles
 ]
 
 
