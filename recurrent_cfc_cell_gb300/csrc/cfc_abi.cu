@@ -147,15 +147,17 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 struct BwdLayout {
   size_t d_pre_off, d_pre_bytes, part_off, part_bytes, total;
   int S_simt;          // split count of the CUDA-core contraction
-  cfc::TcPlan tc;      // plan of the tensor-core weight-gradient contraction
-  cfc::TcPlan tu;      // plan of the tensor-core input-gradient contraction
-  bool dual;           // du in the dW launch (unsplit) rather than after the dW merge
+  cfc::TcPlan tc;      // plan of the tensor-core weight-gradient contraction (no du)
+  cfc::TcPlan tu;      // plan of du beside the dW splits (dual: unsplit, written directly)
+  bool dual;           // large B*K: du unsplit in the dW launch, one merge
+  cfc::TcPlan pw, pu;  // small B*K: dW and du splits sized together for one launch, one merge
+  size_t pu_off;       // offset (floats) of the du partials after the dW partials
 };
 
 // Row tiles (of 128) from which unsplit du tiles keep enough SMs busy beside the dW splits:
 // measured on GB300, the combined launch took the gradient stage of B*K = 262144 from 3.85 to
-// 3.17 ms, while at B*K = 2048 (16 tiles) it was slower than dW, merge, split du (31.6 against
-// 26.3 us).
+// 3.17 ms, while at B*K = 2048 (16 tiles) unsplit du was slower than dW, merge, split du (31.6
+// against 26.3 us); below it both are split, sized together (dwdu_tc_plans).
 constexpr int kDualMinDuTiles = 64;
 
 // Rows (B*K) from which the input projection runs on the tensor cores (bf16 hi/lo split,
@@ -176,16 +178,18 @@ BwdLayout bwd_layout(int B, int K, int C, int n_x) {
   L.S_simt = cfc::dw_simt_splits(static_cast<int>(BK));
   L.tc = cfc::dw_tc_plan(B, K, C, n_x);
   // With enough rows du runs unsplit beside the dW splits (one launch, du written directly);
-  // otherwise it runs after the dW merge, split over 4C, its partials reusing the dW area.
+  // otherwise both run split in one launch, sized together, and one launch merges both.
   L.tu = cfc::du_tc_plan_unsplit(B, K, C, n_x);
   L.dual = L.tu.m_tiles >= kDualMinDuTiles;
-  if (!L.dual) L.tu = cfc::du_tc_plan(B, K, C, n_x);
+  cfc::dwdu_tc_plans(B, K, C, n_x, &L.pw, &L.pu);
+  const size_t pitch = cfc::dw_tc_pitch(n_x + C);
   size_t part = static_cast<size_t>(L.S_simt) * 4 * C * (n_x + C);
-  const size_t ptc = static_cast<size_t>(L.tc.splits) * 4 * C * cfc::dw_tc_pitch(n_x + C);
+  const size_t ptc = static_cast<size_t>(L.tc.splits) * 4 * C * pitch;
   if (ptc > part) part = ptc;
-  if (L.tu.splits > 1) {
-    const size_t pu = static_cast<size_t>(L.tu.splits) * BK * n_x;
-    if (pu > part) part = pu;
+  L.pu_off = static_cast<size_t>(L.pw.splits) * 4 * C * pitch;
+  if (!L.dual) {
+    const size_t ppair = L.pu_off + (L.pu.splits > 1 ? static_cast<size_t>(L.pu.splits) * BK * n_x : 0);
+    if (ppair > part) part = ppair;
   }
   L.part_off = align256(L.d_pre_bytes);
   L.part_bytes = part * sizeof(float);
@@ -339,13 +343,12 @@ int cfc_step_launches(int B, int K, int C, int n_x, int dw_mode, int with_du, in
   if (!launches) return CFC_ERR_NULL_PTR;
   // forward: projection + recurrence; backward: recurrence, dW contraction + its reduction
   // (which also yields db with the tensor cores; a separate db reduction otherwise), and du
-  // (inside the dW launch for large B*K with the tensor cores, else a launch of its own plus
-  // its reduction when the plan splits it).
+  // (inside the dW launch, and its partials inside the dW merge, with the tensor cores; a
+  // launch of its own otherwise).
   int n = 2 + 1 + 2 + (dw_mode == CFC_DW_ACCURATE ? 0 : 1);
   if (with_du) {
     const BwdLayout L = bwd_layout(B, K, C, n_x);
     if (dw_mode != CFC_DW_ACCURATE) n += 1;
-    else if (!L.dual) n += (L.tu.splits > 1) ? 2 : 1;
   }
   *launches = n;
   return CFC_OK;
@@ -394,6 +397,21 @@ int weight_grad(const float* d_pre, const float* u, const float* h0, const float
     rc = cuda_rc(cfc::dwdu_tc_launch(L.tc, L.tu, d_pre, u, H, h0, W, B, K, C, n_x, partial, du,
                                      st->status, s, first_pdl),
                  CFC_ERR_LAUNCH_FAILED);
+  } else if (du) {
+    // dW and du partials from one grid, then one launch merging both.
+    float* pu = L.pu.splits > 1 ? partial + L.pu_off : du;
+    rc = cuda_rc(cfc::dwdu_tc_launch(L.pw, L.pu, d_pre, u, H, h0, W, B, K, C, n_x, partial, pu,
+                                     st->status, s, first_pdl),
+                 CFC_ERR_LAUNCH_FAILED);
+    if (rc != CFC_OK) return rc;
+    const int pitch = cfc::dw_tc_pitch(N);
+    if (L.pu.splits > 1)
+      return cuda_rc(cfc::reduce_axis0_pair_launch(partial, L.pw.splits, M * pitch, pitch, N, dW,
+                                                   db, pu, L.pu.splits, BK * n_x, du, s, true),
+                     CFC_ERR_LAUNCH_FAILED);
+    return cuda_rc(cfc::reduce_axis0_rows_launch(partial, L.pw.splits, M * pitch, pitch, N, dW,
+                                                 db, s, true),
+                   CFC_ERR_LAUNCH_FAILED);
   } else {
     S = L.tc.splits;
     rc = cuda_rc(cfc::dw_tc_launch(L.tc, d_pre, u, H, h0, B, K, C, n_x, partial, st->status, s,
@@ -413,23 +431,8 @@ int weight_grad(const float* d_pre, const float* u, const float* h0, const float
                  CFC_ERR_LAUNCH_FAILED);
   }
   if (rc != CFC_OK) return rc;
-  if (du && dw_mode == CFC_DW_SIMT_FP32) {
+  if (du && dw_mode == CFC_DW_SIMT_FP32)
     rc = cuda_rc(cfc::du_simt_launch(d_pre, W, BK, C, n_x, du, s, true), CFC_ERR_LAUNCH_FAILED);
-  } else if (du && !L.dual) {
-    if (L.tu.splits == 1) {
-      rc = cuda_rc(cfc::du_tc_launch(L.tu, d_pre, W, B, K, C, n_x, du, st->status, s, true),
-                   CFC_ERR_LAUNCH_FAILED);
-    } else {
-      // The du partials reuse the dW partial area: the dW reduction above has read it, and
-      // that reduction completes before this kernel passes its grid-dependency wait.
-      rc = cuda_rc(
-          cfc::du_tc_launch(L.tu, d_pre, W, B, K, C, n_x, partial, st->status, s, true),
-          CFC_ERR_LAUNCH_FAILED);
-      if (rc == CFC_OK)
-        rc = cuda_rc(cfc::reduce_axis0_launch(partial, L.tu.splits, BK * n_x, du, s, true),
-                     CFC_ERR_LAUNCH_FAILED);
-    }
-  }
   return rc;
 }
 

@@ -475,14 +475,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcParams p
 }
 
 // Both contractions in one grid: the first n_w CTAs take the weight-gradient tiles and splits,
-// the rest the input-gradient tiles (which run unsplit).  They read the same d_pre and write
-// disjoint outputs, so one launch replaces two dependent ones.
+// the rest the input-gradient tiles and splits.  They read the same d_pre and write disjoint
+// outputs, so one launch replaces two dependent ones.
 __global__ void __launch_bounds__(kTcThreads, 1) tc_dual_kernel(const TcParams pw,
                                                                 const TcParams pu, int n_w) {
   const int b = blockIdx.x;
   const int tiles_w = pw.m_tiles * ((pw.cols + pw.n_tile - 1) / pw.n_tile);
+  const int tiles_u = pu.m_tiles * ((pu.cols + pu.n_tile - 1) / pu.n_tile);
   if (b < n_w) tc_gemm_body<DwProblem>(pw, b % tiles_w, b / tiles_w);
-  else tc_gemm_body<DuProblem>(pu, b - n_w, 0);
+  else tc_gemm_body<DuProblem>(pu, (b - n_w) % tiles_u, (b - n_w) / tiles_u);
 }
 
 
@@ -512,6 +513,24 @@ TcPlan dw_tc_plan(int B, int K, int C, int n_x) {
 TcPlan du_tc_plan(int B, int K, int C, int n_x) { return tc_plan(B * K, n_x, 4 * C, true); }
 TcPlan du_tc_plan_unsplit(int B, int K, int C, int n_x) {
   return tc_plan(B * K, n_x, 4 * C, false);
+}
+
+void dwdu_tc_plans(int B, int K, int C, int n_x, TcPlan* pw, TcPlan* pu) {
+  // One k-block count per CTA for both, the smallest whose CTAs fit a fixed budget of one
+  // wave (a constant, not the device's SM count, so the split -- hence the summation order --
+  // depends only on the sizes).
+  constexpr int kBudget = 148;
+  *pw = tc_plan(4 * C, dw_tc_pitch(n_x + C), B * K, false);
+  *pu = tc_plan(B * K, n_x, 4 * C, false);
+  const int tw = pw->m_tiles * pw->n_tiles, tu = pu->m_tiles * pu->n_tiles;
+  int kbps = 1;
+  const int kmax = pw->n_kb > pu->n_kb ? pw->n_kb : pu->n_kb;
+  while (kbps < kmax && tw * ((pw->n_kb + kbps - 1) / kbps) + tu * ((pu->n_kb + kbps - 1) / kbps) > kBudget)
+    ++kbps;
+  for (TcPlan* pl : {pw, pu}) {
+    pl->kb_per_split = kbps < pl->n_kb ? kbps : pl->n_kb;
+    pl->splits = (pl->n_kb + pl->kb_per_split - 1) / pl->kb_per_split;
+  }
 }
 
 cudaError_t tc_prepare(int max_smem) {
@@ -593,7 +612,6 @@ cudaError_t dwdu_tc_launch(const TcPlan& pw, const TcPlan& pu, const float* d_pr
                            const float* u, const float* H, const float* h0, const float* W, int B,
                            int K, int C, int n_x, float* partial, float* du, int* status,
                            cudaStream_t s, bool pdl) {
-  if (pu.splits != 1) return cudaErrorInvalidValue;  // du is written directly
   TcParams a = make_params(pw, d_pre, B, K, C, n_x, status);
   a.u = u; a.H = H; a.h0 = h0; a.out = partial;
   a.rows = 4 * C; a.cols = dw_tc_pitch(n_x + C); a.red = B * K;
@@ -602,7 +620,7 @@ cudaError_t dwdu_tc_launch(const TcPlan& pw, const TcPlan& pu, const float* d_pr
   b.rows = B * K; b.cols = n_x; b.red = 4 * C;
   const int n_w = pw.m_tiles * pw.n_tiles * pw.splits;
   LaunchCfg c;
-  c.grid = dim3(n_w + pu.m_tiles * pu.n_tiles, 1, 1);
+  c.grid = dim3(n_w + pu.m_tiles * pu.n_tiles * pu.splits, 1, 1);
   c.block = dim3(kTcThreads, 1, 1);
   c.smem = pw.smem > pu.smem ? pw.smem : pu.smem;
   c.stream = s;

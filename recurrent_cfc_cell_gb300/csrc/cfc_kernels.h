@@ -88,8 +88,10 @@ TcPlan proj_tc_plan(int B, int K, int C, int n_x);
 cudaError_t proj_tc_launch(const TcPlan& pl, const float* u, const float* W, const float* bias,
                            int B, int K, int C, int n_x, float* H, float* cache, int* status,
                            cudaStream_t s, bool pdl);
-// Both in one launch: the dW partials of plan pw and du itself (plan pu must be unsplit).
+// Both in one launch: the dW partials of plan pw and du (or, when pu.splits > 1, its partial
+// blocks [splits][B*K][n_x]).  dwdu_tc_plans splits both so their CTAs fill one wave.
 TcPlan du_tc_plan_unsplit(int B, int K, int C, int n_x);
+void dwdu_tc_plans(int B, int K, int C, int n_x, TcPlan* pw, TcPlan* pu);
 cudaError_t dwdu_tc_launch(const TcPlan& pw, const TcPlan& pu, const float* d_pre,
                            const float* u, const float* H, const float* h0, const float* W, int B,
                            int K, int C, int n_x, float* partial, float* du, int* status,
@@ -107,6 +109,12 @@ cudaError_t reduce_axis0_launch(const float* in, int n_batch, int n_tail, float*
 // out[row][ncol], column ncol to out2[row], the rest (padding) is dropped.
 cudaError_t reduce_axis0_rows_launch(const float* in, int n_batch, int n_tail, int pitch,
                                      int ncol, float* out, float* out2, cudaStream_t s,
+                                     bool pdl);
+// Two such sums in one launch: (in, n_batch, n_tail, pitch, ncol -> out, out2) as
+// reduce_axis0_rows_launch, and (in_b, n_batch_b, n_tail_b -> out_b) as reduce_axis0_launch.
+cudaError_t reduce_axis0_pair_launch(const float* in, int n_batch, int n_tail, int pitch,
+                                     int ncol, float* out, float* out2, const float* in_b,
+                                     int n_batch_b, int n_tail_b, float* out_b, cudaStream_t s,
                                      bool pdl);
 // Row pitch of the tensor-core weight-gradient partials: the n_in columns of z, the all-ones
 // column that yields db, padded to a multiple of 4.

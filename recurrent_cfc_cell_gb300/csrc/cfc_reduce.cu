@@ -40,17 +40,25 @@ __device__ __forceinline__ void put(const OutMap& o, int n, float v) {
   else if (col == o.ncol) o.out2[row] = v;
 }
 
+// One sum: n_tail columns of n_batch rows, each cluster CTA taking rows_per_cta rows.
+struct Seg {
+  const float* in;
+  int n_batch, n_tail, rows_per_cta;
+  OutMap o;
+};
+
+// Column tile `tile` of segment g (every CTA of the cluster along y works on the same tile).
 template <int VEC>
-__global__ void __launch_bounds__(kRowLanes * kColLanes) reduce_axis0_kernel(
-    const float* __restrict__ in, int n_batch, int n_tail, int rows_per_cta, OutMap o) {
+__device__ __forceinline__ void reduce_tile(const Seg& g, int tile) {
   constexpr int TC = kColLanes * VEC;
   __shared__ __align__(16) float part[kRowLanes][TC];
   __shared__ __align__(16) float cta_sum[TC];
-  grid_dep_launch_dependents();
-  grid_dep_wait();
+  const float* __restrict__ in = g.in;
+  const int n_batch = g.n_batch, n_tail = g.n_tail, rows_per_cta = g.rows_per_cta;
+  const OutMap& o = g.o;
   const int tid = threadIdx.x;
   const int cl = tid % kColLanes, rl = tid / kColLanes;
-  const int col = blockIdx.x * TC + cl * VEC;
+  const int col = tile * TC + cl * VEC;
   const int q = static_cast<int>(cluster_rank());
   const int CZ = static_cast<int>(gridDim.y);
   const int lo = q * rows_per_cta;
@@ -102,7 +110,7 @@ __global__ void __launch_bounds__(kRowLanes * kColLanes) reduce_axis0_kernel(
   if (CZ == 1) {
     __syncthreads();
     for (int c = tid; c < TC; c += kRowLanes * kColLanes) {
-      const int n = blockIdx.x * TC + c;
+      const int n = tile * TC + c;
       if (n < n_tail) put(o, n, cta_sum[c]);
     }
     return;
@@ -113,11 +121,28 @@ __global__ void __launch_bounds__(kRowLanes * kColLanes) reduce_axis0_kernel(
       const uint32_t a = smem_addr(&cta_sum[c]);
       float sacc = cta_sum[c];
       for (int qq = 1; qq < CZ; ++qq) sacc += ld_shared_cluster_f32(map_to_rank(a, qq));
-      const int n = blockIdx.x * TC + c;
+      const int n = tile * TC + c;
       if (n < n_tail) put(o, n, sacc);
     }
   }
   cluster_sync_all();
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kRowLanes * kColLanes) reduce_axis0_kernel(const Seg g) {
+  grid_dep_launch_dependents();
+  grid_dep_wait();
+  reduce_tile<VEC>(g, blockIdx.x);
+}
+
+// Two sums in one launch: column tiles [0, tiles_a) of segment a, the rest of segment b.
+template <int VEC>
+__global__ void __launch_bounds__(kRowLanes * kColLanes) reduce_axis0_pair_kernel(
+    const Seg a, const Seg b, int tiles_a) {
+  grid_dep_launch_dependents();
+  grid_dep_wait();
+  if (static_cast<int>(blockIdx.x) < tiles_a) reduce_tile<VEC>(a, blockIdx.x);
+  else reduce_tile<VEC>(b, blockIdx.x - tiles_a);
 }
 
 int choose_cz(int n_batch) {
@@ -132,14 +157,35 @@ cudaError_t launch_vec(const float* in, int n_batch, int n_tail, const OutMap& o
                        bool pdl) {
   constexpr int TC = kColLanes * VEC;
   const int cz = choose_cz(n_batch);
-  const int rows_per_cta = (n_batch + cz - 1) / cz;
+  const Seg g{in, n_batch, n_tail, (n_batch + cz - 1) / cz, o};
   LaunchCfg c;
   c.grid = dim3((n_tail + TC - 1) / TC, cz, 1);
   c.block = dim3(kRowLanes * kColLanes, 1, 1);
   c.stream = s;
   c.pdl = pdl;
   c.cluster = dim3(1, cz, 1);
-  return launch(c, reduce_axis0_kernel<VEC>, in, n_batch, n_tail, rows_per_cta, o);
+  return launch(c, reduce_axis0_kernel<VEC>, g);
+}
+
+template <int VEC>
+cudaError_t launch_pair_vec(const float* in, int n_batch, int n_tail, const OutMap& o,
+                            const float* in_b, int n_batch_b, int n_tail_b, const OutMap& o_b,
+                            cudaStream_t s, bool pdl) {
+  constexpr int TC = kColLanes * VEC;
+  // One cluster shape for both: the larger batch decides it; each segment spreads its own
+  // rows over the cluster's CTAs (its summation order still depends only on its sizes and
+  // the other segment's batch count).
+  const int cz = choose_cz(n_batch > n_batch_b ? n_batch : n_batch_b);
+  const Seg a{in, n_batch, n_tail, (n_batch + cz - 1) / cz, o};
+  const Seg b{in_b, n_batch_b, n_tail_b, (n_batch_b + cz - 1) / cz, o_b};
+  const int tiles_a = (n_tail + TC - 1) / TC;
+  LaunchCfg c;
+  c.grid = dim3(tiles_a + (n_tail_b + TC - 1) / TC, cz, 1);
+  c.block = dim3(kRowLanes * kColLanes, 1, 1);
+  c.stream = s;
+  c.pdl = pdl;
+  c.cluster = dim3(1, cz, 1);
+  return launch(c, reduce_axis0_pair_kernel<VEC>, a, b, tiles_a);
 }
 
 }  // namespace
@@ -147,9 +193,16 @@ cudaError_t launch_vec(const float* in, int n_batch, int n_tail, const OutMap& o
 cudaError_t reduce_axis0_prepare() {
   cudaError_t e = cudaFuncSetAttribute(reduce_axis0_kernel<4>,
                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(reduce_axis0_kernel<1>,
-                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(reduce_axis0_kernel<1>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(reduce_axis0_pair_kernel<4>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(reduce_axis0_pair_kernel<1>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
 }
 
 cudaError_t reduce_axis0_launch(const float* in, int n_batch, int n_tail, float* out,
@@ -164,6 +217,19 @@ cudaError_t reduce_axis0_rows_launch(const float* in, int n_batch, int n_tail, i
   const bool vec = (n_tail % 4 == 0) && (reinterpret_cast<uintptr_t>(in) % 16 == 0);
   return vec ? launch_vec<4>(in, n_batch, n_tail, o, s, pdl)
              : launch_vec<1>(in, n_batch, n_tail, o, s, pdl);
+}
+
+cudaError_t reduce_axis0_pair_launch(const float* in, int n_batch, int n_tail, int pitch,
+                                     int ncol, float* out, float* out2, const float* in_b,
+                                     int n_batch_b, int n_tail_b, float* out_b, cudaStream_t s,
+                                     bool pdl) {
+  const OutMap o{out, out2, pitch, ncol};
+  const OutMap o_b{out_b, nullptr, 0, 0};
+  const bool vec = (n_tail % 4 == 0) && (reinterpret_cast<uintptr_t>(in) % 16 == 0) &&
+                   (n_tail_b % 4 == 0) && (reinterpret_cast<uintptr_t>(in_b) % 16 == 0);
+  return vec ? launch_pair_vec<4>(in, n_batch, n_tail, o, in_b, n_batch_b, n_tail_b, o_b, s, pdl)
+             : launch_pair_vec<1>(in, n_batch, n_tail, o, in_b, n_batch_b, n_tail_b, o_b, s,
+                                  pdl);
 }
 
 }  // namespace cfc
