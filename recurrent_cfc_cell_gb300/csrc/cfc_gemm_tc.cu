@@ -510,7 +510,6 @@ TcPlan tc_plan(int rows, int cols, int red, bool split, int terms = 2, int stage
 TcPlan dw_tc_plan(int B, int K, int C, int n_x) {
   return tc_plan(4 * C, dw_tc_pitch(n_x + C), B * K, true);
 }
-TcPlan du_tc_plan(int B, int K, int C, int n_x) { return tc_plan(B * K, n_x, 4 * C, true); }
 TcPlan du_tc_plan_unsplit(int B, int K, int C, int n_x) {
   return tc_plan(B * K, n_x, 4 * C, false);
 }
@@ -536,9 +535,6 @@ void dwdu_tc_plans(int B, int K, int C, int n_x, TcPlan* pw, TcPlan* pu) {
 cudaError_t tc_prepare(int max_smem) {
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<DwProblem>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc_gemm_kernel<DuProblem>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           max_smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tc_dual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            max_smem);
@@ -573,20 +569,6 @@ cudaError_t dw_tc_launch(const TcPlan& pl, const float* d_pre, const float* u, c
   c.stream = s;
   c.pdl = pdl;
   return launch(c, tc_gemm_kernel<DwProblem>, p);
-}
-
-cudaError_t du_tc_launch(const TcPlan& pl, const float* d_pre, const float* W, int B, int K,
-                         int C, int n_x, float* du, int* status, cudaStream_t s, bool pdl) {
-  TcParams p = make_params(pl, d_pre, B, K, C, n_x, status);
-  p.W = W; p.out = du;
-  p.rows = B * K; p.cols = n_x; p.red = 4 * C;
-  LaunchCfg c;
-  c.grid = dim3(pl.m_tiles * pl.n_tiles, pl.splits, 1);
-  c.block = dim3(kTcThreads, 1, 1);
-  c.smem = pl.smem;
-  c.stream = s;
-  c.pdl = pdl;
-  return launch(c, tc_gemm_kernel<DuProblem>, p);
 }
 
 TcPlan proj_tc_plan(int B, int K, int C, int n_x) {

@@ -74,14 +74,10 @@ struct TcPlan {
   size_t smem;
 };
 TcPlan dw_tc_plan(int B, int K, int C, int n_x);  // split over the B*K rows
-TcPlan du_tc_plan(int B, int K, int C, int n_x);  // split over 4C when B*K is small
 cudaError_t tc_prepare(int max_smem);
 cudaError_t dw_tc_launch(const TcPlan& pl, const float* d_pre, const float* u, const float* H,
                          const float* h0, int B, int K, int C, int n_x, float* partial,
                          int* status, cudaStream_t s, bool pdl);
-// du, or (when pl.splits > 1) its partial blocks [splits][B*K][n_x].
-cudaError_t du_tc_launch(const TcPlan& pl, const float* d_pre, const float* W, int B, int K,
-                         int C, int n_x, float* du, int* status, cudaStream_t s, bool pdl);
 // The input projection X = W_u u + b on the tensor cores (bf16 hi/lo split), written in place
 // into H and cache like inproj_launch.
 TcPlan proj_tc_plan(int B, int K, int C, int n_x);
