@@ -75,15 +75,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 constexpr uint32_t kSuspendHintNs = 100000u;
 
 // Probe of phase `parity` with cluster-scope acquire (remote st.async data written into this
-// CTA's shared memory is visible once it returns true); may suspend the thread meanwhile.
+// CTA's shared memory is visible once it returns true); may suspend the thread for the
+// hardware's own time limit.  No suspend hint: in an exchange-only probe of the recurrences'
+// step (GB300, 32 clusters) this took 0.234 us per step against 0.251 us with the hint.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
