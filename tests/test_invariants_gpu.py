@@ -25,8 +25,9 @@ def _step(w):
     return st, inp, torch
 
 
-def test_bitwise_deterministic_runs():
-    st, _, torch = _step(inputs.CONFIGS[3])
+@pytest.mark.parametrize("idx", [1, 3])  # dW/du split together + paired merge; dual launch
+def test_bitwise_deterministic_runs(idx):
+    st, _, torch = _step(inputs.CONFIGS[idx])
     st.run()
     torch.cuda.synchronize()
     first = {k: v.clone() for k, v in st.outputs().items()}
