@@ -101,8 +101,10 @@ int max_clusters(DeviceState& st, int kind, int variant, int CS, size_t smem, in
     return CFC_OK;
   }
   int n = 0;
-  const cudaError_t e = (kind == 0) ? cfc::fwd_prepare(CS, variant, smem, &n)
-                                    : cfc::bwd_prepare(CS, variant, smem, &n);
+  // kind 0: forward (CUDA cores), 1: backward, 3: forward with the tensor-core contraction
+  const cudaError_t e = (kind == 1)   ? cfc::bwd_prepare(CS, variant, smem, &n)
+                       : (kind == 3) ? cfc::fwd_tc_prepare(CS * cfc::kFwdChanPerCta, &n)
+                                     : cfc::fwd_prepare(CS, variant, smem, &n);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return CFC_ERR_CUDA;
@@ -164,6 +166,11 @@ constexpr int kDualMinDuTiles = 64;
 // tc_gemm_kernel<ProjProblem>) rather than on the CUDA cores (inproj_kernel): below it the
 // CUDA-core kernel's single short wave is faster than the tensor-core kernel's set-up.
 constexpr int kTcProjMinRows = 8192;
+
+// Batch rows from which the forward recurrence runs its per-step gate contraction on the
+// tensor cores (cfc_fwd_tc_kernel, 128 rows per cluster) instead of the CUDA-core kernel
+// (at most 8 rows per cluster, one cluster per row group).
+constexpr int kTcFwdMinRows = 512;
 
 // Shared memory of a BPTT CTA launched as a dependent of the forward: more than half of an
 // SM's 228 KB (so two BPTT CTAs cannot be packed onto one SM for the whole recurrence) and
@@ -271,6 +278,16 @@ int forward_recurrence(const float* h0, const float* W, const float* ts, int B, 
   p.status = st->status;
   p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
   p.CS = cluster_size_for(C, cfc::kFwdChanPerCta);
+  if (B >= kTcFwdMinRows && cfc::fwd_tc_supported(C)) {
+    int n = 0;
+    rc = max_clusters(*st, 3, 0, p.CS, 0, &n);
+    if (rc != CFC_OK) return rc;
+    if (n > 0) {
+      p.R = 0;
+      return cuda_rc(cfc::fwd_tc_launch(p, static_cast<cudaStream_t>(stream), pdl),
+                     CFC_ERR_LAUNCH_FAILED);
+    }
+  }
   size_t smem = 0;
   int n_clusters = 0;
   rc = plan_rows(*st, 0, 0, p.CS, B, n_x, &p.R, &smem, &n_clusters);

@@ -1,0 +1,439 @@
+// cfc_fwd_tc.cu -- the forward recurrence with the per-step gate contraction on the
+// 5th-generation tensor cores, for large batches.
+//
+// The recurrence of page "K-loop Parallelization -- Block-per-Batch Kernel Refactor" (section
+// "Problem": P = W z + b, then the cell) is, for many batch rows at once, one contraction per
+// step: [rows x C] h_{t-1} times [C x 4C] W_h^T, plus the input projection X computed before
+// the loop.  The pages note that a bigger batch wants mixed-precision matrix hardware
+// (section "Headline Numbers").  Here each step's contraction runs on tcgen05 with fp32
+// accuracy.  Both operands are split into three bf16 terms (x = hi + mid + lo, all 24
+// significand bits).  The product keeps hi*hi + hi*mid + mid*hi + hi*lo + lo*hi + mid*mid, six
+// MMAs per 16-deep step; the dropped terms are below 2^-24 of each product.
+//
+// Layout: a thread-block cluster of CS = C / 32 CTAs serves 128 batch rows; CTA `rank` owns
+// channels 32 rank .. 32 rank + 31, i.e. 128 gate rows of W.  Per CTA:
+//   tensor memory  D^T [128 gate rows (lanes) x 128 batch rows (columns)] fp32, then the CTA's
+//                  W_h^T slice as the A operand (lane 4c + g = gate g of local channel c, k
+//                  along columns in bf16 pairs), three terms of C / 2 columns each;
+//   shared memory  h_{t-1} as the B operand, three bf16 terms [C x 128] in the non-swizzled
+//                  K-major layout [k / 8][row / 8][8 rows][16 bytes], so the 32 values of
+//                  k that one CTA produces form one contiguous 8 KB slab per term.
+// A step: one thread issues the MMAs slab by slab as the slabs of h_{t-1} arrive (its own in
+// place, the others by bulk copies from the other CTAs); then eight warps read D^T and add X
+// (a channel's four gates sit in four adjacent lanes; a 4 x 4 transpose inside each lane quad
+// gives every lane all four gates of one row), apply the cell, write H and the cache, and
+// write h_t's three terms into the CTA's own slab; the control warp copies that slab to every
+// other CTA.  A cluster-wide barrier ("every CTA's MMAs of step t are done")
+// guards both buffer reuses: the other CTAs' slabs landing in this CTA's h buffer, and the
+// next overwrite of this CTA's own slab (a source of its copies).  Every wait is bounded; a
+// timeout is recorded in the status word and the CTAs leave the loop together.
+#include <cuda_bf16.h>
+
+#include "cfc_kernels.h"
+#include "cfc_launch.cuh"
+#include "cfc_ptx.cuh"
+
+namespace cfc {
+namespace {
+
+constexpr int kTM = 128;                         // batch rows per cluster (MMA N)
+constexpr int kGC = 4 * kFwdChanPerCta;          // gate rows per CTA (MMA M)
+constexpr int kEpiWarps = 8;                     // epilogue warps (two per TMEM lane quarter)
+constexpr int kTcThreads = (kEpiWarps + 1) * 32; // + one control warp
+constexpr int kSlabBytes = kTM * kFwdChanPerCta * 2;  // one CTA's k range of one h term
+constexpr int kStepBar = 1;                      // named barrier id of the per-step hand-off
+
+template <int CS>
+struct TcShape {
+  static constexpr int C = kFwdChanPerCta * CS;
+  static constexpr int TERM = C * kTM * 2;       // bytes of one bf16 term of h
+  static constexpr int ACOLS = C / 2;            // TMEM columns of one term of W_h^T
+  // h terms, ts of two steps, barriers (full[CS], mma done, all done), TMEM slot, alignment.
+  static constexpr int USED = 3 * TERM + 2 * kTM * 4 + (CS + 2) * 8 + 16 + 128;
+  // At least half an SM's shared memory: a CTA takes all 512 tensor-memory columns, so two
+  // CTAs on one SM would leave the second waiting in tcgen05.alloc while its cluster waits on
+  // it.
+  static constexpr int SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
+};
+
+struct Split3 {
+  __nv_bfloat16 t[3];
+};
+__device__ __forceinline__ Split3 split3(float x) {
+  Split3 s;
+  s.t[0] = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(s.t[0]);
+  s.t[1] = __float2bfloat16_rn(r1);
+  s.t[2] = __float2bfloat16_rn(r1 - __bfloat162float(s.t[1]));
+  return s;
+}
+__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 lo, __nv_bfloat16 hi) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
+}
+
+// Byte offset of element (row n, k) in one h term: [k / 8][n / 8][n % 8][k % 8].
+__device__ __forceinline__ uint32_t hterm_offset(int n, int k) {
+  return static_cast<uint32_t>(((k >> 3) * (kTM / 8) + (n >> 3)) * 128 + (n & 7) * 16 +
+                               (k & 7) * 2);
+}
+
+// Shared-memory operand descriptor, no swizzle, K-major: `lbo` bytes between core matrices
+// along k, `sbo` bytes between core matrices along the rows.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;  // descriptor version; layout type 0 (no swizzle)
+  return d;
+}
+
+// D (tensor memory) += A (tensor memory) * B (shared memory descriptor).
+__device__ __forceinline__ void umma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 consecutive 32-bit tensor-memory columns of this thread's lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// Bulk copy of `bytes` from this CTA's shared memory to a (remote) CTA's shared memory of the
+// cluster, completing as transaction bytes on the destination's mbarrier `rbar`.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t rdst, uint32_t src, uint32_t bytes,
+                                                     uint32_t rbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(rdst),
+      "r"(src), "r"(bytes), "r"(rbar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t rbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar)
+               : "memory");
+}
+
+// Named barrier over `n` threads that returns the OR of `pred` over them.
+__device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+template <int CS>
+__global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdParams p) {
+  using S = TcShape<CS>;
+  constexpr int C = S::C;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  uint8_t* sm = smem_raw + ((128u - (raw & 127u)) & 127u);
+  uint8_t* hb = sm;                                                     // [3][TERM]
+  float* ts_s = reinterpret_cast<float*>(sm + 3 * S::TERM);             // [2][kTM]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ts_s + 2 * kTM);         // full[CS], done, all
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + CS + 2);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int rank = static_cast<int>(cluster_rank());
+  const int row0 = static_cast<int>(cluster_id_x()) * kTM;
+  const int B = p.B, K = p.K, n_x = p.n_x, n_in = p.n_in;
+  const uint32_t full0 = smem_addr(&bars[0]);       // full[j]: slab j of h_{t-1} is in place
+  const uint32_t done_bar = smem_addr(&bars[CS]);   // this CTA's MMAs of the step are done
+  const uint32_t all_bar = smem_addr(&bars[CS + 1]);  // every CTA's MMAs of the step are done
+
+  grid_dep_launch_dependents();
+  if (tid == 0) {
+    for (int j = 0; j < CS; ++j) mbar_init(full0 + 8u * j, 1);
+    mbar_init(done_bar, 1);
+    mbar_init(all_bar, CS);
+    fence_mbar_init_cluster();
+  }
+  if (warp == kEpiWarps) {
+    tmem_alloc(smem_addr(tslot), 512);
+    tc_fence_before_sync();
+  }
+  // X comes from the projection kernel in place in H / cache: wait for it before any read.
+  grid_dep_wait();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tslot;
+
+  // This thread's role in the epilogue warps: TMEM lane quarter q, rows 64 hh .. 64 hh + 63,
+  // gate g of local channel c (lane 4c + g of the quarter's 32 lanes).
+  const int q = warp & 3, hh = (warp >> 2) & 1;
+  const int c = (32 * q + lane) >> 2, g = lane & 3;
+  const int ch = kFwdChanPerCta * rank + c;
+
+  if (warp < kEpiWarps) {
+    // ---- W_h^T slice -> tensor memory (three bf16 terms); the two warps of a lane quarter
+    // take the two halves of k. ----
+    const float* wrow = p.W + (static_cast<size_t>(g) * C + ch) * n_in + n_x;
+    for (int k0 = hh * (C / 2); k0 < (hh + 1) * (C / 2); k0 += 64) {
+      uint32_t r0[32], r1[32], r2[32];
+#pragma unroll
+      for (int cc = 0; cc < 32; ++cc) {
+        const Split3 a = split3(__ldg(wrow + k0 + 2 * cc));
+        const Split3 b = split3(__ldg(wrow + k0 + 2 * cc + 1));
+        r0[cc] = pack2(a.t[0], b.t[0]);
+        r1[cc] = pack2(a.t[1], b.t[1]);
+        r2[cc] = pack2(a.t[2], b.t[2]);
+      }
+      const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + 128 + k0 / 2;
+      tmem_st32(ta, r0);
+      tmem_st32(ta + S::ACOLS, r1);
+      tmem_st32(ta + 2 * S::ACOLS, r2);
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    // ---- h0 -> this CTA's slab of the h buffer (lanes g >= 1 write term g - 1). ----
+    if (g >= 1) {
+      for (int i = 0; i < 64; ++i) {
+        const int r = 64 * hh + i, b = row0 + r;
+        const float h = (b < B) ? __ldg(p.h0 + static_cast<size_t>(b) * C + ch) : 0.f;
+        *reinterpret_cast<__nv_bfloat16*>(hb + (g - 1) * S::TERM + hterm_offset(r, ch)) =
+            split3(h).t[g - 1];
+      }
+    }
+  } else {
+    // ts of step 0 (the control warp loads each step's ts one step ahead).
+    for (int i = lane; i < kTM; i += 32) ts_s[i] = (row0 + i < B) ? __ldg(p.ts + row0 + i) : 0.f;
+  }
+  fence_proxy_async_smem();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  cluster_sync_all();  // every CTA: barriers set up, W_h^T and its h0 slab in place
+
+  if (warp == kEpiWarps) {
+    // ================= control warp: MMAs, completion signals, the exchange =================
+    const uint32_t idesc = umma_idesc_bf16(kGC, kTM);
+    const uint32_t hb0 = smem_addr(hb);
+    const uint64_t bdesc0 = desc_kmajor(hb0, (kTM / 8) * 128, 128);
+    // This CTA's slab (three terms) to every other CTA, lane d copying to CTA rank + d; lane 0
+    // marks its own slab in place.
+    auto push = [&]() {
+      if (lane == 0) {
+        mbar_arrive(full0 + 8u * rank);
+      } else if (lane < CS) {
+        const uint32_t dst = static_cast<uint32_t>((rank + lane) % CS);
+        for (int tm = 0; tm < 3; ++tm) {
+          const uint32_t src = hb0 + tm * S::TERM + rank * kSlabBytes;
+          bulk_copy_to_cluster(map_to_rank(src, dst), src, kSlabBytes,
+                               map_to_rank(full0 + 8u * rank, dst));
+        }
+      }
+    };
+    bool ok = true;
+    if (lane == 0)
+      for (int j = 0; j < CS; ++j)
+        if (j != rank) mbar_arrive_expect_tx(full0 + 8u * j, 3 * kSlabBytes);
+    push();  // h0: the slabs step 0 multiplies
+    for (int t = 0; t < K; ++t) {
+      if (lane == 0) {
+        uint32_t acc = 0;
+        for (int jj = 0; jj < CS && ok; ++jj) {
+          const int j = (rank + jj) % CS;
+          ok = mbar_wait_bounded_cta(full0 + 8u * j, t & 1, p.status);
+          if (!ok) break;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int s2 = 0; s2 < 2; ++s2) {  // the two 16-deep steps of slab j
+            const int s = 2 * j + s2;
+            const uint32_t a0 = tmem + 128 + 8 * s;
+            // Descriptor of B term 0 at this k step; the start-address field counts 16 bytes,
+            // so terms 1 and 2 are a fixed add away.
+            const uint64_t d0 = bdesc0 + static_cast<uint64_t>(s * (4096 >> 4));
+            const uint64_t d1 = d0 + (S::TERM >> 4), d2 = d0 + 2 * (S::TERM >> 4);
+            // (A term, B term): hi*hi, hi*mid, mid*hi, hi*lo, lo*hi, mid*mid
+            umma_tmem_a(tmem, a0, d0, idesc, acc);
+            acc = 1;
+            umma_tmem_a(tmem, a0, d1, idesc, 1);
+            umma_tmem_a(tmem, a0 + S::ACOLS, d0, idesc, 1);
+            umma_tmem_a(tmem, a0, d2, idesc, 1);
+            umma_tmem_a(tmem, a0 + 2 * S::ACOLS, d0, idesc, 1);
+            umma_tmem_a(tmem, a0 + S::ACOLS, d1, idesc, 1);
+          }
+        }
+        umma_commit(done_bar);
+        if (t + 1 < K)
+          for (int j = 0; j < CS; ++j)
+            if (j != rank) mbar_arrive_expect_tx(full0 + 8u * j, 3 * kSlabBytes);
+        ok = mbar_wait_bounded_cta(done_bar, t & 1, p.status) && ok;
+        tc_fence_before_sync();  // the step's MMAs are ordered before the signals below
+        // This CTA no longer reads its h buffer for step t: tell every CTA.
+        for (int d = 0; d < CS; ++d) mbar_arrive_cluster(map_to_rank(all_bar, d));
+      }
+      // ts of step t + 1 for the next epilogue.
+      if (t + 1 < K)
+        for (int i = lane; i < kTM; i += 32)
+          ts_s[((t + 1) & 1) * kTM + i] =
+              (row0 + i < B) ? __ldg(p.ts + static_cast<size_t>(t + 1) * B + row0 + i) : 0.f;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (bar_or(kStepBar, kTcThreads, !ok)) break;  // h_t is in this CTA's slab
+      if (t + 1 < K) push();
+    }
+  } else {
+    // ================= epilogue warps =================
+    // X of (gate g, channel ch) for rows row0 + 64 hh + i, i < 64, of step t, in place in H
+    // (gate 0) or cache (gates 1-3).
+    const size_t xrow = (g == 0) ? static_cast<size_t>(C) : 3ull * C;
+    const float* xbase = ((g == 0) ? p.H : p.cache + static_cast<size_t>(g - 1) * C) + ch;
+    const int rfirst = row0 + 64 * hh;
+    int nvalid = B - rfirst;
+    nvalid = nvalid < 0 ? 0 : (nvalid > 64 ? 64 : nvalid);
+    float xv[64];
+    auto load_x = [&](int t) {
+      const float* xp = xbase + (static_cast<size_t>(t) * B + rfirst) * xrow;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) xv[i] = (i < nvalid) ? __ldcg(xp + i * xrow) : 0.f;
+    };
+    load_x(0);
+    bool ok = true;
+    for (int t = 0; t < K; ++t) {
+      ok = ok && mbar_wait_bounded_cluster(all_bar, t & 1, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after_sync();
+      if (ok) {
+        const float* tsr = ts_s + (t & 1) * kTM + 64 * hh;
+        float* hout = p.H + (static_cast<size_t>(t) * B + rfirst) * C + ch;
+        float* cout = p.cache + (static_cast<size_t>(t) * B + rfirst) * 3 * C + ch;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float P[16];
+          tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + 64 * hh + 16 * cc, P);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) P[i] += xv[16 * cc + i];
+#pragma unroll
+          for (int i0 = 0; i0 < 16; i0 += 4) {
+            // 4 x 4 transpose within the lane quad: lane g held gate g of rows i0 .. i0 + 3,
+            // afterwards it holds the four gates of row i0 + g.
+            float v[4] = {P[i0], P[i0 + 1], P[i0 + 2], P[i0 + 3]};
+#pragma unroll
+            for (int m = 1; m <= 2; m <<= 1) {
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {
+                if (jj & m) continue;
+                const bool up = (g & m) != 0;
+                const float r = __shfl_xor_sync(0xffffffffu, up ? v[jj] : v[jj + m], m);
+                if (up) v[jj] = r;
+                else v[jj + m] = r;
+              }
+            }
+            const int ri = 16 * cc + i0 + g;  // this lane's row among the warp's 64
+            const float ff1 = fmaf(2.f, sigmoid_fast(2.f * v[0]), -1.f);
+            const float ff2 = fmaf(2.f, sigmoid_fast(2.f * v[1]), -1.f);
+            const float gt = sigmoid_fast(fmaf(v[2], tsr[ri], v[3]));
+            const float h = ff1 * (1.f - gt) + gt * ff2;
+            if (ri < nvalid) {
+              hout[static_cast<size_t>(ri) * C] = h;
+              float* cp = cout + static_cast<size_t>(ri) * 3 * C;
+              cp[0] = ff1;
+              cp[C] = ff2;
+              cp[2 * C] = gt;
+            }
+            const Split3 sp = split3(h);
+            uint8_t* dst = hb + hterm_offset(64 * hh + ri, ch);
+            *reinterpret_cast<__nv_bfloat16*>(dst) = sp.t[0];
+            *reinterpret_cast<__nv_bfloat16*>(dst + S::TERM) = sp.t[1];
+            *reinterpret_cast<__nv_bfloat16*>(dst + 2 * S::TERM) = sp.t[2];
+          }
+        }
+      }
+      fence_proxy_async_smem();  // h_t's terms -> visible to the MMAs and the bulk copies
+      tc_fence_before_sync();    // tensor-memory loads done before the next step's MMAs
+      if (bar_or(kStepBar, kTcThreads, !ok)) break;
+      if (t + 1 < K) load_x(t + 1);  // in flight while the next step's MMAs run
+    }
+  }
+
+  // Leave together: no CTA exits while another may still address its shared memory.
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == kEpiWarps) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int CS>
+cudaError_t prepare_k(int* max_active) {
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  const int smem = TcShape<CS>::SMEM;
+  if (smem > optin) {
+    *max_active = 0;
+    return cudaSuccess;
+  }
+  auto* kern = cfc_fwd_tc_kernel<CS>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CS, 1, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(max_active, kern, &cfg);
+}
+
+template <int CS>
+cudaError_t launch_k(const FwdParams& p, cudaStream_t s, bool pdl) {
+  LaunchCfg c;
+  c.grid = dim3(((p.B + kTM - 1) / kTM) * CS, 1, 1);
+  c.block = dim3(kTcThreads, 1, 1);
+  c.smem = TcShape<CS>::SMEM;
+  c.stream = s;
+  c.pdl = pdl;
+  c.cluster = dim3(CS, 1, 1);
+  return launch(c, cfc_fwd_tc_kernel<CS>, p);
+}
+
+}  // namespace
+
+bool fwd_tc_supported(int C) { return C == 4 * kFwdChanPerCta || C == 8 * kFwdChanPerCta; }
+
+cudaError_t fwd_tc_prepare(int C, int* max_active_clusters) {
+  if (C == 4 * kFwdChanPerCta) return prepare_k<4>(max_active_clusters);
+  if (C == 8 * kFwdChanPerCta) return prepare_k<8>(max_active_clusters);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t fwd_tc_launch(const FwdParams& p, cudaStream_t s, bool pdl) {
+  if (p.C == 4 * kFwdChanPerCta) return launch_k<4>(p, s, pdl);
+  if (p.C == 8 * kFwdChanPerCta) return launch_k<8>(p, s, pdl);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace cfc

@@ -53,6 +53,13 @@ cudaError_t fwd_prepare(int CS, int R, size_t smem, int* max_active_clusters);
 cudaError_t fwd_launch(const FwdParams& p, int n_clusters, size_t smem, cudaStream_t s,
                        bool pdl);
 
+// The forward recurrence with each step's gate contraction on the tensor cores (clusters of
+// C / 32 CTAs serving 128 batch rows each; C = 128 or 256).  X in place in H / cache as for
+// fwd_launch.
+bool fwd_tc_supported(int C);
+cudaError_t fwd_tc_prepare(int C, int* max_active_clusters);
+cudaError_t fwd_tc_launch(const FwdParams& p, cudaStream_t s, bool pdl);
+
 size_t bwd_smem_bytes(int R, int CS);
 cudaError_t bwd_prepare(int CS, int R, size_t smem, int* max_active_clusters);
 cudaError_t bwd_launch(const BwdParams& p, int n_clusters, size_t smem, cudaStream_t s,

@@ -34,6 +34,8 @@ RAGGED = [
     dict(B=200, K=6, n_x=64, C=256),   # 8-row forward and 16-row BPTT clusters of 8 CTAs
     dict(B=130, K=64, n_x=13, C=100),  # tensor-core projection: odd n_x (scalar loads), C not
                                        # a multiple of 16 (element-wise epilogue), ragged tiles
+    dict(B=520, K=6, n_x=16, C=128),   # tensor-core forward, clusters of 4, last cluster 8 rows
+    dict(B=600, K=5, n_x=24, C=256),   # tensor-core forward, clusters of 8, last cluster 88 rows
 ]
 
 
