@@ -5,29 +5,31 @@
 // "Problem": P = W z + b, then the cell) is, for many batch rows at once, one contraction per
 // step: [rows x C] h_{t-1} times [C x 4C] W_h^T, plus the input projection X computed before
 // the loop.  The pages note that a bigger batch wants mixed-precision matrix hardware
-// (section "Headline Numbers").  Here each step's contraction runs on tcgen05 with fp32
-// accuracy.  Both operands are split into three bf16 terms (x = hi + mid + lo, all 24
-// significand bits).  The product keeps hi*hi + hi*mid + mid*hi + hi*lo + lo*hi + mid*mid, six
-// MMAs per 16-deep step; the dropped terms are below 2^-24 of each product.
+// (section "Headline Numbers").  Here each step's contraction runs on tcgen05 with fp32-level
+// accuracy.  Both operands are split into two fp16 terms, x = hi + lo with hi = fp16(x) and
+// lo = fp16(x - hi), carrying 22 significand bits.  The product keeps hi*hi + hi*lo + lo*hi,
+// three MMAs per 16-deep step; what is dropped is below about 2^-21 of each product.  h lies
+// in (-1, 1).  Each row of W is scaled by a power of two into [-1, 1) before the split, and
+// the result is scaled back exactly, so no weight over- or underflows fp16.
 //
 // Layout: a thread-block cluster of CS = C / 32 CTAs serves 128 batch rows; CTA `rank` owns
 // channels 32 rank .. 32 rank + 31, i.e. 128 gate rows of W.  Per CTA:
 //   tensor memory  D^T [128 gate rows (lanes) x 128 batch rows (columns)] fp32, then the CTA's
 //                  W_h^T slice as the A operand (lane 4c + g = gate g of local channel c, k
-//                  along columns in bf16 pairs), three terms of C / 2 columns each;
-//   shared memory  h_{t-1} as the B operand, three bf16 terms [C x 128] in the non-swizzled
+//                  along columns in fp16 pairs), two terms of C / 2 columns each;
+//   shared memory  h_{t-1} as the B operand, two fp16 terms [C x 128] in the non-swizzled
 //                  K-major layout [k / 8][row / 8][8 rows][16 bytes], so the 32 values of
 //                  k that one CTA produces form one contiguous 8 KB slab per term.
 // A step: one thread issues the MMAs slab by slab as the slabs of h_{t-1} arrive (its own in
 // place, the others by bulk copies from the other CTAs); then eight warps read D^T and add X
 // (a channel's four gates sit in four adjacent lanes; a 4 x 4 transpose inside each lane quad
 // gives every lane all four gates of one row), apply the cell, write H and the cache, and
-// write h_t's three terms into the CTA's own slab; the control warp copies that slab to every
+// write h_t's two terms into the CTA's own slab; the control warp copies that slab to every
 // other CTA.  A cluster-wide barrier ("every CTA's MMAs of step t are done")
 // guards both buffer reuses: the other CTAs' slabs landing in this CTA's h buffer, and the
 // next overwrite of this CTA's own slab (a source of its copies).  Every wait is bounded; a
 // timeout is recorded in the status word and the CTAs leave the loop together.
-#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "cfc_kernels.h"
 #include "cfc_launch.cuh"
@@ -42,34 +44,38 @@ constexpr int kEpiWarps = 8;                     // epilogue warps (two per TMEM
 constexpr int kTcThreads = (kEpiWarps + 1) * 32; // + one control warp
 constexpr int kSlabBytes = kTM * kFwdChanPerCta * 2;  // one CTA's k range of one h term
 constexpr int kStepBar = 1;                      // named barrier id of the per-step hand-off
+constexpr int kTerms = 2;                        // fp16 terms per operand
 
 template <int CS>
 struct TcShape {
   static constexpr int C = kFwdChanPerCta * CS;
-  static constexpr int TERM = C * kTM * 2;       // bytes of one bf16 term of h
+  static constexpr int TERM = C * kTM * 2;       // bytes of one fp16 term of h
   static constexpr int ACOLS = C / 2;            // TMEM columns of one term of W_h^T
   // h terms, ts of two steps, barriers (full[CS], mma done, all done), TMEM slot, alignment.
-  static constexpr int USED = 3 * TERM + 2 * kTM * 4 + (CS + 2) * 8 + 16 + 128;
+  static constexpr int USED = kTerms * TERM + 2 * kTM * 4 + (CS + 2) * 8 + 16 + 128;
   // At least half an SM's shared memory: a CTA takes all 512 tensor-memory columns, so two
   // CTAs on one SM would leave the second waiting in tcgen05.alloc while its cluster waits on
   // it.
   static constexpr int SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
 };
 
-struct Split3 {
-  __nv_bfloat16 t[3];
+struct Split2 {
+  __half t[2];
 };
-__device__ __forceinline__ Split3 split3(float x) {
-  Split3 s;
-  s.t[0] = __float2bfloat16_rn(x);
-  const float r1 = x - __bfloat162float(s.t[0]);
-  s.t[1] = __float2bfloat16_rn(r1);
-  s.t[2] = __float2bfloat16_rn(r1 - __bfloat162float(s.t[1]));
+__device__ __forceinline__ Split2 split2(float x) {
+  Split2 s;
+  s.t[0] = __float2half_rn(x);
+  s.t[1] = __float2half_rn(x - __half2float(s.t[0]));
   return s;
 }
-__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 lo, __nv_bfloat16 hi) {
-  return static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
-         (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
+__device__ __forceinline__ uint32_t pack2(__half lo, __half hi) {
+  return static_cast<uint32_t>(__half_as_ushort(lo)) |
+         (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+}
+// Instruction descriptor of kind::f16 with fp16 A and B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t umma_idesc_f16in(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Byte offset of element (row n, k) in one h term: [k / 8][n / 8][n % 8][k % 8].
@@ -151,8 +157,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t* sm = smem_raw + ((128u - (raw & 127u)) & 127u);
-  uint8_t* hb = sm;                                                     // [3][TERM]
-  float* ts_s = reinterpret_cast<float*>(sm + 3 * S::TERM);             // [2][kTM]
+  uint8_t* hb = sm;                                                     // [2][TERM]
+  float* ts_s = reinterpret_cast<float*>(sm + kTerms * S::TERM);        // [2][kTM]
   uint64_t* bars = reinterpret_cast<uint64_t*>(ts_s + 2 * kTM);         // full[CS], done, all
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + CS + 2);
 
@@ -188,33 +194,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
   const int c = (32 * q + lane) >> 2, g = lane & 3;
   const int ch = kFwdChanPerCta * rank + c;
 
+  float wunscale = 1.f;  // 2^e: this lane's W row was scaled by 2^-e before the split
   if (warp < kEpiWarps) {
-    // ---- W_h^T slice -> tensor memory (three bf16 terms); the two warps of a lane quarter
-    // take the two halves of k. ----
+    // ---- W_h^T slice -> tensor memory (two fp16 terms); the two warps of a lane quarter
+    // take the two halves of k.  Row scale: max|W| * 2^-e in [0.5, 1). ----
     const float* wrow = p.W + (static_cast<size_t>(g) * C + ch) * n_in + n_x;
+    float wmax = 0.f;
+    for (int k = 0; k < C; ++k) wmax = fmaxf(wmax, fabsf(__ldg(wrow + k)));
+    int e = 0;
+    if (wmax > 0.f) (void)frexpf(wmax, &e);
+    const float wscale = ldexpf(1.f, -e);
+    wunscale = ldexpf(1.f, e);
     for (int k0 = hh * (C / 2); k0 < (hh + 1) * (C / 2); k0 += 64) {
-      uint32_t r0[32], r1[32], r2[32];
+      uint32_t r0[32], r1[32];
 #pragma unroll
       for (int cc = 0; cc < 32; ++cc) {
-        const Split3 a = split3(__ldg(wrow + k0 + 2 * cc));
-        const Split3 b = split3(__ldg(wrow + k0 + 2 * cc + 1));
+        const Split2 a = split2(__ldg(wrow + k0 + 2 * cc) * wscale);
+        const Split2 b = split2(__ldg(wrow + k0 + 2 * cc + 1) * wscale);
         r0[cc] = pack2(a.t[0], b.t[0]);
         r1[cc] = pack2(a.t[1], b.t[1]);
-        r2[cc] = pack2(a.t[2], b.t[2]);
       }
       const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + 128 + k0 / 2;
       tmem_st32(ta, r0);
       tmem_st32(ta + S::ACOLS, r1);
-      tmem_st32(ta + 2 * S::ACOLS, r2);
     }
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-    // ---- h0 -> this CTA's slab of the h buffer (lanes g >= 1 write term g - 1). ----
-    if (g >= 1) {
+    // ---- h0 -> this CTA's slab of the h buffer (lanes g = 1, 2 write term g - 1). ----
+    if (g == 1 || g == 2) {
       for (int i = 0; i < 64; ++i) {
         const int r = 64 * hh + i, b = row0 + r;
         const float h = (b < B) ? __ldg(p.h0 + static_cast<size_t>(b) * C + ch) : 0.f;
-        *reinterpret_cast<__nv_bfloat16*>(hb + (g - 1) * S::TERM + hterm_offset(r, ch)) =
-            split3(h).t[g - 1];
+        *reinterpret_cast<__half*>(hb + (g - 1) * S::TERM + hterm_offset(r, ch)) =
+            split2(h).t[g - 1];
       }
     }
   } else {
@@ -229,7 +240,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
 
   if (warp == kEpiWarps) {
     // ================= control warp: MMAs, completion signals, the exchange =================
-    const uint32_t idesc = umma_idesc_bf16(kGC, kTM);
+    const uint32_t idesc = umma_idesc_f16in(kGC, kTM);
     const uint32_t hb0 = smem_addr(hb);
     const uint64_t bdesc0 = desc_kmajor(hb0, (kTM / 8) * 128, 128);
     // This CTA's slab (three terms) to every other CTA, lane d copying to CTA rank + d; lane 0
@@ -239,7 +250,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
         mbar_arrive(full0 + 8u * rank);
       } else if (lane < CS) {
         const uint32_t dst = static_cast<uint32_t>((rank + lane) % CS);
-        for (int tm = 0; tm < 3; ++tm) {
+        for (int tm = 0; tm < kTerms; ++tm) {
           const uint32_t src = hb0 + tm * S::TERM + rank * kSlabBytes;
           bulk_copy_to_cluster(map_to_rank(src, dst), src, kSlabBytes,
                                map_to_rank(full0 + 8u * rank, dst));
@@ -249,7 +260,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
     bool ok = true;
     if (lane == 0)
       for (int j = 0; j < CS; ++j)
-        if (j != rank) mbar_arrive_expect_tx(full0 + 8u * j, 3 * kSlabBytes);
+        if (j != rank) mbar_arrive_expect_tx(full0 + 8u * j, kTerms * kSlabBytes);
     push();  // h0: the slabs step 0 multiplies
     for (int t = 0; t < K; ++t) {
       if (lane == 0) {
@@ -264,23 +275,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
             const int s = 2 * j + s2;
             const uint32_t a0 = tmem + 128 + 8 * s;
             // Descriptor of B term 0 at this k step; the start-address field counts 16 bytes,
-            // so terms 1 and 2 are a fixed add away.
+            // so term 1 is a fixed add away.
             const uint64_t d0 = bdesc0 + static_cast<uint64_t>(s * (4096 >> 4));
-            const uint64_t d1 = d0 + (S::TERM >> 4), d2 = d0 + 2 * (S::TERM >> 4);
-            // (A term, B term): hi*hi, hi*mid, mid*hi, hi*lo, lo*hi, mid*mid
+            const uint64_t d1 = d0 + (S::TERM >> 4);
+            // (A term, B term): hi*hi, hi*lo, lo*hi
             umma_tmem_a(tmem, a0, d0, idesc, acc);
             acc = 1;
             umma_tmem_a(tmem, a0, d1, idesc, 1);
             umma_tmem_a(tmem, a0 + S::ACOLS, d0, idesc, 1);
-            umma_tmem_a(tmem, a0, d2, idesc, 1);
-            umma_tmem_a(tmem, a0 + 2 * S::ACOLS, d0, idesc, 1);
-            umma_tmem_a(tmem, a0 + S::ACOLS, d1, idesc, 1);
           }
         }
         umma_commit(done_bar);
         if (t + 1 < K)
           for (int j = 0; j < CS; ++j)
-            if (j != rank) mbar_arrive_expect_tx(full0 + 8u * j, 3 * kSlabBytes);
+            if (j != rank) mbar_arrive_expect_tx(full0 + 8u * j, kTerms * kSlabBytes);
         ok = mbar_wait_bounded_cta(done_bar, t & 1, p.status) && ok;
         tc_fence_before_sync();  // the step's MMAs are ordered before the signals below
         // This CTA no longer reads its h buffer for step t: tell every CTA.
@@ -325,7 +333,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
           float P[16];
           tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + 64 * hh + 16 * cc, P);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) P[i] += xv[16 * cc + i];
+          for (int i = 0; i < 16; ++i) P[i] = fmaf(P[i], wunscale, xv[16 * cc + i]);
 #pragma unroll
           for (int i0 = 0; i0 < 16; i0 += 4) {
             // 4 x 4 transpose within the lane quad: lane g held gate g of rows i0 .. i0 + 3,
@@ -354,11 +362,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
               cp[C] = ff2;
               cp[2 * C] = gt;
             }
-            const Split3 sp = split3(h);
+            const Split2 sp = split2(h);
             uint8_t* dst = hb + hterm_offset(64 * hh + ri, ch);
-            *reinterpret_cast<__nv_bfloat16*>(dst) = sp.t[0];
-            *reinterpret_cast<__nv_bfloat16*>(dst + S::TERM) = sp.t[1];
-            *reinterpret_cast<__nv_bfloat16*>(dst + 2 * S::TERM) = sp.t[2];
+            *reinterpret_cast<__half*>(dst) = sp.t[0];
+            *reinterpret_cast<__half*>(dst + S::TERM) = sp.t[1];
           }
         }
       }
