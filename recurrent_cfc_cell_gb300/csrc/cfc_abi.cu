@@ -28,6 +28,7 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 int cuda_rc(cudaError_t e, int code) {
   if (e == cudaSuccess) return CFC_OK;
@@ -101,9 +102,11 @@ int max_clusters(DeviceState& st, int kind, int variant, int CS, size_t smem, in
     return CFC_OK;
   }
   int n = 0;
-  // kind 0: forward (CUDA cores), 1: backward, 3: forward with the tensor-core contraction
+  // kind 0: forward (CUDA cores), 1: backward, 3 / 4: forward / backward with the tensor-core
+  // contraction (4: `variant` is C, the count is of CTAs per SM)
   const cudaError_t e = (kind == 1)   ? cfc::bwd_prepare(CS, variant, smem, &n)
                        : (kind == 3) ? cfc::fwd_tc_prepare(CS * cfc::kFwdChanPerCta, &n)
+                       : (kind == 4) ? cfc::bwd_tc_prepare(variant, &n)
                                      : cfc::fwd_prepare(CS, variant, smem, &n);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
@@ -154,6 +157,8 @@ struct BwdLayout {
   bool dual;           // large B*K: du unsplit in the dW launch, one merge
   cfc::TcPlan pw, pu;  // small B*K: dW and du splits sized together for one launch, one merge
   size_t pu_off;       // offset (floats) of the du partials after the dW partials
+  bool tc_bptt;        // the BPTT runs on the tensor cores (W_h^T pre-split at wsplit_off)
+  size_t wsplit_off;
 };
 
 // Row tiles (of 128) from which unsplit du tiles keep enough SMs busy beside the dW splits:
@@ -171,6 +176,10 @@ constexpr int kTcProjMinRows = 8192;
 // tensor cores (cfc_fwd_tc_kernel, 128 rows per cluster) instead of the CUDA-core kernel
 // (at most 8 rows per cluster, one cluster per row group).
 constexpr int kTcFwdMinRows = 512;
+
+// Batch rows from which the BPTT recurrence runs its per-step contraction on the tensor cores
+// (cfc_bwd_tc_kernel, one CTA per 128 rows); it needs the pre-split W_h^T in the workspace.
+constexpr int kTcBwdMinRows = 1024;
 
 // Shared memory of a BPTT CTA launched as a dependent of the forward: more than half of an
 // SM's 228 KB (so two BPTT CTAs cannot be packed onto one SM for the whole recurrence) and
@@ -201,6 +210,9 @@ BwdLayout bwd_layout(int B, int K, int C, int n_x) {
   L.part_off = align256(L.d_pre_bytes);
   L.part_bytes = part * sizeof(float);
   L.total = L.part_off + L.part_bytes;
+  L.tc_bptt = B >= kTcBwdMinRows && cfc::bwd_tc_supported(C);
+  L.wsplit_off = align256(L.total);
+  if (L.tc_bptt) L.total = L.wsplit_off + cfc::bwd_tc_split_bytes(C);
   return L;
 }
 
@@ -302,7 +314,7 @@ int forward_recurrence(const float* h0, const float* W, const float* ts, int B, 
 // memory is then padded past half an SM, so that two BPTT CTAs never share one SM.
 int backward_recurrence(const float* dH, const float* W, const float* ts, const float* cache,
                         int B, int K, int C, int n_x, float* d_pre, float* dh0,
-                        cfc_stream_t stream, bool pdl) {
+                        cfc_stream_t stream, bool pdl, void* wsplit = nullptr) {
   int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
   if (!dH || !W || !ts || !cache || !d_pre || !dh0) return CFC_ERR_NULL_PTR;
@@ -318,6 +330,21 @@ int backward_recurrence(const float* dH, const float* W, const float* ts, const 
   p.status = st->status;
   p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
   p.CS = cluster_size_for(C, cfc::kBwdChanPerCta);
+  p.wsplit = wsplit;
+  // The tensor-core BPTT moves dH, the cache and d_pre in whole 32-byte sectors.
+  if (wsplit && B >= kTcBwdMinRows && cfc::bwd_tc_supported(C) && aligned32(dH) &&
+      aligned32(cache) && aligned32(d_pre)) {
+    int n = 0;
+    rc = max_clusters(*st, 4, C, 1, 0, &n);
+    if (rc != CFC_OK) return rc;
+    if (n > 0) {
+      const cudaStream_t s = static_cast<cudaStream_t>(stream);
+      rc = cuda_rc(cfc::bwd_tc_split(W, C, n_x, wsplit, s, pdl), CFC_ERR_LAUNCH_FAILED);
+      if (rc != CFC_OK) return rc;
+      p.R = 0;
+      return cuda_rc(cfc::bwd_tc_launch(p, s, true), CFC_ERR_LAUNCH_FAILED);
+    }
+  }
   size_t smem = 0;
   int n_clusters = 0;
   rc = plan_rows(*st, 1, 0, p.CS, B, n_x, &p.R, &smem, &n_clusters,
@@ -363,10 +390,9 @@ int cfc_step_launches(int B, int K, int C, int n_x, int dw_mode, int with_du, in
   // (inside the dW launch, and its partials inside the dW merge, with the tensor cores; a
   // launch of its own otherwise).
   int n = 2 + 1 + 2 + (dw_mode == CFC_DW_ACCURATE ? 0 : 1);
-  if (with_du) {
-    const BwdLayout L = bwd_layout(B, K, C, n_x);
-    if (dw_mode != CFC_DW_ACCURATE) n += 1;
-  }
+  const BwdLayout L = bwd_layout(B, K, C, n_x);
+  if (with_du && dw_mode != CFC_DW_ACCURATE) n += 1;
+  if (L.tc_bptt) n += 1;  // W_h^T pre-split for the tensor-core BPTT
   *launches = n;
   return CFC_OK;
 }
@@ -480,7 +506,8 @@ int cfc_backward(const float* dH, const float* u, const float* h0, const float* 
   const BwdLayout L = bwd_layout(B, K, C, n_x);
   if (ws_bytes < L.total) return CFC_ERR_WS_TOO_SMALL;
   float* d_pre = reinterpret_cast<float*>(static_cast<char*>(ws) + L.d_pre_off);
-  rc = cfc_backward_recurrence(dH, W, ts, cache, B, K, C, n_x, d_pre, dh0, stream);
+  rc = backward_recurrence(dH, W, ts, cache, B, K, C, n_x, d_pre, dh0, stream, false,
+                           L.tc_bptt ? static_cast<char*>(ws) + L.wsplit_off : nullptr);
   if (rc != CFC_OK) return rc;
   return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode, stream,
                      true);
@@ -505,7 +532,8 @@ int cfc_forward_backward(const float* u, const float* h0, const float* W, const 
   if (rc != CFC_OK) return rc;
   // The forward writes only H and cache, which the BPTT reads after its dependency wait.
   float* d_pre = reinterpret_cast<float*>(static_cast<char*>(ws) + L.d_pre_off);
-  rc = backward_recurrence(dH, W, ts, cache, B, K, C, n_x, d_pre, dh0, stream, true);
+  rc = backward_recurrence(dH, W, ts, cache, B, K, C, n_x, d_pre, dh0, stream, true,
+                           L.tc_bptt ? static_cast<char*>(ws) + L.wsplit_off : nullptr);
   if (rc != CFC_OK) return rc;
   return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode, stream,
                      true);

@@ -41,6 +41,7 @@ struct BwdParams {
   int* status;
   int B, K, C, n_x, n_in;
   int CS, R;
+  const void* wsplit;  // tensor-core BPTT: W_h^T pre-split into bf16 terms (bwd_tc_split)
 };
 
 // Every launch function takes `pdl`: schedule the kernel while the previous kernel of the
@@ -59,6 +60,15 @@ cudaError_t fwd_launch(const FwdParams& p, int n_clusters, size_t smem, cudaStre
 bool fwd_tc_supported(int C);
 cudaError_t fwd_tc_prepare(int C, int* max_active_clusters);
 cudaError_t fwd_tc_launch(const FwdParams& p, cudaStream_t s, bool pdl);
+
+// The BPTT recurrence with each step's contraction delta = d_pre W_h on the tensor cores: one
+// CTA per 128 batch rows, no exchange between CTAs (C = 128 or 256).  bwd_tc_split first
+// writes W_h^T as three bf16 terms in the layout the kernel streams (bwd_tc_split_bytes).
+bool bwd_tc_supported(int C);
+size_t bwd_tc_split_bytes(int C);
+cudaError_t bwd_tc_split(const float* W, int C, int n_x, void* wsplit, cudaStream_t s, bool pdl);
+cudaError_t bwd_tc_prepare(int C, int* max_active_ctas);
+cudaError_t bwd_tc_launch(const BwdParams& p, cudaStream_t s, bool pdl);
 
 size_t bwd_smem_bytes(int R, int CS);
 cudaError_t bwd_prepare(int CS, int R, size_t smem, int* max_active_clusters);

@@ -36,6 +36,8 @@ RAGGED = [
                                        # a multiple of 16 (element-wise epilogue), ragged tiles
     dict(B=520, K=6, n_x=16, C=128),   # tensor-core forward, clusters of 4, last cluster 8 rows
     dict(B=600, K=5, n_x=24, C=256),   # tensor-core forward, clusters of 8, last cluster 88 rows
+    dict(B=1100, K=4, n_x=8, C=128),   # tensor-core BPTT, 9 CTAs, the last with 76 rows
+    dict(B=1030, K=3, n_x=16, C=256),  # tensor-core BPTT at the widest state, last CTA 6 rows
 ]
 
 
