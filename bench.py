@@ -91,6 +91,11 @@ def source_digest(paths):
     return h.hexdigest()[:16]
 
 
+def workload_tag(w) -> str:
+    """Short workload name used in the profile summaries' file names (e.g. pages_B32_K64)."""
+    return "_".join(w.name.split("_")[:3])
+
+
 def profiled_traffic(kernel: str, sources: list[str], workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
@@ -292,12 +297,17 @@ def main():
     # ---- per-stage device times: events between the four stage calls, L2 flushed first
     n_stage = min(args.steps, 200)
     i = st.inputs
+    # The BPTT stage with the same workspace-backed kernel choice as the step (tensor cores
+    # for large batches).
+    n_bptt_ws = _lib.bptt_workspace_bytes(w.B, w.K, w.C, w.n_x)
+    bptt_ws = torch.empty(n_bptt_ws, dtype=torch.uint8, device=dev) if n_bptt_ws else None
     stages = [
         ("proj", lambda: _lib.cfc_input_projection(i["u"], i["W"], i["b"], st.H, st.cache)),
         ("fwd_rec", lambda: _lib.cfc_forward_recurrence(i["h0"], i["W"], i["ts"], st.H,
                                                        st.cache)),
-        ("bwd_rec", lambda: _lib.cfc_backward_recurrence(i["dH"], i["W"], i["ts"], st.cache,
-                                                        st.d_pre, st.dh0)),
+        ("bwd_rec", lambda: _lib.cfc_backward_recurrence_ws(i["dH"], i["W"], i["ts"],
+                                                           st.cache, st.d_pre, st.dh0,
+                                                           bptt_ws)),
         ("grad", lambda: _lib.cfc_weight_grad(st.d_pre, i["u"], i["h0"], i["W"], st.H, st.dW,
                                              st.db, st.du, st.ws)),
     ]
@@ -325,19 +335,36 @@ def main():
                          "gbs": byt / (t * 1e-3) / 1e9}
     # The dominant kernel: the larger of the two recurrences (each stage is one launch).
     dominant = max(("fwd_rec", "bwd_rec"), key=lambda k: stage_ms[k])
-    kname = {"fwd_rec": "cfc_fwd_kernel", "bwd_rec": "cfc_bwd_kernel"}[dominant]
-    ksrc = {"fwd_rec": ["recurrent_cfc_cell_gb300/csrc/cfc_fwd.cu"],
-            "bwd_rec": ["recurrent_cfc_cell_gb300/csrc/cfc_bwd.cu"]}[dominant]
-    ksrc = ksrc + ["recurrent_cfc_cell_gb300/csrc/cfc_ptx.cuh",
-                   "recurrent_cfc_cell_gb300/csrc/cfc_kernels.h"]
+    # Which kernel that stage ran: the tensor-core recurrences serve batches of at least 512
+    # (forward) or 1024 (BPTT) rows at C = 128 or 256, the CUDA-core ones the rest.
+    tc_fwd = w.B >= 512 and w.C in (128, 256)
+    tc = tc_fwd if dominant == "fwd_rec" else n_bptt_ws > 0
+    kname = {("fwd_rec", False): "cfc_fwd_kernel", ("bwd_rec", False): "cfc_bwd_kernel",
+             ("fwd_rec", True): "cfc_fwd_tc_kernel",
+             ("bwd_rec", True): "cfc_bwd_tc_kernel"}[(dominant, tc)]
+    ksrc = ["recurrent_cfc_cell_gb300/csrc/" + kname[: -len("_kernel")] + ".cu",
+            "recurrent_cfc_cell_gb300/csrc/cfc_ptx.cuh",
+            "recurrent_cfc_cell_gb300/csrc/cfc_kernels.h"]
     achieved = kernels[dominant]["tflops"]
-    roofline = {"bound": "alu", "achieved": achieved, "peak": fp32_peak_tflops,
-                "unit": "TFLOP/s", "frac": achieved / fp32_peak_tflops,
-                "traffic": profiled_traffic(kname, ksrc, "pages_B32_K64"),
-                "kernel": kname,
-                "peak_note": f"fp32 FMA: {props.multi_processor_count} SMs x 128 lanes x 2 x "
-                             f"{pk['sm_max_mhz']:.0f} MHz",
-                "hbm_frac": kernels[dominant]["gbs"] / pk["hbm_gbs"]}
+    if tc:
+        # Algorithmic fp32-equivalent flops against the dense bf16 tensor peak; each product
+        # is issued as 3 (forward, fp16 terms) or 6 (BPTT, bf16 terms) MMAs.
+        n_mma = 3 if dominant == "fwd_rec" else 6
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                    "traffic": profiled_traffic(kname, ksrc, workload_tag(w)),
+                    "kernel": kname,
+                    "peak_note": f"dense bf16, {pk['source']}; {n_mma} MMAs per product, "
+                                 f"issued frac {n_mma * achieved / pk['bf16_tflops']:.3f}",
+                    "hbm_frac": kernels[dominant]["gbs"] / pk["hbm_gbs"]}
+    else:
+        roofline = {"bound": "alu", "achieved": achieved, "peak": fp32_peak_tflops,
+                    "unit": "TFLOP/s", "frac": achieved / fp32_peak_tflops,
+                    "traffic": profiled_traffic(kname, ksrc, workload_tag(w)),
+                    "kernel": kname,
+                    "peak_note": f"fp32 FMA: {props.multi_processor_count} SMs x 128 lanes x 2 x "
+                                 f"{pk['sm_max_mhz']:.0f} MHz",
+                    "hbm_frac": kernels[dominant]["gbs"] / pk["hbm_gbs"]}
 
     # ---- end to end through the public API with host buffers: every step copies its inputs
     # in from pinned host memory and its gradients out to pinned host memory (one packed copy

@@ -154,6 +154,29 @@ int cfc_backward_recurrence(const float* dH, const float* W, const float* ts,
                             float* dh0, cfc_stream_t stream);
 
 /*
+ * cfc_bptt_workspace_bytes -- bytes of device workspace cfc_backward_recurrence_ws takes for
+ * these sizes: for B >= 1024 and C = 128 or 256 the recurrence runs each step's contraction
+ * delta = d_pre W_h on the tensor cores and first writes W_h^T there as three bf16 terms
+ * (24 C^2 bytes); otherwise 0.  Writes *bytes; returns the argument codes of
+ * cfc_workspace_bytes.
+ */
+int cfc_bptt_workspace_bytes(int B, int K, int C, int n_x, size_t* bytes);
+
+/*
+ * cfc_backward_recurrence_ws -- cfc_backward_recurrence with a workspace, so that it takes
+ * the tensor-core recurrence where cfc_backward would (the same kernels, bitwise the same
+ * d_pre and dh0 as cfc_backward writes).  That path also needs dH, cache and d_pre 32-byte
+ * aligned; otherwise the CUDA-core recurrence runs.
+ *   ws, ws_bytes  device workspace of at least cfc_bptt_workspace_bytes() bytes, 16-byte
+ *                 aligned, owned by the caller (contents are scratch); may be NULL when that
+ *                 size is 0.  Too small: CFC_ERR_WS_TOO_SMALL before any launch.
+ * Other arguments and errors as for cfc_backward_recurrence.
+ */
+int cfc_backward_recurrence_ws(const float* dH, const float* W, const float* ts,
+                               const float* cache, int B, int K, int C, int n_x, float* d_pre,
+                               float* dh0, void* ws, size_t ws_bytes, cfc_stream_t stream);
+
+/*
  * cfc_weight_grad -- the second stage of cfc_backward alone: dW = sum_{t,b} d_pre z^T as one
  * contraction over the B*K rows (z = [u_t ; h_{t-1}], h_{-1} = h0), db = sum_{t,b} d_pre
  * through reduce_axis0, and du = W_u^T d_pre (skipped when du is NULL).  The weight gradient

@@ -22,7 +22,8 @@ CFC_DW_SIMT_FP32 = 2
 EXPORTED = ("cfc_workspace_bytes", "cfc_forward", "cfc_backward", "cfc_backward_recurrence",
             "cfc_weight_grad", "reduce_axis0", "cfc_error_string", "cfc_device_status",
             "cfc_backward_noalloc", "cfc_input_projection", "cfc_forward_recurrence",
-            "cfc_step_launches", "cfc_forward_backward")
+            "cfc_step_launches", "cfc_forward_backward", "cfc_bptt_workspace_bytes",
+            "cfc_backward_recurrence_ws")
 CFC_ERR_SCRATCH_LIMIT = -10
 NOALLOC_SCRATCH_BYTES = 32 << 20  # size of cfc_backward_noalloc's built-in device scratch
 
@@ -56,6 +57,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.cfc_forward_backward.restype = i
     lib.cfc_backward_recurrence.argtypes = [vp] * 4 + [i] * 4 + [vp, vp, vp]
     lib.cfc_backward_recurrence.restype = i
+    lib.cfc_bptt_workspace_bytes.argtypes = [i] * 4 + [vp]
+    lib.cfc_bptt_workspace_bytes.restype = i
+    lib.cfc_backward_recurrence_ws.argtypes = [vp] * 4 + [i] * 4 + [vp, vp, vp, sz, vp]
+    lib.cfc_backward_recurrence_ws.restype = i
     lib.cfc_weight_grad.argtypes = [vp] * 5 + [i] * 4 + [vp] * 4 + [sz, i, vp]
     lib.cfc_weight_grad.restype = i
     lib.reduce_axis0.argtypes = [vp, i, i, vp, vp]
@@ -206,6 +211,35 @@ def cfc_backward_recurrence(dH, W, ts, cache, d_pre, dh0, stream=None) -> None:
         _ptr(cache, "cache", (K, B, 3, C)), B, K, C, n_x, _ptr(d_pre, "d_pre", (K, B, 4, C)),
         _ptr(dh0, "dh0", (B, C)), _stream(stream))
     _check("cfc_backward_recurrence", rc)
+
+
+def bptt_workspace_bytes(B: int, K: int, C: int, n_x: int) -> int:
+    """Workspace bytes cfc_backward_recurrence_ws takes (0: the CUDA-core recurrence runs)."""
+    out = ctypes.c_size_t(0)
+    _check("cfc_bptt_workspace_bytes",
+           load().cfc_bptt_workspace_bytes(B, K, C, n_x, ctypes.byref(out)))
+    return int(out.value)
+
+
+def cfc_backward_recurrence_ws(dH, W, ts, cache, d_pre, dh0, ws=None, stream=None) -> None:
+    """As cfc_backward_recurrence, with a workspace (a uint8 CUDA tensor of at least
+    bptt_workspace_bytes(B, K, C, n_x) bytes, or None when that is 0) so that large batches
+    take the tensor-core recurrence."""
+    import torch
+
+    K, B, C = dH.shape
+    n_x = W.shape[2] - C
+    if ws is None:
+        wp, wn = None, 0
+    else:
+        if ws.dtype != torch.uint8 or not ws.is_cuda or not ws.is_contiguous():
+            raise ValueError("ws must be a contiguous uint8 CUDA tensor")
+        wp, wn = ctypes.c_void_p(ws.data_ptr()), ws.numel()
+    rc = load().cfc_backward_recurrence_ws(
+        _ptr(dH, "dH", (K, B, C)), _ptr(W, "W", (4, C, n_x + C)), _ptr(ts, "ts", (K, B)),
+        _ptr(cache, "cache", (K, B, 3, C)), B, K, C, n_x, _ptr(d_pre, "d_pre", (K, B, 4, C)),
+        _ptr(dh0, "dh0", (B, C)), wp, wn, _stream(stream))
+    _check("cfc_backward_recurrence_ws", rc)
 
 
 def cfc_weight_grad(d_pre, u, h0, W, H, dW, db, du, ws, dw_mode: int = CFC_DW_ACCURATE,

@@ -403,6 +403,29 @@ int cfc_backward_recurrence(const float* dH, const float* W, const float* ts,
   return backward_recurrence(dH, W, ts, cache, B, K, C, n_x, d_pre, dh0, stream, false);
 }
 
+int cfc_bptt_workspace_bytes(int B, int K, int C, int n_x, size_t* bytes) {
+  const int rc = check_dims(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (!bytes) return CFC_ERR_NULL_PTR;
+  *bytes = bwd_layout(B, K, C, n_x).tc_bptt ? cfc::bwd_tc_split_bytes(C) : 0;
+  return CFC_OK;
+}
+
+int cfc_backward_recurrence_ws(const float* dH, const float* W, const float* ts,
+                               const float* cache, int B, int K, int C, int n_x, float* d_pre,
+                               float* dh0, void* ws, size_t ws_bytes, cfc_stream_t stream) {
+  size_t need = 0;
+  const int rc = cfc_bptt_workspace_bytes(B, K, C, n_x, &need);
+  if (rc != CFC_OK) return rc;
+  if (need > 0) {
+    if (!ws) return CFC_ERR_NULL_PTR;
+    if (!aligned16(ws)) return CFC_ERR_MISALIGNED;
+    if (ws_bytes < need) return CFC_ERR_WS_TOO_SMALL;
+  }
+  return backward_recurrence(dH, W, ts, cache, B, K, C, n_x, d_pre, dh0, stream, false,
+                             need > 0 ? ws : nullptr);
+}
+
 }  // extern "C"
 
 namespace {

@@ -8,9 +8,10 @@
 // owns 128 batch rows outright and no data crosses CTAs:
 //   tensor memory  two fp32 accumulators [128 rows (lanes) x C channels]: delta[t+1], read by
 //                  the epilogue, and delta[t], being accumulated (they swap every step);
-//   shared memory  two stages, each one 32-deep chunk of the reduction: the d_pre chunk
-//                  [128 rows x 32 gate rows] (A) and the W_h^T chunk [C x 32 gate rows] (B),
-//                  both in three bf16 terms in the non-swizzled K-major layout.
+//   shared memory  as many stages as fit (3 at C = 256, 4 at C = 128), each one 32-deep chunk
+//                  of the reduction: the d_pre chunk [128 rows x 32 gate rows] (A) and the
+//                  W_h^T chunk [C x 32 gate rows] (B), both in three bf16 terms in the
+//                  non-swizzled K-major layout.
 // The reduction index runs channel-major (k = 4 c + g), so a chunk is 8 channels x 4 gates.
 // Eight epilogue warps turn delta[t+1] plus dH and the cache into d_pre chunk by chunk, the two
 // warps of a tensor-memory lane quarter taking alternate chunks (one row and 8 channels per
@@ -32,7 +33,6 @@ namespace {
 
 constexpr int kBM = 128;                          // batch rows per CTA (MMA M)
 constexpr int kBK = 32;                           // reduction entries per chunk
-constexpr int kBStages = 2;
 constexpr int kBEpiWarps = 8;                     // two per tensor-memory lane quarter
 constexpr int kBThreads = (kBEpiWarps + 1) * 32;  // + one control warp
 constexpr int kBTerms = 3;
@@ -43,7 +43,10 @@ struct BtShape {
   static constexpr int A_TERM = kBM * kBK * 2;    // bytes of one bf16 term of a d_pre chunk
   static constexpr int B_TERM = C * kBK * 2;      // bytes of one bf16 term of a W_h^T chunk
   static constexpr int STAGE = kBTerms * (A_TERM + B_TERM);
-  static constexpr int USED = kBStages * STAGE + (3 * kBStages + 1) * 8 + 16 + 128;
+  // Stages: as many as fit beside the barriers in 227 KB, at most 4.
+  static constexpr int NST_FIT = (227 * 1024 - 512) / STAGE;
+  static constexpr int NST = NST_FIT < 4 ? NST_FIT : 4;
+  static constexpr int USED = NST * STAGE + (3 * NST + 1) * 8 + 16 + 128;
   // At least half an SM's shared memory: each CTA takes all 512 tensor-memory columns.
   static constexpr int SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
   static constexpr size_t SPLIT = static_cast<size_t>(NCH) * kBTerms * B_TERM;
@@ -145,21 +148,23 @@ __global__ void __launch_bounds__(kBThreads, 1) cfc_bwd_tc_kernel(const BwdParam
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t* sm = smem_raw + ((128u - (raw & 127u)) & 127u);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBStages * S::STAGE);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * kBStages + 1);
+  constexpr int NST = S::NST;
+  static_assert(NST >= 2, "two stages at least");
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + NST * S::STAGE);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * NST + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row0 = blockIdx.x * kBM;
   const int B = p.B, K = p.K;
   const uint32_t fa0 = smem_addr(&bars[0]);              // full_a[s]: d_pre chunk written
-  const uint32_t fb0 = smem_addr(&bars[kBStages]);       // full_b[s]: W_h^T chunk landed
-  const uint32_t em0 = smem_addr(&bars[2 * kBStages]);   // empty[s]: chunk's MMAs done
-  const uint32_t done_bar = smem_addr(&bars[3 * kBStages]);  // a step's delta complete
+  const uint32_t fb0 = smem_addr(&bars[NST]);            // full_b[s]: W_h^T chunk landed
+  const uint32_t em0 = smem_addr(&bars[2 * NST]);        // empty[s]: chunk's MMAs done
+  const uint32_t done_bar = smem_addr(&bars[3 * NST]);   // a step's delta complete
   const uint32_t sm0 = smem_addr(sm);
 
   grid_dep_launch_dependents();
   if (tid == 0) {
-    for (int s = 0; s < kBStages; ++s) {
-      mbar_init(fa0 + 8u * s, kBEpiWarps * 32 / kBStages);  // one warp group per stage
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(fa0 + 8u * s, kBEpiWarps * 32 / 2);  // a chunk is written by one warp group
       mbar_init(fb0 + 8u * s, 1);
       mbar_init(em0 + 8u * s, 1);
     }
@@ -187,8 +192,8 @@ __global__ void __launch_bounds__(kBThreads, 1) cfc_bwd_tc_kernel(const BwdParam
         const uint32_t dcur = tmem + static_cast<uint32_t>((n & 1) * C);
         uint32_t acc = 0;
         for (int kc = 0; kc < S::NCH; ++kc) {
-          const int i = n * S::NCH + kc, s = i & 1;
-          const uint32_t ph = (i >> 1) & 1;
+          const int i = n * S::NCH + kc, s = i % NST;
+          const uint32_t ph = (i / NST) & 1;
           ok = mbar_wait_bounded_cta(fa0 + 8u * s, ph, p.status) &&
                mbar_wait_bounded_cta(fb0 + 8u * s, ph, p.status);
           if (!ok) break;
@@ -220,9 +225,8 @@ __global__ void __launch_bounds__(kBThreads, 1) cfc_bwd_tc_kernel(const BwdParam
       bool ok = true;
       for (int n = 0; n < K && ok; ++n) {
         for (int kc = 0; kc < S::NCH; ++kc) {
-          const int i = n * S::NCH + kc, s = i & 1;
-          if (i >= kBStages) ok = mbar_wait_bounded_cta(em0 + 8u * s, ((i - kBStages) >> 1) & 1,
-                                                        p.status);
+          const int i = n * S::NCH + kc, s = i % NST;
+          if (i >= NST) ok = mbar_wait_bounded_cta(em0 + 8u * s, (i / NST - 1) & 1, p.status);
           if (!ok) break;
           mbar_arrive_expect_tx(fb0 + 8u * s, kBTerms * S::B_TERM);
           const uint32_t dst = sm0 + s * S::STAGE + kBTerms * S::A_TERM;
@@ -236,9 +240,8 @@ __global__ void __launch_bounds__(kBThreads, 1) cfc_bwd_tc_kernel(const BwdParam
     }
   } else {
     // ---- epilogue warps: row r = 32 q + lane.  Warp group hh (warps 4 hh .. 4 hh + 3, one per
-    // lane quarter) takes the chunks kc with kc % 2 == hh -- always stage hh, as a step has an
-    // even number of chunks -- and all 8 channels of each, so every global access is a whole
-    // 32-byte sector. ----
+    // lane quarter) takes the chunks kc with kc % 2 == hh and all 8 channels of each, so every
+    // global access is a whole 32-byte sector. ----
     const int q = warp & 3, hh = warp >> 2;
     const int r = 32 * q + lane, b = row0 + r;
     const bool rok = b < B;
@@ -263,8 +266,6 @@ __global__ void __launch_bounds__(kBThreads, 1) cfc_bwd_tc_kernel(const BwdParam
     bool ok = true;
     float cur[4][8], nxt[4][8];
     load8(K - 1, hh, cur);
-    const int s = hh;
-    uint8_t* ast = sm + s * S::STAGE;
     for (int n = 0; n < K && ok; ++n) {
       const int t = K - 1 - n;
       if (n > 0) {
@@ -279,11 +280,6 @@ __global__ void __launch_bounds__(kBThreads, 1) cfc_bwd_tc_kernel(const BwdParam
         // This group's next chunk in flight while this one is worked on.
         if (kc + 2 < S::NCH) load8(t, kc + 2, nxt);
         else if (t > 0) load8(t - 1, hh, nxt);
-        const int i = n * S::NCH + kc;
-        if (i >= kBStages) {
-          ok = mbar_wait_bounded_cta(em0 + 8u * s, ((i - kBStages) >> 1) & 1, p.status);
-          if (!ok) break;
-        }
         float dl[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (n > 0) tmem_ld8(dprev + 8 * kc, dl);
         float pv[4][8];  // [gate][channel]
@@ -299,12 +295,14 @@ __global__ void __launch_bounds__(kBThreads, 1) cfc_bwd_tc_kernel(const BwdParam
         }
         if (rok) {
 #pragma unroll
-          for (int gg = 0; gg < 4; ++gg) st_global_v8(dpp + static_cast<size_t>(gg) * C + 8 * kc, pv[gg]);
+          for (int gg = 0; gg < 4; ++gg)
+            st_global_v8(dpp + static_cast<size_t>(gg) * C + 8 * kc, pv[gg]);
         }
-        // d_pre chunk entries k = 4 c + gg: k-core kq holds channels 2 kq, 2 kq + 1.
+        // The chunk's operand terms, ready before the stage is free.  Entries k = 4 c + gg:
+        // k-core kq holds channels 2 kq and 2 kq + 1.
+        uint32_t w[4][kBTerms][4];
 #pragma unroll
-        for (int kq = 0; kq < 4; ++kq) {
-          uint32_t w[kBTerms][4];
+        for (int kq = 0; kq < 4; ++kq)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int c = 2 * kq + e2;
@@ -312,15 +310,23 @@ __global__ void __launch_bounds__(kBThreads, 1) cfc_bwd_tc_kernel(const BwdParam
             const Split3 s2 = split3(pv[2][c]), s3 = split3(pv[3][c]);
 #pragma unroll
             for (int tm = 0; tm < kBTerms; ++tm) {
-              w[tm][2 * e2] = pack_bf2(s0.t[tm], s1.t[tm]);
-              w[tm][2 * e2 + 1] = pack_bf2(s2.t[tm], s3.t[tm]);
+              w[kq][tm][2 * e2] = pack_bf2(s0.t[tm], s1.t[tm]);
+              w[kq][tm][2 * e2 + 1] = pack_bf2(s2.t[tm], s3.t[tm]);
             }
           }
+        const int i = n * S::NCH + kc, s = i % NST;
+        if (i >= NST) {  // the stage's previous chunk consumed by its MMAs
+          ok = mbar_wait_bounded_cta(em0 + 8u * s, (i / NST - 1) & 1, p.status);
+          if (!ok) break;
+        }
+        uint8_t* ast = sm + s * S::STAGE;
+#pragma unroll
+        for (int kq = 0; kq < 4; ++kq) {
           const uint32_t off = kmajor_offset(r, 8 * kq, kBM);
 #pragma unroll
           for (int tm = 0; tm < kBTerms; ++tm)
             *reinterpret_cast<uint4*>(ast + tm * S::A_TERM + off) =
-                make_uint4(w[tm][0], w[tm][1], w[tm][2], w[tm][3]);
+                make_uint4(w[kq][tm][0], w[kq][tm][1], w[kq][tm][2], w[kq][tm][3]);
         }
         fence_proxy_async_smem();  // the chunk -> visible to the MMAs (async proxy)
         tc_fence_before_sync();    // this chunk's tensor-memory loads precede the arrive

@@ -126,6 +126,35 @@ def test_forward_backward_is_forward_then_backward(shape):
     assert_parity(out, oracle_ref(inp))
 
 
+@pytest.mark.parametrize("shape", [dict(B=1100, K=4, n_x=8, C=128), dict(B=7, K=11, n_x=13, C=100)],
+                         ids=lambda s: "B{B}_K{K}_nx{n_x}_C{C}".format(**s))
+def test_backward_recurrence_ws_is_cfc_backwards_recurrence(shape):
+    """cfc_backward_recurrence_ws (tensor cores at B >= 1024) writes bitwise the d_pre and dh0
+    that cfc_backward writes, and they match the oracle."""
+    import torch
+
+    from recurrent_cfc_cell_gb300 import _lib, build
+    from recurrent_cfc_cell_gb300.step import KLoopStep, to_device
+
+    build.build()
+    inp = inputs.make_inputs(inputs.custom(seed=29, **shape))
+    d = to_device(inp)
+    B, K, C, n_x = shape["B"], shape["K"], shape["C"], shape["n_x"]
+    a = KLoopStep(B, K, C, n_x).bind(**d)
+    a.run()
+    n = _lib.bptt_workspace_bytes(B, K, C, n_x)
+    assert (n > 0) == (B >= 1024)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda") if n else None
+    d_pre = torch.full((K, B, 4, C), float("nan"), device="cuda")
+    dh0 = torch.full((B, C), float("nan"), device="cuda")
+    _lib.cfc_backward_recurrence_ws(d["dH"], d["W"], d["ts"], a.cache, d_pre, dh0, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(d_pre, a.d_pre)
+    assert torch.equal(dh0, a.dh0)
+    assert_parity({"d_pre": d_pre.cpu().numpy(), "dh0": dh0.cpu().numpy()}, oracle_ref(inp),
+                  keys=("d_pre", "dh0"))
+
+
 def test_graph_replay_parity():
     inp = inputs.make_inputs(inputs.CONFIGS[1])
     assert_parity(run_gpu(inp, graph=True), oracle_ref(inp))
