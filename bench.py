@@ -42,11 +42,29 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", type=int, default=1)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's B (a smaller case of it, e.g. for profiling)")
+    ap.add_argument("--seq", type=int, default=None, help="override the workload's K")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
+
+
+def workload(args):
+    """The selected workload, with B / K overridden when asked (renamed after its sizes)."""
+    import dataclasses
+
+    from recurrent_cfc_cell_gb300 import inputs
+
+    w = inputs.CONFIGS[args.workload]
+    if args.batch is None and args.seq is None:
+        return w
+    B = args.batch if args.batch is not None else w.B
+    K = args.seq if args.seq is not None else w.K
+    name = f"{w.name.split('_')[0]}_B{B}_K{K}_nx{w.n_x}_C{w.C}"
+    return dataclasses.replace(w, name=name, B=B, K=K)
 
 
 def dist_env():
@@ -177,7 +195,7 @@ def run_reference(args, rank, world):
     import oracle
     from recurrent_cfc_cell_gb300 import inputs
 
-    w = inputs.CONFIGS[args.workload]
+    w = workload(args)
     inp = inputs.make_inputs(w)
     # calibrate one single-row oracle step, then size each step's sample so the whole run
     # stays near a minute of CPU work
@@ -254,7 +272,7 @@ def main():
         dist.barrier()
     _lib.load()
 
-    w = inputs.CONFIGS[args.workload]
+    w = workload(args)
     inp = inputs.make_inputs(w)
     dinp = to_device(inp, dev)
     st = KLoopStep(w.B, w.K, w.C, w.n_x, device=dev).bind(**dinp)
