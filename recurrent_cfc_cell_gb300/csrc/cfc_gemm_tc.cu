@@ -255,19 +255,34 @@ struct DuProblem : RowMajorOut {
     v[0] = q0.x; v[1] = q0.y; v[2] = q0.z; v[3] = q0.w;
     v[4] = q1.x; v[5] = q1.y; v[6] = q1.z; v[7] = q1.w;
   }
+  // All four A items of a thread and its first B quad are loaded before the first store, so
+  // a stage costs one memory round trip (n_tile <= 128; wider tiles take a second for B).
   static __device__ __forceinline__ void convert(const TcParams& p, uint8_t* a_hi, uint8_t* a_lo,
                                                  uint8_t* b_hi, uint8_t* b_lo, int r0, int n0,
                                                  int m0, int tid) {
-    for (int it = tid; it < kTcM * 8; it += 2 * kConv) {
-      const int it1 = it + kConv;  // kTcM * 8 is a multiple of 2 * kConv
-      float v0[8], v1[8];
-      load_row_chunk(p, r0 + (it >> 3), m0 + 8 * (it & 7), v0);
-      load_row_chunk(p, r0 + (it1 >> 3), m0 + 8 * (it1 & 7), v1);
-      store_split_chunk(a_hi, a_lo, it >> 3, it & 7, v0);
-      store_split_chunk(a_hi, a_lo, it1 >> 3, it1 & 7, v1);
+    static_assert(kTcM * 8 == 4 * kConv, "four A items per thread");
+    const int nB = p.n_tile / 4 * 8;
+    float va[4][8], vb[4][8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int it = tid + j * kConv;
+      load_row_chunk(p, r0 + (it >> 3), m0 + 8 * (it & 7), va[j]);
     }
-    convert_quads(p.n_tile / 4, n0, m0, tid, b_hi, b_lo,
-                  [&](int n, int mc, float (&v)[4][8]) { load_wu_quad(p, n, mc, v); });
+    if (tid < nB) load_wu_quad(p, n0 + 4 * (tid >> 3), m0 + 8 * (tid & 7), vb);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int it = tid + j * kConv;
+      store_split_chunk(a_hi, a_lo, it >> 3, it & 7, va[j]);
+    }
+    if (tid < nB) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) store_split_chunk(b_hi, b_lo, 4 * (tid >> 3) + q, tid & 7, vb[q]);
+    }
+    for (int it = tid + kConv; it < nB; it += kConv) {
+      load_wu_quad(p, n0 + 4 * (it >> 3), m0 + 8 * (it & 7), vb);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) store_split_chunk(b_hi, b_lo, 4 * (it >> 3) + q, it & 7, vb[q]);
+    }
   }
 };
 
@@ -496,9 +511,11 @@ TcPlan tc_plan(int rows, int cols, int red, bool split, int terms = 2, int stage
   const int tiles = pl.m_tiles * pl.n_tiles;
   int s0 = 1;
   if (split) {
-    s0 = (148 + tiles - 1) / tiles;  // a fixed target (not the device's SM count): the
-    if (s0 > pl.n_kb) s0 = pl.n_kb;  // split -- hence the summation order -- depends only
-  }                                  // on the sizes
+    // At most one wave of 148 CTAs (a fixed target, not the device's SM count: the split --
+    // hence the summation order -- depends only on the sizes).
+    s0 = tiles < 148 ? 148 / tiles : 1;
+    if (s0 > pl.n_kb) s0 = pl.n_kb;
+  }
   pl.kb_per_split = (pl.n_kb + s0 - 1) / s0;
   pl.splits = (pl.n_kb + pl.kb_per_split - 1) / pl.kb_per_split;
   pl.smem = static_cast<size_t>(stages) * terms * (kTcM + pl.n_tile) * 128 + 1024 + 128;
