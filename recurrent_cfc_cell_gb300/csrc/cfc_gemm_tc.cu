@@ -225,13 +225,15 @@ struct RowMajorOut {
   }
 };
 
-// Weight gradient: A = d_pre^T (rows m, reduction r), B = z^T (rows n, reduction r).
+// Weight gradient: A = d_pre^T (rows m, reduction r), B = z^T (rows n, reduction r).  With
+// MT = 2 a CTA keeps two 128-row accumulators that share every converted z tile.
+template <int MT>
 struct DwProblem : RowMajorOut {
-  static constexpr int kTerms = 2, kStages = 2;
+  static constexpr int kTerms = 2, kStages = 2, kMT = MT;
   static __device__ __forceinline__ void convert(const TcParams& p, uint8_t* a_hi, uint8_t* a_lo,
                                                  uint8_t* b_hi, uint8_t* b_lo, int m0, int n0,
                                                  int r0, int tid) {
-    convert_quads(kTcM / 4, m0, r0, tid, a_hi, a_lo,
+    convert_quads(kTcM * MT / 4, m0, r0, tid, a_hi, a_lo,
                   [&](int m, int rc, float (&v)[4][8]) { load_dpre_quad(p, m, rc, v); });
     convert_quads(p.n_tile / 4, n0, r0, tid, b_hi, b_lo,
                   [&](int n, int rc, float (&v)[4][8]) { load_z_quad(p, n, rc, v); });
@@ -242,7 +244,7 @@ struct DwProblem : RowMajorOut {
 // reduction m).  A items are (row, 8-entry chunk), two per thread at a time, loads first; a
 // quarter-warp covers the 8 chunks of a row.
 struct DuProblem : RowMajorOut {
-  static constexpr int kTerms = 2, kStages = 2;
+  static constexpr int kTerms = 2, kStages = 2, kMT = 1;
   static __device__ __forceinline__ void load_row_chunk(const TcParams& p, int r, int m,
                                                         float (&v)[8]) {
     const int M = 4 * p.C;
@@ -297,7 +299,7 @@ struct DuProblem : RowMajorOut {
 // dropped terms are below 2^-24 of the product).  The reduction (n_x <= 512) is at most eight
 // 64-entry blocks, and one stage of six tiles fits in shared memory.
 struct ProjProblem {
-  static constexpr int kTerms = 3, kStages = 1;
+  static constexpr int kTerms = 3, kStages = 1, kMT = 1;
   // Entries k .. k+7 of a row of `width` valid values (zero beyond), as two float4 loads when
   // the row start is 16-byte aligned.
   static __device__ __forceinline__ void load8(const float* row, int k, int width, bool vec,
@@ -382,8 +384,10 @@ __device__ __forceinline__ void tc_gemm_body(const TcParams& p, int tile, int sp
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   constexpr int kStages = Problem::kStages, kTerms = Problem::kTerms;
-  // Stage: kTerms A tiles [kTcM rows x 128 B], then kTerms B tiles [n_tile rows x 128 B].
-  const int stage_bytes = kTerms * (kTcM + p.n_tile) * 128;
+  // Stage: kTerms A tiles [mt kTcM rows x 128 B], then kTerms B tiles [n_tile rows x 128 B].
+  constexpr int kMT = Problem::kMT;
+  constexpr int a_rows = kTcM * kMT;
+  const int stage_bytes = kTerms * (a_rows + p.n_tile) * 128;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + kStages * stage_bytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 1);
   const uint32_t full0 = smem_addr(&bars[0]);             // full[s]  = full0 + 8 s
@@ -392,12 +396,15 @@ __device__ __forceinline__ void tc_gemm_body(const TcParams& p, int tile, int sp
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int m0 = (tile % p.m_tiles) * kTcM;
+  const int m0 = (tile % p.m_tiles) * a_rows;
   const int n0 = (tile / p.m_tiles) * p.n_tile;
   const int kb0 = split * p.kb_per_split;
   const int nk = min(p.kb_per_split, p.n_kb - kb0);
-  uint32_t ncols = 32;
-  while (ncols < static_cast<uint32_t>(p.n_tile)) ncols <<= 1;
+  // Accumulator j (rows m0 + 128 j ..) starts at tensor-memory column j * acc_cols, a power
+  // of two (each accumulator where a single one would be allocated).
+  uint32_t acc_cols = 32;
+  while (acc_cols < static_cast<uint32_t>(p.n_tile)) acc_cols <<= 1;
+  const uint32_t ncols = acc_cols * kMT;
 
   grid_dep_launch_dependents();
   if (tid == 0) {
@@ -428,8 +435,8 @@ __device__ __forceinline__ void tc_gemm_body(const TcParams& p, int tile, int sp
         ok = mbar_wait_bounded_cta(empty0 + 8u * s, ((i - kStages) / kStages) & 1u, p.status);
       if (!ok) break;
       uint8_t* st = base + s * stage_bytes;
-      Problem::convert(p, st, st + kTcM * 128, st + kTerms * kTcM * 128,
-                       st + kTerms * kTcM * 128 + p.n_tile * 128, m0, n0, (kb0 + i) * kTcK, tid);
+      Problem::convert(p, st, st + a_rows * 128, st + kTerms * a_rows * 128,
+                       st + kTerms * a_rows * 128 + p.n_tile * 128, m0, n0, (kb0 + i) * kTcK, tid);
       fence_proxy_async_smem();
       mbar_arrive(full0 + 8u * s);
     }
@@ -438,12 +445,14 @@ __device__ __forceinline__ void tc_gemm_body(const TcParams& p, int tile, int sp
     if (ok) ok = mbar_wait_bounded_cta(accb, 0, p.status);
     tc_fence_after_sync();
     const int quarter = warp & 3;  // TMEM lanes this warp may read
-    const int m = m0 + 32 * quarter + lane;
-    for (int c0 = 16 * (warp >> 2); c0 < p.n_tile; c0 += 32) {
-      float v[16];
-      tmem_ld16(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + c0, v);
-      if (!ok || m >= p.rows) continue;
-      Problem::store16(p, split, m, n0 + c0, v);
+    for (int j = 0; j < kMT; ++j) {
+      const int m = m0 + kTcM * j + 32 * quarter + lane;
+      for (int c0 = 16 * (warp >> 2); c0 < p.n_tile; c0 += 32) {
+        float v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + j * acc_cols + c0, v);
+        if (!ok || m >= p.rows) continue;
+        Problem::store16(p, split, m, n0 + c0, v);
+      }
     }
   } else if (lane == 0) {
     // ---- MMA issuer ----
@@ -456,22 +465,27 @@ __device__ __forceinline__ void tc_gemm_body(const TcParams& p, int tile, int sp
       if (!ok) break;
       tc_fence_after_sync();
       const uint32_t st = smem_addr(base + s * stage_bytes);
-      const uint32_t a_hi = st, a_lo = st + kTcM * 128;
-      const uint32_t b_hi = st + kTerms * kTcM * 128, b_lo = b_hi + p.n_tile * 128;
+      const uint32_t b_hi = st + kTerms * a_rows * 128, b_lo = b_hi + p.n_tile * 128;
 #pragma unroll
-      for (int j = 0; j < kTcK / 16; ++j) {
-        const uint32_t koff = 32u * j;
-        umma_bf16(tmem, umma_desc_sw128(a_hi + koff), umma_desc_sw128(b_hi + koff), idesc, acc);
-        acc = 1;
-        umma_bf16(tmem, umma_desc_sw128(a_hi + koff), umma_desc_sw128(b_lo + koff), idesc, 1);
-        umma_bf16(tmem, umma_desc_sw128(a_lo + koff), umma_desc_sw128(b_hi + koff), idesc, 1);
-        if constexpr (kTerms == 3) {  // a_lo / b_lo hold the mid terms; lo follows them
-          const uint32_t a_l3 = a_lo + kTcM * 128, b_l3 = b_lo + p.n_tile * 128;
-          umma_bf16(tmem, umma_desc_sw128(a_hi + koff), umma_desc_sw128(b_l3 + koff), idesc, 1);
-          umma_bf16(tmem, umma_desc_sw128(a_l3 + koff), umma_desc_sw128(b_hi + koff), idesc, 1);
-          umma_bf16(tmem, umma_desc_sw128(a_lo + koff), umma_desc_sw128(b_lo + koff), idesc, 1);
+      for (int mj = 0; mj < kMT; ++mj) {  // accumulator mj: A rows 128 mj .. 128 mj + 127
+        const uint32_t d = tmem + mj * acc_cols;
+        const uint32_t a_hi = st + mj * kTcM * 128, a_lo = a_hi + a_rows * 128;
+#pragma unroll
+        for (int j = 0; j < kTcK / 16; ++j) {
+          const uint32_t koff = 32u * j;
+          umma_bf16(d, umma_desc_sw128(a_hi + koff), umma_desc_sw128(b_hi + koff), idesc,
+                    acc | static_cast<uint32_t>(j > 0));
+          umma_bf16(d, umma_desc_sw128(a_hi + koff), umma_desc_sw128(b_lo + koff), idesc, 1);
+          umma_bf16(d, umma_desc_sw128(a_lo + koff), umma_desc_sw128(b_hi + koff), idesc, 1);
+          if constexpr (kTerms == 3) {  // a_lo / b_lo hold the mid terms; lo follows them
+            const uint32_t a_l3 = a_lo + a_rows * 128, b_l3 = b_lo + p.n_tile * 128;
+            umma_bf16(d, umma_desc_sw128(a_hi + koff), umma_desc_sw128(b_l3 + koff), idesc, 1);
+            umma_bf16(d, umma_desc_sw128(a_l3 + koff), umma_desc_sw128(b_hi + koff), idesc, 1);
+            umma_bf16(d, umma_desc_sw128(a_lo + koff), umma_desc_sw128(b_lo + koff), idesc, 1);
+          }
         }
       }
+      acc = 1;
       umma_commit(empty0 + 8u * s);  // stage reusable once these MMAs have read it
     }
     umma_commit(accb);  // accumulator complete (also after an early stop)
@@ -492,21 +506,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcParams p
 // Both contractions in one grid: the first n_w CTAs take the weight-gradient tiles and splits,
 // the rest the input-gradient tiles and splits.  They read the same d_pre and write disjoint
 // outputs, so one launch replaces two dependent ones.
+template <int MT>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_dual_kernel(const TcParams pw,
                                                                 const TcParams pu, int n_w) {
   const int b = blockIdx.x;
   const int tiles_w = pw.m_tiles * ((pw.cols + pw.n_tile - 1) / pw.n_tile);
   const int tiles_u = pu.m_tiles * ((pu.cols + pu.n_tile - 1) / pu.n_tile);
-  if (b < n_w) tc_gemm_body<DwProblem>(pw, b % tiles_w, b / tiles_w);
+  if (b < n_w) tc_gemm_body<DwProblem<MT>>(pw, b % tiles_w, b / tiles_w);
   else tc_gemm_body<DuProblem>(pu, (b - n_w) % tiles_u, (b - n_w) / tiles_u);
 }
 
 
-TcPlan tc_plan(int rows, int cols, int red, bool split, int terms = 2, int stages = 2) {
+TcPlan tc_plan(int rows, int cols, int red, bool split, int terms = 2, int stages = 2,
+               int mt = 1) {
   TcPlan pl;
+  pl.mt = mt;
   pl.n_tiles = (cols + 255) / 256;
   pl.n_tile = (((cols + pl.n_tiles - 1) / pl.n_tiles) + 15) & ~15;
-  pl.m_tiles = (rows + kTcM - 1) / kTcM;
+  pl.m_tiles = (rows + kTcM * mt - 1) / (kTcM * mt);
   pl.n_kb = (red + kTcK - 1) / kTcK;
   const int tiles = pl.m_tiles * pl.n_tiles;
   int s0 = 1;
@@ -518,14 +535,20 @@ TcPlan tc_plan(int rows, int cols, int red, bool split, int terms = 2, int stage
   }
   pl.kb_per_split = (pl.n_kb + s0 - 1) / s0;
   pl.splits = (pl.n_kb + pl.kb_per_split - 1) / pl.kb_per_split;
-  pl.smem = static_cast<size_t>(stages) * terms * (kTcM + pl.n_tile) * 128 + 1024 + 128;
+  pl.smem = static_cast<size_t>(stages) * terms * (kTcM * mt + pl.n_tile) * 128 + 1024 + 128;
   return pl;
 }
 
 }  // namespace
 
 TcPlan dw_tc_plan(int B, int K, int C, int n_x) {
-  return tc_plan(4 * C, dw_tc_pitch(n_x + C), B * K, true);
+  // For long reductions each CTA keeps two 128-row accumulators that share every converted
+  // z tile, so z is read once per 256 rows of dW instead of once per 128.  Two stages of
+  // 2 x (256 + n_tile) rows of 128 bytes fit in shared memory up to n_tile = 192.
+  const TcPlan one = tc_plan(4 * C, dw_tc_pitch(n_x + C), B * K, true);
+  if (4 * C >= 2 * kTcM && B * K >= 8192 && one.n_tile <= 192)
+    return tc_plan(4 * C, dw_tc_pitch(n_x + C), B * K, true, 2, 2, 2);
+  return one;
 }
 TcPlan du_tc_plan_unsplit(int B, int K, int C, int n_x) {
   return tc_plan(B * K, n_x, 4 * C, false);
@@ -550,12 +573,15 @@ void dwdu_tc_plans(int B, int K, int C, int n_x, TcPlan* pw, TcPlan* pu) {
 }
 
 cudaError_t tc_prepare(int max_smem) {
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<DwProblem>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc_dual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           max_smem);
-  if (e != cudaSuccess) return e;
+  const void* kernels[] = {reinterpret_cast<const void*>(tc_gemm_kernel<DwProblem<1>>),
+                           reinterpret_cast<const void*>(tc_gemm_kernel<DwProblem<2>>),
+                           reinterpret_cast<const void*>(tc_dual_kernel<1>),
+                           reinterpret_cast<const void*>(tc_dual_kernel<2>)};
+  for (const void* k : kernels) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e != cudaSuccess) return e;
+  }
   return cudaFuncSetAttribute(tc_gemm_kernel<ProjProblem>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
 }
@@ -585,7 +611,8 @@ cudaError_t dw_tc_launch(const TcPlan& pl, const float* d_pre, const float* u, c
   c.smem = pl.smem;
   c.stream = s;
   c.pdl = pdl;
-  return launch(c, tc_gemm_kernel<DwProblem>, p);
+  return pl.mt == 2 ? launch(c, tc_gemm_kernel<DwProblem<2>>, p)
+                    : launch(c, tc_gemm_kernel<DwProblem<1>>, p);
 }
 
 TcPlan proj_tc_plan(int B, int K, int C, int n_x) {
@@ -624,7 +651,8 @@ cudaError_t dwdu_tc_launch(const TcPlan& pw, const TcPlan& pu, const float* d_pr
   c.smem = pw.smem > pu.smem ? pw.smem : pu.smem;
   c.stream = s;
   c.pdl = pdl;
-  return launch(c, tc_dual_kernel, a, b, n_w);
+  return pw.mt == 2 ? launch(c, tc_dual_kernel<2>, a, b, n_w)
+                    : launch(c, tc_dual_kernel<1>, a, b, n_w);
 }
 
 }  // namespace cfc

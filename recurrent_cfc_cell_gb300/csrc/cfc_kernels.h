@@ -88,6 +88,7 @@ cudaError_t dw_simt_launch(const float* d_pre, const float* u, const float* H, c
 // dW and du on tcgen05 tensor cores (bf16 hi/lo split, fp32 accumulation in TMEM).
 struct TcPlan {
   int n_tiles, n_tile, m_tiles, n_kb, kb_per_split, splits;
+  int mt;  // 128-row accumulators per CTA (1, or 2 for the weight gradient at large B*K)
   size_t smem;
 };
 TcPlan dw_tc_plan(int B, int K, int C, int n_x);  // split over the B*K rows

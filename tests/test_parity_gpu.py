@@ -160,8 +160,11 @@ def test_graph_replay_parity():
     assert_parity(run_gpu(inp, graph=True), oracle_ref(inp))
 
 
-def test_without_du():
-    inp = inputs.make_inputs(inputs.custom(B=4, K=6, n_x=10, C=48, seed=3))
+@pytest.mark.parametrize("shape", [dict(B=4, K=6, n_x=10, C=48),
+                                   dict(B=300, K=28, n_x=48, C=128)],  # two accumulators per CTA
+                         ids=lambda s: "B{B}_K{K}_nx{n_x}_C{C}".format(**s))
+def test_without_du(shape):
+    inp = inputs.make_inputs(inputs.custom(seed=3, **shape))
     g = run_gpu(inp, with_du=False)
     assert "du" not in g
     assert_parity(g, oracle_ref(inp), keys=("H", "dW", "db", "dh0"))
