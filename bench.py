@@ -231,22 +231,45 @@ def run_reference(args, rank, world):
     return 0
 
 
-def cpu_baseline(w, seconds: float) -> dict:
+def _oracle_shard(w, r0: int, r1: int, seconds: float):
+    """Run the oracle on batch rows r0..r1 of the workload for `seconds`; (units, seconds)."""
     import oracle
     from recurrent_cfc_cell_gb300 import inputs
 
     inp = inputs.make_inputs(w)
+    sub = {k: (v[:, r0:r1] if k in ("u", "ts", "dH") else v[r0:r1] if k == "h0" else v)
+           for k, v in inp.items()}
     n = 0
     t0 = time.perf_counter()
     while True:
-        oracle.step(inp)
+        oracle.step(sub)
         n += 1
         dt = time.perf_counter() - t0
         if dt >= seconds:
-            break
-    return {"value": n * w.units / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} full oracle steps of the workload (B={w.B}, K={w.K}), fp64 C, "
-                      f"single thread, {dt:.1f} s"}
+            return n * (r1 - r0) * w.K, dt
+
+
+def cpu_baseline(w, seconds: float) -> dict:
+    """The oracle on the host cores: single-threaded on the whole workload, and on all cores
+    with the batch rows (independent sequences) split over spawned processes; the all-core
+    figure is the reported one."""
+    import concurrent.futures
+    import multiprocessing
+
+    units1, dt1 = _oracle_shard(w, 0, w.B, seconds)
+    single = units1 / dt1
+    cores = min(os.cpu_count() or 1, w.B)
+    bounds = [(w.B * i // cores, w.B * (i + 1) // cores) for i in range(cores)]
+    ctx = multiprocessing.get_context("spawn")
+    with concurrent.futures.ProcessPoolExecutor(max_workers=cores, mp_context=ctx) as ex:
+        res = list(ex.map(_oracle_shard, [w] * cores, [b[0] for b in bounds],
+                          [b[1] for b in bounds], [seconds] * cores))
+    total = sum(u for u, _ in res) / max(dt for _, dt in res)
+    return {"value": total, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "single_thread_value": single,
+            "sample": f"the workload (B={w.B}, K={w.K}) split by batch rows over {cores} "
+                      f"processes, each running fp64 C oracle steps on its rows for "
+                      f"{seconds:.0f} s; single thread on all rows: {single:.0f} {UNIT}"}
 
 
 # ---------------------------------------------------------------- our arm
