@@ -518,10 +518,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_dual_kernel(const TcParams p
 
 
 TcPlan tc_plan(int rows, int cols, int red, bool split, int terms = 2, int stages = 2,
-               int mt = 1) {
+               int mt = 1, int max_n_tile = 256) {
   TcPlan pl;
   pl.mt = mt;
-  pl.n_tiles = (cols + 255) / 256;
+  pl.n_tiles = (cols + max_n_tile - 1) / max_n_tile;
   pl.n_tile = (((cols + pl.n_tiles - 1) / pl.n_tiles) + 15) & ~15;
   pl.m_tiles = (rows + kTcM * mt - 1) / (kTcM * mt);
   pl.n_kb = (red + kTcK - 1) / kTcK;
@@ -616,7 +616,9 @@ cudaError_t dw_tc_launch(const TcPlan& pl, const float* d_pre, const float* u, c
 }
 
 TcPlan proj_tc_plan(int B, int K, int C, int n_x) {
-  return tc_plan(B * K, 4 * C, n_x, false, ProjProblem::kTerms, ProjProblem::kStages);
+  // Column tiles of at most 128: a 98 KB stage, so two CTAs share an SM and one's loads and
+  // conversion overlap the other's MMAs and stores.
+  return tc_plan(B * K, 4 * C, n_x, false, ProjProblem::kTerms, ProjProblem::kStages, 1, 128);
 }
 
 cudaError_t proj_tc_launch(const TcPlan& pl, const float* u, const float* W, const float* bias,
