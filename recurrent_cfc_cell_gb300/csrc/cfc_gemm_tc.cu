@@ -207,6 +207,7 @@ __device__ __forceinline__ void convert_quads(int n_quads, int row_base, int k_b
 
 // Output columns n .. n+15 of row m (v[0..15]) into the row-major block p.out of split `split`.
 struct RowMajorOut {
+  static constexpr bool kStagedOut = false;
   static __device__ __forceinline__ void store16(const TcParams& p, int split, int m, int n,
                                                  const float (&v)[16]) {
     float* dst = p.out + (static_cast<size_t>(split) * p.rows + m) * p.cols;
@@ -300,6 +301,21 @@ struct DuProblem : RowMajorOut {
 // 64-entry blocks, and one stage of six tiles fits in shared memory.
 struct ProjProblem {
   static constexpr int kTerms = 3, kStages = 1, kMT = 1;
+  // The epilogue stages the tile in shared memory and writes whole row segments (store4)
+  // when rows can be written as float4 (n_x and C multiples of 4).
+  static constexpr bool kStagedOut = true;
+  static __device__ __forceinline__ bool staged(const TcParams& p) { return p.vec != 0; }
+  // Columns n .. n+3 of row r (n a multiple of 4; C a multiple of 4, so one gate holds all
+  // four) plus the bias, into H or the cache.
+  static __device__ __forceinline__ void store4(const TcParams& p, int r, int n, float4 x) {
+    const int C = p.C;
+    if (n >= 4 * C) return;
+    const int g = n / C, c = n - g * C;
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p.bias + n));
+    float* dst = (g == 0) ? p.xh + static_cast<size_t>(r) * C + c
+                          : p.xcache + (static_cast<size_t>(r) * 3 + (g - 1)) * C + c;
+    *reinterpret_cast<float4*>(dst) = make_float4(x.x + b.x, x.y + b.y, x.z + b.z, x.w + b.w);
+  }
   // Entries k .. k+7 of a row of `width` valid values (zero beyond), as two float4 loads when
   // the row start is 16-byte aligned.
   static __device__ __forceinline__ void load8(const float* row, int k, int width, bool vec,
@@ -445,7 +461,34 @@ __device__ __forceinline__ void tc_gemm_body(const TcParams& p, int tile, int sp
     if (ok) ok = mbar_wait_bounded_cta(accb, 0, p.status);
     tc_fence_after_sync();
     const int quarter = warp & 3;  // TMEM lanes this warp may read
-    for (int j = 0; j < kMT; ++j) {
+    bool done = false;
+    if constexpr (Problem::kStagedOut) {
+      if (Problem::staged(p)) {
+        // Every MMA has completed, so the stage buffer is free: the tile goes through it and
+        // each warp then writes whole row segments (a row's n_tile columns are contiguous in
+        // the destination).
+        float* tile = reinterpret_cast<float*>(base);
+        const int pitch = p.n_tile + 4;  // rows 16 bytes apart in bank order
+        const int r = 32 * quarter + lane;
+        for (int c0 = 16 * (warp >> 2); c0 < p.n_tile; c0 += 32) {
+          float v[16];
+          tmem_ld16(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + c0, v);
+          float4* dst = reinterpret_cast<float4*>(tile + r * pitch + c0);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kConv) : "memory");  // warps 0-7 only
+        for (int rr = warp; rr < kTcM; rr += kConv / 32) {
+          const int m = m0 + rr;
+          if (!ok || m >= p.rows) continue;
+          for (int c = 4 * lane; c < p.n_tile; c += 128)
+            Problem::store4(p, m, n0 + c, *reinterpret_cast<const float4*>(tile + rr * pitch + c));
+        }
+        done = true;
+      }
+    }
+    for (int j = 0; j < kMT && !done; ++j) {
       const int m = m0 + kTcM * j + 32 * quarter + lane;
       for (int c0 = 16 * (warp >> 2); c0 < p.n_tile; c0 += 32) {
         float v[16];
