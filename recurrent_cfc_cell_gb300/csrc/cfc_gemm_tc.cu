@@ -207,7 +207,14 @@ __device__ __forceinline__ void convert_quads(int n_quads, int row_base, int k_b
 
 // Output columns n .. n+15 of row m (v[0..15]) into the row-major block p.out of split `split`.
 struct RowMajorOut {
-  static constexpr bool kStagedOut = false;
+  // Staged epilogue (whole row segments per warp store) when rows hold float4s.
+  static constexpr bool kStagedOut = true;
+  static __device__ __forceinline__ bool staged(const TcParams& p) { return (p.cols % 4) == 0; }
+  static __device__ __forceinline__ void store4(const TcParams& p, int split, int m, int n,
+                                                float4 x) {
+    if (n >= p.cols) return;  // cols is a multiple of 4: each quad is wholly in or out
+    *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(split) * p.rows + m) * p.cols + n) = x;
+  }
   static __device__ __forceinline__ void store16(const TcParams& p, int split, int m, int n,
                                                  const float (&v)[16]) {
     float* dst = p.out + (static_cast<size_t>(split) * p.rows + m) * p.cols;
@@ -307,7 +314,7 @@ struct ProjProblem {
   static __device__ __forceinline__ bool staged(const TcParams& p) { return p.vec != 0; }
   // Columns n .. n+3 of row r (n a multiple of 4; C a multiple of 4, so one gate holds all
   // four) plus the bias, into H or the cache.
-  static __device__ __forceinline__ void store4(const TcParams& p, int r, int n, float4 x) {
+  static __device__ __forceinline__ void store4(const TcParams& p, int, int r, int n, float4 x) {
     const int C = p.C;
     if (n >= 4 * C) return;
     const int g = n / C, c = n - g * C;
@@ -462,28 +469,33 @@ __device__ __forceinline__ void tc_gemm_body(const TcParams& p, int tile, int sp
     tc_fence_after_sync();
     const int quarter = warp & 3;  // TMEM lanes this warp may read
     bool done = false;
-    if constexpr (Problem::kStagedOut) {
+    // (Two-accumulator tiles store directly: staging their 200 KB measured slower.)
+    if constexpr (Problem::kStagedOut && kMT == 1) {
       if (Problem::staged(p)) {
         // Every MMA has completed, so the stage buffer is free: the tile goes through it and
         // each warp then writes whole row segments (a row's n_tile columns are contiguous in
         // the destination).
+        // [a_rows][n_tile + 4] floats: at most 128 x 260 x 4 bytes, inside the stage buffers.
         float* tile = reinterpret_cast<float*>(base);
         const int pitch = p.n_tile + 4;  // rows 16 bytes apart in bank order
-        const int r = 32 * quarter + lane;
-        for (int c0 = 16 * (warp >> 2); c0 < p.n_tile; c0 += 32) {
-          float v[16];
-          tmem_ld16(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + c0, v);
-          float4* dst = reinterpret_cast<float4*>(tile + r * pitch + c0);
+        for (int j = 0; j < kMT; ++j) {
+          const int r = kTcM * j + 32 * quarter + lane;
+          for (int c0 = 16 * (warp >> 2); c0 < p.n_tile; c0 += 32) {
+            float v[16];
+            tmem_ld16(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + j * acc_cols + c0, v);
+            float4* dst = reinterpret_cast<float4*>(tile + r * pitch + c0);
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+            for (int e = 0; e < 4; ++e)
+              dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+          }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kConv) : "memory");  // warps 0-7 only
-        for (int rr = warp; rr < kTcM; rr += kConv / 32) {
+        for (int rr = warp; rr < a_rows; rr += kConv / 32) {
           const int m = m0 + rr;
           if (!ok || m >= p.rows) continue;
           for (int c = 4 * lane; c < p.n_tile; c += 128)
-            Problem::store4(p, m, n0 + c, *reinterpret_cast<const float4*>(tile + rr * pitch + c));
+            Problem::store4(p, split, m, n0 + c,
+                            *reinterpret_cast<const float4*>(tile + rr * pitch + c));
         }
         done = true;
       }
