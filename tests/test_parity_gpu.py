@@ -155,6 +155,32 @@ def test_backward_recurrence_ws_is_cfc_backwards_recurrence(shape):
                   keys=("d_pre", "dh0"))
 
 
+def test_backward_recurrence_ws_with_16_byte_aligned_outputs():
+    """The tensor-core BPTT wants dH, cache and d_pre 32-byte aligned; a d_pre that is only
+    16-byte aligned takes the CUDA-core recurrence, with the same parity."""
+    import torch
+
+    from recurrent_cfc_cell_gb300 import _lib, build
+    from recurrent_cfc_cell_gb300.step import KLoopStep, to_device
+
+    build.build()
+    B, K, C, n_x = 1100, 3, 128, 8
+    inp = inputs.make_inputs(inputs.custom(B=B, K=K, n_x=n_x, C=C, seed=37))
+    d = to_device(inp)
+    a = KLoopStep(B, K, C, n_x).bind(**d)
+    a.forward()
+    ws = torch.empty(_lib.bptt_workspace_bytes(B, K, C, n_x), dtype=torch.uint8, device="cuda")
+    n = K * B * 4 * C
+    buf = torch.full((n + 4,), float("nan"), device="cuda")
+    d_pre = buf[4:].view(K, B, 4, C)  # 16 bytes past a 256-byte boundary
+    assert d_pre.data_ptr() % 32 == 16
+    dh0 = torch.empty((B, C), device="cuda")
+    _lib.cfc_backward_recurrence_ws(d["dH"], d["W"], d["ts"], a.cache, d_pre, dh0, ws)
+    torch.cuda.synchronize()
+    assert_parity({"d_pre": d_pre.cpu().numpy(), "dh0": dh0.cpu().numpy()}, oracle_ref(inp),
+                  keys=("d_pre", "dh0"))
+
+
 def test_graph_replay_parity():
     inp = inputs.make_inputs(inputs.CONFIGS[1])
     assert_parity(run_gpu(inp, graph=True), oracle_ref(inp))
