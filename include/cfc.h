@@ -155,7 +155,7 @@ int cfc_backward_recurrence(const float* dH, const float* W, const float* ts,
 
 /*
  * cfc_bptt_workspace_bytes -- bytes of device workspace cfc_backward_recurrence_ws takes for
- * these sizes: for B >= 1024 and C = 128 or 256 the recurrence runs each step's contraction
+ * these sizes: for C = 256 with B >= 1024, or C = 128 with B >= 1185, the recurrence runs each step's contraction
  * delta = d_pre W_h on the tensor cores and first writes W_h^T there as three bf16 terms
  * (24 C^2 bytes); otherwise 0.  Writes *bytes; returns the argument codes of
  * cfc_workspace_bytes.

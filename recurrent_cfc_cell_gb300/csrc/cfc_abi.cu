@@ -174,12 +174,17 @@ constexpr int kTcProjMinRows = 8192;
 
 // Batch rows from which the forward recurrence runs its per-step gate contraction on the
 // tensor cores (cfc_fwd_tc_kernel, 128 rows per cluster) instead of the CUDA-core kernel
-// (at most 8 rows per cluster, one cluster per row group).
-constexpr int kTcFwdMinRows = 512;
+// (at most 8 rows per cluster, one cluster per row group).  The tensor-core step time hardly
+// grows with B, the CUDA-core one about linearly; measured per step, C = 128: 5.3 us (CUDA
+// cores, B = 511) against 7.6 us (tensor cores, B = 512); C = 256: 19.5 against 12.2 us.
+int tc_fwd_min_rows(int C) { return C >= 256 ? 512 : 768; }
 
 // Batch rows from which the BPTT recurrence runs its per-step contraction on the tensor cores
 // (cfc_bwd_tc_kernel, one CTA per 128 rows); it needs the pre-split W_h^T in the workspace.
-constexpr int kTcBwdMinRows = 1024;
+// Measured per step, C = 128: the CUDA-core kernel takes 13.9 us up to B = 1100 and 27.4 us
+// from B = 1200 (a second wave of its 4-CTA clusters), the tensor-core one 19.7 us; C = 256:
+// 44.6 us (CUDA cores, B = 1023) against 43.0 us (tensor cores, B = 1024).
+int tc_bwd_min_rows(int C) { return C >= 256 ? 1024 : 1185; }
 
 // Shared memory of a BPTT CTA launched as a dependent of the forward: more than half of an
 // SM's 228 KB (so two BPTT CTAs cannot be packed onto one SM for the whole recurrence) and
@@ -210,7 +215,7 @@ BwdLayout bwd_layout(int B, int K, int C, int n_x) {
   L.part_off = align256(L.d_pre_bytes);
   L.part_bytes = part * sizeof(float);
   L.total = L.part_off + L.part_bytes;
-  L.tc_bptt = B >= kTcBwdMinRows && cfc::bwd_tc_supported(C);
+  L.tc_bptt = B >= tc_bwd_min_rows(C) && cfc::bwd_tc_supported(C);
   L.wsplit_off = align256(L.total);
   if (L.tc_bptt) L.total = L.wsplit_off + cfc::bwd_tc_split_bytes(C);
   return L;
@@ -290,7 +295,7 @@ int forward_recurrence(const float* h0, const float* W, const float* ts, int B, 
   p.status = st->status;
   p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
   p.CS = cluster_size_for(C, cfc::kFwdChanPerCta);
-  if (B >= kTcFwdMinRows && cfc::fwd_tc_supported(C)) {
+  if (B >= tc_fwd_min_rows(C) && cfc::fwd_tc_supported(C)) {
     int n = 0;
     rc = max_clusters(*st, 3, 0, p.CS, 0, &n);
     if (rc != CFC_OK) return rc;
@@ -332,7 +337,7 @@ int backward_recurrence(const float* dH, const float* W, const float* ts, const 
   p.CS = cluster_size_for(C, cfc::kBwdChanPerCta);
   p.wsplit = wsplit;
   // The tensor-core BPTT moves dH, the cache and d_pre in whole 32-byte sectors.
-  if (wsplit && B >= kTcBwdMinRows && cfc::bwd_tc_supported(C) && aligned32(dH) &&
+  if (wsplit && B >= tc_bwd_min_rows(C) && cfc::bwd_tc_supported(C) && aligned32(dH) &&
       aligned32(cache) && aligned32(d_pre)) {
     int n = 0;
     rc = max_clusters(*st, 4, C, 1, 0, &n);

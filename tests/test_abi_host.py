@@ -161,7 +161,8 @@ def test_binding_refuses_missing_library(tmp_path):
         _lib.load(str(tmp_path / "libcfc.so"))
 
 
-@pytest.mark.parametrize("B,C,expect", [(32, 128, 0), (1023, 256, 0), (1024, 128, 24 * 128 * 128),
+@pytest.mark.parametrize("B,C,expect", [(32, 128, 0), (1023, 256, 0), (1024, 256, 24 * 256 * 256),
+                                        (1184, 128, 0), (1185, 128, 24 * 128 * 128),
                                         (2048, 256, 24 * 256 * 256), (4096, 200, 0)])
 def test_bptt_workspace_bytes(lib, B, C, expect):
     out = ctypes.c_size_t(123)
@@ -174,7 +175,7 @@ def test_bptt_workspace_bytes(lib, B, C, expect):
 def test_bptt_workspace_checked_before_launch(lib):
     f = ctypes.c_void_p(0x10000)
     need = 24 * 128 * 128
-    args = (f, f, f, f, 1024, 4, 128, 8, f, f)
+    args = (f, f, f, f, 1536, 4, 128, 8, f, f)
     assert lib.cfc_backward_recurrence_ws(*args, None, need, None) == NULL_PTR
     assert lib.cfc_backward_recurrence_ws(*args, ctypes.c_void_p(0x10008), need, None) == MISALIGNED
     assert lib.cfc_backward_recurrence_ws(*args, f, need - 16, None) == WS_TOO_SMALL

@@ -34,9 +34,9 @@ RAGGED = [
     dict(B=200, K=6, n_x=64, C=256),   # 8-row forward and 16-row BPTT clusters of 8 CTAs
     dict(B=130, K=64, n_x=13, C=100),  # tensor-core projection: odd n_x (scalar loads), C not
                                        # a multiple of 16 (element-wise epilogue), ragged tiles
-    dict(B=520, K=6, n_x=16, C=128),   # tensor-core forward, clusters of 4, last cluster 8 rows
+    dict(B=800, K=6, n_x=16, C=128),   # tensor-core forward, clusters of 4, last cluster 32 rows
     dict(B=600, K=5, n_x=24, C=256),   # tensor-core forward, clusters of 8, last cluster 88 rows
-    dict(B=1100, K=4, n_x=8, C=128),   # tensor-core BPTT, 9 CTAs, the last with 76 rows
+    dict(B=1600, K=4, n_x=8, C=128),   # tensor-core BPTT, 13 CTAs, the last with 64 rows
     dict(B=1030, K=3, n_x=16, C=256),  # tensor-core BPTT at the widest state, last CTA 6 rows
 ]
 
@@ -126,10 +126,12 @@ def test_forward_backward_is_forward_then_backward(shape):
     assert_parity(out, oracle_ref(inp))
 
 
-@pytest.mark.parametrize("shape", [dict(B=1100, K=4, n_x=8, C=128), dict(B=7, K=11, n_x=13, C=100)],
+@pytest.mark.parametrize("shape", [dict(B=1600, K=4, n_x=8, C=128), dict(B=1030, K=3, n_x=16, C=256),
+                                   dict(B=7, K=11, n_x=13, C=100)],
                          ids=lambda s: "B{B}_K{K}_nx{n_x}_C{C}".format(**s))
 def test_backward_recurrence_ws_is_cfc_backwards_recurrence(shape):
-    """cfc_backward_recurrence_ws (tensor cores at B >= 1024) writes bitwise the d_pre and dh0
+    """cfc_backward_recurrence_ws (tensor cores from B = 1185 at C = 128, 1024 at C = 256)
+    writes bitwise the d_pre and dh0
     that cfc_backward writes, and they match the oracle."""
     import torch
 
@@ -143,7 +145,7 @@ def test_backward_recurrence_ws_is_cfc_backwards_recurrence(shape):
     a = KLoopStep(B, K, C, n_x).bind(**d)
     a.run()
     n = _lib.bptt_workspace_bytes(B, K, C, n_x)
-    assert (n > 0) == (B >= 1024)
+    assert (n > 0) == (B >= (1024 if C == 256 else 1185))
     ws = torch.empty(n, dtype=torch.uint8, device="cuda") if n else None
     d_pre = torch.full((K, B, 4, C), float("nan"), device="cuda")
     dh0 = torch.full((B, C), float("nan"), device="cuda")
@@ -164,7 +166,7 @@ def test_backward_recurrence_ws_with_16_byte_aligned_outputs():
     from recurrent_cfc_cell_gb300.step import KLoopStep, to_device
 
     build.build()
-    B, K, C, n_x = 1100, 3, 128, 8
+    B, K, C, n_x = 1600, 3, 128, 8
     inp = inputs.make_inputs(inputs.custom(B=B, K=K, n_x=n_x, C=C, seed=37))
     d = to_device(inp)
     a = KLoopStep(B, K, C, n_x).bind(**d)
