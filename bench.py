@@ -376,10 +376,10 @@ def main():
                          "gbs": byt / (t * 1e-3) / 1e9}
     # The dominant kernel: the larger of the two recurrences (each stage is one launch).
     dominant = max(("fwd_rec", "bwd_rec"), key=lambda k: stage_ms[k])
-    # Which kernel that stage ran: the tensor-core recurrences serve batches of at least 512
+    # Which kernel that stage ran: the tensor-core recurrences serve batches of at least 384
     # (forward) or 1024 (BPTT) rows at C = 256, 768 or 1185 at C = 128; the CUDA-core ones
     # the rest.
-    tc_fwd = w.C in (128, 256) and w.B >= (512 if w.C == 256 else 768)
+    tc_fwd = w.C in (128, 256) and w.B >= (384 if w.C == 256 else 768)
     tc = tc_fwd if dominant == "fwd_rec" else n_bptt_ws > 0
     kname = {("fwd_rec", False): "cfc_fwd_kernel", ("bwd_rec", False): "cfc_bwd_kernel",
              ("fwd_rec", True): "cfc_fwd_tc_kernel",

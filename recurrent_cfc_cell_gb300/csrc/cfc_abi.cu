@@ -175,9 +175,10 @@ constexpr int kTcProjMinRows = 8192;
 // Batch rows from which the forward recurrence runs its per-step gate contraction on the
 // tensor cores (cfc_fwd_tc_kernel, 128 rows per cluster) instead of the CUDA-core kernel
 // (at most 8 rows per cluster, one cluster per row group).  The tensor-core step time hardly
-// grows with B, the CUDA-core one about linearly; measured per step, C = 128: 5.3 us (CUDA
-// cores, B = 511) against 7.6 us (tensor cores, B = 512); C = 256: 19.5 against 12.2 us.
-int tc_fwd_min_rows(int C) { return C >= 256 ? 512 : 768; }
+// grows with B, the CUDA-core one in steps of cluster waves; measured per step, C = 128: 5.3
+// us (CUDA cores, B = 511) and 7.9 us (B = 767) against 7.6-7.7 us (tensor cores); C = 256:
+// 11.8 us (CUDA cores, B <= 300) and 15.7 us (B = 400) against 12.2 us (tensor cores).
+int tc_fwd_min_rows(int C) { return C >= 256 ? 384 : 768; }
 
 // Batch rows from which the BPTT recurrence runs its per-step contraction on the tensor cores
 // (cfc_bwd_tc_kernel, one CTA per 128 rows); it needs the pre-split W_h^T in the workspace.
