@@ -245,6 +245,18 @@ const char* cfc_error_string(int code);
  */
 int cfc_device_status(int* status);
 
+/*
+ * cfc_wait_self_test -- checks, on the device, that an abandoned wait is reported rather than
+ * hung: enqueues on `stream` one single-thread kernel that waits, with the bounded wait every
+ * kernel of the library uses, on an mbarrier that nothing completes.  After the wait limit
+ * (2 s) the kernel records a timeout in the device status word and returns; cfc_device_status
+ * then reports 1 (and clears it).  No fault is raised and the context stays usable.  Do not
+ * call it while other work of this library runs on the device: their waits would see the
+ * status word and stop too.  Returns CFC_OK, CFC_ERR_UNSUPPORTED_DEVICE, CFC_ERR_CUDA or
+ * CFC_ERR_LAUNCH_FAILED.
+ */
+int cfc_wait_self_test(cfc_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

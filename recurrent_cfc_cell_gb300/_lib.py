@@ -23,7 +23,7 @@ EXPORTED = ("cfc_workspace_bytes", "cfc_forward", "cfc_backward", "cfc_backward_
             "cfc_weight_grad", "reduce_axis0", "cfc_error_string", "cfc_device_status",
             "cfc_backward_noalloc", "cfc_input_projection", "cfc_forward_recurrence",
             "cfc_step_launches", "cfc_forward_backward", "cfc_bptt_workspace_bytes",
-            "cfc_backward_recurrence_ws")
+            "cfc_backward_recurrence_ws", "cfc_wait_self_test")
 CFC_ERR_SCRATCH_LIMIT = -10
 NOALLOC_SCRATCH_BYTES = 32 << 20  # size of cfc_backward_noalloc's built-in device scratch
 
@@ -77,6 +77,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.cfc_error_string.restype = ctypes.c_char_p
     lib.cfc_device_status.argtypes = [ctypes.POINTER(i)]
     lib.cfc_device_status.restype = i
+    lib.cfc_wait_self_test.argtypes = [vp]
+    lib.cfc_wait_self_test.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -262,6 +264,12 @@ def reduce_axis0(per_batch, out, stream=None) -> None:
     rc = load().reduce_axis0(_ptr(per_batch, "per_batch"), n_batch, n_tail,
                              _ptr(out, "out", (n_tail,)), _stream(stream))
     _check("reduce_axis0", rc)
+
+
+def cfc_wait_self_test(stream=None) -> None:
+    """Enqueue the self-test kernel whose bounded wait runs out (read the result with
+    device_status(): 1 after about 2 s)."""
+    _check("cfc_wait_self_test", load().cfc_wait_self_test(_stream(stream)))
 
 
 def device_status() -> int:

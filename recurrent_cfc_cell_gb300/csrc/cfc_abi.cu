@@ -10,6 +10,11 @@
 #include "cfc.h"
 #include "cfc_kernels.h"
 
+namespace cfc {
+// Launcher of the failure-detection self-test kernel (cfc_selftest.cu).
+cudaError_t wait_self_test_launch(int* status, cudaStream_t s);
+}  // namespace cfc
+
 namespace {
 
 // Kernels record abandoned waits here; cfc_device_status reads and clears it.
@@ -580,6 +585,15 @@ int reduce_axis0(const float* per_batch, int n_batch, int n_tail, float* out,
   if (rc != CFC_OK) return rc;
   return cuda_rc(cfc::reduce_axis0_launch(per_batch, n_batch, n_tail, out,
                                           static_cast<cudaStream_t>(stream), false),
+                 CFC_ERR_LAUNCH_FAILED);
+}
+
+int cfc_wait_self_test(cfc_stream_t stream) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  const int rc = device_state(&st);
+  if (rc != CFC_OK) return rc;
+  return cuda_rc(cfc::wait_self_test_launch(st->status, static_cast<cudaStream_t>(stream)),
                  CFC_ERR_LAUNCH_FAILED);
 }
 
