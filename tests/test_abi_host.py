@@ -179,3 +179,17 @@ def test_bptt_workspace_checked_before_launch(lib):
     assert lib.cfc_backward_recurrence_ws(*args, None, need, None) == NULL_PTR
     assert lib.cfc_backward_recurrence_ws(*args, ctypes.c_void_p(0x10008), need, None) == MISALIGNED
     assert lib.cfc_backward_recurrence_ws(*args, f, need - 16, None) == WS_TOO_SMALL
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    """The boundary is a C ABI: include/cfc.h compiles as C99 with no C++ or CUDA headers."""
+    import shutil
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "cfc.h"\nint main(void) { return cfc_error_string(0) == 0; }\n')
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), "-c", str(src), "-o",
+                    str(tmp_path / "use_header.o")], check=True, capture_output=True)
