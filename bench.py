@@ -49,6 +49,10 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-largest", action="store_true",
+                    help="skip the record of the largest (2048 x 128 x 256) workload")
+    ap.add_argument("--dw-modes", default="0,1",
+                    help="tensor-core weight-gradient modes timed on the largest workload")
     return ap.parse_args()
 
 
@@ -221,7 +225,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": dict(w.describe(), sample_rows=rows, l2="n/a (CPU)"),
+        "config": dict(w.describe()),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{rows} of {w.B} batch rows x K={w.K} per step, fp64 C, "
                                    "single thread"},
@@ -270,6 +274,222 @@ def cpu_baseline(w, seconds: float) -> dict:
             "sample": f"the workload (B={w.B}, K={w.K}) split by batch rows over {cores} "
                       f"processes, each running fp64 C oracle steps on its rows for "
                       f"{seconds:.0f} s; single thread on all rows: {single:.0f} {UNIT}"}
+
+
+# ---------------------------------------------------------------- parity (oracle leg)
+def _bf16_bits_to_f32(a):
+    import numpy as np
+
+    return (np.asarray(a).astype(np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def decode_dpre(raw, C: int, dw_mode: int):
+    """The workspace head after cfc_backward -> fp32-valued d_pre [K, B, 4, C] (the layout the
+    public header documents for each mode)."""
+    import numpy as np
+
+    raw = np.asarray(raw)
+    if dw_mode in (2, 3):
+        return raw
+    K, B = raw.shape[:2]
+    d = _bf16_bits_to_f32(raw[:, :, 0, : 4 * C]).astype(np.float64)
+    if dw_mode == 0:
+        d = d + _bf16_bits_to_f32(raw[:, :, 1, : 4 * C])
+    return d.reshape(K, B, 4, C)
+
+
+def oracle_parity(inp: dict, gpu: dict, rows=None) -> dict:
+    """Part of the CPU-baseline leg: one more run of the oracle (on all rows, or on the listed
+    rows when the workload is too large for a bounded sample), compared with the GPU's outputs
+    of the timed step: max|x - y| / max|y| per tensor (dW and db only on all rows)."""
+    import numpy as np
+
+    import oracle
+
+    if rows is not None:
+        rows = np.asarray(rows)
+        inp = {k: (np.ascontiguousarray(v[:, rows]) if k in ("u", "ts", "dH")
+                   else np.ascontiguousarray(v[rows]) if k == "h0" else v)
+               for k, v in inp.items()}
+        gpu = {k: (v[:, rows] if k in ("H", "cache", "d_pre", "du") else v[rows] if k == "dh0"
+                   else None) for k, v in gpu.items()}
+    ref = oracle.step(inp)
+    ref["cache"] = np.stack([ref["ff1"], ref["ff2"], ref["gate"]], axis=2)
+    out = {}
+    for k in ("H", "cache", "d_pre", "du", "dh0", "dW", "db"):
+        if gpu.get(k) is None or k not in ref:
+            continue
+        out[k] = oracle.rel_err(gpu[k], ref[k])
+    return {"max_rel_err": out, "rows": "all" if rows is None else [int(r) for r in rows],
+            "metric": "max|x-y| / max|y| per tensor against the fp64 oracle"}
+
+
+# ---------------------------------------------------------------- measured peaks
+def measure_peaks(torch, _lib, dev) -> dict:
+    """fp32 FMA rate and L2 read bandwidth from the library's probes, dense tf32 from a cuBLAS
+    matmul (torch, TF32 allowed), the SM count; best of several CUDA-event-timed runs."""
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    stream = torch.cuda.current_stream()
+
+    def best(fn, reps=5):
+        ts = []
+        for k in range(reps + 2):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            work = fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if k >= 2:
+                ts.append((a.elapsed_time(b), work))
+        return min(ts)
+
+    out = torch.empty(sms * 8 * 256, dtype=torch.float32, device=dev)
+    ms, flop = best(lambda: _lib.probe_fma(out, sms * 8, 20000))
+    fma = flop / (ms * 1e-3) / 1e12
+    buf = torch.ones(8 << 20, dtype=torch.float32, device=dev)  # 32 MB, inside the 129 MB L2
+    ms, nbytes = best(lambda: _lib.probe_l2_read(buf, 40, out, sms * 8))
+    l2 = nbytes / (ms * 1e-3) / 1e9
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        a = torch.randn(8192, 8192, device=dev)
+        b = torch.randn(8192, 8192, device=dev)
+        ms, fl = best(lambda: (torch.matmul(a, b), 2.0 * 8192 ** 3)[1])
+        tf32 = fl / (ms * 1e-3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    del a, b, buf, out
+    return {"sms": sms, "fp32_fma_tflops": fma, "l2_read_gbs": l2, "tf32_tflops": tf32,
+            "how": "fp32: cfc_probe_fma (8 packed-FMA chains per thread, 8 CTAs of 256 per SM); "
+                   "L2: cfc_probe_l2_read over a 32 MB buffer, 40 passes; tf32: torch.matmul "
+                   "8192^3 with TF32 allowed (cuBLAS); best of 5, CUDA events"}
+
+
+# ---------------------------------------------------------------- stage timing
+def stage_times(torch, _lib, st, flush, stream, n: int) -> dict:
+    """Device time of each stage of one step, CUDA events between the stage calls, L2 flushed
+    before each group: the projection, the forward recurrence, the BPTT recurrence (into an
+    fp32 d_pre at the workspace head, the same kernels as in the step), the standalone gradient
+    stage (cfc_weight_grad from that fp32 d_pre), and the whole cfc_backward.  "grad" is the
+    gradient chain as cfc_backward runs it (BPTT writing the contraction's operand rows
+    directly): cfc_backward minus the BPTT stage."""
+    i = st.inputs
+    n_bptt = _lib.bptt_workspace_bytes(st.B, st.K, st.C, st.n_x)
+    bptt_ws = torch.empty(n_bptt, dtype=torch.uint8, device=st.device) if n_bptt else None
+    d32 = st.d_pre_fp32_view
+    stages = [
+        ("proj", lambda: _lib.cfc_input_projection(i["u"], i["W"], i["b"], st.H, st.cache)),
+        ("fwd_rec", lambda: _lib.cfc_forward_recurrence(i["h0"], i["W"], i["ts"], st.H,
+                                                       st.cache)),
+        ("bwd_rec", lambda: _lib.cfc_backward_recurrence_ws(i["dH"], i["W"], i["ts"], st.cache,
+                                                           d32, st.dh0, bptt_ws)),
+        ("grad_standalone", lambda: _lib.cfc_weight_grad(d32, i["u"], i["h0"], i["W"], st.H,
+                                                         st.dW, st.db, st.du, st.ws,
+                                                         dw_mode=st.dw_mode)),
+        ("bwd", lambda: st.backward()),
+    ]
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+             for _ in range(n)]
+    for ev in marks:
+        flush.zero_()
+        ev[0].record(stream)
+        for j, (_, fn) in enumerate(stages):
+            fn()
+            ev[j + 1].record(stream)
+    torch.cuda.synchronize()
+    out = {name: sum(ev[j].elapsed_time(ev[j + 1]) for ev in marks) / n
+           for j, (name, _) in enumerate(stages)}
+    out["grad"] = max(out["bwd"] - out["bwd_rec"], 1e-6)
+    return out
+
+
+def kernel_table(w, stage_ms: dict, pk: dict, mp: dict | None) -> dict:
+    wpu = work_per_unit(w)
+    fp32_peak = mp["fp32_fma_tflops"] if mp else None
+    tab = {}
+    for name in ("proj", "fwd_rec", "bwd_rec", "grad"):
+        t = stage_ms[name]
+        flop = wpu[name]["flop"] * w.units
+        byt = wpu[name]["bytes"] * w.units
+        e = {"ms": t, "tflops": flop / (t * 1e-3) / 1e12, "gbs": byt / (t * 1e-3) / 1e9}
+        e["hbm_frac"] = e["gbs"] / pk["hbm_gbs"]
+        e["bf16_frac"] = e["tflops"] / pk["bf16_tflops"]
+        if fp32_peak:
+            e["fp32_frac"] = e["tflops"] / fp32_peak
+        tab[name] = e
+    return tab
+
+
+def timed_replays(torch, st, flush, stream, steps: int) -> float:
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for k in range(steps):
+        flush.zero_()
+        starts[k].record(stream)
+        st.replay()
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps
+
+
+def outputs_np(st) -> dict:
+    out = {k: v.cpu().numpy() for k, v in st.outputs().items()}
+    out["d_pre"] = decode_dpre(out["d_pre"], st.C, st.dw_mode)
+    return out
+
+
+def largest_record(torch, _lib, inputs, KLoopStep, to_device, dev, flush, stream, pk, mp,
+                   modes, local: int, with_parity: bool) -> dict:
+    """The largest workload (B=2048, K=128, n_x=64, C=256), measured in this run: step time
+    (graph replays, L2 flushed), stage times, each stage's fractions, clocks, and the weight-
+    gradient stage in each tensor-core mode with its tensor-pipe fraction."""
+    w = inputs.CONFIGS[4]
+    inp = inputs.make_inputs(w)
+    dinp = to_device(inp, dev)
+    st = KLoopStep(w.B, w.K, w.C, w.n_x, device=dev).bind(**dinp)
+    st.capture()
+    for _ in range(3):
+        flush.zero_()
+        st.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ms = timed_replays(torch, st, flush, stream, 10)
+    clock_info = clocks.stop()
+    parity = None
+    if with_parity:
+        gpu = outputs_np(st)
+        parity = oracle_parity(inp, gpu, rows=[0, 777, 1500, w.B - 1])
+        del gpu
+    stg = stage_times(torch, _lib, st, flush, stream, 5)
+    kern = kernel_table(w, stg, pk, mp)
+    # The contraction stage per mode: flops of dW (with db) and du, against the peak of the
+    # operand type; accurate mode issues three products per algorithmic one.
+    wpu = work_per_unit(w)
+    flop = wpu["grad"]["flop"] * w.units
+    contraction = {}
+    names = {0: "accurate", 1: "bf16", 2: "tf32"}
+    del st
+    torch.cuda.empty_cache()
+    for m in modes:
+        sm = KLoopStep(w.B, w.K, w.C, w.n_x, dw_mode=m, device=dev).bind(**dinp)
+        sm.forward()
+        t = stage_times(torch, _lib, sm, flush, stream, 5)
+        peak = mp["tf32_tflops"] if (m == 2 and mp) else pk["bf16_tflops"]
+        ach = flop / (t["grad"] * 1e-3) / 1e12
+        issued = 3 if m == 0 else 1
+        contraction[names[m]] = {
+            "grad_ms": t["grad"], "grad_standalone_ms": t["grad_standalone"],
+            "achieved_tflops": ach, "peak_tflops": peak, "frac": ach / peak,
+            "issued_frac": issued * ach / peak,
+            "peak_note": ("measured tf32 (cuBLAS)" if m == 2 else "measured dense bf16 burst")}
+        del sm
+        torch.cuda.empty_cache()
+    return {"workload": w.name, "ms_per_step": ms, "value": w.units / (ms * 1e-3), "unit": UNIT,
+            "steps": 10, "warmup": 3, "stages": stg, "kernels": kern,
+            "contraction": contraction, "clocks": clock_info, "parity_sampled": parity}
 
 
 # ---------------------------------------------------------------- our arm
@@ -335,45 +555,11 @@ def main():
     value = units_per_step / (ms * 1e-3)
     launches_per_step = _lib.step_launches(w.B, w.K, w.C, w.n_x)
 
-    # ---- per-stage device times: events between the four stage calls, L2 flushed first
-    n_stage = min(args.steps, 200)
-    i = st.inputs
-    # The BPTT stage with the same workspace-backed kernel choice as the step (tensor cores
-    # for large batches).
-    n_bptt_ws = _lib.bptt_workspace_bytes(w.B, w.K, w.C, w.n_x)
-    bptt_ws = torch.empty(n_bptt_ws, dtype=torch.uint8, device=dev) if n_bptt_ws else None
-    stages = [
-        ("proj", lambda: _lib.cfc_input_projection(i["u"], i["W"], i["b"], st.H, st.cache)),
-        ("fwd_rec", lambda: _lib.cfc_forward_recurrence(i["h0"], i["W"], i["ts"], st.H,
-                                                       st.cache)),
-        ("bwd_rec", lambda: _lib.cfc_backward_recurrence_ws(i["dH"], i["W"], i["ts"],
-                                                           st.cache, st.d_pre, st.dh0,
-                                                           bptt_ws)),
-        ("grad", lambda: _lib.cfc_weight_grad(st.d_pre, i["u"], i["h0"], i["W"], st.H, st.dW,
-                                             st.db, st.du, st.ws)),
-    ]
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
-             for _ in range(n_stage)]
-    for ev in marks:
-        flush.zero_()
-        ev[0].record(stream)
-        for j, (_, fn) in enumerate(stages):
-            fn()
-            ev[j + 1].record(stream)
-    torch.cuda.synchronize()
-    stage_ms = {name: sum(ev[j].elapsed_time(ev[j + 1]) for ev in marks) / n_stage
-                for j, (name, _) in enumerate(stages)}
-
     pk = peaks()
-    props = torch.cuda.get_device_properties(dev)
-    fp32_peak_tflops = props.multi_processor_count * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
-    wpu = work_per_unit(w)
-    kernels = {}
-    for name, t in stage_ms.items():
-        flop = wpu[name]["flop"] * w.units
-        byt = wpu[name]["bytes"] * w.units
-        kernels[name] = {"ms": t, "tflops": flop / (t * 1e-3) / 1e12,
-                         "gbs": byt / (t * 1e-3) / 1e9}
+    mp = measure_peaks(torch, _lib, dev)
+    stage_ms = stage_times(torch, _lib, st, flush, stream, min(args.steps, 200))
+    kernels = kernel_table(w, stage_ms, pk, mp)
+    n_bptt_ws = _lib.bptt_workspace_bytes(w.B, w.K, w.C, w.n_x)
     # The dominant kernel: the larger of the two recurrences (each stage is one launch).
     dominant = max(("fwd_rec", "bwd_rec"), key=lambda k: stage_ms[k])
     # Which kernel that stage ran: the tensor-core recurrences serve batches of at least 384
@@ -396,16 +582,16 @@ def main():
                     "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
                     "traffic": profiled_traffic(kname, ksrc, workload_tag(w)),
                     "kernel": kname,
-                    "peak_note": f"dense bf16, {pk['source']}; {n_mma} MMAs per product, "
+                    "peak_note": f"dense bf16 burst, {pk['source']}; {n_mma} MMAs per product, "
                                  f"issued frac {n_mma * achieved / pk['bf16_tflops']:.3f}",
                     "hbm_frac": kernels[dominant]["gbs"] / pk["hbm_gbs"]}
     else:
-        roofline = {"bound": "alu", "achieved": achieved, "peak": fp32_peak_tflops,
-                    "unit": "TFLOP/s", "frac": achieved / fp32_peak_tflops,
+        peak = mp["fp32_fma_tflops"]
+        roofline = {"bound": "alu", "achieved": achieved, "peak": peak,
+                    "unit": "TFLOP/s", "frac": achieved / peak,
                     "traffic": profiled_traffic(kname, ksrc, workload_tag(w)),
                     "kernel": kname,
-                    "peak_note": f"fp32 FMA: {props.multi_processor_count} SMs x 128 lanes x 2 x "
-                                 f"{pk['sm_max_mhz']:.0f} MHz",
+                    "peak_note": "fp32 FMA rate measured in this run by cfc_probe_fma",
                     "hbm_frac": kernels[dominant]["gbs"] / pk["hbm_gbs"]}
 
     # ---- end to end through the public API with host buffers: every step copies its inputs
@@ -436,11 +622,23 @@ def main():
     e2e = {"value": units_per_step / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
     status = _lib.device_status()
+    gpu_out = outputs_np(st) if rank == 0 else None
+    del ste
+    largest = None
+    if not args.no_largest and w.name != inputs.CONFIGS[4].name:
+        modes = [int(m) for m in args.dw_modes.split(",") if m.strip()]
+        largest = largest_record(torch, _lib, inputs, KLoopStep, to_device, dev, flush, stream,
+                                 pk, mp, modes, local, rank == 0 and world == 1)
+        status = status or _lib.device_status()
 
     if rank == 0:
         cpu = None
+        parity = None
         if not args.no_cpu_baseline and world == 1:
             cpu = cpu_baseline(w, args.cpu_seconds)
+            # the oracle once more on the whole workload when that is a bounded sample
+            parity = oracle_parity(inp, gpu_out) if w.units <= 65536 else oracle_parity(
+                inp, gpu_out, rows=[0, w.B // 2, w.B - 1])
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -451,7 +649,9 @@ def main():
                            graph="one CUDA graph per step", dw_mode="accurate"),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "clocks": clock_info,
-            "kernels": kernels, "device_status": status, "peaks_source": pk["source"],
+            "kernels": kernels, "stages_ms": stage_ms, "parity": parity,
+            "measured_peaks": mp, "largest_config": largest,
+            "device_status": status, "peaks_source": pk["source"],
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -53,9 +53,23 @@ extern "C" {
 #define CFC_ERR_CUDA (-9)               /* another CUDA runtime call failed                  */
 #define CFC_ERR_SCRATCH_LIMIT (-10)     /* problem needs more than the built-in scratch holds */
 
-/* Weight-gradient contraction modes for cfc_backward (argument dw_mode). */
-#define CFC_DW_ACCURATE 0  /* fp32-accurate result (relative error ~1e-6 of max|dW|)          */
-#define CFC_DW_SIMT_FP32 2 /* CUDA-core fp32 FMA contraction (the reference path)             */
+/*
+ * Weight-gradient contraction modes for cfc_backward (argument dw_mode): how dW, db and du are
+ * computed from d_pre.  The recurrences (H, d_pre, dh0) are the same in every mode.
+ *   CFC_DW_ACCURATE   tensor cores, each fp32 operand as two bf16 terms (hi + lo, 16
+ *                     significand bits) and three products per step; measured error against
+ *                     the fp64 oracle ~5e-6 of max|dW| (up to 5e-5 on the 2048 x 128 x 256
+ *                     workload, whose gradient cancels heavily).
+ *   CFC_DW_BF16       tensor cores, one bf16 product per step: about 2^-9 relative error per
+ *                     product, ~1e-3 of max|dW|.  For throughput, not for the 1e-4 tolerance.
+ *   CFC_DW_TF32       tensor cores, one tf32 product per step (10 explicit mantissa bits).
+ *                     For throughput, not for the 1e-4 tolerance.
+ *   CFC_DW_SIMT_FP32  CUDA-core fp32 FMA contraction (the reference path).
+ */
+#define CFC_DW_ACCURATE 0
+#define CFC_DW_BF16 1
+#define CFC_DW_TF32 2
+#define CFC_DW_SIMT_FP32 3
 
 typedef void* cfc_stream_t; /* a cudaStream_t */
 
@@ -63,8 +77,14 @@ typedef void* cfc_stream_t; /* a cudaStream_t */
  * cfc_workspace_bytes -- bytes of device workspace cfc_backward needs for these sizes and
  * dw_mode.  Writes *bwd_ws_bytes; the forward cache is always K*B*3*C floats and needs no
  * query.  Returns CFC_OK, CFC_ERR_INVALID_DIM, CFC_ERR_NULL_PTR or CFC_ERR_INVALID_ARG.
- * The workspace layout is: d_pre [K][B][4][C] fp32 at offset 0 (the pre-activation gradients
- * dL/dP, readable after cfc_backward completes), then internal split-contraction partials.
+ * The workspace starts with the pre-activation gradients dL/dP of every step and row, readable
+ * after cfc_backward completes, in the form the mode's contraction reads:
+ *   CFC_DW_TF32, CFC_DW_SIMT_FP32: fp32 d_pre [K][B][4][C];
+ *   CFC_DW_ACCURATE, CFC_DW_BF16:  K*B rows of 4*MP bytes, MP = 4C rounded up to a multiple of
+ *     8; row (t, b) holds MP bf16 values hi[g*C + c] = bf16(d_pre) and then MP bf16 values
+ *     lo[g*C + c] = bf16(d_pre - hi) (CFC_DW_BF16 leaves lo unwritten).  hi + lo is d_pre to
+ *     16 significand bits.
+ * The rest is internal (contraction operands and split partial sums).
  */
 int cfc_workspace_bytes(int B, int K, int C, int n_x, int dw_mode, size_t* bwd_ws_bytes);
 
@@ -121,8 +141,8 @@ int cfc_step_launches(int B, int K, int C, int n_x, int dw_mode, int with_du, in
  *   du    [K][B][n_x]   OUTPUT: dL/du (may be NULL to skip it)
  *   dh0   [B][C]        OUTPUT: dL/dh0
  *   ws, ws_bytes        device workspace of at least cfc_workspace_bytes() bytes, 16-byte
- *                       aligned; its first K*B*4*C floats receive d_pre
- *   dw_mode             CFC_DW_ACCURATE or CFC_DW_SIMT_FP32
+ *                       aligned; its head receives d_pre (see cfc_workspace_bytes)
+ *   dw_mode             one of the CFC_DW_* modes
  */
 int cfc_backward(const float* dH, const float* u, const float* h0, const float* W,
                  const float* ts, const float* H, const float* cache, int B, int K, int C,
@@ -182,10 +202,13 @@ int cfc_backward_recurrence_ws(const float* dH, const float* W, const float* ts,
  * through reduce_axis0, and du = W_u^T d_pre (skipped when du is NULL).  The weight gradient
  * as a dense contraction over the batch replaces the per-sample atomicAdd accumulation, as
  * the DQN plan on page "H100 Epoch Optimization Phase 2" (Task 2) does for its layers.
- *   d_pre [K][B][4][C]  input (e.g. from cfc_backward_recurrence)
+ *   d_pre [K][B][4][C]  fp32 input (e.g. from cfc_backward_recurrence)
  *   u, h0, W, H         the forward's inputs and output
  *   dW, db, du          OUTPUTS as for cfc_backward
- *   ws, ws_bytes        workspace as for cfc_backward (d_pre may live at its head)
+ *   ws, ws_bytes        workspace as for cfc_backward.  d_pre may lie outside it, or, when C
+ *                       is even, start exactly at its head: for CFC_DW_ACCURATE / CFC_DW_BF16
+ *                       the stage first rewrites d_pre into the head's bf16 form, in place
+ *                       in that case.  Any other overlap returns CFC_ERR_INVALID_ARG.
  */
 int cfc_weight_grad(const float* d_pre, const float* u, const float* h0, const float* W,
                     const float* H, int B, int K, int C, int n_x, float* dW, float* db,
@@ -221,7 +244,10 @@ int reduce_axis0(const float* per_batch, int n_batch, int n_tail, float* out,
  *     rejected with CFC_ERR_SCRATCH_LIMIT before any work is enqueued.  (The 32 x 64 x 128 and
  *     32 x 64 x 256 workloads fit; 256 x 64 x 128 does not.)
  *   - Set-up: the first call on each device looks up the array's device address on the current
- *     device; make that first call before any stream capture begins.
+ *     device; make that first call before any stream capture begins.  The address is kept for
+ *     the life of the process, so do not call cudaDeviceReset between calls (the library's
+ *     other per-device set-up, done by the first call of any entry point, is kept the same
+ *     way).
  *   - Sharing: all calls share the one array.  Nothing in it needs to start at zero (every
  *     entry a call reads, the same call wrote first), but calls whose work overlaps on the GPU
  *     -- concurrent streams, or several host threads -- race on it.  Serialise them (one
@@ -234,14 +260,38 @@ int cfc_backward_noalloc(const float* dH, const float* u, const float* h0, const
                          int n_x, float* dW, float* db, float* du, float* dh0, int dw_mode,
                          cfc_stream_t stream);
 
+/*
+ * Measurement aids.  (The pages have no counterpart: they set the roofline denominators of the
+ * CUDA-core kernels on the device at hand.)  Each enqueues one throughput kernel on `stream`
+ * and writes, on the host, the work it does; the caller times the call with CUDA events.
+ *
+ * cfc_probe_fma -- `blocks` CTAs of 256 threads, each running 8 independent chains of `iters`
+ * packed fp32 FMAs; `out` (device, blocks * 256 floats) receives one sum per thread; *flop the
+ * floating-point operations performed (4 per packed FMA).
+ *
+ * cfc_probe_l2_read -- `blocks` CTAs of 256 threads read the n_floats floats at `buf` (device,
+ * 16-byte aligned) `passes` times with 16-byte loads cached in L2 only; `out` (device, blocks *
+ * 256 floats) receives one sum per thread; *bytes the bytes read.  With `buf` smaller than the
+ * L2 cache, this measures L2 read bandwidth.
+ *
+ * Both return CFC_OK, CFC_ERR_NULL_PTR, CFC_ERR_INVALID_DIM, CFC_ERR_MISALIGNED or
+ * CFC_ERR_LAUNCH_FAILED.
+ */
+int cfc_probe_fma(float* out, int blocks, int iters, double* flop, cfc_stream_t stream);
+int cfc_probe_l2_read(const float* buf, size_t n_floats, int passes, float* out, int blocks,
+                      double* bytes, cfc_stream_t stream);
+
 /* cfc_error_string -- static English text for a status code (never NULL). */
 const char* cfc_error_string(int code);
 
 /*
  * cfc_device_status -- synchronises the current device, then reads and clears the library's
  * device status word (set by a kernel that abandoned a bounded wait).  *status receives 0 when
- * no kernel reported a problem.  Returns CFC_OK, CFC_ERR_NULL_PTR or CFC_ERR_CUDA.  This is
- * the only entry point that synchronises.
+ * no kernel reported a problem since the last read.  A nonzero value means that some call
+ * enqueued since then left its outputs incomplete: treat the outputs of every such call as
+ * invalid.  Kernels only write the word, never read it, so a value left unread does not
+ * affect later calls.  Returns CFC_OK, CFC_ERR_NULL_PTR or CFC_ERR_CUDA.  This is the only
+ * entry point that synchronises.
  */
 int cfc_device_status(int* status);
 
@@ -250,10 +300,9 @@ int cfc_device_status(int* status);
  * hung: enqueues on `stream` one single-thread kernel that waits, with the bounded wait every
  * kernel of the library uses, on an mbarrier that nothing completes.  After the wait limit
  * (2 s) the kernel records a timeout in the device status word and returns; cfc_device_status
- * then reports 1 (and clears it).  No fault is raised and the context stays usable.  Do not
- * call it while other work of this library runs on the device: their waits would see the
- * status word and stop too.  Returns CFC_OK, CFC_ERR_UNSUPPORTED_DEVICE, CFC_ERR_CUDA or
- * CFC_ERR_LAUNCH_FAILED.
+ * then reports 1 (and clears it).  No fault is raised and the context stays usable, and
+ * other work of this library, before or after it, is not affected.  Returns CFC_OK,
+ * CFC_ERR_UNSUPPORTED_DEVICE, CFC_ERR_CUDA or CFC_ERR_LAUNCH_FAILED.
  */
 int cfc_wait_self_test(cfc_stream_t stream);
 

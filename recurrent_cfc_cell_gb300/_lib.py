@@ -15,15 +15,25 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libcfc.so")
 
 CFC_OK = 0
-CFC_DW_ACCURATE = 0
-CFC_DW_SIMT_FP32 = 2
+CFC_DW_ACCURATE = 0   # tensor cores, two bf16 terms per operand (three products per step)
+CFC_DW_BF16 = 1       # tensor cores, one bf16 product per step
+CFC_DW_TF32 = 2       # tensor cores, one tf32 product per step
+CFC_DW_SIMT_FP32 = 3  # CUDA-core fp32
+DW_MODES = (CFC_DW_ACCURATE, CFC_DW_BF16, CFC_DW_TF32, CFC_DW_SIMT_FP32)
+
+
+def dpre_operand_pitch(C: int, dw_mode: int) -> int:
+    """bf16 values per term in a d_pre row of the workspace head (modes ACCURATE and BF16), as
+    include/cfc.h documents: 4C rounded up to a multiple of 8."""
+    return (4 * C + 7) // 8 * 8
 
 # Public C symbols declared in include/cfc.h (checked by the test suite).
 EXPORTED = ("cfc_workspace_bytes", "cfc_forward", "cfc_backward", "cfc_backward_recurrence",
             "cfc_weight_grad", "reduce_axis0", "cfc_error_string", "cfc_device_status",
             "cfc_backward_noalloc", "cfc_input_projection", "cfc_forward_recurrence",
             "cfc_step_launches", "cfc_forward_backward", "cfc_bptt_workspace_bytes",
-            "cfc_backward_recurrence_ws", "cfc_wait_self_test")
+            "cfc_backward_recurrence_ws", "cfc_wait_self_test", "cfc_probe_fma",
+            "cfc_probe_l2_read")
 CFC_ERR_SCRATCH_LIMIT = -10
 NOALLOC_SCRATCH_BYTES = 32 << 20  # size of cfc_backward_noalloc's built-in device scratch
 
@@ -79,6 +89,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.cfc_device_status.restype = i
     lib.cfc_wait_self_test.argtypes = [vp]
     lib.cfc_wait_self_test.restype = i
+    dptr = ctypes.POINTER(ctypes.c_double)
+    lib.cfc_probe_fma.argtypes = [vp, i, i, dptr, vp]
+    lib.cfc_probe_fma.restype = i
+    lib.cfc_probe_l2_read.argtypes = [vp, sz, i, vp, i, dptr, vp]
+    lib.cfc_probe_l2_read.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -270,6 +285,23 @@ def cfc_wait_self_test(stream=None) -> None:
     """Enqueue the self-test kernel whose bounded wait runs out (read the result with
     device_status(): 1 after about 2 s)."""
     _check("cfc_wait_self_test", load().cfc_wait_self_test(_stream(stream)))
+
+
+def probe_fma(out, blocks: int, iters: int, stream=None) -> float:
+    """Enqueue the fp32 FMA throughput probe; returns the flops it performs."""
+    flop = ctypes.c_double(0)
+    _check("cfc_probe_fma", load().cfc_probe_fma(_ptr(out, "out"), blocks, iters,
+                                                 ctypes.byref(flop), _stream(stream)))
+    return flop.value
+
+
+def probe_l2_read(buf, passes: int, out, blocks: int, stream=None) -> float:
+    """Enqueue the L2 read-bandwidth probe over ``buf``; returns the bytes it reads."""
+    nbytes = ctypes.c_double(0)
+    _check("cfc_probe_l2_read",
+           load().cfc_probe_l2_read(_ptr(buf, "buf"), buf.numel(), passes, _ptr(out, "out"), blocks,
+                                    ctypes.byref(nbytes), _stream(stream)))
+    return nbytes.value
 
 
 def device_status() -> int:

@@ -29,7 +29,18 @@ struct DeviceState {
 };
 
 constexpr int kMaxDevices = 64;
+// Shared memory per CTA the launch plans assume (GB300's opt-in limit, 227 KB): plans, hence
+// workspace sizes and summation orders, depend only on the problem sizes.
+constexpr int kSmemBudget = 227 * 1024;
 std::mutex g_mu;
+
+bool valid_mode(int m) {
+  return m == CFC_DW_ACCURATE || m == CFC_DW_BF16 || m == CFC_DW_TF32 || m == CFC_DW_SIMT_FP32;
+}
+// bf16 operand planes the BPTT writes for the contraction (0: fp32 d_pre).
+int dpre_planes(int mode) {
+  return mode == CFC_DW_ACCURATE ? 2 : mode == CFC_DW_BF16 ? 1 : 0;
+}
 DeviceState g_dev[kMaxDevices];
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -70,6 +81,8 @@ int device_state(DeviceState** out) {
         rc = cuda_rc(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
                      CFC_ERR_CUDA);
       if (rc == CFC_OK) rc = cuda_rc(cfc::tc_prepare(optin), CFC_ERR_CUDA);
+      if (rc == CFC_OK && optin < kSmemBudget) rc = CFC_ERR_UNSUPPORTED_DEVICE;
+      if (rc == CFC_OK) rc = cuda_rc(cfc::contract_prepare(optin), CFC_ERR_CUDA);
       if (rc != CFC_OK) return rc;  // retried on the next call
       st.status = static_cast<int*>(addr);
       st.init = true;
@@ -155,23 +168,17 @@ int plan_rows(DeviceState& st, int kind, int variant, int CS, int B, int n_x, in
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct BwdLayout {
-  size_t d_pre_off, d_pre_bytes, part_off, part_bytes, total;
-  int S_simt;          // split count of the CUDA-core contraction
-  cfc::TcPlan tc;      // plan of the tensor-core weight-gradient contraction (no du)
-  cfc::TcPlan tu;      // plan of du beside the dW splits (dual: unsplit, written directly)
-  bool dual;           // large B*K: du unsplit in the dW launch, one merge
-  cfc::TcPlan pw, pu;  // small B*K: dW and du splits sized together for one launch, one merge
-  size_t pu_off;       // offset (floats) of the du partials after the dW partials
-  bool tc_bptt;        // the BPTT runs on the tensor cores (W_h^T pre-split at wsplit_off)
+  size_t d_pre_off, d_pre_bytes;  // d_pre: fp32 rows, or the bf16 operand rows (4 mp bytes)
+  size_t z_off, wt_off;           // contraction operands z [B*K] rows and W_u^T [n_x] rows
+  size_t dt_off, zt_off;          // tf32: d_pre^T [4C][bkp] and z^T [n_in + 1][bkp] (fp32)
+  size_t part_off, part_bytes;    // split partials of the weight-gradient contraction
+  size_t total;
+  int mp;                         // d_pre operand pitch
+  int S_simt;                     // split count of the CUDA-core contraction
+  cfc::ContractPlan pdw, pdu;     // tensor-core dW and du plans
+  bool tc_bptt;                   // the BPTT runs on the tensor cores (W_h^T pre-split at wsplit_off)
   size_t wsplit_off;
 };
-
-// Row tiles (of 128) from which unsplit du tiles keep enough SMs busy beside the dW splits:
-// measured on GB300, the combined launch took the gradient stage of B*K = 262144 from 3.85 to
-// 3.17 ms, while at B*K = 2048 (16 tiles) unsplit du was slower than dW, merge, split du (31.6
-// against 26.3 us); below it both are split, sized together (dwdu_tc_plans).
-constexpr int kDualMinDuTiles = 64;
-
 // Rows (B*K) from which the input projection runs on the tensor cores (bf16 hi/lo split,
 // tc_gemm_kernel<ProjProblem>) rather than on the CUDA cores (inproj_kernel): below it the
 // CUDA-core kernel's single short wave is faster than the tensor-core kernel's set-up.
@@ -197,29 +204,34 @@ int tc_bwd_min_rows(int C) { return C >= 256 ? 1024 : 1185; }
 // little enough to sit beside a forward CTA of 32 channels per CTA up to 128 channels.
 constexpr size_t kDependentBwdSmem = 116 * 1024;
 
-BwdLayout bwd_layout(int B, int K, int C, int n_x) {
-  BwdLayout L;
+BwdLayout bwd_layout(int B, int K, int C, int n_x, int mode) {
+  BwdLayout L{};
   const size_t BK = static_cast<size_t>(B) * K;
+  const int n_in = n_x + C;
   L.d_pre_off = 0;
-  L.d_pre_bytes = BK * 4 * C * sizeof(float);
-  L.S_simt = cfc::dw_simt_splits(static_cast<int>(BK));
-  L.tc = cfc::dw_tc_plan(B, K, C, n_x);
-  // With enough rows du runs unsplit beside the dW splits (one launch, du written directly);
-  // otherwise both run split in one launch, sized together, and one launch merges both.
-  L.tu = cfc::du_tc_plan_unsplit(B, K, C, n_x);
-  L.dual = L.tu.m_tiles >= kDualMinDuTiles;
-  cfc::dwdu_tc_plans(B, K, C, n_x, &L.pw, &L.pu);
-  const size_t pitch = cfc::dw_tc_pitch(n_x + C);
-  size_t part = static_cast<size_t>(L.S_simt) * 4 * C * (n_x + C);
-  const size_t ptc = static_cast<size_t>(L.tc.splits) * 4 * C * pitch;
-  if (ptc > part) part = ptc;
-  L.pu_off = static_cast<size_t>(L.pw.splits) * 4 * C * pitch;
-  if (!L.dual) {
-    const size_t ppair = L.pu_off + (L.pu.splits > 1 ? static_cast<size_t>(L.pu.splits) * BK * n_x : 0);
-    if (ppair > part) part = ppair;
+  if (mode == CFC_DW_SIMT_FP32) {
+    L.mp = 4 * C;
+    L.d_pre_bytes = BK * 4 * C * sizeof(float);
+    L.S_simt = cfc::dw_simt_splits(static_cast<int>(BK));
+    L.z_off = L.wt_off = L.part_off = align256(L.d_pre_bytes);
+    L.part_bytes = static_cast<size_t>(L.S_simt) * 4 * C * n_in * sizeof(float);
+  } else {
+    const int form = mode;  // the tensor-core modes are the operand forms
+    L.mp = cfc::contract_m_pitch(C, form);
+    L.d_pre_bytes = BK * 4 * static_cast<size_t>(L.mp);  // 4 mp bytes per row in every form
+    L.z_off = align256(L.d_pre_bytes);
+    L.wt_off = align256(L.z_off + BK * 4 * static_cast<size_t>(cfc::contract_z_pitch(n_in, form)));
+    L.part_off = align256(L.wt_off + static_cast<size_t>(n_x) * 4 * cfc::contract_wt_pitch(C));
+    if (form == cfc::kFormTf32) {
+      const size_t bkp = cfc::contract_bk_pitch(static_cast<int>(BK));
+      L.dt_off = L.part_off;
+      L.zt_off = align256(L.dt_off + static_cast<size_t>(4) * C * bkp * sizeof(float));
+      L.part_off = align256(L.zt_off + static_cast<size_t>(n_in + 1) * bkp * sizeof(float));
+    }
+    L.pdw = cfc::dw_contract_plan(B, K, C, n_x, form, kSmemBudget);
+    L.pdu = cfc::du_contract_plan(B, K, C, n_x, form, kSmemBudget);
+    L.part_bytes = static_cast<size_t>(L.pdw.splits) * 4 * C * cfc::dw_tc_pitch(n_in) * sizeof(float);
   }
-  L.part_off = align256(L.d_pre_bytes);
-  L.part_bytes = part * sizeof(float);
   L.total = L.part_off + L.part_bytes;
   L.tc_bptt = B >= tc_bwd_min_rows(C) && cfc::bwd_tc_supported(C);
   L.wsplit_off = align256(L.total);
@@ -252,9 +264,9 @@ const char* cfc_error_string(int code) {
 int cfc_workspace_bytes(int B, int K, int C, int n_x, int dw_mode, size_t* bwd_ws_bytes) {
   const int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
-  if (dw_mode != CFC_DW_ACCURATE && dw_mode != CFC_DW_SIMT_FP32) return CFC_ERR_INVALID_ARG;
+  if (!valid_mode(dw_mode)) return CFC_ERR_INVALID_ARG;
   if (!bwd_ws_bytes) return CFC_ERR_NULL_PTR;
-  *bwd_ws_bytes = bwd_layout(B, K, C, n_x).total;
+  *bwd_ws_bytes = bwd_layout(B, K, C, n_x, dw_mode).total;
   return CFC_OK;
 }
 
@@ -325,7 +337,8 @@ int forward_recurrence(const float* h0, const float* W, const float* ts, int B, 
 // memory is then padded past half an SM, so that two BPTT CTAs never share one SM.
 int backward_recurrence(const float* dH, const float* W, const float* ts, const float* cache,
                         int B, int K, int C, int n_x, float* d_pre, float* dh0,
-                        cfc_stream_t stream, bool pdl, void* wsplit = nullptr) {
+                        cfc_stream_t stream, bool pdl, void* wsplit = nullptr, int dplanes = 0,
+                        int dpitch = 0) {
   int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
   if (!dH || !W || !ts || !cache || !d_pre || !dh0) return CFC_ERR_NULL_PTR;
@@ -342,6 +355,8 @@ int backward_recurrence(const float* dH, const float* W, const float* ts, const 
   p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
   p.CS = cluster_size_for(C, cfc::kBwdChanPerCta);
   p.wsplit = wsplit;
+  p.dplanes = dplanes;
+  p.dpitch = dpitch;
   // The tensor-core BPTT moves dH, the cache and d_pre in whole 32-byte sectors.
   if (wsplit && B >= tc_bwd_min_rows(C) && cfc::bwd_tc_supported(C) && aligned32(dH) &&
       aligned32(cache) && aligned32(d_pre)) {
@@ -394,16 +409,16 @@ int cfc_forward(const float* u, const float* h0, const float* W, const float* b,
 int cfc_step_launches(int B, int K, int C, int n_x, int dw_mode, int with_du, int* launches) {
   const int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
-  if (dw_mode != CFC_DW_ACCURATE && dw_mode != CFC_DW_SIMT_FP32) return CFC_ERR_INVALID_ARG;
+  if (!valid_mode(dw_mode)) return CFC_ERR_INVALID_ARG;
   if (!launches) return CFC_ERR_NULL_PTR;
-  // forward: projection + recurrence; backward: recurrence, dW contraction + its reduction
-  // (which also yields db with the tensor cores; a separate db reduction otherwise), and du
-  // (inside the dW launch, and its partials inside the dW merge, with the tensor cores; a
-  // launch of its own otherwise).
-  int n = 2 + 1 + 2 + (dw_mode == CFC_DW_ACCURATE ? 0 : 1);
-  const BwdLayout L = bwd_layout(B, K, C, n_x);
-  if (with_du && dw_mode != CFC_DW_ACCURATE) n += 1;
-  if (L.tc_bptt) n += 1;  // W_h^T pre-split for the tensor-core BPTT
+  // forward: projection + recurrence; backward: the recurrence (after the W_h^T pre-split on
+  // the tensor-core path), then either the operand build, the dW contraction, du and the merge
+  // (tensor-core modes), or the dW contraction, its merge, the db sum and du (CUDA cores).
+  int n = 2 + 1 + 3 + (with_du ? 1 : 0);
+  const BwdLayout L = bwd_layout(B, K, C, n_x, dw_mode);
+  if (L.tc_bptt) n += 1;
+  if (dw_mode == CFC_DW_TF32) n += 2;  // transposed copies of d_pre and z
+  if (L.tc_bptt && dpre_planes(dw_mode) > 0) n += 1;  // d_pre split after the tensor-core BPTT
   *launches = n;
   return CFC_OK;
 }
@@ -418,7 +433,7 @@ int cfc_bptt_workspace_bytes(int B, int K, int C, int n_x, size_t* bytes) {
   const int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
   if (!bytes) return CFC_ERR_NULL_PTR;
-  *bytes = bwd_layout(B, K, C, n_x).tc_bptt ? cfc::bwd_tc_split_bytes(C) : 0;
+  *bytes = bwd_layout(B, K, C, n_x, CFC_DW_ACCURATE).tc_bptt ? cfc::bwd_tc_split_bytes(C) : 0;
   return CFC_OK;
 }
 
@@ -441,76 +456,133 @@ int cfc_backward_recurrence_ws(const float* dH, const float* W, const float* ts,
 
 namespace {
 
+// The d_pre form the BPTT of cfc_backward writes: the contraction's bf16 rows straight from
+// the CUDA-core recurrence; fp32 from the tensor-core recurrence, split in place afterwards
+// (measured on GB300 at B=2048, K=128, C=256: the recurrence took 6.74 ms writing bf16 rows
+// and 5.40 ms writing fp32; the split pass takes about 0.3 ms).  C is 128 or 256 there, so the
+// rows' operand bytes are their fp32 bytes and the in-place split is safe.
+int bptt_dplanes(const BwdLayout& L, int mode) {
+  return L.tc_bptt ? 0 : dpre_planes(mode);
+}
+
+// The standalone weight-gradient stage splits an fp32 d_pre into the workspace head.  That is
+// safe when d_pre lies outside the head, or is the head itself with rows whose operand bytes
+// are their fp32 bytes (each row is rewritten from its own values only); any other overlap is
+// rejected.
+struct BwdLayoutCheck {
+  bool ok;
+};
+BwdLayoutCheck check_dpre_alias(const float* d_pre, bool dpre_in_ws, const char* head,
+                                const BwdLayout& L, int B, int K, int C, int mode) {
+  if (dpre_in_ws || mode == CFC_DW_SIMT_FP32 || mode == CFC_DW_TF32) return {true};
+  const char* a = reinterpret_cast<const char*>(d_pre);
+  const size_t a_bytes = static_cast<size_t>(B) * K * 4 * C * sizeof(float);
+  const bool overlap = a < head + L.d_pre_bytes && head < a + a_bytes;
+  if (!overlap) return {true};
+  return {a == head && L.mp == 4 * C};
+}
+
 // `first_pdl`: the previous kernel of the stream is this library's BPTT recurrence of the same
 // backward call; every later kernel here follows one of this function's own kernels.
+// `dpre_in_ws`: d_pre is already in the workspace head in the mode's operand form (written so
+// by the BPTT of cfc_backward); otherwise d_pre is fp32 [K][B][4][C] anywhere.
+// `build_first`: the previous kernel is the BPTT recurrence, which releases its dependents only
+// after its own dependency wait, so the operand build (which needs only the forward's outputs)
+// runs beside it; otherwise the d_pre split comes first and the build runs beside that.
 int weight_grad(const float* d_pre, const float* u, const float* h0, const float* W,
                 const float* H, int B, int K, int C, int n_x, float* dW, float* db, float* du,
-                void* ws, size_t ws_bytes, int dw_mode, cfc_stream_t stream, bool first_pdl) {
+                void* ws, size_t ws_bytes, int dw_mode, cfc_stream_t stream, bool first_pdl,
+                bool dpre_in_ws, bool build_first = false) {
   int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
-  if (dw_mode != CFC_DW_ACCURATE && dw_mode != CFC_DW_SIMT_FP32) return CFC_ERR_INVALID_ARG;
+  if (!valid_mode(dw_mode)) return CFC_ERR_INVALID_ARG;
   if (!d_pre || !u || !h0 || !W || !H || !dW || !db || !ws) return CFC_ERR_NULL_PTR;
   if (!aligned16(d_pre) || !aligned16(u) || !aligned16(h0) || !aligned16(W) || !aligned16(H) ||
       !aligned16(dW) || !aligned16(db) || (du && !aligned16(du)) || !aligned16(ws))
     return CFC_ERR_MISALIGNED;
-  const BwdLayout L = bwd_layout(B, K, C, n_x);
+  const BwdLayout L = bwd_layout(B, K, C, n_x, dw_mode);
   if (ws_bytes < L.total) return CFC_ERR_WS_TOO_SMALL;
+  char* w = static_cast<char*>(ws);
+  const BwdLayoutCheck chk = check_dpre_alias(d_pre, dpre_in_ws, w + L.d_pre_off, L, B, K, C,
+                                              dw_mode);
+  if (!chk.ok) return CFC_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* st = nullptr;
   rc = device_state(&st);
   if (rc != CFC_OK) return rc;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + L.part_off);
+  float* partial = reinterpret_cast<float*>(w + L.part_off);
   const int BK = B * K;
   const int M = 4 * C, N = n_x + C;
-  int S = 0;
   if (dw_mode == CFC_DW_SIMT_FP32) {
-    S = L.S_simt;
+    const int S = L.S_simt;
     rc = cuda_rc(cfc::dw_simt_launch(d_pre, u, H, h0, B, K, C, n_x, S, partial, s, first_pdl),
                  CFC_ERR_LAUNCH_FAILED);
-  } else if (du && L.dual) {
-    // dW partials and du from one grid: both read only d_pre (and the inputs).
-    S = L.tc.splits;
-    rc = cuda_rc(cfc::dwdu_tc_launch(L.tc, L.tu, d_pre, u, H, h0, W, B, K, C, n_x, partial, du,
-                                     st->status, s, first_pdl),
+    if (rc == CFC_OK)
+      rc = cuda_rc(cfc::reduce_axis0_launch(partial, S, M * N, dW, s, true), CFC_ERR_LAUNCH_FAILED);
+    if (rc == CFC_OK)
+      rc = cuda_rc(cfc::reduce_axis0_launch(d_pre, BK, M, db, s, true), CFC_ERR_LAUNCH_FAILED);
+    if (rc == CFC_OK && du)
+      rc = cuda_rc(cfc::du_simt_launch(d_pre, W, BK, C, n_x, du, s, true), CFC_ERR_LAUNCH_FAILED);
+    return rc;
+  }
+  // Tensor cores: the operand form is the mode.  The d_pre operand: the fp32 d_pre itself
+  // (tf32), the rows the BPTT left in the workspace head, or a split of the fp32 d_pre into
+  // the head (in place when d_pre is the head and a row's operand bytes are its fp32 bytes).
+  const int form = dw_mode;
+  const void* dop = form == cfc::kFormTf32 ? static_cast<const void*>(d_pre) : w + L.d_pre_off;
+  const bool split = form != cfc::kFormTf32 && !dpre_in_ws;
+  bool pdl = first_pdl;
+  auto launch_build = [&]() {
+    rc = cuda_rc(cfc::build_operands_launch(form, u, H, h0, W, B, K, C, n_x, w + L.z_off,
+                                            w + L.wt_off, s, pdl),
                  CFC_ERR_LAUNCH_FAILED);
-  } else if (du) {
-    // dW and du partials from one grid, then one launch merging both.
-    float* pu = L.pu.splits > 1 ? partial + L.pu_off : du;
-    rc = cuda_rc(cfc::dwdu_tc_launch(L.pw, L.pu, d_pre, u, H, h0, W, B, K, C, n_x, partial, pu,
-                                     st->status, s, first_pdl),
+    pdl = true;
+  };
+  auto launch_split = [&]() {
+    rc = cuda_rc(cfc::split_dpre_launch(form, d_pre, BK, C, w + L.d_pre_off, s, pdl),
                  CFC_ERR_LAUNCH_FAILED);
-    if (rc != CFC_OK) return rc;
-    const int pitch = cfc::dw_tc_pitch(N);
-    if (L.pu.splits > 1)
-      return cuda_rc(cfc::reduce_axis0_pair_launch(partial, L.pw.splits, M * pitch, pitch, N, dW,
-                                                   db, pu, L.pu.splits, BK * n_x, du, s, true),
-                     CFC_ERR_LAUNCH_FAILED);
-    return cuda_rc(cfc::reduce_axis0_rows_launch(partial, L.pw.splits, M * pitch, pitch, N, dW,
-                                                 db, s, true),
+    pdl = true;
+  };
+  if (build_first || !split) {
+    launch_build();
+    if (rc == CFC_OK && split) launch_split();
+  } else {
+    launch_split();
+    if (rc == CFC_OK) launch_build();
+  }
+  if (rc != CFC_OK) return rc;
+  const void* a_dw = dop;
+  const void* b_dw = w + L.z_off;
+  if (form == cfc::kFormTf32) {
+    // The tf32 weight gradient reads K-major copies: d_pre^T and z^T.
+    const int bkp = cfc::contract_bk_pitch(BK);
+    float* dt = reinterpret_cast<float*>(w + L.dt_off);
+    float* zt = reinterpret_cast<float*>(w + L.zt_off);
+    rc = cuda_rc(cfc::transpose_launch(d_pre, BK, M, M, dt, bkp, s, true), CFC_ERR_LAUNCH_FAILED);
+    if (rc == CFC_OK)
+      rc = cuda_rc(cfc::transpose_launch(reinterpret_cast<const float*>(w + L.z_off), BK, N + 1,
+                                         cfc::contract_z_pitch(N, form), zt, bkp, s, true),
                    CFC_ERR_LAUNCH_FAILED);
-  } else {
-    S = L.tc.splits;
-    rc = cuda_rc(cfc::dw_tc_launch(L.tc, d_pre, u, H, h0, B, K, C, n_x, partial, st->status, s,
-                                   first_pdl),
-                 CFC_ERR_LAUNCH_FAILED);
+    if (rc != CFC_OK) return rc;
+    a_dw = dt;
+    b_dw = zt;
   }
+  const int pitch = cfc::dw_tc_pitch(N);
+  rc = cuda_rc(cfc::dw_contract_launch(L.pdw, form, a_dw, b_dw, B, K, C, n_x, partial,
+                                       pitch, st->status, s, true),
+               CFC_ERR_LAUNCH_FAILED);
   if (rc != CFC_OK) return rc;
-  if (dw_mode == CFC_DW_SIMT_FP32) {
-    rc = cuda_rc(cfc::reduce_axis0_launch(partial, S, M * N, dW, s, true),
+  if (du) {
+    rc = cuda_rc(cfc::du_contract_launch(L.pdu, form, dop, w + L.wt_off, B, K, C, n_x, du,
+                                         st->status, s, true, true),
                  CFC_ERR_LAUNCH_FAILED);
     if (rc != CFC_OK) return rc;
-    rc = cuda_rc(cfc::reduce_axis0_launch(d_pre, BK, M, db, s, true), CFC_ERR_LAUNCH_FAILED);
-  } else {
-    // One merge for both: the partial rows carry the all-ones column, i.e. db.
-    const int pitch = cfc::dw_tc_pitch(N);
-    rc = cuda_rc(cfc::reduce_axis0_rows_launch(partial, S, M * pitch, pitch, N, dW, db, s, true),
-                 CFC_ERR_LAUNCH_FAILED);
   }
-  if (rc != CFC_OK) return rc;
-  if (du && dw_mode == CFC_DW_SIMT_FP32)
-    rc = cuda_rc(cfc::du_simt_launch(d_pre, W, BK, C, n_x, du, s, true), CFC_ERR_LAUNCH_FAILED);
-  return rc;
+  // One merge for both: the partial rows carry the all-ones column, i.e. db.
+  return cuda_rc(cfc::reduce_axis0_rows_launch(partial, L.pdw.splits, M * pitch, pitch, N, dW, db,
+                                               s, true),
+                 CFC_ERR_LAUNCH_FAILED);
 }
 
 }  // namespace
@@ -521,7 +593,7 @@ int cfc_weight_grad(const float* d_pre, const float* u, const float* h0, const f
                     const float* H, int B, int K, int C, int n_x, float* dW, float* db,
                     float* du, void* ws, size_t ws_bytes, int dw_mode, cfc_stream_t stream) {
   return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode,
-                     stream, false);
+                     stream, false, false);
 }
 
 int cfc_backward(const float* dH, const float* u, const float* h0, const float* W,
@@ -530,21 +602,23 @@ int cfc_backward(const float* dH, const float* u, const float* h0, const float* 
                  size_t ws_bytes, int dw_mode, cfc_stream_t stream) {
   int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
-  if (dw_mode != CFC_DW_ACCURATE && dw_mode != CFC_DW_SIMT_FP32) return CFC_ERR_INVALID_ARG;
+  if (!valid_mode(dw_mode)) return CFC_ERR_INVALID_ARG;
   if (!dH || !u || !h0 || !W || !ts || !H || !cache || !dW || !db || !dh0 || !ws)
     return CFC_ERR_NULL_PTR;
   if (!aligned16(dH) || !aligned16(u) || !aligned16(h0) || !aligned16(W) || !aligned16(ts) ||
       !aligned16(H) || !aligned16(cache) || !aligned16(dW) || !aligned16(db) ||
       (du && !aligned16(du)) || !aligned16(dh0) || !aligned16(ws))
     return CFC_ERR_MISALIGNED;
-  const BwdLayout L = bwd_layout(B, K, C, n_x);
+  const BwdLayout L = bwd_layout(B, K, C, n_x, dw_mode);
   if (ws_bytes < L.total) return CFC_ERR_WS_TOO_SMALL;
   float* d_pre = reinterpret_cast<float*>(static_cast<char*>(ws) + L.d_pre_off);
+  const int dplanes = bptt_dplanes(L, dw_mode);
   rc = backward_recurrence(dH, W, ts, cache, B, K, C, n_x, d_pre, dh0, stream, false,
-                           L.tc_bptt ? static_cast<char*>(ws) + L.wsplit_off : nullptr);
+                           L.tc_bptt ? static_cast<char*>(ws) + L.wsplit_off : nullptr, dplanes,
+                           L.mp);
   if (rc != CFC_OK) return rc;
   return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode, stream,
-                     true);
+                     true, dplanes == dpre_planes(dw_mode), true);
 }
 
 int cfc_forward_backward(const float* u, const float* h0, const float* W, const float* b,
@@ -553,24 +627,26 @@ int cfc_forward_backward(const float* u, const float* h0, const float* W, const 
                          void* ws, size_t ws_bytes, int dw_mode, cfc_stream_t stream) {
   int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
-  if (dw_mode != CFC_DW_ACCURATE && dw_mode != CFC_DW_SIMT_FP32) return CFC_ERR_INVALID_ARG;
+  if (!valid_mode(dw_mode)) return CFC_ERR_INVALID_ARG;
   if (!u || !h0 || !W || !b || !ts || !dH || !H || !cache || !dW || !db || !dh0 || !ws)
     return CFC_ERR_NULL_PTR;
   if (!aligned16(u) || !aligned16(h0) || !aligned16(W) || !aligned16(b) || !aligned16(ts) ||
       !aligned16(dH) || !aligned16(H) || !aligned16(cache) || !aligned16(dW) ||
       !aligned16(db) || (du && !aligned16(du)) || !aligned16(dh0) || !aligned16(ws))
     return CFC_ERR_MISALIGNED;
-  const BwdLayout L = bwd_layout(B, K, C, n_x);
+  const BwdLayout L = bwd_layout(B, K, C, n_x, dw_mode);
   if (ws_bytes < L.total) return CFC_ERR_WS_TOO_SMALL;
   rc = cfc_forward(u, h0, W, b, ts, B, K, C, n_x, H, cache, stream);
   if (rc != CFC_OK) return rc;
   // The forward writes only H and cache, which the BPTT reads after its dependency wait.
   float* d_pre = reinterpret_cast<float*>(static_cast<char*>(ws) + L.d_pre_off);
+  const int dplanes = bptt_dplanes(L, dw_mode);
   rc = backward_recurrence(dH, W, ts, cache, B, K, C, n_x, d_pre, dh0, stream, true,
-                           L.tc_bptt ? static_cast<char*>(ws) + L.wsplit_off : nullptr);
+                           L.tc_bptt ? static_cast<char*>(ws) + L.wsplit_off : nullptr, dplanes,
+                           L.mp);
   if (rc != CFC_OK) return rc;
   return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode, stream,
-                     true);
+                     true, dplanes == dpre_planes(dw_mode), true);
 }
 
 int reduce_axis0(const float* per_batch, int n_batch, int n_tail, float* out,

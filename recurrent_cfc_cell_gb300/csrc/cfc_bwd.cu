@@ -38,6 +38,8 @@
 //     uses predicated loads, stores and st.async;
 //   * the W_h^T columns are read once, coalesced, into shared memory and from there into
 //     registers (a direct load would fetch one 32-byte sector per 4-byte value).
+#include <cuda_bf16.h>
+
 #include "cfc_kernels.h"
 #include "cfc_launch.cuh"
 #include "cfc_ptx.cuh"
@@ -151,7 +153,8 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || (CS == 4 && (RT == 0 
   float* pre = dg + 2 * R * S::GROW;     // ring path: [kPre][R][8 warps][4][5]
   const int pre_floats = RT > 0 ? 0 : kPre * R * kWarps * 4 * kPreComp;
   uint64_t* bars = reinterpret_cast<uint64_t*>(pre + pre_floats);
-  grid_dep_launch_dependents();
+  // Dependents are released only after this kernel's own dependency wait (below): the
+  // operand build that follows reads the forward's H without waiting for this kernel.
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -180,7 +183,13 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || (CS == 4 && (RT == 0 
   bool rok[RR];
 #pragma unroll
   for (int r = 0; r < RR; ++r) rok[r] = row0 + r < B;
-  const bool stores = (lane & 1) == 0 && ch < C;  // one lane per (channel, gate) stores d_pre
+  // fp32 output: one lane of each (channel, gate) pair stores d_pre.  bf16 operand rows (2 *
+  // dpitch values per row): the even lane stores the hi term, the odd lane the lo term.
+  const bool planes = p.dplanes > 0;
+  const bool stores = ch < C && ((lane & 1) == 0 || p.dplanes == 2);
+  const size_t prow = 2 * static_cast<size_t>(p.dpitch);  // bf16 values per operand row
+  __nv_bfloat16* dqp = reinterpret_cast<__nv_bfloat16*>(p.d_pre) + t_last * prow +
+                       ((lane & 1) ? p.dpitch : 0) + static_cast<size_t>(gq) * C + chc;
 
   // W_h^T columns of this warp's four channels over gathered rows [lane*RS, lane*RS + RS).
   // Gathered row q*128 + 4i + g is W row g*C + 32q + i.  Staged through shared memory as
@@ -211,6 +220,7 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || (CS == 4 && (RT == 0 
           // unless this launch is a dependent one), then start the step K-1 loads, in flight
           // together with the first chunk of W_h^T.
           grid_dep_wait();
+          grid_dep_launch_dependents();
           load_step_regs<RR>(dHp, cp, tsp, C, rok, cur);
           dHp -= bc;
           cp -= 3 * bc;
@@ -258,6 +268,7 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || (CS == 4 && (RT == 0 
   if constexpr (RT == 0) {
     // The ring lives where the W_h^T staging was: start it only now.
     grid_dep_wait();
+    grid_dep_launch_dependents();
     issue_pre(p, pre, K - 1, row0, rank, warp, lane);
     cp_async_commit();
     issue_pre(p, pre, K - 2, row0, rank, warp, lane);
@@ -344,11 +355,21 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || (CS == 4 && (RT == 0 
       for (int rb = 0; rb < RB; ++rb)
         st_async_v4_if(pushes, pdst + static_cast<uint32_t>((r0 + rb) * S::GROW * 4), dq[rb].x,
                        dq[rb].y, dq[rb].z, dq[rb].w, pbar);
+      if (planes) {
 #pragma unroll
-      for (int rb = 0; rb < RB; ++rb)
-        if (stores && row0 + r0 + rb < B) dpp[static_cast<size_t>(r0 + rb) * 4 * C] = dpv[rb];
+        for (int rb = 0; rb < RB; ++rb) {
+          const __nv_bfloat16 hi = __float2bfloat16_rn(dpv[rb]);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(dpv[rb] - __bfloat162float(hi));
+          if (stores && row0 + r0 + rb < B) dqp[static_cast<size_t>(r0 + rb) * prow] = (lane & 1) ? lo : hi;
+        }
+      } else {
+#pragma unroll
+        for (int rb = 0; rb < RB; ++rb)
+          if (stores && row0 + r0 + rb < B) dpp[static_cast<size_t>(r0 + rb) * 4 * C] = dpv[rb];
+      }
     }
     dpp -= 4 * bc;
+    dqp -= static_cast<size_t>(B) * prow;
     if constexpr (RT > 0) {
       if (t >= 1) {
 #pragma unroll

@@ -161,7 +161,6 @@ __global__ void __launch_bounds__(kBThreads, 1) cfc_bwd_tc_kernel(const BwdParam
   const uint32_t done_bar = smem_addr(&bars[3 * NST]);   // a step's delta complete
   const uint32_t sm0 = smem_addr(sm);
 
-  grid_dep_launch_dependents();
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(fa0 + 8u * s, kBEpiWarps * 32 / 2);  // a chunk is written by one warp group
@@ -173,7 +172,10 @@ __global__ void __launch_bounds__(kBThreads, 1) cfc_bwd_tc_kernel(const BwdParam
   }
   // dH, the cache and the pre-split W_h^T come from earlier kernels; tensor memory is taken
   // only after they have finished, so this kernel never waits for columns they hold.
+  // Dependents are released only after this wait: the operand build that follows reads the
+  // forward's H without waiting for this kernel.
   grid_dep_wait();
+  grid_dep_launch_dependents();
   if (warp == kBEpiWarps) {
     tmem_alloc(smem_addr(tslot), 512);
     tc_fence_before_sync();
@@ -188,6 +190,7 @@ __global__ void __launch_bounds__(kBThreads, 1) cfc_bwd_tc_kernel(const BwdParam
       const uint32_t idesc = umma_idesc_bf16(kBM, C);
       constexpr uint32_t kLboA = (kBM / 8) * 128, kLboB = (C / 8) * 128;
       bool ok = true;
+      int commits = 0;  // phases of done_bar this thread has committed
       for (int n = 0; n < K && ok; ++n) {
         const uint32_t dcur = tmem + static_cast<uint32_t>((n & 1) * C);
         uint32_t acc = 0;
@@ -218,11 +221,17 @@ __global__ void __launch_bounds__(kBThreads, 1) cfc_bwd_tc_kernel(const BwdParam
           umma_commit(em0 + 8u * s);  // the stage may be refilled once these MMAs are done
         }
         umma_commit(done_bar);
+        ++commits;
       }
+      // After an early stop the epilogue may leave before the last committed MMAs finish;
+      // they depend on nothing outside this CTA, so wait for them before tensor memory is
+      // freed.
+      if (!ok && commits > 0) (void)mbar_wait_bounded_cta(done_bar, (commits - 1) & 1, p.status);
     } else if (lane == 1) {
       // ---- W_h^T chunk producer ----
       const uint8_t* wsplit = static_cast<const uint8_t*>(p.wsplit);
       bool ok = true;
+      int issued = 0;  // chunks whose copies this thread has started
       for (int n = 0; n < K && ok; ++n) {
         for (int kc = 0; kc < S::NCH; ++kc) {
           const int i = n * S::NCH + kc, s = i % NST;
@@ -235,8 +244,15 @@ __global__ void __launch_bounds__(kBThreads, 1) cfc_bwd_tc_kernel(const BwdParam
             bulk_g2s(dst + tm * S::B_TERM,
                      wsplit + (static_cast<size_t>(kc) * kBTerms + tm) * S::B_TERM, S::B_TERM,
                      fb0 + 8u * s);
+          ++issued;
         }
       }
+      // After an early stop, no copy into this CTA's shared memory may still be in flight when
+      // it exits: wait for the last chunks' copies to land (bulk copies from global memory
+      // always complete).
+      if (!ok)
+        for (int i = issued > NST ? issued - NST : 0; i < issued; ++i)
+          (void)mbar_wait_bounded_cta(fb0 + 8u * (i % NST), (i / NST) & 1, p.status);
     }
   } else {
     // ---- epilogue warps: row r = 32 q + lane.  Warp group hh (warps 4 hh .. 4 hh + 3, one per
@@ -426,6 +442,7 @@ cudaError_t bwd_tc_prepare(int C, int* max_active_ctas) {
 }
 
 cudaError_t bwd_tc_launch(const BwdParams& p, cudaStream_t s, bool pdl) {
+  if (p.dplanes != 0) return cudaErrorInvalidValue;  // this recurrence writes fp32 d_pre only
   if (p.C == 128) return launch_k<128>(p, s, pdl);
   if (p.C == 256) return launch_k<256>(p, s, pdl);
   return cudaErrorInvalidValue;

@@ -544,6 +544,9 @@ __device__ __forceinline__ void tc_gemm_body(const TcParams& p, int tile, int sp
       umma_commit(empty0 + 8u * s);  // stage reusable once these MMAs have read it
     }
     umma_commit(accb);  // accumulator complete (also after an early stop)
+    // Whatever the converters did, the MMAs issued here finish before tensor memory is freed:
+    // they depend on nothing outside this CTA, so this wait always completes.
+    (void)mbar_wait_bounded_cta(accb, 0, p.status);
   }
   tc_fence_before_sync();
   __syncthreads();

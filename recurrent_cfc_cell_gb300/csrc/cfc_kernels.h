@@ -42,6 +42,10 @@ struct BwdParams {
   int B, K, C, n_x, n_in;
   int CS, R;
   const void* wsplit;  // tensor-core BPTT: W_h^T pre-split into bf16 terms (bwd_tc_split)
+  // d_pre output form: 0 = fp32 [K][B][4][C] at d_pre; 1 or 2 = that many bf16 planes in the
+  // contraction's operand rows (4 * dpitch bytes per row: hi, then lo) at d_pre.
+  int dplanes;
+  int dpitch;
 };
 
 // Every launch function takes `pdl`: schedule the kernel while the previous kernel of the
@@ -110,6 +114,50 @@ cudaError_t dwdu_tc_launch(const TcPlan& pw, const TcPlan& pu, const float* d_pr
                            const float* u, const float* H, const float* h0, const float* W, int B,
                            int K, int C, int n_x, float* partial, float* du, int* status,
                            cudaStream_t s, bool pdl);
+
+// ---- TMA-fed contractions (cfc_contract.cu) ----
+// Operand forms of the backward contractions, one per tensor-core weight-gradient mode.
+constexpr int kFormBf16x2 = 0;  // two bf16 planes, hi and lo: three MMAs per step (accurate)
+constexpr int kFormBf16 = 1;    // the hi plane alone: one MMA per step
+constexpr int kFormTf32 = 2;    // the fp32 values: one kind::tf32 MMA per step
+// Operand layout: row r of an operand occupies 4 * pitch bytes.  bf16 forms: the hi plane's
+// `pitch` values, then the lo plane's (unused in the bf16 form); tf32: `pitch` floats.  With
+// pitch = 4C a d_pre row has exactly the bytes of its fp32 row.
+int contract_m_pitch(int C, int form);     // d_pre rows: >= 4C (exactly 4C for tf32)
+int contract_wt_pitch(int C);              // W_u^T rows: >= 4C
+int contract_bk_pitch(int BK);             // tf32 transposed operands: rows of >= B*K floats
+// dst[c][r] = src[r][c] (fp32; rows sp / dp floats apart).
+cudaError_t transpose_launch(const float* src, int rows, int cols, int sp, float* dst, int dp,
+                             cudaStream_t s, bool pdl);
+int contract_z_pitch(int n_in, int form);  // z rows: >= n_in + 1
+
+struct ContractPlan {
+  int mt;       // 128-row accumulators per CTA
+  int n_tile, n_tiles, m_tiles;
+  int n_kb, kb_per_split, splits;
+  int stages;
+  size_t smem;
+};
+ContractPlan dw_contract_plan(int B, int K, int C, int n_x, int form, int smem_budget);
+ContractPlan du_contract_plan(int B, int K, int C, int n_x, int form, int smem_budget);
+cudaError_t contract_prepare(int max_smem);
+// z rows [u ; h_{t-1} ; 1] (B*K of them) and W_u^T rows (n_x) in the operand form.
+cudaError_t build_operands_launch(int form, const float* u, const float* H, const float* h0,
+                                  const float* W, int B, int K, int C, int n_x, void* z, void* wt,
+                                  cudaStream_t s, bool pdl);
+// fp32 d_pre [B*K][4C] -> the bf16 operand rows (may be in place when the pitch is 4C).
+cudaError_t split_dpre_launch(int form, const float* d_pre, int BK, int C, void* planes,
+                              cudaStream_t s, bool pdl);
+// dW partials [splits][4C][ldo] (column n_in is db) from the d_pre operand and z.
+cudaError_t dw_contract_launch(const ContractPlan& pl, int form, const void* dpre, const void* z,
+                               int B, int K, int C, int n_x, float* partial, int ldo,
+                               int* status, cudaStream_t s, bool pdl);
+// du [B*K][n_x] from the d_pre operand and W_u^T.  `defer_wait`: launched right after the
+// weight-gradient contraction of the same call, whose operands it shares; it then runs beside
+// that kernel and waits for it only at its end.
+cudaError_t du_contract_launch(const ContractPlan& pl, int form, const void* dpre, const void* wt,
+                               int B, int K, int C, int n_x, float* du, int* status,
+                               cudaStream_t s, bool pdl, bool defer_wait);
 
 // du[r][k] = sum_m d_pre[r][m] * W[m][k] for k < n_x (SIMT fp32).
 cudaError_t du_simt_launch(const float* d_pre, const float* W, int BK, int C, int n_x,

@@ -25,13 +25,23 @@ std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, looked up once per device.  In
-// host code the array's name is only a host-side stand-in, never a device address.
+// host code the array's name is only a host-side stand-in, never a device address.  The
+// device is checked first, so a device of another compute capability gets the same
+// CFC_ERR_UNSUPPORTED_DEVICE as from cfc_backward.  The address is cached for the life of the
+// process: it does not survive cudaDeviceReset.
 int noalloc_scratch(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     (void)cudaGetLastError();
     return CFC_ERR_UNSUPPORTED_DEVICE;
   }
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return CFC_ERR_UNSUPPORTED_DEVICE;
+  }
+  if (major != 10 || minor != 3) return CFC_ERR_UNSUPPORTED_DEVICE;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (g_noalloc_ptr[dev] == nullptr) {
     void* p = nullptr;

@@ -103,19 +103,19 @@ __device__ __forceinline__ bool mbar_try_wait_cta(uint32_t bar, uint32_t parity)
 }
 
 // Wait for phase `parity` of `bar`; returns false (and records a timeout in *status) when
-// the wait exceeds kWaitLimitNs or another CTA has already recorded a failure.
+// the wait exceeds kWaitLimitNs.  The status word is only ever written here, never read: a
+// flag left by an earlier launch (until cfc_device_status reads and clears it) cannot make a
+// later launch give up.  Each wait measures its own limit, so after a failure the other waits
+// of the same launch end within that limit too.
 __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity,
                                                           int* status) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((it & 255u) == 0u) {
-      if (*reinterpret_cast<volatile int*>(status) != kStatusOk) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        atomicExch(status, kStatusTimeout);
-        return false;
-      }
+    if ((it & 255u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicExch(status, kStatusTimeout);
+      return false;
     }
   }
 }
@@ -126,12 +126,9 @@ __device__ __forceinline__ bool mbar_wait_bounded_cta(uint32_t bar, uint32_t par
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_cta(bar, parity)) return true;
-    if ((it & 255u) == 0u) {
-      if (*reinterpret_cast<volatile int*>(status) != kStatusOk) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        atomicExch(status, kStatusTimeout);
-        return false;
-      }
+    if ((it & 255u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicExch(status, kStatusTimeout);
+      return false;
     }
   }
 }

@@ -37,8 +37,25 @@ class KLoopStep:
         self.graph = None
 
     @property
+    def d_pre_is_fp32(self) -> bool:
+        return self.dw_mode in (_lib.CFC_DW_TF32, _lib.CFC_DW_SIMT_FP32)
+
+    @property
     def d_pre(self) -> torch.Tensor:
-        """Pre-activation gradients [K, B, 4, C] (head of the workspace, valid after backward)."""
+        """The head of the workspace, where the backward pass leaves the pre-activation
+        gradients (valid after backward), as include/cfc.h lays it out for the mode: fp32
+        [K, B, 4, C] for the TF32 and SIMT modes; otherwise the raw bf16 operand rows as int16
+        [K, B, 2, MP] (term, then MP = 4C rounded up to 8 values: hi, lo)."""
+        K, B, C = self.K, self.B, self.C
+        if self.d_pre_is_fp32:
+            return self.ws[: 16 * K * B * C].view(torch.float32).view(K, B, 4, C)
+        mp = _lib.dpre_operand_pitch(C, self.dw_mode)
+        return self.ws[: 4 * K * B * mp].view(torch.int16).view(K, B, 2, mp)
+
+    @property
+    def d_pre_fp32_view(self) -> torch.Tensor:
+        """The head of the workspace viewed as fp32 [K, B, 4, C]: where the stage entry points
+        (cfc_backward_recurrence_ws, then cfc_weight_grad) may keep an fp32 d_pre in place."""
         n = self.K * self.B * 4 * self.C
         return self.ws[: 4 * n].view(torch.float32).view(self.K, self.B, 4, self.C)
 

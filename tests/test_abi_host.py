@@ -193,3 +193,27 @@ def test_header_compiles_as_plain_c(tmp_path):
     subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
                     "-I", os.path.join(ROOT, "include"), "-c", str(src), "-o",
                     str(tmp_path / "use_header.o")], check=True, capture_output=True)
+
+
+def test_weight_grad_rejects_an_unsafe_in_place_d_pre(lib):
+    """cfc_weight_grad may rewrite an fp32 d_pre in place at the workspace head only when C is
+    even (each row's operand bytes are then its fp32 bytes); other overlaps are refused before
+    anything is launched."""
+    B, K, n_x = 3, 4, 5
+    f = ctypes.c_void_p(0x100000)
+    for C, mode, want in ((41, 0, INVALID_ARG), (41, 1, INVALID_ARG)):
+        rc_ws, n = ws_bytes(lib, B, K, C, n_x, mode)
+        assert rc_ws == OK
+        d_pre = ctypes.c_void_p(0x100000)  # the head of ws
+        rc = lib.cfc_weight_grad(d_pre, f, f, f, f, B, K, C, n_x, f, f, f, f, n, mode, None)
+        assert rc == want, (C, mode, rc)
+        inside = ctypes.c_void_p(0x100000 + 256)  # inside the head, not at it
+        rc = lib.cfc_weight_grad(inside, f, f, f, f, B, K, 40, n_x, f, f, f, f, 1 << 30, mode,
+                                 None)
+        assert rc == INVALID_ARG
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+def test_workspace_bytes_per_mode(lib, mode):
+    rc, n = ws_bytes(lib, 32, 64, 128, 48, mode)
+    assert rc == OK and n >= 32 * 64 * 4 * 128 * 4

@@ -6,7 +6,8 @@ import numpy as np
 import pytest
 
 import oracle
-from gpu_helpers import GRAD_TOL, H_TOL, assert_parity, oracle_ref, run_gpu
+from gpu_helpers import (GRAD_TOL, H_TOL, assert_parity, errors, oracle_ref, outputs_np, report,
+                         run_gpu, split_planes)
 from recurrent_cfc_cell_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -122,8 +123,7 @@ def test_forward_backward_is_forward_then_backward(shape):
     for name, x in a.outputs().items():
         y = b.outputs()[name]
         assert torch.equal(x, y), name
-    out = {k: v.cpu().numpy() for k, v in b.outputs().items()}
-    assert_parity(out, oracle_ref(inp))
+    assert_parity(outputs_np(b), oracle_ref(inp))
 
 
 @pytest.mark.parametrize("shape", [dict(B=1600, K=4, n_x=8, C=128), dict(B=1030, K=3, n_x=16, C=256),
@@ -131,8 +131,8 @@ def test_forward_backward_is_forward_then_backward(shape):
                          ids=lambda s: "B{B}_K{K}_nx{n_x}_C{C}".format(**s))
 def test_backward_recurrence_ws_is_cfc_backwards_recurrence(shape):
     """cfc_backward_recurrence_ws (tensor cores from B = 1185 at C = 128, 1024 at C = 256)
-    writes bitwise the d_pre and dh0
-    that cfc_backward writes, and they match the oracle."""
+    writes bitwise the dh0 that cfc_backward writes, and an fp32 d_pre whose bf16 hi / lo split
+    is bitwise the operand rows cfc_backward leaves in its workspace; both match the oracle."""
     import torch
 
     from recurrent_cfc_cell_gb300 import _lib, build
@@ -151,7 +151,10 @@ def test_backward_recurrence_ws_is_cfc_backwards_recurrence(shape):
     dh0 = torch.full((B, C), float("nan"), device="cuda")
     _lib.cfc_backward_recurrence_ws(d["dH"], d["W"], d["ts"], a.cache, d_pre, dh0, ws)
     torch.cuda.synchronize()
-    assert torch.equal(d_pre, a.d_pre)
+    raw = a.d_pre.cpu().numpy().view(np.uint16)
+    mp = raw.shape[-1]
+    want = split_planes(d_pre.cpu().numpy(), mp)
+    assert np.array_equal(raw[..., : 4 * C], want[..., : 4 * C])
     assert torch.equal(dh0, a.dh0)
     assert_parity({"d_pre": d_pre.cpu().numpy(), "dh0": dh0.cpu().numpy()}, oracle_ref(inp),
                   keys=("d_pre", "dh0"))
@@ -199,8 +202,59 @@ def test_without_du(shape):
 
 
 def test_simt_fp32_mode_parity():
+    from recurrent_cfc_cell_gb300 import _lib
+
     inp = inputs.make_inputs(inputs.CONFIGS[1])
-    assert_parity(run_gpu(inp, dw_mode=2), oracle_ref(inp))
+    assert_parity(run_gpu(inp, dw_mode=_lib.CFC_DW_SIMT_FP32), oracle_ref(inp))
+
+
+# Single-pass tensor-core modes: not meant for the 1e-4 gradient tolerance.  Their measured
+# errors are reported; the recurrences (H, d_pre before rounding, dh0) are the same as in the
+# accurate mode, and dW / db / du stay within these bounds.
+SINGLE_PASS_BOUND = {1: 3e-2, 2: 1e-2}  # CFC_DW_BF16, CFC_DW_TF32
+
+
+@pytest.mark.parametrize("mode", [1, 2], ids=["bf16", "tf32"])
+@pytest.mark.parametrize("idx", [1, 2, 3])
+def test_single_pass_modes_report_their_error(mode, idx):
+    inp = inputs.make_inputs(inputs.CONFIGS[idx])
+    ref = oracle_ref(inp)
+    g = run_gpu(inp, dw_mode=mode)
+    errs = errors(g, ref, ("H", "cache", "dW", "db", "du", "dh0"))
+    report(f"mode{mode}::{inputs.CONFIGS[idx].name}", errs)
+    assert errs["H"] <= H_TOL and errs["cache"] <= H_TOL and errs["dh0"] <= GRAD_TOL
+    for k in ("dW", "db", "du"):
+        assert np.isfinite(errs[k]) and errs[k] <= SINGLE_PASS_BOUND[mode], (k, errs)
+    # The single pass is measurably less exact than the accurate mode (a real single pass ran).
+    assert errs["dW"] > 1e-5
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2, 3], ids=["accurate", "bf16", "tf32", "simt"])
+@pytest.mark.parametrize("in_place", [False, True], ids=["separate", "in_place"])
+def test_weight_grad_stage_from_fp32_d_pre(mode, in_place):
+    """The two stages called alone: cfc_backward_recurrence_ws writes an fp32 d_pre, then
+    cfc_weight_grad forms the mode's operands from it -- from a separate buffer, or in place
+    at the head of the workspace -- and gives the gradients of cfc_backward in the same mode."""
+    import torch
+
+    from recurrent_cfc_cell_gb300 import _lib, build
+    from recurrent_cfc_cell_gb300.step import KLoopStep, to_device
+
+    build.build()
+    B, K, C, n_x = 9, 7, 72, 20
+    inp = inputs.make_inputs(inputs.custom(B=B, K=K, n_x=n_x, C=C, seed=43))
+    d = to_device(inp)
+    a = KLoopStep(B, K, C, n_x, dw_mode=mode).bind(**d)
+    a.run()
+    st = KLoopStep(B, K, C, n_x, dw_mode=mode).bind(**d)
+    st.forward()
+    d_pre = st.d_pre_fp32_view if in_place else torch.empty((K, B, 4, C), device="cuda")
+    _lib.cfc_backward_recurrence(d["dH"], d["W"], d["ts"], st.cache, d_pre, st.dh0)
+    _lib.cfc_weight_grad(d_pre, d["u"], d["h0"], d["W"], st.H, st.dW, st.db, st.du, st.ws,
+                         dw_mode=mode)
+    torch.cuda.synchronize()
+    for k in ("dW", "db", "du"):
+        assert torch.equal(getattr(st, k), getattr(a, k)), k
 
 
 def test_zero_upstream_gradient_gives_zero_gradients():
@@ -218,35 +272,3 @@ def test_ts_zero_gives_zero_time_a_gradient():
     assert np.all(g["d_pre"][:, :, 2] == 0.0)
     assert np.max(np.abs(g["dW"][2])) <= 1e-6 * np.max(np.abs(g["dW"][3]))
     assert_parity(g, oracle_ref(inp))
-
-
-@pytest.mark.slow
-def test_stress_workload_sampled_rows_and_contraction():
-    """Throughput-stress workload (B=2048, K=128, C=256) in the launch configuration the
-    benchmark times.  Batch rows are independent, so the oracle runs four sampled rows alone
-    and every per-row output (H, cache, d_pre, du, dh0) is compared on those rows.  dW and db
-    are sums over all rows; they are checked as the fp64 contraction of the kernel's own d_pre
-    with z = [u ; h_{t-1}] (a property that holds at any size)."""
-    import torch
-
-    w = inputs.CONFIGS[4]
-    inp = inputs.make_inputs(w)
-    g = run_gpu(inp)
-    rows = np.array([0, 777, 1500, w.B - 1])
-    sub = {"u": inp["u"][:, rows], "h0": inp["h0"][rows], "W": inp["W"], "b": inp["b"],
-           "ts": inp["ts"][:, rows], "dH": inp["dH"][:, rows]}
-    ref = oracle_ref(sub)
-    gsub = {"H": g["H"][:, rows], "cache": g["cache"][:, rows], "d_pre": g["d_pre"][:, rows],
-            "du": g["du"][:, rows], "dh0": g["dh0"][rows]}
-    assert_parity(gsub, ref, keys=("H", "cache", "d_pre", "du", "dh0"))
-
-    K, B, n_x = inp["u"].shape
-    C = inp["h0"].shape[1]
-    d_pre = torch.from_numpy(g["d_pre"]).reshape(K * B, 4 * C).double()
-    hprev = np.concatenate([inp["h0"][None], g["H"][:-1]], axis=0)
-    z = torch.from_numpy(np.concatenate([inp["u"], hprev], axis=2).reshape(K * B, n_x + C)).double()
-    dW_ref = (d_pre.T @ z).reshape(4, C, n_x + C).numpy()
-    db_ref = d_pre.sum(0).reshape(4, C).numpy()
-    assert oracle.rel_err(g["dW"], dW_ref) <= GRAD_TOL
-    assert oracle.rel_err(g["db"], db_ref) <= GRAD_TOL
-    assert H_TOL <= GRAD_TOL
