@@ -176,6 +176,7 @@ struct BwdLayout {
   int mp;                         // d_pre operand pitch
   int S_simt;                     // split count of the CUDA-core contraction
   cfc::ContractPlan pdw, pdu;     // tensor-core dW and du plans
+  size_t pu_off;                  // du split partials (floats into the partials), if du is split
   bool tc_bptt;                   // the BPTT runs on the tensor cores (W_h^T pre-split at wsplit_off)
   size_t wsplit_off;
 };
@@ -228,9 +229,10 @@ BwdLayout bwd_layout(int B, int K, int C, int n_x, int mode) {
       L.zt_off = align256(L.dt_off + static_cast<size_t>(4) * C * bkp * sizeof(float));
       L.part_off = align256(L.zt_off + static_cast<size_t>(n_in + 1) * bkp * sizeof(float));
     }
-    L.pdw = cfc::dw_contract_plan(B, K, C, n_x, form, kSmemBudget);
-    L.pdu = cfc::du_contract_plan(B, K, C, n_x, form, kSmemBudget);
-    L.part_bytes = static_cast<size_t>(L.pdw.splits) * 4 * C * cfc::dw_tc_pitch(n_in) * sizeof(float);
+    cfc::contract_plans(B, K, C, n_x, form, kSmemBudget, &L.pdw, &L.pdu);
+    L.pu_off = static_cast<size_t>(L.pdw.splits) * 4 * C * cfc::dw_tc_pitch(n_in);
+    L.part_bytes = L.pu_off * sizeof(float);
+    if (L.pdu.splits > 1) L.part_bytes += static_cast<size_t>(L.pdu.splits) * BK * n_x * sizeof(float);
   }
   L.total = L.part_off + L.part_bytes;
   L.tc_bptt = B >= tc_bwd_min_rows(C) && cfc::bwd_tc_supported(C);
@@ -573,13 +575,19 @@ int weight_grad(const float* d_pre, const float* u, const float* h0, const float
                                        pitch, st->status, s, true),
                CFC_ERR_LAUNCH_FAILED);
   if (rc != CFC_OK) return rc;
+  float* du_out = (du && L.pdu.splits > 1) ? partial + L.pu_off : du;
   if (du) {
-    rc = cuda_rc(cfc::du_contract_launch(L.pdu, form, dop, w + L.wt_off, B, K, C, n_x, du,
+    rc = cuda_rc(cfc::du_contract_launch(L.pdu, form, dop, w + L.wt_off, B, K, C, n_x, du_out,
                                          st->status, s, true, true),
                  CFC_ERR_LAUNCH_FAILED);
     if (rc != CFC_OK) return rc;
   }
-  // One merge for both: the partial rows carry the all-ones column, i.e. db.
+  // One merge: the dW partial rows carry the all-ones column, i.e. db; with split du, its
+  // partials in the same launch.
+  if (du && L.pdu.splits > 1)
+    return cuda_rc(cfc::reduce_axis0_pair_launch(partial, L.pdw.splits, M * pitch, pitch, N, dW,
+                                                 db, du_out, L.pdu.splits, BK * n_x, du, s, true),
+                   CFC_ERR_LAUNCH_FAILED);
   return cuda_rc(cfc::reduce_axis0_rows_launch(partial, L.pdw.splits, M * pitch, pitch, N, dW, db,
                                                s, true),
                  CFC_ERR_LAUNCH_FAILED);

@@ -613,6 +613,35 @@ ContractPlan du_contract_plan(int B, int K, int C, int n_x, int form, int smem_b
   return finish_plan(p, form, 4, smem_budget / 2 - 1024);
 }
 
+// Rows (B*K) below which both contractions are split, sized together: a tiny problem is all
+// latency, so more and shorter CTAs help, and one launch merges both sets of partials.
+constexpr int kJointSplitMaxRows = 8192;
+
+void contract_plans(int B, int K, int C, int n_x, int form, int smem_budget, ContractPlan* pw,
+                    ContractPlan* pu) {
+  *pw = dw_contract_plan(B, K, C, n_x, form, smem_budget);
+  *pu = du_contract_plan(B, K, C, n_x, form, smem_budget);
+  if (B * K >= kJointSplitMaxRows) return;
+  // One 128-row accumulator per dW CTA, and the smallest common k-blocks-per-split whose CTAs
+  // fit a fixed budget of one wave (a constant, not the device's SM count: the splits, hence
+  // the summation orders, depend only on the sizes).
+  constexpr int kBudget = 148;
+  ContractPlan w = *pw;
+  w.mt = 1;
+  w.m_tiles = (4 * C + 127) / 128;
+  const int tw = w.m_tiles * w.n_tiles, tu = pu->m_tiles * pu->n_tiles;
+  int kbps = 1;
+  const int kmax = w.n_kb > pu->n_kb ? w.n_kb : pu->n_kb;
+  while (kbps < kmax &&
+         tw * ((w.n_kb + kbps - 1) / kbps) + tu * ((pu->n_kb + kbps - 1) / kbps) > kBudget)
+    ++kbps;
+  for (ContractPlan* p : {&w, pu}) {
+    p->kb_per_split = kbps < p->n_kb ? kbps : p->n_kb;
+    p->splits = (p->n_kb + p->kb_per_split - 1) / p->kb_per_split;
+  }
+  *pw = finish_plan(w, form, 8, smem_budget);
+}
+
 cudaError_t contract_prepare(int max_smem) {
   cudaError_t e = set_attrs_form<kFormBf16x2>(max_smem);
   if (e == cudaSuccess) e = set_attrs_form<kFormBf16>(max_smem);
@@ -744,7 +773,8 @@ cudaError_t du_contract_launch(const ContractPlan& pl, int form, const void* dpr
   CArgs g{};
   g.M = BK; g.N = n_x; g.n_tile = pl.n_tile; g.m_tiles = pl.m_tiles; g.n_tiles = pl.n_tiles;
   g.n_kb = pl.n_kb; g.kb_per_split = pl.kb_per_split; g.stages = pl.stages;
-  g.out = du; g.ldo = n_x; g.n_store = n_x; g.split_stride = 0;
+  g.out = du; g.ldo = n_x; g.n_store = n_x;
+  g.split_stride = static_cast<size_t>(BK) * n_x;  // split partials, when the plan splits
   g.status = status;
   g.defer_wait = defer_wait ? 1 : 0;
   switch (form) {

@@ -1,31 +1,22 @@
-// cfc_gemm_tc.cu -- the two dense contractions of the backward pass on the 5th-generation
-// tensor cores (tcgen05, accumulator in tensor memory):
+// cfc_gemm_tc.cu -- the input projection of the forward pass on the 5th-generation tensor cores
+// (tcgen05, accumulator in tensor memory), for B*K >= 8192 rows:
 //
-//   dW[m][n] = sum_{r < B*K} d_pre[r][m] * z[r][n],   m < 4C, n < n_in,  z[r] = [u[r] ; h_{r-B}]
-//   du[r][k] = sum_{m < 4C}  d_pre[r][m] * W[m][k],   k < n_x
+//   X[r][n] = sum_{k < n_x} u[r][k] * W[n][k] + b[n],   r < B*K, n < 4C
 //
-// (h_{r-B} is h0[r] for the first B rows).  The DQN plan on page "H100 Epoch Optimization
-// Phase 2" (Task 2) replaces per-sample atomic weight-gradient accumulation by one GEMM over
-// the batch, "dW = dY^T X"; here the sum runs over batch and time, B*K rows.
+// X does not depend on h, so it leaves the serial recurrence as one parallel contraction over
+// all steps; the epilogue adds the bias and hands X to the recurrence in place (gate ff1 in H,
+// gates ff2 / ta / tb in the cache).
 //
-// Precision: operands are fp32.  Each is split into bf16 hi = bf16(x) and lo = bf16(x - hi),
-// and the tile product is hi*hi + hi*lo + lo*hi (three tcgen05.mma per 16-row step, fp32
-// accumulation in TMEM), which keeps the per-product relative error near 2^-16 -- well inside
-// the 1e-4 gradient tolerance, where a single bf16 pass (2^-9) is not.
+// Precision: X feeds the forward, whose tolerance is 1e-5 of max|H|.  Operands are fp32; each is
+// split into three bf16 terms x = hi + mid + lo (all 24 significand bits) and the tile product
+// keeps hi*hi + hi*mid + mid*hi + hi*lo + lo*hi + mid*mid (six tcgen05.mma per 16-row step, fp32
+// accumulation in TMEM); the dropped terms are below 2^-24 of the product.
 //
-// One kernel template serves both: a CTA computes a 128 x n_tile output block over a range of
-// the reduction index.  Warps 0-7 load fp32 operand rows (coalesced; two items per thread in
-// flight), split them and write the bf16 halves into 128-byte-swizzled K-major tiles (64
-// reduction entries per stage, two stages); warp 8 owns the TMEM accumulator and one lane
-// issues the MMAs; mbarriers hand the stages back and forth; after the last stage warps 0-7
-// read the accumulator with tcgen05.ld and store it.  When there are fewer output tiles than
-// about one per SM the reduction index is split, each split writing a partial block, and
-// reduce_axis0 sums the splits in order (bitwise reproducible; the split depends only on the
-// sizes).
-//
-// The bias gradient comes out of the same contraction: z gets one more column, all ones, so
-// the weight-gradient partial row m ends with sum_r d_pre[r][m] = db[m] (rows padded to
-// dw_tc_pitch(n_in) columns; the merge routes that column to db).
+// A CTA computes a 128-row x n_tile block: warps 0-7 load fp32 operand rows (coalesced), split
+// them and write the bf16 terms into 128-byte-swizzled K-major tiles (64 reduction entries per
+// stage; n_x <= 512 is at most eight stages); warp 8 owns the TMEM accumulator and one lane
+// issues the MMAs; after the last stage the tile goes through shared memory so each warp writes
+// whole row segments.
 #include <cuda_bf16.h>
 
 #include "cfc_kernels.h"
@@ -63,25 +54,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 a, __nv_bfloat16 b
          (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
-// Split 8 fp32 values (consecutive reduction rows of one tile row) into hi / lo bf16 chunks and
-// store both 16-byte chunks at their swizzled position.
-__device__ __forceinline__ void store_split_chunk(uint8_t* hi_tile, uint8_t* lo_tile, int row,
-                                                  int kchunk, const float (&v)[8]) {
-  __nv_bfloat16 h[8], l[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    h[i] = __float2bfloat16_rn(v[i]);
-    l[i] = __float2bfloat16_rn(v[i] - __bfloat162float(h[i]));
-  }
-  const uint32_t off = sw128_offset(row, kchunk * 8);
-  *reinterpret_cast<uint4*>(hi_tile + off) =
-      make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]),
-                 pack_bf16x2(h[6], h[7]));
-  *reinterpret_cast<uint4*>(lo_tile + off) =
-      make_uint4(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]), pack_bf16x2(l[4], l[5]),
-                 pack_bf16x2(l[6], l[7]));
-}
-
 // Split 8 fp32 values into three bf16 terms x = hi + mid + lo (8 significand bits each, so the
 // three carry all 24 of fp32; each difference is exact in fp32) and store the three chunks.
 __device__ __forceinline__ void store_split3_chunk(uint8_t* hi_tile, uint8_t* mid_tile,
@@ -106,195 +78,6 @@ __device__ __forceinline__ void store_split3_chunk(uint8_t* hi_tile, uint8_t* mi
       make_uint4(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]), pack_bf16x2(l[4], l[5]),
                  pack_bf16x2(l[6], l[7]));
 }
-
-// z[r][n] for n < n_in, 1 at n == n_in (the bias-gradient column), 0 beyond.
-__device__ __forceinline__ float4 z_quad(const TcParams& p, int r, int n) {
-  if (n >= p.n_in) return make_float4(n == p.n_in ? 1.f : 0.f, 0.f, 0.f, 0.f);
-  if (n < p.n_x) return __ldg(reinterpret_cast<const float4*>(p.u + static_cast<size_t>(r) * p.n_x + n));
-  const int j = n - p.n_x;
-  const float* src = (r >= p.B) ? p.H + static_cast<size_t>(r - p.B) * p.C + j
-                                : p.h0 + static_cast<size_t>(r) * p.C + j;
-  return __ldg(reinterpret_cast<const float4*>(src));
-}
-
-__device__ __forceinline__ float z_at(const TcParams& p, int r, int n) {
-  if (n >= p.n_in) return n == p.n_in ? 1.f : 0.f;
-  if (n < p.n_x) return __ldg(p.u + static_cast<size_t>(r) * p.n_x + n);
-  const int j = n - p.n_x;
-  return (r >= p.B) ? __ldg(p.H + static_cast<size_t>(r - p.B) * p.C + j)
-                    : __ldg(p.h0 + static_cast<size_t>(r) * p.C + j);
-}
-
-// Weight gradient: A = d_pre^T (rows m, reduction r), B = z^T (rows n, reduction r).
-// Item = (4 consecutive tile rows, 8 consecutive reduction rows); the 8 threads of a
-// quarter-warp take the 8 chunks of one row quad, so their 16-byte stores hit distinct banks.
-// Load 8 consecutive reduction entries of 4 consecutive rows (a "row quad") of d_pre^T:
-// d_pre[r0 + 8c + i][m .. m+3], i < 8.
-__device__ __forceinline__ void load_dpre_quad(const TcParams& p, int m, int r0c, float (&v)[4][8]) {
-  const int M = 4 * p.C;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = r0c + i;
-    float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r < p.BK && m < M)
-      q = __ldg(reinterpret_cast<const float4*>(p.d_pre + static_cast<size_t>(r) * M + m));
-    v[0][i] = q.x; v[1][i] = q.y; v[2][i] = q.z; v[3][i] = q.w;
-  }
-}
-
-// The same for z^T: z[r0 + 8c + i][n .. n+3].
-__device__ __forceinline__ void load_z_quad(const TcParams& p, int n, int r0c, float (&v)[4][8]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = r0c + i;
-    float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r < p.BK) {
-      if (p.vec) {
-        q = z_quad(p, r, n);
-      } else {
-        q.x = z_at(p, r, n);
-        q.y = z_at(p, r, n + 1);
-        q.z = z_at(p, r, n + 2);
-        q.w = z_at(p, r, n + 3);
-      }
-    }
-    v[0][i] = q.x; v[1][i] = q.y; v[2][i] = q.z; v[3][i] = q.w;
-  }
-}
-
-// The same for W_u^T: W[m0 + 8c + i][n .. n+3] (columns >= n_x read as 0).
-__device__ __forceinline__ void load_wu_quad(const TcParams& p, int n, int m0c, float (&v)[4][8]) {
-  const int M = 4 * p.C;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int m = m0c + i;
-    float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (m < M) {
-      const float* src = p.W + static_cast<size_t>(m) * p.n_in + n;
-      if (p.vec && n < p.n_x) {
-        q = __ldg(reinterpret_cast<const float4*>(src));
-      } else {
-        q.x = (n < p.n_x) ? __ldg(src) : 0.f;
-        q.y = (n + 1 < p.n_x) ? __ldg(src + 1) : 0.f;
-        q.z = (n + 2 < p.n_x) ? __ldg(src + 2) : 0.f;
-        q.w = (n + 3 < p.n_x) ? __ldg(src + 3) : 0.f;
-      }
-    }
-    v[0][i] = q.x; v[1][i] = q.y; v[2][i] = q.z; v[3][i] = q.w;
-  }
-}
-
-// Row-quad items (4 tile rows x 8 reduction entries), two per thread at a time with all loads
-// issued before the stores.  The 8 threads of a quarter-warp take the 8 chunks of one quad, so
-// their 16-byte stores hit distinct banks.
-template <class Load>
-__device__ __forceinline__ void convert_quads(int n_quads, int row_base, int k_base, int tid,
-                                              uint8_t* hi, uint8_t* lo, Load load) {
-  const int n_items = n_quads * 8;
-  for (int it = tid; it < n_items; it += 2 * kConv) {
-    const int it1 = it + kConv;
-    float v0[4][8], v1[4][8];
-    load(row_base + 4 * (it >> 3), k_base + 8 * (it & 7), v0);
-    if (it1 < n_items) load(row_base + 4 * (it1 >> 3), k_base + 8 * (it1 & 7), v1);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) store_split_chunk(hi, lo, 4 * (it >> 3) + j, it & 7, v0[j]);
-    if (it1 < n_items) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) store_split_chunk(hi, lo, 4 * (it1 >> 3) + j, it1 & 7, v1[j]);
-    }
-  }
-}
-
-// Output columns n .. n+15 of row m (v[0..15]) into the row-major block p.out of split `split`.
-struct RowMajorOut {
-  // Staged epilogue (whole row segments per warp store) when rows hold float4s.
-  static constexpr bool kStagedOut = true;
-  static __device__ __forceinline__ bool staged(const TcParams& p) { return (p.cols % 4) == 0; }
-  static __device__ __forceinline__ void store4(const TcParams& p, int split, int m, int n,
-                                                float4 x) {
-    if (n >= p.cols) return;  // cols is a multiple of 4: each quad is wholly in or out
-    *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(split) * p.rows + m) * p.cols + n) = x;
-  }
-  static __device__ __forceinline__ void store16(const TcParams& p, int split, int m, int n,
-                                                 const float (&v)[16]) {
-    float* dst = p.out + (static_cast<size_t>(split) * p.rows + m) * p.cols;
-    const bool vec_out = (p.cols % 4) == 0;
-#pragma unroll
-    for (int c = 0; c < 16; c += 4) {
-      const int nc = n + c;
-      if (vec_out && nc + 3 < p.cols) {
-        *reinterpret_cast<float4*>(dst + nc) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (nc + e < p.cols) dst[nc + e] = v[c + e];
-      }
-    }
-  }
-};
-
-// Weight gradient: A = d_pre^T (rows m, reduction r), B = z^T (rows n, reduction r).  With
-// MT = 2 a CTA keeps two 128-row accumulators that share every converted z tile.
-template <int MT>
-struct DwProblem : RowMajorOut {
-  static constexpr int kTerms = 2, kStages = 2, kMT = MT;
-  static __device__ __forceinline__ void convert(const TcParams& p, uint8_t* a_hi, uint8_t* a_lo,
-                                                 uint8_t* b_hi, uint8_t* b_lo, int m0, int n0,
-                                                 int r0, int tid) {
-    convert_quads(kTcM * MT / 4, m0, r0, tid, a_hi, a_lo,
-                  [&](int m, int rc, float (&v)[4][8]) { load_dpre_quad(p, m, rc, v); });
-    convert_quads(p.n_tile / 4, n0, r0, tid, b_hi, b_lo,
-                  [&](int n, int rc, float (&v)[4][8]) { load_z_quad(p, n, rc, v); });
-  }
-};
-
-// Input gradient: A = d_pre (rows r, reduction m: already K-major), B = W_u^T (rows k,
-// reduction m).  A items are (row, 8-entry chunk), two per thread at a time, loads first; a
-// quarter-warp covers the 8 chunks of a row.
-struct DuProblem : RowMajorOut {
-  static constexpr int kTerms = 2, kStages = 2, kMT = 1;
-  static __device__ __forceinline__ void load_row_chunk(const TcParams& p, int r, int m,
-                                                        float (&v)[8]) {
-    const int M = 4 * p.C;
-    float4 q0 = make_float4(0.f, 0.f, 0.f, 0.f), q1 = q0;
-    if (r < p.BK && m < M) {  // M is a multiple of 4: each quad is wholly in or out
-      const float* src = p.d_pre + static_cast<size_t>(r) * M + m;
-      q0 = __ldg(reinterpret_cast<const float4*>(src));
-      if (m + 4 < M) q1 = __ldg(reinterpret_cast<const float4*>(src + 4));
-    }
-    v[0] = q0.x; v[1] = q0.y; v[2] = q0.z; v[3] = q0.w;
-    v[4] = q1.x; v[5] = q1.y; v[6] = q1.z; v[7] = q1.w;
-  }
-  // All four A items of a thread and its first B quad are loaded before the first store, so
-  // a stage costs one memory round trip (n_tile <= 128; wider tiles take a second for B).
-  static __device__ __forceinline__ void convert(const TcParams& p, uint8_t* a_hi, uint8_t* a_lo,
-                                                 uint8_t* b_hi, uint8_t* b_lo, int r0, int n0,
-                                                 int m0, int tid) {
-    static_assert(kTcM * 8 == 4 * kConv, "four A items per thread");
-    const int nB = p.n_tile / 4 * 8;
-    float va[4][8], vb[4][8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int it = tid + j * kConv;
-      load_row_chunk(p, r0 + (it >> 3), m0 + 8 * (it & 7), va[j]);
-    }
-    if (tid < nB) load_wu_quad(p, n0 + 4 * (tid >> 3), m0 + 8 * (tid & 7), vb);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int it = tid + j * kConv;
-      store_split_chunk(a_hi, a_lo, it >> 3, it & 7, va[j]);
-    }
-    if (tid < nB) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) store_split_chunk(b_hi, b_lo, 4 * (tid >> 3) + q, tid & 7, vb[q]);
-    }
-    for (int it = tid + kConv; it < nB; it += kConv) {
-      load_wu_quad(p, n0 + 4 * (it >> 3), m0 + 8 * (it & 7), vb);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) store_split_chunk(b_hi, b_lo, 4 * (it >> 3) + q, it & 7, vb[q]);
-    }
-  }
-};
 
 // Input projection: A = u (rows r, reduction k < n_x: K-major as stored), B = W_u (rows n < 4C,
 // the first n_x columns of W: K-major as stored).  The epilogue adds the bias and hands X to
@@ -561,20 +344,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcParams p
   tc_gemm_body<Problem>(p, blockIdx.x, blockIdx.y);
 }
 
-// Both contractions in one grid: the first n_w CTAs take the weight-gradient tiles and splits,
-// the rest the input-gradient tiles and splits.  They read the same d_pre and write disjoint
-// outputs, so one launch replaces two dependent ones.
-template <int MT>
-__global__ void __launch_bounds__(kTcThreads, 1) tc_dual_kernel(const TcParams pw,
-                                                                const TcParams pu, int n_w) {
-  const int b = blockIdx.x;
-  const int tiles_w = pw.m_tiles * ((pw.cols + pw.n_tile - 1) / pw.n_tile);
-  const int tiles_u = pu.m_tiles * ((pu.cols + pu.n_tile - 1) / pu.n_tile);
-  if (b < n_w) tc_gemm_body<DwProblem<MT>>(pw, b % tiles_w, b / tiles_w);
-  else tc_gemm_body<DuProblem>(pu, (b - n_w) % tiles_u, (b - n_w) / tiles_u);
-}
-
-
 TcPlan tc_plan(int rows, int cols, int red, bool split, int terms = 2, int stages = 2,
                int mt = 1, int max_n_tile = 256) {
   TcPlan pl;
@@ -599,47 +368,7 @@ TcPlan tc_plan(int rows, int cols, int red, bool split, int terms = 2, int stage
 
 }  // namespace
 
-TcPlan dw_tc_plan(int B, int K, int C, int n_x) {
-  // For long reductions each CTA keeps two 128-row accumulators that share every converted
-  // z tile, so z is read once per 256 rows of dW instead of once per 128.  Two stages of
-  // 2 x (256 + n_tile) rows of 128 bytes fit in shared memory up to n_tile = 192.
-  const TcPlan one = tc_plan(4 * C, dw_tc_pitch(n_x + C), B * K, true);
-  if (4 * C >= 2 * kTcM && B * K >= 8192 && one.n_tile <= 192)
-    return tc_plan(4 * C, dw_tc_pitch(n_x + C), B * K, true, 2, 2, 2);
-  return one;
-}
-TcPlan du_tc_plan_unsplit(int B, int K, int C, int n_x) {
-  return tc_plan(B * K, n_x, 4 * C, false);
-}
-
-void dwdu_tc_plans(int B, int K, int C, int n_x, TcPlan* pw, TcPlan* pu) {
-  // One k-block count per CTA for both, the smallest whose CTAs fit a fixed budget of one
-  // wave (a constant, not the device's SM count, so the split -- hence the summation order --
-  // depends only on the sizes).
-  constexpr int kBudget = 148;
-  *pw = tc_plan(4 * C, dw_tc_pitch(n_x + C), B * K, false);
-  *pu = tc_plan(B * K, n_x, 4 * C, false);
-  const int tw = pw->m_tiles * pw->n_tiles, tu = pu->m_tiles * pu->n_tiles;
-  int kbps = 1;
-  const int kmax = pw->n_kb > pu->n_kb ? pw->n_kb : pu->n_kb;
-  while (kbps < kmax && tw * ((pw->n_kb + kbps - 1) / kbps) + tu * ((pu->n_kb + kbps - 1) / kbps) > kBudget)
-    ++kbps;
-  for (TcPlan* pl : {pw, pu}) {
-    pl->kb_per_split = kbps < pl->n_kb ? kbps : pl->n_kb;
-    pl->splits = (pl->n_kb + pl->kb_per_split - 1) / pl->kb_per_split;
-  }
-}
-
 cudaError_t tc_prepare(int max_smem) {
-  const void* kernels[] = {reinterpret_cast<const void*>(tc_gemm_kernel<DwProblem<1>>),
-                           reinterpret_cast<const void*>(tc_gemm_kernel<DwProblem<2>>),
-                           reinterpret_cast<const void*>(tc_dual_kernel<1>),
-                           reinterpret_cast<const void*>(tc_dual_kernel<2>)};
-  for (const void* k : kernels) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-    if (e != cudaSuccess) return e;
-  }
   return cudaFuncSetAttribute(tc_gemm_kernel<ProjProblem>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
 }
@@ -656,22 +385,6 @@ TcParams make_params(const TcPlan& pl, const float* d_pre, int B, int K, int C, 
   return p;
 }
 }  // namespace
-
-cudaError_t dw_tc_launch(const TcPlan& pl, const float* d_pre, const float* u, const float* H,
-                         const float* h0, int B, int K, int C, int n_x, float* partial,
-                         int* status, cudaStream_t s, bool pdl) {
-  TcParams p = make_params(pl, d_pre, B, K, C, n_x, status);
-  p.u = u; p.H = H; p.h0 = h0; p.out = partial;
-  p.rows = 4 * C; p.cols = dw_tc_pitch(n_x + C); p.red = B * K;
-  LaunchCfg c;
-  c.grid = dim3(pl.m_tiles * pl.n_tiles, pl.splits, 1);
-  c.block = dim3(kTcThreads, 1, 1);
-  c.smem = pl.smem;
-  c.stream = s;
-  c.pdl = pdl;
-  return pl.mt == 2 ? launch(c, tc_gemm_kernel<DwProblem<2>>, p)
-                    : launch(c, tc_gemm_kernel<DwProblem<1>>, p);
-}
 
 TcPlan proj_tc_plan(int B, int K, int C, int n_x) {
   // Column tiles of at most 128: a 98 KB stage, so two CTAs share an SM and one's loads and
@@ -692,27 +405,6 @@ cudaError_t proj_tc_launch(const TcPlan& pl, const float* u, const float* W, con
   c.stream = s;
   c.pdl = pdl;
   return launch(c, tc_gemm_kernel<ProjProblem>, p);
-}
-
-cudaError_t dwdu_tc_launch(const TcPlan& pw, const TcPlan& pu, const float* d_pre,
-                           const float* u, const float* H, const float* h0, const float* W, int B,
-                           int K, int C, int n_x, float* partial, float* du, int* status,
-                           cudaStream_t s, bool pdl) {
-  TcParams a = make_params(pw, d_pre, B, K, C, n_x, status);
-  a.u = u; a.H = H; a.h0 = h0; a.out = partial;
-  a.rows = 4 * C; a.cols = dw_tc_pitch(n_x + C); a.red = B * K;
-  TcParams b = make_params(pu, d_pre, B, K, C, n_x, status);
-  b.W = W; b.out = du;
-  b.rows = B * K; b.cols = n_x; b.red = 4 * C;
-  const int n_w = pw.m_tiles * pw.n_tiles * pw.splits;
-  LaunchCfg c;
-  c.grid = dim3(n_w + pu.m_tiles * pu.n_tiles * pu.splits, 1, 1);
-  c.block = dim3(kTcThreads, 1, 1);
-  c.smem = pw.smem > pu.smem ? pw.smem : pu.smem;
-  c.stream = s;
-  c.pdl = pdl;
-  return pw.mt == 2 ? launch(c, tc_dual_kernel<2>, a, b, n_w)
-                    : launch(c, tc_dual_kernel<1>, a, b, n_w);
 }
 
 }  // namespace cfc

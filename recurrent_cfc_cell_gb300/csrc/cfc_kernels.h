@@ -89,30 +89,17 @@ cudaError_t dw_simt_launch(const float* d_pre, const float* u, const float* H, c
                            int B, int K, int C, int n_x, int S, float* partial, cudaStream_t s,
                            bool pdl);
 
-// dW and du on tcgen05 tensor cores (bf16 hi/lo split, fp32 accumulation in TMEM).
+// The input projection X = W_u u + b on the tensor cores (three bf16 terms per operand, six
+// products), written in place into H and cache like inproj_launch.
 struct TcPlan {
   int n_tiles, n_tile, m_tiles, n_kb, kb_per_split, splits;
-  int mt;  // 128-row accumulators per CTA (1, or 2 for the weight gradient at large B*K)
+  int mt;  // 128-row accumulators per CTA
   size_t smem;
 };
-TcPlan dw_tc_plan(int B, int K, int C, int n_x);  // split over the B*K rows
 cudaError_t tc_prepare(int max_smem);
-cudaError_t dw_tc_launch(const TcPlan& pl, const float* d_pre, const float* u, const float* H,
-                         const float* h0, int B, int K, int C, int n_x, float* partial,
-                         int* status, cudaStream_t s, bool pdl);
-// The input projection X = W_u u + b on the tensor cores (bf16 hi/lo split), written in place
-// into H and cache like inproj_launch.
 TcPlan proj_tc_plan(int B, int K, int C, int n_x);
 cudaError_t proj_tc_launch(const TcPlan& pl, const float* u, const float* W, const float* bias,
                            int B, int K, int C, int n_x, float* H, float* cache, int* status,
-                           cudaStream_t s, bool pdl);
-// Both in one launch: the dW partials of plan pw and du (or, when pu.splits > 1, its partial
-// blocks [splits][B*K][n_x]).  dwdu_tc_plans splits both so their CTAs fill one wave.
-TcPlan du_tc_plan_unsplit(int B, int K, int C, int n_x);
-void dwdu_tc_plans(int B, int K, int C, int n_x, TcPlan* pw, TcPlan* pu);
-cudaError_t dwdu_tc_launch(const TcPlan& pw, const TcPlan& pu, const float* d_pre,
-                           const float* u, const float* H, const float* h0, const float* W, int B,
-                           int K, int C, int n_x, float* partial, float* du, int* status,
                            cudaStream_t s, bool pdl);
 
 // ---- TMA-fed contractions (cfc_contract.cu) ----
@@ -140,6 +127,10 @@ struct ContractPlan {
 };
 ContractPlan dw_contract_plan(int B, int K, int C, int n_x, int form, int smem_budget);
 ContractPlan du_contract_plan(int B, int K, int C, int n_x, int form, int smem_budget);
+// Both plans as the backward pass uses them: for small B*K both are split, sized together so
+// their CTAs fill one wave (du then writes split partials [splits][B*K][n_x]).
+void contract_plans(int B, int K, int C, int n_x, int form, int smem_budget, ContractPlan* pw,
+                    ContractPlan* pu);
 cudaError_t contract_prepare(int max_smem);
 // z rows [u ; h_{t-1} ; 1] (B*K of them) and W_u^T rows (n_x) in the operand form.
 cudaError_t build_operands_launch(int form, const float* u, const float* H, const float* h0,
@@ -152,7 +143,8 @@ cudaError_t split_dpre_launch(int form, const float* d_pre, int BK, int C, void*
 cudaError_t dw_contract_launch(const ContractPlan& pl, int form, const void* dpre, const void* z,
                                int B, int K, int C, int n_x, float* partial, int ldo,
                                int* status, cudaStream_t s, bool pdl);
-// du [B*K][n_x] from the d_pre operand and W_u^T.  `defer_wait`: launched right after the
+// du [B*K][n_x] (or, when the plan splits, partials [splits][B*K][n_x]) from the d_pre operand
+// and W_u^T.  `defer_wait`: launched right after the
 // weight-gradient contraction of the same call, whose operands it shares; it then runs beside
 // that kernel and waits for it only at its end.
 cudaError_t du_contract_launch(const ContractPlan& pl, int form, const void* dpre, const void* wt,
