@@ -121,10 +121,12 @@ int max_clusters(DeviceState& st, int kind, int variant, int CS, size_t smem, in
   }
   int n = 0;
   // kind 0: forward (CUDA cores), 1: backward, 3 / 4: forward / backward with the tensor-core
-  // contraction (4: `variant` is C, the count is of CTAs per SM)
+  // contraction (4: `variant` is C, the count is of CTAs per SM), 5: backward with the
+  // cluster-split tensor-core contraction (`variant` is C)
   const cudaError_t e = (kind == 1)   ? cfc::bwd_prepare(CS, variant, smem, &n)
                        : (kind == 3) ? cfc::fwd_tc_prepare(CS * cfc::kFwdChanPerCta, &n)
                        : (kind == 4) ? cfc::bwd_tc_prepare(variant, &n)
+                       : (kind == 5) ? cfc::bwd_ks_prepare(variant, &n)
                                      : cfc::fwd_prepare(CS, variant, smem, &n);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
@@ -362,15 +364,23 @@ int backward_recurrence(const float* dH, const float* W, const float* ts, const 
   // The tensor-core BPTT moves dH, the cache and d_pre in whole 32-byte sectors.
   if (wsplit && B >= tc_bwd_min_rows(C) && cfc::bwd_tc_supported(C) && aligned32(dH) &&
       aligned32(cache) && aligned32(d_pre)) {
-    int n = 0;
-    rc = max_clusters(*st, 4, C, 1, 0, &n);
+    // The cluster-split recurrence (C / 32 CTAs per 128 rows) when all its clusters fit in one
+    // wave, else the single-CTA one.  Measured on GB300 at C = 256, K = 32: 26 us per step for
+    // 8 or 12 clusters, 50.5 us for 16 (at most 15 clusters of 8 are resident, so 16 run in two
+    // waves), against 43 us for the single-CTA recurrence.
+    int n_ks = 0, n = 0;
+    rc = max_clusters(*st, 5, C, C / 32, 0, &n_ks);
     if (rc != CFC_OK) return rc;
-    if (n > 0) {
+    if (n_ks < (B + 127) / 128) n_ks = 0;
+    if (n_ks <= 0) rc = max_clusters(*st, 4, C, 1, 0, &n);
+    if (rc != CFC_OK) return rc;
+    if (n_ks > 0 || n > 0) {
       const cudaStream_t s = static_cast<cudaStream_t>(stream);
       rc = cuda_rc(cfc::bwd_tc_split(W, C, n_x, wsplit, s, pdl), CFC_ERR_LAUNCH_FAILED);
       if (rc != CFC_OK) return rc;
       p.R = 0;
-      return cuda_rc(cfc::bwd_tc_launch(p, s, true), CFC_ERR_LAUNCH_FAILED);
+      return cuda_rc(n_ks > 0 ? cfc::bwd_ks_launch(p, s, true) : cfc::bwd_tc_launch(p, s, true),
+                     CFC_ERR_LAUNCH_FAILED);
     }
   }
   size_t smem = 0;

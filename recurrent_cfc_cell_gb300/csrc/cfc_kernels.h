@@ -74,6 +74,12 @@ cudaError_t bwd_tc_split(const float* W, int C, int n_x, void* wsplit, cudaStrea
 cudaError_t bwd_tc_prepare(int C, int* max_active_ctas);
 cudaError_t bwd_tc_launch(const BwdParams& p, cudaStream_t s, bool pdl);
 
+// The BPTT recurrence with each step's contraction split along its reduction over a cluster of
+// C / 32 CTAs per 128 batch rows (C = 128 or 256); reads the same pre-split W_h^T as
+// bwd_tc_launch and writes fp32 d_pre.
+cudaError_t bwd_ks_prepare(int C, int* max_active_clusters);
+cudaError_t bwd_ks_launch(const BwdParams& p, cudaStream_t s, bool pdl);
+
 size_t bwd_smem_bytes(int R, int CS);
 cudaError_t bwd_prepare(int CS, int R, size_t smem, int* max_active_clusters);
 cudaError_t bwd_launch(const BwdParams& p, int n_clusters, size_t smem, cudaStream_t s,

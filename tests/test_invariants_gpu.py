@@ -25,9 +25,16 @@ def _step(w):
     return st, inp, torch
 
 
-@pytest.mark.parametrize("idx", [1, 3])  # dW/du split together + paired merge; dual launch
-def test_bitwise_deterministic_runs(idx):
-    st, _, torch = _step(inputs.CONFIGS[idx])
+DETERMINISM_CASES = [
+    inputs.CONFIGS[1],                                  # contractions split together, paired merge
+    inputs.CONFIGS[3],                                  # dW split over 128 CTAs, du unsplit
+    inputs.custom(B=1030, K=6, n_x=16, C=256, seed=8),  # cluster-split tensor-core BPTT
+]
+
+
+@pytest.mark.parametrize("w", DETERMINISM_CASES, ids=lambda w: w.name)
+def test_bitwise_deterministic_runs(w):
+    st, _, torch = _step(w)
     st.run()
     torch.cuda.synchronize()
     first = {k: v.clone() for k, v in st.outputs().items()}
