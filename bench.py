@@ -51,8 +51,12 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-largest", action="store_true",
                     help="skip the record of the largest (2048 x 128 x 256) workload")
-    ap.add_argument("--dw-modes", default="0,1",
+    ap.add_argument("--dw-modes", default="0,1,2",
                     help="tensor-core weight-gradient modes timed on the largest workload")
+    ap.add_argument("--profile", action="store_true",
+                    help="only run --steps eager training steps of the workload (for ncu "
+                         "captures: the step's kernels and nothing else), print nothing")
+    ap.add_argument("--dw-mode", type=int, default=0, help="weight-gradient mode (--profile)")
     return ap.parse_args()
 
 
@@ -260,7 +264,10 @@ def cpu_baseline(w, seconds: float) -> dict:
     import concurrent.futures
     import multiprocessing
 
-    units1, dt1 = _oracle_shard(w, 0, w.B, seconds)
+    # The single-thread leg on at most 128 rows: one oracle step of the whole largest workload
+    # (2048 rows x 128 steps) would take minutes; rows are independent, so the rate per row-step
+    # is the same.
+    units1, dt1 = _oracle_shard(w, 0, min(w.B, 128), seconds)
     single = units1 / dt1
     cores = min(os.cpu_count() or 1, w.B)
     bounds = [(w.B * i // cores, w.B * (i + 1) // cores) for i in range(cores)]
@@ -273,7 +280,8 @@ def cpu_baseline(w, seconds: float) -> dict:
             "single_thread_value": single,
             "sample": f"the workload (B={w.B}, K={w.K}) split by batch rows over {cores} "
                       f"processes, each running fp64 C oracle steps on its rows for "
-                      f"{seconds:.0f} s; single thread on all rows: {single:.0f} {UNIT}"}
+                      f"{seconds:.0f} s; single thread on {min(w.B, 128)} rows: "
+                      f"{single:.0f} {UNIT}"}
 
 
 # ---------------------------------------------------------------- parity (oracle leg)
@@ -518,6 +526,12 @@ def main():
     w = workload(args)
     inp = inputs.make_inputs(w)
     dinp = to_device(inp, dev)
+    if args.profile:
+        st = KLoopStep(w.B, w.K, w.C, w.n_x, dw_mode=args.dw_mode, device=dev).bind(**dinp)
+        for _ in range(args.steps):
+            st.run()
+        torch.cuda.synchronize()
+        return 0 if _lib.device_status() == 0 else 1
     st = KLoopStep(w.B, w.K, w.C, w.n_x, device=dev).bind(**dinp)
     st.capture()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
