@@ -289,10 +289,11 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_ks_kernel(const BwdParams
     const int ch0 = kChan * rank + 16 * h;  // this thread's 16 channels
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
     const uint32_t recv_s = smem_addr(recv);
-    // This thread's row of sender block `slot` in any CTA's receive buffer: 16-byte chunk v of
-    // the row at position v ^ (r % 8), so the reads of a warp (32 rows) hit distinct banks.
+    // 16-byte chunk v (channels 4 v .. 4 v + 3) of this thread's row in sender block `slot` of
+    // any CTA's receive buffer.  Chunk-major ([slot][v][row]): the 32 lanes of a warp (32
+    // consecutive rows) store one contiguous 512-byte run per st.async and read one per load.
     auto recv_addr = [&](int slot, int v) {
-      return recv_s + static_cast<uint32_t>(((slot * kRows + r) * kChan + 4 * (v ^ (r & 7))) * 4);
+      return recv_s + static_cast<uint32_t>(((slot * (kChan / 4) + v) * kRows + r) * 16);
     };
     float in[4][16];  // dH, ff1, ff2, gate of this row's 16 channels at step t
     auto load_inputs = [&](int t) {
@@ -310,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_ks_kernel(const BwdParams
           for (int c = 0; c < 16; ++c) in[e][c] = 0.f;
       }
     };
-    load_inputs(K - 1);
+    load_inputs(K - 1);  // step K-1 has no exchange before it
     bool ok = true;
     for (int n = 0; n <= K && ok; ++n) {
       const int t = K - 1 - n;
@@ -337,6 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_ks_kernel(const BwdParams
                         v[4 * c4 + 2], v[4 * c4 + 3], rbar);
         }
         tc_fence_before_sync();  // the drain precedes the next step's MMAs (via a_ready)
+        // This step's inputs: in flight while the other CTAs' blocks arrive (the last exchange,
+        // n = K, only gives dh0 and reads no step's inputs).
+        if (t >= 0) load_inputs(t);
         ok = mbar_wait_bounded_cluster(recv_full, (n - 1) & 1, p.status);
         if (bar_or(kEpiBar, kEpiWarps * 32, !ok)) {
           ok = false;
@@ -410,7 +414,6 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_ks_kernel(const BwdParams
         tc_fence_before_sync();
         mbar_arrive(a_ready);
       }
-      if (t > 0) load_inputs(t - 1);  // in flight through the next MMA and exchange
     }
   }
 

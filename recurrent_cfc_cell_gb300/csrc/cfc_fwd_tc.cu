@@ -38,21 +38,26 @@
 namespace cfc {
 namespace {
 
-constexpr int kTM = 128;                         // batch rows per cluster (MMA N)
 constexpr int kGC = 4 * kFwdChanPerCta;          // gate rows per CTA (MMA M)
 constexpr int kEpiWarps = 8;                     // epilogue warps (two per TMEM lane quarter)
 constexpr int kTcThreads = (kEpiWarps + 1) * 32; // + one control warp
-constexpr int kSlabBytes = kTM * kFwdChanPerCta * 2;  // one CTA's k range of one h term
 constexpr int kStepBar = 1;                      // named barrier id of the per-step hand-off
 constexpr int kTerms = 2;                        // fp16 terms per operand
+constexpr uint32_t kACol0 = 256;                 // W_h^T terms start here; D^T takes NR columns
 
-template <int CS>
+// NR: batch rows per cluster (MMA N), 128 or 144.  144 lets 15 clusters cover 2048 rows:
+// GB300 keeps at most 15 clusters of 8 CTAs resident, so 16 clusters of 128 rows ran in two
+// waves.
+template <int CS, int NR>
 struct TcShape {
   static constexpr int C = kFwdChanPerCta * CS;
-  static constexpr int TERM = C * kTM * 2;       // bytes of one fp16 term of h
+  static constexpr int TERM = C * NR * 2;        // bytes of one fp16 term of h
+  static constexpr int SLAB = NR * kFwdChanPerCta * 2;  // one CTA's k range of one h term
+  static constexpr int HR = NR / 2;              // rows of one epilogue warp half
   static constexpr int ACOLS = C / 2;            // TMEM columns of one term of W_h^T
+  static_assert(NR % 16 == 0 && HR % 8 == 0 && NR <= 256, "row tile");
   // h terms, ts of two steps, barriers (full[CS], mma done, all done), TMEM slot, alignment.
-  static constexpr int USED = kTerms * TERM + 2 * kTM * 4 + (CS + 2) * 8 + 16 + 128;
+  static constexpr int USED = kTerms * TERM + 2 * NR * 4 + (CS + 2) * 8 + 16 + 128;
   // At least half an SM's shared memory: a CTA takes all 512 tensor-memory columns, so two
   // CTAs on one SM would leave the second waiting in tcgen05.alloc while its cluster waits on
   // it.
@@ -78,10 +83,24 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16in(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Byte offset of element (row n, k) in one h term: [k / 8][n / 8][n % 8][k % 8].
+// Byte offset of element (row n, k) in one h term of NR rows: [k / 8][n / 8][n % 8][k % 8].
+template <int NR>
 __device__ __forceinline__ uint32_t hterm_offset(int n, int k) {
-  return static_cast<uint32_t>(((k >> 3) * (kTM / 8) + (n >> 3)) * 128 + (n & 7) * 16 +
+  return static_cast<uint32_t>(((k >> 3) * (NR / 8) + (n >> 3)) * 128 + (n & 7) * 16 +
                                (k & 7) * 2);
+}
+
+// Tensor-memory load of 8 consecutive fp32 columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Shared-memory operand descriptor, no swizzle, K-major: `lbo` bytes between core matrices
@@ -150,22 +169,23 @@ __device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
   return r != 0;
 }
 
-template <int CS>
+template <int CS, int NR>
 __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdParams p) {
-  using S = TcShape<CS>;
+  using S = TcShape<CS, NR>;
+  constexpr int HR = S::HR;
   constexpr int C = S::C;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t* sm = smem_raw + ((128u - (raw & 127u)) & 127u);
   uint8_t* hb = sm;                                                     // [2][TERM]
-  float* ts_s = reinterpret_cast<float*>(sm + kTerms * S::TERM);        // [2][kTM]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ts_s + 2 * kTM);         // full[CS], done, all
+  float* ts_s = reinterpret_cast<float*>(sm + kTerms * S::TERM);        // [2][NR]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ts_s + 2 * NR);          // full[CS], done, all
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + CS + 2);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int rank = static_cast<int>(cluster_rank());
-  const int row0 = static_cast<int>(cluster_id_x()) * kTM;
+  const int row0 = static_cast<int>(cluster_id_x()) * NR;
   const int B = p.B, K = p.K, n_x = p.n_x, n_in = p.n_in;
   const uint32_t full0 = smem_addr(&bars[0]);       // full[j]: slab j of h_{t-1} is in place
   const uint32_t done_bar = smem_addr(&bars[CS]);   // this CTA's MMAs of the step are done
@@ -188,7 +208,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
   tc_fence_after_sync();
   const uint32_t tmem = *tslot;
 
-  // This thread's role in the epilogue warps: TMEM lane quarter q, rows 64 hh .. 64 hh + 63,
+  // This thread's role in the epilogue warps: TMEM lane quarter q, rows HR hh .. HR hh + HR - 1,
   // gate g of local channel c (lane 4c + g of the quarter's 32 lanes).
   const int q = warp & 3, hh = (warp >> 2) & 1;
   const int c = (32 * q + lane) >> 2, g = lane & 3;
@@ -214,23 +234,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
         r0[cc] = pack2(a.t[0], b.t[0]);
         r1[cc] = pack2(a.t[1], b.t[1]);
       }
-      const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + 128 + k0 / 2;
+      const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + kACol0 + k0 / 2;
       tmem_st32(ta, r0);
       tmem_st32(ta + S::ACOLS, r1);
     }
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     // ---- h0 -> this CTA's slab of the h buffer (lanes g = 1, 2 write term g - 1). ----
     if (g == 1 || g == 2) {
-      for (int i = 0; i < 64; ++i) {
-        const int r = 64 * hh + i, b = row0 + r;
+      for (int i = 0; i < HR; ++i) {
+        const int r = HR * hh + i, b = row0 + r;
         const float h = (b < B) ? __ldg(p.h0 + static_cast<size_t>(b) * C + ch) : 0.f;
-        *reinterpret_cast<__half*>(hb + (g - 1) * S::TERM + hterm_offset(r, ch)) =
+        *reinterpret_cast<__half*>(hb + (g - 1) * S::TERM + hterm_offset<NR>(r, ch)) =
             split2(h).t[g - 1];
       }
     }
   } else {
     // ts of step 0 (the control warp loads each step's ts one step ahead).
-    for (int i = lane; i < kTM; i += 32) ts_s[i] = (row0 + i < B) ? __ldg(p.ts + row0 + i) : 0.f;
+    for (int i = lane; i < NR; i += 32) ts_s[i] = (row0 + i < B) ? __ldg(p.ts + row0 + i) : 0.f;
   }
   fence_proxy_async_smem();
   tc_fence_before_sync();
@@ -240,9 +260,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
 
   if (warp == kEpiWarps) {
     // ================= control warp: MMAs, completion signals, the exchange =================
-    const uint32_t idesc = umma_idesc_f16in(kGC, kTM);
+    const uint32_t idesc = umma_idesc_f16in(kGC, NR);
     const uint32_t hb0 = smem_addr(hb);
-    const uint64_t bdesc0 = desc_kmajor(hb0, (kTM / 8) * 128, 128);
+    const uint64_t bdesc0 = desc_kmajor(hb0, (NR / 8) * 128, 128);
     // This CTA's slab (three terms) to every other CTA, lane d copying to CTA rank + d; lane 0
     // marks its own slab in place.
     auto push = [&]() {
@@ -251,8 +271,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
       } else if (lane < CS) {
         const uint32_t dst = static_cast<uint32_t>((rank + lane) % CS);
         for (int tm = 0; tm < kTerms; ++tm) {
-          const uint32_t src = hb0 + tm * S::TERM + rank * kSlabBytes;
-          bulk_copy_to_cluster(map_to_rank(src, dst), src, kSlabBytes,
+          const uint32_t src = hb0 + tm * S::TERM + rank * S::SLAB;
+          bulk_copy_to_cluster(map_to_rank(src, dst), src, S::SLAB,
                                map_to_rank(full0 + 8u * rank, dst));
         }
       }
@@ -260,7 +280,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
     bool ok = true;
     if (lane == 0)
       for (int j = 0; j < CS; ++j)
-        if (j != rank) mbar_arrive_expect_tx(full0 + 8u * j, kTerms * kSlabBytes);
+        if (j != rank) mbar_arrive_expect_tx(full0 + 8u * j, kTerms * S::SLAB);
     push();  // h0: the slabs step 0 multiplies
     for (int t = 0; t < K; ++t) {
       if (lane == 0) {
@@ -273,10 +293,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
 #pragma unroll
           for (int s2 = 0; s2 < 2; ++s2) {  // the two 16-deep steps of slab j
             const int s = 2 * j + s2;
-            const uint32_t a0 = tmem + 128 + 8 * s;
+            const uint32_t a0 = tmem + kACol0 + 8 * s;
             // Descriptor of B term 0 at this k step; the start-address field counts 16 bytes,
             // so term 1 is a fixed add away.
-            const uint64_t d0 = bdesc0 + static_cast<uint64_t>(s * (4096 >> 4));
+            const uint64_t d0 = bdesc0 + static_cast<uint64_t>(s * ((NR * 32) >> 4));
             const uint64_t d1 = d0 + (S::TERM >> 4);
             // (A term, B term): hi*hi, hi*lo, lo*hi
             umma_tmem_a(tmem, a0, d0, idesc, acc);
@@ -288,7 +308,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
         umma_commit(done_bar);
         if (t + 1 < K)
           for (int j = 0; j < CS; ++j)
-            if (j != rank) mbar_arrive_expect_tx(full0 + 8u * j, kTerms * kSlabBytes);
+            if (j != rank) mbar_arrive_expect_tx(full0 + 8u * j, kTerms * S::SLAB);
         ok = mbar_wait_bounded_cta(done_bar, t & 1, p.status) && ok;
         tc_fence_before_sync();  // the step's MMAs are ordered before the signals below
         // This CTA no longer reads its h buffer for step t: tell every CTA.
@@ -296,8 +316,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
       }
       // ts of step t + 1 for the next epilogue.
       if (t + 1 < K)
-        for (int i = lane; i < kTM; i += 32)
-          ts_s[((t + 1) & 1) * kTM + i] =
+        for (int i = lane; i < NR; i += 32)
+          ts_s[((t + 1) & 1) * NR + i] =
               (row0 + i < B) ? __ldg(p.ts + static_cast<size_t>(t + 1) * B + row0 + i) : 0.f;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (bar_or(kStepBar, kTcThreads, !ok)) break;  // h_t is in this CTA's slab
@@ -305,18 +325,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
     }
   } else {
     // ================= epilogue warps =================
-    // X of (gate g, channel ch) for rows row0 + 64 hh + i, i < 64, of step t, in place in H
+    // X of (gate g, channel ch) for rows row0 + HR hh + i, i < HR, of step t, in place in H
     // (gate 0) or cache (gates 1-3).
     const size_t xrow = (g == 0) ? static_cast<size_t>(C) : 3ull * C;
     const float* xbase = ((g == 0) ? p.H : p.cache + static_cast<size_t>(g - 1) * C) + ch;
-    const int rfirst = row0 + 64 * hh;
+    const int rfirst = row0 + HR * hh;
     int nvalid = B - rfirst;
-    nvalid = nvalid < 0 ? 0 : (nvalid > 64 ? 64 : nvalid);
-    float xv[64];
+    nvalid = nvalid < 0 ? 0 : (nvalid > HR ? HR : nvalid);
+    float xv[HR];
     auto load_x = [&](int t) {
       const float* xp = xbase + (static_cast<size_t>(t) * B + rfirst) * xrow;
 #pragma unroll
-      for (int i = 0; i < 64; ++i) xv[i] = (i < nvalid) ? __ldcg(xp + i * xrow) : 0.f;
+      for (int i = 0; i < HR; ++i) xv[i] = (i < nvalid) ? __ldcg(xp + i * xrow) : 0.f;
     };
     load_x(0);
     bool ok = true;
@@ -325,17 +345,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after_sync();
       if (ok) {
-        const float* tsr = ts_s + (t & 1) * kTM + 64 * hh;
+        const float* tsr = ts_s + (t & 1) * NR + HR * hh;
         float* hout = p.H + (static_cast<size_t>(t) * B + rfirst) * C + ch;
         float* cout = p.cache + (static_cast<size_t>(t) * B + rfirst) * 3 * C + ch;
+        const uint32_t dq = tmem + (static_cast<uint32_t>(32 * q) << 16) + HR * hh;
+        // Rows ibase .. ibase + n - 1 of this warp half (n = 16, or 8 for the tail of 72).
+        auto rows = [&](float (&P)[16], int ibase, int n) {
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          float P[16];
-          tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + 64 * hh + 16 * cc, P);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) P[i] = fmaf(P[i], wunscale, xv[16 * cc + i]);
+          for (int i = 0; i < 16; ++i)
+            if (i < n) P[i] = fmaf(P[i], wunscale, xv[ibase + i]);
 #pragma unroll
           for (int i0 = 0; i0 < 16; i0 += 4) {
+            if (i0 >= n) break;
             // 4 x 4 transpose within the lane quad: lane g held gate g of rows i0 .. i0 + 3,
             // afterwards it holds the four gates of row i0 + g.
             float v[4] = {P[i0], P[i0 + 1], P[i0 + 2], P[i0 + 3]};
@@ -350,7 +371,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
                 else v[jj + m] = r;
               }
             }
-            const int ri = 16 * cc + i0 + g;  // this lane's row among the warp's 64
+            const int ri = ibase + i0 + g;  // this lane's row among the warp half's HR
             const float ff1 = fmaf(2.f, sigmoid_fast(2.f * v[0]), -1.f);
             const float ff2 = fmaf(2.f, sigmoid_fast(2.f * v[1]), -1.f);
             const float gt = sigmoid_fast(fmaf(v[2], tsr[ri], v[3]));
@@ -363,10 +384,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
               cp[2 * C] = gt;
             }
             const Split2 sp = split2(h);
-            uint8_t* dst = hb + hterm_offset(64 * hh + ri, ch);
+            uint8_t* dst = hb + hterm_offset<NR>(HR * hh + ri, ch);
             *reinterpret_cast<__half*>(dst) = sp.t[0];
             *reinterpret_cast<__half*>(dst + S::TERM) = sp.t[1];
           }
+        };
+#pragma unroll
+        for (int cc = 0; cc < HR / 16; ++cc) {
+          float P[16];
+          tmem_ld16(dq + 16 * cc, P);
+          rows(P, 16 * cc, 16);
+        }
+        if constexpr (HR % 16 == 8) {
+          float P[16];
+          float P8[8];
+          tmem_ld8(dq + HR - 8, P8);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) P[i] = P8[i];
+#pragma unroll
+          for (int i = 8; i < 16; ++i) P[i] = 0.f;
+          rows(P, HR - 8, 8);
         }
       }
       fence_proxy_async_smem();  // h_t's terms -> visible to the MMAs and the bulk copies
@@ -386,19 +423,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
   }
 }
 
-template <int CS>
+template <int CS, int NR>
 cudaError_t prepare_k(int* max_active) {
   int dev = 0, optin = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
-  const int smem = TcShape<CS>::SMEM;
+  const int smem = TcShape<CS, NR>::SMEM;
   if (smem > optin) {
     *max_active = 0;
     return cudaSuccess;
   }
-  auto* kern = cfc_fwd_tc_kernel<CS>;
+  auto* kern = cfc_fwd_tc_kernel<CS, NR>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -415,31 +452,36 @@ cudaError_t prepare_k(int* max_active) {
   return cudaOccupancyMaxActiveClusters(max_active, kern, &cfg);
 }
 
-template <int CS>
+template <int CS, int NR>
 cudaError_t launch_k(const FwdParams& p, cudaStream_t s, bool pdl) {
   LaunchCfg c;
-  c.grid = dim3(((p.B + kTM - 1) / kTM) * CS, 1, 1);
+  c.grid = dim3(((p.B + NR - 1) / NR) * CS, 1, 1);
   c.block = dim3(kTcThreads, 1, 1);
-  c.smem = TcShape<CS>::SMEM;
+  c.smem = TcShape<CS, NR>::SMEM;
   c.stream = s;
   c.pdl = pdl;
   c.cluster = dim3(CS, 1, 1);
-  return launch(c, cfc_fwd_tc_kernel<CS>, p);
+  return launch(c, cfc_fwd_tc_kernel<CS, NR>, p);
 }
 
 }  // namespace
 
 bool fwd_tc_supported(int C) { return C == 4 * kFwdChanPerCta || C == 8 * kFwdChanPerCta; }
 
-cudaError_t fwd_tc_prepare(int C, int* max_active_clusters) {
-  if (C == 4 * kFwdChanPerCta) return prepare_k<4>(max_active_clusters);
-  if (C == 8 * kFwdChanPerCta) return prepare_k<8>(max_active_clusters);
+// `rows`: batch rows per cluster, 128 or 144 (FwdParams::R at launch).
+cudaError_t fwd_tc_prepare(int C, int rows, int* max_active_clusters) {
+  if (C == 4 * kFwdChanPerCta)
+    return rows == 144 ? prepare_k<4, 144>(max_active_clusters) : prepare_k<4, 128>(max_active_clusters);
+  if (C == 8 * kFwdChanPerCta)
+    return rows == 144 ? prepare_k<8, 144>(max_active_clusters) : prepare_k<8, 128>(max_active_clusters);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t fwd_tc_launch(const FwdParams& p, cudaStream_t s, bool pdl) {
-  if (p.C == 4 * kFwdChanPerCta) return launch_k<4>(p, s, pdl);
-  if (p.C == 8 * kFwdChanPerCta) return launch_k<8>(p, s, pdl);
+  if (p.C == 4 * kFwdChanPerCta)
+    return p.R == 144 ? launch_k<4, 144>(p, s, pdl) : launch_k<4, 128>(p, s, pdl);
+  if (p.C == 8 * kFwdChanPerCta)
+    return p.R == 144 ? launch_k<8, 144>(p, s, pdl) : launch_k<8, 128>(p, s, pdl);
   return cudaErrorInvalidValue;
 }
 

@@ -59,10 +59,10 @@ cudaError_t fwd_launch(const FwdParams& p, int n_clusters, size_t smem, cudaStre
                        bool pdl);
 
 // The forward recurrence with each step's gate contraction on the tensor cores (clusters of
-// C / 32 CTAs serving 128 batch rows each; C = 128 or 256).  X in place in H / cache as for
-// fwd_launch.
+// C / 32 CTAs serving 128 or 144 batch rows each, FwdParams::R; C = 128 or 256).  X in place
+// in H / cache as for fwd_launch.
 bool fwd_tc_supported(int C);
-cudaError_t fwd_tc_prepare(int C, int* max_active_clusters);
+cudaError_t fwd_tc_prepare(int C, int rows, int* max_active_clusters);
 cudaError_t fwd_tc_launch(const FwdParams& p, cudaStream_t s, bool pdl);
 
 // The BPTT recurrence with each step's contraction delta = d_pre W_h on the tensor cores: one

@@ -39,6 +39,8 @@ RAGGED = [
     dict(B=600, K=5, n_x=24, C=256),   # tensor-core forward, clusters of 8, last cluster 88 rows
     dict(B=1600, K=4, n_x=8, C=128),   # tensor-core BPTT, 13 CTAs, the last with 64 rows
     dict(B=1030, K=3, n_x=16, C=256),  # tensor-core BPTT at the widest state, last CTA 6 rows
+    dict(B=2050, K=3, n_x=16, C=256),  # tensor-core forward with 144-row clusters (15 of them
+                                       # cover 2160 rows), the last one 34 rows
 ]
 
 
