@@ -120,14 +120,11 @@ int max_clusters(DeviceState& st, int kind, int variant, int CS, size_t smem, in
     return CFC_OK;
   }
   int n = 0;
-  // kind 0: forward (CUDA cores), 1: backward, 3 / 4: forward / backward with the tensor-core
-  // contraction (3: `variant` is the rows per cluster; 4: `variant` is C, the count is of CTAs
-  // per SM), 5: backward with the
-  // cluster-split tensor-core contraction (`variant` is C)
+  // kind 0: forward (CUDA cores), 1: backward, 3 / 6: forward / backward with the tensor-core
+  // contraction (`variant` is the rows per cluster, C = 32 CS)
   const cudaError_t e = (kind == 1)   ? cfc::bwd_prepare(CS, variant, smem, &n)
                        : (kind == 3) ? cfc::fwd_tc_prepare(CS * cfc::kFwdChanPerCta, variant, &n)
-                       : (kind == 4) ? cfc::bwd_tc_prepare(variant, &n)
-                       : (kind == 5) ? cfc::bwd_ks_prepare(variant, &n)
+                       : (kind == 6) ? cfc::bwd_l2x_prepare(32 * CS, variant, &n)
                                      : cfc::fwd_prepare(CS, variant, smem, &n);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
@@ -238,9 +235,9 @@ BwdLayout bwd_layout(int B, int K, int C, int n_x, int mode) {
     if (L.pdu.splits > 1) L.part_bytes += static_cast<size_t>(L.pdu.splits) * BK * n_x * sizeof(float);
   }
   L.total = L.part_off + L.part_bytes;
-  L.tc_bptt = B >= tc_bwd_min_rows(C) && cfc::bwd_tc_supported(C);
+  L.tc_bptt = B >= tc_bwd_min_rows(C) && cfc::bwd_l2x_supported(C);
   L.wsplit_off = align256(L.total);
-  if (L.tc_bptt) L.total = L.wsplit_off + cfc::bwd_tc_split_bytes(C);
+  if (L.tc_bptt) L.total = L.wsplit_off + cfc::bwd_l2x_ws_bytes(B, C);
   return L;
 }
 
@@ -370,26 +367,25 @@ int backward_recurrence(const float* dH, const float* W, const float* ts, const 
   p.wsplit = wsplit;
   p.dplanes = dplanes;
   p.dpitch = dpitch;
+  p.xbuf = nullptr;
   // The tensor-core BPTT moves dH, the cache and d_pre in whole 32-byte sectors.
-  if (wsplit && B >= tc_bwd_min_rows(C) && cfc::bwd_tc_supported(C) && aligned32(dH) &&
+  if (wsplit && B >= tc_bwd_min_rows(C) && cfc::bwd_l2x_supported(C) && aligned32(dH) &&
       aligned32(cache) && aligned32(d_pre)) {
-    // The cluster-split recurrence (C / 32 CTAs per 128 rows) when all its clusters fit in one
-    // wave, else the single-CTA one.  Measured on GB300 at C = 256, K = 32: 26 us per step for
-    // 8 or 12 clusters, 50.5 us for 16 (at most 15 clusters of 8 are resident, so 16 run in two
-    // waves), against 43 us for the single-CTA recurrence.
-    int n_ks = 0, n = 0;
-    rc = max_clusters(*st, 5, C, C / 32, 0, &n_ks);
+    // Clusters of C / 32 CTAs per 128 rows when they are all resident at once, else per 144
+    // rows (2048 rows: 15 clusters of 8 CTAs, the most GB300 keeps resident).
+    int n128 = 0, n = 0;
+    rc = max_clusters(*st, 6, 128, C / 32, 0, &n128);
     if (rc != CFC_OK) return rc;
-    if (n_ks < (B + 127) / 128) n_ks = 0;
-    if (n_ks <= 0) rc = max_clusters(*st, 4, C, 1, 0, &n);
+    const int NR = cfc::bwd_l2x_rows(B, n128);
+    rc = NR == 128 ? CFC_OK : max_clusters(*st, 6, NR, C / 32, 0, &n);
     if (rc != CFC_OK) return rc;
-    if (n_ks > 0 || n > 0) {
+    if (NR == 128 || n > 0) {
       const cudaStream_t s = static_cast<cudaStream_t>(stream);
-      rc = cuda_rc(cfc::bwd_tc_split(W, C, n_x, wsplit, s, pdl), CFC_ERR_LAUNCH_FAILED);
+      rc = cuda_rc(cfc::bwd_l2x_split(W, C, n_x, wsplit, s, pdl), CFC_ERR_LAUNCH_FAILED);
       if (rc != CFC_OK) return rc;
-      p.R = 0;
-      return cuda_rc(n_ks > 0 ? cfc::bwd_ks_launch(p, s, true) : cfc::bwd_tc_launch(p, s, true),
-                     CFC_ERR_LAUNCH_FAILED);
+      p.R = NR;
+      p.xbuf = reinterpret_cast<float*>(static_cast<char*>(wsplit) + cfc::bwd_l2x_image_bytes(C));
+      return cuda_rc(cfc::bwd_l2x_launch(p, NR, s, true), CFC_ERR_LAUNCH_FAILED);
     }
   }
   size_t smem = 0;
@@ -454,7 +450,7 @@ int cfc_bptt_workspace_bytes(int B, int K, int C, int n_x, size_t* bytes) {
   const int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
   if (!bytes) return CFC_ERR_NULL_PTR;
-  *bytes = bwd_layout(B, K, C, n_x, CFC_DW_ACCURATE).tc_bptt ? cfc::bwd_tc_split_bytes(C) : 0;
+  *bytes = bwd_layout(B, K, C, n_x, CFC_DW_ACCURATE).tc_bptt ? cfc::bwd_l2x_ws_bytes(B, C) : 0;
   return CFC_OK;
 }
 

@@ -46,6 +46,7 @@ struct BwdParams {
   // contraction's operand rows (4 * dpitch bytes per row: hi, then lo) at d_pre.
   int dplanes;
   int dpitch;
+  float* xbuf;         // bwd_l2x_launch: the clusters' exchange blocks (bwd_l2x_ws_bytes)
 };
 
 // Every launch function takes `pdl`: schedule the kernel while the previous kernel of the
@@ -79,6 +80,19 @@ cudaError_t bwd_tc_launch(const BwdParams& p, cudaStream_t s, bool pdl);
 // bwd_tc_launch and writes fp32 d_pre.
 cudaError_t bwd_ks_prepare(int C, int* max_active_clusters);
 cudaError_t bwd_ks_launch(const BwdParams& p, cudaStream_t s, bool pdl);
+
+// The BPTT recurrence with each step's contraction split along its reduction over a cluster of
+// C / 32 CTAs per NR = 128 or 144 batch rows (rows along the MMA's N side, C = 128 or 256), the
+// partial sums exchanged through L2.  Workspace (bwd_l2x_ws_bytes): the W_h^T image written by
+// bwd_l2x_split (bwd_l2x_image_bytes), then the exchange blocks (BwdParams::xbuf).  Writes fp32
+// d_pre.  bwd_l2x_rows: 128 when ceil(B / 128) clusters of that tile are resident at once.
+bool bwd_l2x_supported(int C);
+int bwd_l2x_rows(int B, int max_clusters_128);
+size_t bwd_l2x_image_bytes(int C);
+size_t bwd_l2x_ws_bytes(int B, int C);
+cudaError_t bwd_l2x_prepare(int C, int NR, int* max_active_clusters);
+cudaError_t bwd_l2x_split(const float* W, int C, int n_x, void* ws, cudaStream_t s, bool pdl);
+cudaError_t bwd_l2x_launch(const BwdParams& p, int NR, cudaStream_t s, bool pdl);
 
 size_t bwd_smem_bytes(int R, int CS);
 cudaError_t bwd_prepare(int CS, int R, size_t smem, int* max_active_clusters);

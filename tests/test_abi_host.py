@@ -161,9 +161,20 @@ def test_binding_refuses_missing_library(tmp_path):
         _lib.load(str(tmp_path / "libcfc.so"))
 
 
-@pytest.mark.parametrize("B,C,expect", [(32, 128, 0), (1023, 256, 0), (1024, 256, 24 * 256 * 256),
-                                        (1184, 128, 0), (1185, 128, 24 * 128 * 128),
-                                        (2048, 256, 24 * 256 * 256), (4096, 200, 0)])
+def _l2x_bytes(B, C):
+    """The tensor-core BPTT's workspace: per CTA of a C / 32 cluster, the W_h^T slice as two fp16
+    terms (C x 128 entries each: C * 512 bytes) and C output scales (fp32), 256-byte aligned;
+    then per cluster two step-parities of C/32 x C/32 exchange blocks of [rows x 32] fp32, for
+    the larger of the two row tiles (128 or 144 rows per cluster) rounded up over B."""
+    cs = C // 32
+    image = -(-(cs * C * 512 + cs * C * 4) // 256) * 256
+    rows = max(-(-B // nr) * nr for nr in (128, 144))
+    return image + rows * 2 * cs * cs * 32 * 4
+
+
+@pytest.mark.parametrize("B,C,expect", [(32, 128, 0), (1023, 256, 0), (1024, 256, _l2x_bytes(1024, 256)),
+                                        (1184, 128, 0), (1185, 128, _l2x_bytes(1185, 128)),
+                                        (2048, 256, _l2x_bytes(2048, 256)), (4096, 200, 0)])
 def test_bptt_workspace_bytes(lib, B, C, expect):
     out = ctypes.c_size_t(123)
     assert lib.cfc_bptt_workspace_bytes(B, 8, C, 16, ctypes.byref(out)) == OK
