@@ -577,21 +577,21 @@ def main():
     # The dominant kernel: the larger of the two recurrences (each stage is one launch).
     dominant = max(("fwd_rec", "bwd_rec"), key=lambda k: stage_ms[k])
     # Which kernel that stage ran: the tensor-core recurrences serve batches of at least 384
-    # (forward) or 1024 (BPTT) rows at C = 256, 768 or 1185 at C = 128; the CUDA-core ones
+    # (forward) or 129 (BPTT) rows at C = 256, 768 or 513 at C = 128; the CUDA-core ones
     # the rest.
     tc_fwd = w.C in (128, 256) and w.B >= (384 if w.C == 256 else 768)
     tc = tc_fwd if dominant == "fwd_rec" else n_bptt_ws > 0
     kname = {("fwd_rec", False): "cfc_fwd_kernel", ("bwd_rec", False): "cfc_bwd_kernel",
              ("fwd_rec", True): "cfc_fwd_tc_kernel",
-             ("bwd_rec", True): "cfc_bwd_tc_kernel"}[(dominant, tc)]
+             ("bwd_rec", True): "cfc_bwd_l2x_kernel"}[(dominant, tc)]
     ksrc = ["recurrent_cfc_cell_gb300/csrc/" + kname[: -len("_kernel")] + ".cu",
             "recurrent_cfc_cell_gb300/csrc/cfc_ptx.cuh",
             "recurrent_cfc_cell_gb300/csrc/cfc_kernels.h"]
     achieved = kernels[dominant]["tflops"]
     if tc:
         # Algorithmic fp32-equivalent flops against the dense bf16 tensor peak; each product
-        # is issued as 3 (forward, fp16 terms) or 6 (BPTT, bf16 terms) MMAs.
-        n_mma = 3 if dominant == "fwd_rec" else 6
+        # is issued as 3 MMAs (hi*hi, hi*lo, lo*hi of the fp16 terms) in both recurrences.
+        n_mma = 3
         roofline = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
                     "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
                     "traffic": profiled_traffic(kname, ksrc, workload_tag(w)),

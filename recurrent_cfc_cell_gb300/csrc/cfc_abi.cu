@@ -194,11 +194,11 @@ constexpr int kTcProjMinRows = 8192;
 int tc_fwd_min_rows(int C) { return C >= 256 ? 384 : 768; }
 
 // Batch rows from which the BPTT recurrence runs its per-step contraction on the tensor cores
-// (cfc_bwd_tc_kernel, one CTA per 128 rows); it needs the pre-split W_h^T in the workspace.
-// Measured per step, C = 128: the CUDA-core kernel takes 13.9 us up to B = 1100 and 27.4 us
-// from B = 1200 (a second wave of its 4-CTA clusters), the tensor-core one 19.7 us; C = 256:
-// 44.6 us (CUDA cores, B = 1023) against 43.0 us (tensor cores, B = 1024).
-int tc_bwd_min_rows(int C) { return C >= 256 ? 1024 : 1185; }
+// (cfc_bwd_l2x_kernel, clusters of C / 32 CTAs per 128 or 144 rows); it needs the W_h^T image
+// and the exchange blocks in the workspace.  Measured per step on GB300 (K = 32), C = 256: the
+// CUDA-core kernel 9.7 us at B = 128 and 18.6 us at B = 256, the tensor-core one 10.2 us at
+// either; C = 128: 7.6 us (CUDA cores, B = 512) and 14.5 us (B = 768) against 8.4-8.7 us.
+int tc_bwd_min_rows(int C) { return C >= 256 ? 129 : 513; }
 
 // Shared memory of a BPTT CTA launched as a dependent of the forward: more than half of an
 // SM's 228 KB (so two BPTT CTAs cannot be packed onto one SM for the whole recurrence) and
@@ -640,8 +640,11 @@ int cfc_backward(const float* dH, const float* u, const float* h0, const float* 
                            L.tc_bptt ? static_cast<char*>(ws) + L.wsplit_off : nullptr, dplanes,
                            L.mp);
   if (rc != CFC_OK) return rc;
+  // The operand build runs beside the CUDA-core BPTT (a few SMs); the tensor-core BPTT fills
+  // most SMs and its L2 exchange slows down under a concurrent stream of HBM traffic (GB300,
+  // B = 2048, K = 128, C = 256: 2.82 ms with the build beside it, 2.66 ms after it).
   return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode, stream,
-                     true, dplanes == dpre_planes(dw_mode), true);
+                     true, dplanes == dpre_planes(dw_mode), !L.tc_bptt);
 }
 
 int cfc_forward_backward(const float* u, const float* h0, const float* W, const float* b,
@@ -668,8 +671,11 @@ int cfc_forward_backward(const float* u, const float* h0, const float* W, const 
                            L.tc_bptt ? static_cast<char*>(ws) + L.wsplit_off : nullptr, dplanes,
                            L.mp);
   if (rc != CFC_OK) return rc;
+  // The operand build runs beside the CUDA-core BPTT (a few SMs); the tensor-core BPTT fills
+  // most SMs and its L2 exchange slows down under a concurrent stream of HBM traffic (GB300,
+  // B = 2048, K = 128, C = 256: 2.82 ms with the build beside it, 2.66 ms after it).
   return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode, stream,
-                     true, dplanes == dpre_planes(dw_mode), true);
+                     true, dplanes == dpre_planes(dw_mode), !L.tc_bptt);
 }
 
 int reduce_axis0(const float* per_batch, int n_batch, int n_tail, float* out,

@@ -69,7 +69,7 @@ struct XShape {
   static constexpr int BLOCK = NR * kChan;          // floats of one exchange block
   static constexpr int PW = NR / kRowsPerWarp;      // epilogue warps with rows
   static constexpr int NBARS = 6;                   // wfull, done[2], b_ready, xfull, spare
-  static constexpr int USED = W_BYTES + B_BYTES + 2 * NR * 4 + NBARS * 8 + 16 + 1024;
+  static constexpr int USED = W_BYTES + B_BYTES + 2 * NR * 4 + BLOCK * 4 + NBARS * 8 + 16 + 1024;
   // At least half an SM's shared memory: a CTA takes all 512 tensor-memory columns.
   static constexpr int SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
   static_assert(NR % 16 == 0 && NR <= kMaxNR && PW <= kEpiWarps, "row tile");
@@ -98,16 +98,59 @@ __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t adesc, uint64_
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
+// Tensor-memory loads of 8 / 16 consecutive fp32 columns of this warp's 32 lanes, without the
+// wait: several are issued back to back and tmem_wait_ld8 (below) completes them.
+__device__ __forceinline__ void tmem_ld8_nw(uint32_t taddr, uint32_t* r) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
                  "=r"(r[6]), "=r"(r[7])
                : "r"(taddr)
                : "memory");
+}
+__device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+// Ties 8 loaded registers to a point after the wait, so no use of them moves above it.
+__device__ __forceinline__ void tmem_after_wait8(uint32_t* r) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]));
+}
+
+// Reads NC (a multiple of 8, at most 64) columns of the partial starting at column c0 (one
+// wait for all of them), scales them back and stores them into the exchange block `blk`
+// (row-major [rows][32], this lane's output column): in global memory (L2 only), or in this
+// CTA's shared memory when `to_smem` (a warp-uniform choice).
+template <int NC>
+__device__ __forceinline__ void drain_piece(uint32_t dmem, int c0, float os,
+                                            const float* __restrict__ ri,
+                                            float* __restrict__ blk, bool to_smem) {
+  static_assert(NC % 8 == 0 && NC <= 64, "piece");
+  uint32_t r[NC];
+  float rs[NC];  // the row scales, read before any store (the block may be in shared memory)
+#pragma unroll
+  for (int j = 0; j < NC; ++j) rs[j] = ri[c0 + j];
+#pragma unroll
+  for (int j = 0; j + 16 <= NC; j += 16) tmem_ld16_nw(dmem + c0 + j, r + j);
+  if constexpr (NC % 16 != 0) tmem_ld8_nw(dmem + c0 + NC - 8, r + NC - 8);
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+  for (int j = 0; j < NC; j += 8) tmem_after_wait8(r + j);
+  if (to_smem) {
+#pragma unroll
+    for (int j = 0; j < NC; ++j) blk[(c0 + j) * kChan] = (__uint_as_float(r[j]) * os) * rs[j];
+  } else {
+#pragma unroll
+    for (int j = 0; j < NC; ++j)
+      __stcg(blk + (c0 + j) * kChan, (__uint_as_float(r[j]) * os) * rs[j]);
+  }
 }
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
@@ -218,7 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_l2x_kernel(const BwdParam
   uint8_t* bterm = sm + S::W_BYTES;
   const uint32_t sB = smem_addr(bterm);
   float* rinv = reinterpret_cast<float*>(sm + S::W_BYTES + S::B_BYTES);  // [2][NR]: 2^-e_row
-  uint64_t* bars = reinterpret_cast<uint64_t*>(rinv + 2 * NR);
+  float* own = rinv + 2 * NR;  // [NR][32]: this CTA's own exchange block
+  uint64_t* bars = reinterpret_cast<uint64_t*>(own + S::BLOCK);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + S::NBARS);
   const uint32_t wfull = smem_addr(&bars[0]);
   const uint32_t done0 = smem_addr(&bars[1]);    // + 8 h: MMAs of output half h committed
@@ -232,7 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_l2x_kernel(const BwdParam
   const int B = p.B, K = p.K;
   const uint8_t* wimg = static_cast<const uint8_t*>(p.wsplit);
   const float* oscale = reinterpret_cast<const float*>(wimg + static_cast<size_t>(CS) * S::W_BYTES);
-  // Exchange blocks of this cluster: [parity][dest][src][NR][32] fp32.
+  // Exchange blocks of this cluster: [parity][dest][src][NR][32] fp32 (the blocks with
+  // dest == src are not used: each CTA keeps its own in shared memory).
   float* xb = p.xbuf + static_cast<size_t>(cid) * 2 * CS * CS * S::BLOCK;
 
   if (tid == 0) {
@@ -296,12 +341,12 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_l2x_kernel(const BwdParam
   } else {
     // ---- epilogue warps ----
     // Drain role (warps 0 .. 7): tensor-memory lane quarter q holds outputs 32 q .. 32 q + 31
-    // of output half dh, i.e. channel block `dest`; columns are batch rows.
+    // of output half dh, i.e. channel block `dest`; columns are batch rows.  The block for this
+    // CTA's own channels stays in shared memory (`own`); the others go to L2.
     const int q = warp & 3;
     const int dh = (S::HALVES == 2) ? (warp >> 2) : 0;
     const int dest = 4 * dh + q;
     const int col_lo = (S::HALVES == 2) ? 0 : (warp >> 2) * (NR / 2);
-    const int col_hi = (S::HALVES == 2) ? NR : col_lo + NR / 2;
     const bool drainer = warp < kDrainWarps;
     const float os = drainer ? __ldg(oscale + rank * C + 128 * dh + 32 * q + lane) : 0.f;
     const uint32_t dmem = tmem + (static_cast<uint32_t>(32 * q) << 16) +
@@ -322,20 +367,35 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_l2x_kernel(const BwdParam
           if (dok) {
             tc_fence_after_sync();
             const float* ri = rinv + (par ^ 1) * NR;  // row scales of the B this MMA read
-            float* blk = xb + (static_cast<size_t>((par * CS + dest) * CS + rank)) * S::BLOCK + lane;
-            int c0 = col_lo;
-            for (; c0 + 8 <= col_hi; c0 += 8) {
-              float v[8];
-              tmem_ld8(dmem + c0, v);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) __stcg(blk + (c0 + j) * kChan, (v[j] * os) * ri[c0 + j]);
-            }
+            float* blk = dest == rank
+                             ? own + lane
+                             : xb + (static_cast<size_t>((par * CS + dest) * CS + rank)) * S::BLOCK + lane;
+            constexpr int DC = S::HALVES == 2 ? NR : NR / 2;  // columns per drain warp
+            const bool mine = dest == rank;
+#pragma unroll 1
+            for (int pc = 0; pc < DC / 64; ++pc)
+              drain_piece<64>(dmem, col_lo + 64 * pc, os, ri, blk, mine);
+            if constexpr (DC % 64 != 0)
+              drain_piece<DC % 64>(dmem, col_lo + DC - DC % 64, os, ri, blk, mine);
             tc_fence_before_sync();  // the reads precede the next step's MMAs (via b_ready)
             __syncwarp();
-            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            if (dest != rank) asm volatile("fence.acq_rel.gpu;" ::: "memory");
             if (lane == 0) mbar_arrive_remote(map_to_rank(xfull, dest));
           }
           ok = dok;
+        } else if (t >= 0) {
+          // ---- warp 8: this step's inputs towards L2 while the exchange runs (per row the
+          // CTA's 128-byte slices of dH and of the three cache planes, and ts) ----
+          for (int j = lane; j < 5 * NR; j += 32) {
+            const int b = row0 + j / 5, kind = j % 5;
+            if (b < B) {
+              const size_t tb = static_cast<size_t>(t) * B + b;
+              prefetch_l2(kind == 0   ? static_cast<const void*>(p.dH + tb * C + kChan * rank)
+                          : kind == 4 ? static_cast<const void*>(p.ts + tb)
+                                      : static_cast<const void*>(p.cache + (tb * 3 + (kind - 1)) * C +
+                                                                 kChan * rank));
+            }
+          }
         }
         if (ok) ok = mbar_wait_bounded_cluster(xfull, (n - 1) & 1, p.status);
         // All of this CTA's MMAs of the step (they read B) are done before B is rewritten: the
@@ -348,22 +408,46 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_l2x_kernel(const BwdParam
       }
       if (has_rows) {
         const float* in = xb + static_cast<size_t>(par * CS + rank) * CS * S::BLOCK + 2 * cp;
-#pragma unroll 1
+        // Two batches of 4 rows, unrolled so that the second batch's loads can be in flight
+        // while the first one computes.
+#pragma unroll
         for (int ib = 0; ib < 2; ++ib) {
           int rr[4];
-          float2 delta[4];
+          bool rv[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             rr[i] = kRowsPerWarp * warp + 2 * (4 * ib + i) + rsub;
-            delta[i] = make_float2(0.f, 0.f);
+            rv[i] = row0 + rr[i] < B;
           }
+          // This step's inputs and the exchange blocks, all loads issued before any is used
+          // (rows past B read row 0 of the step and are zeroed).
+          float2 dHv[4], f1[4], f2[4], gg[4];
+          float tsv[4];
+          const int tt = t >= 0 ? t : 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const size_t tb = static_cast<size_t>(tt) * B + (rv[i] ? row0 + rr[i] : 0);
+            dHv[i] = __ldcg(reinterpret_cast<const float2*>(p.dH + tb * C + ch));
+            const float* cpp = p.cache + tb * 3 * C + ch;
+            f1[i] = __ldcg(reinterpret_cast<const float2*>(cpp));
+            f2[i] = __ldcg(reinterpret_cast<const float2*>(cpp + C));
+            gg[i] = __ldcg(reinterpret_cast<const float2*>(cpp + 2 * C));
+            tsv[i] = __ldg(p.ts + tb);
+          }
+          float2 delta[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) delta[i] = make_float2(0.f, 0.f);
           if (n > 0) {
             float2 x[CS][4];
 #pragma unroll
             for (int s = 0; s < CS; ++s)
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                x[s][i] = __ldcg(reinterpret_cast<const float2*>(in + s * S::BLOCK + rr[i] * kChan));
+              for (int i = 0; i < 4; ++i) {
+                const int off = s * S::BLOCK + rr[i] * kChan;
+                x[s][i] = s == rank
+                              ? *reinterpret_cast<const float2*>(own + rr[i] * kChan + 2 * cp)
+                              : __ldcg(reinterpret_cast<const float2*>(in + off));
+              }
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -374,69 +458,62 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_l2x_kernel(const BwdParam
           }
           if (n == K) {  // the last exchange: delta = W_h^T d_pre[0] = dh0
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int b = row0 + rr[i];
-              if (b < B) *reinterpret_cast<float2*>(p.dh0 + static_cast<size_t>(b) * C + ch) = delta[i];
-            }
+            for (int i = 0; i < 4; ++i)
+              if (rv[i])
+                *reinterpret_cast<float2*>(p.dh0 + static_cast<size_t>(row0 + rr[i]) * C + ch) =
+                    delta[i];
             continue;
           }
           // ---- d_pre of step t for two channels of each of the 4 rows ----
-          float2 dHv[4], f1[4], f2[4], gg[4];
-          float tsv[4];
+          float pv[4][2][4];  // [row][channel][gate]
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int b = row0 + rr[i];
-            if (b < B) {
-              const size_t tb = static_cast<size_t>(t) * B + b;
-              dHv[i] = __ldcg(reinterpret_cast<const float2*>(p.dH + tb * C + ch));
-              const float* cpp = p.cache + tb * 3 * C + ch;
-              f1[i] = __ldcg(reinterpret_cast<const float2*>(cpp));
-              f2[i] = __ldcg(reinterpret_cast<const float2*>(cpp + C));
-              gg[i] = __ldcg(reinterpret_cast<const float2*>(cpp + 2 * C));
-              tsv[i] = __ldg(p.ts + tb);
-            } else {
-              dHv[i] = f1[i] = f2[i] = gg[i] = make_float2(0.f, 0.f);
-              tsv[i] = 0.f;
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int b = row0 + rr[i];
-            float pv[2][4];  // [channel][gate]
+            const float z = rv[i] ? 1.f : 0.f;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-              const float dhv = (c ? dHv[i].y : dHv[i].x) + (c ? delta[i].y : delta[i].x);
+              const float dhv = z * ((c ? dHv[i].y : dHv[i].x) + (c ? delta[i].y : delta[i].x));
               const float a1 = c ? f1[i].y : f1[i].x, a2 = c ? f2[i].y : f2[i].x;
               const float g = c ? gg[i].y : gg[i].x;
               const float ds = dhv * (a2 - a1) * g * (1.f - g);
-              pv[c][0] = dhv * (1.f - g) * (1.f - a1 * a1);
-              pv[c][1] = dhv * g * (1.f - a2 * a2);
-              pv[c][2] = ds * tsv[i];
-              pv[c][3] = ds;
+              pv[i][c][0] = dhv * (1.f - g) * (1.f - a1 * a1);
+              pv[i][c][1] = dhv * g * (1.f - a2 * a2);
+              pv[i][c][2] = ds * tsv[i];
+              pv[i][c][3] = ds;
             }
-            if (b < B) {
-              float* dpp = p.d_pre + (static_cast<size_t>(t) * B + b) * 4 * C + ch;
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (rv[i]) {
+              float* dpp = p.d_pre + (static_cast<size_t>(t) * B + row0 + rr[i]) * 4 * C + ch;
 #pragma unroll
               for (int g = 0; g < 4; ++g)
                 *reinterpret_cast<float2*>(dpp + static_cast<size_t>(g) * C) =
-                    make_float2(pv[0][g], pv[1][g]);
+                    make_float2(pv[i][0][g], pv[i][1][g]);
             }
-            // Row scale: the largest magnitude over the row's 128 entries (16 lanes).
-            float m = 0.f;
+          // Row scales: the largest magnitude over each row's 128 entries (16 lanes).
+          float m[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            m[i] = 0.f;
 #pragma unroll
             for (int c = 0; c < 2; ++c)
 #pragma unroll
-              for (int g = 0; g < 4; ++g) m = fmaxf(m, fabsf(pv[c][g]));
+              for (int g = 0; g < 4; ++g) m[i] = fmaxf(m[i], fabsf(pv[i][c][g]));
+          }
 #pragma unroll
-            for (int d = 8; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
-            const int e = pow2_exponent(m);
+          for (int d = 8; d > 0; d >>= 1)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], d));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int e = pow2_exponent(m[i]);
             const float sc = pow2f(e);
             uint32_t hw[4], lw[4];
 #pragma unroll
             for (int c = 0; c < 2; ++c)
 #pragma unroll
               for (int gp = 0; gp < 2; ++gp) {
-                const float x0 = pv[c][2 * gp] * sc, x1 = pv[c][2 * gp + 1] * sc;
+                const float x0 = pv[i][c][2 * gp] * sc, x1 = pv[i][c][2 * gp + 1] * sc;
                 const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
                 hw[2 * c + gp] = pack_h2(h0, h1);
                 lw[2 * c + gp] = pack_h2(__float2half_rn(x0 - __half2float(h0)),
@@ -452,19 +529,6 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_l2x_kernel(const BwdParam
         }
       }
       if (n == K) break;
-      // The next step's inputs towards L2 while this step's exchange runs.
-      if (has_rows && t >= 1 && cp < 4) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int b = row0 + kRowsPerWarp * warp + 2 * i + rsub;
-          if (b < B) {
-            const size_t tb = static_cast<size_t>(t - 1) * B + b;
-            prefetch_l2(cp == 0 ? static_cast<const void*>(p.dH + tb * C + kChan * rank)
-                                : static_cast<const void*>(p.cache + (tb * 3 + (cp - 1)) * C +
-                                                           kChan * rank));
-          }
-        }
-      }
       fence_proxy_async_smem();  // the B terms -> visible to the MMAs
       tc_fence_before_sync();
       mbar_arrive(b_ready);

@@ -41,7 +41,7 @@ struct BwdParams {
   int* status;
   int B, K, C, n_x, n_in;
   int CS, R;
-  const void* wsplit;  // tensor-core BPTT: W_h^T pre-split into bf16 terms (bwd_tc_split)
+  const void* wsplit;  // tensor-core BPTT: the W_h^T image (bwd_l2x_split)
   // d_pre output form: 0 = fp32 [K][B][4][C] at d_pre; 1 or 2 = that many bf16 planes in the
   // contraction's operand rows (4 * dpitch bytes per row: hi, then lo) at d_pre.
   int dplanes;
@@ -65,21 +65,6 @@ cudaError_t fwd_launch(const FwdParams& p, int n_clusters, size_t smem, cudaStre
 bool fwd_tc_supported(int C);
 cudaError_t fwd_tc_prepare(int C, int rows, int* max_active_clusters);
 cudaError_t fwd_tc_launch(const FwdParams& p, cudaStream_t s, bool pdl);
-
-// The BPTT recurrence with each step's contraction delta = d_pre W_h on the tensor cores: one
-// CTA per 128 batch rows, no exchange between CTAs (C = 128 or 256).  bwd_tc_split first
-// writes W_h^T as three bf16 terms in the layout the kernel streams (bwd_tc_split_bytes).
-bool bwd_tc_supported(int C);
-size_t bwd_tc_split_bytes(int C);
-cudaError_t bwd_tc_split(const float* W, int C, int n_x, void* wsplit, cudaStream_t s, bool pdl);
-cudaError_t bwd_tc_prepare(int C, int* max_active_ctas);
-cudaError_t bwd_tc_launch(const BwdParams& p, cudaStream_t s, bool pdl);
-
-// The BPTT recurrence with each step's contraction split along its reduction over a cluster of
-// C / 32 CTAs per 128 batch rows (C = 128 or 256); reads the same pre-split W_h^T as
-// bwd_tc_launch and writes fp32 d_pre.
-cudaError_t bwd_ks_prepare(int C, int* max_active_clusters);
-cudaError_t bwd_ks_launch(const BwdParams& p, cudaStream_t s, bool pdl);
 
 // The BPTT recurrence with each step's contraction split along its reduction over a cluster of
 // C / 32 CTAs per NR = 128 or 144 batch rows (rows along the MMA's N side, C = 128 or 256), the

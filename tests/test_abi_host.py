@@ -172,8 +172,9 @@ def _l2x_bytes(B, C):
     return image + rows * 2 * cs * cs * 32 * 4
 
 
-@pytest.mark.parametrize("B,C,expect", [(32, 128, 0), (1023, 256, 0), (1024, 256, _l2x_bytes(1024, 256)),
-                                        (1184, 128, 0), (1185, 128, _l2x_bytes(1185, 128)),
+@pytest.mark.parametrize("B,C,expect", [(32, 128, 0), (128, 256, 0), (129, 256, _l2x_bytes(129, 256)),
+                                        (1024, 256, _l2x_bytes(1024, 256)),
+                                        (512, 128, 0), (513, 128, _l2x_bytes(513, 128)),
                                         (2048, 256, _l2x_bytes(2048, 256)), (4096, 200, 0)])
 def test_bptt_workspace_bytes(lib, B, C, expect):
     out = ctypes.c_size_t(123)
