@@ -435,7 +435,6 @@ int cfc_step_launches(int B, int K, int C, int n_x, int dw_mode, int with_du, in
   const BwdLayout L = bwd_layout(B, K, C, n_x, dw_mode);
   if (L.tc_bptt) n += 1;
   if (dw_mode == CFC_DW_TF32) n += 2;  // transposed copies of d_pre and z
-  if (L.tc_bptt && dpre_planes(dw_mode) > 0) n += 1;  // d_pre split after the tensor-core BPTT
   *launches = n;
   return CFC_OK;
 }
@@ -473,14 +472,11 @@ int cfc_backward_recurrence_ws(const float* dH, const float* W, const float* ts,
 
 namespace {
 
-// The d_pre form the BPTT of cfc_backward writes: the contraction's bf16 rows straight from
-// the CUDA-core recurrence; fp32 from the tensor-core recurrence, split in place afterwards
-// (measured on GB300 at B=2048, K=128, C=256: the recurrence took 6.74 ms writing bf16 rows
-// and 5.40 ms writing fp32; the split pass takes about 0.3 ms).  C is 128 or 256 there, so the
-// rows' operand bytes are their fp32 bytes and the in-place split is safe.
-int bptt_dplanes(const BwdLayout& L, int mode) {
-  return L.tc_bptt ? 0 : dpre_planes(mode);
-}
+// The d_pre form the BPTT of cfc_backward writes: the contraction's operand rows, straight
+// from either recurrence (fp32 rows for the TF32 and SIMT modes).  The tensor-core recurrence
+// once wrote fp32 and a pass split it in place afterwards: 0.32 ms of HBM traffic at B=2048,
+// K=128, C=256 that writing the rows directly does not cost.
+int bptt_dplanes(const BwdLayout& /*L*/, int mode) { return dpre_planes(mode); }
 
 // The standalone weight-gradient stage splits an fp32 d_pre into the workspace head.  That is
 // safe when d_pre lies outside the head, or is the head itself with rows whose operand bytes
@@ -640,11 +636,12 @@ int cfc_backward(const float* dH, const float* u, const float* h0, const float* 
                            L.tc_bptt ? static_cast<char*>(ws) + L.wsplit_off : nullptr, dplanes,
                            L.mp);
   if (rc != CFC_OK) return rc;
-  // The operand build runs beside the CUDA-core BPTT (a few SMs); the tensor-core BPTT fills
+  // The operand build runs beside the CUDA-core BPTT (a few SMs).  The tensor-core BPTT fills
   // most SMs and its L2 exchange slows down under a concurrent stream of HBM traffic (GB300,
-  // B = 2048, K = 128, C = 256: 2.82 ms with the build beside it, 2.66 ms after it).
+  // B = 2048, K = 128, C = 256: 2.82 ms with the build beside it, 2.66 ms after it), so there
+  // the gradient stage starts as an ordinary launch, after the recurrence.
   return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode, stream,
-                     true, dplanes == dpre_planes(dw_mode), !L.tc_bptt);
+                     !L.tc_bptt, dplanes == dpre_planes(dw_mode), !L.tc_bptt);
 }
 
 int cfc_forward_backward(const float* u, const float* h0, const float* W, const float* b,
@@ -671,11 +668,12 @@ int cfc_forward_backward(const float* u, const float* h0, const float* W, const 
                            L.tc_bptt ? static_cast<char*>(ws) + L.wsplit_off : nullptr, dplanes,
                            L.mp);
   if (rc != CFC_OK) return rc;
-  // The operand build runs beside the CUDA-core BPTT (a few SMs); the tensor-core BPTT fills
+  // The operand build runs beside the CUDA-core BPTT (a few SMs).  The tensor-core BPTT fills
   // most SMs and its L2 exchange slows down under a concurrent stream of HBM traffic (GB300,
-  // B = 2048, K = 128, C = 256: 2.82 ms with the build beside it, 2.66 ms after it).
+  // B = 2048, K = 128, C = 256: 2.82 ms with the build beside it, 2.66 ms after it), so there
+  // the gradient stage starts as an ordinary launch, after the recurrence.
   return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode, stream,
-                     true, dplanes == dpre_planes(dw_mode), !L.tc_bptt);
+                     !L.tc_bptt, dplanes == dpre_planes(dw_mode), !L.tc_bptt);
 }
 
 int reduce_axis0(const float* per_batch, int n_batch, int n_tail, float* out,

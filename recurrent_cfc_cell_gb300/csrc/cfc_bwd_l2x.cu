@@ -24,8 +24,9 @@
 //      own channels in rank order (a fixed order: bitwise reproducible).  Tensor memory cannot
 //      be read by another SM, and a shared-memory exchange of these blocks was slower than L2;
 //   3. forms dh = dH + delta and the four gate gradients of its 32 channels for each row,
-//      writes them to global memory (fp32 d_pre, for the weight gradients) and writes their two
-//      fp16 terms into shared memory as the next step's B.
+//      writes them to global memory for the weight gradients (fp32 d_pre, or straight in the
+//      contraction's operand rows: bf16 hi and, with two planes, lo = bf16(x - hi)) and writes
+//      their two fp16 terms into shared memory as the next step's B.
 // The last exchange gives dh0.  15 clusters of 144 rows cover 2048 rows in one wave (GB300
 // keeps at most 15 clusters of 8 CTAs resident).
 //
@@ -35,6 +36,7 @@
 // warp 9 lane 0 loads W_h^T and issues the MMAs.  Every wait is bounded; a timeout is recorded
 // in the status word, and all CTAs leave through one final cluster barrier, so none exits while
 // another may still arrive on its barriers.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "cfc_kernels.h"
@@ -76,6 +78,11 @@ struct XShape {
   static_assert(HALVES * NR <= 512, "tensor-memory columns");
   static_assert(W_BYTES % kWPiece == 0, "W image pieces");
 };
+
+__device__ __forceinline__ uint32_t pack_b2(__nv_bfloat16 lo, __nv_bfloat16 hi) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
+}
 
 __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
   return static_cast<uint32_t>(__half_as_ushort(lo)) |
@@ -177,10 +184,6 @@ __device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
       : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
       : "memory");
   return r != 0;
-}
-
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // Power-of-two scale for a row whose largest magnitude is m: the exponent e with
@@ -484,11 +487,28 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_l2x_kernel(const BwdParam
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             if (rv[i]) {
-              float* dpp = p.d_pre + (static_cast<size_t>(t) * B + row0 + rr[i]) * 4 * C + ch;
+              const size_t row = static_cast<size_t>(t) * B + row0 + rr[i];
+              if (p.dplanes == 0) {
+                float* dpp = p.d_pre + row * 4 * C + ch;
 #pragma unroll
-              for (int g = 0; g < 4; ++g)
-                *reinterpret_cast<float2*>(dpp + static_cast<size_t>(g) * C) =
-                    make_float2(pv[i][0][g], pv[i][1][g]);
+                for (int g = 0; g < 4; ++g)
+                  *reinterpret_cast<float2*>(dpp + static_cast<size_t>(g) * C) =
+                      make_float2(pv[i][0][g], pv[i][1][g]);
+              } else {
+                // Operand row: 2 dpitch bf16 values, hi at k = g C + channel, lo dpitch on.
+                __nv_bfloat16* q = reinterpret_cast<__nv_bfloat16*>(p.d_pre) +
+                                   row * 2 * static_cast<size_t>(p.dpitch) + ch;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                  const __nv_bfloat16 h0 = __float2bfloat16_rn(pv[i][0][g]);
+                  const __nv_bfloat16 h1 = __float2bfloat16_rn(pv[i][1][g]);
+                  *reinterpret_cast<uint32_t*>(q + static_cast<size_t>(g) * C) = pack_b2(h0, h1);
+                  if (p.dplanes == 2)
+                    *reinterpret_cast<uint32_t*>(q + p.dpitch + static_cast<size_t>(g) * C) =
+                        pack_b2(__float2bfloat16_rn(pv[i][0][g] - __bfloat162float(h0)),
+                                __float2bfloat16_rn(pv[i][1][g] - __bfloat162float(h1)));
+                }
+              }
             }
           // Row scales: the largest magnitude over each row's 128 entries (16 lanes).
           float m[4];
@@ -642,7 +662,8 @@ cudaError_t bwd_l2x_split(const float* W, int C, int n_x, void* ws, cudaStream_t
 }
 
 cudaError_t bwd_l2x_launch(const BwdParams& p, int NR, cudaStream_t s, bool pdl) {
-  if (p.dplanes != 0 || p.xbuf == nullptr) return cudaErrorInvalidValue;  // fp32 d_pre only
+  if (p.dplanes < 0 || p.dplanes > 2 || p.xbuf == nullptr) return cudaErrorInvalidValue;
+  if (p.dplanes > 0 && (p.dpitch < 4 * p.C || p.dpitch % 8 != 0)) return cudaErrorInvalidValue;
   if (p.C == 128 && NR == 128) return launch_k<128, 128>(p, s, pdl);
   if (p.C == 128 && NR == 144) return launch_k<128, 144>(p, s, pdl);
   if (p.C == 256 && NR == 128) return launch_k<256, 128>(p, s, pdl);

@@ -48,6 +48,11 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Bring the 128-byte line holding `p` into L2 (no register result, nothing waits for it).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Address of the same shared-memory location in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
   uint32_t r;
