@@ -441,6 +441,58 @@ def timed_replays(torch, st, flush, stream, steps: int) -> float:
     return sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps
 
 
+class _Bf16StateStep:
+    """The bf16-state training step (cfc_forward_bf16 + cfc_backward_bf16) in one CUDA graph."""
+
+    def __init__(self, torch, _lib, w, d, dev):
+        B, K, C, n_x = w.B, w.K, w.C, w.n_x
+        self.H = torch.empty((K, B, C), dtype=torch.bfloat16, device=dev)
+        self.cache = torch.empty((K, B, 3, C), dtype=torch.bfloat16, device=dev)
+        self.fws = torch.empty(_lib.forward_bf16_workspace_bytes(B, K, C, n_x),
+                               dtype=torch.uint8, device=dev)
+        self.ws = torch.empty(_lib.workspace_bytes(B, K, C, n_x, _lib.CFC_DW_BF16),
+                              dtype=torch.uint8, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.out = {"dW": torch.empty((4, C, n_x + C), **f32), "db": torch.empty((4, C), **f32),
+                    "du": torch.empty((K, B, n_x), **f32), "dh0": torch.empty((B, C), **f32)}
+        self.d, self._lib, self.torch = d, _lib, torch
+        self.run()  # eager first: sets the kernels' attributes before capture
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.run()
+        torch.cuda.current_stream().wait_stream(s)
+        with torch.cuda.graph(self.graph):
+            self.run()
+
+    def run(self):
+        d, o, L = self.d, self.out, self._lib
+        L.cfc_forward_bf16(d["u"], d["h0"], d["W"], d["b"], d["ts"], self.H, self.cache, self.fws)
+        L.cfc_backward_bf16(d["dH"], d["u"], d["h0"], d["W"], d["ts"], self.H, self.cache,
+                            o["dW"], o["db"], o["du"], o["dh0"], self.ws)
+
+    def replay(self):
+        self.graph.replay()
+
+
+def bf16_state_record(torch, _lib, w, d, dev, flush, stream, steps: int) -> dict:
+    """Step time of the bf16-state variant on workload `w` (graph replays, L2 flushed), and the
+    bytes of the activations kept from forward to backward (H and the cache) in each dtype."""
+    sb = _Bf16StateStep(torch, _lib, w, d, dev)
+    for _ in range(3):
+        flush.zero_()
+        sb.replay()
+    torch.cuda.synchronize()
+    ms = timed_replays(torch, sb, flush, stream, steps)
+    status = _lib.device_status()
+    act = w.units * 4 * w.C
+    return {"ms_per_step": ms, "value": w.units / (ms * 1e-3), "unit": UNIT, "steps": steps,
+            "activation_bytes_bf16": 2 * act, "activation_bytes_fp32": 4 * act,
+            "device_status": status}
+
+
 def outputs_np(st) -> dict:
     out = {k: v.cpu().numpy() for k, v in st.outputs().items()}
     out["d_pre"] = decode_dpre(out["d_pre"], st.C, st.dw_mode)
@@ -481,6 +533,8 @@ def largest_record(torch, _lib, inputs, KLoopStep, to_device, dev, flush, stream
     names = {0: "accurate", 1: "bf16", 2: "tf32"}
     del st
     torch.cuda.empty_cache()
+    bf16 = bf16_state_record(torch, _lib, w, dinp, dev, flush, stream, 10)
+    torch.cuda.empty_cache()
     for m in modes:
         sm = KLoopStep(w.B, w.K, w.C, w.n_x, dw_mode=m, device=dev).bind(**dinp)
         sm.forward()
@@ -497,7 +551,8 @@ def largest_record(torch, _lib, inputs, KLoopStep, to_device, dev, flush, stream
         torch.cuda.empty_cache()
     return {"workload": w.name, "ms_per_step": ms, "value": w.units / (ms * 1e-3), "unit": UNIT,
             "steps": 10, "warmup": 3, "stages": stg, "kernels": kern,
-            "contraction": contraction, "clocks": clock_info, "parity_sampled": parity}
+            "contraction": contraction, "clocks": clock_info, "parity_sampled": parity,
+            "bf16_state": bf16}
 
 
 # ---------------------------------------------------------------- our arm
@@ -638,6 +693,8 @@ def main():
     status = _lib.device_status()
     gpu_out = outputs_np(st) if rank == 0 else None
     del ste
+    bf16 = bf16_state_record(torch, _lib, w, dinp, dev, flush, stream, min(args.steps, 200))
+    status = status or bf16["device_status"]
     largest = None
     if not args.no_largest and w.name != inputs.CONFIGS[4].name:
         modes = [int(m) for m in args.dw_modes.split(",") if m.strip()]
@@ -664,7 +721,7 @@ def main():
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "clocks": clock_info,
             "kernels": kernels, "stages_ms": stage_ms, "parity": parity,
-            "measured_peaks": mp, "largest_config": largest,
+            "measured_peaks": mp, "largest_config": largest, "bf16_state": bf16,
             "device_status": status, "peaks_source": pk["source"],
         }
         print(json.dumps(line), flush=True)

@@ -60,8 +60,9 @@ extern "C" {
  *                     significand bits) and three products per step; measured error against
  *                     the fp64 oracle ~5e-6 of max|dW| (up to 5e-5 on the 2048 x 128 x 256
  *                     workload, whose gradient cancels heavily).
- *   CFC_DW_BF16       tensor cores, one bf16 product per step: about 2^-9 relative error per
- *                     product, ~1e-3 of max|dW|.  For throughput, not for the 1e-4 tolerance.
+ *   CFC_DW_BF16       tensor cores, one bf16 product per step: each operand rounded to bf16
+ *                     (relative error at most 2^-8, so at most 2^-7 per product), measured
+ *                     2e-3 to 3e-3 of max|dW|.  For throughput, not for the 1e-4 tolerance.
  *   CFC_DW_TF32       tensor cores, one tf32 product per step (10 explicit mantissa bits).
  *                     For throughput, not for the 1e-4 tolerance.
  *   CFC_DW_SIMT_FP32  CUDA-core fp32 FMA contraction (the reference path).
@@ -161,6 +162,55 @@ int cfc_forward_backward(const float* u, const float* h0, const float* W, const 
                          const float* ts, const float* dH, int B, int K, int C, int n_x,
                          float* H, float* cache, float* dW, float* db, float* du, float* dh0,
                          void* ws, size_t ws_bytes, int dw_mode, cfc_stream_t stream);
+
+/*
+ * BF16 state.  The pages defer mixed precision to a future spec (page "K-loop
+ * Parallelization -- Block-per-Batch Kernel Refactor", section "Non-goals", and section
+ * "Post-refactor bottleneck analysis": "BF16 trunk").  Here it is the storage of the per-step
+ * activations in bf16 with all arithmetic and accumulation in fp32: H and the cache are
+ * written as bf16 (round to nearest even of exactly the fp32 values cfc_forward computes; the
+ * recurrence itself carries h in fp32), the backward reads them as bf16, keeps d_pre in one
+ * bf16 plane and computes dW, db and du with single-pass bf16 contractions (as CFC_DW_BF16).
+ * The persistent activation memory (H and cache, kept from forward to backward) is halved.
+ * Accuracy: H and the cache are cfc_forward's rounded to bf16 (relative error at most 2^-8,
+ * the bf16 unit roundoff); the gradients carry the bf16 rounding of the cache, d_pre and z
+ * (measured 2e-3 to 4e-3 of the largest entry, max-normalised, against the fp64 definition;
+ * bound 2^-6).  C must be even.  H and cache point to uint16 storage of
+ * bf16 values in the layouts of cfc_forward ([K][B][C], [K][B][3][C]).
+ */
+
+/*
+ * cfc_forward_bf16_workspace_bytes -- device workspace cfc_forward_bf16 needs: the input
+ * projection X = W_u u + b of every step in fp32 (4 C floats per batch row and step, plus
+ * alignment).  Returns CFC_OK, CFC_ERR_INVALID_DIM (also for odd C) or CFC_ERR_NULL_PTR.
+ */
+int cfc_forward_bf16_workspace_bytes(int B, int K, int C, int n_x, size_t* bytes);
+
+/*
+ * cfc_forward_bf16 -- cfc_forward with H and the cache stored as bf16.
+ *   u, h0, W, b, ts     as for cfc_forward (fp32)
+ *   H     [K][B][C]     OUTPUT, bf16
+ *   cache [K][B][3][C]  OUTPUT, bf16 (ff1, ff2, gate)
+ *   ws, ws_bytes        16-byte aligned device workspace of at least
+ *                       cfc_forward_bf16_workspace_bytes() bytes (transient: it may be reused
+ *                       once the call's work on the stream is done)
+ * Returns the error codes of cfc_forward, CFC_ERR_INVALID_DIM for odd C and
+ * CFC_ERR_WS_TOO_SMALL.
+ */
+int cfc_forward_bf16(const float* u, const float* h0, const float* W, const float* b,
+                     const float* ts, int B, int K, int C, int n_x, void* H, void* cache,
+                     void* ws, size_t ws_bytes, cfc_stream_t stream);
+
+/*
+ * cfc_backward_bf16 -- cfc_backward for the bf16 H and cache of cfc_forward_bf16.  The
+ * workspace is that of cfc_workspace_bytes(B, K, C, n_x, CFC_DW_BF16, ...); its head receives
+ * d_pre as bf16 operand rows.  Outputs dW, db, du (may be NULL), dh0 are fp32, as for
+ * cfc_backward.  Returns the error codes of cfc_backward and CFC_ERR_INVALID_DIM for odd C.
+ */
+int cfc_backward_bf16(const float* dH, const float* u, const float* h0, const float* W,
+                      const float* ts, const void* H, const void* cache, int B, int K, int C,
+                      int n_x, float* dW, float* db, float* du, float* dh0, void* ws,
+                      size_t ws_bytes, cfc_stream_t stream);
 
 /*
  * cfc_backward_recurrence -- the first stage of cfc_backward alone: the reverse-time

@@ -33,7 +33,8 @@ EXPORTED = ("cfc_workspace_bytes", "cfc_forward", "cfc_backward", "cfc_backward_
             "cfc_backward_noalloc", "cfc_input_projection", "cfc_forward_recurrence",
             "cfc_step_launches", "cfc_forward_backward", "cfc_bptt_workspace_bytes",
             "cfc_backward_recurrence_ws", "cfc_wait_self_test", "cfc_probe_fma",
-            "cfc_probe_l2_read")
+            "cfc_probe_l2_read", "cfc_forward_bf16_workspace_bytes", "cfc_forward_bf16",
+            "cfc_backward_bf16")
 CFC_ERR_SCRATCH_LIMIT = -10
 NOALLOC_SCRATCH_BYTES = 32 << 20  # size of cfc_backward_noalloc's built-in device scratch
 
@@ -94,6 +95,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.cfc_probe_fma.restype = i
     lib.cfc_probe_l2_read.argtypes = [vp, sz, i, vp, i, dptr, vp]
     lib.cfc_probe_l2_read.restype = i
+    lib.cfc_forward_bf16_workspace_bytes.argtypes = [i] * 4 + [ctypes.POINTER(sz)]
+    lib.cfc_forward_bf16_workspace_bytes.restype = i
+    lib.cfc_forward_bf16.argtypes = [vp] * 5 + [i] * 4 + [vp, vp, vp, sz, vp]
+    lib.cfc_forward_bf16.restype = i
+    lib.cfc_backward_bf16.argtypes = [vp] * 7 + [i] * 4 + [vp] * 5 + [sz, vp]
+    lib.cfc_backward_bf16.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -120,6 +127,27 @@ def _ptr(t, name: str, shape=None):
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _ptr16(t, name: str, shape):
+    """A contiguous bfloat16 CUDA tensor of the given shape (bf16 H / cache)."""
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _ws(ws):
+    import torch
+
+    if ws.dtype != torch.uint8 or not ws.is_cuda or not ws.is_contiguous():
+        raise ValueError("ws must be a contiguous uint8 CUDA tensor")
+    return ctypes.c_void_p(ws.data_ptr()), ws.numel()
 
 
 def _stream(stream):
@@ -309,3 +337,40 @@ def device_status() -> int:
     v = ctypes.c_int(0)
     _check("cfc_device_status", load().cfc_device_status(ctypes.byref(v)))
     return v.value
+
+
+def forward_bf16_workspace_bytes(B: int, K: int, C: int, n_x: int) -> int:
+    """Workspace of cfc_forward_bf16 (X = W_u u + b in fp32)."""
+    out = ctypes.c_size_t(0)
+    _check("cfc_forward_bf16_workspace_bytes",
+           load().cfc_forward_bf16_workspace_bytes(B, K, C, n_x, ctypes.byref(out)))
+    return out.value
+
+
+def cfc_forward_bf16(u, h0, W, b, ts, H, cache, ws, stream=None) -> None:
+    """bf16 H [K,B,C] and cache [K,B,3,C] <- the forward with fp32 arithmetic."""
+    K, B, n_x = u.shape
+    C = h0.shape[1]
+    n_in = n_x + C
+    wp, wn = _ws(ws)
+    rc = load().cfc_forward_bf16(
+        _ptr(u, "u", (K, B, n_x)), _ptr(h0, "h0", (B, C)), _ptr(W, "W", (4, C, n_in)),
+        _ptr(b, "b", (4, C)), _ptr(ts, "ts", (K, B)), B, K, C, n_x,
+        _ptr16(H, "H", (K, B, C)), _ptr16(cache, "cache", (K, B, 3, C)), wp, wn,
+        _stream(stream))
+    _check("cfc_forward_bf16", rc)
+
+
+def cfc_backward_bf16(dH, u, h0, W, ts, H, cache, dW, db, du, dh0, ws, stream=None) -> None:
+    """dW, db, du (optional), dh0 <- the backward of the bf16 H / cache of cfc_forward_bf16."""
+    K, B, n_x = u.shape
+    C = h0.shape[1]
+    n_in = n_x + C
+    wp, wn = _ws(ws)
+    rc = load().cfc_backward_bf16(
+        _ptr(dH, "dH", (K, B, C)), _ptr(u, "u", (K, B, n_x)), _ptr(h0, "h0", (B, C)),
+        _ptr(W, "W", (4, C, n_in)), _ptr(ts, "ts", (K, B)), _ptr16(H, "H", (K, B, C)),
+        _ptr16(cache, "cache", (K, B, 3, C)), B, K, C, n_x, _ptr(dW, "dW", (4, C, n_in)),
+        _ptr(db, "db", (4, C)), _ptr(du, "du", (K, B, n_x)), _ptr(dh0, "dh0", (B, C)),
+        wp, wn, _stream(stream))
+    _check("cfc_backward_bf16", rc)

@@ -300,7 +300,9 @@ namespace {
 // `pdl`: the previous kernel of the stream is one of this library's kernels of the same call
 // (see cfc_launch.cuh).
 int forward_recurrence(const float* h0, const float* W, const float* ts, int B, int K, int C,
-                       int n_x, float* H, float* cache, cfc_stream_t stream, bool pdl) {
+                       int n_x, float* H, float* cache, cfc_stream_t stream, bool pdl,
+                       const float* xH = nullptr, const float* xcache = nullptr,
+                       bool out_bf16 = false) {
   int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
   if (!h0 || !W || !ts || !H || !cache) return CFC_ERR_NULL_PTR;
@@ -312,6 +314,9 @@ int forward_recurrence(const float* h0, const float* W, const float* ts, int B, 
   if (rc != CFC_OK) return rc;
   cfc::FwdParams p;
   p.u = nullptr; p.h0 = h0; p.W = W; p.bias = nullptr; p.ts = ts; p.H = H; p.cache = cache;
+  p.xH = xH ? xH : H;  // X in place in H / cache unless given apart (bf16 outputs)
+  p.xcache = xcache ? xcache : cache;
+  p.out_bf16 = out_bf16 ? 1 : 0;
   p.status = st->status;
   p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
   p.CS = cluster_size_for(C, cfc::kFwdChanPerCta);
@@ -348,7 +353,7 @@ int forward_recurrence(const float* h0, const float* W, const float* ts, int B, 
 int backward_recurrence(const float* dH, const float* W, const float* ts, const float* cache,
                         int B, int K, int C, int n_x, float* d_pre, float* dh0,
                         cfc_stream_t stream, bool pdl, void* wsplit = nullptr, int dplanes = 0,
-                        int dpitch = 0) {
+                        int dpitch = 0, bool cache_bf16 = false) {
   int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
   if (!dH || !W || !ts || !cache || !d_pre || !dh0) return CFC_ERR_NULL_PTR;
@@ -367,6 +372,7 @@ int backward_recurrence(const float* dH, const float* W, const float* ts, const 
   p.wsplit = wsplit;
   p.dplanes = dplanes;
   p.dpitch = dpitch;
+  p.cache_bf16 = cache_bf16 ? 1 : 0;
   p.xbuf = nullptr;
   // The tensor-core BPTT moves dH, the cache and d_pre in whole 32-byte sectors.
   if (wsplit && B >= tc_bwd_min_rows(C) && cfc::bwd_l2x_supported(C) && aligned32(dH) &&
@@ -505,7 +511,7 @@ BwdLayoutCheck check_dpre_alias(const float* d_pre, bool dpre_in_ws, const char*
 int weight_grad(const float* d_pre, const float* u, const float* h0, const float* W,
                 const float* H, int B, int K, int C, int n_x, float* dW, float* db, float* du,
                 void* ws, size_t ws_bytes, int dw_mode, cfc_stream_t stream, bool first_pdl,
-                bool dpre_in_ws, bool build_first = false) {
+                bool dpre_in_ws, bool build_first = false, bool h_bf16 = false) {
   int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
   if (!valid_mode(dw_mode)) return CFC_ERR_INVALID_ARG;
@@ -528,6 +534,7 @@ int weight_grad(const float* d_pre, const float* u, const float* h0, const float
   const int BK = B * K;
   const int M = 4 * C, N = n_x + C;
   if (dw_mode == CFC_DW_SIMT_FP32) {
+    if (h_bf16) return CFC_ERR_INVALID_ARG;  // the CUDA-core contraction reads an fp32 H
     const int S = L.S_simt;
     rc = cuda_rc(cfc::dw_simt_launch(d_pre, u, H, h0, B, K, C, n_x, S, partial, s, first_pdl),
                  CFC_ERR_LAUNCH_FAILED);
@@ -547,8 +554,8 @@ int weight_grad(const float* d_pre, const float* u, const float* h0, const float
   const bool split = form != cfc::kFormTf32 && !dpre_in_ws;
   bool pdl = first_pdl;
   auto launch_build = [&]() {
-    rc = cuda_rc(cfc::build_operands_launch(form, u, H, h0, W, B, K, C, n_x, w + L.z_off,
-                                            w + L.wt_off, s, pdl),
+    rc = cuda_rc(cfc::build_operands_launch(form, u, H, h_bf16 ? 1 : 0, h0, W, B, K, C, n_x,
+                                            w + L.z_off, w + L.wt_off, s, pdl),
                  CFC_ERR_LAUNCH_FAILED);
     pdl = true;
   };
@@ -674,6 +681,70 @@ int cfc_forward_backward(const float* u, const float* h0, const float* W, const 
   // the gradient stage starts as an ordinary launch, after the recurrence.
   return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode, stream,
                      !L.tc_bptt, dplanes == dpre_planes(dw_mode), !L.tc_bptt);
+}
+
+// ---- bf16 state: H, the cache and d_pre stored as bf16, fp32 arithmetic ----
+
+static size_t bf16_x_offset(int B, int K, int C) {
+  return align256(static_cast<size_t>(K) * B * C * sizeof(float));
+}
+
+int cfc_forward_bf16_workspace_bytes(int B, int K, int C, int n_x, size_t* bytes) {
+  const int rc = check_dims(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (C % 2 != 0) return CFC_ERR_INVALID_DIM;
+  if (!bytes) return CFC_ERR_NULL_PTR;
+  *bytes = bf16_x_offset(B, K, C) + static_cast<size_t>(K) * B * 3 * C * sizeof(float);
+  return CFC_OK;
+}
+
+int cfc_forward_bf16(const float* u, const float* h0, const float* W, const float* b,
+                     const float* ts, int B, int K, int C, int n_x, void* H, void* cache,
+                     void* ws, size_t ws_bytes, cfc_stream_t stream) {
+  size_t need = 0;
+  int rc = cfc_forward_bf16_workspace_bytes(B, K, C, n_x, &need);
+  if (rc != CFC_OK) return rc;
+  if (!u || !h0 || !W || !b || !ts || !H || !cache || !ws) return CFC_ERR_NULL_PTR;
+  if (!aligned16(u) || !aligned16(h0) || !aligned16(W) || !aligned16(b) || !aligned16(ts) ||
+      !aligned16(H) || !aligned16(cache) || !aligned16(ws))
+    return CFC_ERR_MISALIGNED;
+  if (ws_bytes < need) return CFC_ERR_WS_TOO_SMALL;
+  // X = W_u u + b in fp32, in the layouts of H and cache, in the workspace; then the
+  // recurrence reads it there and stores H and the cache in bf16.
+  float* xH = static_cast<float*>(ws);
+  float* xcache = reinterpret_cast<float*>(static_cast<char*>(ws) + bf16_x_offset(B, K, C));
+  rc = cfc_input_projection(u, W, b, B, K, C, n_x, xH, xcache, stream);
+  if (rc != CFC_OK) return rc;
+  return forward_recurrence(h0, W, ts, B, K, C, n_x, static_cast<float*>(H),
+                            static_cast<float*>(cache), stream, false, xH, xcache, true);
+}
+
+int cfc_backward_bf16(const float* dH, const float* u, const float* h0, const float* W,
+                      const float* ts, const void* H, const void* cache, int B, int K, int C,
+                      int n_x, float* dW, float* db, float* du, float* dh0, void* ws,
+                      size_t ws_bytes, cfc_stream_t stream) {
+  int rc = check_dims(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (C % 2 != 0) return CFC_ERR_INVALID_DIM;
+  if (!dH || !u || !h0 || !W || !ts || !H || !cache || !dW || !db || !dh0 || !ws)
+    return CFC_ERR_NULL_PTR;
+  if (!aligned16(dH) || !aligned16(u) || !aligned16(h0) || !aligned16(W) || !aligned16(ts) ||
+      !aligned16(H) || !aligned16(cache) || !aligned16(dW) || !aligned16(db) ||
+      (du && !aligned16(du)) || !aligned16(dh0) || !aligned16(ws))
+    return CFC_ERR_MISALIGNED;
+  const int mode = CFC_DW_BF16;  // d_pre in one bf16 plane, single-pass bf16 contractions
+  const BwdLayout L = bwd_layout(B, K, C, n_x, mode);
+  if (ws_bytes < L.total) return CFC_ERR_WS_TOO_SMALL;
+  float* d_pre = reinterpret_cast<float*>(static_cast<char*>(ws) + L.d_pre_off);
+  const int dplanes = bptt_dplanes(L, mode);
+  rc = backward_recurrence(dH, W, ts, static_cast<const float*>(cache), B, K, C, n_x, d_pre, dh0,
+                           stream, false,
+                           L.tc_bptt ? static_cast<char*>(ws) + L.wsplit_off : nullptr, dplanes,
+                           L.mp, true);
+  if (rc != CFC_OK) return rc;
+  return weight_grad(d_pre, u, h0, W, static_cast<const float*>(H), B, K, C, n_x, dW, db, du, ws,
+                     ws_bytes, mode, stream, !L.tc_bptt, dplanes == dpre_planes(mode),
+                     !L.tc_bptt, true);
 }
 
 int reduce_axis0(const float* per_batch, int n_batch, int n_tail, float* out,

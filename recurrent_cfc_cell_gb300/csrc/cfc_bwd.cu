@@ -52,7 +52,10 @@ constexpr int kPre = 3;      // prefetch ring depth (copies run two steps ahead)
 constexpr int kRowBlock = 4; // rows per phase block of the ring path (its row counts are multiples)
 constexpr int kPreComp = 5;  // dH, ff1, ff2, gate, ts
 
-// Lanes 8*cj + c (c < 5) copy component c of this warp's channel cj for step t.
+// Lanes 8*cj + c (c < 5) copy component c of this warp's channel cj for step t.  A bf16 cache
+// component is copied as the 4-byte pair of channels (ch & ~1, ch | 1) that holds it (C is even
+// then), and the consumer takes its half (ring_value).
+template <bool BF>
 __device__ __forceinline__ void issue_pre(const BwdParams& p, float* pre, int t, int row0,
                                           int rank, int warp, int lane) {
   if (t < 0) return;
@@ -64,9 +67,12 @@ __device__ __forceinline__ void issue_pre(const BwdParams& p, float* pre, int t,
     const int b = row0 + r;
     if (b >= p.B) break;
     const size_t tb = static_cast<size_t>(t) * p.B + b;
-    const float* src = (c == 0) ? p.dH + tb * p.C + ch
-                     : (c == 4) ? p.ts + tb
-                                : p.cache + (tb * 3 + (c - 1)) * p.C + ch;
+    const void* src =
+        (c == 0)       ? static_cast<const void*>(p.dH + tb * p.C + ch)
+        : (c == 4)     ? static_cast<const void*>(p.ts + tb)
+        : BF           ? static_cast<const void*>(reinterpret_cast<const __nv_bfloat16*>(p.cache) +
+                                                  (tb * 3 + (c - 1)) * p.C + (ch & ~1))
+                       : static_cast<const void*>(p.cache + (tb * 3 + (c - 1)) * p.C + ch);
     float* dst = pre + ((((t % kPre) * p.R + r) * kWarps + warp) * 4 + cj) * kPreComp + c;
     cp_async_4(smem_addr(dst), src);
   }
@@ -122,25 +128,43 @@ __device__ __forceinline__ float gathered_delta(const float2 (&wt)[4][RS / 2], c
 }
 
 // Prefetched inputs of one step for RT rows (register path): dH, ff1, ff2, gate, ts.  dHp,
-// cp and tsp address row row0 of the step; row r is C, 3C and 1 floats further on.
-template <int RT>
+// cp (cpb: the same element of a bf16 cache, read when BF) and tsp address row row0 of the
+// step; row r is C, 3C and 1 elements further on.
+template <int RT, bool BF>
 __device__ __forceinline__ void load_step_regs(const float* dHp, const float* cp,
-                                               const float* tsp, int C, const bool (&rok)[RT],
+                                               const __nv_bfloat16* cpb, const float* tsp, int C,
+                                               const bool (&rok)[RT],
                                                float (&v)[RT][kPreComp]) {
 #pragma unroll
   for (int r = 0; r < RT; ++r) {
     const size_t o = static_cast<size_t>(r) * C;
     v[r][0] = rok[r] ? __ldcg(dHp + o) : 0.f;
-    v[r][1] = rok[r] ? __ldcg(cp + 3 * o) : 0.f;
-    v[r][2] = rok[r] ? __ldcg(cp + 3 * o + C) : 0.f;
-    v[r][3] = rok[r] ? __ldcg(cp + 3 * o + 2 * C) : 0.f;
+    if constexpr (BF) {
+      v[r][1] = rok[r] ? __bfloat162float(cpb[3 * o]) : 0.f;
+      v[r][2] = rok[r] ? __bfloat162float(cpb[3 * o + C]) : 0.f;
+      v[r][3] = rok[r] ? __bfloat162float(cpb[3 * o + 2 * C]) : 0.f;
+    } else {
+      v[r][1] = rok[r] ? __ldcg(cp + 3 * o) : 0.f;
+      v[r][2] = rok[r] ? __ldcg(cp + 3 * o + C) : 0.f;
+      v[r][3] = rok[r] ? __ldcg(cp + 3 * o + 2 * C) : 0.f;
+    }
     v[r][4] = rok[r] ? __ldg(tsp + r) : 0.f;
   }
 }
 
+// A ring slot as the consumer's value: components 1-3 of a bf16 cache hold the channel pair
+// (ch & ~1, ch | 1); bf16 -> fp32 puts the 16 bits in the upper half.
+template <bool BF>
+__device__ __forceinline__ float ring_value(float slot, int c, int ch) {
+  if (!BF || c == 0 || c == 4) return slot;
+  const uint32_t u = __float_as_uint(slot);
+  return __uint_as_float((ch & 1) ? (u & 0xffff0000u) : (u << 16));
+}
+
 // RT = 1, 2, 4: rows per cluster fixed at compile time, inputs prefetched into registers.
 // RT = 0: p.R rows (any count), inputs through the cp.async ring.
-template <int CS, int RT>
+// BF: the cache holds bf16 elements (BwdParams::cache_bf16).
+template <int CS, int RT, bool BF>
 // Two CTAs per SM fit (128 registers) wherever the variant allows it without spilling, so a
 // BPTT CTA launched as a dependent of the forward can stage its weights beside a running
 // forward CTA.
@@ -176,7 +200,10 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || (CS == 4 && (RT == 0 
   const int chc = ch < C ? ch : 0;  // padded channels address a valid location
   const size_t t_last = static_cast<size_t>(K - 1) * B + row0;
   const float* dHp = p.dH + t_last * C + chc;
-  const float* cp = p.cache + t_last * 3 * C + chc;
+  // The same cache element as fp32 (cp) or, BF, as bf16 (cpb); only one of them is used.
+  const float* cp = BF ? nullptr : p.cache + t_last * 3 * C + chc;
+  const __nv_bfloat16* cpb =
+      BF ? reinterpret_cast<const __nv_bfloat16*>(p.cache) + t_last * 3 * C + chc : nullptr;
   const float* tsp = p.ts + t_last;
   float* dpp = p.d_pre + (t_last * 4 + gq) * C + chc;  // d_pre of this lane's gate
   const size_t bc = static_cast<size_t>(B) * C;
@@ -221,9 +248,9 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || (CS == 4 && (RT == 0 
           // together with the first chunk of W_h^T.
           grid_dep_wait();
           grid_dep_launch_dependents();
-          load_step_regs<RR>(dHp, cp, tsp, C, rok, cur);
+          load_step_regs<RR, BF>(dHp, cp, cpb, tsp, C, rok, cur);
           dHp -= bc;
-          cp -= 3 * bc;
+          if constexpr (BF) cpb -= 3 * bc; else cp -= 3 * bc;
           tsp -= B;
         }
       }
@@ -269,9 +296,9 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || (CS == 4 && (RT == 0 
     // The ring lives where the W_h^T staging was: start it only now.
     grid_dep_wait();
     grid_dep_launch_dependents();
-    issue_pre(p, pre, K - 1, row0, rank, warp, lane);
+    issue_pre<BF>(p, pre, K - 1, row0, rank, warp, lane);
     cp_async_commit();
-    issue_pre(p, pre, K - 2, row0, rank, warp, lane);
+    issue_pre<BF>(p, pre, K - 2, row0, rank, warp, lane);
     cp_async_commit();
   }
   cluster_sync_all();
@@ -283,15 +310,15 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || (CS == 4 && (RT == 0 
     float nxt[RR][kPreComp];
     if constexpr (RT > 0) {
       if (t >= 1) {  // step t - 1, used one step later
-        load_step_regs<RR>(dHp, cp, tsp, C, rok, nxt);
+        load_step_regs<RR, BF>(dHp, cp, cpb, tsp, C, rok, nxt);
         dHp -= bc;
-        cp -= 3 * bc;
+        if constexpr (BF) cpb -= 3 * bc; else cp -= 3 * bc;
         tsp -= B;
       }
     } else {
       // Ring: step t-2 goes into the slot step t+1 used; every lane of the warp has read it.
       __syncwarp();
-      issue_pre(p, pre, t - 2, row0, rank, warp, lane);
+      issue_pre<BF>(p, pre, t - 2, row0, rank, warp, lane);
       cp_async_commit();
     }
 
@@ -330,7 +357,8 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || (CS == 4 && (RT == 0 
         float v[kPreComp];  // dH, ff1, ff2, gate, ts of (t, b, ch)
 #pragma unroll
         for (int c = 0; c < kPreComp; ++c)
-          v[c] = RT > 0 ? cur[RT > 0 ? rb : 0][c] : pre_t[r * kWarps * 4 * kPreComp + c];
+          v[c] = RT > 0 ? cur[RT > 0 ? rb : 0][c]
+                        : ring_value<BF>(pre_t[r * kWarps * 4 * kPreComp + c], c, ch);
         const float dh = v[0] + delta[rb];
         const float f1 = v[1], f2 = v[2], g = v[3];
         const float ds = dh * (f2 - f1) * g * (1.f - g);
@@ -409,11 +437,15 @@ cudaError_t prepare_k(size_t smem, int* max_active) {
     *max_active = 0;
     return cudaSuccess;
   }
-  auto* kern = cfc_bwd_kernel<CS, RT>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e != cudaSuccess) return e;
+  // The bf16-cache variant has the same launch bounds and shared memory, hence the same
+  // occupancy: both get the attributes, the fp32 one is measured.
+  auto* kern = cfc_bwd_kernel<CS, RT, false>;
+  for (auto* k : {cfc_bwd_kernel<CS, RT, false>, cfc_bwd_kernel<CS, RT, true>}) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CS, 1, 1);
   cfg.blockDim = dim3(kRecThreads, 1, 1);
@@ -437,7 +469,8 @@ cudaError_t launch_k(const BwdParams& p, int n_clusters, size_t smem, cudaStream
   c.stream = s;
   c.pdl = pdl;
   c.cluster = dim3(CS, 1, 1);
-  return launch(c, cfc_bwd_kernel<CS, RT>, p);
+  return p.cache_bf16 ? launch(c, cfc_bwd_kernel<CS, RT, true>, p)
+                      : launch(c, cfc_bwd_kernel<CS, RT, false>, p);
 }
 
 // Row groups of 1, 2 or 4 use the register-prefetch kernels, larger ones the ring kernel.

@@ -253,7 +253,8 @@ __global__ void __launch_bounds__(256) bwd_l2x_split_kernel(const float* __restr
   if (lane == 0) oscale[rank * C + o] = pow2f(-e);
 }
 
-template <int C, int NR>
+// BF: the cache holds bf16 elements (BwdParams::cache_bf16).
+template <int C, int NR, bool BF>
 __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_l2x_kernel(const BwdParams p) {
   using S = XShape<C, NR>;
   constexpr int CS = S::CS;
@@ -388,15 +389,18 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_l2x_kernel(const BwdParam
           ok = dok;
         } else if (t >= 0) {
           // ---- warp 8: this step's inputs towards L2 while the exchange runs (per row the
-          // CTA's 128-byte slices of dH and of the three cache planes, and ts) ----
+          // CTA's 128-byte slices of dH and of the three cache planes (64 bytes in bf16), and
+          // ts) ----
           for (int j = lane; j < 5 * NR; j += 32) {
             const int b = row0 + j / 5, kind = j % 5;
             if (b < B) {
               const size_t tb = static_cast<size_t>(t) * B + b;
+              const size_t ce = (tb * 3 + (kind - 1)) * C + kChan * rank;  // cache element
               prefetch_l2(kind == 0   ? static_cast<const void*>(p.dH + tb * C + kChan * rank)
                           : kind == 4 ? static_cast<const void*>(p.ts + tb)
-                                      : static_cast<const void*>(p.cache + (tb * 3 + (kind - 1)) * C +
-                                                                 kChan * rank));
+                          : BF
+                              ? static_cast<const void*>(reinterpret_cast<const __nv_bfloat16*>(p.cache) + ce)
+                              : static_cast<const void*>(p.cache + ce));
             }
           }
         }
@@ -431,10 +435,19 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_l2x_kernel(const BwdParam
           for (int i = 0; i < 4; ++i) {
             const size_t tb = static_cast<size_t>(tt) * B + (rv[i] ? row0 + rr[i] : 0);
             dHv[i] = __ldcg(reinterpret_cast<const float2*>(p.dH + tb * C + ch));
-            const float* cpp = p.cache + tb * 3 * C + ch;
-            f1[i] = __ldcg(reinterpret_cast<const float2*>(cpp));
-            f2[i] = __ldcg(reinterpret_cast<const float2*>(cpp + C));
-            gg[i] = __ldcg(reinterpret_cast<const float2*>(cpp + 2 * C));
+            if constexpr (BF) {  // bf16 pairs of channels (ch, ch + 1)
+              const unsigned int* cq = reinterpret_cast<const unsigned int*>(
+                  reinterpret_cast<const __nv_bfloat16*>(p.cache) + tb * 3 * C + ch);
+              const unsigned int a = __ldcg(cq), b2 = __ldcg(cq + C / 2), c2 = __ldcg(cq + C);
+              f1[i] = make_float2(__uint_as_float(a << 16), __uint_as_float(a & 0xffff0000u));
+              f2[i] = make_float2(__uint_as_float(b2 << 16), __uint_as_float(b2 & 0xffff0000u));
+              gg[i] = make_float2(__uint_as_float(c2 << 16), __uint_as_float(c2 & 0xffff0000u));
+            } else {
+              const float* cpp = p.cache + tb * 3 * C + ch;
+              f1[i] = __ldcg(reinterpret_cast<const float2*>(cpp));
+              f2[i] = __ldcg(reinterpret_cast<const float2*>(cpp + C));
+              gg[i] = __ldcg(reinterpret_cast<const float2*>(cpp + 2 * C));
+            }
             tsv[i] = __ldg(p.ts + tb);
           }
           float2 delta[4];
@@ -577,9 +590,12 @@ cudaError_t prepare_k(int* max_active_clusters) {
     *max_active_clusters = 0;
     return cudaSuccess;
   }
-  auto* kern = cfc_bwd_l2x_kernel<C, NR>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
-  if (e != cudaSuccess) return e;
+  // Both cache dtypes: same launch bounds and shared memory, so the same occupancy.
+  auto* kern = cfc_bwd_l2x_kernel<C, NR, false>;
+  for (auto* k : {cfc_bwd_l2x_kernel<C, NR, false>, cfc_bwd_l2x_kernel<C, NR, true>}) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(S::CS, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -604,7 +620,8 @@ cudaError_t launch_k(const BwdParams& p, cudaStream_t s, bool pdl) {
   c.stream = s;
   c.pdl = pdl;
   c.cluster = dim3(S::CS, 1, 1);
-  return launch(c, cfc_bwd_l2x_kernel<C, NR>, p);
+  return p.cache_bf16 ? launch(c, cfc_bwd_l2x_kernel<C, NR, true>, p)
+                      : launch(c, cfc_bwd_l2x_kernel<C, NR, false>, p);
 }
 
 template <int C>

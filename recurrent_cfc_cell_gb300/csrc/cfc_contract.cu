@@ -366,11 +366,12 @@ __device__ __forceinline__ void put8(uint8_t* row, int pitch, int col, const flo
 // z rows [u ; h_{t-1} ; 1] (h_{-1} = h0) and W_u^T rows (wt[k][m] = W[m][k]) in the operand form,
 // eight columns per item.  Columns past the valid ones are written as zeros up to the next
 // multiple of 8 (the pitches are multiples of 8); the contraction never reads beyond them.
-template <int FORM>
-__global__ void build_operands_kernel(const float* __restrict__ u, const float* __restrict__ H,
-                                      const float* __restrict__ h0, const float* __restrict__ W,
-                                      int B, int BK, int C, int n_x, uint8_t* z, int zp,
-                                      uint8_t* wt, int mp) {
+// HB: H holds bf16 elements.
+template <int FORM, bool HB>
+__global__ void build_operands_kernel(const float* __restrict__ u, const void* __restrict__ H,
+                                      const float* __restrict__ h0,
+                                      const float* __restrict__ W, int B, int BK, int C, int n_x,
+                                      uint8_t* z, int zp, uint8_t* wt, int mp) {
   // u, H, h0 and W are complete when this kernel starts: it follows either nothing of the same
   // call, or a kernel that releases its dependents only after its own dependency wait (the
   // BPTT recurrence, the d_pre split).  So the build runs beside that kernel and waits for it
@@ -387,13 +388,28 @@ __global__ void build_operands_kernel(const float* __restrict__ u, const float* 
     float v[8];
     if (i < z_items) {
       const int r = static_cast<int>(i / zg), c0 = 8 * static_cast<int>(i - static_cast<long long>(r) * zg);
-      const float* hrow = r < B ? h0 + static_cast<size_t>(r) * C : H + static_cast<size_t>(r - B) * C;
+      // h_{t-1}: h0 for the first step, else the previous step's row of H (fp32 or bf16).
+      const float* hrow = r < B ? h0 + static_cast<size_t>(r) * C
+                                : static_cast<const float*>(H) + static_cast<size_t>(r - B) * C;
+      if constexpr (HB) {
+        const __nv_bfloat16* hrow16 =
+            static_cast<const __nv_bfloat16*>(H) + static_cast<size_t>(r < B ? 0 : r - B) * C;
+        const bool from_h0 = r < B;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int n = c0 + e;
-        v[e] = n < n_x ? __ldg(u + static_cast<size_t>(r) * n_x + n)
-             : n < n_in ? __ldg(hrow + (n - n_x))
-             : n == n_in ? 1.f : 0.f;
+        for (int e = 0; e < 8; ++e) {
+          const int n = c0 + e;
+          v[e] = n < n_x ? __ldg(u + static_cast<size_t>(r) * n_x + n)
+               : n < n_in ? (from_h0 ? __ldg(hrow + (n - n_x)) : __bfloat162float(hrow16[n - n_x]))
+               : n == n_in ? 1.f : 0.f;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int n = c0 + e;
+          v[e] = n < n_x ? __ldg(u + static_cast<size_t>(r) * n_x + n)
+               : n < n_in ? __ldg(hrow + (n - n_x))
+               : n == n_in ? 1.f : 0.f;
+        }
       }
       put8<FORM>(z + static_cast<size_t>(r) * 4 * zp, zp, c0, v);
     } else {
@@ -662,7 +678,8 @@ LaunchCfg grid_stride_cfg(long long items, cudaStream_t s, bool pdl) {
 }
 }  // namespace
 
-cudaError_t build_operands_launch(int form, const float* u, const float* H, const float* h0,
+cudaError_t build_operands_launch(int form, const float* u, const void* H, int h_bf16,
+                                  const float* h0,
                                   const float* W, int B, int K, int C, int n_x, void* z, void* wt,
                                   cudaStream_t s, bool pdl) {
   const int BK = B * K;
@@ -673,13 +690,17 @@ cudaError_t build_operands_launch(int form, const float* u, const float* H, cons
   const int zp = contract_z_pitch(n_x + C, form), mp = contract_wt_pitch(C);
   uint8_t* z8 = static_cast<uint8_t*>(z);
   uint8_t* w8 = static_cast<uint8_t*>(wt);
+  if (h_bf16) {  // the bf16-state backward: single-pass bf16 operands only
+    if (form != kFormBf16) return cudaErrorInvalidValue;
+    return launch(c, build_operands_kernel<kFormBf16, true>, u, H, h0, W, B, BK, C, n_x, z8, zp, w8, mp);
+  }
   switch (form) {
     case kFormBf16x2:
-      return launch(c, build_operands_kernel<kFormBf16x2>, u, H, h0, W, B, BK, C, n_x, z8, zp, w8, mp);
+      return launch(c, build_operands_kernel<kFormBf16x2, false>, u, H, h0, W, B, BK, C, n_x, z8, zp, w8, mp);
     case kFormBf16:
-      return launch(c, build_operands_kernel<kFormBf16>, u, H, h0, W, B, BK, C, n_x, z8, zp, w8, mp);
+      return launch(c, build_operands_kernel<kFormBf16, false>, u, H, h0, W, B, BK, C, n_x, z8, zp, w8, mp);
     default:
-      return launch(c, build_operands_kernel<kFormTf32>, u, H, h0, W, B, BK, C, n_x, z8, zp, w8, mp);
+      return launch(c, build_operands_kernel<kFormTf32, false>, u, H, h0, W, B, BK, C, n_x, z8, zp, w8, mp);
   }
 }
 

@@ -37,6 +37,8 @@
 //     the serial chain);
 //   * the W_h block of the CTA is read coalesced into shared memory in the prologue and from
 //     there into registers.
+#include <cuda_bf16.h>
+
 #include "cfc_kernels.h"
 #include "cfc_launch.cuh"
 #include "cfc_ptx.cuh"
@@ -72,7 +74,8 @@ __device__ __forceinline__ int hpos(int j) {
   return (j / S::HS) * S::HSP + (j % S::HS);
 }
 
-template <int CS, int R>
+// BF: H and the cache are stored as bf16 (FwdParams::out_bf16), X read from xH / xcache.
+template <int CS, int R, bool BF>
 __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || R >= 8) ? 1 : 2) cfc_fwd_kernel(const FwdParams p) {
   using S = FwdShape<CS>;
   extern __shared__ __align__(16) float smem[];
@@ -100,10 +103,14 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || R >= 8) ? 1 : 2) cfc_
   const int chc = ch < C ? ch : 0;  // padded channels read a valid location
   const size_t xrow = (g == 0) ? static_cast<size_t>(C) : 3ull * C;
   const size_t srow = (sl == 0) ? static_cast<size_t>(C) : 3ull * C;
-  const float* xp = ((g == 0) ? p.H : p.cache + static_cast<size_t>(g - 1) * C) + chc +
+  const float* xp = ((g == 0) ? p.xH : p.xcache + static_cast<size_t>(g - 1) * C) + chc +
                     static_cast<size_t>(row0) * xrow;
-  float* sp = ((sl == 0) ? p.H : p.cache + static_cast<size_t>(sl > 0 && sl < 4 ? sl - 1 : 0) * C) +
-              chc + static_cast<size_t>(row0) * srow;
+  // Output of this lane: element offset `so` in H (sl == 0) or in the cache (ff1, ff2, gate),
+  // fp32 or bf16.
+  const bool to_h = sl == 0;
+  size_t so = static_cast<size_t>(to_h ? 0 : sl > 0 && sl < 4 ? sl - 1 : 0) * C + chc +
+              static_cast<size_t>(row0) * srow;
+  constexpr bool obf = BF;
   const float* tsp = p.ts + row0;
   const size_t xstep = static_cast<size_t>(B) * xrow, sstep = static_cast<size_t>(B) * srow;
   bool xok[R], sok[R], rok[R];
@@ -294,8 +301,14 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || R >= 8) ? 1 : 2) cfc_
                      hq[r].y, hq[r].z, hq[r].w, pbar);
 #pragma unroll
     for (int r = 0; r < R; ++r)
-      if (sok[r]) sp[r * srow] = sv[r];
-    sp += sstep;
+      if (sok[r]) {
+        const size_t o = so + r * srow;
+        if constexpr (obf)
+          reinterpret_cast<__nv_bfloat16*>(to_h ? p.H : p.cache)[o] = __float2bfloat16_rn(sv[r]);
+        else
+          (to_h ? p.H : p.cache)[o] = sv[r];
+      }
+    so += sstep;
     if (t + 1 < K) {
 #pragma unroll
       for (int r = 0; r < R; ++r) {
@@ -320,11 +333,15 @@ cudaError_t prepare_k(size_t smem, int* max_active) {
     *max_active = 0;
     return cudaSuccess;
   }
-  auto* kern = cfc_fwd_kernel<CS, R>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e != cudaSuccess) return e;
+  // The bf16-output variant has the same launch bounds and shared memory, hence the same
+  // occupancy: both get the attributes, the fp32 one is measured.
+  auto* kern = cfc_fwd_kernel<CS, R, false>;
+  for (auto* k : {cfc_fwd_kernel<CS, R, false>, cfc_fwd_kernel<CS, R, true>}) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CS, 1, 1);
   cfg.blockDim = dim3(kRecThreads, 1, 1);
@@ -348,7 +365,8 @@ cudaError_t launch_k(const FwdParams& p, int n_clusters, size_t smem, cudaStream
   c.stream = s;
   c.pdl = pdl;
   c.cluster = dim3(CS, 1, 1);
-  return launch(c, cfc_fwd_kernel<CS, R>, p);
+  return p.out_bf16 ? launch(c, cfc_fwd_kernel<CS, R, true>, p)
+                    : launch(c, cfc_fwd_kernel<CS, R, false>, p);
 }
 
 template <int CS>

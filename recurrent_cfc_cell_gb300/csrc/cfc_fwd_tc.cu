@@ -29,6 +29,7 @@
 // guards both buffer reuses: the other CTAs' slabs landing in this CTA's h buffer, and the
 // next overwrite of this CTA's own slab (a source of its copies).  Every wait is bounded; a
 // timeout is recorded in the status word and the CTAs leave the loop together.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "cfc_kernels.h"
@@ -169,7 +170,7 @@ __device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
   return r != 0;
 }
 
-template <int CS, int NR>
+template <int CS, int NR, bool BF>
 __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdParams p) {
   using S = TcShape<CS, NR>;
   constexpr int HR = S::HR;
@@ -325,10 +326,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
     }
   } else {
     // ================= epilogue warps =================
-    // X of (gate g, channel ch) for rows row0 + HR hh + i, i < HR, of step t, in place in H
-    // (gate 0) or cache (gates 1-3).
+    // X of (gate g, channel ch) for rows row0 + HR hh + i, i < HR, of step t, in the layout of
+    // H (gate 0) or cache (gates 1-3): in place there unless the outputs are bf16.
     const size_t xrow = (g == 0) ? static_cast<size_t>(C) : 3ull * C;
-    const float* xbase = ((g == 0) ? p.H : p.cache + static_cast<size_t>(g - 1) * C) + ch;
+    const float* xbase = ((g == 0) ? p.xH : p.xcache + static_cast<size_t>(g - 1) * C) + ch;
+    constexpr bool obf = BF;  // H and the cache stored as bf16
     const int rfirst = row0 + HR * hh;
     int nvalid = B - rfirst;
     nvalid = nvalid < 0 ? 0 : (nvalid > HR ? HR : nvalid);
@@ -346,8 +348,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
       tc_fence_after_sync();
       if (ok) {
         const float* tsr = ts_s + (t & 1) * NR + HR * hh;
-        float* hout = p.H + (static_cast<size_t>(t) * B + rfirst) * C + ch;
-        float* cout = p.cache + (static_cast<size_t>(t) * B + rfirst) * 3 * C + ch;
+        const size_t ho = (static_cast<size_t>(t) * B + rfirst) * C + ch;  // element offsets
+        const size_t co = (static_cast<size_t>(t) * B + rfirst) * 3 * C + ch;
         const uint32_t dq = tmem + (static_cast<uint32_t>(32 * q) << 16) + HR * hh;
         // Rows ibase .. ibase + n - 1 of this warp half (n = 16, or 8 for the tail of 72).
         auto rows = [&](float (&P)[16], int ibase, int n) {
@@ -377,11 +379,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
             const float gt = sigmoid_fast(fmaf(v[2], tsr[ri], v[3]));
             const float h = ff1 * (1.f - gt) + gt * ff2;
             if (ri < nvalid) {
-              hout[static_cast<size_t>(ri) * C] = h;
-              float* cp = cout + static_cast<size_t>(ri) * 3 * C;
-              cp[0] = ff1;
-              cp[C] = ff2;
-              cp[2 * C] = gt;
+              const size_t hi = ho + static_cast<size_t>(ri) * C;
+              const size_t ci = co + static_cast<size_t>(ri) * 3 * C;
+              if constexpr (obf) {
+                __nv_bfloat16* hb16 = reinterpret_cast<__nv_bfloat16*>(p.H);
+                __nv_bfloat16* cb16 = reinterpret_cast<__nv_bfloat16*>(p.cache);
+                hb16[hi] = __float2bfloat16_rn(h);
+                cb16[ci] = __float2bfloat16_rn(ff1);
+                cb16[ci + C] = __float2bfloat16_rn(ff2);
+                cb16[ci + 2 * C] = __float2bfloat16_rn(gt);
+              } else {
+                p.H[hi] = h;
+                p.cache[ci] = ff1;
+                p.cache[ci + C] = ff2;
+                p.cache[ci + 2 * C] = gt;
+              }
             }
             const Split2 sp = split2(h);
             uint8_t* dst = hb + hterm_offset<NR>(HR * hh + ri, ch);
@@ -435,9 +447,12 @@ cudaError_t prepare_k(int* max_active) {
     *max_active = 0;
     return cudaSuccess;
   }
-  auto* kern = cfc_fwd_tc_kernel<CS, NR>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
+  // Both output dtypes: same launch bounds and shared memory, so the same occupancy.
+  auto* kern = cfc_fwd_tc_kernel<CS, NR, false>;
+  for (auto* k : {cfc_fwd_tc_kernel<CS, NR, false>, cfc_fwd_tc_kernel<CS, NR, true>}) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CS, 1, 1);
   cfg.blockDim = dim3(kTcThreads, 1, 1);
@@ -461,7 +476,8 @@ cudaError_t launch_k(const FwdParams& p, cudaStream_t s, bool pdl) {
   c.stream = s;
   c.pdl = pdl;
   c.cluster = dim3(CS, 1, 1);
-  return launch(c, cfc_fwd_tc_kernel<CS, NR>, p);
+  return p.out_bf16 ? launch(c, cfc_fwd_tc_kernel<CS, NR, true>, p)
+                    : launch(c, cfc_fwd_tc_kernel<CS, NR, false>, p);
 }
 
 }  // namespace

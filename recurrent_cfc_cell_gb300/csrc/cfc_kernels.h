@@ -23,8 +23,13 @@ struct FwdParams {
   const float* W;      // [4][C][n_in]
   const float* bias;   // [4][C]
   const float* ts;     // [K][B]
-  float* H;            // [K][B][C]
-  float* cache;        // [K][B][3][C]  (ff1, ff2, gate)
+  float* H;            // [K][B][C]              (bf16 elements when out_bf16)
+  float* cache;        // [K][B][3][C]  (ff1, ff2, gate; bf16 elements when out_bf16)
+  // X = W_u u + b in the layouts of H (gate 0) and cache (gates 1-3), fp32: the same arrays as
+  // H / cache (written there in place by the projection) unless the outputs are bf16.
+  const float* xH;
+  const float* xcache;
+  int out_bf16;        // H and cache are stored as bf16 (round to nearest even)
   int* status;         // device status word
   int B, K, C, n_x, n_in;
   int CS;              // CTAs per cluster
@@ -46,6 +51,7 @@ struct BwdParams {
   // contraction's operand rows (4 * dpitch bytes per row: hi, then lo) at d_pre.
   int dplanes;
   int dpitch;
+  int cache_bf16;      // the cache holds bf16 elements
   float* xbuf;         // bwd_l2x_launch: the clusters' exchange blocks (bwd_l2x_ws_bytes)
 };
 
@@ -137,10 +143,11 @@ ContractPlan du_contract_plan(int B, int K, int C, int n_x, int form, int smem_b
 void contract_plans(int B, int K, int C, int n_x, int form, int smem_budget, ContractPlan* pw,
                     ContractPlan* pu);
 cudaError_t contract_prepare(int max_smem);
-// z rows [u ; h_{t-1} ; 1] (B*K of them) and W_u^T rows (n_x) in the operand form.
-cudaError_t build_operands_launch(int form, const float* u, const float* H, const float* h0,
-                                  const float* W, int B, int K, int C, int n_x, void* z, void* wt,
-                                  cudaStream_t s, bool pdl);
+// z rows [u ; h_{t-1} ; 1] (B*K of them) and W_u^T rows (n_x) in the operand form; H is fp32,
+// or bf16 when h_bf16.
+cudaError_t build_operands_launch(int form, const float* u, const void* H, int h_bf16,
+                                  const float* h0, const float* W, int B, int K, int C, int n_x,
+                                  void* z, void* wt, cudaStream_t s, bool pdl);
 // fp32 d_pre [B*K][4C] -> the bf16 operand rows (may be in place when the pitch is 4C).
 cudaError_t split_dpre_launch(int form, const float* d_pre, int BK, int C, void* planes,
                               cudaStream_t s, bool pdl);

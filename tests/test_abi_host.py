@@ -229,3 +229,22 @@ def test_weight_grad_rejects_an_unsafe_in_place_d_pre(lib):
 def test_workspace_bytes_per_mode(lib, mode):
     rc, n = ws_bytes(lib, 32, 64, 128, 48, mode)
     assert rc == OK and n >= 32 * 64 * 4 * 128 * 4
+
+
+def test_bf16_state_argument_checks(lib):
+    """The bf16-state entry points: workspace size (X of every step in fp32: [K][B][C] padded
+    to 256 bytes, then [K][B][3][C]), odd C and missing pointers refused before any launch."""
+    out = ctypes.c_size_t(0)
+    assert lib.cfc_forward_bf16_workspace_bytes(4, 8, 32, 16, ctypes.byref(out)) == OK
+    assert out.value == -(-(8 * 4 * 32 * 4) // 256) * 256 + 8 * 4 * 3 * 32 * 4
+    assert lib.cfc_forward_bf16_workspace_bytes(4, 8, 33, 16, ctypes.byref(out)) == INVALID_DIM
+    assert lib.cfc_forward_bf16_workspace_bytes(4, 8, 32, 16, None) == NULL_PTR
+    f = ctypes.c_void_p(0x10000)
+    big = ctypes.c_size_t(1 << 30)
+    assert lib.cfc_forward_bf16(*([f] * 5), 4, 8, 33, 16, f, f, f, big, None) == INVALID_DIM
+    assert lib.cfc_forward_bf16(*([f] * 5), 4, 8, 32, 16, None, f, f, big, None) == NULL_PTR
+    assert lib.cfc_forward_bf16(*([f] * 5), 4, 8, 32, 16, f, f, f, ctypes.c_size_t(16),
+                                None) == WS_TOO_SMALL
+    assert lib.cfc_backward_bf16(*([f] * 7), 4, 8, 33, 16, *([f] * 5), big, None) == INVALID_DIM
+    assert lib.cfc_backward_bf16(*([f] * 5), None, f, 4, 8, 32, 16, *([f] * 5), big,
+                                 None) == NULL_PTR
