@@ -111,3 +111,66 @@ def make_inputs(w: Workload) -> dict:
     return {"u": np.ascontiguousarray(u), "h0": np.ascontiguousarray(h0),
             "W": np.ascontiguousarray(W), "b": np.ascontiguousarray(b),
             "ts": np.ascontiguousarray(ts), "dH": np.ascontiguousarray(dH)}
+
+
+# ---- the pages' own leaky (tau-decay) cell ----
+#
+# Its backward names grad_w_in [B,128,128], grad_w_rec [B,128,128], grad_b and grad_tau [B,128]
+# (page "K-loop Parallelization -- Block-per-Batch Kernel Refactor", section "Per-Kernel
+# Breakdown"), so the pages' shape is 128 inputs and 128 hidden units at B = 32 over 64 steps.
+# Readings: W = [W_in | W_rec] is one [C, n_x + C] matrix, U(-1/sqrt(n_in), 1/sqrt(n_in)) like
+# the four-gate cell's; tau (a time constant per hidden unit, positive) is U(0.5, 4); ts, x, h0,
+# b and dH follow the four-gate workloads.  Draw order: W, b, tau, h0, x, ts, dH.
+# Layouts: x [K, B, n_x], h0 [B, C], W [C, n_x + C], b [C], tau [C], ts [K, B], dH [K, B, C].
+
+@dataclasses.dataclass(frozen=True)
+class DecayWorkload:
+    """Shape and value distributions of one synthetic workload of the tau-decay cell."""
+
+    name: str
+    B: int
+    K: int
+    n_x: int
+    C: int
+    seed: int
+    tau_range: tuple = (0.5, 4.0)
+    ts_range: tuple = (0.5, 2.0)
+
+    @property
+    def n_in(self) -> int:
+        return self.n_x + self.C
+
+    @property
+    def units(self) -> int:
+        return self.B * self.K
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "B": self.B, "K": self.K, "n_x": self.n_x, "C": self.C,
+                "seed": self.seed, "cell": "tau-decay"}
+
+
+DECAY_CONFIGS = [
+    DecayWorkload("decay_tiny_B4_K8_nx16_C32", B=4, K=8, n_x=16, C=32, seed=10),
+    DecayWorkload("decay_pages_B32_K64_nx128_C128", B=32, K=64, n_x=128, C=128, seed=11),
+    DecayWorkload("decay_batch_B256_K64_nx128_C128", B=256, K=64, n_x=128, C=128, seed=12),
+]
+
+
+def decay_custom(B: int, K: int, n_x: int, C: int, seed: int = 17, **kw) -> DecayWorkload:
+    return DecayWorkload(f"decay_custom_B{B}_K{K}_nx{n_x}_C{C}", B=B, K=K, n_x=n_x, C=C,
+                         seed=seed, **kw)
+
+
+def make_decay_inputs(w: DecayWorkload) -> dict:
+    """Draw x, h0, W, b, tau, ts, dH for the tau-decay workload ``w`` (fp32, C-contiguous)."""
+    rng = np.random.default_rng(w.seed)
+    B, K, n_x, C, n_in = w.B, w.K, w.n_x, w.C, w.n_in
+    lim = 1.0 / math.sqrt(n_in)
+    W = rng.uniform(-lim, lim, size=(C, n_in)).astype(np.float32)
+    b = rng.normal(0.0, 0.01, size=C).astype(np.float32)
+    tau = rng.uniform(w.tau_range[0], w.tau_range[1], size=C).astype(np.float32)
+    h0 = rng.normal(0.0, 0.1, size=(B, C)).astype(np.float32)
+    x = rng.normal(0.0, 1.0, size=(K, B, n_x)).astype(np.float32)
+    ts = rng.uniform(w.ts_range[0], w.ts_range[1], size=(K, B)).astype(np.float32)
+    dH = rng.normal(0.0, 1.0, size=(K, B, C)).astype(np.float32)
+    return {"x": x, "h0": h0, "W": W, "b": b, "tau": tau, "ts": ts, "dH": dH}
