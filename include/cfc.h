@@ -213,6 +213,50 @@ int cfc_backward_bf16(const float* dH, const float* u, const float* h0, const fl
                       size_t ws_bytes, cfc_stream_t stream);
 
 /*
+ * The pages' own leaky (tau-decay) cell.  Page "K-loop Parallelization -- Block-per-Batch
+ * Kernel Refactor" names its backward's gradients grad_w_in, grad_w_rec, grad_b and grad_tau
+ * (section "Per-Kernel Breakdown") and a per-block decay vector sdecay (section "Large
+ * shared-mem note"), without equations.  The cell computed (a reading of those names):
+ *
+ *     a_t = W [x_t ; h_{t-1}] + b,  e_t = tanh(a_t),  d_t = exp(-ts[t][b] / tau),
+ *     h_t = d_t * h_{t-1} + (1 - d_t) * e_t            (per hidden unit; h_{-1} = h0)
+ *
+ * with the exact gradients dW (= [dW_in | dW_rec]), db, dtau, dx and dh0 of L = sum dH * H.
+ * Sizes: 1 <= C <= 128 hidden units, 1 <= n_x <= 512 inputs; every tau must be positive.
+ * Layouts: x [K][B][n_x], h0 [B][C], W [C][n_x + C], b [C], tau [C], ts [K][B],
+ * H and E [K][B][C] (E = tanh(a_t), read by the backward), dH [K][B][C], dW [C][n_x + C],
+ * db [C], dtau [C], dx [K][B][n_x], dh0 [B][C].
+ */
+
+/*
+ * cfc_decay_forward -- the K-step forward of the tau-decay cell: the input projection
+ * W_in x_t + b for every step at once (written into E), then one persistent launch of the
+ * recurrence, which overwrites E with tanh(a_t) and writes H.  Returns the argument codes of
+ * cfc_forward (CFC_ERR_INVALID_DIM also for C > 128).
+ */
+int cfc_decay_forward(const float* x, const float* h0, const float* W, const float* b,
+                      const float* tau, const float* ts, int B, int K, int C, int n_x, float* H,
+                      float* E, cfc_stream_t stream);
+
+/*
+ * cfc_decay_workspace_bytes -- device workspace cfc_decay_backward needs (the gradients of
+ * the pre-activations as contraction operand rows, the contraction's other operands and split
+ * partial sums, and per-row dtau sums).  Returns CFC_OK, CFC_ERR_INVALID_DIM or CFC_ERR_NULL_PTR.
+ */
+int cfc_decay_workspace_bytes(int B, int K, int C, int n_x, size_t* bytes);
+
+/*
+ * cfc_decay_backward -- BPTT of the tau-decay cell, then dW and db as one dense contraction
+ * over the B*K rows on the tensor cores (two bf16 terms per operand, three products, as
+ * CFC_DW_ACCURATE), dx as a second one, and dtau as a fixed-order sum over the batch rows.
+ * dx may be NULL.  Outputs are overwritten.  Returns the codes of cfc_backward.
+ */
+int cfc_decay_backward(const float* dH, const float* x, const float* h0, const float* W,
+                       const float* tau, const float* ts, const float* H, const float* E, int B,
+                       int K, int C, int n_x, float* dW, float* db, float* dtau, float* dx,
+                       float* dh0, void* ws, size_t ws_bytes, cfc_stream_t stream);
+
+/*
  * cfc_backward_recurrence -- the first stage of cfc_backward alone: the reverse-time
  * recurrence, writing the pre-activation gradients and dh0.
  *   dH, W, ts, cache   as for cfc_backward

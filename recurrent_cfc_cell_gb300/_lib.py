@@ -34,7 +34,8 @@ EXPORTED = ("cfc_workspace_bytes", "cfc_forward", "cfc_backward", "cfc_backward_
             "cfc_step_launches", "cfc_forward_backward", "cfc_bptt_workspace_bytes",
             "cfc_backward_recurrence_ws", "cfc_wait_self_test", "cfc_probe_fma",
             "cfc_probe_l2_read", "cfc_forward_bf16_workspace_bytes", "cfc_forward_bf16",
-            "cfc_backward_bf16")
+            "cfc_backward_bf16", "cfc_decay_forward", "cfc_decay_workspace_bytes",
+            "cfc_decay_backward")
 CFC_ERR_SCRATCH_LIMIT = -10
 NOALLOC_SCRATCH_BYTES = 32 << 20  # size of cfc_backward_noalloc's built-in device scratch
 
@@ -101,6 +102,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.cfc_forward_bf16.restype = i
     lib.cfc_backward_bf16.argtypes = [vp] * 7 + [i] * 4 + [vp] * 5 + [sz, vp]
     lib.cfc_backward_bf16.restype = i
+    lib.cfc_decay_forward.argtypes = [vp] * 6 + [i] * 4 + [vp, vp, vp]
+    lib.cfc_decay_forward.restype = i
+    lib.cfc_decay_workspace_bytes.argtypes = [i] * 4 + [ctypes.POINTER(sz)]
+    lib.cfc_decay_workspace_bytes.restype = i
+    lib.cfc_decay_backward.argtypes = [vp] * 8 + [i] * 4 + [vp] * 6 + [sz, vp]
+    lib.cfc_decay_backward.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -374,3 +381,38 @@ def cfc_backward_bf16(dH, u, h0, W, ts, H, cache, dW, db, du, dh0, ws, stream=No
         _ptr(db, "db", (4, C)), _ptr(du, "du", (K, B, n_x)), _ptr(dh0, "dh0", (B, C)),
         wp, wn, _stream(stream))
     _check("cfc_backward_bf16", rc)
+
+
+# ---- the pages' tau-decay cell ----
+
+def decay_workspace_bytes(B: int, K: int, C: int, n_x: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("cfc_decay_workspace_bytes",
+           load().cfc_decay_workspace_bytes(B, K, C, n_x, ctypes.byref(out)))
+    return out.value
+
+
+def cfc_decay_forward(x, h0, W, b, tau, ts, H, E, stream=None) -> None:
+    """H [K,B,C] and E = tanh(a) [K,B,C] <- the tau-decay cell over K steps."""
+    K, B, n_x = x.shape
+    C = h0.shape[1]
+    rc = load().cfc_decay_forward(
+        _ptr(x, "x", (K, B, n_x)), _ptr(h0, "h0", (B, C)), _ptr(W, "W", (C, n_x + C)),
+        _ptr(b, "b", (C,)), _ptr(tau, "tau", (C,)), _ptr(ts, "ts", (K, B)), B, K, C, n_x,
+        _ptr(H, "H", (K, B, C)), _ptr(E, "E", (K, B, C)), _stream(stream))
+    _check("cfc_decay_forward", rc)
+
+
+def cfc_decay_backward(dH, x, h0, W, tau, ts, H, E, dW, db, dtau, dx, dh0, ws,
+                       stream=None) -> None:
+    """dW, db, dtau, dx (optional), dh0 <- BPTT of the tau-decay cell."""
+    K, B, n_x = x.shape
+    C = h0.shape[1]
+    wp, wn = _ws(ws)
+    rc = load().cfc_decay_backward(
+        _ptr(dH, "dH", (K, B, C)), _ptr(x, "x", (K, B, n_x)), _ptr(h0, "h0", (B, C)),
+        _ptr(W, "W", (C, n_x + C)), _ptr(tau, "tau", (C,)), _ptr(ts, "ts", (K, B)),
+        _ptr(H, "H", (K, B, C)), _ptr(E, "E", (K, B, C)), B, K, C, n_x,
+        _ptr(dW, "dW", (C, n_x + C)), _ptr(db, "db", (C,)), _ptr(dtau, "dtau", (C,)),
+        _ptr(dx, "dx", (K, B, n_x)), _ptr(dh0, "dh0", (B, C)), wp, wn, _stream(stream))
+    _check("cfc_decay_backward", rc)

@@ -793,3 +793,139 @@ int cfc_device_status(int* status) {
 }
 
 }  // extern "C"
+
+// ---- the pages' tau-decay cell ----
+
+namespace {
+
+// Backward workspace of the decay cell (offsets in bytes): da as bf16 operand rows, z rows,
+// W_in^T rows, per-row dtau sums, then the contractions' split partials.
+struct DecayLayout {
+  int mp, zp, wp, ldo;
+  size_t da_off, z_off, wt_off, dtau_off, part_off, pu_off, total;
+  cfc::ContractPlan pdw, pdu;
+};
+
+DecayLayout decay_layout(int B, int K, int C, int n_x) {
+  DecayLayout L{};
+  const int form = cfc::kFormBf16x2;
+  const size_t BK = static_cast<size_t>(B) * K;
+  const int n_in = n_x + C;
+  L.mp = (C + 7) & ~7;
+  L.wp = L.mp;
+  L.zp = cfc::contract_z_pitch(n_in, form);
+  L.ldo = cfc::dw_tc_pitch(n_in);
+  L.da_off = 0;
+  L.z_off = align256(BK * 4 * L.mp);
+  L.wt_off = align256(L.z_off + BK * 4 * L.zp);
+  L.dtau_off = align256(L.wt_off + static_cast<size_t>(n_x) * 4 * L.wp);
+  L.part_off = align256(L.dtau_off + static_cast<size_t>(B) * C * sizeof(float));
+  cfc::contract_plans_mn(static_cast<int>(BK), C, n_in + 1, n_x, form, kSmemBudget, &L.pdw,
+                         &L.pdu);
+  L.pu_off = static_cast<size_t>(L.pdw.splits) * C * L.ldo;  // floats into the partials
+  size_t part = L.pu_off * sizeof(float);
+  if (L.pdu.splits > 1) part += static_cast<size_t>(L.pdu.splits) * BK * n_x * sizeof(float);
+  L.total = L.part_off + part;
+  return L;
+}
+
+int decay_check(int B, int K, int C, int n_x) {
+  const int rc = check_dims(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (!cfc::decay_supported(C, n_x)) return CFC_ERR_INVALID_DIM;
+  return CFC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cfc_decay_forward(const float* x, const float* h0, const float* W, const float* b,
+                      const float* tau, const float* ts, int B, int K, int C, int n_x, float* H,
+                      float* E, cfc_stream_t stream) {
+  int rc = decay_check(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (!x || !h0 || !W || !b || !tau || !ts || !H || !E) return CFC_ERR_NULL_PTR;
+  if (!aligned16(x) || !aligned16(h0) || !aligned16(W) || !aligned16(b) || !aligned16(tau) ||
+      !aligned16(ts) || !aligned16(H) || !aligned16(E))
+    return CFC_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != CFC_OK) return rc;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = cuda_rc(cfc::decay_proj_launch(x, W, b, B * K, C, n_x, E, s), CFC_ERR_LAUNCH_FAILED);
+  if (rc != CFC_OK) return rc;
+  return cuda_rc(cfc::decay_fwd_launch(h0, W, tau, ts, B, K, C, n_x, H, E, s),
+                 CFC_ERR_LAUNCH_FAILED);
+}
+
+int cfc_decay_workspace_bytes(int B, int K, int C, int n_x, size_t* bytes) {
+  const int rc = decay_check(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (!bytes) return CFC_ERR_NULL_PTR;
+  *bytes = decay_layout(B, K, C, n_x).total;
+  return CFC_OK;
+}
+
+int cfc_decay_backward(const float* dH, const float* x, const float* h0, const float* W,
+                       const float* tau, const float* ts, const float* H, const float* E, int B,
+                       int K, int C, int n_x, float* dW, float* db, float* dtau, float* dx,
+                       float* dh0, void* ws, size_t ws_bytes, cfc_stream_t stream) {
+  int rc = decay_check(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (!dH || !x || !h0 || !W || !tau || !ts || !H || !E || !dW || !db || !dtau || !dh0 || !ws)
+    return CFC_ERR_NULL_PTR;
+  if (!aligned16(dH) || !aligned16(x) || !aligned16(h0) || !aligned16(W) || !aligned16(tau) ||
+      !aligned16(ts) || !aligned16(H) || !aligned16(E) || !aligned16(dW) || !aligned16(db) ||
+      !aligned16(dtau) || (dx && !aligned16(dx)) || !aligned16(dh0) || !aligned16(ws))
+    return CFC_ERR_MISALIGNED;
+  const DecayLayout L = decay_layout(B, K, C, n_x);
+  if (ws_bytes < L.total) return CFC_ERR_WS_TOO_SMALL;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != CFC_OK) return rc;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  const int form = cfc::kFormBf16x2;
+  const int BK = B * K, n_in = n_x + C, N = n_in + 1;
+  float* dtau_part = reinterpret_cast<float*>(w + L.dtau_off);
+  float* partial = reinterpret_cast<float*>(w + L.part_off);
+  // 1. BPTT: da straight into operand rows, dh0, per-row dtau sums.
+  rc = cuda_rc(cfc::decay_bwd_launch(dH, h0, W, tau, ts, H, E, B, K, C, n_x, w + L.da_off, L.mp,
+                                     dh0, dtau_part, s),
+               CFC_ERR_LAUNCH_FAILED);
+  // 2. z rows [x ; h_{t-1} ; 1] and W_in^T rows (W has C rows).
+  if (rc == CFC_OK)
+    rc = cuda_rc(cfc::build_operands_launch(form, x, H, 0, h0, W, B, K, C, n_x, w + L.z_off,
+                                            w + L.wt_off, s, false, C),
+                 CFC_ERR_LAUNCH_FAILED);
+  // 3. dW (with db in the ones column) and dx, one contraction each, dx beside dW.
+  if (rc == CFC_OK)
+    rc = cuda_rc(cfc::dw_contract_launch_mn(L.pdw, form, w + L.da_off, w + L.z_off, BK, C, N,
+                                            L.mp, L.zp, partial, L.ldo, st->status, s, true),
+                 CFC_ERR_LAUNCH_FAILED);
+  float* dx_out = (dx && L.pdu.splits > 1) ? partial + L.pu_off : dx;
+  if (rc == CFC_OK && dx)
+    rc = cuda_rc(cfc::du_contract_launch_mn(L.pdu, form, w + L.da_off, w + L.wt_off, BK, C, n_x,
+                                            L.mp, L.wp, dx_out, st->status, s, true, true),
+                 CFC_ERR_LAUNCH_FAILED);
+  // 4. One merge of the split partials, then dtau over the batch rows.
+  if (rc == CFC_OK) {
+    if (dx && L.pdu.splits > 1)
+      rc = cuda_rc(cfc::reduce_axis0_pair_launch(partial, L.pdw.splits, C * L.ldo, L.ldo, n_in,
+                                                 dW, db, dx_out, L.pdu.splits, BK * n_x, dx, s,
+                                                 true),
+                   CFC_ERR_LAUNCH_FAILED);
+    else
+      rc = cuda_rc(cfc::reduce_axis0_rows_launch(partial, L.pdw.splits, C * L.ldo, L.ldo, n_in,
+                                                 dW, db, s, true),
+                   CFC_ERR_LAUNCH_FAILED);
+  }
+  if (rc == CFC_OK)
+    rc = cuda_rc(cfc::reduce_axis0_launch(dtau_part, B, C, dtau, s, true), CFC_ERR_LAUNCH_FAILED);
+  return rc;
+}
+
+}  // extern "C"

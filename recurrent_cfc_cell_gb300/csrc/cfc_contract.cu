@@ -371,14 +371,14 @@ template <int FORM, bool HB>
 __global__ void build_operands_kernel(const float* __restrict__ u, const void* __restrict__ H,
                                       const float* __restrict__ h0,
                                       const float* __restrict__ W, int B, int BK, int C, int n_x,
-                                      uint8_t* z, int zp, uint8_t* wt, int mp) {
+                                      int M, uint8_t* z, int zp, uint8_t* wt, int mp) {
   // u, H, h0 and W are complete when this kernel starts: it follows either nothing of the same
   // call, or a kernel that releases its dependents only after its own dependency wait (the
   // BPTT recurrence, the d_pre split).  So the build runs beside that kernel and waits for it
   // only at the end, which keeps "this kernel complete" implying "every earlier kernel
   // complete" for the contractions that wait on it.
   grid_dep_launch_dependents();
-  const int n_in = n_x + C, zn = n_in + 1, M = 4 * C;
+  const int n_in = n_x + C, zn = n_in + 1;  // M: the W rows (gate rows) of W_u^T
   const int zg = (zn + 7) / 8, wg = (M + 7) / 8;  // 8-column groups per row
   const long long z_items = static_cast<long long>(BK) * zg;
   const long long total = z_items + static_cast<long long>(n_x) * wg;
@@ -583,10 +583,13 @@ int contract_wt_pitch(int C) { return (4 * C + 7) & ~7; }
 // CTAs fill about one wave of a fixed 148 (a constant, not the device's SM count: the split,
 // hence the summation order, depends only on the sizes).
 ContractPlan dw_contract_plan(int B, int K, int C, int n_x, int form, int smem_budget) {
+  return dw_contract_plan_mn(B * K, 4 * C, n_x + C + 1, form, smem_budget);
+}
+
+ContractPlan dw_contract_plan_mn(int BK, int M, int N, int form, int smem_budget) {
   ContractPlan p{};
   // Column tiles: whole 128-byte atoms for MN-major operands (bf16), multiples of 16 (K-major).
   const int atom = form == kFormTf32 ? 16 : atom_of(form);
-  const int N = n_x + C + 1, M = 4 * C, BK = B * K;
   p.mt = M >= 256 ? 2 : 1;
   p.n_tiles = (N + 255) / 256;
   int nt = (N + p.n_tiles - 1) / p.n_tiles;
@@ -616,14 +619,18 @@ ContractPlan dw_contract_plan(int B, int K, int C, int n_x, int form, int smem_b
 // At most two stages' worth of shared memory per CTA, so two CTAs share an SM and one's set-up
 // and stores overlap the other's copies.
 ContractPlan du_contract_plan(int B, int K, int C, int n_x, int form, int smem_budget) {
+  return du_contract_plan_mn(B * K, 4 * C, n_x, form, smem_budget);
+}
+
+ContractPlan du_contract_plan_mn(int BK, int M, int n_x, int form, int smem_budget) {
   ContractPlan p{};
   const int atom = atom_of(form);
   p.mt = 1;
   p.n_tiles = (n_x + 255) / 256;
   const int nt = (n_x + p.n_tiles - 1) / p.n_tiles;
   p.n_tile = (nt + 15) / 16 * 16;
-  p.m_tiles = (B * K + 127) / 128;
-  p.n_kb = (4 * C + atom - 1) / atom;
+  p.m_tiles = (BK + 127) / 128;
+  p.n_kb = (M + atom - 1) / atom;
   p.kb_per_split = p.n_kb;
   p.splits = 1;
   return finish_plan(p, form, 4, smem_budget / 2 - 1024);
@@ -635,16 +642,21 @@ constexpr int kJointSplitMaxRows = 8192;
 
 void contract_plans(int B, int K, int C, int n_x, int form, int smem_budget, ContractPlan* pw,
                     ContractPlan* pu) {
-  *pw = dw_contract_plan(B, K, C, n_x, form, smem_budget);
-  *pu = du_contract_plan(B, K, C, n_x, form, smem_budget);
-  if (B * K >= kJointSplitMaxRows) return;
+  contract_plans_mn(B * K, 4 * C, n_x + C + 1, n_x, form, smem_budget, pw, pu);
+}
+
+void contract_plans_mn(int BK, int M, int N, int n_x, int form, int smem_budget, ContractPlan* pw,
+                       ContractPlan* pu) {
+  *pw = dw_contract_plan_mn(BK, M, N, form, smem_budget);
+  *pu = du_contract_plan_mn(BK, M, n_x, form, smem_budget);
+  if (BK >= kJointSplitMaxRows) return;
   // One 128-row accumulator per dW CTA, and the smallest common k-blocks-per-split whose CTAs
   // fit a fixed budget of one wave (a constant, not the device's SM count: the splits, hence
   // the summation orders, depend only on the sizes).
   constexpr int kBudget = 148;
   ContractPlan w = *pw;
   w.mt = 1;
-  w.m_tiles = (4 * C + 127) / 128;
+  w.m_tiles = (M + 127) / 128;
   const int tw = w.m_tiles * w.n_tiles, tu = pu->m_tiles * pu->n_tiles;
   int kbps = 1;
   const int kmax = w.n_kb > pu->n_kb ? w.n_kb : pu->n_kb;
@@ -681,26 +693,27 @@ LaunchCfg grid_stride_cfg(long long items, cudaStream_t s, bool pdl) {
 cudaError_t build_operands_launch(int form, const float* u, const void* H, int h_bf16,
                                   const float* h0,
                                   const float* W, int B, int K, int C, int n_x, void* z, void* wt,
-                                  cudaStream_t s, bool pdl) {
+                                  cudaStream_t s, bool pdl, int M) {
   const int BK = B * K;
+  if (M <= 0) M = 4 * C;
   const long long items = static_cast<long long>(BK) * ((n_x + C + 1 + 7) / 8) +
-                          static_cast<long long>(n_x) * ((4 * C + 7) / 8);
+                          static_cast<long long>(n_x) * ((M + 7) / 8);
   LaunchCfg c = grid_stride_cfg(items, s, pdl);
   if (c.grid.x > 2 * 148) c.grid.x = 2 * 148;  // resident beside the kernel it runs next to
-  const int zp = contract_z_pitch(n_x + C, form), mp = contract_wt_pitch(C);
+  const int zp = contract_z_pitch(n_x + C, form), mp = (M + 7) & ~7;  // W_u^T row pitch
   uint8_t* z8 = static_cast<uint8_t*>(z);
   uint8_t* w8 = static_cast<uint8_t*>(wt);
   if (h_bf16) {  // the bf16-state backward: single-pass bf16 operands only
     if (form != kFormBf16) return cudaErrorInvalidValue;
-    return launch(c, build_operands_kernel<kFormBf16, true>, u, H, h0, W, B, BK, C, n_x, z8, zp, w8, mp);
+    return launch(c, build_operands_kernel<kFormBf16, true>, u, H, h0, W, B, BK, C, n_x, M, z8, zp, w8, mp);
   }
   switch (form) {
     case kFormBf16x2:
-      return launch(c, build_operands_kernel<kFormBf16x2, false>, u, H, h0, W, B, BK, C, n_x, z8, zp, w8, mp);
+      return launch(c, build_operands_kernel<kFormBf16x2, false>, u, H, h0, W, B, BK, C, n_x, M, z8, zp, w8, mp);
     case kFormBf16:
-      return launch(c, build_operands_kernel<kFormBf16, false>, u, H, h0, W, B, BK, C, n_x, z8, zp, w8, mp);
+      return launch(c, build_operands_kernel<kFormBf16, false>, u, H, h0, W, B, BK, C, n_x, M, z8, zp, w8, mp);
     default:
-      return launch(c, build_operands_kernel<kFormTf32, false>, u, H, h0, W, B, BK, C, n_x, z8, zp, w8, mp);
+      return launch(c, build_operands_kernel<kFormTf32, false>, u, H, h0, W, B, BK, C, n_x, M, z8, zp, w8, mp);
   }
 }
 
@@ -731,10 +744,17 @@ cudaError_t split_dpre_launch(int form, const float* d_pre, int BK, int C, void*
 cudaError_t dw_contract_launch(const ContractPlan& pl, int form, const void* dpre, const void* z,
                                int B, int K, int C, int n_x, float* partial, int ldo,
                                int* status, cudaStream_t s, bool pdl) {
+  return dw_contract_launch_mn(pl, form, dpre, z, B * K, 4 * C, n_x + C + 1,
+                               contract_m_pitch(C, form), contract_z_pitch(n_x + C, form),
+                               partial, ldo, status, s, pdl);
+}
+
+cudaError_t dw_contract_launch_mn(const ContractPlan& pl, int form, const void* dpre,
+                                  const void* z, int BK, int M, int N, int mp, int zp,
+                                  float* partial, int ldo, int* status, cudaStream_t s,
+                                  bool pdl) {
   const bool f32 = form == kFormTf32;
   const int atom = atom_of(form);
-  const int BK = B * K, M = 4 * C, N = n_x + C + 1;
-  const int mp = contract_m_pitch(C, form), zp = contract_z_pitch(n_x + C, form);
   const uint8_t* d8 = static_cast<const uint8_t*>(dpre);
   const uint8_t* z8 = static_cast<const uint8_t*>(z);
   CUtensorMap a0, a1, b0, b1;
@@ -775,10 +795,16 @@ cudaError_t dw_contract_launch(const ContractPlan& pl, int form, const void* dpr
 cudaError_t du_contract_launch(const ContractPlan& pl, int form, const void* dpre, const void* wt,
                                int B, int K, int C, int n_x, float* du, int* status,
                                cudaStream_t s, bool pdl, bool defer_wait) {
+  return du_contract_launch_mn(pl, form, dpre, wt, B * K, 4 * C, n_x, contract_m_pitch(C, form),
+                               contract_wt_pitch(C), du, status, s, pdl, defer_wait);
+}
+
+cudaError_t du_contract_launch_mn(const ContractPlan& pl, int form, const void* dpre,
+                                  const void* wt, int BK, int M, int n_x, int mp, int wp,
+                                  float* du, int* status, cudaStream_t s, bool pdl,
+                                  bool defer_wait) {
   const bool f32 = form == kFormTf32;
   const int atom = atom_of(form);
-  const int BK = B * K, M = 4 * C;
-  const int mp = contract_m_pitch(C, form), wp = contract_wt_pitch(C);
   const uint8_t* d8 = static_cast<const uint8_t*>(dpre);
   const uint8_t* w8 = static_cast<const uint8_t*>(wt);
   CUtensorMap a0, a1, b0, b1;

@@ -142,12 +142,19 @@ ContractPlan du_contract_plan(int B, int K, int C, int n_x, int form, int smem_b
 // their CTAs fill one wave (du then writes split partials [splits][B*K][n_x]).
 void contract_plans(int B, int K, int C, int n_x, int form, int smem_budget, ContractPlan* pw,
                     ContractPlan* pu);
+// The same with the sizes explicit (the four-gate cell: M = 4C gate rows, N = n_x + C + 1 z
+// columns; the decay cell: M = C): d_pre [BK][M], z [BK][N], W_u^T [n_x][M].
+ContractPlan dw_contract_plan_mn(int BK, int M, int N, int form, int smem_budget);
+ContractPlan du_contract_plan_mn(int BK, int M, int n_x, int form, int smem_budget);
+void contract_plans_mn(int BK, int M, int N, int n_x, int form, int smem_budget,
+                       ContractPlan* pw, ContractPlan* pu);
 cudaError_t contract_prepare(int max_smem);
 // z rows [u ; h_{t-1} ; 1] (B*K of them) and W_u^T rows (n_x) in the operand form; H is fp32,
-// or bf16 when h_bf16.
+// or bf16 when h_bf16.  W has M rows of n_x + C (M <= 0: 4C, the four gates); W_u^T rows are
+// (M + 7) & ~7 values apart.
 cudaError_t build_operands_launch(int form, const float* u, const void* H, int h_bf16,
                                   const float* h0, const float* W, int B, int K, int C, int n_x,
-                                  void* z, void* wt, cudaStream_t s, bool pdl);
+                                  void* z, void* wt, cudaStream_t s, bool pdl, int M = 0);
 // fp32 d_pre [B*K][4C] -> the bf16 operand rows (may be in place when the pitch is 4C).
 cudaError_t split_dpre_launch(int form, const float* d_pre, int BK, int C, void* planes,
                               cudaStream_t s, bool pdl);
@@ -162,6 +169,15 @@ cudaError_t dw_contract_launch(const ContractPlan& pl, int form, const void* dpr
 cudaError_t du_contract_launch(const ContractPlan& pl, int form, const void* dpre, const void* wt,
                                int B, int K, int C, int n_x, float* du, int* status,
                                cudaStream_t s, bool pdl, bool defer_wait);
+// The two contractions with the sizes and operand pitches explicit (mp: d_pre rows, zp: z
+// rows, wp: W_u^T rows; 4 * pitch bytes per row).
+cudaError_t dw_contract_launch_mn(const ContractPlan& pl, int form, const void* dpre,
+                                  const void* z, int BK, int M, int N, int mp, int zp,
+                                  float* partial, int ldo, int* status, cudaStream_t s, bool pdl);
+cudaError_t du_contract_launch_mn(const ContractPlan& pl, int form, const void* dpre,
+                                  const void* wt, int BK, int M, int n_x, int mp, int wp,
+                                  float* du, int* status, cudaStream_t s, bool pdl,
+                                  bool defer_wait);
 
 // du[r][k] = sum_m d_pre[r][m] * W[m][k] for k < n_x (SIMT fp32).
 cudaError_t du_simt_launch(const float* d_pre, const float* W, int BK, int C, int n_x,
@@ -182,6 +198,21 @@ cudaError_t reduce_axis0_pair_launch(const float* in, int n_batch, int n_tail, i
                                      int ncol, float* out, float* out2, const float* in_b,
                                      int n_batch_b, int n_tail_b, float* out_b, cudaStream_t s,
                                      bool pdl);
+// The pages' tau-decay cell (cfc_decay.cu): hidden width at most kDecayMaxC.
+constexpr int kDecayMaxC = 128;
+bool decay_supported(int C, int n_x);
+// X = W_in x + b for the B*K rows, into E [B*K][C].
+cudaError_t decay_proj_launch(const float* x, const float* W, const float* b, int BK, int C,
+                              int n_x, float* E, cudaStream_t s);
+// The K-step recurrence reading X from E and writing H and E = tanh(a).
+cudaError_t decay_fwd_launch(const float* h0, const float* W, const float* tau, const float* ts,
+                             int B, int K, int C, int n_x, float* H, float* E, cudaStream_t s);
+// BPTT: da as bf16 operand rows (2 mp values per row, hi then lo), dh0, per-row dtau sums.
+cudaError_t decay_bwd_launch(const float* dH, const float* h0, const float* W, const float* tau,
+                             const float* ts, const float* H, const float* E, int B, int K,
+                             int C, int n_x, void* da_rows, int mp, float* dh0, float* dtau_part,
+                             cudaStream_t s);
+
 // Row pitch of the tensor-core weight-gradient partials: the n_in columns of z, the all-ones
 // column that yields db, padded to a multiple of 4.
 inline int dw_tc_pitch(int n_in) { return (n_in + 1 + 3) & ~3; }

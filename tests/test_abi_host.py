@@ -248,3 +248,23 @@ def test_bf16_state_argument_checks(lib):
     assert lib.cfc_backward_bf16(*([f] * 7), 4, 8, 33, 16, *([f] * 5), big, None) == INVALID_DIM
     assert lib.cfc_backward_bf16(*([f] * 5), None, f, 4, 8, 32, 16, *([f] * 5), big,
                                  None) == NULL_PTR
+
+
+def test_decay_argument_checks(lib):
+    """The tau-decay entry points: C beyond 128 and missing pointers refused before any launch;
+    the workspace grows with the batch."""
+    out = ctypes.c_size_t(0)
+    assert lib.cfc_decay_workspace_bytes(4, 8, 129, 16, ctypes.byref(out)) == INVALID_DIM
+    assert lib.cfc_decay_workspace_bytes(4, 8, 128, 16, None) == NULL_PTR
+    assert lib.cfc_decay_workspace_bytes(4, 8, 128, 16, ctypes.byref(out)) == OK
+    small = out.value
+    assert lib.cfc_decay_workspace_bytes(40, 8, 128, 16, ctypes.byref(out)) == OK
+    assert out.value > small
+    f = ctypes.c_void_p(0x10000)
+    assert lib.cfc_decay_forward(*([f] * 6), 4, 8, 129, 16, f, f, None) == INVALID_DIM
+    assert lib.cfc_decay_forward(*([f] * 6), 4, 8, 32, 16, None, f, None) == NULL_PTR
+    big = ctypes.c_size_t(1 << 30)
+    assert lib.cfc_decay_backward(*([f] * 8), 4, 8, 32, 16, *([f] * 5), f, ctypes.c_size_t(16),
+                                  None) == WS_TOO_SMALL
+    assert lib.cfc_decay_backward(*([f] * 8), 4, 8, 32, 16, None, *([f] * 4), f, big,
+                                  None) == NULL_PTR
