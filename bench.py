@@ -493,6 +493,115 @@ def bf16_state_record(torch, _lib, w, d, dev, flush, stream, steps: int) -> dict
             "device_status": status}
 
 
+class _DecayStep:
+    """One training step of the pages' tau-decay cell (cfc_decay_forward + cfc_decay_backward)."""
+
+    def __init__(self, torch, _lib, w, d, dev):
+        B, K, C, n_x = w.B, w.K, w.C, w.n_x
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.H = torch.empty((K, B, C), **f32)
+        self.E = torch.empty((K, B, C), **f32)
+        self.out = {"dW": torch.empty((C, n_x + C), **f32), "db": torch.empty((C,), **f32),
+                    "dtau": torch.empty((C,), **f32), "dx": torch.empty((K, B, n_x), **f32),
+                    "dh0": torch.empty((B, C), **f32)}
+        self.ws = torch.empty(_lib.decay_workspace_bytes(B, K, C, n_x), dtype=torch.uint8,
+                              device=dev)
+        self.d, self._lib, self.graph = d, _lib, None
+
+    def forward(self):
+        d = self.d
+        self._lib.cfc_decay_forward(d["x"], d["h0"], d["W"], d["b"], d["tau"], d["ts"], self.H,
+                                    self.E)
+
+    def backward(self):
+        d, o = self.d, self.out
+        self._lib.cfc_decay_backward(d["dH"], d["x"], d["h0"], d["W"], d["tau"], d["ts"], self.H,
+                                     self.E, o["dW"], o["db"], o["dtau"], o["dx"], o["dh0"],
+                                     self.ws)
+
+    def run(self):
+        self.forward()
+        self.backward()
+
+    def capture(self, torch):
+        self.run()
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.run()
+        torch.cuda.current_stream().wait_stream(s)
+        with torch.cuda.graph(self.graph):
+            self.run()
+
+    def replay(self):
+        self.graph.replay()
+
+
+def _timed(torch, fn, flush, stream, n: int) -> float:
+    """Mean ms of fn() over n calls, each after an L2 flush, CUDA events on `stream`."""
+    tot = 0.0
+    for _ in range(n):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        tot += a.elapsed_time(b)
+    return tot / n
+
+
+def decay_record(torch, _lib, inputs, dev, flush, stream, mp, steps: int,
+                 with_parity: bool) -> list:
+    """The pages' tau-decay cell on its pages-shaped and larger-batch workloads: step time
+    (graph replays, L2 flushed), the two stages, the recurrences against the measured FP32 FMA
+    rate, and the oracle comparison of every output on the pages-shaped workload."""
+    recs = []
+    for w in inputs.DECAY_CONFIGS[1:]:
+        inp = inputs.make_decay_inputs(w)
+        d = {k: torch.from_numpy(v).to(dev).contiguous() for k, v in inp.items()}
+        st = _DecayStep(torch, _lib, w, d, dev)
+        st.capture(torch)
+        for _ in range(3):
+            flush.zero_()
+            st.replay()
+        torch.cuda.synchronize()
+        ms = timed_replays(torch, st, flush, stream, steps)
+        fwd_ms = _timed(torch, st.forward, flush, stream, 20)
+        bwd_ms = _timed(torch, st.backward, flush, stream, 20)
+        # Per (b, t) unit: the recurrent mat-vec (2 C^2 flop) in each direction, the projection
+        # (2 C n_x), and the weight and input gradients (2 C (n_in + 1) + 2 C n_x).
+        C, n_x = w.C, w.n_x
+        rec_flop = 2.0 * C * C * w.units
+        peak = mp["fp32_fma_tflops"] if mp else None
+        fwd_tf = rec_flop / (fwd_ms * 1e-3) / 1e12
+        bwd_tf = rec_flop / (bwd_ms * 1e-3) / 1e12
+        rec = {"workload": w.name, "config": w.describe(), "ms_per_step": ms,
+               "value": w.units / (ms * 1e-3), "unit": UNIT, "steps": steps,
+               "stages_ms": {"forward": fwd_ms, "backward": bwd_ms},
+               "recurrence_tflops": {"forward": fwd_tf, "backward": bwd_tf},
+               "fp32_fma_frac": ({"forward": fwd_tf / peak, "backward": bwd_tf / peak}
+                                 if peak else None),
+               "flop_per_unit": {"recurrences": 4.0 * C * C, "projection": 2.0 * C * n_x,
+                                 "gradients": 2.0 * C * (n_x + C + 1) + 2.0 * C * n_x},
+               "device_status": _lib.device_status()}
+        if with_parity and w.units <= 4096:
+            import oracle
+            import oracle.decay
+
+            ref = oracle.decay.step(inp)
+            got = {"H": st.H.cpu().numpy(), "E": st.E.cpu().numpy()}
+            got.update({k: v.cpu().numpy() for k, v in st.out.items()})
+            rec["parity"] = {"max_rel_err": {k: oracle.rel_err(got[k], ref[k]) for k in got},
+                             "metric": "max|x-y| / max|y| per tensor against the fp64 oracle"}
+        recs.append(rec)
+        del st
+        torch.cuda.empty_cache()
+    return recs
+
+
 def outputs_np(st) -> dict:
     out = {k: v.cpu().numpy() for k, v in st.outputs().items()}
     out["d_pre"] = decode_dpre(out["d_pre"], st.C, st.dw_mode)
@@ -695,6 +804,9 @@ def main():
     del ste
     bf16 = bf16_state_record(torch, _lib, w, dinp, dev, flush, stream, min(args.steps, 200))
     status = status or bf16["device_status"]
+    decay = decay_record(torch, _lib, inputs, dev, flush, stream, mp, min(args.steps, 200),
+                         rank == 0 and not args.no_cpu_baseline)
+    status = status or max(r["device_status"] for r in decay)
     largest = None
     if not args.no_largest and w.name != inputs.CONFIGS[4].name:
         modes = [int(m) for m in args.dw_modes.split(",") if m.strip()]
@@ -722,6 +834,7 @@ def main():
             "gpu_launches": launches_per_step * args.steps, "clocks": clock_info,
             "kernels": kernels, "stages_ms": stage_ms, "parity": parity,
             "measured_peaks": mp, "largest_config": largest, "bf16_state": bf16,
+            "decay_cell": decay,
             "device_status": status, "peaks_source": pk["source"],
         }
         print(json.dumps(line), flush=True)
