@@ -389,7 +389,7 @@ def stage_times(torch, _lib, st, flush, stream, n: int) -> dict:
     stages = [
         ("proj", lambda: _lib.cfc_input_projection(i["u"], i["W"], i["b"], st.H, st.cache)),
         ("fwd_rec", lambda: _lib.cfc_forward_recurrence(i["h0"], i["W"], i["ts"], st.H,
-                                                       st.cache)),
+                                                       st.cache, ws=st.fws)),
         ("bwd_rec", lambda: _lib.cfc_backward_recurrence_ws(i["dH"], i["W"], i["ts"], st.cache,
                                                            d32, st.dh0, bptt_ws)),
         ("grad_standalone", lambda: _lib.cfc_weight_grad(d32, i["u"], i["h0"], i["W"], st.H,

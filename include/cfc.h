@@ -75,9 +75,10 @@ extern "C" {
 typedef void* cfc_stream_t; /* a cudaStream_t */
 
 /*
- * cfc_workspace_bytes -- bytes of device workspace cfc_backward needs for these sizes and
- * dw_mode.  Writes *bwd_ws_bytes; the forward cache is always K*B*3*C floats and needs no
- * query.  Returns CFC_OK, CFC_ERR_INVALID_DIM, CFC_ERR_NULL_PTR or CFC_ERR_INVALID_ARG.
+ * cfc_workspace_bytes -- bytes of device workspace cfc_backward (and cfc_forward_backward,
+ * whose forward uses its tail) needs for these sizes and dw_mode.  Writes *bwd_ws_bytes; the
+ * forward cache is always K*B*3*C floats and needs no query.  Returns CFC_OK,
+ * CFC_ERR_INVALID_DIM, CFC_ERR_NULL_PTR or CFC_ERR_INVALID_ARG.
  * The workspace starts with the pre-activation gradients dL/dP of every step and row, readable
  * after cfc_backward completes, in the form the mode's contraction reads:
  *   CFC_DW_TF32, CFC_DW_SIMT_FP32: fp32 d_pre [K][B][4][C];
@@ -90,6 +91,15 @@ typedef void* cfc_stream_t; /* a cudaStream_t */
 int cfc_workspace_bytes(int B, int K, int C, int n_x, int dw_mode, size_t* bwd_ws_bytes);
 
 /*
+ * cfc_forward_workspace_bytes -- bytes of device workspace cfc_forward and
+ * cfc_forward_recurrence need: 0 below the batch sizes that take the tensor-core recurrence
+ * (B >= 384 at C = 256, B >= 768 at C = 128), otherwise its exchange buffer, 8*C bytes per
+ * batch row rounded up to a whole row tile (about 4.4 MB at B = 2048, C = 256).  Writes
+ * *bytes; returns CFC_OK, CFC_ERR_INVALID_DIM or CFC_ERR_NULL_PTR.
+ */
+int cfc_forward_workspace_bytes(int B, int K, int C, int n_x, size_t* bytes);
+
+/*
  * cfc_forward -- the K-step forward recurrence (successor of cfc_step_batched, which ran one
  * step per launch; page "K-loop Parallelization -- Block-per-Batch Kernel Refactor", section
  * "Problem").  One persistent launch runs all K steps.
@@ -100,11 +110,15 @@ int cfc_workspace_bytes(int B, int K, int C, int n_x, int dw_mode, size_t* bwd_w
  *   ts    [K][B]       time-scale per step and row (multiplies P_ta only)
  *   H     [K][B][C]    OUTPUT: h_t for every step
  *   cache [K][B][3][C] OUTPUT: ff1, ff2 and the gate s for every step (read by cfc_backward)
- * Exactly cfc_input_projection followed by cfc_forward_recurrence (two launches).
+ *   ws, ws_bytes       device workspace of at least cfc_forward_workspace_bytes() bytes,
+ *                      16-byte aligned; may be NULL when that is 0.  Transient: free for other
+ *                      use once the call's work on the stream is done.
+ * Exactly cfc_input_projection followed by cfc_forward_recurrence (two launches).  Returns
+ * CFC_ERR_NULL_PTR / CFC_ERR_WS_TOO_SMALL for a missing or short workspace.
  */
 int cfc_forward(const float* u, const float* h0, const float* W, const float* b,
-                const float* ts, int B, int K, int C, int n_x, float* H, float* cache,
-                cfc_stream_t stream);
+                const float* ts, int B, int K, int C, int n_x, float* H, float* cache, void* ws,
+                size_t ws_bytes, cfc_stream_t stream);
 
 /*
  * cfc_input_projection -- the first stage of cfc_forward alone: X = W_u u_t + b for every step
@@ -118,10 +132,11 @@ int cfc_input_projection(const float* u, const float* W, const float* b, int B, 
 /*
  * cfc_forward_recurrence -- the second stage of cfc_forward alone: the K-step recurrence,
  * adding W_h h_{t-1} to the X that cfc_input_projection left in H / cache and overwriting
- * H / cache with the outputs.  h0, W, ts, H, cache as for cfc_forward.
+ * H / cache with the outputs.  h0, W, ts, H, cache, ws, ws_bytes as for cfc_forward.
  */
 int cfc_forward_recurrence(const float* h0, const float* W, const float* ts, int B, int K,
-                           int C, int n_x, float* H, float* cache, cfc_stream_t stream);
+                           int C, int n_x, float* H, float* cache, void* ws, size_t ws_bytes,
+                           cfc_stream_t stream);
 
 /*
  * cfc_step_launches -- number of kernel launches one cfc_forward plus one cfc_backward enqueue
@@ -152,7 +167,8 @@ int cfc_backward(const float* dH, const float* u, const float* h0, const float* 
 
 /*
  * cfc_forward_backward -- one training step: exactly cfc_forward followed by cfc_backward,
- * with the same arguments, outputs and workspace, and bitwise the same results.  Because the
+ * with the same arguments and outputs, and bitwise the same results.  One workspace of
+ * cfc_workspace_bytes() bytes serves both (the forward's part is its tail).  Because the
  * forward writes nothing the backward recurrence reads before its dependency wait (W, dH),
  * the recurrence is launched as a programmatic dependent of the forward: its clusters are
  * scheduled and stage W_h^T while the forward's last steps run.  Returns the error codes of
@@ -182,7 +198,8 @@ int cfc_forward_backward(const float* u, const float* h0, const float* W, const 
 /*
  * cfc_forward_bf16_workspace_bytes -- device workspace cfc_forward_bf16 needs: the input
  * projection X = W_u u + b of every step in fp32 (4 C floats per batch row and step, plus
- * alignment).  Returns CFC_OK, CFC_ERR_INVALID_DIM (also for odd C) or CFC_ERR_NULL_PTR.
+ * alignment), then the recurrence's own (cfc_forward_workspace_bytes).  Returns CFC_OK,
+ * CFC_ERR_INVALID_DIM (also for odd C) or CFC_ERR_NULL_PTR.
  */
 int cfc_forward_bf16_workspace_bytes(int B, int K, int C, int n_x, size_t* bytes);
 

@@ -35,7 +35,7 @@ EXPORTED = ("cfc_workspace_bytes", "cfc_forward", "cfc_backward", "cfc_backward_
             "cfc_backward_recurrence_ws", "cfc_wait_self_test", "cfc_probe_fma",
             "cfc_probe_l2_read", "cfc_forward_bf16_workspace_bytes", "cfc_forward_bf16",
             "cfc_backward_bf16", "cfc_decay_forward", "cfc_decay_workspace_bytes",
-            "cfc_decay_backward")
+            "cfc_decay_backward", "cfc_forward_workspace_bytes")
 CFC_ERR_SCRATCH_LIMIT = -10
 NOALLOC_SCRATCH_BYTES = 32 << 20  # size of cfc_backward_noalloc's built-in device scratch
 
@@ -61,7 +61,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     lib.cfc_workspace_bytes.argtypes = [i, i, i, i, i, ctypes.POINTER(sz)]
     lib.cfc_workspace_bytes.restype = i
-    lib.cfc_forward.argtypes = [vp] * 5 + [i] * 4 + [vp, vp, vp]
+    lib.cfc_forward.argtypes = [vp] * 5 + [i] * 4 + [vp, vp, vp, sz, vp]
     lib.cfc_forward.restype = i
     lib.cfc_backward.argtypes = [vp] * 7 + [i] * 4 + [vp] * 5 + [sz, i, vp]
     lib.cfc_backward.restype = i
@@ -79,7 +79,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.reduce_axis0.restype = i
     lib.cfc_input_projection.argtypes = [vp] * 3 + [i] * 4 + [vp, vp, vp]
     lib.cfc_input_projection.restype = i
-    lib.cfc_forward_recurrence.argtypes = [vp] * 3 + [i] * 4 + [vp, vp, vp]
+    lib.cfc_forward_recurrence.argtypes = [vp] * 3 + [i] * 4 + [vp, vp, vp, sz, vp]
     lib.cfc_forward_recurrence.restype = i
     lib.cfc_step_launches.argtypes = [i] * 6 + [ctypes.POINTER(i)]
     lib.cfc_step_launches.restype = i
@@ -97,6 +97,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.cfc_probe_l2_read.argtypes = [vp, sz, i, vp, i, dptr, vp]
     lib.cfc_probe_l2_read.restype = i
     lib.cfc_forward_bf16_workspace_bytes.argtypes = [i] * 4 + [ctypes.POINTER(sz)]
+    lib.cfc_forward_workspace_bytes.argtypes = [i] * 4 + [ctypes.POINTER(sz)]
+    lib.cfc_forward_workspace_bytes.restype = i
     lib.cfc_forward_bf16_workspace_bytes.restype = i
     lib.cfc_forward_bf16.argtypes = [vp] * 5 + [i] * 4 + [vp, vp, vp, sz, vp]
     lib.cfc_forward_bf16.restype = i
@@ -171,15 +173,38 @@ def workspace_bytes(B: int, K: int, C: int, n_x: int, dw_mode: int = CFC_DW_ACCU
     return out.value
 
 
-def cfc_forward(u, h0, W, b, ts, H, cache, stream=None) -> None:
-    """H [K,B,C] and cache [K,B,3,C] <- forward recurrence over K steps."""
+def forward_workspace_bytes(B: int, K: int, C: int, n_x: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("cfc_forward_workspace_bytes",
+           load().cfc_forward_workspace_bytes(B, K, C, n_x, ctypes.byref(out)))
+    return out.value
+
+
+def _fwd_ws(ws, B, K, C, n_x, like):
+    """(pointer, bytes) of the forward's workspace: `ws`, or a fresh device buffer when the
+    caller gave none and the sizes need one."""
+    if ws is None:
+        need = forward_workspace_bytes(B, K, C, n_x)
+        if need == 0:
+            return None, 0, None
+        import torch
+
+        ws = torch.empty(need, dtype=torch.uint8, device=like.device)
+    p, n = _ws(ws)
+    return p, n, ws
+
+
+def cfc_forward(u, h0, W, b, ts, H, cache, ws=None, stream=None) -> None:
+    """H [K,B,C] and cache [K,B,3,C] <- forward recurrence over K steps.  `ws`: a uint8
+    device buffer of forward_workspace_bytes() bytes (allocated here when None and needed)."""
     K, B, n_x = u.shape
     C = h0.shape[1]
     n_in = n_x + C
+    wp, wn, _keep = _fwd_ws(ws, B, K, C, n_x, H)
     rc = load().cfc_forward(
         _ptr(u, "u", (K, B, n_x)), _ptr(h0, "h0", (B, C)), _ptr(W, "W", (4, C, n_in)),
         _ptr(b, "b", (4, C)), _ptr(ts, "ts", (K, B)), B, K, C, n_x,
-        _ptr(H, "H", (K, B, C)), _ptr(cache, "cache", (K, B, 3, C)), _stream(stream))
+        _ptr(H, "H", (K, B, C)), _ptr(cache, "cache", (K, B, 3, C)), wp, wn, _stream(stream))
     _check("cfc_forward", rc)
 
 
@@ -194,13 +219,15 @@ def cfc_input_projection(u, W, b, H, cache, stream=None) -> None:
     _check("cfc_input_projection", rc)
 
 
-def cfc_forward_recurrence(h0, W, ts, H, cache, stream=None) -> None:
-    """The K-step recurrence on top of the projection left in H / cache."""
+def cfc_forward_recurrence(h0, W, ts, H, cache, ws=None, stream=None) -> None:
+    """The K-step recurrence on top of the projection left in H / cache (`ws` as for
+    cfc_forward)."""
     K, B, C = H.shape
     n_x = W.shape[2] - C
+    wp, wn, _keep = _fwd_ws(ws, B, K, C, n_x, H)
     rc = load().cfc_forward_recurrence(
         _ptr(h0, "h0", (B, C)), _ptr(W, "W", (4, C, n_x + C)), _ptr(ts, "ts", (K, B)),
-        B, K, C, n_x, _ptr(H, "H", (K, B, C)), _ptr(cache, "cache", (K, B, 3, C)),
+        B, K, C, n_x, _ptr(H, "H", (K, B, C)), _ptr(cache, "cache", (K, B, 3, C)), wp, wn,
         _stream(stream))
     _check("cfc_forward_recurrence", rc)
 

@@ -179,6 +179,7 @@ struct BwdLayout {
   size_t pu_off;                  // du split partials (floats into the partials), if du is split
   bool tc_bptt;                   // the BPTT runs on the tensor cores (W_h^T pre-split at wsplit_off)
   size_t wsplit_off;
+  size_t fwd_off;                 // cfc_forward_backward: the forward's workspace, last
 };
 // Rows (B*K) from which the input projection runs on the tensor cores (bf16 hi/lo split,
 // tc_gemm_kernel<ProjProblem>) rather than on the CUDA cores (inproj_kernel): below it the
@@ -192,6 +193,22 @@ constexpr int kTcProjMinRows = 8192;
 // us (CUDA cores, B = 511) and 7.9 us (B = 767) against 7.6-7.7 us (tensor cores); C = 256:
 // 11.8 us (CUDA cores, B <= 300) and 15.7 us (B = 400) against 12.2 us (tensor cores).
 int tc_fwd_min_rows(int C) { return C >= 256 ? 384 : 768; }
+
+// Workspace of the forward recurrence: the tensor-core kernel's exchange buffer, none for the
+// CUDA-core kernel.
+size_t fwd_ws_bytes(int B, int C) {
+  return (B >= tc_fwd_min_rows(C) && cfc::fwd_tc_supported(C)) ? cfc::fwd_tc_xch_bytes(B, C) : 0;
+}
+
+// CFC_OK when `ws` can hold the forward's workspace (nothing is needed below the tensor-core
+// row threshold, and ws may then be NULL).
+int check_fwd_ws(int B, int C, const void* ws, size_t ws_bytes) {
+  const size_t need = fwd_ws_bytes(B, C);
+  if (need == 0) return CFC_OK;
+  if (!ws) return CFC_ERR_NULL_PTR;
+  if (!aligned16(ws)) return CFC_ERR_MISALIGNED;
+  return ws_bytes < need ? CFC_ERR_WS_TOO_SMALL : CFC_OK;
+}
 
 // Batch rows from which the BPTT recurrence runs its per-step contraction on the tensor cores
 // (cfc_bwd_l2x_kernel, clusters of C / 32 CTAs per 128 or 144 rows); it needs the W_h^T image
@@ -238,6 +255,10 @@ BwdLayout bwd_layout(int B, int K, int C, int n_x, int mode) {
   L.tc_bptt = B >= tc_bwd_min_rows(C) && cfc::bwd_l2x_supported(C);
   L.wsplit_off = align256(L.total);
   if (L.tc_bptt) L.total = L.wsplit_off + cfc::bwd_l2x_ws_bytes(B, C);
+  // Apart from everything the backward writes: the backward recurrence is a dependent launch
+  // of the forward and may start while the forward still exchanges through it.
+  L.fwd_off = align256(L.total);
+  if (fwd_ws_bytes(B, C) > 0) L.total = L.fwd_off + fwd_ws_bytes(B, C);
   return L;
 }
 
@@ -299,8 +320,10 @@ namespace {
 
 // `pdl`: the previous kernel of the stream is one of this library's kernels of the same call
 // (see cfc_launch.cuh).
+// `xch`: the workspace of fwd_ws_bytes(B, C) bytes (checked by the caller; NULL when none is
+// needed).
 int forward_recurrence(const float* h0, const float* W, const float* ts, int B, int K, int C,
-                       int n_x, float* H, float* cache, cfc_stream_t stream, bool pdl,
+                       int n_x, float* H, float* cache, void* xch, cfc_stream_t stream, bool pdl,
                        const float* xH = nullptr, const float* xcache = nullptr,
                        bool out_bf16 = false) {
   int rc = check_dims(B, K, C, n_x);
@@ -320,7 +343,9 @@ int forward_recurrence(const float* h0, const float* W, const float* ts, int B, 
   p.status = st->status;
   p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
   p.CS = cluster_size_for(C, cfc::kFwdChanPerCta);
-  if (B >= tc_fwd_min_rows(C) && cfc::fwd_tc_supported(C)) {
+  p.xch = xch;
+  if (fwd_ws_bytes(B, C) > 0) {
+    if (!xch) return CFC_ERR_NULL_PTR;
     // 128 rows per cluster, or 144 when 128-row clusters would not all be resident at once
     // (at C = 256, 2048 rows need 16 clusters of 8 CTAs and GB300 keeps 15: measured 21.3 us
     // per step in two waves against 12.2 us in one).
@@ -407,26 +432,54 @@ int backward_recurrence(const float* dH, const float* W, const float* ts, const 
 
 extern "C" {
 
-int cfc_forward_recurrence(const float* h0, const float* W, const float* ts, int B, int K,
-                           int C, int n_x, float* H, float* cache, cfc_stream_t stream) {
-  return forward_recurrence(h0, W, ts, B, K, C, n_x, H, cache, stream, false);
+int cfc_forward_workspace_bytes(int B, int K, int C, int n_x, size_t* bytes) {
+  const int rc = check_dims(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  if (!bytes) return CFC_ERR_NULL_PTR;
+  *bytes = fwd_ws_bytes(B, C);
+  return CFC_OK;
 }
 
-int cfc_forward(const float* u, const float* h0, const float* W, const float* b,
-                const float* ts, int B, int K, int C, int n_x, float* H, float* cache,
+int cfc_forward_recurrence(const float* h0, const float* W, const float* ts, int B, int K,
+                           int C, int n_x, float* H, float* cache, void* ws, size_t ws_bytes,
+                           cfc_stream_t stream) {
+  int rc = check_dims(B, K, C, n_x);
+  if (rc != CFC_OK) return rc;
+  rc = check_fwd_ws(B, C, ws, ws_bytes);
+  if (rc != CFC_OK) return rc;
+  return forward_recurrence(h0, W, ts, B, K, C, n_x, H, cache, ws, stream, false);
+}
+
+}  // extern "C"
+
+namespace {
+// cfc_forward after its argument checks; `xch` as for forward_recurrence.
+int forward_all(const float* u, const float* h0, const float* W, const float* b,
+                const float* ts, int B, int K, int C, int n_x, float* H, float* cache, void* xch,
                 cfc_stream_t stream) {
+  const int rc = cfc_input_projection(u, W, b, B, K, C, n_x, H, cache, stream);
+  if (rc != CFC_OK) return rc;
+  // Not a dependent launch: scheduled early, the recurrence clusters land on SMs the
+  // projection still occupies and end up two CTAs to an SM, which slows every one of the K
+  // steps (measured on GB300: the training step took 149.6 us this way against 140.7 us).
+  return forward_recurrence(h0, W, ts, B, K, C, n_x, H, cache, xch, stream, false);
+}
+}  // namespace
+
+extern "C" {
+
+int cfc_forward(const float* u, const float* h0, const float* W, const float* b,
+                const float* ts, int B, int K, int C, int n_x, float* H, float* cache, void* ws,
+                size_t ws_bytes, cfc_stream_t stream) {
   int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
   if (!u || !h0 || !W || !b || !ts || !H || !cache) return CFC_ERR_NULL_PTR;
   if (!aligned16(u) || !aligned16(h0) || !aligned16(W) || !aligned16(b) || !aligned16(ts) ||
       !aligned16(H) || !aligned16(cache))
     return CFC_ERR_MISALIGNED;
-  rc = cfc_input_projection(u, W, b, B, K, C, n_x, H, cache, stream);
+  rc = check_fwd_ws(B, C, ws, ws_bytes);
   if (rc != CFC_OK) return rc;
-  // Not a dependent launch: scheduled early, the recurrence clusters land on SMs the
-  // projection still occupies and end up two CTAs to an SM, which slows every one of the K
-  // steps (measured on GB300: the training step took 149.6 us this way against 140.7 us).
-  return forward_recurrence(h0, W, ts, B, K, C, n_x, H, cache, stream, false);
+  return forward_all(u, h0, W, b, ts, B, K, C, n_x, H, cache, ws, stream);
 }
 
 int cfc_step_launches(int B, int K, int C, int n_x, int dw_mode, int with_du, int* launches) {
@@ -666,7 +719,8 @@ int cfc_forward_backward(const float* u, const float* h0, const float* W, const 
     return CFC_ERR_MISALIGNED;
   const BwdLayout L = bwd_layout(B, K, C, n_x, dw_mode);
   if (ws_bytes < L.total) return CFC_ERR_WS_TOO_SMALL;
-  rc = cfc_forward(u, h0, W, b, ts, B, K, C, n_x, H, cache, stream);
+  rc = forward_all(u, h0, W, b, ts, B, K, C, n_x, H, cache, static_cast<char*>(ws) + L.fwd_off,
+                   stream);
   if (rc != CFC_OK) return rc;
   // The forward writes only H and cache, which the BPTT reads after its dependency wait.
   float* d_pre = reinterpret_cast<float*>(static_cast<char*>(ws) + L.d_pre_off);
@@ -689,12 +743,17 @@ static size_t bf16_x_offset(int B, int K, int C) {
   return align256(static_cast<size_t>(K) * B * C * sizeof(float));
 }
 
+// After X (gate 0, then gates 1-3): the recurrence's own workspace.
+static size_t bf16_xch_offset(int B, int K, int C) {
+  return align256(bf16_x_offset(B, K, C) + static_cast<size_t>(K) * B * 3 * C * sizeof(float));
+}
+
 int cfc_forward_bf16_workspace_bytes(int B, int K, int C, int n_x, size_t* bytes) {
   const int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
   if (C % 2 != 0) return CFC_ERR_INVALID_DIM;
   if (!bytes) return CFC_ERR_NULL_PTR;
-  *bytes = bf16_x_offset(B, K, C) + static_cast<size_t>(K) * B * 3 * C * sizeof(float);
+  *bytes = bf16_xch_offset(B, K, C) + fwd_ws_bytes(B, C);
   return CFC_OK;
 }
 
@@ -716,7 +775,9 @@ int cfc_forward_bf16(const float* u, const float* h0, const float* W, const floa
   rc = cfc_input_projection(u, W, b, B, K, C, n_x, xH, xcache, stream);
   if (rc != CFC_OK) return rc;
   return forward_recurrence(h0, W, ts, B, K, C, n_x, static_cast<float*>(H),
-                            static_cast<float*>(cache), stream, false, xH, xcache, true);
+                            static_cast<float*>(cache),
+                            static_cast<char*>(ws) + bf16_xch_offset(B, K, C), stream, false,
+                            xH, xcache, true);
 }
 
 int cfc_backward_bf16(const float* dH, const float* u, const float* h0, const float* W,

@@ -160,18 +160,6 @@ __device__ __forceinline__ void drain_piece(uint32_t dmem, int c0, float os,
   }
 }
 
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t rbar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar)
-               : "memory");
-}
 
 __device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
   uint32_t r;
@@ -383,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_l2x_kernel(const BwdParam
               drain_piece<DC % 64>(dmem, col_lo + DC - DC % 64, os, ri, blk, mine);
             tc_fence_before_sync();  // the reads precede the next step's MMAs (via b_ready)
             __syncwarp();
-            if (dest != rank) asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            if (dest != rank) fence_acq_rel_gpu();
             if (lane == 0) mbar_arrive_remote(map_to_rank(xfull, dest));
           }
           ok = dok;

@@ -12,23 +12,30 @@
 // in (-1, 1).  Each row of W is scaled by a power of two into [-1, 1) before the split, and
 // the result is scaled back exactly, so no weight over- or underflows fp16.
 //
-// Layout: a thread-block cluster of CS = C / 32 CTAs serves 128 batch rows; CTA `rank` owns
-// channels 32 rank .. 32 rank + 31, i.e. 128 gate rows of W.  Per CTA:
-//   tensor memory  D^T [128 gate rows (lanes) x 128 batch rows (columns)] fp32, then the CTA's
+// Layout: a thread-block cluster of CS = C / 32 CTAs serves NR = 128 or 144 batch rows; CTA
+// `rank` owns channels 32 rank .. 32 rank + 31, i.e. 128 gate rows of W.  Per CTA:
+//   tensor memory  D^T [128 gate rows (lanes) x NR batch rows (columns)] fp32, then the CTA's
 //                  W_h^T slice as the A operand (lane 4c + g = gate g of local channel c, k
 //                  along columns in fp16 pairs), two terms of C / 2 columns each;
-//   shared memory  h_{t-1} as the B operand, two fp16 terms [C x 128] in the non-swizzled
+//   shared memory  h_{t-1} as the B operand, two fp16 terms [C x NR] in the non-swizzled
 //                  K-major layout [k / 8][row / 8][8 rows][16 bytes], so the 32 values of
-//                  k that one CTA produces form one contiguous 8 KB slab per term.
-// A step: one thread issues the MMAs slab by slab as the slabs of h_{t-1} arrive (its own in
-// place, the others by bulk copies from the other CTAs); then eight warps read D^T and add X
-// (a channel's four gates sit in four adjacent lanes; a 4 x 4 transpose inside each lane quad
-// gives every lane all four gates of one row), apply the cell, write H and the cache, and
-// write h_t's two terms into the CTA's own slab; the control warp copies that slab to every
-// other CTA.  A cluster-wide barrier ("every CTA's MMAs of step t are done")
-// guards both buffer reuses: the other CTAs' slabs landing in this CTA's h buffer, and the
-// next overwrite of this CTA's own slab (a source of its copies).  Every wait is bounded; a
-// timeout is recorded in the status word and the CTAs leave the loop together.
+//                  k that one CTA produces form one contiguous slab per term.
+// Roles (320 threads): eight epilogue warps, a control warp whose lane 0 issues the MMAs and
+// an exchange warp whose lane 0 moves the slabs.  A step t: the control thread issues the
+// MMAs slab by slab as the slabs of h_{t-1} land (its own first) and commits them to `done`;
+// the epilogue warps wait for `done`, read D^T and add X (a channel's four gates sit in four
+// adjacent lanes; a 4 x 4 transpose inside each lane quad gives every lane all four gates of
+// one row), apply the cell, write H and the cache and write h_t's two terms into the CTA's
+// own slab, then mark it full.  The exchange thread copies that slab to the CTA's slot of an
+// exchange buffer in global memory (bulk copy, completion awaited), announces it by a remote
+// mbarrier arrive on every other CTA, and bulk-loads the other CTAs' slabs of h_t from L2 as
+// they are announced.  The slabs of the cluster used to travel between shared memories
+// (bulk copies into distributed shared memory); on GB300 with 15 clusters of 8 CTAs those
+// took 4 to 6 us per step to land against about 2 us through L2.  A slab of the exchange
+// buffer is rewritten two steps later (slots alternate with the step parity, and so do the
+// announcing barriers): by then every CTA has loaded it, because it needed this CTA's next
+// slab first.  No CTA waits for another except for the data it reads.  Every wait is
+// bounded; a timeout is recorded in the status word and every role leaves its loop.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -41,8 +48,9 @@ namespace {
 
 constexpr int kGC = 4 * kFwdChanPerCta;          // gate rows per CTA (MMA M)
 constexpr int kEpiWarps = 8;                     // epilogue warps (two per TMEM lane quarter)
-constexpr int kTcThreads = (kEpiWarps + 1) * 32; // + one control warp
-constexpr int kStepBar = 1;                      // named barrier id of the per-step hand-off
+constexpr int kCtlWarp = kEpiWarps;              // lane 0 issues the MMAs
+constexpr int kXchWarp = kEpiWarps + 1;          // lane 0 runs the exchange
+constexpr int kTcThreads = (kEpiWarps + 2) * 32;
 constexpr int kTerms = 2;                        // fp16 terms per operand
 constexpr uint32_t kACol0 = 256;                 // W_h^T terms start here; D^T takes NR columns
 
@@ -54,11 +62,13 @@ struct TcShape {
   static constexpr int C = kFwdChanPerCta * CS;
   static constexpr int TERM = C * NR * 2;        // bytes of one fp16 term of h
   static constexpr int SLAB = NR * kFwdChanPerCta * 2;  // one CTA's k range of one h term
+  static constexpr int XSLOT = kTerms * SLAB;    // one CTA's exchange slot: its slab, both terms
   static constexpr int HR = NR / 2;              // rows of one epilogue warp half
   static constexpr int ACOLS = C / 2;            // TMEM columns of one term of W_h^T
+  static constexpr int NBARS = 3 * CS + 2;       // full[CS], done, fin, ready[2][CS]
   static_assert(NR % 16 == 0 && HR % 8 == 0 && NR <= 256, "row tile");
-  // h terms, ts of two steps, barriers (full[CS], mma done, all done), TMEM slot, alignment.
-  static constexpr int USED = kTerms * TERM + 2 * NR * 4 + (CS + 2) * 8 + 16 + 128;
+  // h terms, each epilogue warp's ts, barriers, TMEM slot, alignment.
+  static constexpr int USED = kTerms * TERM + kEpiWarps * HR * 4 + NBARS * 8 + 16 + 128;
   // At least half an SM's shared memory: a CTA takes all 512 tensor-memory columns, so two
   // CTAs on one SM would leave the second waiting in tcgen05.alloc while its cluster waits on
   // it.
@@ -140,36 +150,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
-// Bulk copy of `bytes` from this CTA's shared memory to a (remote) CTA's shared memory of the
-// cluster, completing as transaction bytes on the destination's mbarrier `rbar`.
-__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t rdst, uint32_t src, uint32_t bytes,
-                                                     uint32_t rbar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-      "[%3];" ::"r"(rdst),
-      "r"(src), "r"(bytes), "r"(rbar)
-      : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t rbar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar)
-               : "memory");
-}
-
-// Named barrier over `n` threads that returns the OR of `pred` over them.
-__device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-
 template <int CS, int NR, bool BF>
 __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdParams p) {
   using S = TcShape<CS, NR>;
@@ -179,27 +159,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t* sm = smem_raw + ((128u - (raw & 127u)) & 127u);
   uint8_t* hb = sm;                                                     // [2][TERM]
-  float* ts_s = reinterpret_cast<float*>(sm + kTerms * S::TERM);        // [2][NR]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ts_s + 2 * NR);          // full[CS], done, all
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + CS + 2);
+  float* ts_w = reinterpret_cast<float*>(sm + kTerms * S::TERM);        // [kEpiWarps][HR]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ts_w + kEpiWarps * HR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + S::NBARS);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int rank = static_cast<int>(cluster_rank());
-  const int row0 = static_cast<int>(cluster_id_x()) * NR;
+  const int cluster = static_cast<int>(cluster_id_x());
+  const int n_clusters = static_cast<int>(gridDim.x) / CS;
+  const int row0 = cluster * NR;
   const int B = p.B, K = p.K, n_x = p.n_x, n_in = p.n_in;
-  const uint32_t full0 = smem_addr(&bars[0]);       // full[j]: slab j of h_{t-1} is in place
-  const uint32_t done_bar = smem_addr(&bars[CS]);   // this CTA's MMAs of the step are done
-  const uint32_t all_bar = smem_addr(&bars[CS + 1]);  // every CTA's MMAs of the step are done
+  const uint32_t full0 = smem_addr(&bars[0]);          // full[j]: slab j of the step's h in place
+  const uint32_t done_bar = smem_addr(&bars[CS]);      // this CTA's MMAs of the step are done
+  const uint32_t fin_bar = smem_addr(&bars[CS + 1]);   // every MMA of this CTA is done (exit)
+  const uint32_t ready0 = smem_addr(&bars[CS + 2]);    // ready[par][j]: CTA j's slab is in L2
+  uint8_t* const xch = static_cast<uint8_t*>(p.xch);
+  // Exchange slot of CTA r of this cluster for step parity par.
+  auto slot = [&](int par, int r) {
+    return xch + static_cast<size_t>((par * n_clusters + cluster) * CS + r) * S::XSLOT;
+  };
 
   grid_dep_launch_dependents();
   if (tid == 0) {
-    for (int j = 0; j < CS; ++j) mbar_init(full0 + 8u * j, 1);
+    // The own slab is filled by the eight epilogue warps, the others by one bulk load each.
+    for (int j = 0; j < CS; ++j) mbar_init(full0 + 8u * j, j == rank ? kEpiWarps : 1);
     mbar_init(done_bar, 1);
-    mbar_init(all_bar, CS);
+    mbar_init(fin_bar, 1);
+    for (int i = 0; i < 2 * CS; ++i) mbar_init(ready0 + 8u * i, kEpiWarps);
     fence_mbar_init_cluster();
   }
-  if (warp == kEpiWarps) {
+  if (warp == kCtlWarp) {
     tmem_alloc(smem_addr(tslot), 512);
     tc_fence_before_sync();
   }
@@ -240,54 +230,48 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
       tmem_st32(ta + S::ACOLS, r1);
     }
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-    // ---- h0 -> this CTA's slab of the h buffer (lanes g = 1, 2 write term g - 1). ----
+    // ---- h0 -> this CTA's slab of the h buffer and its exchange slot of step parity 0
+    // (lanes g = 1, 2 write term g - 1). ----
     if (g == 1 || g == 2) {
+      uint8_t* const xs = slot(0, rank) + (g - 1) * S::SLAB - rank * S::SLAB;
       for (int i = 0; i < HR; ++i) {
         const int r = HR * hh + i, b = row0 + r;
         const float h = (b < B) ? __ldg(p.h0 + static_cast<size_t>(b) * C + ch) : 0.f;
-        *reinterpret_cast<__half*>(hb + (g - 1) * S::TERM + hterm_offset<NR>(r, ch)) =
-            split2(h).t[g - 1];
+        const uint32_t off = hterm_offset<NR>(r, ch);
+        const __half v = split2(h).t[g - 1];
+        *reinterpret_cast<__half*>(hb + (g - 1) * S::TERM + off) = v;
+        __stcg(reinterpret_cast<unsigned short*>(xs + off), __half_as_ushort(v));
       }
     }
-  } else {
-    // ts of step 0 (the control warp loads each step's ts one step ahead).
-    for (int i = lane; i < NR; i += 32) ts_s[i] = (row0 + i < B) ? __ldg(p.ts + row0 + i) : 0.f;
+    // ts of step 0 for this warp's rows (each warp keeps its own copy).
+    for (int i = lane; i < HR; i += 32) {
+      const int b = row0 + HR * hh + i;
+      ts_w[warp * HR + i] = (b < B) ? __ldg(p.ts + b) : 0.f;
+    }
   }
   fence_proxy_async_smem();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  cluster_sync_all();  // every CTA: barriers set up, W_h^T and its h0 slab in place
+  cluster_sync_all();  // every CTA: barriers set up (remote arrives may follow), W_h^T in place
+  if (warp < kEpiWarps) {
+    // The h0 slab is in place here and in L2: mark it full and announce it.
+    fence_acq_rel_gpu();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(full0 + 8u * rank);
+    else if (lane < CS) mbar_arrive_remote(map_to_rank(ready0 + 8u * rank, (rank + lane) % CS));
+  }
 
-  if (warp == kEpiWarps) {
-    // ================= control warp: MMAs, completion signals, the exchange =================
-    const uint32_t idesc = umma_idesc_f16in(kGC, NR);
-    const uint32_t hb0 = smem_addr(hb);
-    const uint64_t bdesc0 = desc_kmajor(hb0, (NR / 8) * 128, 128);
-    // This CTA's slab (three terms) to every other CTA, lane d copying to CTA rank + d; lane 0
-    // marks its own slab in place.
-    auto push = [&]() {
-      if (lane == 0) {
-        mbar_arrive(full0 + 8u * rank);
-      } else if (lane < CS) {
-        const uint32_t dst = static_cast<uint32_t>((rank + lane) % CS);
-        for (int tm = 0; tm < kTerms; ++tm) {
-          const uint32_t src = hb0 + tm * S::TERM + rank * S::SLAB;
-          bulk_copy_to_cluster(map_to_rank(src, dst), src, S::SLAB,
-                               map_to_rank(full0 + 8u * rank, dst));
-        }
-      }
-    };
-    bool ok = true;
-    if (lane == 0)
-      for (int j = 0; j < CS; ++j)
-        if (j != rank) mbar_arrive_expect_tx(full0 + 8u * j, kTerms * S::SLAB);
-    push();  // h0: the slabs step 0 multiplies
-    for (int t = 0; t < K; ++t) {
-      if (lane == 0) {
+  if (warp == kCtlWarp) {
+    // ================= control thread: the MMAs =================
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_f16in(kGC, NR);
+      const uint64_t bdesc0 = desc_kmajor(smem_addr(hb), (NR / 8) * 128, 128);
+      bool ok = true;
+      for (int t = 0; t < K && ok; ++t) {
         uint32_t acc = 0;
-        for (int jj = 0; jj < CS && ok; ++jj) {
-          const int j = (rank + jj) % CS;
+        for (int jj = 0; jj < CS; ++jj) {
+          const int j = (rank + jj) % CS;  // own slab first, then in rank order
           ok = mbar_wait_bounded_cta(full0 + 8u * j, t & 1, p.status);
           if (!ok) break;
           tc_fence_after_sync();
@@ -306,24 +290,54 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
             umma_tmem_a(tmem, a0 + S::ACOLS, d0, idesc, 1);
           }
         }
-        umma_commit(done_bar);
-        if (t + 1 < K)
-          for (int j = 0; j < CS; ++j)
-            if (j != rank) mbar_arrive_expect_tx(full0 + 8u * j, kTerms * S::SLAB);
-        ok = mbar_wait_bounded_cta(done_bar, t & 1, p.status) && ok;
-        tc_fence_before_sync();  // the step's MMAs are ordered before the signals below
-        // This CTA no longer reads its h buffer for step t: tell every CTA.
-        for (int d = 0; d < CS; ++d) mbar_arrive_cluster(map_to_rank(all_bar, d));
+        if (ok) umma_commit(done_bar);
       }
-      // ts of step t + 1 for the next epilogue.
-      if (t + 1 < K)
-        for (int i = lane; i < NR; i += 32)
-          ts_s[((t + 1) & 1) * NR + i] =
-              (row0 + i < B) ? __ldg(p.ts + static_cast<size_t>(t + 1) * B + row0 + i) : 0.f;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (bar_or(kStepBar, kTcThreads, !ok)) break;  // h_t is in this CTA's slab
-      if (t + 1 < K) push();
+      // Every MMA this thread issued has completed before tensor memory is freed.
+      umma_commit(fin_bar);
+      (void)mbar_wait_bounded_cta(fin_bar, 0, p.status);
     }
+  } else if (warp == kXchWarp) {
+    // ================= exchange warp =================
+    // Step s multiplies h_{s-1}.  Once this CTA's MMAs of step s - 1 are done (its epilogue
+    // has filled the own slab), lane jj = 1 .. CS - 1 loads slab rank + jj from L2 as soon as
+    // all eight epilogue warps of that CTA have announced it.
+    const uint32_t hb0 = smem_addr(hb);
+    const bool peer = lane >= 1 && lane < CS;
+    const int j = (rank + lane) % CS;  // the slab this lane loads
+    bool ok = true;
+    int armed = -1;  // the last step whose slab this lane requested
+    for (int s = 0; s < K; ++s) {
+      const int par = s & 1;
+      if (lane == 0) ok = mbar_wait_bounded_cta(full0 + 8u * rank, s & 1, p.status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const uint32_t rb = ready0 + 8u * (par * CS + j);
+      bool pending = peer;
+      const uint64_t t0 = global_timer_ns();
+      for (uint32_t it = 1; __any_sync(0xffffffffu, pending); ++it) {
+        if (pending && mbar_test_wait_cluster(rb, (s >> 1) & 1)) {
+          fence_proxy_async_global();
+          const uint32_t fb = full0 + 8u * j;
+          mbar_arrive_expect_tx(fb, S::XSLOT);
+          const uint8_t* const src = slot(par, j);
+          for (int tm = 0; tm < kTerms; ++tm)
+            bulk_g2s(hb0 + tm * S::TERM + j * S::SLAB, src + tm * S::SLAB, S::SLAB, fb);
+          armed = s;
+          pending = false;
+        }
+        if ((it & 255u) == 0u &&
+            __any_sync(0xffffffffu, global_timer_ns() - t0 > kWaitLimitNs)) {  // warp-uniform
+          if (pending) atomicExch(p.status, kStatusTimeout);
+          ok = false;
+          break;
+        }
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+    }
+    // No bulk load into this CTA's shared memory is in flight when it exits (they read L2
+    // only, so they complete).
+    if (armed >= 0) (void)mbar_wait_bounded_cta(full0 + 8u * j, armed & 1, p.status);
   } else {
     // ================= epilogue warps =================
     // X of (gate g, channel ch) for rows row0 + HR hh + i, i < HR, of step t, in the layout of
@@ -340,17 +354,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
 #pragma unroll
       for (int i = 0; i < HR; ++i) xv[i] = (i < nvalid) ? __ldcg(xp + i * xrow) : 0.f;
     };
+    // ts of the next step for this warp's rows: lane i holds rows i, i + 32, ...
+    constexpr int kTsPerLane = (HR + 31) / 32;
+    float tsn[kTsPerLane];
+    auto load_ts = [&](int t) {
+#pragma unroll
+      for (int k = 0; k < kTsPerLane; ++k) {
+        const int i = lane + 32 * k, b = rfirst + i;
+        tsn[k] = (i < HR && b < B) ? __ldg(p.ts + static_cast<size_t>(t) * B + b) : 0.f;
+      }
+    };
+    float* const tsw = ts_w + warp * HR;
     load_x(0);
-    bool ok = true;
     for (int t = 0; t < K; ++t) {
-      ok = ok && mbar_wait_bounded_cluster(all_bar, t & 1, p.status);
+      bool ok = mbar_wait_bounded_cta(done_bar, t & 1, p.status);
       ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
       tc_fence_after_sync();
-      if (ok) {
-        const float* tsr = ts_s + (t & 1) * NR + HR * hh;
+      if (t > 0) {
+        __syncwarp();  // the previous step's reads of tsw are done
+#pragma unroll
+        for (int k = 0; k < kTsPerLane; ++k)
+          if (lane + 32 * k < HR) tsw[lane + 32 * k] = tsn[k];
+        __syncwarp();
+      }
+      {
+        const float* tsr = tsw;
         const size_t ho = (static_cast<size_t>(t) * B + rfirst) * C + ch;  // element offsets
         const size_t co = (static_cast<size_t>(t) * B + rfirst) * 3 * C + ch;
         const uint32_t dq = tmem + (static_cast<uint32_t>(32 * q) << 16) + HR * hh;
+        // h_t is the operand of step t + 1: its exchange slot has that step's parity.
+        uint8_t* const xs = slot((t + 1) & 1, rank) - rank * S::SLAB;
         // Rows ibase .. ibase + n - 1 of this warp half (n = 16, or 8 for the tail of 72).
         auto rows = [&](float (&P)[16], int ibase, int n) {
 #pragma unroll
@@ -396,9 +430,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
               }
             }
             const Split2 sp = split2(h);
-            uint8_t* dst = hb + hterm_offset<NR>(HR * hh + ri, ch);
+            const uint32_t off = hterm_offset<NR>(HR * hh + ri, ch);
+            uint8_t* dst = hb + off;
             *reinterpret_cast<__half*>(dst) = sp.t[0];
             *reinterpret_cast<__half*>(dst + S::TERM) = sp.t[1];
+            if (t + 1 < K) {
+              __stcg(reinterpret_cast<unsigned short*>(xs + off), __half_as_ushort(sp.t[0]));
+              __stcg(reinterpret_cast<unsigned short*>(xs + off + S::SLAB),
+                     __half_as_ushort(sp.t[1]));
+            }
           }
         };
 #pragma unroll
@@ -418,18 +458,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
           rows(P, HR - 8, 8);
         }
       }
-      fence_proxy_async_smem();  // h_t's terms -> visible to the MMAs and the bulk copies
+      fence_proxy_async_smem();  // h_t's terms -> visible to the MMAs
       tc_fence_before_sync();    // tensor-memory loads done before the next step's MMAs
-      if (bar_or(kStepBar, kTcThreads, !ok)) break;
-      if (t + 1 < K) load_x(t + 1);  // in flight while the next step's MMAs run
+      if (t + 1 < K) {
+        fence_acq_rel_gpu();     // h_t's terms in L2 before the announcements below
+        __syncwarp();
+        // This warp's part of h_t: in the own slab (lane 0), in L2 for every other CTA.
+        if (lane == 0) mbar_arrive(full0 + 8u * rank);
+        else if (lane < CS)
+          mbar_arrive_remote(
+              map_to_rank(ready0 + 8u * (((t + 1) & 1) * CS + rank), (rank + lane) % CS));
+        load_x(t + 1);  // in flight while the exchange and the next step's MMAs run
+        load_ts(t + 1);
+      }
     }
   }
 
-  // Leave together: no CTA exits while another may still address its shared memory.
+  // Leave together: no CTA exits while another may still address its shared memory or arrive
+  // on its barriers.
   tc_fence_before_sync();
   __syncthreads();
   cluster_sync_all();
-  if (warp == kEpiWarps) {
+  if (warp == kCtlWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
   }
@@ -483,6 +533,14 @@ cudaError_t launch_k(const FwdParams& p, cudaStream_t s, bool pdl) {
 }  // namespace
 
 bool fwd_tc_supported(int C) { return C == 4 * kFwdChanPerCta || C == 8 * kFwdChanPerCta; }
+
+// Two step parities x clusters x CTAs x one slot (both terms of a CTA's slab): 8 C bytes per
+// row of the padded batch, for whichever row tile (128 or 144) the launch takes.
+size_t fwd_tc_xch_bytes(int B, int C) {
+  const size_t r128 = static_cast<size_t>((B + 127) / 128) * 128;
+  const size_t r144 = static_cast<size_t>((B + 143) / 144) * 144;
+  return 8 * static_cast<size_t>(C) * (r128 > r144 ? r128 : r144);
+}
 
 // `rows`: batch rows per cluster, 128 or 144 (FwdParams::R at launch).
 cudaError_t fwd_tc_prepare(int C, int rows, int* max_active_clusters) {

@@ -34,6 +34,7 @@ struct FwdParams {
   int B, K, C, n_x, n_in;
   int CS;              // CTAs per cluster
   int R;               // batch rows per cluster
+  void* xch;           // tensor-core forward: the exchange buffer (fwd_tc_xch_bytes)
 };
 
 struct BwdParams {
@@ -71,6 +72,9 @@ cudaError_t fwd_launch(const FwdParams& p, int n_clusters, size_t smem, cudaStre
 bool fwd_tc_supported(int C);
 cudaError_t fwd_tc_prepare(int C, int rows, int* max_active_clusters);
 cudaError_t fwd_tc_launch(const FwdParams& p, cudaStream_t s, bool pdl);
+// Bytes of the tensor-core forward's exchange buffer for B rows (either row tile), 16-byte
+// aligned slots.
+size_t fwd_tc_xch_bytes(int B, int C);
 
 // The BPTT recurrence with each step's contraction split along its reduction over a cluster of
 // C / 32 CTAs per NR = 128 or 144 batch rows (rows along the MMA's N side, C = 128 or 256), the

@@ -33,6 +33,10 @@ class KLoopStep:
         self.dh0 = torch.empty((B, C), **f32)
         self.ws = torch.empty(_lib.workspace_bytes(B, K, C, n_x, dw_mode), dtype=torch.uint8,
                               device=dev)
+        # The forward's own workspace (its exchange buffer at large B), apart from ws so that a
+        # forward never overwrites the d_pre a backward left at the head of ws.
+        nf = _lib.forward_workspace_bytes(B, K, C, n_x)
+        self.fws = torch.empty(nf, dtype=torch.uint8, device=dev) if nf else None
         self.inputs = None
         self.graph = None
 
@@ -67,7 +71,7 @@ class KLoopStep:
     def forward(self, stream=None) -> None:
         i = self.inputs
         _lib.cfc_forward(i["u"], i["h0"], i["W"], i["b"], i["ts"], self.H, self.cache,
-                         stream=stream)
+                         ws=self.fws, stream=stream)
 
     def backward(self, stream=None) -> None:
         i = self.inputs

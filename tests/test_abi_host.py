@@ -69,7 +69,8 @@ def test_workspace_holds_d_pre(lib, B, K, C, n_x):
 def test_invalid_dims(lib, B, K, C, n_x):
     assert ws_bytes(lib, B, K, C, n_x)[0] == INVALID_DIM
     fake = ctypes.c_void_p(0x10000)
-    rc = lib.cfc_forward(fake, fake, fake, fake, fake, B, K, C, n_x, fake, fake, None)
+    rc = lib.cfc_forward(fake, fake, fake, fake, fake, B, K, C, n_x, fake, fake, None, 0,
+                         None)
     assert rc == INVALID_DIM
 
 
@@ -87,11 +88,11 @@ def test_null_and_misaligned_pointers(lib):
     for k in range(5):
         a = list(args)
         a[k] = None
-        assert lib.cfc_forward(*a, 4, 8, 32, 16, f, f, None) == NULL_PTR
+        assert lib.cfc_forward(*a, 4, 8, 32, 16, f, f, None, 0, None) == NULL_PTR
         a[k] = odd
-        assert lib.cfc_forward(*a, 4, 8, 32, 16, f, f, None) == MISALIGNED
-    assert lib.cfc_forward(*args, 4, 8, 32, 16, None, f, None) == NULL_PTR
-    assert lib.cfc_forward(*args, 4, 8, 32, 16, f, odd, None) == MISALIGNED
+        assert lib.cfc_forward(*a, 4, 8, 32, 16, f, f, None, 0, None) == MISALIGNED
+    assert lib.cfc_forward(*args, 4, 8, 32, 16, None, f, None, 0, None) == NULL_PTR
+    assert lib.cfc_forward(*args, 4, 8, 32, 16, f, odd, None, 0, None) == MISALIGNED
     # backward: du may be NULL, everything else may not
     b7 = [f] * 7
     outs = [f, f, f, f, f]  # dW, db, du, dh0, ws
@@ -151,7 +152,7 @@ def test_no_device_is_reported_not_crashed(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     f = ctypes.c_void_p(0x10000)
-    assert lib.cfc_forward(*([f] * 5), 4, 8, 32, 16, f, f, None) == UNSUPPORTED
+    assert lib.cfc_forward(*([f] * 5), 4, 8, 32, 16, f, f, None, 0, None) == UNSUPPORTED
     st = ctypes.c_int(0)
     assert lib.cfc_device_status(ctypes.byref(st)) == UNSUPPORTED
 
@@ -191,6 +192,45 @@ def test_bptt_workspace_checked_before_launch(lib):
     assert lib.cfc_backward_recurrence_ws(*args, None, need, None) == NULL_PTR
     assert lib.cfc_backward_recurrence_ws(*args, ctypes.c_void_p(0x10008), need, None) == MISALIGNED
     assert lib.cfc_backward_recurrence_ws(*args, f, need - 16, None) == WS_TOO_SMALL
+
+
+def _fwd_xch_bytes(B, C):
+    """The tensor-core forward's exchange buffer: two step parities x clusters x C / 32 CTAs x
+    one slot (the CTA's slab of h as two fp16 terms, rows x 32 channels x 2 bytes each), for the
+    larger of the two row tiles (128 or 144 rows per cluster) rounded up over B."""
+    rows = max(-(-B // nr) * nr for nr in (128, 144))
+    return 2 * (C // 32) * 2 * rows * 32 * 2
+
+
+@pytest.mark.parametrize("B,C,expect", [(32, 128, 0), (383, 256, 0), (384, 256, _fwd_xch_bytes(384, 256)),
+                                        (767, 128, 0), (768, 128, _fwd_xch_bytes(768, 128)),
+                                        (2048, 256, _fwd_xch_bytes(2048, 256)), (4096, 200, 0)])
+def test_forward_workspace_bytes(lib, B, C, expect):
+    out = ctypes.c_size_t(123)
+    assert lib.cfc_forward_workspace_bytes(B, 8, C, 16, ctypes.byref(out)) == OK
+    assert out.value == expect
+    assert lib.cfc_forward_workspace_bytes(B, 8, C, 16, None) == NULL_PTR
+    assert lib.cfc_forward_workspace_bytes(B, 0, C, 16, ctypes.byref(out)) == INVALID_DIM
+    # cfc_forward_backward's workspace holds the forward's after the backward's own
+    bwd = ctypes.c_size_t(0)
+    assert lib.cfc_workspace_bytes(B, 8, C, 16, 0, ctypes.byref(bwd)) == OK
+    assert bwd.value >= expect + K_ROWS_D_PRE(B, 8, C)
+
+
+def K_ROWS_D_PRE(B, K, C):
+    return K * B * 4 * C * 4
+
+
+def test_forward_workspace_checked_before_launch(lib):
+    f = ctypes.c_void_p(0x10000)
+    need = _fwd_xch_bytes(2048, 256)
+    args = [f] * 5 + [2048, 4, 256, 16, f, f]
+    assert lib.cfc_forward(*args, None, need, None) == NULL_PTR
+    assert lib.cfc_forward(*args, ctypes.c_void_p(0x10008), need, None) == MISALIGNED
+    assert lib.cfc_forward(*args, f, need - 16, None) == WS_TOO_SMALL
+    rargs = [f] * 3 + [2048, 4, 256, 16, f, f]
+    assert lib.cfc_forward_recurrence(*rargs, None, need, None) == NULL_PTR
+    assert lib.cfc_forward_recurrence(*rargs, f, need - 16, None) == WS_TOO_SMALL
 
 
 def test_header_compiles_as_plain_c(tmp_path):
