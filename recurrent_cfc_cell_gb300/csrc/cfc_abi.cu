@@ -200,6 +200,11 @@ size_t fwd_ws_bytes(int B, int C) {
   return (B >= tc_fwd_min_rows(C) && cfc::fwd_tc_supported(C)) ? cfc::fwd_tc_xch_bytes(B, C) : 0;
 }
 
+// The tensor-core recurrence forms the input projection itself (one launch for the forward).
+bool fwd_fused(int B, int C, int n_x) {
+  return fwd_ws_bytes(B, C) > 0 && n_x <= cfc::kFwdFuseMaxInputs;
+}
+
 // CFC_OK when `ws` can hold the forward's workspace (nothing is needed below the tensor-core
 // row threshold, and ws may then be NULL).
 int check_fwd_ws(int B, int C, const void* ws, size_t ws_bytes) {
@@ -321,11 +326,13 @@ namespace {
 // `pdl`: the previous kernel of the stream is one of this library's kernels of the same call
 // (see cfc_launch.cuh).
 // `xch`: the workspace of fwd_ws_bytes(B, C) bytes (checked by the caller; NULL when none is
-// needed).
+// needed).  `u`, `b` (fused form, only where fwd_fused holds): the recurrence forms X = W_u u + b
+// itself and nothing reads X from memory.
 int forward_recurrence(const float* h0, const float* W, const float* ts, int B, int K, int C,
                        int n_x, float* H, float* cache, void* xch, cfc_stream_t stream, bool pdl,
                        const float* xH = nullptr, const float* xcache = nullptr,
-                       bool out_bf16 = false) {
+                       bool out_bf16 = false, const float* u = nullptr,
+                       const float* b = nullptr) {
   int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
   if (!h0 || !W || !ts || !H || !cache) return CFC_ERR_NULL_PTR;
@@ -344,6 +351,8 @@ int forward_recurrence(const float* h0, const float* W, const float* ts, int B, 
   p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
   p.CS = cluster_size_for(C, cfc::kFwdChanPerCta);
   p.xch = xch;
+  p.fuse_u = 0;
+  const bool fuse = u && b;
   if (fwd_ws_bytes(B, C) > 0) {
     if (!xch) return CFC_ERR_NULL_PTR;
     // 128 rows per cluster, or 144 when 128-row clusters would not all be resident at once
@@ -359,9 +368,30 @@ int forward_recurrence(const float* h0, const float* W, const float* ts, int B, 
       if (n144 > 0 && (B + 143) / 144 <= n144) p.R = 144;
     }
     if (n > 0) {
+      if (fuse) {
+        p.u = u;
+        p.bias = b;
+        p.fuse_u = 1;
+      }
       return cuda_rc(cfc::fwd_tc_launch(p, static_cast<cudaStream_t>(stream), pdl),
                      CFC_ERR_LAUNCH_FAILED);
     }
+  }
+  if (fuse) {
+    // The tensor-core clusters cannot be scheduled: the CUDA-core recurrence reads X, which
+    // the projection writes first (into H / cache; bf16 outputs have no room for it).
+    if (out_bf16) return CFC_ERR_UNSUPPORTED_DEVICE;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (B * K >= kTcProjMinRows) {
+      const cfc::TcPlan pl = cfc::proj_tc_plan(B, K, C, n_x);
+      rc = cuda_rc(cfc::proj_tc_launch(pl, u, W, b, B, K, C, n_x, H, cache, st->status, s, pdl),
+                   CFC_ERR_LAUNCH_FAILED);
+    } else {
+      rc = cuda_rc(cfc::inproj_launch(u, W, b, B * K, C, n_x, H, cache, s, pdl),
+                   CFC_ERR_LAUNCH_FAILED);
+    }
+    if (rc != CFC_OK) return rc;
+    pdl = false;
   }
   size_t smem = 0;
   int n_clusters = 0;
@@ -457,6 +487,11 @@ namespace {
 int forward_all(const float* u, const float* h0, const float* W, const float* b,
                 const float* ts, int B, int K, int C, int n_x, float* H, float* cache, void* xch,
                 cfc_stream_t stream) {
+  // Large batches: the tensor-core recurrence forms X itself (X never goes through memory:
+  // at B = 2048, K = 128, C = 256 that is 1.07 GB written and read back).
+  if (fwd_fused(B, C, n_x))
+    return forward_recurrence(h0, W, ts, B, K, C, n_x, H, cache, xch, stream, false, nullptr,
+                              nullptr, false, u, b);
   const int rc = cfc_input_projection(u, W, b, B, K, C, n_x, H, cache, stream);
   if (rc != CFC_OK) return rc;
   // Not a dependent launch: scheduled early, the recurrence clusters land on SMs the
@@ -487,10 +522,11 @@ int cfc_step_launches(int B, int K, int C, int n_x, int dw_mode, int with_du, in
   if (rc != CFC_OK) return rc;
   if (!valid_mode(dw_mode)) return CFC_ERR_INVALID_ARG;
   if (!launches) return CFC_ERR_NULL_PTR;
-  // forward: projection + recurrence; backward: the recurrence (after the W_h^T pre-split on
+  // forward: projection + recurrence (the recurrence alone where it forms the projection
+  // itself); backward: the recurrence (after the W_h^T pre-split on
   // the tensor-core path), then either the operand build, the dW contraction, du and the merge
   // (tensor-core modes), or the dW contraction, its merge, the db sum and du (CUDA cores).
-  int n = 2 + 1 + 3 + (with_du ? 1 : 0);
+  int n = (fwd_fused(B, C, n_x) ? 1 : 2) + 1 + 3 + (with_du ? 1 : 0);
   const BwdLayout L = bwd_layout(B, K, C, n_x, dw_mode);
   if (L.tc_bptt) n += 1;
   if (dw_mode == CFC_DW_TF32) n += 2;  // transposed copies of d_pre and z
@@ -743,8 +779,10 @@ static size_t bf16_x_offset(int B, int K, int C) {
   return align256(static_cast<size_t>(K) * B * C * sizeof(float));
 }
 
-// After X (gate 0, then gates 1-3): the recurrence's own workspace.
-static size_t bf16_xch_offset(int B, int K, int C) {
+// After X (gate 0, then gates 1-3): the recurrence's own workspace.  The fused forward keeps
+// no X: only that workspace.
+static size_t bf16_xch_offset(int B, int K, int C, int n_x) {
+  if (fwd_fused(B, C, n_x)) return 0;
   return align256(bf16_x_offset(B, K, C) + static_cast<size_t>(K) * B * 3 * C * sizeof(float));
 }
 
@@ -753,7 +791,7 @@ int cfc_forward_bf16_workspace_bytes(int B, int K, int C, int n_x, size_t* bytes
   if (rc != CFC_OK) return rc;
   if (C % 2 != 0) return CFC_ERR_INVALID_DIM;
   if (!bytes) return CFC_ERR_NULL_PTR;
-  *bytes = bf16_xch_offset(B, K, C) + fwd_ws_bytes(B, C);
+  *bytes = bf16_xch_offset(B, K, C, n_x) + fwd_ws_bytes(B, C);
   return CFC_OK;
 }
 
@@ -768,6 +806,10 @@ int cfc_forward_bf16(const float* u, const float* h0, const float* W, const floa
       !aligned16(H) || !aligned16(cache) || !aligned16(ws))
     return CFC_ERR_MISALIGNED;
   if (ws_bytes < need) return CFC_ERR_WS_TOO_SMALL;
+  if (fwd_fused(B, C, n_x))
+    return forward_recurrence(h0, W, ts, B, K, C, n_x, static_cast<float*>(H),
+                              static_cast<float*>(cache), ws, stream, false, nullptr, nullptr,
+                              true, u, b);
   // X = W_u u + b in fp32, in the layouts of H and cache, in the workspace; then the
   // recurrence reads it there and stores H and the cache in bf16.
   float* xH = static_cast<float*>(ws);
@@ -776,7 +818,7 @@ int cfc_forward_bf16(const float* u, const float* h0, const float* W, const floa
   if (rc != CFC_OK) return rc;
   return forward_recurrence(h0, W, ts, B, K, C, n_x, static_cast<float*>(H),
                             static_cast<float*>(cache),
-                            static_cast<char*>(ws) + bf16_xch_offset(B, K, C), stream, false,
+                            static_cast<char*>(ws) + bf16_xch_offset(B, K, C, n_x), stream, false,
                             xH, xcache, true);
 }
 

@@ -53,11 +53,18 @@ constexpr int kXchWarp = kEpiWarps + 1;          // lane 0 runs the exchange
 constexpr int kTcThreads = (kEpiWarps + 2) * 32;
 constexpr int kTerms = 2;                        // fp16 terms per operand
 constexpr uint32_t kACol0 = 256;                 // W_h^T terms start here; D^T takes NR columns
+// Fused input projection: W_u^T as three bf16 terms of kUMax / 2 columns each from kUCol0
+// (between D^T's at most 144 columns and W_h^T), u_t as three bf16 terms in shared memory.
+constexpr int kUTerms = 3;
+constexpr int kUMax = 64;                        // inputs the fused form takes (n_x <= 64)
+constexpr uint32_t kUCol0 = 160;
+static_assert(kUMax == kFwdFuseMaxInputs, "fused input width");
+static_assert(kUCol0 + kUTerms * kUMax / 2 <= kACol0, "W_u^T below W_h^T in tensor memory");
 
 // NR: batch rows per cluster (MMA N), 128 or 144.  144 lets 15 clusters cover 2048 rows:
 // GB300 keeps at most 15 clusters of 8 CTAs resident, so 16 clusters of 128 rows ran in two
 // waves.
-template <int CS, int NR>
+template <int CS, int NR, bool FU = false>
 struct TcShape {
   static constexpr int C = kFwdChanPerCta * CS;
   static constexpr int TERM = C * NR * 2;        // bytes of one fp16 term of h
@@ -65,10 +72,17 @@ struct TcShape {
   static constexpr int XSLOT = kTerms * SLAB;    // one CTA's exchange slot: its slab, both terms
   static constexpr int HR = NR / 2;              // rows of one epilogue warp half
   static constexpr int ACOLS = C / 2;            // TMEM columns of one term of W_h^T
-  static constexpr int NBARS = 3 * CS + 2;       // full[CS], done, fin, ready[2][CS]
+  // u_t (fused form): [k / 8][n / 8][8 rows][16 B] with k groups ULBO bytes apart, 16 more than
+  // packed, so that lanes storing eight k groups of one row hit eight different bank groups.
+  static constexpr int ULBO = NR * 16 + 16;
+  static constexpr int UTERM = kUMax / 8 * ULBO;  // bytes of one bf16 term of u_t
+  static constexpr int UBYTES = FU ? kUTerms * UTERM : 0;
+  static constexpr int NBARS = 3 * CS + 3;       // full[CS], done, fin, ufull, ready[2][CS]
   static_assert(NR % 16 == 0 && HR % 8 == 0 && NR <= 256, "row tile");
-  // h terms, each epilogue warp's ts, barriers, TMEM slot, alignment.
-  static constexpr int USED = kTerms * TERM + kEpiWarps * HR * 4 + NBARS * 8 + 16 + 128;
+  static_assert(NR <= static_cast<int>(kUCol0), "D^T below W_u^T");
+  // h terms, u terms, each epilogue warp's ts, barriers, TMEM slot, alignment.
+  static constexpr int USED =
+      kTerms * TERM + UBYTES + kEpiWarps * HR * 4 + NBARS * 8 + 16 + 128;
   // At least half an SM's shared memory: a CTA takes all 512 tensor-memory columns, so two
   // CTAs on one SM would leave the second waiting in tcgen05.alloc while its cluster waits on
   // it.
@@ -92,6 +106,44 @@ __device__ __forceinline__ uint32_t pack2(__half lo, __half hi) {
 __host__ __device__ constexpr uint32_t umma_idesc_f16in(int M, int N) {
   return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Three bf16 terms x = hi + mid + lo (8 significand bits each, so the three carry all 24 of
+// fp32; each difference is exact in fp32), packed in pairs: pk[term] = (term of a, of b).
+__device__ __forceinline__ void split3_pair(float a, float b, uint32_t (&pk)[kUTerms]) {
+  const __nv_bfloat16 ah = __float2bfloat16_rn(a), bh = __float2bfloat16_rn(b);
+  const float ar = a - __bfloat162float(ah), br = b - __bfloat162float(bh);
+  const __nv_bfloat16 am = __float2bfloat16_rn(ar), bm = __float2bfloat16_rn(br);
+  const __nv_bfloat16 al = __float2bfloat16_rn(ar - __bfloat162float(am));
+  const __nv_bfloat16 bl = __float2bfloat16_rn(br - __bfloat162float(bm));
+  pk[0] = static_cast<uint32_t>(__bfloat16_as_ushort(ah)) |
+          (static_cast<uint32_t>(__bfloat16_as_ushort(bh)) << 16);
+  pk[1] = static_cast<uint32_t>(__bfloat16_as_ushort(am)) |
+          (static_cast<uint32_t>(__bfloat16_as_ushort(bm)) << 16);
+  pk[2] = static_cast<uint32_t>(__bfloat16_as_ushort(al)) |
+          (static_cast<uint32_t>(__bfloat16_as_ushort(bl)) << 16);
+}
+
+// Loads issued where they stand: prefetches into registers for the next step would otherwise
+// be moved down to their use by the compiler, and their latency would land on the step's
+// critical path.  (Read-only data; the global address of `p`.)
+__device__ __forceinline__ float4 ld_early_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_early(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+// Data another launch of this stream wrote (X from the projection): the L2 copy.
+__device__ __forceinline__ float ld_early_cg(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
 }
 
 // Byte offset of element (row n, k) in one h term of NR rows: [k / 8][n / 8][n % 8][k % 8].
@@ -136,6 +188,17 @@ __device__ __forceinline__ void umma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// 16 consecutive 32-bit tensor-memory columns of this thread's lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
 // 32 consecutive 32-bit tensor-memory columns of this thread's lane.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
@@ -150,16 +213,19 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
-template <int CS, int NR, bool BF>
+// FU: the input projection is fused (X = W_u u_t + b is not read from memory: u_t enters the
+// step's contraction, b the epilogue).
+template <int CS, int NR, bool BF, bool FU>
 __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdParams p) {
-  using S = TcShape<CS, NR>;
+  using S = TcShape<CS, NR, FU>;
   constexpr int HR = S::HR;
   constexpr int C = S::C;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t* sm = smem_raw + ((128u - (raw & 127u)) & 127u);
   uint8_t* hb = sm;                                                     // [2][TERM]
-  float* ts_w = reinterpret_cast<float*>(sm + kTerms * S::TERM);        // [kEpiWarps][HR]
+  uint8_t* ub = sm + kTerms * S::TERM;                                  // FU: [3][UTERM]
+  float* ts_w = reinterpret_cast<float*>(ub + S::UBYTES);               // [kEpiWarps][HR]
   uint64_t* bars = reinterpret_cast<uint64_t*>(ts_w + kEpiWarps * HR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + S::NBARS);
 
@@ -173,7 +239,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
   const uint32_t full0 = smem_addr(&bars[0]);          // full[j]: slab j of the step's h in place
   const uint32_t done_bar = smem_addr(&bars[CS]);      // this CTA's MMAs of the step are done
   const uint32_t fin_bar = smem_addr(&bars[CS + 1]);   // every MMA of this CTA is done (exit)
-  const uint32_t ready0 = smem_addr(&bars[CS + 2]);    // ready[par][j]: CTA j's slab is in L2
+  const uint32_t ufull = smem_addr(&bars[CS + 2]);     // FU: u of the step in place, D^T free
+  const uint32_t ready0 = smem_addr(&bars[CS + 3]);    // ready[par][j]: CTA j's slab is in L2
+  const int KU = (n_x + 15) & ~15;                     // FU: inputs padded to whole MMA steps
   uint8_t* const xch = static_cast<uint8_t*>(p.xch);
   // Exchange slot of CTA r of this cluster for step parity par.
   auto slot = [&](int par, int r) {
@@ -186,6 +254,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
     for (int j = 0; j < CS; ++j) mbar_init(full0 + 8u * j, j == rank ? kEpiWarps : 1);
     mbar_init(done_bar, 1);
     mbar_init(fin_bar, 1);
+    mbar_init(ufull, kEpiWarps);
     for (int i = 0; i < 2 * CS; ++i) mbar_init(ready0 + 8u * i, kEpiWarps);
     fence_mbar_init_cluster();
   }
@@ -193,7 +262,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
     tmem_alloc(smem_addr(tslot), 512);
     tc_fence_before_sync();
   }
-  // X comes from the projection kernel in place in H / cache: wait for it before any read.
+  // X comes from the projection kernel in place in H / cache (unfused form), and the previous
+  // kernel may still read what this one writes: wait for it before any global access.
   grid_dep_wait();
   __syncthreads();
   tc_fence_after_sync();
@@ -204,6 +274,64 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
   const int q = warp & 3, hh = (warp >> 2) & 1;
   const int c = (32 * q + lane) >> 2, g = lane & 3;
   const int ch = kFwdChanPerCta * rank + c;
+
+  // FU: u_t of the cluster's rows -> the three bf16 terms of the u operand (epilogue warps,
+  // loaded into registers one step ahead).  Item (row n, inputs k0 .. k0 + 7), the eight k
+  // groups of a row in eight consecutive lanes: a warp's loads touch 4 rows (8 lines of 128
+  // bytes, not 32), and its 16-byte stores, with the k groups ULBO apart, 32 distinct bank
+  // slots per 128 bytes.  Zero beyond B and n_x.
+  constexpr int kUItems = (NR * kUMax / 8 + kEpiWarps * 32 - 1) / (kEpiWarps * 32);
+  float un[FU ? kUItems : 1][8];
+  auto load_u = [&](int t) {
+    if constexpr (FU) {
+      const bool vec = (n_x & 3) == 0;
+#pragma unroll
+      for (int m = 0; m < kUItems; ++m) {
+        const int it = tid + m * kEpiWarps * 32;
+        const int n = it / (kUMax / 8), k0 = 8 * (it % (kUMax / 8)), b = row0 + n;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) un[m][i] = 0.f;
+        if (n < NR && k0 < KU && b < B) {
+          const float* src = p.u + (static_cast<size_t>(t) * B + b) * n_x + k0;
+          if (vec && k0 + 8 <= n_x) {
+            const float4 q0 = ld_early_f4(src);
+            const float4 q1 = ld_early_f4(src + 4);
+            un[m][0] = q0.x; un[m][1] = q0.y; un[m][2] = q0.z; un[m][3] = q0.w;
+            un[m][4] = q1.x; un[m][5] = q1.y; un[m][6] = q1.z; un[m][7] = q1.w;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (k0 + i < n_x) un[m][i] = ld_early(src + i);
+          }
+        }
+      }
+    }
+  };
+  auto store_u = [&]() {
+    if constexpr (FU) {
+#pragma unroll
+      for (int m = 0; m < kUItems; ++m) {
+        const int it = tid + m * kEpiWarps * 32;
+        const int n = it / (kUMax / 8), k0 = 8 * (it % (kUMax / 8));
+        if (n < NR && k0 < KU) {
+          uint32_t w[kUTerms][4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t pk[kUTerms];
+            split3_pair(un[m][2 * i], un[m][2 * i + 1], pk);
+#pragma unroll
+            for (int tm = 0; tm < kUTerms; ++tm) w[tm][i] = pk[tm];
+          }
+          const uint32_t off = static_cast<uint32_t>((k0 >> 3) * S::ULBO + (n >> 3) * 128 +
+                                                     (n & 7) * 16);
+#pragma unroll
+          for (int tm = 0; tm < kUTerms; ++tm)
+            *reinterpret_cast<uint4*>(ub + tm * S::UTERM + off) =
+                make_uint4(w[tm][0], w[tm][1], w[tm][2], w[tm][3]);
+        }
+      }
+    }
+  };
 
   float wunscale = 1.f;  // 2^e: this lane's W row was scaled by 2^-e before the split
   if (warp < kEpiWarps) {
@@ -228,6 +356,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
       const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + kACol0 + k0 / 2;
       tmem_st32(ta, r0);
       tmem_st32(ta + S::ACOLS, r1);
+    }
+    if constexpr (FU) {
+      // ---- W_u^T (same row scale) -> tensor memory, three bf16 terms; the two warps of a
+      // lane quarter take inputs 0 .. 31 and 32 .. 63 (zero beyond n_x). ----
+      const float* urow = p.W + (static_cast<size_t>(g) * C + ch) * n_in;
+      uint32_t r[kUTerms][16];
+#pragma unroll
+      for (int cc = 0; cc < 16; ++cc) {
+        const int k = kUMax / 2 * hh + 2 * cc;
+        const float a = (k < n_x) ? __ldg(urow + k) * wscale : 0.f;
+        const float b = (k + 1 < n_x) ? __ldg(urow + k + 1) * wscale : 0.f;
+        uint32_t pk[kUTerms];
+        split3_pair(a, b, pk);
+#pragma unroll
+        for (int tm = 0; tm < kUTerms; ++tm) r[tm][cc] = pk[tm];
+      }
+      const uint32_t tu = tmem + (static_cast<uint32_t>(32 * q) << 16) + kUCol0 + 16 * hh;
+#pragma unroll
+      for (int tm = 0; tm < kUTerms; ++tm) tmem_st16(tu + tm * (kUMax / 2), r[tm]);
+      load_u(0);
+      store_u();
+      if (K > 1) load_u(1);
     }
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     // ---- h0 -> this CTA's slab of the h buffer and its exchange slot of step parity 0
@@ -258,8 +408,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
     // The h0 slab is in place here and in L2: mark it full and announce it.
     fence_acq_rel_gpu();
     __syncwarp();
-    if (lane == 0) mbar_arrive(full0 + 8u * rank);
-    else if (lane < CS) mbar_arrive_remote(map_to_rank(ready0 + 8u * rank, (rank + lane) % CS));
+    if (lane == 0) {
+      mbar_arrive(full0 + 8u * rank);
+      if (FU) mbar_arrive(ufull);  // u_0 in place (written before the CTA barrier above)
+    } else if (lane < CS) {
+      mbar_arrive_remote(map_to_rank(ready0 + 8u * rank, (rank + lane) % CS));
+    }
   }
 
   if (warp == kCtlWarp) {
@@ -267,6 +421,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_f16in(kGC, NR);
       const uint64_t bdesc0 = desc_kmajor(smem_addr(hb), (NR / 8) * 128, 128);
+      const uint32_t idesc_u = umma_idesc_bf16(kGC, NR);
+      const uint64_t udesc0 = desc_kmajor(smem_addr(ub), S::ULBO, 128);
       bool ok = true;
       for (int t = 0; t < K && ok; ++t) {
         uint32_t acc = 0;
@@ -288,6 +444,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
             acc = 1;
             umma_tmem_a(tmem, a0, d1, idesc, 1);
             umma_tmem_a(tmem, a0 + S::ACOLS, d0, idesc, 1);
+          }
+          if (FU && jj == 0) {
+            // W_u u_t right after the own slab (whose wait also says the epilogue has read
+            // D^T), while the other CTAs' slabs are still on their way.
+            ok = mbar_wait_bounded_cta(ufull, t & 1, p.status);
+            if (!ok) break;
+            tc_fence_after_sync();
+            for (int s = 0; s < KU / 16; ++s) {
+              const uint32_t a0 = tmem + kUCol0 + 8 * s;
+              const uint64_t d0 = udesc0 + static_cast<uint64_t>(s * ((2 * S::ULBO) >> 4));
+              constexpr uint32_t UT = S::UTERM >> 4, AT = kUMax / 2;
+              // (A term, B term): hi*hi, hi*mid, mid*hi, hi*lo, lo*hi, mid*mid
+              umma_tmem_a(tmem, a0, d0, idesc_u, 1);
+              umma_tmem_a(tmem, a0, d0 + UT, idesc_u, 1);
+              umma_tmem_a(tmem, a0 + AT, d0, idesc_u, 1);
+              umma_tmem_a(tmem, a0, d0 + 2 * UT, idesc_u, 1);
+              umma_tmem_a(tmem, a0 + 2 * AT, d0, idesc_u, 1);
+              umma_tmem_a(tmem, a0 + AT, d0 + UT, idesc_u, 1);
+            }
           }
         }
         if (ok) umma_commit(done_bar);
@@ -340,19 +515,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
     if (armed >= 0) (void)mbar_wait_bounded_cta(full0 + 8u * j, armed & 1, p.status);
   } else {
     // ================= epilogue warps =================
-    // X of (gate g, channel ch) for rows row0 + HR hh + i, i < HR, of step t, in the layout of
-    // H (gate 0) or cache (gates 1-3): in place there unless the outputs are bf16.
+    // Unfused: X of (gate g, channel ch) for rows row0 + HR hh + i, i < HR, of step t, in the
+    // layout of H (gate 0) or cache (gates 1-3): in place there unless the outputs are bf16.
+    // Fused: the bias of (gate g, channel ch) instead.
     const size_t xrow = (g == 0) ? static_cast<size_t>(C) : 3ull * C;
     const float* xbase = ((g == 0) ? p.xH : p.xcache + static_cast<size_t>(g - 1) * C) + ch;
     constexpr bool obf = BF;  // H and the cache stored as bf16
     const int rfirst = row0 + HR * hh;
     int nvalid = B - rfirst;
     nvalid = nvalid < 0 ? 0 : (nvalid > HR ? HR : nvalid);
-    float xv[HR];
+    const float bv = FU ? __ldg(p.bias + g * C + ch) : 0.f;
+    float xv[FU ? 1 : HR];
     auto load_x = [&](int t) {
-      const float* xp = xbase + (static_cast<size_t>(t) * B + rfirst) * xrow;
+      if constexpr (!FU) {
+        const float* xp = xbase + (static_cast<size_t>(t) * B + rfirst) * xrow;
 #pragma unroll
-      for (int i = 0; i < HR; ++i) xv[i] = (i < nvalid) ? __ldcg(xp + i * xrow) : 0.f;
+        for (int i = 0; i < HR; ++i) xv[i] = (i < nvalid) ? ld_early_cg(xp + i * xrow) : 0.f;
+      }
     };
     // ts of the next step for this warp's rows: lane i holds rows i, i + 32, ...
     constexpr int kTsPerLane = (HR + 31) / 32;
@@ -389,7 +568,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
         auto rows = [&](float (&P)[16], int ibase, int n) {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            if (i < n) P[i] = fmaf(P[i], wunscale, xv[ibase + i]);
+            if (i < n) P[i] = fmaf(P[i], wunscale, FU ? bv : xv[FU ? 0 : ibase + i]);
 #pragma unroll
           for (int i0 = 0; i0 < 16; i0 += 4) {
             if (i0 >= n) break;
@@ -468,7 +647,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
         else if (lane < CS)
           mbar_arrive_remote(
               map_to_rank(ready0 + 8u * (((t + 1) & 1) * CS + rank), (rank + lane) % CS));
-        load_x(t + 1);  // in flight while the exchange and the next step's MMAs run
+        if constexpr (FU) {
+          // u_{t+1} (in registers) -> the u operand (the MMAs of step t that read it are done:
+          // `done` was waited above); then the loads of u_{t+2}.
+          store_u();
+          if (t + 2 < K) load_u(t + 2);
+          fence_proxy_async_smem();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ufull);
+        } else {
+          load_x(t + 1);  // in flight while the exchange and the next step's MMAs run
+        }
         load_ts(t + 1);
       }
     }
@@ -492,21 +682,24 @@ cudaError_t prepare_k(int* max_active) {
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
-  const int smem = TcShape<CS, NR>::SMEM;
-  if (smem > optin) {
+  // The fused form needs the most shared memory; the occupancy asked for is its.
+  const int smem = TcShape<CS, NR, false>::SMEM, smem_fu = TcShape<CS, NR, true>::SMEM;
+  if (smem_fu > optin) {
     *max_active = 0;
     return cudaSuccess;
   }
-  // Both output dtypes: same launch bounds and shared memory, so the same occupancy.
-  auto* kern = cfc_fwd_tc_kernel<CS, NR, false>;
-  for (auto* k : {cfc_fwd_tc_kernel<CS, NR, false>, cfc_fwd_tc_kernel<CS, NR, true>}) {
+  for (auto* k : {cfc_fwd_tc_kernel<CS, NR, false, false>, cfc_fwd_tc_kernel<CS, NR, true, false>}) {
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  for (auto* k : {cfc_fwd_tc_kernel<CS, NR, false, true>, cfc_fwd_tc_kernel<CS, NR, true, true>}) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_fu);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CS, 1, 1);
   cfg.blockDim = dim3(kTcThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = smem_fu;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CS;
@@ -514,7 +707,7 @@ cudaError_t prepare_k(int* max_active) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(max_active, kern, &cfg);
+  return cudaOccupancyMaxActiveClusters(max_active, cfc_fwd_tc_kernel<CS, NR, false, true>, &cfg);
 }
 
 template <int CS, int NR>
@@ -522,12 +715,15 @@ cudaError_t launch_k(const FwdParams& p, cudaStream_t s, bool pdl) {
   LaunchCfg c;
   c.grid = dim3(((p.B + NR - 1) / NR) * CS, 1, 1);
   c.block = dim3(kTcThreads, 1, 1);
-  c.smem = TcShape<CS, NR>::SMEM;
+  c.smem = p.fuse_u ? TcShape<CS, NR, true>::SMEM : TcShape<CS, NR, false>::SMEM;
   c.stream = s;
   c.pdl = pdl;
   c.cluster = dim3(CS, 1, 1);
-  return p.out_bf16 ? launch(c, cfc_fwd_tc_kernel<CS, NR, true>, p)
-                    : launch(c, cfc_fwd_tc_kernel<CS, NR, false>, p);
+  if (p.fuse_u)
+    return p.out_bf16 ? launch(c, cfc_fwd_tc_kernel<CS, NR, true, true>, p)
+                      : launch(c, cfc_fwd_tc_kernel<CS, NR, false, true>, p);
+  return p.out_bf16 ? launch(c, cfc_fwd_tc_kernel<CS, NR, true, false>, p)
+                    : launch(c, cfc_fwd_tc_kernel<CS, NR, false, false>, p);
 }
 
 }  // namespace

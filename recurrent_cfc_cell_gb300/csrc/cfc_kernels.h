@@ -35,6 +35,8 @@ struct FwdParams {
   int CS;              // CTAs per cluster
   int R;               // batch rows per cluster
   void* xch;           // tensor-core forward: the exchange buffer (fwd_tc_xch_bytes)
+  int fuse_u;          // tensor-core forward: X = W_u u + b formed in the step (u, bias set),
+                       // not read from xH / xcache; needs n_x <= kFwdFuseMaxInputs
 };
 
 struct BwdParams {
@@ -70,6 +72,8 @@ cudaError_t fwd_launch(const FwdParams& p, int n_clusters, size_t smem, cudaStre
 // C / 32 CTAs serving 128 or 144 batch rows each, FwdParams::R; C = 128 or 256).  X in place
 // in H / cache as for fwd_launch.
 bool fwd_tc_supported(int C);
+// Inputs up to which the tensor-core forward can form the input projection itself.
+constexpr int kFwdFuseMaxInputs = 64;
 cudaError_t fwd_tc_prepare(int C, int rows, int* max_active_clusters);
 cudaError_t fwd_tc_launch(const FwdParams& p, cudaStream_t s, bool pdl);
 // Bytes of the tensor-core forward's exchange buffer for B rows (either row tile), 16-byte

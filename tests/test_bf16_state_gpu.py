@@ -26,7 +26,7 @@ BF16_GRAD_TOL = 2.0 ** -6
 # the tensor-core recurrences (C = 256 from 129 rows for the BPTT, 384 for the forward).
 SHAPES = [dict(B=32, K=64, n_x=48, C=128), dict(B=7, K=11, n_x=13, C=100),
           dict(B=500, K=4, n_x=16, C=128), dict(B=200, K=5, n_x=8, C=256),
-          dict(B=800, K=4, n_x=16, C=256)]
+          dict(B=800, K=4, n_x=16, C=256), dict(B=400, K=3, n_x=80, C=256)]
 
 
 def _ids(s):

@@ -41,6 +41,9 @@ RAGGED = [
     dict(B=1030, K=3, n_x=16, C=256),  # tensor-core BPTT at the widest state, last CTA 6 rows
     dict(B=2050, K=3, n_x=16, C=256),  # tensor-core forward with 144-row clusters (15 of them
                                        # cover 2160 rows), the last one 34 rows
+    dict(B=400, K=3, n_x=100, C=256),  # tensor-core forward too wide in n_x to form the
+                                       # projection itself: projection kernel, then X read
+    dict(B=790, K=4, n_x=61, C=128),   # fused projection, n_x not a multiple of 4 or 16
 ]
 
 
@@ -51,11 +54,12 @@ def test_ragged_parity(shape):
 
 
 @pytest.mark.parametrize("shape", [dict(B=32, K=64, n_x=48, C=128), dict(B=7, K=11, n_x=13, C=100),
-                                   dict(B=5, K=6, n_x=64, C=256)],
+                                   dict(B=5, K=6, n_x=64, C=256), dict(B=600, K=4, n_x=24, C=256)],
                          ids=lambda s: "B{B}_K{K}_nx{n_x}_C{C}".format(**s))
 def test_two_stage_forward_matches_oracle(shape):
-    """The two stage entry points cfc_forward is made of, called one after the other: the
-    projection kernel, then the recurrence that reads X from H / cache."""
+    """The two stage entry points, called one after the other: the projection kernel, then the
+    recurrence that reads X from H / cache (cfc_forward itself, at the tensor-core batch sizes,
+    forms the projection inside the recurrence)."""
     import torch
 
     from recurrent_cfc_cell_gb300 import _lib, build
