@@ -109,19 +109,22 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16in(int M, int N) {
 }
 
 // Three bf16 terms x = hi + mid + lo (8 significand bits each, so the three carry all 24 of
-// fp32; each difference is exact in fp32), packed in pairs: pk[term] = (term of a, of b).
+// fp32; each difference is exact in fp32), packed in pairs: pk[term] = (term of a, of b) with
+// a in the low half.  One packed conversion per term; a bf16 value widens to fp32 by a 16-bit
+// shift (conversions share the narrow pipe with the cell's exponentials and reciprocals).
+__device__ __forceinline__ float bf16_lo_f32(uint32_t pk) { return __uint_as_float(pk << 16); }
+__device__ __forceinline__ float bf16_hi_f32(uint32_t pk) {
+  return __uint_as_float(pk & 0xFFFF0000u);
+}
+__device__ __forceinline__ uint32_t bf16x2_rn(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);  // .x = a (low half), .y = b
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
 __device__ __forceinline__ void split3_pair(float a, float b, uint32_t (&pk)[kUTerms]) {
-  const __nv_bfloat16 ah = __float2bfloat16_rn(a), bh = __float2bfloat16_rn(b);
-  const float ar = a - __bfloat162float(ah), br = b - __bfloat162float(bh);
-  const __nv_bfloat16 am = __float2bfloat16_rn(ar), bm = __float2bfloat16_rn(br);
-  const __nv_bfloat16 al = __float2bfloat16_rn(ar - __bfloat162float(am));
-  const __nv_bfloat16 bl = __float2bfloat16_rn(br - __bfloat162float(bm));
-  pk[0] = static_cast<uint32_t>(__bfloat16_as_ushort(ah)) |
-          (static_cast<uint32_t>(__bfloat16_as_ushort(bh)) << 16);
-  pk[1] = static_cast<uint32_t>(__bfloat16_as_ushort(am)) |
-          (static_cast<uint32_t>(__bfloat16_as_ushort(bm)) << 16);
-  pk[2] = static_cast<uint32_t>(__bfloat16_as_ushort(al)) |
-          (static_cast<uint32_t>(__bfloat16_as_ushort(bl)) << 16);
+  pk[0] = bf16x2_rn(a, b);
+  const float ar = a - bf16_lo_f32(pk[0]), br = b - bf16_hi_f32(pk[0]);
+  pk[1] = bf16x2_rn(ar, br);
+  pk[2] = bf16x2_rn(ar - bf16_lo_f32(pk[1]), br - bf16_hi_f32(pk[1]));
 }
 
 // Loads issued where they stand: prefetches into registers for the next step would otherwise
