@@ -93,6 +93,12 @@ def peaks():
 
 
 # ---------------------------------------------------------------- algorithmic work per unit
+def fwd_fused(w) -> bool:
+    """cfc_forward forms the input projection inside the tensor-core recurrence (B >= 384 at
+    C = 256, B >= 768 at C = 128, n_x <= 64): one launch, no X in memory."""
+    return w.C in (128, 256) and w.B >= (384 if w.C == 256 else 768) and w.n_x <= 64
+
+
 def work_per_unit(w):
     """FLOPs and HBM bytes per (batch row, step) of each stage (fp32 = 4 bytes)."""
     C, n_x, n_in = w.C, w.n_x, w.n_in
@@ -101,6 +107,12 @@ def work_per_unit(w):
         "proj": {"flop": 8 * C * n_x, "bytes": 4 * (n_x + 4 * C)},
         # forward recurrence: W_h h_{t-1} (4C x C); reads X and ts, writes h_t and the cache
         "fwd_rec": {"flop": 8 * C * C, "bytes": 4 * (4 * C + 1 + 4 * C)},
+        # the whole forward as cfc_forward runs it: projection and recurrence; where the
+        # tensor-core recurrence forms the projection itself X never goes through memory
+        # (reads u and ts, writes h_t and the cache), otherwise both stages' bytes
+        "fwd": {"flop": 8 * C * n_x + 8 * C * C,
+                "bytes": (4 * (n_x + 1 + 4 * C) if fwd_fused(w)
+                          else 4 * (n_x + 4 * C) + 4 * (4 * C + 1 + 4 * C))},
         # BPTT recurrence: W_h^T d_pre (4C x C); reads dH, cache, ts; writes d_pre
         "bwd_rec": {"flop": 8 * C * C, "bytes": 4 * (C + 3 * C + 1 + 4 * C)},
         # dW contraction (4C x n_in per row) + du (4C x n_x) + db; reads d_pre, u, h
@@ -377,7 +389,8 @@ def measure_peaks(torch, _lib, dev) -> dict:
 # ---------------------------------------------------------------- stage timing
 def stage_times(torch, _lib, st, flush, stream, n: int) -> dict:
     """Device time of each stage of one step, CUDA events between the stage calls, L2 flushed
-    before each group: the projection, the forward recurrence, the BPTT recurrence (into an
+    before each group: the whole forward (cfc_forward, as the step runs it), then its two stage
+    entry points (the projection, the forward recurrence), the BPTT recurrence (into an
     fp32 d_pre at the workspace head, the same kernels as in the step), the standalone gradient
     stage (cfc_weight_grad from that fp32 d_pre), and the whole cfc_backward.  "grad" is the
     gradient chain as cfc_backward runs it (BPTT writing the contraction's operand rows
@@ -387,6 +400,7 @@ def stage_times(torch, _lib, st, flush, stream, n: int) -> dict:
     bptt_ws = torch.empty(n_bptt, dtype=torch.uint8, device=st.device) if n_bptt else None
     d32 = st.d_pre_fp32_view
     stages = [
+        ("fwd", lambda: st.forward()),
         ("proj", lambda: _lib.cfc_input_projection(i["u"], i["W"], i["b"], st.H, st.cache)),
         ("fwd_rec", lambda: _lib.cfc_forward_recurrence(i["h0"], i["W"], i["ts"], st.H,
                                                        st.cache, ws=st.fws)),
@@ -416,7 +430,7 @@ def kernel_table(w, stage_ms: dict, pk: dict, mp: dict | None) -> dict:
     wpu = work_per_unit(w)
     fp32_peak = mp["fp32_fma_tflops"] if mp else None
     tab = {}
-    for name in ("proj", "fwd_rec", "bwd_rec", "grad"):
+    for name in ("fwd", "proj", "fwd_rec", "bwd_rec", "grad"):
         t = stage_ms[name]
         flop = wpu[name]["flop"] * w.units
         byt = wpu[name]["bytes"] * w.units
@@ -739,14 +753,16 @@ def main():
     kernels = kernel_table(w, stage_ms, pk, mp)
     n_bptt_ws = _lib.bptt_workspace_bytes(w.B, w.K, w.C, w.n_x)
     # The dominant kernel: the larger of the two recurrences (each stage is one launch).
-    dominant = max(("fwd_rec", "bwd_rec"), key=lambda k: stage_ms[k])
+    # (Where the forward forms the projection itself, its stage is the whole cfc_forward.)
+    fwd_key = "fwd" if fwd_fused(w) else "fwd_rec"
+    dominant = max((fwd_key, "bwd_rec"), key=lambda k: stage_ms[k])
     # Which kernel that stage ran: the tensor-core recurrences serve batches of at least 384
     # (forward) or 129 (BPTT) rows at C = 256, 768 or 513 at C = 128; the CUDA-core ones
     # the rest.
     tc_fwd = w.C in (128, 256) and w.B >= (384 if w.C == 256 else 768)
-    tc = tc_fwd if dominant == "fwd_rec" else n_bptt_ws > 0
+    tc = tc_fwd if dominant == fwd_key else n_bptt_ws > 0
     kname = {("fwd_rec", False): "cfc_fwd_kernel", ("bwd_rec", False): "cfc_bwd_kernel",
-             ("fwd_rec", True): "cfc_fwd_tc_kernel",
+             ("fwd_rec", True): "cfc_fwd_tc_kernel", ("fwd", True): "cfc_fwd_tc_kernel",
              ("bwd_rec", True): "cfc_bwd_l2x_kernel"}[(dominant, tc)]
     ksrc = ["recurrent_cfc_cell_gb300/csrc/" + kname[: -len("_kernel")] + ".cu",
             "recurrent_cfc_cell_gb300/csrc/cfc_ptx.cuh",

@@ -79,11 +79,6 @@ struct XShape {
   static_assert(W_BYTES % kWPiece == 0, "W image pieces");
 };
 
-__device__ __forceinline__ uint32_t pack_b2(__nv_bfloat16 lo, __nv_bfloat16 hi) {
-  return static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
-         (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
-}
-
 __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
   return static_cast<uint32_t>(__half_as_ushort(lo)) |
          (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
@@ -501,13 +496,11 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_l2x_kernel(const BwdParam
                                    row * 2 * static_cast<size_t>(p.dpitch) + ch;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
-                  const __nv_bfloat16 h0 = __float2bfloat16_rn(pv[i][0][g]);
-                  const __nv_bfloat16 h1 = __float2bfloat16_rn(pv[i][1][g]);
-                  *reinterpret_cast<uint32_t*>(q + static_cast<size_t>(g) * C) = pack_b2(h0, h1);
+                  uint32_t hi2, lo2;
+                  bf16_split2_pair(pv[i][0][g], pv[i][1][g], hi2, lo2);
+                  *reinterpret_cast<uint32_t*>(q + static_cast<size_t>(g) * C) = hi2;
                   if (p.dplanes == 2)
-                    *reinterpret_cast<uint32_t*>(q + p.dpitch + static_cast<size_t>(g) * C) =
-                        pack_b2(__float2bfloat16_rn(pv[i][0][g] - __bfloat162float(h0)),
-                                __float2bfloat16_rn(pv[i][1][g] - __bfloat162float(h1)));
+                    *reinterpret_cast<uint32_t*>(q + p.dpitch + static_cast<size_t>(g) * C) = lo2;
                 }
               }
             }
@@ -535,10 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1) cfc_bwd_l2x_kernel(const BwdParam
 #pragma unroll
               for (int gp = 0; gp < 2; ++gp) {
                 const float x0 = pv[i][c][2 * gp] * sc, x1 = pv[i][c][2 * gp + 1] * sc;
-                const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-                hw[2 * c + gp] = pack_h2(h0, h1);
-                lw[2 * c + gp] = pack_h2(__float2half_rn(x0 - __half2float(h0)),
-                                         __float2half_rn(x1 - __half2float(h1)));
+                f16_split2_pair(x0, x1, hw[2 * c + gp], lw[2 * c + gp]);
               }
             // k = 8 cp .. 8 cp + 7 of row rr[i]: one 16-byte chunk per term.
             const uint32_t off = b_offset<NR>(rr[i], cp);

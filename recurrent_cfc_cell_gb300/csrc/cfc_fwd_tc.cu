@@ -110,16 +110,7 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16in(int M, int N) {
 
 // Three bf16 terms x = hi + mid + lo (8 significand bits each, so the three carry all 24 of
 // fp32; each difference is exact in fp32), packed in pairs: pk[term] = (term of a, of b) with
-// a in the low half.  One packed conversion per term; a bf16 value widens to fp32 by a 16-bit
-// shift (conversions share the narrow pipe with the cell's exponentials and reciprocals).
-__device__ __forceinline__ float bf16_lo_f32(uint32_t pk) { return __uint_as_float(pk << 16); }
-__device__ __forceinline__ float bf16_hi_f32(uint32_t pk) {
-  return __uint_as_float(pk & 0xFFFF0000u);
-}
-__device__ __forceinline__ uint32_t bf16x2_rn(float a, float b) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);  // .x = a (low half), .y = b
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
+// a in the low half, one packed conversion per term.
 __device__ __forceinline__ void split3_pair(float a, float b, uint32_t (&pk)[kUTerms]) {
   pk[0] = bf16x2_rn(a, b);
   const float ar = a - bf16_lo_f32(pk[0]), br = b - bf16_hi_f32(pk[0]);

@@ -2,8 +2,11 @@
 // distributed shared memory, mbarriers, asynchronous remote stores (st.async), and bounded
 // waits that report a timeout instead of spinning forever.
 #pragma once
-#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
+
+#include <cstdint>
 
 namespace cfc {
 
@@ -360,6 +363,35 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
 __device__ __forceinline__ uint32_t sw128_offset(int row, int k) {
   return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 +
                                ((((k >> 3) ^ (row & 7)) & 7) << 4) + ((k & 7) << 1));
+}
+
+// ---- packed conversions: one instruction converts two values, and a bf16 widens to fp32 by
+// a 16-bit shift.  (Conversions share a narrow pipe with the exponentials and reciprocals.)
+// Packed pairs hold the first value in the low half.
+__device__ __forceinline__ uint32_t bf16x2_rn(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);  // .x = a (low half), .y = b
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ float bf16_lo_f32(uint32_t pk) { return __uint_as_float(pk << 16); }
+__device__ __forceinline__ float bf16_hi_f32(uint32_t pk) {
+  return __uint_as_float(pk & 0xFFFF0000u);
+}
+__device__ __forceinline__ uint32_t f16x2_rn(float a, float b) {
+  const __half2 v = __floats2half2_rn(a, b);  // .x = a (low half), .y = b
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+// Two terms of a pair: hi = bf16(x), lo = bf16(x - hi), packed; the same values as converting
+// one at a time.
+__device__ __forceinline__ void bf16_split2_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = bf16x2_rn(a, b);
+  lo = bf16x2_rn(a - bf16_lo_f32(hi), b - bf16_hi_f32(hi));
+}
+// Two terms of a pair: hi = fp16(x), lo = fp16(x - hi), packed; the same values as converting
+// one at a time.
+__device__ __forceinline__ void f16_split2_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = f16x2_rn(a, b);
+  const float2 w = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  lo = f16x2_rn(a - w.x, b - w.y);
 }
 
 // Single-precision sigmoid from the hardware exponential and reciprocal (__expf, __fdividef):
