@@ -351,7 +351,6 @@ int forward_recurrence(const float* h0, const float* W, const float* ts, int B, 
   p.B = B; p.K = K; p.C = C; p.n_x = n_x; p.n_in = n_x + C;
   p.CS = cluster_size_for(C, cfc::kFwdChanPerCta);
   p.xch = xch;
-  p.fuse_u = 0;
   const bool fuse = u && b;
   if (fwd_ws_bytes(B, C) > 0) {
     if (!xch) return CFC_ERR_NULL_PTR;
@@ -368,10 +367,9 @@ int forward_recurrence(const float* h0, const float* W, const float* ts, int B, 
       if (n144 > 0 && (B + 143) / 144 <= n144) p.R = 144;
     }
     if (n > 0) {
-      if (fuse) {
+      if (fuse) {  // a non-NULL u asks the kernel for the fused form
         p.u = u;
         p.bias = b;
-        p.fuse_u = 1;
       }
       return cuda_rc(cfc::fwd_tc_launch(p, static_cast<cudaStream_t>(stream), pdl),
                      CFC_ERR_LAUNCH_FAILED);

@@ -118,28 +118,6 @@ __device__ __forceinline__ void split3_pair(float a, float b, uint32_t (&pk)[kUT
   pk[2] = bf16x2_rn(ar - bf16_lo_f32(pk[1]), br - bf16_hi_f32(pk[1]));
 }
 
-// Loads issued where they stand: prefetches into registers for the next step would otherwise
-// be moved down to their use by the compiler, and their latency would land on the step's
-// critical path.  (Read-only data; the global address of `p`.)
-__device__ __forceinline__ float4 ld_early_f4(const float* p) {
-  float4 v;
-  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "l"(p));
-  return v;
-}
-__device__ __forceinline__ float ld_early(const float* p) {
-  float v;
-  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
-}
-// Data another launch of this stream wrote (X from the projection): the L2 copy.
-__device__ __forceinline__ float ld_early_cg(const float* p) {
-  float v;
-  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
-}
-
 // Byte offset of element (row n, k) in one h term of NR rows: [k / 8][n / 8][n % 8][k % 8].
 template <int NR>
 __device__ __forceinline__ uint32_t hterm_offset(int n, int k) {
@@ -709,11 +687,12 @@ cudaError_t launch_k(const FwdParams& p, cudaStream_t s, bool pdl) {
   LaunchCfg c;
   c.grid = dim3(((p.B + NR - 1) / NR) * CS, 1, 1);
   c.block = dim3(kTcThreads, 1, 1);
-  c.smem = p.fuse_u ? TcShape<CS, NR, true>::SMEM : TcShape<CS, NR, false>::SMEM;
+  const bool fuse = p.u != nullptr;
+  c.smem = fuse ? TcShape<CS, NR, true>::SMEM : TcShape<CS, NR, false>::SMEM;
   c.stream = s;
   c.pdl = pdl;
   c.cluster = dim3(CS, 1, 1);
-  if (p.fuse_u)
+  if (fuse)
     return p.out_bf16 ? launch(c, cfc_fwd_tc_kernel<CS, NR, true, true>, p)
                       : launch(c, cfc_fwd_tc_kernel<CS, NR, false, true>, p);
   return p.out_bf16 ? launch(c, cfc_fwd_tc_kernel<CS, NR, true, false>, p)

@@ -18,6 +18,8 @@ constexpr int kMaxRowsPerCluster = 32;  // backward recurrence
 constexpr int kMaxFwdRows = 8;         // forward recurrence (rows are a template parameter)
 
 struct FwdParams {
+  // Set (with bias) only where the tensor-core recurrence forms X = W_u u + b itself
+  // (n_x <= kFwdFuseMaxInputs); otherwise X is read from xH / xcache and u is NULL.
   const float* u;      // [K][B][n_x]
   const float* h0;     // [B][C]
   const float* W;      // [4][C][n_in]
@@ -35,8 +37,6 @@ struct FwdParams {
   int CS;              // CTAs per cluster
   int R;               // batch rows per cluster
   void* xch;           // tensor-core forward: the exchange buffer (fwd_tc_xch_bytes)
-  int fuse_u;          // tensor-core forward: X = W_u u + b formed in the step (u, bias set),
-                       // not read from xH / xcache; needs n_x <= kFwdFuseMaxInputs
 };
 
 struct BwdParams {

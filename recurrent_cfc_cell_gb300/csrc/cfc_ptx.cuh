@@ -365,6 +365,28 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int k) {
                                ((((k >> 3) ^ (row & 7)) & 7) << 4) + ((k & 7) << 1));
 }
 
+// Loads issued where they stand: prefetches into registers for the next step would otherwise
+// be moved down to their use by the compiler, and their latency would land on the step's
+// critical path.  (ld_early, ld_early_f4: read-only data; `p` a global address.)
+__device__ __forceinline__ float4 ld_early_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_early(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+// Data another launch of this stream wrote (X from the projection): the L2 copy.
+__device__ __forceinline__ float ld_early_cg(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
 // ---- packed conversions: one instruction converts two values, and a bf16 widens to fp32 by
 // a 16-bit shift.  (Conversions share a narrow pipe with the exponentials and reciprocals.)
 // Packed pairs hold the first value in the low half.
