@@ -383,6 +383,9 @@ __global__ void build_operands_kernel(const float* __restrict__ u, const void* _
   const long long z_items = static_cast<long long>(BK) * zg;
   const long long total = z_items + static_cast<long long>(n_x) * wg;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  // Whole 16-byte loads when u's and H's rows start on 16 bytes (n_x, C multiples of 4): an
+  // item of 8 columns then lies wholly in u, wholly in h, or straddles the end of a region.
+  const bool vec = (n_x & 3) == 0 && (C & 3) == 0;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
        i += stride) {
     float v[8];
@@ -391,7 +394,29 @@ __global__ void build_operands_kernel(const float* __restrict__ u, const void* _
       // h_{t-1}: h0 for the first step, else the previous step's row of H (fp32 or bf16).
       const float* hrow = r < B ? h0 + static_cast<size_t>(r) * C
                                 : static_cast<const float*>(H) + static_cast<size_t>(r - B) * C;
-      if constexpr (HB) {
+      const bool in_u = c0 + 8 <= n_x, in_h = c0 >= n_x && c0 + 8 <= n_in;
+      if (vec && in_u) {
+        const float4* src = reinterpret_cast<const float4*>(u + static_cast<size_t>(r) * n_x + c0);
+        const float4 a = __ldg(src), b = __ldg(src + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+      } else if (vec && in_h && (!HB || r < B)) {
+        const float4* src = reinterpret_cast<const float4*>(hrow + (c0 - n_x));
+        const float4 a = __ldg(src), b = __ldg(src + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+      } else if (HB && vec && in_h && (C & 7) == 0 && (n_x & 7) == 0) {
+        // Eight bf16 values of H: one 16-byte load (the row start and c0 - n_x are multiples
+        // of 8 elements).
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(H) + static_cast<size_t>(r - B) * C + (c0 - n_x)));
+        const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[2 * e] = __uint_as_float(q[e] << 16);
+          v[2 * e + 1] = __uint_as_float(q[e] & 0xFFFF0000u);
+        }
+      } else if constexpr (HB) {
         const __nv_bfloat16* hrow16 =
             static_cast<const __nv_bfloat16*>(H) + static_cast<size_t>(r < B ? 0 : r - B) * C;
         const bool from_h0 = r < B;
