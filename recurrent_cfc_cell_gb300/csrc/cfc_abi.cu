@@ -406,7 +406,8 @@ int forward_recurrence(const float* h0, const float* W, const float* ts, int B, 
 int backward_recurrence(const float* dH, const float* W, const float* ts, const float* cache,
                         int B, int K, int C, int n_x, float* d_pre, float* dh0,
                         cfc_stream_t stream, bool pdl, void* wsplit = nullptr, int dplanes = 0,
-                        int dpitch = 0, bool cache_bf16 = false) {
+                        int dpitch = 0, bool cache_bf16 = false, int* free_sms = nullptr) {
+  if (free_sms) *free_sms = 0;
   int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
   if (!dH || !W || !ts || !cache || !d_pre || !dh0) return CFC_ERR_NULL_PTR;
@@ -444,6 +445,10 @@ int backward_recurrence(const float* dH, const float* W, const float* ts, const 
       if (rc != CFC_OK) return rc;
       p.R = NR;
       p.xbuf = reinterpret_cast<float*>(static_cast<char*>(wsplit) + cfc::bwd_l2x_image_bytes(C));
+      // SMs the recurrence leaves idle while every one of its clusters is resident.
+      const int clusters = (B + NR - 1) / NR;
+      if (free_sms && clusters <= (NR == 128 ? n128 : n))
+        *free_sms = st->sms - clusters * (C / 32) > 0 ? st->sms - clusters * (C / 32) : 0;
       return cuda_rc(cfc::bwd_l2x_launch(p, NR, s, true), CFC_ERR_LAUNCH_FAILED);
     }
   }
@@ -595,10 +600,12 @@ BwdLayoutCheck check_dpre_alias(const float* d_pre, bool dpre_in_ws, const char*
 // `build_first`: the previous kernel is the BPTT recurrence, which releases its dependents only
 // after its own dependency wait, so the operand build (which needs only the forward's outputs)
 // runs beside it; otherwise the d_pre split comes first and the build runs beside that.
+// `build_ctas` > 0: the build takes exactly that many CTAs (the SMs the recurrence leaves idle).
 int weight_grad(const float* d_pre, const float* u, const float* h0, const float* W,
                 const float* H, int B, int K, int C, int n_x, float* dW, float* db, float* du,
                 void* ws, size_t ws_bytes, int dw_mode, cfc_stream_t stream, bool first_pdl,
-                bool dpre_in_ws, bool build_first = false, bool h_bf16 = false) {
+                bool dpre_in_ws, bool build_first = false, bool h_bf16 = false,
+                int build_ctas = 0) {
   int rc = check_dims(B, K, C, n_x);
   if (rc != CFC_OK) return rc;
   if (!valid_mode(dw_mode)) return CFC_ERR_INVALID_ARG;
@@ -642,7 +649,7 @@ int weight_grad(const float* d_pre, const float* u, const float* h0, const float
   bool pdl = first_pdl;
   auto launch_build = [&]() {
     rc = cuda_rc(cfc::build_operands_launch(form, u, H, h_bf16 ? 1 : 0, h0, W, B, K, C, n_x,
-                                            w + L.z_off, w + L.wt_off, s, pdl),
+                                            w + L.z_off, w + L.wt_off, s, pdl, 0, build_ctas),
                  CFC_ERR_LAUNCH_FAILED);
     pdl = true;
   };
@@ -698,6 +705,23 @@ int weight_grad(const float* d_pre, const float* u, const float* h0, const float
                  CFC_ERR_LAUNCH_FAILED);
 }
 
+// The gradient stage right after the BPTT recurrence of the same call.  Beside the CUDA-core
+// BPTT (a few SMs) the operand build runs at its usual width.  The tensor-core BPTT holds most
+// SMs, one CTA each; the build then runs beside it on the SMs it leaves idle and nowhere else
+// (1024-thread CTAs, which cannot share an SM with a recurrence CTA), so it never competes with
+// the recurrence for issue slots.  With too few idle SMs the build follows the recurrence.
+constexpr int kMinBesideSms = 8;
+
+int weight_grad_after_bptt(const float* d_pre, const float* u, const float* h0, const float* W,
+                           const float* H, int B, int K, int C, int n_x, float* dW, float* db,
+                           float* du, void* ws, size_t ws_bytes, int dw_mode,
+                           cfc_stream_t stream, const BwdLayout& L, bool dpre_in_ws,
+                           int free_sms, bool h_bf16) {
+  const bool beside = !L.tc_bptt || free_sms >= kMinBesideSms;
+  return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode, stream,
+                     beside, dpre_in_ws, beside, h_bf16, L.tc_bptt && beside ? free_sms : 0);
+}
+
 }  // namespace
 
 extern "C" {
@@ -726,16 +750,14 @@ int cfc_backward(const float* dH, const float* u, const float* h0, const float* 
   if (ws_bytes < L.total) return CFC_ERR_WS_TOO_SMALL;
   float* d_pre = reinterpret_cast<float*>(static_cast<char*>(ws) + L.d_pre_off);
   const int dplanes = bptt_dplanes(L, dw_mode);
+  int free_sms = 0;
   rc = backward_recurrence(dH, W, ts, cache, B, K, C, n_x, d_pre, dh0, stream, false,
                            L.tc_bptt ? static_cast<char*>(ws) + L.wsplit_off : nullptr, dplanes,
-                           L.mp);
+                           L.mp, false, &free_sms);
   if (rc != CFC_OK) return rc;
-  // The operand build runs beside the CUDA-core BPTT (a few SMs).  The tensor-core BPTT fills
-  // most SMs and its L2 exchange slows down under a concurrent stream of HBM traffic (GB300,
-  // B = 2048, K = 128, C = 256: 2.82 ms with the build beside it, 2.66 ms after it), so there
-  // the gradient stage starts as an ordinary launch, after the recurrence.
-  return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode, stream,
-                     !L.tc_bptt, dplanes == dpre_planes(dw_mode), !L.tc_bptt);
+  return weight_grad_after_bptt(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes,
+                                dw_mode, stream, L, dplanes == dpre_planes(dw_mode), free_sms,
+                                false);
 }
 
 int cfc_forward_backward(const float* u, const float* h0, const float* W, const float* b,
@@ -759,16 +781,14 @@ int cfc_forward_backward(const float* u, const float* h0, const float* W, const 
   // The forward writes only H and cache, which the BPTT reads after its dependency wait.
   float* d_pre = reinterpret_cast<float*>(static_cast<char*>(ws) + L.d_pre_off);
   const int dplanes = bptt_dplanes(L, dw_mode);
+  int free_sms = 0;
   rc = backward_recurrence(dH, W, ts, cache, B, K, C, n_x, d_pre, dh0, stream, true,
                            L.tc_bptt ? static_cast<char*>(ws) + L.wsplit_off : nullptr, dplanes,
-                           L.mp);
+                           L.mp, false, &free_sms);
   if (rc != CFC_OK) return rc;
-  // The operand build runs beside the CUDA-core BPTT (a few SMs).  The tensor-core BPTT fills
-  // most SMs and its L2 exchange slows down under a concurrent stream of HBM traffic (GB300,
-  // B = 2048, K = 128, C = 256: 2.82 ms with the build beside it, 2.66 ms after it), so there
-  // the gradient stage starts as an ordinary launch, after the recurrence.
-  return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode, stream,
-                     !L.tc_bptt, dplanes == dpre_planes(dw_mode), !L.tc_bptt);
+  return weight_grad_after_bptt(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes,
+                                dw_mode, stream, L, dplanes == dpre_planes(dw_mode), free_sms,
+                                false);
 }
 
 // ---- bf16 state: H, the cache and d_pre stored as bf16, fp32 arithmetic ----
@@ -838,14 +858,15 @@ int cfc_backward_bf16(const float* dH, const float* u, const float* h0, const fl
   if (ws_bytes < L.total) return CFC_ERR_WS_TOO_SMALL;
   float* d_pre = reinterpret_cast<float*>(static_cast<char*>(ws) + L.d_pre_off);
   const int dplanes = bptt_dplanes(L, mode);
+  int free_sms = 0;
   rc = backward_recurrence(dH, W, ts, static_cast<const float*>(cache), B, K, C, n_x, d_pre, dh0,
                            stream, false,
                            L.tc_bptt ? static_cast<char*>(ws) + L.wsplit_off : nullptr, dplanes,
-                           L.mp, true);
+                           L.mp, true, &free_sms);
   if (rc != CFC_OK) return rc;
-  return weight_grad(d_pre, u, h0, W, static_cast<const float*>(H), B, K, C, n_x, dW, db, du, ws,
-                     ws_bytes, mode, stream, !L.tc_bptt, dplanes == dpre_planes(mode),
-                     !L.tc_bptt, true);
+  return weight_grad_after_bptt(d_pre, u, h0, W, static_cast<const float*>(H), B, K, C, n_x, dW,
+                                db, du, ws, ws_bytes, mode, stream, L,
+                                dplanes == dpre_planes(mode), free_sms, true);
 }
 
 int reduce_axis0(const float* per_batch, int n_batch, int n_tail, float* out,

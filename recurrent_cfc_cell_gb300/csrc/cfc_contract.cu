@@ -368,7 +368,7 @@ __device__ __forceinline__ void put8(uint8_t* row, int pitch, int col, const flo
 // multiple of 8 (the pitches are multiples of 8); the contraction never reads beyond them.
 // HB: H holds bf16 elements.
 template <int FORM, bool HB>
-__global__ void build_operands_kernel(const float* __restrict__ u, const void* __restrict__ H,
+__global__ void __launch_bounds__(1024) build_operands_kernel(const float* __restrict__ u, const void* __restrict__ H,
                                       const float* __restrict__ h0,
                                       const float* __restrict__ W, int B, int BK, int C, int n_x,
                                       int M, uint8_t* z, int zp, uint8_t* wt, int mp) {
@@ -718,13 +718,19 @@ LaunchCfg grid_stride_cfg(long long items, cudaStream_t s, bool pdl) {
 cudaError_t build_operands_launch(int form, const float* u, const void* H, int h_bf16,
                                   const float* h0,
                                   const float* W, int B, int K, int C, int n_x, void* z, void* wt,
-                                  cudaStream_t s, bool pdl, int M) {
+                                  cudaStream_t s, bool pdl, int M, int ctas) {
   const int BK = B * K;
   if (M <= 0) M = 4 * C;
   const long long items = static_cast<long long>(BK) * ((n_x + C + 1 + 7) / 8) +
                           static_cast<long long>(n_x) * ((M + 7) / 8);
   LaunchCfg c = grid_stride_cfg(items, s, pdl);
   if (c.grid.x > 2 * 148) c.grid.x = 2 * 148;  // resident beside the kernel it runs next to
+  if (ctas > 0) {
+    // 1024 threads at 48 registers: one CTA per SM, and none beside a CTA that holds more than
+    // a quarter of the SM's registers.
+    c.grid = dim3(static_cast<unsigned>(ctas), 1, 1);
+    c.block = dim3(1024, 1, 1);
+  }
   const int zp = contract_z_pitch(n_x + C, form), mp = (M + 7) & ~7;  // W_u^T row pitch
   uint8_t* z8 = static_cast<uint8_t*>(z);
   uint8_t* w8 = static_cast<uint8_t*>(wt);

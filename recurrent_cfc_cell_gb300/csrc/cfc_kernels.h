@@ -159,10 +159,13 @@ void contract_plans_mn(int BK, int M, int N, int n_x, int form, int smem_budget,
 cudaError_t contract_prepare(int max_smem);
 // z rows [u ; h_{t-1} ; 1] (B*K of them) and W_u^T rows (n_x) in the operand form; H is fp32,
 // or bf16 when h_bf16.  W has M rows of n_x + C (M <= 0: 4C, the four gates); W_u^T rows are
-// (M + 7) & ~7 values apart.
+// (M + 7) & ~7 values apart.  `ctas` > 0: exactly that many CTAs of 1024 threads, for a build
+// that runs on the SMs a concurrent kernel leaves idle; otherwise a grid-stride launch of up
+// to two 256-thread CTAs per SM.
 cudaError_t build_operands_launch(int form, const float* u, const void* H, int h_bf16,
                                   const float* h0, const float* W, int B, int K, int C, int n_x,
-                                  void* z, void* wt, cudaStream_t s, bool pdl, int M = 0);
+                                  void* z, void* wt, cudaStream_t s, bool pdl, int M = 0,
+                                  int ctas = 0);
 // fp32 d_pre [B*K][4C] -> the bf16 operand rows (may be in place when the pitch is 4C).
 cudaError_t split_dpre_launch(int form, const float* d_pre, int BK, int C, void* planes,
                               cudaStream_t s, bool pdl);
