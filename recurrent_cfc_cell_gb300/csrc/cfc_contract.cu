@@ -59,14 +59,15 @@ struct Form {
   static constexpr int kAtom = kAtomBytes / kElem;          // 64 bf16 or 32 fp32
   static constexpr int kTerms = FORM == kFormBf16x2 ? 2 : 1;
   static constexpr int kKStep = FORM == kFormTf32 ? 8 : 16;  // reduction depth of one MMA
-  static constexpr int kSteps = kAtom / kKStep;              // MMAs per k-block and term pair
 };
 
 struct CArgs {
   int M, N;             // rows and columns of the result
   int n_tile;           // columns of a tile
   int m_tiles, n_tiles;
-  int n_kb;             // k-blocks of the reduction (kAtom entries each)
+  int n_kb;             // k-blocks of the reduction (kd entries each)
+  int kd;               // reduction entries per k-block: a multiple of 16 for MN-major
+                        // tiles, the atom row (kAtom) for K-major ones
   int kb_per_split;
   int stages;
   float* out;           // [splits][M][ldo] (split_stride floats apart)
@@ -142,12 +143,16 @@ __global__ void __launch_bounds__(kCThreads, 1)
                     const CArgs g) {
   using F = Form<FORM>;
   constexpr int kTerms = F::kTerms;
-  constexpr uint32_t kABytes = MT * 128 * kAtomBytes;  // one term of A: MT*128 output rows
+  // Reduction entries of one stage: MN-major tiles take g.kd rows of 128-byte atoms, K-major
+  // tiles one atom row (the swizzle width) per output row.
+  const int kd = A_MN ? g.kd : F::kAtom;
+  const uint32_t rb = static_cast<uint32_t>(kd) * F::kElem;  // bytes per output index
+  const uint32_t kABytes = MT * 128 * rb;                    // one term of A: MT*128 outputs
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(base);
-  const uint32_t b_bytes = static_cast<uint32_t>(g.n_tile) * kAtomBytes;
+  const uint32_t b_bytes = static_cast<uint32_t>(g.n_tile) * rb;
   const uint32_t stage_bytes = kTerms * (kABytes + b_bytes);
   const int stages = g.stages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + stages * stage_bytes);
@@ -217,18 +222,16 @@ __global__ void __launch_bounds__(kCThreads, 1)
           const uint32_t sa = st + t * kABytes;
           const uint32_t sb = st + kTerms * kABytes + t * b_bytes;
           if constexpr (A_MN) {
-            // box {kAtom output rows, kAtom reduction rows}: one atom column per box
+            // box {kAtom outputs, kd reduction rows}: one atom column per box
 #pragma unroll
             for (int a = 0; a < MT * 128 / F::kAtom; ++a)
-              tma_load_2d(sa + a * (F::kAtom * kAtomBytes), ma, m0 + a * F::kAtom,
-                          kb * F::kAtom, bar);
+              tma_load_2d(sa + a * (kd * kAtomBytes), ma, m0 + a * F::kAtom, kb * kd, bar);
           } else {
             tma_load_2d(sa, ma, kb * F::kAtom, m0, bar);  // box {kAtom, MT*128 rows}
           }
           if constexpr (B_MN) {
             for (int a = 0; a < g.n_tile / F::kAtom; ++a)
-              tma_load_2d(sb + a * (F::kAtom * kAtomBytes), mb, n0 + a * F::kAtom,
-                          kb * F::kAtom, bar);
+              tma_load_2d(sb + a * (kd * kAtomBytes), mb, n0 + a * F::kAtom, kb * kd, bar);
           } else {
             tma_load_2d(sb, mb, kb * F::kAtom, n0, bar);  // box {kAtom, n_tile rows}
           }
@@ -245,9 +248,11 @@ __global__ void __launch_bounds__(kCThreads, 1)
     if (lane == 0) {
       // ---- MMA issuer ----
       const uint32_t idesc = idesc_form<FORM>(128, g.n_tile, A_MN, B_MN);
-      // MN-major: atoms along the output index are kAtom reduction rows x 128 B apart, groups
+      // MN-major: atoms along the output index are kd reduction rows x 128 B apart, groups
       // of 8 reduction rows 1024 B apart; one MMA step spans kKStep / 8 groups.
-      constexpr uint32_t kLbo = F::kAtom * kAtomBytes, kSbo = 1024;
+      const uint32_t kLbo = static_cast<uint32_t>(kd) * kAtomBytes;
+      constexpr uint32_t kSbo = 1024;
+      const int ksteps = kd / F::kKStep;
       constexpr uint32_t kMnStep = (F::kKStep / 8) * 1024;
       constexpr uint32_t kKStepBytes = F::kKStep * F::kElem;  // K-major: 32 B per step
       uint32_t acc = 0;
@@ -262,9 +267,9 @@ __global__ void __launch_bounds__(kCThreads, 1)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           const uint32_t d = tmem + mt * acc_cols;
-          const uint32_t sa = st + mt * (128 * kAtomBytes);
-#pragma unroll
-          for (int j = 0; j < F::kSteps; ++j) {
+          const uint32_t sa = st + mt * (128 * rb);
+#pragma unroll 4
+          for (int j = 0; j < ksteps; ++j) {
             uint64_t ad[kTerms], bd[kTerms];
 #pragma unroll
             for (int t = 0; t < kTerms; ++t) {
@@ -575,13 +580,19 @@ cudaError_t set_attrs_form(int max_smem) {
   return cudaSuccess;
 }
 
-size_t stage_bytes(int form, int mt, int n_tile) {
-  return static_cast<size_t>(terms_of(form)) * (mt * 128 + n_tile) * kAtomBytes;
+// Bytes of one stage: `rb` bytes per output index (kd entries of an MN-major tile, or one
+// 128-byte atom row of a K-major one).
+size_t stage_bytes(int form, int mt, int n_tile, int rb) {
+  return static_cast<size_t>(terms_of(form)) * (mt * 128 + n_tile) * rb;
+}
+
+int row_bytes(int form, int kd, bool mn) {
+  return mn ? kd * (form == kFormTf32 ? 4 : 2) : kAtomBytes;
 }
 
 // Stages: as many as fit (at most `max_stages`), leaving room for alignment and barriers.
-ContractPlan finish_plan(ContractPlan p, int form, int max_stages, int smem_budget) {
-  const size_t sb = stage_bytes(form, p.mt, p.n_tile);
+ContractPlan finish_plan(ContractPlan p, int form, int max_stages, int smem_budget, bool mn) {
+  const size_t sb = stage_bytes(form, p.mt, p.n_tile, row_bytes(form, p.kd, mn));
   const size_t extra = 1024 + (2 * kCMaxStages + 2) * 8 + 16;
   int st = static_cast<int>((smem_budget - extra) / sb);
   if (st > max_stages) st = max_stages;
@@ -611,6 +622,14 @@ ContractPlan dw_contract_plan(int B, int K, int C, int n_x, int form, int smem_b
   return dw_contract_plan_mn(B * K, 4 * C, n_x + C + 1, form, smem_budget);
 }
 
+// Rows (B*K) below which both contractions are split, sized together: a tiny problem is all
+// latency, so more and shorter CTAs help, and one launch merges both sets of partials.
+constexpr int kJointSplitMaxRows = 8192;
+// Reduction rows per stage of the MN-major (bf16) weight gradient above that size: 32 rows
+// give twice the stages of 64 in the same shared memory (four of 56 KB at 256 x 192 tiles,
+// accurate form), so each stage's copy has three stages of MMAs to land behind.
+constexpr int kMnDeepKd = 32;
+
 ContractPlan dw_contract_plan_mn(int BK, int M, int N, int form, int smem_budget) {
   ContractPlan p{};
   // Column tiles: whole 128-byte atoms for MN-major operands (bf16), multiples of 16 (K-major).
@@ -624,11 +643,15 @@ ContractPlan dw_contract_plan_mn(int BK, int M, int N, int form, int smem_budget
     nt = (N + p.n_tiles - 1) / p.n_tiles;
     p.n_tile = (nt + atom - 1) / atom * atom;
   }
+  const bool mn = form != kFormTf32;
+  p.kd = mn && BK >= kJointSplitMaxRows ? kMnDeepKd : atom_of(form);
   // Two stages of two accumulators must fit; otherwise one accumulator per CTA.
-  if (p.mt == 2 && 2 * stage_bytes(form, 2, p.n_tile) + 2048 > static_cast<size_t>(smem_budget))
+  if (p.mt == 2 &&
+      2 * stage_bytes(form, 2, p.n_tile, row_bytes(form, p.kd, mn)) + 2048 >
+          static_cast<size_t>(smem_budget))
     p.mt = 1;
   p.m_tiles = (M + 128 * p.mt - 1) / (128 * p.mt);
-  p.n_kb = (BK + atom_of(form) - 1) / atom_of(form);
+  p.n_kb = (BK + p.kd - 1) / p.kd;
   const int tiles = p.m_tiles * p.n_tiles;
   // At least four k-blocks per split: the copies of a CTA's blocks are in flight together, so
   // a longer range costs little, and every split adds a partial block to the merge.
@@ -637,7 +660,7 @@ ContractPlan dw_contract_plan_mn(int BK, int M, int N, int form, int smem_budget
   if (s0 < 1) s0 = 1;
   p.kb_per_split = (p.n_kb + s0 - 1) / s0;
   p.splits = (p.n_kb + p.kb_per_split - 1) / p.kb_per_split;
-  return finish_plan(p, form, 8, smem_budget);
+  return finish_plan(p, form, 8, smem_budget, mn);
 }
 
 // Input gradient: rows B*K, columns n_x, reduction 4C; one 128-row tile per CTA, not split.
@@ -655,15 +678,13 @@ ContractPlan du_contract_plan_mn(int BK, int M, int n_x, int form, int smem_budg
   const int nt = (n_x + p.n_tiles - 1) / p.n_tiles;
   p.n_tile = (nt + 15) / 16 * 16;
   p.m_tiles = (BK + 127) / 128;
+  p.kd = atom;
   p.n_kb = (M + atom - 1) / atom;
   p.kb_per_split = p.n_kb;
   p.splits = 1;
-  return finish_plan(p, form, 4, smem_budget / 2 - 1024);
+  return finish_plan(p, form, 4, smem_budget / 2 - 1024, false);
 }
 
-// Rows (B*K) below which both contractions are split, sized together: a tiny problem is all
-// latency, so more and shorter CTAs help, and one launch merges both sets of partials.
-constexpr int kJointSplitMaxRows = 8192;
 
 void contract_plans(int B, int K, int C, int n_x, int form, int smem_budget, ContractPlan* pw,
                     ContractPlan* pu) {
@@ -692,7 +713,7 @@ void contract_plans_mn(int BK, int M, int N, int n_x, int form, int smem_budget,
     p->kb_per_split = kbps < p->n_kb ? kbps : p->n_kb;
     p->splits = (p->n_kb + p->kb_per_split - 1) / p->kb_per_split;
   }
-  *pw = finish_plan(w, form, 8, smem_budget);
+  *pw = finish_plan(w, form, 8, smem_budget, form != kFormTf32);
 }
 
 cudaError_t contract_prepare(int max_smem) {
@@ -795,19 +816,19 @@ cudaError_t dw_contract_launch_mn(const ContractPlan& pl, int form, const void* 
     e = make_map(&a0, true, d8, BK, M, row, atom, 128 * pl.mt);
     if (e == cudaSuccess) e = make_map(&b0, true, z8, BK, N, row, atom, pl.n_tile);
   } else {
-    e = make_map(&a0, false, d8, M, BK, 4ull * mp, atom, atom);
-    if (e == cudaSuccess) e = make_map(&b0, false, z8, N, BK, 4ull * zp, atom, atom);
+    e = make_map(&a0, false, d8, M, BK, 4ull * mp, atom, pl.kd);
+    if (e == cudaSuccess) e = make_map(&b0, false, z8, N, BK, 4ull * zp, atom, pl.kd);
   }
   a1 = a0;
   b1 = b0;
   if (e == cudaSuccess && form == kFormBf16x2) {
-    e = make_map(&a1, false, d8 + 2 * mp, M, BK, 4ull * mp, atom, atom);
-    if (e == cudaSuccess) e = make_map(&b1, false, z8 + 2 * zp, N, BK, 4ull * zp, atom, atom);
+    e = make_map(&a1, false, d8 + 2 * mp, M, BK, 4ull * mp, atom, pl.kd);
+    if (e == cudaSuccess) e = make_map(&b1, false, z8 + 2 * zp, N, BK, 4ull * zp, atom, pl.kd);
   }
   if (e != cudaSuccess) return e;
   CArgs g{};
   g.M = M; g.N = N; g.n_tile = pl.n_tile; g.m_tiles = pl.m_tiles; g.n_tiles = pl.n_tiles;
-  g.n_kb = pl.n_kb; g.kb_per_split = pl.kb_per_split; g.stages = pl.stages;
+  g.n_kb = pl.n_kb; g.kd = pl.kd; g.kb_per_split = pl.kb_per_split; g.stages = pl.stages;
   g.out = partial; g.ldo = ldo; g.n_store = ldo < N ? ldo : N;
   g.split_stride = static_cast<size_t>(M) * ldo;
   g.status = status;
@@ -850,7 +871,7 @@ cudaError_t du_contract_launch_mn(const ContractPlan& pl, int form, const void* 
   if (e != cudaSuccess) return e;
   CArgs g{};
   g.M = BK; g.N = n_x; g.n_tile = pl.n_tile; g.m_tiles = pl.m_tiles; g.n_tiles = pl.n_tiles;
-  g.n_kb = pl.n_kb; g.kb_per_split = pl.kb_per_split; g.stages = pl.stages;
+  g.n_kb = pl.n_kb; g.kd = pl.kd; g.kb_per_split = pl.kb_per_split; g.stages = pl.stages;
   g.out = du; g.ldo = n_x; g.n_store = n_x;
   g.split_stride = static_cast<size_t>(BK) * n_x;  // split partials, when the plan splits
   g.status = status;

@@ -141,6 +141,7 @@ struct ContractPlan {
   int mt;       // 128-row accumulators per CTA
   int n_tile, n_tiles, m_tiles;
   int n_kb, kb_per_split, splits;
+  int kd;       // reduction entries per k-block
   int stages;
   size_t smem;
 };
