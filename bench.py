@@ -790,7 +790,7 @@ def main():
 
     # ---- end to end through the public API with host buffers: every step copies its inputs
     # in from pinned host memory and its gradients out to pinned host memory (one packed copy
-    # each way, captured with the step's kernels in one graph).
+    # each way by the library's copy kernel, captured with the step's kernels in one graph).
     ste = KLoopStep(w.B, w.K, w.C, w.n_x, device=dev).stage_host()
     for k, v in inp.items():
         ste.host_in[k].copy_(torch.from_numpy(v))

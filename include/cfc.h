@@ -392,6 +392,19 @@ int cfc_probe_fma(float* out, int blocks, int iters, double* flop, cfc_stream_t 
 int cfc_probe_l2_read(const float* buf, size_t n_floats, int passes, float* out, int blocks,
                       double* bytes, cfc_stream_t stream);
 
+/*
+ * cfc_copy -- dst[0 .. bytes) <- src[0 .. bytes), enqueued on `stream` as one kernel of the
+ * library (the SMs move the data; no copy engine).  For bringing a step's inputs in from the
+ * host and its gradients back: each of src and dst is device memory, managed memory, or host
+ * memory that is pinned or registered with CUDA and so mapped into the device's address space
+ * (read and written directly over the host link).  Both pointers and `bytes` must be multiples
+ * of 16 (CFC_ERR_MISALIGNED); the ranges must not overlap, and memory the device cannot reach
+ * is refused (CFC_ERR_INVALID_ARG).  bytes == 0 enqueues nothing.  The caller owns both buffers
+ * and keeps them alive until the copy has run.  Returns CFC_OK, CFC_ERR_NULL_PTR,
+ * CFC_ERR_MISALIGNED, CFC_ERR_INVALID_ARG or CFC_ERR_LAUNCH_FAILED.
+ */
+int cfc_copy(const void* src, void* dst, size_t bytes, cfc_stream_t stream);
+
 /* cfc_error_string -- static English text for a status code (never NULL). */
 const char* cfc_error_string(int code);
 

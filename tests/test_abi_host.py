@@ -308,3 +308,15 @@ def test_decay_argument_checks(lib):
                                   None) == WS_TOO_SMALL
     assert lib.cfc_decay_backward(*([f] * 8), 4, 8, 32, 16, None, *([f] * 4), f, big,
                                   None) == NULL_PTR
+
+
+def test_copy_argument_errors(lib):
+    """cfc_copy refuses missing and unaligned buffers before it touches a device, and a copy of
+    no bytes enqueues nothing."""
+    p16, q16 = ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20)  # never dereferenced
+    assert lib.cfc_copy(None, q16, 16, None) == NULL_PTR
+    assert lib.cfc_copy(p16, None, 16, None) == NULL_PTR
+    assert lib.cfc_copy(ctypes.c_void_p((1 << 20) + 8), q16, 16, None) == MISALIGNED
+    assert lib.cfc_copy(p16, ctypes.c_void_p((2 << 20) + 4), 16, None) == MISALIGNED
+    assert lib.cfc_copy(p16, q16, 24, None) == MISALIGNED
+    assert lib.cfc_copy(p16, q16, 0, None) == OK
