@@ -44,6 +44,9 @@ RAGGED = [
     dict(B=400, K=3, n_x=100, C=256),  # tensor-core forward too wide in n_x to form the
                                        # projection itself: projection kernel, then X read
     dict(B=790, K=4, n_x=61, C=128),   # fused projection, n_x not a multiple of 4 or 16
+    dict(B=2300, K=2, n_x=16, C=256),  # 16 clusters of 144 rows, more than stay resident: both
+                                       # recurrences in two waves, the operand build after the
+                                       # BPTT (no idle SMs to run beside it)
 ]
 
 
