@@ -15,12 +15,17 @@
 // four-gate cell; this file holds the recurrences.
 //
 // Layout of a recurrence CTA (CP = C rounded up to 32, at most 128; 2 CP threads; R batch rows):
-// thread 2 i + hf owns hidden unit i and half hf of the mat-vec's reduction: in the forward, the
-// row W_rec[i][hf CP/2 ..] in registers; in the BPTT, the column W_rec[hf CP/2 .. ][i] (for
-// W_rec^T da).  The vector of the step (h_{t-1}, or da_t) sits in shared memory, double
-// buffered, so each step needs one CTA barrier.  The pair's partial sums meet by one shuffle.
-// Per-row inputs of the next step are loaded one step ahead.  The rows of a CTA run in phases
-// (all mat-vecs, then all updates) so their latency chains overlap.
+// eight lanes serve a quad of four hidden units.  Lane sl of the eight holds, for each of the
+// quad's units, the weights of the reduction entries in chunks 8 q + sl (4 entries a chunk):
+// in the forward the rows W_rec[unit][..], in the BPTT the columns W_rec[..][unit] (for
+// W_rec^T da).  Every vector value a lane loads from shared memory feeds four FMAs (one per
+// unit), and the eight lanes of a warp quarter read eight consecutive 16-byte chunks (no bank
+// conflicts; the four quads of a warp read the same chunks, a broadcast).  A reduce-scatter of
+// three shuffle levels leaves unit (lane >> 1) & 3 of the quad in each lane pair; the even
+// lane of the pair writes it.  The vector of the step (h_{t-1}, or da_t) sits in shared
+// memory, double buffered, so each step needs one CTA barrier.  Per-row inputs of the next
+// step are loaded one step ahead.  The rows of a CTA run in phases (all mat-vecs, then all
+// updates) so their latency chains overlap.
 #include <cuda_bf16.h>
 
 #include "cfc_kernels.h"
@@ -30,48 +35,83 @@
 namespace cfc {
 namespace {
 
-constexpr int kProjRows = 8;  // rows per projection CTA (one warp each)
+// Projection tiles: 64 rows x 64 hidden units per CTA of 256 threads, each thread 4 rows x 4
+// consecutive units, k in chunks of 64 through shared memory.
+constexpr int kPR = 64, kPC = 64, kPK = 64;
+constexpr int kPLoads = kPK * kPR / 256;  // elements of each operand tile per thread
 
-// X[r][c] = b[c] + sum_k x[r][k] W[c][k] (k < n_x) for the B*K rows r, written into E (the
-// recurrence reads X there and overwrites it with tanh(a)).  W_in^T is staged through shared
-// memory 32 inputs at a time; lane l of warp w computes channels l, l + 32, ... of row w.
+// X[r][c] = b[c] + sum_{k < n_x} x[r][k] W[c][k] for the B*K rows r, written into E (the
+// recurrence reads X there and overwrites it with tanh(a)).  A chunk's global loads (x and W_in
+// rows, consecutive threads walking k) are all issued before any is stored.
 __global__ void __launch_bounds__(256) decay_proj_kernel(const float* __restrict__ x,
                                                          const float* __restrict__ W,
                                                          const float* __restrict__ bias, int BK,
                                                          int C, int n_x, float* __restrict__ E) {
-  __shared__ float wt[32][129];          // [k][c] chunk of W_in^T
-  __shared__ float xs[kProjRows][32];    // [row][k] chunk of x
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.x * kProjRows + warp;
+  __shared__ __align__(16) float xs[kPK][kPR + 4];  // [k][row]
+  __shared__ __align__(16) float ws[kPK][kPC + 4];  // [k][unit]
   const int n_in = n_x + C;
-  float acc[4];
+  const int r0 = blockIdx.y * kPR, c0 = blockIdx.x * kPC;
+  const int tid = threadIdx.x;
+  const int tr = tid >> 4, tc = tid & 15;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < n_x; k0 += kPK) {
+    float xr[kPLoads], wr[kPLoads];
+#pragma unroll
+    for (int q = 0; q < kPLoads; ++q) {
+      const int e = tid + q * 256;
+      const int rr = e / kPK, kk = e % kPK;
+      const int r = r0 + rr, c = c0 + rr, k = k0 + kk;
+      xr[q] = (r < BK && k < n_x) ? __ldg(x + static_cast<size_t>(r) * n_x + k) : 0.f;
+      wr[q] = (c < C && k < n_x) ? __ldg(W + static_cast<size_t>(c) * n_in + k) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < kPLoads; ++q) {
+      const int e = tid + q * 256;
+      xs[e % kPK][e / kPK] = xr[q];
+      ws[e % kPK][e / kPK] = wr[q];
+    }
+    __syncthreads();
+    const int kn = min(kPK, n_x - k0);
+    for (int kk = 0; kk < kn; ++kk) {
+      const float4 a = *reinterpret_cast<const float4*>(&xs[kk][tr * 4]);
+      const float4 w = *reinterpret_cast<const float4*>(&ws[kk][tc * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w};
+      const float wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], wv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const int c = lane + 32 * j;
-    acc[j] = c < C ? __ldg(bias + c) : 0.f;
-  }
-  for (int k0 = 0; k0 < n_x; k0 += 32) {
-    __syncthreads();
-    for (int e = threadIdx.x; e < 32 * 128; e += 256) {
-      const int c = e >> 5, k = e & 31;
-      wt[k][c] = (c < C && k0 + k < n_x) ? __ldg(W + static_cast<size_t>(c) * n_in + k0 + k) : 0.f;
-    }
-    xs[warp][lane] = (r < BK && k0 + lane < n_x) ? __ldg(x + static_cast<size_t>(r) * n_x + k0 + lane) : 0.f;
-    __syncthreads();
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-      const float xv = xs[warp][k];
+    const int c = c0 + tc * 4 + j;
+    if (c >= C) continue;
+    const float bc = __ldg(bias + c);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[j] = fmaf(wt[k][lane + 32 * j], xv, acc[j]);
+    for (int i = 0; i < 4; ++i) {
+      const int r = r0 + tr * 4 + i;
+      if (r < BK) E[static_cast<size_t>(r) * C + c] = acc[i][j] + bc;
     }
   }
-  if (r < BK) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = lane + 32 * j;
-      if (c < C) E[static_cast<size_t>(r) * C + c] = acc[j];
-    }
-  }
+}
+
+// Chunks of four reduction entries a lane holds (chunks 8 q + sl, q < kQ) and the reduction
+// over the eight lanes of a unit quad: a[u] is the lane's partial sum of unit u; the result,
+// the full sum of unit (lane >> 1) & 3, is in both lanes of each pair.
+template <int CP>
+struct Quad {
+  static constexpr int kQ = CP / 32;
+};
+__device__ __forceinline__ float quad_reduce_scatter(const float (&a)[4], int lane) {
+  const bool b2 = lane & 4, b1 = lane & 2;
+  const float k0 = b2 ? a[2] : a[0], k1 = b2 ? a[3] : a[1];
+  const float s0 = k0 + __shfl_xor_sync(0xffffffffu, b2 ? a[0] : a[2], 4);
+  const float s1 = k1 + __shfl_xor_sync(0xffffffffu, b2 ? a[1] : a[3], 4);
+  float acc = (b1 ? s1 : s0) + __shfl_xor_sync(0xffffffffu, b1 ? s0 : s1, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  return acc;
 }
 
 struct DecayFwdParams {
@@ -87,28 +127,37 @@ struct DecayFwdParams {
 // Forward recurrence, one CTA per R batch rows, all K steps.
 template <int CP, int R>
 __global__ void __launch_bounds__(2 * CP) decay_fwd_kernel(const DecayFwdParams p) {
-  constexpr int HALF = CP / 2;
+  constexpr int kQ = Quad<CP>::kQ;
   __shared__ __align__(16) float hs[2][R][CP];  // h_{t-1} of the rows, double buffered
-  const int tid = threadIdx.x, i = tid >> 1, hf = tid & 1;
+  const int tid = threadIdx.x, lane = tid & 31, sl = lane & 7;
   const int B = p.B, K = p.K, C = p.C, n_in = p.n_x + C;
   const int row0 = blockIdx.x * R;
+  const int ubase = 4 * (tid >> 3);            // the quad's first unit
+  const int i = ubase + ((lane >> 1) & 3);     // this lane pair's unit after the reduction
+  const bool writer = (lane & 1) == 0;
   const bool ok_i = i < C;
-  // W_rec[i][HALF hf + j], paired for the packed FMA.
-  float2 w[HALF / 2];
+  // W_rec[ubase + u][4 (8 q + sl) + e], paired for the packed FMA.
+  float2 w[4][kQ][2];
 #pragma unroll
-  for (int j = 0; j < HALF / 2; ++j) {
-    const int c0 = HALF * hf + 2 * j;
-    const float* wr = p.W + static_cast<size_t>(ok_i ? i : 0) * n_in + p.n_x;
-    w[j] = make_float2(ok_i && c0 < C ? __ldg(wr + c0) : 0.f,
-                       ok_i && c0 + 1 < C ? __ldg(wr + c0 + 1) : 0.f);
+  for (int u = 0; u < 4; ++u) {
+    const int unit = ubase + u;
+    const float* wr = p.W + static_cast<size_t>(unit < C ? unit : 0) * n_in + p.n_x;
+#pragma unroll
+    for (int q = 0; q < kQ; ++q)
+#pragma unroll
+      for (int ep = 0; ep < 2; ++ep) {
+        const int k = 4 * (8 * q + sl) + 2 * ep;
+        w[u][q][ep] = make_float2(unit < C && k < C ? __ldg(wr + k) : 0.f,
+                                  unit < C && k + 1 < C ? __ldg(wr + k + 1) : 0.f);
+      }
   }
   const float inv_tau = ok_i ? 1.f / __ldg(p.tau + i) : 0.f;
   bool rok[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     rok[r] = row0 + r < B;
-    // The pair's first lane writes each slot once (zero where no channel or row lives).
-    if (hf == 0)
+    // The pair's even lane writes each slot once (zero where no unit or row lives).
+    if (writer)
       hs[0][r][i] = (ok_i && rok[r]) ? __ldg(p.h0 + static_cast<size_t>(row0 + r) * C + i) : 0.f;
   }
   float xn[R], tn[R];
@@ -138,24 +187,33 @@ __global__ void __launch_bounds__(2 * CP) decay_fwd_kernel(const DecayFwdParams 
     float a[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const float4* hv = reinterpret_cast<const float4*>(&hs[cur][r][HALF * hf]);
-      float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+      const float4* hv = reinterpret_cast<const float4*>(&hs[cur][r][0]);
+      float2 acc2[4];
 #pragma unroll
-      for (int q = 0; q < HALF / 4; ++q) {
-        const float4 v = hv[q];
-        s0 = fma2(w[2 * q], make_float2(v.x, v.y), s0);
-        s1 = fma2(w[2 * q + 1], make_float2(v.z, v.w), s1);
+      for (int u = 0; u < 4; ++u) acc2[u] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        const float4 v = hv[8 * q + sl];
+        const float2 v01 = make_float2(v.x, v.y), v23 = make_float2(v.z, v.w);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          acc2[u] = fma2(w[u][q][0], v01, acc2[u]);
+          acc2[u] = fma2(w[u][q][1], v23, acc2[u]);
+        }
       }
-      a[r] = (s0.x + s0.y) + (s1.x + s1.y);
+      float au[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) au[u] = acc2[u].x + acc2[u].y;
+      a[r] = quad_reduce_scatter(au, lane);
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const float at = a[r] + __shfl_xor_sync(0xffffffffu, a[r], 1) + xc[r];
+      const float at = a[r] + xc[r];
       const float e = tanhf(at);
       const float d = __expf(-tc[r] * inv_tau);
       const float hp = hs[cur][r][ok_i ? i : 0];
       const float h = d * hp + (1.f - d) * e;
-      if (hf == 0) {
+      if (writer) {
         hs[cur ^ 1][r][i] = ok_i ? h : 0.f;
         if (ok_i && rok[r]) {
           const size_t o = (static_cast<size_t>(t) * B + row0 + r) * C + i;
@@ -187,20 +245,30 @@ struct DecayBwdParams {
 //   G_{t-1} = dH[t-1] + G d + W_rec^T da.
 template <int CP, int R>
 __global__ void __launch_bounds__(2 * CP) decay_bwd_kernel(const DecayBwdParams p) {
-  constexpr int HALF = CP / 2;
+  constexpr int kQ = Quad<CP>::kQ;
   __shared__ __align__(16) float das[2][R][CP];  // da of the step, double buffered
-  const int tid = threadIdx.x, j = tid >> 1, hf = tid & 1;
+  const int tid = threadIdx.x, lane = tid & 31, sl = lane & 7;
   const int B = p.B, K = p.K, C = p.C, n_in = p.n_x + C;
   const int row0 = blockIdx.x * R;
+  const int ubase = 4 * (tid >> 3);            // the quad's first unit
+  const int j = ubase + ((lane >> 1) & 3);     // this lane pair's unit after the reduction
+  const bool writer = (lane & 1) == 0;
   const bool ok_j = j < C;
-  // Column j of W_rec over the rows i = HALF hf + 2 q (+1), paired for the packed FMA.
-  float2 wc[HALF / 2];
+  // Column ubase + u of W_rec over the rows 4 (8 q + sl) + e, paired for the packed FMA.
+  float2 wc[4][kQ][2];
 #pragma unroll
-  for (int q = 0; q < HALF / 2; ++q) {
-    const int i0 = HALF * hf + 2 * q;
-    const float* col = p.W + p.n_x + (ok_j ? j : 0);
-    wc[q] = make_float2(ok_j && i0 < C ? __ldg(col + static_cast<size_t>(i0) * n_in) : 0.f,
-                        ok_j && i0 + 1 < C ? __ldg(col + static_cast<size_t>(i0 + 1) * n_in) : 0.f);
+  for (int u = 0; u < 4; ++u) {
+    const int unit = ubase + u;
+    const float* col = p.W + p.n_x + (unit < C ? unit : 0);
+#pragma unroll
+    for (int q = 0; q < kQ; ++q)
+#pragma unroll
+      for (int ep = 0; ep < 2; ++ep) {
+        const int k = 4 * (8 * q + sl) + 2 * ep;
+        wc[u][q][ep] =
+            make_float2(unit < C && k < C ? __ldg(col + static_cast<size_t>(k) * n_in) : 0.f,
+                        unit < C && k + 1 < C ? __ldg(col + static_cast<size_t>(k + 1) * n_in) : 0.f);
+      }
   }
   const float inv_tau = ok_j ? 1.f / __ldg(p.tau + j) : 0.f;
   bool rok[R];
@@ -239,7 +307,7 @@ __global__ void __launch_bounds__(2 * CP) decay_bwd_kernel(const DecayBwdParams 
       dv[r] = d;
       const float da = G[r] * (1.f - d) * (1.f - ec[r] * ec[r]);
       acc[r] += G[r] * (hpc[r] - ec[r]) * d * tsc[r] * inv_tau * inv_tau;
-      if (hf == 0) {
+      if (writer) {
         das[cur][r][j] = ok_j ? da : 0.f;
         if (ok_j && rok[r]) {
           __nv_bfloat16* q = p.da + (static_cast<size_t>(t) * B + row0 + r) * 2 * p.mp + j;
@@ -252,22 +320,29 @@ __global__ void __launch_bounds__(2 * CP) decay_bwd_kernel(const DecayBwdParams 
     __syncthreads();
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const float4* dv4 = reinterpret_cast<const float4*>(&das[cur][r][HALF * hf]);
-      float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+      const float4* dv4 = reinterpret_cast<const float4*>(&das[cur][r][0]);
+      float2 acc2[4];
 #pragma unroll
-      for (int q = 0; q < HALF / 4; ++q) {
-        const float4 v = dv4[q];
-        s0 = fma2(wc[2 * q], make_float2(v.x, v.y), s0);
-        s1 = fma2(wc[2 * q + 1], make_float2(v.z, v.w), s1);
+      for (int u = 0; u < 4; ++u) acc2[u] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        const float4 v = dv4[8 * q + sl];
+        const float2 v01 = make_float2(v.x, v.y), v23 = make_float2(v.z, v.w);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          acc2[u] = fma2(wc[u][q][0], v01, acc2[u]);
+          acc2[u] = fma2(wc[u][q][1], v23, acc2[u]);
+        }
       }
-      const float part = (s0.x + s0.y) + (s1.x + s1.y);
-      const float delta = part + __shfl_xor_sync(0xffffffffu, part, 1);
-      G[r] = G[r] * dv[r] + delta;
+      float au[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) au[u] = acc2[u].x + acc2[u].y;
+      G[r] = G[r] * dv[r] + quad_reduce_scatter(au, lane);
     }
   }
 #pragma unroll
   for (int r = 0; r < R; ++r)
-    if (hf == 0 && ok_j && rok[r]) {
+    if (writer && ok_j && rok[r]) {
       const size_t o = static_cast<size_t>(row0 + r) * C + j;
       p.dh0[o] = G[r];
       p.dtau_part[o] = acc[r];
@@ -312,8 +387,8 @@ cudaError_t decay_proj_launch(const float* x, const float* W, const float* b, in
                               int n_x, float* E, cudaStream_t s) {
   if (C > kDecayMaxC) return cudaErrorInvalidValue;
   LaunchCfg c;
-  c.grid = dim3((BK + kProjRows - 1) / kProjRows, 1, 1);
-  c.block = dim3(32 * kProjRows, 1, 1);
+  c.grid = dim3((C + kPC - 1) / kPC, (BK + kPR - 1) / kPR, 1);
+  c.block = dim3(256, 1, 1);
   c.stream = s;
   return launch(c, decay_proj_kernel, x, W, b, BK, C, n_x, E);
 }
