@@ -97,6 +97,9 @@ __global__ void __launch_bounds__(256) decay_proj_kernel(const float* __restrict
   }
 }
 
+// Slots of the BPTT's input ring (copies run two steps ahead of their use).
+constexpr int kDecayRing = 3;
+
 // Chunks of four reduction entries a lane holds (chunks 8 q + sl, q < kQ) and the reduction
 // over the eight lanes of a unit quad: a[u] is the lane's partial sum of unit u; the result,
 // the full sum of unit (lane >> 1) & 3, is in both lanes of each pair.
@@ -247,6 +250,7 @@ template <int CP, int R>
 __global__ void __launch_bounds__(2 * CP) decay_bwd_kernel(const DecayBwdParams p) {
   constexpr int kQ = Quad<CP>::kQ;
   __shared__ __align__(16) float das[2][R][CP];  // da of the step, double buffered
+  __shared__ __align__(16) float ring[kDecayRing][R][4][CP];  // dH, e, h_{t-1}, ts by step
   const int tid = threadIdx.x, lane = tid & 31, sl = lane & 7;
   const int B = p.B, K = p.K, C = p.C, n_in = p.n_x + C;
   const int row0 = blockIdx.x * R;
@@ -274,39 +278,55 @@ __global__ void __launch_bounds__(2 * CP) decay_bwd_kernel(const DecayBwdParams 
   bool rok[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) rok[r] = row0 + r < B;
-  // Inputs of step t for the rows: dH, e = tanh(a), h_{t-1}, ts.
-  auto load = [&](int t, float (&dh)[R], float (&e)[R], float (&hp)[R], float (&tv)[R]) {
+  // The inputs of each step -- dH, e = tanh(a), h_{t-1} (units along the row) and ts -- arrive
+  // in a ring of kDecayRing shared-memory slots by cp.async, two steps ahead of their use:
+  // thread u < C copies unit u of the three vectors, thread C copies ts.  Slots of units and
+  // rows that do not exist stay zero.
+  for (int e = tid; e < kDecayRing * R * 4 * CP; e += 2 * CP) (&ring[0][0][0][0])[e] = 0.f;
+  __syncthreads();
+  auto issue = [&](int t) {
+    const int sl3 = t % kDecayRing;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const bool v = ok_j && rok[r];
+      if (!rok[r]) continue;
       const size_t tb = static_cast<size_t>(t) * B + row0 + r;
-      dh[r] = v ? __ldcg(p.dH + tb * C + j) : 0.f;
-      e[r] = v ? __ldcg(p.E + tb * C + j) : 0.f;
-      hp[r] = !v ? 0.f
-            : t > 0 ? __ldcg(p.H + (tb - B) * C + j)
-                    : __ldg(p.h0 + static_cast<size_t>(row0 + r) * C + j);
-      tv[r] = rok[r] ? __ldg(p.ts + tb) : 0.f;
+      if (tid < C) {
+        cp_async_4(smem_addr(&ring[sl3][r][0][tid]), p.dH + tb * C + tid);
+        cp_async_4(smem_addr(&ring[sl3][r][1][tid]), p.E + tb * C + tid);
+        cp_async_4(smem_addr(&ring[sl3][r][2][tid]),
+                   t > 0 ? p.H + (tb - B) * C + tid
+                         : p.h0 + static_cast<size_t>(row0 + r) * C + tid);
+      } else if (tid == C) {
+        cp_async_4(smem_addr(&ring[sl3][r][3][0]), p.ts + tb);
+      }
     }
   };
-  float G[R], acc[R], dHn[R], en[R], hpn[R], tsn[R];
+  float G[R], acc[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) G[r] = acc[r] = 0.f;
-  load(K - 1, dHn, en, hpn, tsn);
+  issue(K - 1);
+  cp_async_commit();
+  if (K >= 2) issue(K - 2);
+  cp_async_commit();
+  cp_async_wait<1>();  // step K - 1's copies (K - 2's may be pending)
+  __syncthreads();
   for (int t = K - 1; t >= 0; --t) {
-    const int cur = t & 1;
-    float dHc[R], ec[R], hpc[R], tsc[R], dv[R];
+    const int cur = t & 1, sl3 = t % kDecayRing;
+    // Step t - 2 goes into the slot step t + 1 used (every thread is past it: the barrier of
+    // step t + 1); one group per step, empty at the end, keeps the wait count uniform.
+    if (t >= 2) issue(t - 2);
+    cp_async_commit();
+    float dv[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      dHc[r] = dHn[r]; ec[r] = en[r]; hpc[r] = hpn[r]; tsc[r] = tsn[r];
-    }
-    if (t >= 1) load(t - 1, dHn, en, hpn, tsn);  // one step ahead
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      G[r] += dHc[r];
-      const float d = __expf(-tsc[r] * inv_tau);
+      const int jj = ok_j ? j : 0;
+      const float dHc = ring[sl3][r][0][jj], ec = ring[sl3][r][1][jj];
+      const float hpc = ring[sl3][r][2][jj], tsc = ring[sl3][r][3][0];
+      G[r] += ok_j ? dHc : 0.f;
+      const float d = __expf(-tsc * inv_tau);
       dv[r] = d;
-      const float da = G[r] * (1.f - d) * (1.f - ec[r] * ec[r]);
-      acc[r] += G[r] * (hpc[r] - ec[r]) * d * tsc[r] * inv_tau * inv_tau;
+      const float da = G[r] * (1.f - d) * (1.f - ec * ec);
+      acc[r] += G[r] * (hpc - ec) * d * tsc * inv_tau * inv_tau;
       if (writer) {
         das[cur][r][j] = ok_j ? da : 0.f;
         if (ok_j && rok[r]) {
@@ -317,6 +337,7 @@ __global__ void __launch_bounds__(2 * CP) decay_bwd_kernel(const DecayBwdParams 
         }
       }
     }
+    cp_async_wait<1>();  // step t - 1's copies are in (step t - 2's may be pending)
     __syncthreads();
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -340,6 +361,7 @@ __global__ void __launch_bounds__(2 * CP) decay_bwd_kernel(const DecayBwdParams 
       G[r] = G[r] * dv[r] + quad_reduce_scatter(au, lane);
     }
   }
+  cp_async_wait<0>();
 #pragma unroll
   for (int r = 0; r < R; ++r)
     if (writer && ok_j && rok[r]) {
