@@ -221,10 +221,11 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || R >= 8) ? 1 : 2) cfc_
   const float* xnext = xp + xstep;  // X and ts of step t + 1
   const float* tsnext = tsp + B;
   uint32_t phase = 0;  // bit s: parity of the next phase of bars[s] to wait for
-  for (int t = 0; t < K; ++t) {
+  // One step: X and ts of step t in (xcur, tcur), those of step t + 1 loaded into (xn, tn).
+  // Two calls per loop iteration with the arrays swapped: no register copies of pending loads.
+  auto body = [&](int t, float (&xcur)[R], float (&tcur)[R], float (&xn)[R],
+                  float (&tn)[R]) -> bool {
     const int s = t & 1;
-    // X and ts of the next step; consumed one step later, so their latency is hidden.
-    float xn[R], tn[R];
     if (t + 1 < K) {
       load_step(xnext, tsnext, xn, tn);
       xnext += xstep;
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || R >= 8) ? 1 : 2) cfc_
       const bool ok = __all_sync(
           0xffffffffu, mbar_wait_bounded_cluster(bar0 + 8u * s, (phase >> s) & 1u, p.status));
       phase ^= (1u << s);
-      if (!ok) break;
+      if (!ok) return false;
       if (tid == 0 && t + 2 <= K - 1) mbar_arrive_expect_tx(bar0 + 8u * s, tx_bytes);
     }
 
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || R >= 8) ? 1 : 2) cfc_
       const float s1 = k1 + __shfl_xor_sync(0xffffffffu, b2 ? a[1] : a[3], 4);
       float acc = (b1 ? s1 : s0) + __shfl_xor_sync(0xffffffffu, b1 ? s0 : s1, 2);
       acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      P[r] = acc + xc[r];
+      P[r] = acc + xcur[r];
     }
     float hn[R], sv[R];
 #pragma unroll
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || R >= 8) ? 1 : 2) cfc_
       // Activations: lanes of gate 0 / 1 evaluate tanh(P) = 2 sigmoid(2P) - 1, lanes of gate
       // 2 the time gate sigmoid(P_ta ts + P_tb) (P_tb from the gate-3 lane two lanes up).
       const float P_tb = __shfl_sync(0xffffffffu, P[r], (lane + 2) & 31);
-      const float x = (g < 2) ? 2.f * P[r] : fmaf(P[r], tc[r], P_tb);
+      const float x = (g < 2) ? 2.f * P[r] : fmaf(P[r], tcur[r], P_tb);
       const float sg = sigmoid_fast(x);
       const float y = (g < 2) ? fmaf(2.f, sg, -1.f) : sg;
       const float f1 = __shfl_sync(0xffffffffu, y, base + 0);
@@ -309,13 +310,12 @@ __global__ void __launch_bounds__(kRecThreads, (CS >= 8 || R >= 8) ? 1 : 2) cfc_
           (to_h ? p.H : p.cache)[o] = sv[r];
       }
     so += sstep;
-    if (t + 1 < K) {
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        xc[r] = xn[r];
-        tc[r] = tn[r];
-      }
-    }
+    return true;
+  };
+  float xb[R], tb[R];
+  for (int t = 0; t < K; t += 2) {
+    if (!body(t, xc, tc, xb, tb)) break;
+    if (t + 1 < K && !body(t + 1, xb, tb, xc, tc)) break;
   }
   // No CTA leaves while a peer may still address its shared memory.
   cluster_sync_all();
