@@ -1018,10 +1018,13 @@ int cfc_decay_backward(const float* dH, const float* x, const float* h0, const f
   rc = cuda_rc(cfc::decay_bwd_launch(dH, h0, W, tau, ts, H, E, B, K, C, n_x, w + L.da_off, L.mp,
                                      dh0, dtau_part, s),
                CFC_ERR_LAUNCH_FAILED);
-  // 2. z rows [x ; h_{t-1} ; 1] and W_in^T rows (W has C rows).
+  // 2. z rows [x ; h_{t-1} ; 1] and W_in^T rows (W has C rows): beside the BPTT on the SMs it
+  // leaves idle (1024-thread CTAs, which do not fit beside a BPTT CTA), else after it.
+  const int idle = st->sms - cfc::decay_bwd_ctas(B);
+  const bool beside = idle >= kMinBesideSms;
   if (rc == CFC_OK)
     rc = cuda_rc(cfc::build_operands_launch(form, x, H, 0, h0, W, B, K, C, n_x, w + L.z_off,
-                                            w + L.wt_off, s, false, C),
+                                            w + L.wt_off, s, beside, C, beside ? idle : 0),
                  CFC_ERR_LAUNCH_FAILED);
   // 3. dW (with db in the ones column) and dx, one contraction each, dx beside dW.
   if (rc == CFC_OK)

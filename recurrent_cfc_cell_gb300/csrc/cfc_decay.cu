@@ -251,6 +251,9 @@ __global__ void __launch_bounds__(2 * CP) decay_bwd_kernel(const DecayBwdParams 
   constexpr int kQ = Quad<CP>::kQ;
   __shared__ __align__(16) float das[2][R][CP];  // da of the step, double buffered
   __shared__ __align__(16) float ring[kDecayRing][R][4][CP];  // dH, e, h_{t-1}, ts by step
+  // The first kernel of its call (an ordinary launch): its dependents -- the operand build,
+  // which reads only the forward's outputs and the inputs -- may start beside it at once.
+  grid_dep_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, sl = lane & 7;
   const int B = p.B, K = p.K, C = p.C, n_in = p.n_x + C;
   const int row0 = blockIdx.x * R;
@@ -404,6 +407,8 @@ cudaError_t bwd_cp(const DecayBwdParams& p, int R, cudaStream_t s) {
 }  // namespace
 
 bool decay_supported(int C, int n_x) { return C >= 1 && C <= kDecayMaxC && n_x >= 1; }
+
+int decay_bwd_ctas(int B) { return (B + decay_rows(B) - 1) / decay_rows(B); }
 
 cudaError_t decay_proj_launch(const float* x, const float* W, const float* b, int BK, int C,
                               int n_x, float* E, cudaStream_t s) {
