@@ -457,6 +457,7 @@ int backward_recurrence(const float* dH, const float* W, const float* ts, const 
   rc = plan_rows(*st, 1, 0, p.CS, B, n_x, &p.R, &smem, &n_clusters,
                  pdl ? kDependentBwdSmem : 0);
   if (rc != CFC_OK) return rc;
+  if (free_sms && st->sms > n_clusters * p.CS) *free_sms = st->sms - n_clusters * p.CS;
   return cuda_rc(cfc::bwd_launch(p, n_clusters, smem, static_cast<cudaStream_t>(stream), pdl),
                  CFC_ERR_LAUNCH_FAILED);
 }
@@ -705,11 +706,11 @@ int weight_grad(const float* d_pre, const float* u, const float* h0, const float
                  CFC_ERR_LAUNCH_FAILED);
 }
 
-// The gradient stage right after the BPTT recurrence of the same call.  Beside the CUDA-core
-// BPTT (a few SMs) the operand build runs at its usual width.  The tensor-core BPTT holds most
-// SMs, one CTA each; the build then runs beside it on the SMs it leaves idle and nowhere else
-// (1024-thread CTAs, which cannot share an SM with a recurrence CTA), so it never competes with
-// the recurrence for issue slots.  With too few idle SMs the build follows the recurrence.
+// The gradient stage right after the BPTT recurrence of the same call.  The operand build runs
+// beside the recurrence on the SMs it leaves idle and nowhere else (1024-thread CTAs, which
+// cannot share an SM with a recurrence CTA), so it never competes with the recurrence for issue
+// slots.  With too few idle SMs it runs at its usual width: still beside the CUDA-core BPTT,
+// after the tensor-core one (which holds most SMs).
 constexpr int kMinBesideSms = 8;
 
 int weight_grad_after_bptt(const float* d_pre, const float* u, const float* h0, const float* W,
@@ -717,9 +718,10 @@ int weight_grad_after_bptt(const float* d_pre, const float* u, const float* h0, 
                            float* du, void* ws, size_t ws_bytes, int dw_mode,
                            cfc_stream_t stream, const BwdLayout& L, bool dpre_in_ws,
                            int free_sms, bool h_bf16) {
-  const bool beside = !L.tc_bptt || free_sms >= kMinBesideSms;
+  const bool idle = free_sms >= kMinBesideSms;
+  const bool beside = !L.tc_bptt || idle;
   return weight_grad(d_pre, u, h0, W, H, B, K, C, n_x, dW, db, du, ws, ws_bytes, dw_mode, stream,
-                     beside, dpre_in_ws, beside, h_bf16, L.tc_bptt && beside ? free_sms : 0);
+                     beside, dpre_in_ws, beside, h_bf16, idle ? free_sms : 0);
 }
 
 }  // namespace
