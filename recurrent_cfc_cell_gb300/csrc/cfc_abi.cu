@@ -13,6 +13,8 @@
 namespace cfc {
 // Launcher of the failure-detection self-test kernel (cfc_selftest.cu).
 cudaError_t wait_self_test_launch(int* status, cudaStream_t s);
+// CTAs of the tau-decay BPTT launch for B rows (cfc_decay.cu).
+int decay_bwd_ctas(int B);
 }  // namespace cfc
 
 namespace {

@@ -213,8 +213,6 @@ cudaError_t reduce_axis0_pair_launch(const float* in, int n_batch, int n_tail, i
 // The pages' tau-decay cell (cfc_decay.cu): hidden width at most kDecayMaxC.
 constexpr int kDecayMaxC = 128;
 bool decay_supported(int C, int n_x);
-// CTAs of the decay BPTT launch (one per group of rows).
-int decay_bwd_ctas(int B);
 // X = W_in x + b for the B*K rows, into E [B*K][C].
 cudaError_t decay_proj_launch(const float* x, const float* W, const float* b, int BK, int C,
                               int n_x, float* E, cudaStream_t s);
