@@ -108,6 +108,29 @@ def test_host_staged_graph_step_parity():
     assert n_out == 4 * (4 * 72 * 84 + 4 * 72 + 9 * 6 * 12 + 6 * 72)
 
 
+def test_host_staged_graph_step_parity_tensor_core_shape():
+    """The host-staged graph step at a batch the tensor-core recurrences take (B=600, C=256: the
+    forward with its fused projection, the L2-exchange BPTT with the operand build on its idle
+    SMs), inputs and gradients moved by the copy kernel."""
+    import torch
+
+    from recurrent_cfc_cell_gb300 import build
+    from recurrent_cfc_cell_gb300.step import KLoopStep
+
+    build.build()
+    shape = dict(B=600, K=3, n_x=24, C=256)
+    st = KLoopStep(shape["B"], shape["K"], shape["C"], shape["n_x"]).stage_host()
+    st.capture(with_host_io=True)
+    inp = inputs.make_inputs(inputs.custom(seed=41, **shape))
+    for k, v in inp.items():
+        st.host_in[k].copy_(torch.from_numpy(v))
+    st.replay()
+    torch.cuda.synchronize()
+    got = {k: v.numpy().copy() for k, v in st.host_out.items()}
+    got["H"] = st.H.cpu().numpy()
+    assert_parity(got, oracle_ref(inp), keys=("H", "dW", "db", "du", "dh0"))
+
+
 @pytest.mark.parametrize("shape", [dict(B=32, K=64, n_x=48, C=128), dict(B=7, K=11, n_x=13, C=100),
                                    dict(B=40, K=9, n_x=64, C=256)],
                          ids=lambda s: "B{B}_K{K}_nx{n_x}_C{C}".format(**s))
