@@ -373,10 +373,11 @@ __device__ __forceinline__ void put8(uint8_t* row, int pitch, int col, const flo
 // multiple of 8 (the pitches are multiples of 8); the contraction never reads beyond them.
 // HB: H holds bf16 elements.
 template <int FORM, bool HB>
-__global__ void __launch_bounds__(1024) build_operands_kernel(const float* __restrict__ u, const void* __restrict__ H,
-                                      const float* __restrict__ h0,
-                                      const float* __restrict__ W, int B, int BK, int C, int n_x,
-                                      int M, uint8_t* z, int zp, uint8_t* wt, int mp) {
+__global__ void __launch_bounds__(1024)
+    build_operands_kernel(const float* __restrict__ u, const void* __restrict__ H,
+                          const float* __restrict__ h0, const float* __restrict__ W, int B,
+                          int BK, int C, int n_x, int M, uint8_t* z, int zp, uint8_t* wt,
+                          int mp) {
   // u, H, h0 and W are complete when this kernel starts: it follows either nothing of the same
   // call, or a kernel that releases its dependents only after its own dependency wait (the
   // BPTT recurrence, the d_pre split).  So the build runs beside that kernel and waits for it
