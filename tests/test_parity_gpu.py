@@ -47,6 +47,9 @@ RAGGED = [
     dict(B=2300, K=2, n_x=16, C=256),  # 16 clusters of 144 rows, more than stay resident: both
                                        # recurrences in two waves, the operand build after the
                                        # BPTT (no idle SMs to run beside it)
+    dict(B=600, K=1, n_x=24, C=256),   # tensor-core recurrences over a single step: no
+                                       # exchange in the forward, dh0 from the first exchange
+    dict(B=900, K=2, n_x=32, C=128),   # tensor-core recurrences at C = 128, two steps
 ]
 
 
