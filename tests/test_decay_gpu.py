@@ -16,11 +16,11 @@ H_TOL, GRAD_TOL = 1e-5, 1e-4
 OUTS = ("H", "E", "dW", "db", "dtau", "dx", "dh0")
 
 # The three workloads (tiny; the pages' shape, 128 inputs and 128 hidden units; a larger
-# batch), and ragged ones: odd sizes, C below 32 / 64 / 128, and batches that take 1, 2 and 4
-# rows per CTA.
+# batch), and ragged ones: odd sizes, C below 32 / 64 / 128, batches that take 1, 2 and 4 rows
+# per CTA, and one- and two-step sequences (the BPTT's input ring barely filled).
 SHAPES = [(w.B, w.K, w.n_x, w.C, w.seed) for w in inputs.DECAY_CONFIGS] + [
     (7, 11, 13, 100, 21), (5, 6, 3, 17, 22), (9, 5, 40, 64, 23), (300, 4, 24, 128, 24),
-    (700, 3, 16, 96, 25)]
+    (700, 3, 16, 96, 25), (9, 1, 8, 64, 26), (6, 2, 5, 33, 27)]
 
 
 def _ids(s):
