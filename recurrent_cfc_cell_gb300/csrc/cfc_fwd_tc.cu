@@ -529,6 +529,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
           if (lane + 32 * k < HR) tsw[lane + 32 * k] = tsn[k];
         __syncwarp();
       }
+      // The H / cache stores of the warp half's last 8 rows (when HR % 16 == 8) are issued
+      // after the release fence and the announcements below: the fence waits for every store
+      // the thread has in flight, and these would be the youngest.
+      float dfv[2][4];
+      size_t dfh[2], dfc[2];
+      bool dfo[2] = {false, false};
       {
         const float* tsr = tsw;
         const size_t ho = (static_cast<size_t>(t) * B + rfirst) * C + ch;  // element offsets
@@ -537,7 +543,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
         // h_t is the operand of step t + 1: its exchange slot has that step's parity.
         uint8_t* const xs = slot((t + 1) & 1, rank) - rank * S::SLAB;
         // Rows ibase .. ibase + n - 1 of this warp half (n = 16, or 8 for the tail of 72).
-        auto rows = [&](float (&P)[16], int ibase, int n) {
+        auto rows = [&](float (&P)[16], int ibase, int n, bool defer) {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             if (i < n) P[i] = fmaf(P[i], wunscale, FU ? bv : xv[FU ? 0 : ibase + i]);
@@ -563,7 +569,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
             const float ff2 = fmaf(2.f, sigmoid_fast(2.f * v[1]), -1.f);
             const float gt = sigmoid_fast(fmaf(v[2], tsr[ri], v[3]));
             const float h = ff1 * (1.f - gt) + gt * ff2;
-            if (ri < nvalid) {
+            if (defer) {
+              const int j = i0 >> 2;
+              dfo[j] = ri < nvalid;
+              dfv[j][0] = h; dfv[j][1] = ff1; dfv[j][2] = ff2; dfv[j][3] = gt;
+              dfh[j] = ho + static_cast<size_t>(ri) * C;
+              dfc[j] = co + static_cast<size_t>(ri) * 3 * C;
+            } else if (ri < nvalid) {
               const size_t hi = ho + static_cast<size_t>(ri) * C;
               const size_t ci = co + static_cast<size_t>(ri) * 3 * C;
               if constexpr (obf) {
@@ -596,7 +608,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
         for (int cc = 0; cc < HR / 16; ++cc) {
           float P[16];
           tmem_ld16(dq + 16 * cc, P);
-          rows(P, 16 * cc, 16);
+          rows(P, 16 * cc, 16, false);
         }
         if constexpr (HR % 16 == 8) {
           float P[16];
@@ -606,7 +618,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
           for (int i = 0; i < 8; ++i) P[i] = P8[i];
 #pragma unroll
           for (int i = 8; i < 16; ++i) P[i] = 0.f;
-          rows(P, HR - 8, 8);
+          rows(P, HR - 8, 8, true);
         }
       }
       fence_proxy_async_smem();  // h_t's terms -> visible to the MMAs
@@ -632,6 +644,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) cfc_fwd_tc_kernel(const FwdPara
           load_x(t + 1);  // in flight while the exchange and the next step's MMAs run
         }
         load_ts(t + 1);
+      }
+      if constexpr (HR % 16 == 8) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          if (dfo[j]) {
+            if constexpr (obf) {
+              __nv_bfloat16* hb16 = reinterpret_cast<__nv_bfloat16*>(p.H);
+              __nv_bfloat16* cb16 = reinterpret_cast<__nv_bfloat16*>(p.cache);
+              hb16[dfh[j]] = __float2bfloat16_rn(dfv[j][0]);
+              cb16[dfc[j]] = __float2bfloat16_rn(dfv[j][1]);
+              cb16[dfc[j] + C] = __float2bfloat16_rn(dfv[j][2]);
+              cb16[dfc[j] + 2 * C] = __float2bfloat16_rn(dfv[j][3]);
+            } else {
+              p.H[dfh[j]] = dfv[j][0];
+              p.cache[dfc[j]] = dfv[j][1];
+              p.cache[dfc[j] + C] = dfv[j][2];
+              p.cache[dfc[j] + 2 * C] = dfv[j][3];
+            }
+          }
       }
     }
   }
